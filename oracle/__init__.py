@@ -1,0 +1,232 @@
+"""float64 CPU oracle for the selective state-space scan -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never uses it and
+shares no code with it; the two meet only through the seeded input generator
+(``selective_scan_mamba_gb300.synth``), which holds none of the method's
+arithmetic.
+
+The arithmetic lives in ``oracle.c`` (plain sequential loops in double
+precision, each routine citing the passage it follows); this module compiles it
+with the host C compiler on first use and calls it through ctypes.  Every array
+argument is a float64 numpy array in the library's layout; ``None`` stands for an
+optional input that is absent.
+
+Parity pins: every routine is pinned by tests in ``tests/test_oracle_pins.py``
+(closed forms, brute-force unrolled sums, chunked-versus-sequential agreement,
+split continuation, degenerate cases, high-precision references for softplus and
+phi1).  None is left unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DISC_EXP_EULER = 0
+DISC_ZOH = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP, portable flags)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+                   "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.c_void_p
+    i = ctypes.c_int
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_phi1.restype = ctypes.c_double
+    lib.oracle_phi1.argtypes = [ctypes.c_double]
+    lib.oracle_mamba1_scan.restype = i
+    lib.oracle_mamba1_scan.argtypes = [i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp, dp, i,
+                                       dp, dp]
+    lib.oracle_ssd_sequential.restype = i
+    lib.oracle_ssd_sequential.argtypes = [i, i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp, dp,
+                                          i, dp, dp]
+    lib.oracle_ssd_chunked.restype = i
+    lib.oracle_ssd_chunked.argtypes = [i, i, i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp, dp,
+                                       i, dp, dp]
+    lib.oracle_state_update.restype = i
+    lib.oracle_state_update.argtypes = [i, i, i, i, i, i, dp, dp, dp, dp, i, dp, dp, dp, dp, dp,
+                                        i, dp]
+    lib.oracle_num_threads.restype = i
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(_LIB)
+    return _lib
+
+
+class use_library:
+    """Context manager: route every call of this module to another build of the
+    oracle (used by the test that plants mistakes in a copy of oracle.c)."""
+
+    def __init__(self, path):
+        self.path = path
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        self.saved = _load()
+        _lib = _bind(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def _f64(a, shape=None):
+    """Contiguous float64 copy/view of an optional array, checked against shape."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError(f"oracle: expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def softplus(v: float) -> float:
+    return _load().oracle_softplus(float(v))
+
+
+def phi1(zv: float) -> float:
+    return _load().oracle_phi1(float(zv))
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def mamba1_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                h0=None, disc=DISC_EXP_EULER, ngroups=None):
+    """Mamba-1 selective scan.  x, delta, z: [batch, dim, L]; B, C: [batch, G, N, L];
+    A: [dim, N].  Returns (y [batch, dim, L], h_final [batch, dim, N])."""
+    x = _f64(x)
+    batch, dim, L = x.shape
+    A = _f64(A)
+    N = A.shape[1]
+    B = _f64(B)
+    if B.ndim == 3:  # [batch, N, L] means one group
+        B = B[:, None]
+    G = B.shape[1] if ngroups is None else ngroups
+    B = _f64(B, (batch, G, N, L))
+    C = _f64(C if np.ndim(C) == 4 else np.asarray(C)[:, None], (batch, G, N, L))
+    delta = _f64(delta, (batch, dim, L))
+    A = _f64(A, (dim, N))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim, L))
+    delta_bias = _f64(delta_bias, (dim,))
+    h0 = _f64(h0, (batch, dim, N))
+    y = np.empty((batch, dim, L), np.float64)
+    hf = np.empty((batch, dim, N), np.float64)
+    rc = _load().oracle_mamba1_scan(batch, dim, N, L, G, _p(x), _p(delta), _p(delta_bias),
+                                    int(bool(delta_softplus)), _p(A), _p(B), _p(C), _p(D), _p(z),
+                                    _p(h0), int(disc), _p(y), _p(hf))
+    if rc:
+        raise ValueError("oracle_mamba1_scan: invalid arguments")
+    return y, hf
+
+
+def _ssd_args(x, dt, A, B, C, D, z, dt_bias, h0):
+    x = _f64(x)
+    batch, L, H, P = x.shape
+    B = _f64(B)
+    G, N = B.shape[2], B.shape[3]
+    B = _f64(B, (batch, L, G, N))
+    C = _f64(C, (batch, L, G, N))
+    dt = _f64(dt, (batch, L, H))
+    A = _f64(A, (H,))
+    D = _f64(D, (H,))
+    z = _f64(z, (batch, L, H, P))
+    dt_bias = _f64(dt_bias, (H,))
+    h0 = _f64(h0, (batch, H, P, N))
+    return x, dt, A, B, C, D, z, dt_bias, h0, (batch, L, H, P, G, N)
+
+
+def ssd_sequential(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
+                   disc=DISC_EXP_EULER):
+    """Mamba-2 sequential scan.  x, z: [batch, L, H, P]; dt: [batch, L, H];
+    B, C: [batch, L, G, N]; A, D, dt_bias: [H].  Returns (y, h_final [batch, H, P, N])."""
+    x, dt, A, B, C, D, z, dt_bias, h0, (batch, L, H, P, G, N) = _ssd_args(
+        x, dt, A, B, C, D, z, dt_bias, h0)
+    y = np.empty((batch, L, H, P), np.float64)
+    hf = np.empty((batch, H, P, N), np.float64)
+    rc = _load().oracle_ssd_sequential(batch, L, H, P, N, G, _p(x), _p(dt), _p(dt_bias),
+                                       int(bool(dt_softplus)), _p(A), _p(B), _p(C), _p(D), _p(z),
+                                       _p(h0), int(disc), _p(y), _p(hf))
+    if rc:
+        raise ValueError("oracle_ssd_sequential: invalid arguments")
+    return y, hf
+
+
+def ssd_chunked(x, dt, A, B, C, chunk, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
+                disc=DISC_EXP_EULER):
+    """Mamba-2 chunked SSD with chunk size ``chunk``; same layouts as ssd_sequential."""
+    x, dt, A, B, C, D, z, dt_bias, h0, (batch, L, H, P, G, N) = _ssd_args(
+        x, dt, A, B, C, D, z, dt_bias, h0)
+    y = np.empty((batch, L, H, P), np.float64)
+    hf = np.empty((batch, H, P, N), np.float64)
+    rc = _load().oracle_ssd_chunked(batch, L, H, P, N, G, int(chunk), _p(x), _p(dt), _p(dt_bias),
+                                    int(bool(dt_softplus)), _p(A), _p(B), _p(C), _p(D), _p(z),
+                                    _p(h0), int(disc), _p(y), _p(hf))
+    if rc:
+        raise ValueError("oracle_ssd_chunked: invalid arguments")
+    return y, hf
+
+
+def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
+                 disc=DISC_EXP_EULER):
+    """One decode step.  state: [batch, H, P, N] (a new array is returned, the
+    input is not modified); x, z: [batch, H, P]; dt: [batch, H]; B, C: [batch, G, N];
+    A: [H] or [H, N].  Returns (y [batch, H, P], new_state)."""
+    st = np.array(state, dtype=np.float64, copy=True, order="C")
+    batch, H, P, N = st.shape
+    B = _f64(B)
+    G = B.shape[1]
+    B = _f64(B, (batch, G, N))
+    C = _f64(C, (batch, G, N))
+    x = _f64(x, (batch, H, P))
+    dt = _f64(dt, (batch, H))
+    A = _f64(A)
+    a_per_state = 1 if A.ndim == 2 else 0
+    A = _f64(A, (H, N) if a_per_state else (H,))
+    D = _f64(D, (H,))
+    z = _f64(z, (batch, H, P))
+    dt_bias = _f64(dt_bias, (H,))
+    y = np.empty((batch, H, P), np.float64)
+    rc = _load().oracle_state_update(batch, H, P, N, G, a_per_state, _p(st), _p(x), _p(dt),
+                                     _p(dt_bias), int(bool(dt_softplus)), _p(A), _p(B), _p(C),
+                                     _p(D), _p(z), int(disc), _p(y))
+    if rc:
+        raise ValueError("oracle_state_update: invalid arguments")
+    return y, st

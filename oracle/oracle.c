@@ -1,0 +1,314 @@
+/*
+ * oracle.c -- plain, slow, sequential float64 CPU reference for the selective
+ * state-space scan.  TEST INFRASTRUCTURE ONLY: the product path (the CUDA
+ * library under selective_scan_mamba_gb300/) never links, loads or calls this
+ * file; only the tests, the smoke check and the CPU-baseline leg of the bench
+ * do.  It shares no header, helper, table or constant with the CUDA path.
+ *
+ * Every routine is the definition written out, in the order the pages state
+ * it, with no blocking, fusion or reordering:
+ *
+ *   - "From S4 to Mamba-3" (ssmbench case study), section 03/System,
+ *     mamba_minimal.py entry: Mamba-1 is an input-dependent (Delta, B, C)
+ *     selective scan run as an explicit time loop, with an incremental step()
+ *     for decoding.
+ *   - same page, mamba2_minimal.py entry: a scalar A per head turns the
+ *     recurrence into SSD, computed as chunked decayed-attention matmuls with a
+ *     carried (N, P) state, next to a sequential scan used as its reference.
+ *   - same page, s4_minimal.py entry and "Likely questions" Q01: exact ZOH for a
+ *     diagonal A gives B-bar = Delta*B*(e^z - 1)/z with z = Delta*a, with the
+ *     Taylor series 1 + z/2 + z^2/6 used for |z| < 1e-4.
+ *   - same page, mamba3_minimal.py entry and section 04/Approach: the
+ *     exponential-Euler rule (A-bar = exp(Delta*A), B-bar = Delta*B) is the
+ *     form Mamba-3 reduces to at lambda = 1, theta = 0; it is the default here.
+ *
+ * Readings where the pages leave a step open (each listed in the design notes):
+ *   - Delta = softplus(delta + bias) when softplus is requested, computed here
+ *     in the overflow-safe form max(v,0) + log1p(exp(-|v|)).
+ *   - the output uses the state after step t: y_t = C_t . h_t + D x_t;
+ *   - the skip term is added before the gate: y = (C.h + D x) * SiLU(z);
+ *   - a missing initial state means zeros.
+ *
+ * Layouts (row-major, last index fastest) are the library's:
+ *   Mamba-1 : x, delta, z, y [batch, dim, seqlen]; B, C [batch, ngroups, dstate,
+ *             seqlen]; A [dim, dstate]; D, bias [dim]; h0, h_final [batch, dim,
+ *             dstate]; channel d reads group d / (dim / ngroups).
+ *   SSD     : x, z, y [batch, seqlen, nheads, headdim]; dt [batch, seqlen,
+ *             nheads]; B, C [batch, seqlen, ngroups, dstate]; A, D, bias
+ *             [nheads]; h0, h_final [batch, nheads, headdim, dstate]; head h
+ *             reads group h / (nheads / ngroups).
+ *   Step    : state [batch, nheads, headdim, dstate]; x, z, y [batch, nheads,
+ *             headdim]; dt [batch, nheads]; B, C [batch, ngroups, dstate];
+ *             A [nheads] (a_per_state = 0) or [nheads, dstate] (= 1).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_DISC_EXP_EULER 0
+#define ORACLE_DISC_ZOH 1
+
+/* softplus(v) = log(1 + e^v), written in a form that neither overflows for
+ * large v nor loses the small result for very negative v. */
+double oracle_softplus(double v) {
+    double m = v > 0.0 ? v : 0.0;
+    return m + log1p(exp(-fabs(v)));
+}
+
+/* phi1(z) = (e^z - 1) / z, the ZOH input factor; for |z| < 1e-4 the pages use
+ * the Taylor polynomial 1 + z/2 + z^2/6 to avoid 0/0 ("From S4 to Mamba-3",
+ * Likely questions Q01). */
+double oracle_phi1(double z) {
+    if (fabs(z) < 1e-4) return 1.0 + z / 2.0 + z * z / 6.0;
+    return (exp(z) - 1.0) / z;
+}
+
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+static double step_delta(double raw, const double* bias, int idx, int use_softplus) {
+    double v = raw + (bias ? bias[idx] : 0.0);
+    return use_softplus ? oracle_softplus(v) : v;
+}
+
+/* Discretised input weight for one (Delta, a) pair: Delta under
+ * exponential-Euler, Delta * phi1(Delta * a) under ZOH. */
+static double input_weight(double delta, double a, int disc) {
+    if (disc == ORACLE_DISC_ZOH) return delta * oracle_phi1(delta * a);
+    return delta;
+}
+
+/* Mamba-1 selective scan ("From S4 to Mamba-3", 03/System, mamba_minimal.py):
+ * for every (b, d) run the recurrence over time, for every state n:
+ *   h[n] <- exp(Delta_t A[d,n]) h[n] + w(Delta_t, A[d,n]) B[n,t] x_t
+ *   y_t  = sum_n C[n,t] h[n] + D[d] x_t, then y_t *= SiLU(z_t).          */
+int oracle_mamba1_scan(int batch, int dim, int dstate, int seqlen, int ngroups,
+                       const double* x, const double* delta, const double* delta_bias,
+                       int delta_softplus, const double* A, const double* B, const double* C,
+                       const double* Dskip, const double* z, const double* h0, int disc,
+                       double* y, double* h_final) {
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0 || dim % ngroups)
+        return 1;
+    int per_group = dim / ngroups;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int d = 0; d < dim; ++d) {
+            int g = d / per_group;
+            double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+            size_t row = ((size_t)b * dim + d) * (size_t)seqlen;
+            for (int n = 0; n < dstate; ++n)
+                h[n] = h0 ? h0[((size_t)b * dim + d) * dstate + n] : 0.0;
+            for (int t = 0; t < seqlen; ++t) {
+                double dt = step_delta(delta[row + t], delta_bias, d, delta_softplus);
+                double xt = x[row + t];
+                double acc = 0.0;
+                for (int n = 0; n < dstate; ++n) {
+                    double a = A[(size_t)d * dstate + n];
+                    size_t bc = (((size_t)b * ngroups + g) * dstate + n) * (size_t)seqlen + t;
+                    h[n] = exp(dt * a) * h[n] + input_weight(dt, a, disc) * B[bc] * xt;
+                    acc += C[bc] * h[n];
+                }
+                if (Dskip) acc += Dskip[d] * xt;
+                if (z) acc *= silu(z[row + t]);
+                y[row + t] = acc;
+            }
+            if (h_final)
+                for (int n = 0; n < dstate; ++n)
+                    h_final[((size_t)b * dim + d) * dstate + n] = h[n];
+            free(h);
+        }
+    }
+    return 0;
+}
+
+/* Mamba-2 sequential scan, the reference the pages test the chunked form
+ * against ("From S4 to Mamba-3", 03/System, mamba2_minimal.py): scalar A per
+ * head, state h[p, n] per (batch, head):
+ *   h[p,n] <- exp(Delta_t A_h) h[p,n] + w(Delta_t, A_h) x_t[p] B_t[n]
+ *   y_t[p] = sum_n C_t[n] h[p,n] + D_h x_t[p], then gated.                 */
+int oracle_ssd_sequential(int batch, int seqlen, int nheads, int headdim, int dstate,
+                          int ngroups, const double* x, const double* dt,
+                          const double* dt_bias, int dt_softplus, const double* A,
+                          const double* B, const double* C, const double* Dskip,
+                          const double* z, const double* h0, int disc, double* y,
+                          double* h_final) {
+    if (batch < 0 || seqlen < 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0 ||
+        nheads % ngroups)
+        return 1;
+    int per_group = nheads / ngroups;
+    size_t PN = (size_t)headdim * dstate;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int hd = 0; hd < nheads; ++hd) {
+            int g = hd / per_group;
+            double* h = (double*)malloc(sizeof(double) * PN);
+            for (size_t i = 0; i < PN; ++i)
+                h[i] = h0 ? h0[((size_t)b * nheads + hd) * PN + i] : 0.0;
+            for (int t = 0; t < seqlen; ++t) {
+                double d_t = step_delta(dt[((size_t)b * seqlen + t) * nheads + hd], dt_bias, hd,
+                                        dt_softplus);
+                double decay = exp(d_t * A[hd]);
+                double w = input_weight(d_t, A[hd], disc);
+                const double* xt = x + (((size_t)b * seqlen + t) * nheads + hd) * headdim;
+                const double* Bt = B + (((size_t)b * seqlen + t) * ngroups + g) * dstate;
+                const double* Ct = C + (((size_t)b * seqlen + t) * ngroups + g) * dstate;
+                double* yt = y + (((size_t)b * seqlen + t) * nheads + hd) * headdim;
+                const double* zt = z ? z + (((size_t)b * seqlen + t) * nheads + hd) * headdim : NULL;
+                for (int p = 0; p < headdim; ++p) {
+                    double acc = 0.0;
+                    for (int n = 0; n < dstate; ++n) {
+                        double* hp = h + (size_t)p * dstate + n;
+                        *hp = decay * *hp + w * xt[p] * Bt[n];
+                        acc += Ct[n] * *hp;
+                    }
+                    if (Dskip) acc += Dskip[hd] * xt[p];
+                    if (zt) acc *= silu(zt[p]);
+                    yt[p] = acc;
+                }
+            }
+            if (h_final) memcpy(h_final + ((size_t)b * nheads + hd) * PN, h, sizeof(double) * PN);
+            free(h);
+        }
+    }
+    return 0;
+}
+
+/* Mamba-2 chunked SSD ("From S4 to Mamba-3", 03/System, mamba2_minimal.py, and
+ * 04/Approach "Chunked SSD with a sequential reference"): the sequence is cut
+ * into chunks of Q steps (the last one may be shorter).  Inside a chunk, with
+ * s_t the running sum of Delta*A_h from the chunk start up to and including t:
+ *   decayed attention  y_t += sum_{s<=t} (C_t . B_s) exp(s_t - s_s) w_s x_s
+ *   carried state      y_t += exp(s_t) C_t . h_in
+ *   chunk state        S    = sum_s exp(s_end - s_s) w_s x_s B_s^T   (P x N)
+ *   state passing      h_out = exp(s_end) h_in + S
+ * followed by the skip term and the gate.  This is written independently of
+ * oracle_ssd_sequential and must agree with it. */
+int oracle_ssd_chunked(int batch, int seqlen, int nheads, int headdim, int dstate, int ngroups,
+                       int chunk, const double* x, const double* dt, const double* dt_bias,
+                       int dt_softplus, const double* A, const double* B, const double* C,
+                       const double* Dskip, const double* z, const double* h0, int disc,
+                       double* y, double* h_final) {
+    if (batch < 0 || seqlen < 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0 ||
+        nheads % ngroups || chunk <= 0)
+        return 1;
+    int per_group = nheads / ngroups;
+    size_t PN = (size_t)headdim * dstate;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int hd = 0; hd < nheads; ++hd) {
+            int g = hd / per_group;
+            double* h = (double*)malloc(sizeof(double) * PN);      /* carried state */
+            double* S = (double*)malloc(sizeof(double) * PN);      /* chunk state   */
+            double* cum = (double*)malloc(sizeof(double) * (size_t)chunk);
+            double* w = (double*)malloc(sizeof(double) * (size_t)chunk);
+            for (size_t i = 0; i < PN; ++i)
+                h[i] = h0 ? h0[((size_t)b * nheads + hd) * PN + i] : 0.0;
+            for (int c0 = 0; c0 < seqlen; c0 += chunk) {
+                int q = seqlen - c0 < chunk ? seqlen - c0 : chunk;
+                /* running sums of Delta*A inside the chunk, and input weights */
+                double run = 0.0;
+                for (int i = 0; i < q; ++i) {
+                    int t = c0 + i;
+                    double d_t = step_delta(dt[((size_t)b * seqlen + t) * nheads + hd], dt_bias,
+                                            hd, dt_softplus);
+                    run += d_t * A[hd];
+                    cum[i] = run;
+                    w[i] = input_weight(d_t, A[hd], disc);
+                }
+                /* outputs of the chunk */
+                for (int i = 0; i < q; ++i) {
+                    int t = c0 + i;
+                    const double* Ct = C + (((size_t)b * seqlen + t) * ngroups + g) * dstate;
+                    for (int p = 0; p < headdim; ++p) {
+                        double acc = 0.0;
+                        for (int j = 0; j <= i; ++j) {        /* decayed attention */
+                            int s = c0 + j;
+                            const double* Bs = B + (((size_t)b * seqlen + s) * ngroups + g) * dstate;
+                            double cb = 0.0;
+                            for (int n = 0; n < dstate; ++n) cb += Ct[n] * Bs[n];
+                            double xs = x[(((size_t)b * seqlen + s) * nheads + hd) * headdim + p];
+                            acc += cb * exp(cum[i] - cum[j]) * w[j] * xs;
+                        }
+                        double ch = 0.0;                      /* carried state */
+                        for (int n = 0; n < dstate; ++n) ch += Ct[n] * h[(size_t)p * dstate + n];
+                        acc += exp(cum[i]) * ch;
+                        size_t yi = (((size_t)b * seqlen + t) * nheads + hd) * headdim + p;
+                        if (Dskip) acc += Dskip[hd] * x[yi];
+                        if (z) acc *= silu(z[yi]);
+                        y[yi] = acc;
+                    }
+                }
+                /* chunk state and state passing */
+                for (size_t i = 0; i < PN; ++i) S[i] = 0.0;
+                for (int j = 0; j < q; ++j) {
+                    int s = c0 + j;
+                    double f = exp(cum[q - 1] - cum[j]) * w[j];
+                    const double* Bs = B + (((size_t)b * seqlen + s) * ngroups + g) * dstate;
+                    const double* xs = x + (((size_t)b * seqlen + s) * nheads + hd) * headdim;
+                    for (int p = 0; p < headdim; ++p)
+                        for (int n = 0; n < dstate; ++n)
+                            S[(size_t)p * dstate + n] += f * xs[p] * Bs[n];
+                }
+                double chunk_decay = exp(cum[q - 1]);
+                for (size_t i = 0; i < PN; ++i) h[i] = chunk_decay * h[i] + S[i];
+            }
+            if (h_final) memcpy(h_final + ((size_t)b * nheads + hd) * PN, h, sizeof(double) * PN);
+            free(h);
+            free(S);
+            free(cum);
+            free(w);
+        }
+    }
+    return 0;
+}
+
+/* One decoding step ("From S4 to Mamba-3", 03/System: the incremental step()
+ * of mamba_minimal.py and the O(1)-state recurrent decode).  The state is
+ * updated in place:
+ *   h[p,n] <- exp(Delta A) h[p,n] + w(Delta, A) x[p] B[n]
+ *   y[p]    = sum_n C[n] h[p,n] + D x[p], then gated,
+ * with A = A[h] (a_per_state = 0, Mamba-2 form) or A[h, n] (a_per_state = 1,
+ * Mamba-1 form). */
+int oracle_state_update(int batch, int nheads, int headdim, int dstate, int ngroups,
+                        int a_per_state, double* state, const double* x, const double* dt,
+                        const double* dt_bias, int dt_softplus, const double* A, const double* B,
+                        const double* C, const double* Dskip, const double* z, int disc,
+                        double* y) {
+    if (batch < 0 || nheads <= 0 || headdim <= 0 || dstate <= 0 || ngroups <= 0 ||
+        nheads % ngroups)
+        return 1;
+    int per_group = nheads / ngroups;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int hd = 0; hd < nheads; ++hd) {
+            int g = hd / per_group;
+            double d_t = step_delta(dt[(size_t)b * nheads + hd], dt_bias, hd, dt_softplus);
+            const double* Bb = B + ((size_t)b * ngroups + g) * dstate;
+            const double* Cb = C + ((size_t)b * ngroups + g) * dstate;
+            for (int p = 0; p < headdim; ++p) {
+                size_t xi = ((size_t)b * nheads + hd) * headdim + p;
+                double* hrow = state + xi * dstate;
+                double acc = 0.0;
+                for (int n = 0; n < dstate; ++n) {
+                    double a = a_per_state ? A[(size_t)hd * dstate + n] : A[hd];
+                    hrow[n] = exp(d_t * a) * hrow[n] + input_weight(d_t, a, disc) * x[xi] * Bb[n];
+                    acc += Cb[n] * hrow[n];
+                }
+                if (Dskip) acc += Dskip[hd] * x[xi];
+                if (z) acc *= silu(z[xi]);
+                y[xi] = acc;
+            }
+        }
+    }
+    return 0;
+}
+
+/* Number of OpenMP threads a parallel region here will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,72 @@
+"""Plants plausible mistakes in a COPY of the oracle (on the CPU) and checks that
+the pins in test_oracle_pins.py catch every one of them.  The real oracle is
+never modified."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement): a dropped term, a wrong sign, a wrong
+# index, a transposed operand, a wrong Taylor coefficient, and so on.
+MUTATIONS = [
+    ("drop_skip_term", "if (Dskip) acc += Dskip[d] * xt;", ""),
+    ("gate_sign", "return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    ("y_before_update",
+     "h[n] = exp(dt * a) * h[n] + input_weight(dt, a, disc) * B[bc] * xt;\n                    acc += C[bc] * h[n];",
+     "acc += C[bc] * h[n];\n                    h[n] = exp(dt * a) * h[n] + input_weight(dt, a, disc) * B[bc] * xt;"),
+    ("B_C_swapped", "* B[bc] * xt;", "* C[bc] * xt;"),
+    ("taylor_coefficient", "return 1.0 + z / 2.0 + z * z / 6.0;", "return 1.0 + z / 2.0 + z * z / 2.0;"),
+    ("softplus_sign", "return m + log1p(exp(-fabs(v)));", "return m - log1p(exp(-fabs(v)));"),
+    ("bias_ignored", "double v = raw + (bias ? bias[idx] : 0.0);", "double v = raw;"),
+    ("group_index", "int g = d / per_group;", "int g = d % ngroups;"),
+    ("ssd_decay_sign", "acc += cb * exp(cum[i] - cum[j]) * w[j] * xs;",
+     "acc += cb * exp(cum[j] - cum[i]) * w[j] * xs;"),
+    ("ssd_carried_state_dropped", "acc += exp(cum[i]) * ch;", ""),
+    ("ssd_chunk_state_decay", "double f = exp(cum[q - 1] - cum[j]) * w[j];",
+     "double f = w[j];"),
+    ("ssd_seq_B_index", "acc += Ct[n] * *hp;", "acc += Bt[n] * *hp;"),
+    ("step_zoh_ignored", "hrow[n] = exp(d_t * a) * hrow[n] + input_weight(d_t, a, disc) * x[xi] * Bb[n];",
+     "hrow[n] = exp(d_t * a) * hrow[n] + d_t * x[xi] * Bb[n];"),
+    ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
+     "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
+]
+
+PIN_CHECKS = [
+    lambda o: pins.test_softplus_matches_high_precision(o, -5.0),
+    lambda o: pins.test_softplus_matches_high_precision(o, 3.0),
+    lambda o: pins.test_phi1_log_grid(o),
+    lambda o: pins.test_zoh_steady_state(o),
+    lambda o: pins.test_mamba1_brute_force(o, True, True),
+    lambda o: pins.test_mamba1_brute_force(o, False, True),
+    lambda o: pins.test_ssd_brute_force(o, True),
+    lambda o: pins.test_ssd_brute_force(o, False),
+    lambda o: pins.test_ssd_chunked_equals_sequential(o, 300, 64),
+    lambda o: pins.test_step_response_closed_form(o),
+    lambda o: pins.test_mamba1_decode_equals_scan(o),
+    lambda o: pins.test_ssd_decode_equals_scan(o, False),
+    lambda o: pins.test_ssd_decode_equals_scan(o, True),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, oracle_mod, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation {name} no longer applies"
+    mutated = tmp_path / "oracle_mut.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                    str(mutated), "-o", str(lib), "-lm"], check=True)
+    caught = 0
+    with oracle.use_library(str(lib)):
+        for check in PIN_CHECKS:
+            try:
+                check(oracle)
+            except AssertionError:
+                caught += 1
+    assert caught > 0, f"planted mistake {name!r} passed every pin"
