@@ -1,0 +1,528 @@
+"""Benchmark of the selective-scan hot path on GB300.
+
+Headline: the Mamba-1 selective scan on a Mamba-130m-shaped layer (batch 8, d_inner
+1536, d_state 16, L 2048, bf16 x/delta/z/B/C, fp32 state, SiLU gate), reported as
+state updates per second (batch * L * d_inner * d_state / time) and as achieved HBM
+GB/s against the measured copy bandwidth.  One step = one ssm_scan_fwd call over one
+batch; several input sets (together larger than L2) rotate between steps.
+
+Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
+the decode update (780m-shaped, 1024 steps) and the long-context Mamba-1 sweep.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) each rank runs its own batch (weak
+scaling, no collective on the data path) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_scan_mamba_gb300 import synth  # noqa: E402
+
+WORKLOAD = "m1_130m_layer"
+METRIC = "scan state-updates/s (B*L*D*N) and achieved HBM GB/s as % of GB300 peak"
+UNIT = "state-updates/s"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic bytes and work
+# ---------------------------------------------------------------------------------------
+def m1_bytes(batch, dim, N, L, es_in=2, es_out=2, with_z=True, h_final=False):
+    """Each input element read once, each output written once."""
+    per_row = (2 + (1 if with_z else 0)) * es_in + es_out  # x, delta, (z) in; y out
+    b = batch * dim * L * per_row + 2 * batch * N * L * es_in  # + B, C
+    b += dim * N * 4 + dim * 8  # A, D, bias
+    if h_final:
+        b += batch * dim * N * 4
+    return b
+
+
+def ssd_bytes(batch, L, H, P, N, G, es=2, with_z=False):
+    b = batch * L * H * P * es * (2 + (1 if with_z else 0))  # x, (z) in, y out
+    b += batch * L * H * es  # dt
+    b += 2 * batch * L * G * N * es  # B, C
+    b += batch * H * P * N * 4  # h_final
+    return b
+
+
+def ssd_flops(batch, L, H, P, N, G, Q):
+    """Dense per-chunk tile products: C.B^T (per group), (CB^T o L).X, chunk states, C.h."""
+    nch = -(-L // Q)
+    per_bhc = 2 * Q * Q * P + 2 * P * Q * N + 2 * Q * N * P
+    per_bgc = 2 * Q * Q * N
+    return batch * nch * (H * per_bhc + G * per_bgc)
+
+
+def step_bytes(batch, H, P, N, G, es=2, with_z=True):
+    b = 2 * batch * H * P * N * 4  # state read + write
+    b += batch * H * P * es * (2 + (1 if with_z else 0))  # x, z, y
+    b += batch * H * es + 2 * batch * G * N * es
+    return b
+
+
+# ---------------------------------------------------------------------------------------
+# clocks under load
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as fh:
+                for line in fh:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 8:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        loaded = [s for s, p in zip(sm, pw) if p is not None and p > 250.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = []
+        for i, n in enumerate(names):
+            if any(r[4 + i].lower() == "active" for r in rows):
+                reasons.append(n)
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def _dev(inp, torch):
+    out = {}
+    for k, v in inp.arrays.items():
+        if inp.dtypes[k] == synth.BF16:
+            out[k] = torch.from_numpy(synth.bf16_bits(v).view(np.int16).copy()).cuda().view(
+                torch.bfloat16)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v)).cuda()
+    return out
+
+
+def time_launches(torch, fn, n, warmup, stream):
+    """Average device time of fn() over n calls, CUDA events on the launching stream."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / n
+
+
+def bench_ours(args, rank, world):
+    import torch
+    import selective_scan_mamba_gb300 as ssm
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", dev))
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+    cfg = synth.WORKLOADS[WORKLOAD]
+    Bt, D, N, L = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"]
+    inp = synth.mamba1(Bt, D, N, L, dtype=cfg["dtype"], delta_scale=cfg["delta_scale"],
+                       with_z=cfg["with_z"], seed=rank)
+    base = _dev(inp, torch)
+    # rotating input sets: together larger than L2 (129 MB), so no step reads another's
+    # inputs from cache
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = m1_bytes(Bt, D, N, L)
+    nsets = max(2, -(-3 * l2 // set_bytes))
+    sets = []
+    for k in range(nsets):
+        s = {n: (torch.roll(t, shifts=17 * k, dims=-1).contiguous()
+                 if n in ("x", "delta", "z", "B", "C") else t) for n, t in base.items()}
+        s["y"] = torch.empty_like(s["x"])
+        sets.append(s)
+    torch.cuda.synchronize()
+
+    def step(i):
+        s = sets[i % nsets]
+        ssm.ssm_scan_fwd(s["x"], s["delta"], s["A"], s["B"], s["C"], D=s["D"], z=s["z"],
+                         delta_bias=s["delta_bias"], y=s["y"])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    with ClockSampler(dev) as clk:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    clocks = clk.summary()
+    if dist:
+        tt = torch.tensor([t_step], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step = float(tt.item())
+    updates = Bt * L * D * N
+    value = updates * world / t_step
+    gbs = set_bytes / t_step / 1e9
+
+    # end to end through the public API with host buffers: pinned inputs copied in,
+    # y copied back, every step inside the timed region
+    host = {n: t.cpu().pin_memory() for n, t in sets[0].items() if n in ("x", "delta", "z", "B", "C")}
+    dbuf = {n: torch.empty_like(sets[0][n]) for n in host}
+    y_host = torch.empty(sets[0]["y"].shape, dtype=sets[0]["y"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step(i):
+        for n, t in host.items():
+            dbuf[n].copy_(t, non_blocking=True)
+        s = sets[0]
+        y = ssm.ssm_scan_fwd(dbuf["x"], dbuf["delta"], s["A"], dbuf["B"], dbuf["C"], D=s["D"],
+                             z=dbuf["z"], delta_bias=s["delta_bias"], y=s["y"])
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    t_e2e = time_launches(torch, e2e_step, e2e_steps, 2, stream)
+    if dist:
+        tt = torch.tensor([t_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+
+    paths = {}
+    if rank == 0 and not args.headline_only:
+        paths = other_paths(args, torch, ssm, peaks, stream, l2)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Mamba-1 selective scan, Mamba-130m-shaped layer",
+                   "batch": Bt, "d_inner": D, "d_state": N, "seq_len": L,
+                   "inputs": "bf16 x, delta, z, B, C; fp32 A, D, bias; fp32 state; bf16 y",
+                   "l2": f"{nsets} rotating input sets, {nsets * set_bytes / 1e6:.0f} MB > "
+                         f"L2 {l2 / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "hbm_gbs": gbs,
+        "hbm_frac": gbs / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("m1_scan_tiled"),
+                     "kernel": "m1_scan_tiled", "bytes_per_launch": set_bytes,
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)"},
+        "e2e": {"value": updates * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "paths": paths,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_seconds)
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = _source_digest()
+    try:
+        with open(path) as fh:
+            for line in fh:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == kernel and parts[2] == src:
+                    return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+def _source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_scan_mamba_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def other_paths(args, torch, ssm, peaks, stream, l2):
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    # Mamba-2 chunked SSD, 130m-shaped
+    c4 = synth.WORKLOADS["ssd_130m"]
+    s_inp = synth.ssd(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
+                      c4["ngroups"], dtype=c4["dtype"], delta_scale=c4["delta_scale"], seed=0)
+    t = _dev(s_inp, torch)
+    nb = ssd_bytes(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
+                   c4["ngroups"])
+    nsets = max(2, -(-3 * l2 // nb))
+    sets = []
+    for k in range(nsets):
+        s = {n: (torch.roll(v, shifts=k, dims=1).contiguous() if n in ("x", "dt", "B", "C") else v)
+             for n, v in t.items()}
+        s["y"] = torch.empty_like(s["x"])
+        s["hf"] = torch.empty((c4["batch"], c4["nheads"], c4["headdim"], c4["dstate"]),
+                              dtype=torch.float32, device="cuda")
+        sets.append(s)
+    for Q in c4["chunks"]:
+        ws = torch.empty(ssm.ssd_chunk_scan_workspace_size(sets[0]["x"], sets[0]["B"], Q),
+                         dtype=torch.uint8, device="cuda")
+
+        def f(i, Q=Q, ws=ws):
+            s = sets[i % nsets]
+            ssm.ssd_chunk_scan_fwd(s["x"], s["dt"], s["A"], s["B"], s["C"], Q, D=s["D"],
+                                   dt_bias=s["dt_bias"], y=s["y"], h_final=s["hf"], workspace=ws)
+        n = max(5, min(args.steps, 20))
+        tsec = time_launches(torch, f, n, 3, stream)
+        fl = ssd_flops(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
+                       c4["ngroups"], Q)
+        t_roof = max(nb / (hbm * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+        upd = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
+        out[f"ssd_130m_chunk{Q}"] = {
+            "ms": tsec * 1e3, "state_updates_per_s": upd / tsec, "hbm_gbs": nb / tsec / 1e9,
+            "tflops": fl / tsec / 1e12, "roofline_s": t_roof, "roofline_frac": t_roof / tsec,
+            "bytes": nb, "flops": fl}
+    del sets
+    # decode step, 780m-shaped: 4 layers' states rotate (each 100.7 MB; together > L2)
+    c5 = synth.WORKLOADS["step_780m"]
+    Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
+    par = _dev(synth.step_params(H, N, seed=0), torch)
+    states = [torch.from_numpy(synth.step_state(Bt, H, P, N, seed=k)).cuda() for k in range(4)]
+    toks = [_dev(synth.step_tokens(Bt, H, P, N, G, step=k, seed=0), torch) for k in range(8)]
+    y = torch.empty((Bt, H, P), dtype=torch.bfloat16, device="cuda")
+
+    def g(i):
+        tk = toks[i % 8]
+        ssm.ssm_state_update(states[i % 4], tk["x"], tk["dt"], par["A"], tk["B"], tk["C"],
+                             D=par["D"], z=tk["z"], dt_bias=par["dt_bias"], y=y)
+    steps = c5["steps"]
+    # the 1024-step decode is captured once in a CUDA graph and replayed
+    gs = torch.cuda.Stream()
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        for i in range(4):
+            g(i)
+    stream.wait_stream(gs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(steps):
+            g(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    tstep = e0.elapsed_time(e1) / 1e3 / steps
+    sb = step_bytes(Bt, H, P, N, G)
+    out["decode_780m"] = {"us_per_step": tstep * 1e6, "steps": steps,
+                          "state_updates_per_s": Bt * H * P * N / tstep,
+                          "hbm_gbs": sb / tstep / 1e9, "hbm_frac": sb / tstep / 1e9 / hbm,
+                          "bytes_per_step": sb, "note": "4 layer states rotate (403 MB > L2)"}
+    del states, graph
+    # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
+    c3 = synth.WORKLOADS["m1_790m_long"]
+    sweep = {}
+    for L in c3["seqlens"]:
+        inp = synth.mamba1(1, c3["dim"], c3["dstate"], L, dtype=c3["dtype"],
+                           delta_scale=c3["delta_scale"], with_z=False, seed=0)
+        tt = _dev(inp, torch)
+        yb = torch.empty_like(tt["x"])
+        hf = torch.empty((1, c3["dim"], c3["dstate"]), dtype=torch.float32, device="cuda")
+
+        def m(i, tt=tt, yb=yb, hf=hf):
+            ssm.ssm_scan_fwd(tt["x"], tt["delta"], tt["A"], tt["B"], tt["C"], D=tt["D"],
+                             delta_bias=tt["delta_bias"], y=yb, h_final=hf)
+        tsec = time_launches(torch, m, 5, 2, stream)
+        nbytes = m1_bytes(1, c3["dim"], c3["dstate"], L, with_z=False, h_final=True)
+        sweep[str(L)] = {"ms": tsec * 1e3,
+                         "state_updates_per_s": c3["dim"] * c3["dstate"] * L / tsec,
+                         "hbm_gbs": nbytes / tsec / 1e9, "hbm_frac": nbytes / tsec / 1e9 / hbm}
+        del tt, yb, hf
+    out["m1_790m_long"] = sweep
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# CPU baseline: the float64 oracle, as it stands, on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------
+def cpu_baseline(inp, budget_s=10.0):
+    import oracle
+    oracle.build()
+    f = inp.f64
+    dims = inp.dims
+    D, N, L = dims["dim"], dims["dstate"], dims["seqlen"]
+    x, dl, z = f("x"), f("delta"), f("z")
+    B, C, A, Dv, bias = f("B"), f("C"), f("A"), f("D"), f("delta_bias")
+
+    batch = dims["batch"]
+
+    def run(nb):
+        t0 = time.perf_counter()
+        oracle.mamba1_scan(x[:nb], dl[:nb], A, B[:nb], C[:nb], D=Dv,
+                           z=None if z is None else z[:nb], delta_bias=bias)
+        return time.perf_counter() - t0
+
+    # whole batch rows of the workload, repeated until about budget_s of CPU time
+    nb, reps, total = 1, 0, 0.0
+    first = run(1)
+    nb = max(1, min(batch, int(budget_s / max(first, 1e-3) / 4)))
+    while total < budget_s and reps < 64:
+        total += run(nb)
+        reps += 1
+    upd = reps * nb * D * L * N
+    return {"value": upd / total, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} x {nb} batch rows ({nb * D} channels x {L} steps x {N} states), "
+                      f"float64 sequential oracle, {total:.1f} s"}
+
+
+def bench_reference(args, rank, world):
+    """The reference arm is the float64 CPU oracle on this workload (each step a bounded
+    sample), timed on the host cores; rank 0 only."""
+    if rank != 0:
+        return None
+    cfg = synth.WORKLOADS[WORKLOAD]
+    inp = synth.mamba1(1, cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
+                       delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+    import oracle
+    oracle.build()
+    f = inp.f64
+    nch = 96
+    args_ = (f("x")[:, :nch], f("delta")[:, :nch], f("A")[:nch], f("B"), f("C"))
+    kw = dict(D=f("D")[:nch], z=f("z")[:, :nch], delta_bias=f("delta_bias")[:nch])
+    for _ in range(args.warmup):
+        oracle.mamba1_scan(*args_, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mamba1_scan(*args_, **kw)
+    dt = (time.perf_counter() - t0) / args.steps
+    L, N = cfg["seqlen"], cfg["dstate"]
+    value = nch * L * N / dt
+    sample = f"{nch} channels of one batch row per step ({L} steps x {N} states), float64 oracle"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "Mamba-1 selective scan, Mamba-130m-shaped layer",
+                       "batch": cfg["batch"], "d_inner": cfg["dim"], "d_state": N, "seq_len": L},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the SSD, decode and long-context measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        res = bench_reference(args, rank, world)
+    else:
+        res = bench_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * ssmscan.h -- C ABI of libssmscan, a single-GPU (GB300, sm_103a) library of the
+ * selective state-space scan used by Mamba-1 and Mamba-2.
+ *
+ * The operation, as the pages describe it ("From S4 to Mamba-3", ssmbench case
+ * study, section 03/System):
+ *   - mamba_minimal.py: Mamba-1 makes Delta, B and C input-dependent (selective)
+ *     and runs the scan as an explicit time loop; an incremental step() serves
+ *     decoding and must equal the full forward pass (09/Validation).
+ *   - mamba2_minimal.py: with a scalar A per head the recurrence becomes SSD,
+ *     computed as chunked decayed-attention matmuls with a carried (N, P) state;
+ *     it must equal the sequential scan for aligned and misaligned chunk sizes
+ *     (04/Approach "Chunked SSD with a sequential reference").
+ *   - s4_minimal.py and Likely questions Q01: exact ZOH for a diagonal A gives
+ *     B-bar = Delta*B*(e^z - 1)/z, z = Delta*a (optional here, SSM_DISC_ZOH).
+ *   - mamba3_minimal.py / 04/Approach: the exponential-Euler rule A-bar =
+ *     exp(Delta*A), B-bar = Delta*B that Mamba-3 reduces to at lambda = 1,
+ *     theta = 0 (the default here, SSM_DISC_EXP_EULER).
+ *
+ * In formulas, per channel (Mamba-1) or per head (Mamba-2), for t = 0..L-1:
+ *   Delta_t = softplus(delta_t + bias)      (or delta_t + bias without softplus)
+ *   h_t     = exp(Delta_t A) (.) h_{t-1} + w_t B_t x_t,
+ *             w_t = Delta_t (exp-Euler) or Delta_t (e^z - 1)/z, z = Delta_t A (ZOH)
+ *   y_t     = (C_t . h_t + D x_t) * SiLU(z_t)     (gate only when z is given)
+ * with h_{-1} = h0 (zeros when h0 is NULL) and h_final = h_{L-1}.
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every buffer.  The library allocates nothing
+ *     and keeps no state except a per-thread error message.
+ *   - Pointers: every tensor pointer is a DEVICE pointer of the current CUDA
+ *     device; tensors are dense, row-major (last index fastest), and 16-byte
+ *     aligned.  Optional tensors (marked "nullable") may be NULL.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Every call is asynchronous on that stream; results are
+ *     ready when the stream reaches that point.
+ *   - Errors: arguments are validated before anything is launched.  Bad
+ *     arguments return SSM_ERR_INVALID_ARG, shapes outside what the kernels
+ *     support return SSM_ERR_UNSUPPORTED, and a failed launch returns
+ *     SSM_ERR_CUDA; in each case ssm_last_error() describes the problem and
+ *     nothing has been written.  There is no CPU fallback.
+ *   - Aliasing: outputs must not overlap inputs, except the decode state, which
+ *     is updated in place by design.
+ *   - Precision: inputs are bfloat16 or float32; A, D, biases and all states are
+ *     float32; every accumulation is float32.
+ */
+#ifndef SSMSCAN_H
+#define SSMSCAN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSM_ABI_VERSION 1
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,  /* null required pointer, bad size, misaligned pointer */
+    SSM_ERR_UNSUPPORTED = 2,  /* valid, but outside the shapes the kernels implement */
+    SSM_ERR_CUDA = 3,         /* a CUDA call or launch failed */
+    SSM_ERR_TIMEOUT = 4       /* reserved: a bounded device-side wait gave up */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef enum {
+    SSM_DISC_EXP_EULER = 0,   /* A-bar = exp(Delta A), B-bar = Delta B                 */
+    SSM_DISC_ZOH = 1          /* A-bar = exp(Delta A), B-bar = Delta B (e^z - 1)/z     */
+} ssm_disc;
+
+/* ---------------------------------------------------------------------------
+ * Mamba-1 selective scan (diagonal A per channel)
+ *   ("From S4 to Mamba-3", 03/System, mamba_minimal.py)
+ *
+ * Shapes, Bt = batch, D = dim (d_inner), N = dstate, L = seqlen, G = ngroups:
+ *   x, delta, z : [Bt, D, L]   in_dtype        (z nullable: no gate)
+ *   y           : [Bt, D, L]   out_dtype
+ *   B, C        : [Bt, G, N, L] in_dtype       (channel d uses group d / (D / G))
+ *   A           : [D, N]       float32
+ *   D_skip      : [D]          float32         (nullable: no skip term)
+ *   delta_bias  : [D]          float32         (nullable: zero)
+ *   h0, h_final : [Bt, D, N]   float32         (nullable: zero start / not written)
+ * Limits: 1 <= N <= 256, G divides D, L >= 0 (L = 0 only copies h0 to h_final).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int batch, dim, dstate, seqlen, ngroups;
+    ssm_dtype in_dtype, out_dtype;
+    const void* x;
+    const void* delta;
+    const float* delta_bias;
+    int delta_softplus;        /* nonzero: Delta = softplus(delta + bias) */
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D_skip;
+    const void* z;
+    const float* h0;
+    void* y;
+    float* h_final;
+    ssm_disc disc;
+} ssm_scan_params;
+
+/* Device scratch the scan needs for this problem, in bytes (0 for most shapes:
+ * long sequences with few channels are split in time and carry their segment
+ * states through this buffer). */
+size_t ssm_scan_workspace_size(const ssm_scan_params* p);
+
+/* Runs the scan.  `workspace` is a device buffer of at least
+ * ssm_scan_workspace_size(p) bytes (may be NULL when that is 0); its contents
+ * on entry do not matter. */
+ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Mamba-2 chunked SSD scan (scalar A per head)
+ *   ("From S4 to Mamba-3", 03/System, mamba2_minimal.py; 04/Approach)
+ *
+ * Shapes, Bt = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
+ * G = ngroups, Q = chunk_size:
+ *   x, z, y     : [Bt, L, H, P]   in_dtype / out_dtype for y  (z nullable)
+ *   dt          : [Bt, L, H]      in_dtype
+ *   dt_bias     : [H]             float32 (nullable)
+ *   A, D_skip   : [H]             float32 (D_skip nullable)
+ *   B, C        : [Bt, L, G, N]   in_dtype (head h uses group h / (H / G))
+ *   h0, h_final : [Bt, H, P, N]   float32 (nullable)
+ * The sequence is processed in chunks of Q steps; the last chunk may be short.
+ * Inside a chunk the output is a decayed-attention product and chunk states are
+ * passed between chunks, so the result equals the sequential scan up to
+ * rounding.  Limits: Q in {64, 128, 256}; P in {32, 64, 128}; N in {64, 128};
+ * G divides H.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
+    ssm_dtype in_dtype, out_dtype;
+    const void* x;
+    const void* dt;
+    const float* dt_bias;
+    int dt_softplus;           /* nonzero: Delta = softplus(dt + dt_bias) */
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D_skip;
+    const void* z;
+    const float* h0;
+    void* y;
+    float* h_final;
+    ssm_disc disc;
+} ssd_params;
+
+/* Device scratch needed by ssd_chunk_scan_fwd, in bytes (the float32 chunk
+ * states and per-chunk decay sums).  Only the sizes in `p` are read; returns 0
+ * when they are invalid or unsupported. */
+size_t ssd_chunk_scan_workspace_size(const ssd_params* p);
+
+/* Runs the chunked scan; `workspace` is a device buffer of at least
+ * ssd_chunk_scan_workspace_size(p) bytes, contents on entry irrelevant. */
+ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-step decode update, in place on the state
+ *   ("From S4 to Mamba-3", 03/System: the incremental step() for decoding)
+ *
+ * Shapes, Bt = batch, H = nheads, P = headdim, N = dstate, G = ngroups:
+ *   state  : [Bt, H, P, N]  float32, read and overwritten with the new state
+ *   x, z, y: [Bt, H, P]     in_dtype / out_dtype for y  (z nullable)
+ *   dt     : [Bt, H]        in_dtype;  dt_bias [H] float32 (nullable)
+ *   A      : [H] float32 (a_per_state = 0, Mamba-2 form) or
+ *            [H, N] float32 (a_per_state = 1, Mamba-1 form: H = channels, P = 1)
+ *   B, C   : [Bt, G, N]     in_dtype (head h uses group h / (H / G))
+ *   D_skip : [H] float32 (nullable)
+ * Limits: N a multiple of 4 up to 256 for the vectorised path (other N are
+ * served by a scalar path); G divides H.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int batch, nheads, headdim, dstate, ngroups;
+    int a_per_state;
+    ssm_dtype in_dtype, out_dtype;
+    float* state;
+    const void* x;
+    const void* dt;
+    const float* dt_bias;
+    int dt_softplus;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D_skip;
+    const void* z;
+    void* y;
+    ssm_disc disc;
+} ssm_step_params;
+
+ssm_status ssm_state_update(const ssm_step_params* p, void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* ssm_last_error(void);
+
+/* SSM_ABI_VERSION of the loaded library. */
+int ssm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSMSCAN_H */

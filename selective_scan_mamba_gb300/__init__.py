@@ -1,0 +1,237 @@
+"""selective_scan_mamba_gb300 -- GB300-native selective state-space scan.
+
+A thin Python binding over libssmscan's C ABI (include/ssmscan.h).  The three entry
+points keep the C names:
+
+  * ssm_scan_fwd        -- Mamba-1 selective scan (diagonal A per channel)
+  * ssd_chunk_scan_fwd  -- Mamba-2 chunked SSD scan (scalar A per head)
+  * ssm_state_update    -- one decode step, in place on the state
+
+Each takes CUDA torch tensors in the library's layouts, checks them, fills the C
+parameter struct and calls the library on the current torch stream.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and a missing GPU or library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import SsmError  # noqa: F401
+
+__all__ = ["ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+           "ssd_chunk_scan_workspace_size", "SsmError", "lib"]
+
+
+def lib():
+    """The loaded shared library (ctypes.CDLL)."""
+    return _lib.load()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return _lib.SSM_BF16
+    if t.dtype == torch.float32:
+        return _lib.SSM_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _out_dtype(code):
+    torch = _torch()
+    return torch.bfloat16 if code == _lib.SSM_BF16 else torch.float32
+
+
+def _ptr(t, name, shape=None, dtype=None):
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _disc(disc):
+    if disc in ("exp_euler", _lib.SSM_DISC_EXP_EULER, None):
+        return _lib.SSM_DISC_EXP_EULER
+    if disc in ("zoh", _lib.SSM_DISC_ZOH):
+        return _lib.SSM_DISC_ZOH
+    raise ValueError(f"unknown discretisation {disc!r}")
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final, disc):
+    torch = _torch()
+    batch, dim, L = x.shape
+    if B.dim() == 3:
+        B = B.unsqueeze(1)
+        C = C.unsqueeze(1)
+    G, N = B.shape[1], B.shape[2]
+    f32 = torch.float32
+    p = _lib.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = batch, dim, N, L, G
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(y)
+    p.x = _ptr(x, "x")
+    p.delta = _ptr(delta, "delta", (batch, dim, L), x.dtype)
+    p.delta_bias = _ptr(delta_bias, "delta_bias", (dim,), f32)
+    p.delta_softplus = int(bool(delta_softplus))
+    p.A = _ptr(A, "A", (dim, N), f32)
+    p.B = _ptr(B, "B", (batch, G, N, L), x.dtype)
+    p.C = _ptr(C, "C", (batch, G, N, L), x.dtype)
+    p.D_skip = _ptr(D, "D", (dim,), f32)
+    p.z = _ptr(z, "z", (batch, dim, L), x.dtype)
+    p.h0 = _ptr(h0, "h0", (batch, dim, N), f32)
+    p.y = _ptr(y, "y", (batch, dim, L))
+    p.h_final = _ptr(h_final, "h_final", (batch, dim, N), f32)
+    p.disc = _disc(disc)
+    return p
+
+
+def ssm_scan_workspace_size(x, B) -> int:
+    """Scratch bytes ssm_scan_fwd needs for these shapes."""
+    p = _lib.ScanParams()
+    p.batch, p.dim, p.seqlen = x.shape
+    p.dstate = B.shape[-2]
+    p.ngroups = 1 if B.dim() == 3 else B.shape[1]
+    return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
+
+
+def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 h0=None, *, y=None, h_final=None, out_dtype=None, return_final_state=False,
+                 disc="exp_euler", workspace=None, stream=None):
+    """Mamba-1 selective scan.
+
+    x, delta, z: [batch, dim, L] (bfloat16 or float32); B, C: [batch, G, N, L] or
+    [batch, N, L]; A: [dim, N] float32; D, delta_bias: [dim] float32; h0: [batch, dim, N]
+    float32.  Returns y [batch, dim, L] (dtype ``out_dtype``, default x's), and the final
+    state [batch, dim, N] float32 when ``return_final_state``.
+    """
+    torch = _torch()
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    if return_final_state and h_final is None:
+        h_final = torch.empty((x.shape[0], x.shape[1], A.shape[1]), dtype=torch.float32,
+                              device=x.device)
+    p = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final, disc)
+    need = int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    _lib.check(lib().ssm_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    return (y, h_final) if return_final_state else y
+
+
+def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h_final, disc):
+    torch = _torch()
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    f32 = torch.float32
+    p = _lib.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = batch, L, H, P, N, G
+    p.chunk_size = int(chunk_size)
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(y)
+    p.x = _ptr(x, "x")
+    p.dt = _ptr(dt, "dt", (batch, L, H), x.dtype)
+    p.dt_bias = _ptr(dt_bias, "dt_bias", (H,), f32)
+    p.dt_softplus = int(bool(dt_softplus))
+    p.A = _ptr(A, "A", (H,), f32)
+    p.B = _ptr(B, "B", (batch, L, G, N), x.dtype)
+    p.C = _ptr(C, "C", (batch, L, G, N), x.dtype)
+    p.D_skip = _ptr(D, "D", (H,), f32)
+    p.z = _ptr(z, "z", (batch, L, H, P), x.dtype)
+    p.h0 = _ptr(h0, "h0", (batch, H, P, N), f32)
+    p.y = _ptr(y, "y", (batch, L, H, P))
+    p.h_final = _ptr(h_final, "h_final", (batch, H, P, N), f32)
+    p.disc = _disc(disc)
+    return p
+
+
+def ssd_chunk_scan_workspace_size(x, B, chunk_size) -> int:
+    """Scratch bytes ssd_chunk_scan_fwd needs for these shapes and chunk size."""
+    p = _lib.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim = x.shape
+    p.ngroups, p.dstate = B.shape[2], B.shape[3]
+    p.chunk_size = int(chunk_size)
+    p.in_dtype = _lib.SSM_BF16
+    p.out_dtype = _lib.SSM_BF16
+    return int(lib().ssd_chunk_scan_workspace_size(ctypes.byref(p)))
+
+
+def ssd_chunk_scan_fwd(x, dt, A, B, C, chunk_size=64, D=None, z=None, dt_bias=None,
+                       dt_softplus=True, h0=None, *, y=None, h_final=None, out_dtype=None,
+                       return_final_state=False, disc="exp_euler", workspace=None, stream=None):
+    """Mamba-2 chunked SSD scan.
+
+    x, z: [batch, L, H, P]; dt: [batch, L, H]; B, C: [batch, L, G, N] (bfloat16 or
+    float32); A, D, dt_bias: [H] float32; h0: [batch, H, P, N] float32.  Returns y
+    [batch, L, H, P] and, when ``return_final_state``, the final state.
+    """
+    torch = _torch()
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    if return_final_state and h_final is None:
+        h_final = torch.empty((x.shape[0], x.shape[2], x.shape[3], B.shape[3]),
+                              dtype=torch.float32, device=x.device)
+    p = _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h_final, disc)
+    need = int(lib().ssd_chunk_scan_workspace_size(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _lib.check(lib().ssd_chunk_scan_fwd(ctypes.byref(p), workspace.data_ptr(), workspace.numel(),
+                                        _stream(stream)))
+    return (y, h_final) if return_final_state else y
+
+
+def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, *,
+                     y=None, out_dtype=None, disc="exp_euler", stream=None):
+    """One decode step, updating ``state`` [batch, H, P, N] float32 in place.
+
+    x, z: [batch, H, P]; dt: [batch, H]; B, C: [batch, G, N]; A: [H] (Mamba-2 form) or
+    [H, N] (Mamba-1 form); D, dt_bias: [H].  Returns y [batch, H, P].
+    """
+    torch = _torch()
+    batch, H, P, N = state.shape
+    G = B.shape[1]
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    f32 = torch.float32
+    p = _lib.StepParams()
+    p.batch, p.nheads, p.headdim, p.dstate, p.ngroups = batch, H, P, N, G
+    p.a_per_state = 1 if A.dim() == 2 else 0
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(y)
+    p.state = _ptr(state, "state", (batch, H, P, N), f32)
+    p.x = _ptr(x, "x", (batch, H, P))
+    p.dt = _ptr(dt, "dt", (batch, H), x.dtype)
+    p.dt_bias = _ptr(dt_bias, "dt_bias", (H,), f32)
+    p.dt_softplus = int(bool(dt_softplus))
+    p.A = _ptr(A, "A", (H, N) if A.dim() == 2 else (H,), f32)
+    p.B = _ptr(B, "B", (batch, G, N), x.dtype)
+    p.C = _ptr(C, "C", (batch, G, N), x.dtype)
+    p.D_skip = _ptr(D, "D", (H,), f32)
+    p.z = _ptr(z, "z", (batch, H, P), x.dtype)
+    p.y = _ptr(y, "y", (batch, H, P))
+    p.disc = _disc(disc)
+    _lib.check(lib().ssm_state_update(ctypes.byref(p), _stream(stream)))
+    return y

@@ -1,0 +1,300 @@
+// api.cu -- the C ABI of libssmscan: argument checks, launch planning, status codes.
+// Every check runs on the host before anything is launched; a rejected call touches
+// neither the GPU nor any buffer.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "launch.h"
+#include "ssmscan.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+ssm_status fail(ssm_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ssm_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(SSM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dtype_ok(ssm_dtype d) { return d == SSM_F32 || d == SSM_BF16; }
+
+// Host-side fault hook for tests of the error paths: SSM_FAULT_INJECT=launch makes the
+// next launch report a CUDA error without touching the GPU.
+bool injected_launch_fault() {
+    const char* v = getenv("SSM_FAULT_INJECT");
+    return v && strcmp(v, "launch") == 0;
+}
+
+#define REQUIRE(cond, ...)                                    \
+    do {                                                      \
+        if (!(cond)) return fail(SSM_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+#define REQUIRE_PTR(p, name)                                                       \
+    do {                                                                           \
+        if ((p) == nullptr) return fail(SSM_ERR_INVALID_ARG, "%s is NULL", name);  \
+        if (!aligned16(p)) return fail(SSM_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+#define OPTIONAL_PTR(p, name)                                                      \
+    do {                                                                           \
+        if ((p) != nullptr && !aligned16(p))                                       \
+            return fail(SSM_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);   \
+    } while (0)
+
+ssm_status check_scan(const ssm_scan_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->batch >= 1 && p->dim >= 1 && p->dstate >= 1 && p->seqlen >= 0 && p->ngroups >= 1,
+            "bad sizes: batch=%d dim=%d dstate=%d seqlen=%d ngroups=%d", p->batch, p->dim,
+            p->dstate, p->seqlen, p->ngroups);
+    REQUIRE(p->dim % p->ngroups == 0, "ngroups=%d does not divide dim=%d", p->ngroups, p->dim);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(p->disc == SSM_DISC_EXP_EULER || p->disc == SSM_DISC_ZOH, "unknown discretisation");
+    REQUIRE(static_cast<long long>(p->batch) * p->dim * (p->seqlen > 0 ? p->seqlen : 1) < (1LL << 40),
+            "tensor too large");
+    if (p->dstate > 256) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 256", p->dstate);
+    if (static_cast<long long>(p->batch) * p->dim > (1LL << 31) - 1)
+        return fail(SSM_ERR_UNSUPPORTED, "batch*dim too large");
+    REQUIRE_PTR(p->A, "A");
+    OPTIONAL_PTR(p->delta_bias, "delta_bias");
+    OPTIONAL_PTR(p->D_skip, "D_skip");
+    OPTIONAL_PTR(p->h0, "h0");
+    OPTIONAL_PTR(p->h_final, "h_final");
+    if (p->seqlen > 0) {
+        REQUIRE_PTR(p->x, "x");
+        REQUIRE_PTR(p->delta, "delta");
+        REQUIRE_PTR(p->B, "B");
+        REQUIRE_PTR(p->C, "C");
+        REQUIRE_PTR(p->y, "y");
+        OPTIONAL_PTR(p->z, "z");
+    }
+    return SSM_OK;
+}
+
+ssm::M1Args scan_args(const ssm_scan_params* p) {
+    ssm::M1Args a;
+    a.batch = p->batch;
+    a.dim = p->dim;
+    a.dstate = p->dstate;
+    a.seqlen = p->seqlen;
+    a.ngroups = p->ngroups;
+    a.in_dtype = p->in_dtype;
+    a.out_dtype = p->out_dtype;
+    a.x = p->x;
+    a.delta = p->delta;
+    a.delta_bias = p->delta_bias;
+    a.delta_softplus = p->delta_softplus;
+    a.A = p->A;
+    a.B = p->B;
+    a.C = p->C;
+    a.D = p->D_skip;
+    a.z = p->z;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.h_final = p->h_final;
+    a.disc = p->disc;
+    a.cpb_max = 0;
+    return a;
+}
+
+ssm_status check_ssd_sizes(const ssd_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->batch >= 1 && p->seqlen >= 0 && p->nheads >= 1 && p->headdim >= 1 &&
+                p->dstate >= 1 && p->ngroups >= 1 && p->chunk_size >= 1,
+            "bad sizes: batch=%d seqlen=%d nheads=%d headdim=%d dstate=%d ngroups=%d chunk=%d",
+            p->batch, p->seqlen, p->nheads, p->headdim, p->dstate, p->ngroups, p->chunk_size);
+    REQUIRE(p->nheads % p->ngroups == 0, "ngroups=%d does not divide nheads=%d", p->ngroups,
+            p->nheads);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(p->disc == SSM_DISC_EXP_EULER || p->disc == SSM_DISC_ZOH, "unknown discretisation");
+    if (p->chunk_size != 64 && p->chunk_size != 128 && p->chunk_size != 256)
+        return fail(SSM_ERR_UNSUPPORTED, "chunk_size=%d (supported: 64, 128, 256)", p->chunk_size);
+    if (p->headdim != 32 && p->headdim != 64 && p->headdim != 128)
+        return fail(SSM_ERR_UNSUPPORTED, "headdim=%d (supported: 32, 64, 128)", p->headdim);
+    if (p->dstate != 64 && p->dstate != 128)
+        return fail(SSM_ERR_UNSUPPORTED, "dstate=%d (supported: 64, 128)", p->dstate);
+    if (p->headdim * p->dstate > 8192)
+        return fail(SSM_ERR_UNSUPPORTED, "headdim*dstate=%d > 8192", p->headdim * p->dstate);
+    return SSM_OK;
+}
+
+ssm_status check_ssd(const ssd_params* p) {
+    ssm_status st = check_ssd_sizes(p);
+    if (st != SSM_OK) return st;
+    REQUIRE_PTR(p->A, "A");
+    OPTIONAL_PTR(p->dt_bias, "dt_bias");
+    OPTIONAL_PTR(p->D_skip, "D_skip");
+    OPTIONAL_PTR(p->h0, "h0");
+    OPTIONAL_PTR(p->h_final, "h_final");
+    if (p->seqlen > 0) {
+        REQUIRE_PTR(p->x, "x");
+        REQUIRE_PTR(p->dt, "dt");
+        REQUIRE_PTR(p->B, "B");
+        REQUIRE_PTR(p->C, "C");
+        REQUIRE_PTR(p->y, "y");
+        OPTIONAL_PTR(p->z, "z");
+    }
+    return SSM_OK;
+}
+
+ssm_status check_step(const ssm_step_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->batch >= 1 && p->nheads >= 1 && p->headdim >= 1 && p->dstate >= 1 &&
+                p->ngroups >= 1,
+            "bad sizes: batch=%d nheads=%d headdim=%d dstate=%d ngroups=%d", p->batch, p->nheads,
+            p->headdim, p->dstate, p->ngroups);
+    REQUIRE(p->nheads % p->ngroups == 0, "ngroups=%d does not divide nheads=%d", p->ngroups,
+            p->nheads);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(p->disc == SSM_DISC_EXP_EULER || p->disc == SSM_DISC_ZOH, "unknown discretisation");
+    REQUIRE(p->a_per_state == 0 || p->a_per_state == 1, "a_per_state must be 0 or 1");
+    if (p->dstate > 4096) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 4096", p->dstate);
+    REQUIRE_PTR(p->state, "state");
+    REQUIRE_PTR(p->x, "x");
+    REQUIRE_PTR(p->dt, "dt");
+    REQUIRE_PTR(p->A, "A");
+    REQUIRE_PTR(p->B, "B");
+    REQUIRE_PTR(p->C, "C");
+    REQUIRE_PTR(p->y, "y");
+    OPTIONAL_PTR(p->dt_bias, "dt_bias");
+    OPTIONAL_PTR(p->D_skip, "D_skip");
+    OPTIONAL_PTR(p->z, "z");
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_abi_version(void) { return SSM_ABI_VERSION; }
+
+const char* ssm_last_error(void) { return g_err; }
+
+size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
+    (void)p;
+    return 0;
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    g_err[0] = '\0';
+    ssm_status st = check_scan(p);
+    if (st != SSM_OK) return st;
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->seqlen == 0) {
+        if (p->h_final) {
+            const size_t bytes = static_cast<size_t>(p->batch) * p->dim * p->dstate * sizeof(float);
+            cudaError_t e = p->h0 ? cudaMemcpyAsync(p->h_final, p->h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(p->h_final, 0, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd (empty sequence)");
+        }
+        return SSM_OK;
+    }
+    ssm::M1Args a = scan_args(p);
+    ssm::M1Plan plan;
+    cudaError_t e = ssm::m1_plan(a, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd plan");
+    e = ssm::m1_launch(a, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
+    return SSM_OK;
+}
+
+size_t ssd_chunk_scan_workspace_size(const ssd_params* p) {
+    if (check_ssd_sizes(p) != SSM_OK) return 0;
+    return ssm::ssd_workspace_bytes(p->batch, p->seqlen, p->nheads, p->headdim, p->dstate,
+                                    p->chunk_size);
+}
+
+ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_ssd(p);
+    if (st != SSM_OK) return st;
+    const size_t need = ssm::ssd_workspace_bytes(p->batch, p->seqlen, p->nheads, p->headdim,
+                                                 p->dstate, p->chunk_size);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    ssm::SsdArgs a;
+    a.batch = p->batch;
+    a.seqlen = p->seqlen;
+    a.nheads = p->nheads;
+    a.headdim = p->headdim;
+    a.dstate = p->dstate;
+    a.ngroups = p->ngroups;
+    a.chunk = p->chunk_size;
+    a.in_dtype = p->in_dtype;
+    a.out_dtype = p->out_dtype;
+    a.x = p->x;
+    a.dt = p->dt;
+    a.dt_bias = p->dt_bias;
+    a.dt_softplus = p->dt_softplus;
+    a.A = p->A;
+    a.B = p->B;
+    a.C = p->C;
+    a.D = p->D_skip;
+    a.z = p->z;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.h_final = p->h_final;
+    a.disc = p->disc;
+    const size_t nch = (static_cast<size_t>(p->seqlen) + p->chunk_size - 1) / p->chunk_size;
+    const size_t states = static_cast<size_t>(p->batch) * p->nheads * nch * p->headdim * p->dstate *
+                          sizeof(float);
+    a.ws_states = static_cast<float*>(workspace);
+    a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((states + 255) / 256) * 256);
+    cudaError_t e = ssm::ssd_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_chunk_scan_fwd launch");
+    return SSM_OK;
+}
+
+ssm_status ssm_state_update(const ssm_step_params* p, void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_step(p);
+    if (st != SSM_OK) return st;
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    ssm::StepArgs a;
+    a.batch = p->batch;
+    a.nheads = p->nheads;
+    a.headdim = p->headdim;
+    a.dstate = p->dstate;
+    a.ngroups = p->ngroups;
+    a.a_per_state = p->a_per_state;
+    a.in_dtype = p->in_dtype;
+    a.out_dtype = p->out_dtype;
+    a.state = p->state;
+    a.x = p->x;
+    a.dt = p->dt;
+    a.dt_bias = p->dt_bias;
+    a.dt_softplus = p->dt_softplus;
+    a.A = p->A;
+    a.B = p->B;
+    a.C = p->C;
+    a.D = p->D_skip;
+    a.z = p->z;
+    a.y = p->y;
+    a.disc = p->disc;
+    cudaError_t e = ssm::step_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_state_update launch");
+    return SSM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// launch.h -- internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "ssmscan.h"
+
+namespace ssm {
+
+constexpr int kM1MaxThreads = 384;  // block-size cap of the tiled Mamba-1 kernel
+constexpr int kM1MaxPairs = 2;      // (batch, group) B/C rows one CTA may span
+
+// Mamba-1 scan arguments (device pointers, dims) as the kernels see them.
+struct M1Args {
+    int batch, dim, dstate, seqlen, ngroups;
+    ssm_dtype in_dtype, out_dtype;
+    const void* x;
+    const void* delta;
+    const float* delta_bias;
+    int delta_softplus;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* h0;
+    void* y;
+    float* h_final;
+    ssm_disc disc;
+    int cpb_max;  // channels per CTA (tiled path)
+};
+
+struct M1Plan {
+    enum Kind { kGeneric = 0, kTiled = 1 } kind;
+    int tpc;      // threads per channel (tiled path)
+    int grid;     // CTAs (tiled path)
+    int cpb_max;  // channels per CTA (tiled path)
+    size_t smem;  // dynamic shared memory per CTA (tiled path)
+};
+
+size_t m1_tiled_smem_bytes(int cpb, int N, int T, size_t elem_size);
+int m1_tile_steps(ssm_dtype in_dtype);
+cudaError_t m1_plan(const M1Args& a, M1Plan* plan);
+cudaError_t m1_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
+
+// Decode-step arguments.
+struct StepArgs {
+    int batch, nheads, headdim, dstate, ngroups, a_per_state;
+    ssm_dtype in_dtype, out_dtype;
+    float* state;
+    const void* x;
+    const void* dt;
+    const float* dt_bias;
+    int dt_softplus;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    void* y;
+    ssm_disc disc;
+};
+cudaError_t step_launch(const StepArgs& a, cudaStream_t s);
+
+// SSD arguments.
+struct SsdArgs {
+    int batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
+    ssm_dtype in_dtype, out_dtype;
+    const void* x;
+    const void* dt;
+    const float* dt_bias;
+    int dt_softplus;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* h0;
+    void* y;
+    float* h_final;
+    ssm_disc disc;
+    float* ws_states;  // [batch, nheads, nchunks, headdim, dstate] chunk states, then h_in
+    float* ws_decay;   // [batch, nheads, nchunks] exp(sum of Delta*A over the chunk)
+};
+size_t ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, int chunk);
+cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
+
+}  // namespace ssm

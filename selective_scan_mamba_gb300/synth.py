@@ -28,8 +28,9 @@ BF16 = "bf16"
 def bf16_bits(a) -> np.ndarray:
     """Round float32 values to bfloat16 (round to nearest, ties to even); return the
     16-bit patterns as uint16.  Inputs are finite."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    # finite inputs stay below 0xFF800000, so the sum cannot wrap in 32 bits
+    r = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
     return r.astype(np.uint16)
 
 

@@ -1,0 +1,160 @@
+"""Host-side checks of the C ABI, no GPU needed: the library builds and loads, exports
+every entry point include/ssmscan.h declares, and rejects bad arguments before it
+launches anything (so these calls never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_scan_mamba_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssmscan.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:ssm_status|size_t|int|const char\*)\s+(\w+)\s*\(",
+                                 text, re.M)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_lib.SYMBOLS) <= set(declared_functions())
+
+
+def test_abi_version(lib):
+    assert lib.ssm_abi_version() == 1
+
+
+
+FAKE = 0x7F0000000000  # a 16-byte aligned address; never dereferenced by these calls
+
+
+def scan_params(**kw):
+    p = _lib.ScanParams()
+    p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = 2, 32, 16, 64, 1
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    for f in ("x", "delta", "A", "B", "C", "y"):
+        setattr(p, f, FAKE)
+    p.delta_softplus = 1
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, _lib.SSM_ERR_INVALID_ARG),
+    ("dim", -1, _lib.SSM_ERR_INVALID_ARG),
+    ("seqlen", -5, _lib.SSM_ERR_INVALID_ARG),
+    ("ngroups", 3, _lib.SSM_ERR_INVALID_ARG),   # does not divide dim
+    ("in_dtype", 7, _lib.SSM_ERR_INVALID_ARG),
+    ("disc", 9, _lib.SSM_ERR_INVALID_ARG),
+    ("dstate", 300, _lib.SSM_ERR_UNSUPPORTED),
+    ("x", None, _lib.SSM_ERR_INVALID_ARG),
+    ("y", FAKE + 8, _lib.SSM_ERR_INVALID_ARG),  # misaligned
+    ("A", None, _lib.SSM_ERR_INVALID_ARG),
+    ("h0", FAKE + 4, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_scan_rejects_bad_arguments(lib, field, value, status):
+    p = scan_params(**{field: value})
+    rc = lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None)
+    assert rc == status
+    assert lib.ssm_last_error().decode()
+
+
+def test_scan_null_params(lib):
+    assert lib.ssm_scan_fwd(None, None, 0, None) == _lib.SSM_ERR_INVALID_ARG
+
+
+def ssd_params(**kw):
+    p = _lib.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = 2, 256, 4, 64, 128, 1, 64
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    for f in ("x", "dt", "A", "B", "C", "y"):
+        setattr(p, f, FAKE)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("chunk_size", 100, _lib.SSM_ERR_UNSUPPORTED),
+    ("headdim", 48, _lib.SSM_ERR_UNSUPPORTED),
+    ("dstate", 16, _lib.SSM_ERR_UNSUPPORTED),
+    ("ngroups", 3, _lib.SSM_ERR_INVALID_ARG),
+    ("nheads", 0, _lib.SSM_ERR_INVALID_ARG),
+    ("B", None, _lib.SSM_ERR_INVALID_ARG),
+    ("dt", FAKE + 2, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_ssd_rejects_bad_arguments(lib, field, value, status):
+    p = ssd_params(**{field: value})
+    need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
+    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, max(need, 1 << 30), None)
+    assert rc == status
+
+
+def test_ssd_workspace_size_and_shortfall(lib):
+    p = ssd_params()
+    need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
+    nch = 256 // 64
+    assert need >= 2 * 4 * nch * 64 * 128 * 4
+    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, need - 1, None)
+    assert rc == _lib.SSM_ERR_INVALID_ARG
+    assert "workspace" in lib.ssm_last_error().decode()
+    assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(ssd_params(chunk_size=7))) == 0
+
+
+def step_params(**kw):
+    p = _lib.StepParams()
+    p.batch, p.nheads, p.headdim, p.dstate, p.ngroups = 4, 8, 16, 64, 1
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    for f in ("state", "x", "dt", "A", "B", "C", "y"):
+        setattr(p, f, FAKE)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("state", None, _lib.SSM_ERR_INVALID_ARG),
+    ("a_per_state", 2, _lib.SSM_ERR_INVALID_ARG),
+    ("ngroups", 3, _lib.SSM_ERR_INVALID_ARG),
+    ("headdim", 0, _lib.SSM_ERR_INVALID_ARG),
+    ("z", FAKE + 1, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_step_rejects_bad_arguments(lib, field, value, status):
+    p = step_params(**{field: value})
+    assert lib.ssm_state_update(ctypes.byref(p), None) == status
+
+
+def test_injected_launch_fault_reports_cuda_error(lib, monkeypatch):
+    """The host-side fault hook turns a valid call into SSM_ERR_CUDA before any CUDA call."""
+    monkeypatch.setenv("SSM_FAULT_INJECT", "launch")
+    assert lib.ssm_state_update(ctypes.byref(step_params()), None) == _lib.SSM_ERR_CUDA
+    assert "injected" in lib.ssm_last_error().decode()
+    assert lib.ssm_scan_fwd(ctypes.byref(scan_params()), None, 0, None) == _lib.SSM_ERR_CUDA
+    p = ssd_params()
+    need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, need, None) == _lib.SSM_ERR_CUDA
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import selective_scan_mamba_gb300 as ssm
+    x = torch.zeros(1, 4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssm.ssm_scan_fwd(x, x, torch.zeros(4, 16), torch.zeros(1, 16, 8, dtype=torch.bfloat16),
+                         torch.zeros(1, 16, 8, dtype=torch.bfloat16))

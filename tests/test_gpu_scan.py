@@ -1,0 +1,190 @@
+"""GPU parity of the Mamba-1 selective scan (ssm_scan_fwd) against the float64 oracle.
+
+Inputs come from the seeded generator; the oracle reads the identical values.  The
+tolerance is max|y_gpu - y_ref| <= 1e-5 max|y_ref| for float32 inputs and
+2e-3 max|y_ref| for bfloat16 inputs with float32 state (the same for h_final); a
+bfloat16 output may in addition differ by the half-ulp of its own rounding.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import selective_scan_mamba_gb300 as ssm
+from selective_scan_mamba_gb300 import synth
+from tests.helpers import TOL_BF16, TOL_F32, check, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def run_gpu(inp, out_dtype=None, disc="exp_euler", final=True, h0=True, softplus=True):
+    import torch
+    t = to_device(inp)
+    od = {"bf16": torch.bfloat16, "f32": torch.float32}[out_dtype] if out_dtype else None
+    y, hf = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t.get("D"),
+                             z=t.get("z"), delta_bias=t["delta_bias"], delta_softplus=softplus,
+                             h0=t.get("h0") if h0 else None, out_dtype=od,
+                             return_final_state=True, disc=disc)
+    torch.cuda.synchronize()
+    return to_numpy(y), to_numpy(hf)
+
+
+def run_oracle(oracle, inp, disc=0, h0=True, rows=None, softplus=True):
+    f = inp.f64
+    x, dl, z = f("x"), f("delta"), f("z")
+    B, C, h0a = f("B"), f("C"), f("h0") if h0 else None
+    A, D, bias = f("A"), f("D"), f("delta_bias")
+    if rows is not None:  # a sample of (b, d) channels, run one at a time
+        ys, hs = [], []
+        for b, d in rows:
+            y, h = oracle.mamba1_scan(x[b:b + 1, d:d + 1], dl[b:b + 1, d:d + 1], A[d:d + 1],
+                                      B[b:b + 1, :1] if B.shape[1] == 1 else
+                                      B[b:b + 1, d // (x.shape[1] // B.shape[1])][:, None],
+                                      C[b:b + 1, :1] if C.shape[1] == 1 else
+                                      C[b:b + 1, d // (x.shape[1] // C.shape[1])][:, None],
+                                      D=None if D is None else D[d:d + 1],
+                                      z=None if z is None else z[b:b + 1, d:d + 1],
+                                      delta_bias=bias[d:d + 1], delta_softplus=softplus,
+                                      h0=None if h0a is None else h0a[b:b + 1, d:d + 1], disc=disc)
+            ys.append(y[0, 0])
+            hs.append(h[0, 0])
+        return np.stack(ys), np.stack(hs)
+    return oracle.mamba1_scan(x, dl, A, B, C, D=D, z=z, delta_bias=bias, delta_softplus=softplus,
+                              h0=h0a, disc=disc)
+
+
+def test_tiny_fp32_config(oracle_mod):
+    """Mamba-1 selective scan fwd, tiny, fp32: batch 1, d_inner 64, d_state 16, L 256."""
+    inp = synth.mamba1(1, 64, 16, 256, dtype=synth.F32, delta_scale=0.5, with_z=False, seed=0)
+    y, hf = run_gpu(inp, h0=False)
+    yr, hr = run_oracle(oracle_mod, inp, h0=False)
+    check(y, yr, TOL_F32, what="y")
+    check(hf, hr, TOL_F32, what="h_final")
+
+
+@pytest.mark.parametrize("tpc", ["1", "2", "4"])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_bf16_tiled_multi_cta_ragged(oracle_mod, monkeypatch, tpc, out):
+    """Several CTAs, CTAs spanning a batch boundary, a ragged last tile, z, D, h0."""
+    monkeypatch.setenv("SSM_M1_TPC", tpc)
+    inp = synth.mamba1(3, 200, 16, 136, dtype=synth.BF16, delta_scale=1.0, with_z=True,
+                       with_h0=True, seed=1)
+    y, hf = run_gpu(inp, out_dtype=out)
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, out_bf16=(out == "bf16"), what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
+@pytest.mark.parametrize("tpc", ["2", "4"])
+def test_fp32_tiled_with_gate_and_groups(oracle_mod, monkeypatch, tpc):
+    monkeypatch.setenv("SSM_M1_TPC", tpc)
+    inp = synth.mamba1(2, 320, 16, 100, dtype=synth.F32, with_z=True, with_h0=True, ngroups=2,
+                       seed=2)
+    y, hf = run_gpu(inp, out_dtype="f32")
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_F32, what="y")
+    check(hf, hr, TOL_F32, what="h_final")
+
+
+@pytest.mark.parametrize("L,N,dtype,disc", [
+    (33, 16, synth.BF16, "exp_euler"),   # row not a whole number of 16-byte chunks
+    (31, 5, synth.F32, "exp_euler"),     # dstate outside the tiled set
+    (64, 16, synth.F32, "zoh"),          # ZOH discretisation
+    (17, 40, synth.BF16, "zoh"),
+    (1, 16, synth.F32, "exp_euler"),
+    (2, 3, synth.F32, "exp_euler"),
+])
+def test_generic_path(oracle_mod, L, N, dtype, disc):
+    inp = synth.mamba1(2, 12, N, L, dtype=dtype, with_z=True, with_h0=True, seed=3)
+    y, hf = run_gpu(inp, disc=disc)
+    yr, hr = run_oracle(oracle_mod, inp, disc=1 if disc == "zoh" else 0)
+    tol = TOL_F32 if dtype == synth.F32 else TOL_BF16
+    check(y, yr, tol, out_bf16=(dtype == synth.BF16), what="y")
+    check(hf, hr, tol, what="h_final")
+
+
+def test_no_softplus_no_skip(oracle_mod):
+    inp = synth.mamba1(2, 40, 16, 64, dtype=synth.F32, with_D=False, seed=4)
+    # without softplus the step is delta + bias: keep it positive
+    inp.arrays["delta"] = np.abs(inp.arrays["delta"]) * 0.1
+    inp.arrays["delta_bias"] = np.full_like(inp.arrays["delta_bias"], 0.01)
+    y, hf = run_gpu(inp, h0=False, softplus=False)
+    yr, hr = run_oracle(oracle_mod, inp, h0=False, softplus=False)
+    check(y, yr, TOL_F32, what="y")
+    check(hf, hr, TOL_F32, what="h_final")
+
+
+def test_empty_sequence_copies_state():
+    import torch
+    inp = synth.mamba1(2, 8, 16, 0, dtype=synth.BF16, with_h0=True, seed=5)
+    y, hf = run_gpu(inp)
+    assert y.shape == (2, 8, 0)
+    assert np.array_equal(hf, inp.arrays["h0"].astype(np.float64))
+
+
+def test_split_continuation_matches_full(oracle_mod):
+    """scan(0:L) equals scan(0:k) followed by scan(k:L) from the carried state."""
+    import torch
+    inp = synth.mamba1(2, 64, 16, 256, dtype=synth.F32, with_z=True, with_h0=True, seed=6)
+    t = to_device(inp)
+    y, hf = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                             delta_bias=t["delta_bias"], h0=t["h0"], return_final_state=True)
+    k = 96
+    part = {n: t[n][..., :k].contiguous() for n in ("x", "delta", "z", "B", "C")}
+    rest = {n: t[n][..., k:].contiguous() for n in ("x", "delta", "z", "B", "C")}
+    y1, h1 = ssm.ssm_scan_fwd(part["x"], part["delta"], t["A"], part["B"], part["C"], D=t["D"],
+                              z=part["z"], delta_bias=t["delta_bias"], h0=t["h0"],
+                              return_final_state=True)
+    y2, h2 = ssm.ssm_scan_fwd(rest["x"], rest["delta"], t["A"], rest["B"], rest["C"], D=t["D"],
+                              z=rest["z"], delta_bias=t["delta_bias"], h0=h1,
+                              return_final_state=True)
+    torch.cuda.synchronize()
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(to_numpy(torch.cat([y1, y2], dim=-1)), yr, TOL_F32, what="y split")
+    check(to_numpy(h2), hr, TOL_F32, what="h split")
+
+
+def _sample_rows(batch, dim, n, seed):
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(batch * dim, size=n, replace=False)
+    rows = [(int(i) // dim, int(i) % dim) for i in idx]
+    # always include the first and last channels and a batch boundary
+    rows += [(0, 0), (batch - 1, dim - 1)] + ([(1, 0), (0, dim - 1)] if batch > 1 else [])
+    return sorted(set(rows))
+
+
+def test_130m_layer_full_size_sampled(oracle_mod):
+    """Mamba-1 130m-shaped layer scan (batch 8, d_inner 1536, d_state 16, L 2048, bf16, z),
+    in the launch configuration the benchmark times; 48 sampled channels checked."""
+    cfg = synth.WORKLOADS["m1_130m_layer"]
+    inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
+                       delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+    y, hf = run_gpu(inp, h0=False)
+    rows = _sample_rows(cfg["batch"], cfg["dim"], 44, seed=1)
+    yr, hr = run_oracle(oracle_mod, inp, h0=False, rows=rows)
+    ys = np.stack([y[b, d] for b, d in rows])
+    hs = np.stack([hf[b, d] for b, d in rows])
+    # the normalisation is the max over the sampled rows of the reference
+    check(ys, yr, TOL_BF16, out_bf16=True, what="y sampled")
+    check(hs, hr, TOL_BF16, what="h_final sampled")
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("L", [1024, 32768])
+def test_790m_long_context_sampled(oracle_mod, L):
+    """Long-context sweep, Mamba-1 790m-shaped: batch 1, d_inner 3072, d_state 16, no z."""
+    cfg = synth.WORKLOADS["m1_790m_long"]
+    inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], L, dtype=cfg["dtype"],
+                       delta_scale=cfg["delta_scale"], with_z=False, seed=0)
+    y, hf = run_gpu(inp, h0=False)
+    rows = _sample_rows(1, cfg["dim"], 20, seed=2)
+    yr, hr = run_oracle(oracle_mod, inp, h0=False, rows=rows)
+    check(np.stack([y[b, d] for b, d in rows]), yr, TOL_BF16, out_bf16=True, what="y sampled")
+    check(np.stack([hf[b, d] for b, d in rows]), hr, TOL_BF16, what="h_final sampled")

@@ -1,0 +1,114 @@
+"""GPU parity of the Mamba-2 chunked SSD scan (ssd_chunk_scan_fwd) against the float64
+oracle's sequential scan (the reference the pages test the chunked form against).
+Tolerances as in test_gpu_scan.py."""
+import numpy as np
+import pytest
+
+import selective_scan_mamba_gb300 as ssm
+from selective_scan_mamba_gb300 import synth
+from tests.helpers import TOL_BF16, TOL_F32, check, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def run_gpu(inp, chunk, out_dtype=None, disc="exp_euler", h0=True):
+    import torch
+    t = to_device(inp)
+    od = {"bf16": torch.bfloat16, "f32": torch.float32}[out_dtype] if out_dtype else None
+    y, hf = ssm.ssd_chunk_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk, D=t.get("D"),
+                                   z=t.get("z"), dt_bias=t["dt_bias"],
+                                   h0=t.get("h0") if h0 else None, out_dtype=od,
+                                   return_final_state=True, disc=disc)
+    torch.cuda.synchronize()
+    return to_numpy(y), to_numpy(hf)
+
+
+def run_oracle(oracle, inp, disc=0, h0=True, heads=None):
+    f = inp.f64
+    args = dict(D=f("D"), z=f("z"), dt_bias=f("dt_bias"), h0=f("h0") if h0 else None, disc=disc)
+    if heads is None:
+        return oracle.ssd_sequential(f("x"), f("dt"), f("A"), f("B"), f("C"), **args)
+    # sampled (b, h): run the oracle on one batch row and one head at a time
+    H = f("x").shape[2]
+    G = f("B").shape[2]
+    ys, hs = [], []
+    for b, h in heads:
+        g = h // (H // G)
+        sl = lambda a: None if a is None else a  # noqa: E731
+        y, hf = oracle.ssd_sequential(
+            f("x")[b:b + 1, :, h:h + 1], f("dt")[b:b + 1, :, h:h + 1], f("A")[h:h + 1],
+            f("B")[b:b + 1, :, g:g + 1], f("C")[b:b + 1, :, g:g + 1],
+            D=None if args["D"] is None else args["D"][h:h + 1],
+            z=None if args["z"] is None else args["z"][b:b + 1, :, h:h + 1],
+            dt_bias=args["dt_bias"][h:h + 1],
+            h0=None if args["h0"] is None else args["h0"][b:b + 1, h:h + 1], disc=disc)
+        ys.append(y[0, :, 0])
+        hs.append(hf[0, 0])
+    return np.stack(ys), np.stack(hs)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("P,N", [(64, 128), (32, 64), (128, 64)])
+def test_small_ragged(oracle_mod, chunk, P, N):
+    """Several chunks and a ragged last chunk (L = 300), 2 groups, z, D, h0, bf16."""
+    inp = synth.ssd(2, 300, 4, P, N, 2, dtype=synth.BF16, with_z=True, with_h0=True, seed=1)
+    y, hf = run_gpu(inp, chunk)
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, out_bf16=True, what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_fp32_inputs(oracle_mod, chunk):
+    inp = synth.ssd(2, 200, 3, 64, 64, 1, dtype=synth.F32, with_z=True, with_h0=True, seed=2)
+    y, hf = run_gpu(inp, chunk, out_dtype="f32")
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_F32, what="y")
+    check(hf, hr, TOL_F32, what="h_final")
+
+
+def test_zoh(oracle_mod):
+    inp = synth.ssd(1, 130, 2, 64, 128, 1, dtype=synth.F32, with_z=False, seed=3)
+    y, hf = run_gpu(inp, 64, out_dtype="f32", disc="zoh", h0=False)
+    yr, hr = run_oracle(oracle_mod, inp, disc=1, h0=False)
+    check(y, yr, TOL_F32, what="y")
+    check(hf, hr, TOL_F32, what="h_final")
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65])
+def test_short_sequences(oracle_mod, L):
+    inp = synth.ssd(1, L, 2, 32, 64, 1, dtype=synth.BF16, with_z=True, with_h0=True, seed=4)
+    y, hf = run_gpu(inp, 64, out_dtype="f32")
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
+def test_empty_sequence():
+    inp = synth.ssd(1, 0, 2, 32, 64, 1, dtype=synth.BF16, with_h0=True, seed=5)
+    y, hf = run_gpu(inp, 64)
+    assert y.shape == (1, 0, 2, 32)
+    assert np.array_equal(hf, inp.arrays["h0"].astype(np.float64))
+
+
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_130m_full_size_sampled(oracle_mod, chunk):
+    """Mamba-2 SSD 130m-shaped: batch 4, 24 heads x headdim 64, d_state 128, ngroups 1,
+    L 4096; 6 sampled (batch, head) pairs against the sequential oracle."""
+    cfg = synth.WORKLOADS["ssd_130m"]
+    inp = synth.ssd(cfg["batch"], cfg["seqlen"], cfg["nheads"], cfg["headdim"], cfg["dstate"],
+                    cfg["ngroups"], dtype=cfg["dtype"], delta_scale=cfg["delta_scale"],
+                    with_z=False, seed=0)
+    y, hf = run_gpu(inp, chunk, h0=False)
+    heads = [(0, 0), (0, 23), (1, 7), (2, 12), (3, 0), (3, 23)]
+    yr, hr = run_oracle(oracle_mod, inp, h0=False, heads=heads)
+    check(np.stack([y[b, :, h] for b, h in heads]), yr, TOL_BF16, out_bf16=True, what="y sampled")
+    check(np.stack([hf[b, h] for b, h in heads]), hr, TOL_BF16, what="h_final sampled")
+    assert np.all(np.isfinite(y))

@@ -1,0 +1,97 @@
+"""GPU parity of the decode step (ssm_state_update) against the float64 oracle, step by
+step, and decode-equals-scan on the GPU.  Tolerances as in test_gpu_scan.py."""
+import numpy as np
+import pytest
+
+import selective_scan_mamba_gb300 as ssm
+from selective_scan_mamba_gb300 import synth
+from tests.helpers import TOL_BF16, TOL_F32, check, to_device, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def _steps(oracle, batch, H, P, N, G, nsteps, dtype, a_per_state=False, disc="exp_euler",
+           with_z=True, rows=None, seed=0):
+    import torch
+    par = synth.step_params(H, N, a_per_state=a_per_state, seed=seed)
+    tp = to_device(par)
+    st0 = synth.step_state(batch, H, P, N, seed=seed)
+    state = torch.from_numpy(st0).cuda()
+    ref_state = st0.astype(np.float64)
+    if rows is not None:
+        ref_state = ref_state[rows]
+    fp = par.f64
+    tol = TOL_F32 if dtype == synth.F32 else TOL_BF16
+    for k in range(nsteps):
+        tok = synth.step_tokens(batch, H, P, N, G, step=k, dtype=dtype, with_z=with_z, seed=seed)
+        tt = to_device(tok)
+        y = ssm.ssm_state_update(state, tt["x"], tt["dt"], tp["A"], tt["B"], tt["C"], D=tp["D"],
+                                 z=tt.get("z"), dt_bias=tp["dt_bias"], disc=disc,
+                                 out_dtype=torch.float32)
+        f = tok.f64
+        sel = (lambda a: a) if rows is None else (lambda a: None if a is None else a[rows])
+        yr, ref_state = oracle.state_update(ref_state, sel(f("x")), sel(f("dt")), fp("A"),
+                                            sel(f("B")), sel(f("C")), D=fp("D"), z=sel(f("z")),
+                                            dt_bias=fp("dt_bias"),
+                                            disc=1 if disc == "zoh" else 0)
+        torch.cuda.synchronize()
+        if rows is None:
+            yg, sg = to_numpy(y), to_numpy(state)
+        else:
+            idx = torch.tensor(rows, device=state.device)
+            yg, sg = to_numpy(y[idx]), to_numpy(state[idx])
+        check(yg, yr, tol, what=f"y step {k}")
+        check(sg, ref_state, tol, what=f"state step {k}")
+
+
+@pytest.mark.parametrize("N", [16, 32, 64, 128, 256, 24])
+def test_mamba2_form(oracle_mod, N):
+    _steps(oracle_mod, 3, 4, 8, N, 2, 6, synth.BF16)
+
+
+def test_mamba2_form_fp32_zoh(oracle_mod):
+    _steps(oracle_mod, 2, 4, 16, 64, 1, 5, synth.F32, disc="zoh")
+
+
+def test_mamba1_form(oracle_mod):
+    """Mamba-1 decode: heads are channels, headdim 1, A [channels, N]."""
+    _steps(oracle_mod, 4, 48, 1, 16, 1, 8, synth.F32, a_per_state=True)
+
+
+def test_decode_equals_scan_on_gpu():
+    """Feeding the scan's inputs one step at a time through ssm_state_update reproduces
+    ssm_scan_fwd's outputs and final state (step() equals the full forward)."""
+    import torch
+    batch, dim, N, L = 2, 64, 16, 40
+    inp = synth.mamba1(batch, dim, N, L, dtype=synth.F32, with_z=True, with_h0=True, seed=7)
+    t = to_device(inp)
+    y, hf = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                             delta_bias=t["delta_bias"], h0=t["h0"], return_final_state=True)
+    state = t["h0"].clone().view(batch, dim, 1, N)
+    ys = []
+    for k in range(L):
+        yk = ssm.ssm_state_update(state, t["x"][:, :, k:k + 1].contiguous(),
+                                  t["delta"][:, :, k].contiguous(), t["A"],
+                                  t["B"][:, :, :, k].contiguous(), t["C"][:, :, :, k].contiguous(),
+                                  D=t["D"], z=t["z"][:, :, k:k + 1].contiguous(),
+                                  dt_bias=t["delta_bias"])
+        ys.append(yk)
+    torch.cuda.synchronize()
+    check(to_numpy(torch.cat(ys, dim=2)), to_numpy(y), TOL_F32, what="decode vs scan y")
+    check(to_numpy(state.view(batch, dim, N)), to_numpy(hf), TOL_F32, what="decode vs scan h")
+
+
+def test_780m_full_size_every_step_sampled(oracle_mod):
+    """Decode state update, Mamba2-780m-shaped: batch 64, 48 heads x headdim 64, d_state
+    128, 1024 consecutive steps on the GPU; y and state of two batch rows checked against
+    the oracle after every step."""
+    cfg = synth.WORKLOADS["step_780m"]
+    _steps(oracle_mod, cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"],
+           cfg["ngroups"], cfg["steps"], cfg["dtype"], rows=[0, 37])
