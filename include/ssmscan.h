@@ -159,6 +159,35 @@ ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t works
                               void* stream);
 
 /* ---------------------------------------------------------------------------
+ * SSD scan without caller-provided scratch.
+ * (This entry point has no counterpart in the paper; it exists for callers of
+ * the library.)
+ *
+ * ssd_chunk_scan_fwd needs a device workspace from the caller.  Some callers
+ * cannot allocate device memory: a plugin whose host framework reserves all
+ * device memory in its own pool, or a serving loop that forbids allocation
+ * once it is running.  This variant takes the same parameters and keeps its
+ * scratch in one fixed device array inside the library, of
+ * SSM_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
+ * holds until the process exits.  It allocates nothing.
+ *   - Problems whose scratch (ssd_chunk_scan_workspace_size) exceeds the array
+ *     are rejected with SSM_ERR_INVALID_ARG and a message saying so.
+ *   - The first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (that device must be current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the array: calls whose GPU work may overlap (other
+ *     streams, other host threads) race on it; the caller must order them.
+ *     The array keeps the last call's contents, and no part of it needs to
+ *     start at zero.
+ * ------------------------------------------------------------------------- */
+#define SSM_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+ssm_status ssd_chunk_scan_fwd_noalloc(const ssd_params* p, void* stream);
+
+/* Size in bytes of the library's fixed scratch array (SSM_NOALLOC_SCRATCH_BYTES). */
+size_t ssd_noalloc_scratch_capacity(void);
+
+/* ---------------------------------------------------------------------------
  * Single-step decode update, in place on the state
  *   ("From S4 to Mamba-3", 03/System: the incremental step() for decoding)
  *

@@ -177,6 +177,10 @@ ssm_status check_step(const ssm_step_params* p) {
 
 }  // namespace
 
+namespace ssm {
+ssm_status set_error(ssm_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace ssm
+
 extern "C" {
 
 int ssm_abi_version(void) { return SSM_ABI_VERSION; }

@@ -43,6 +43,7 @@ int m1_tile_steps(ssm_dtype in_dtype);
 cudaError_t m1_plan(const M1Args& a, M1Plan* plan);
 cudaError_t m1_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
 
+
 // Decode-step arguments.
 struct StepArgs {
     int batch, nheads, headdim, dstate, ngroups, a_per_state;
@@ -84,5 +85,8 @@ struct SsdArgs {
 };
 size_t ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, int chunk);
 cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
+
+// Records `msg` as this thread's ssm_last_error() text and returns `st`.
+ssm_status set_error(ssm_status st, const char* msg);
 
 }  // namespace ssm

@@ -1,0 +1,77 @@
+"""ssd_chunk_scan_fwd_noalloc: the chunked SSD scan for callers that cannot allocate
+device memory (for example a plugin whose host framework owns every byte of device
+memory, or a serving loop that may not allocate once running).  It keeps its scratch
+in the library's own fixed device array instead of a caller workspace.
+
+Checked here through the C ABI: two calls in a row match the regular entry point
+(which gets a caller workspace) within the parity tolerance, and a problem too big
+for the fixed array is refused with a clear message.  The file name makes pytest
+collect it last."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import selective_scan_mamba_gb300 as ssm
+from selective_scan_mamba_gb300 import _lib, synth
+from tests.helpers import TOL_BF16, check, to_device, to_numpy
+
+
+def _noalloc_fn():
+    lib = _lib.load()
+    fn = lib.ssd_chunk_scan_fwd_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(_lib.SsdParams), ctypes.c_void_p]
+    cap = lib.ssd_noalloc_scratch_capacity
+    cap.restype = ctypes.c_size_t
+    cap.argtypes = []
+    return lib, fn, int(cap())
+
+
+def test_capacity_is_the_documented_32_mib():
+    _, _, cap = _noalloc_fn()
+    assert cap == 32 << 20
+
+
+def test_oversized_problem_is_refused_on_the_host():
+    """Refused before any GPU work: the size query alone decides."""
+    lib, fn, cap = _noalloc_fn()
+    p = _lib.SsdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = \
+        4, 4096, 24, 64, 128, 1, 64
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    fake = 0x7F0000000000
+    for f in ("x", "dt", "A", "B", "C", "y"):
+        setattr(p, f, fake)
+    assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(p)) > cap
+    assert fn(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
+    msg = lib.ssm_last_error().decode()
+    assert "fixed" in msg and "scratch" in msg
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_noalloc_matches_workspace_entry_point_twice(chunk):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    lib, fn, cap = _noalloc_fn()
+    inp = synth.ssd(2, 1000, 8, 64, 128, 2, dtype=synth.BF16, with_z=True, with_h0=True, seed=21)
+    t = to_device(inp)
+    assert ssm.ssd_chunk_scan_workspace_size(t["x"], t["B"], chunk) <= cap
+    y_ref, h_ref = ssm.ssd_chunk_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk,
+                                          D=t["D"], z=t["z"], dt_bias=t["dt_bias"], h0=t["h0"],
+                                          return_final_state=True)
+    torch.cuda.synchronize()
+    y_ref, h_ref = to_numpy(y_ref), to_numpy(h_ref)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        y = torch.full_like(t["x"], float("nan"))
+        hf = torch.full((2, 8, 64, 128), float("nan"), dtype=torch.float32, device="cuda")
+        p = ssm._ssd_params(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk, t["D"], t["z"],
+                            t["dt_bias"], True, t["h0"], y, hf, "exp_euler")
+        rc = fn(ctypes.byref(p), stream)
+        assert rc == _lib.SSM_OK, lib.ssm_last_error().decode()
+        torch.cuda.synchronize()
+        check(to_numpy(y), y_ref, TOL_BF16, out_bf16=True, what=f"y, call {call}")
+        check(to_numpy(hf), h_ref, TOL_BF16, what=f"h_final, call {call}")
