@@ -225,6 +225,11 @@ ssm_status ssm_state_update(const ssm_step_params* p, void* stream);
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* ssm_last_error(void);
 
+/* Diagnostics: how many bounded device-side waits (a kernel waiting for its own
+ * asynchronous copies) gave up since the previous call, on the current device;
+ * 0 in correct operation.  Reading it synchronises with the device and clears it. */
+unsigned int ssm_wait_timeouts(void);
+
 /* SSM_ABI_VERSION of the loaded library. */
 int ssm_abi_version(void);
 

@@ -165,21 +165,8 @@ __device__ __forceinline__ float phi1f(float zz) {
 // ---------------------------------------------------------------------------------------
 // packed float32x2 arithmetic (sm_100+): one instruction, two lanes of work
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
-    unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
-    unsigned long long rc = *reinterpret_cast<unsigned long long*>(&c);
-    unsigned long long rd;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-    return *reinterpret_cast<float2*>(&rd);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    unsigned long long ra = *reinterpret_cast<unsigned long long*>(&a);
-    unsigned long long rb = *reinterpret_cast<unsigned long long*>(&b);
-    unsigned long long rd;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-    return *reinterpret_cast<float2*>(&rd);
-}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // ---------------------------------------------------------------------------------------
 // asynchronous global->shared copies (16 bytes, zero-filled past src_bytes)

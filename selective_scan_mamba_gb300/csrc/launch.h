@@ -31,7 +31,7 @@ struct M1Args {
 };
 
 struct M1Plan {
-    enum Kind { kGeneric = 0, kTiled = 1 } kind;
+    enum Kind { kGeneric = 0, kTiled = 1, kTma = 2 } kind;
     int tpc;      // threads per channel (tiled path)
     int grid;     // CTAs (tiled path)
     int cpb_max;  // channels per CTA (tiled path)
@@ -43,6 +43,16 @@ int m1_tile_steps(ssm_dtype in_dtype);
 cudaError_t m1_plan(const M1Args& a, M1Plan* plan);
 cudaError_t m1_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
 
+// bf16 fast path staged by TMA (scan_m1_tma.cu)
+size_t m1_tma_smem_bytes(int cpb);
+cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan);
+cudaError_t m1_tma_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
+unsigned int m1_tma_wait_timeouts();
+
+// TMA tensor map of a row-major [rows][inner] tensor (tmap.cu)
+cudaError_t encode_tmap_2d(struct CUtensorMap_st* map, const void* base, int elem_bytes,
+                           unsigned long long inner, unsigned long long rows, unsigned box_inner,
+                           unsigned box_rows, bool swizzle128);
 
 // Decode-step arguments.
 struct StepArgs {
