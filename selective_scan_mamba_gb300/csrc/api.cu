@@ -228,24 +228,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
     return SSM_OK;
 }
 
-size_t ssd_chunk_scan_workspace_size(const ssd_params* p) {
-    if (check_ssd_sizes(p) != SSM_OK) return 0;
-    return ssm::ssd_workspace_bytes(p->batch, p->seqlen, p->nheads, p->headdim, p->dstate,
-                                    p->chunk_size);
-}
-
-ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t workspace_bytes,
-                              void* stream) {
-    g_err[0] = '\0';
-    ssm_status st = check_ssd(p);
-    if (st != SSM_OK) return st;
-    const size_t need = ssm::ssd_workspace_bytes(p->batch, p->seqlen, p->nheads, p->headdim,
-                                                 p->dstate, p->chunk_size);
-    if (workspace_bytes < need)
-        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
-    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
-        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
-    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+static ssm::SsdArgs ssd_args(const ssd_params* p, void* workspace) {
     ssm::SsdArgs a;
     a.batch = p->batch;
     a.seqlen = p->seqlen;
@@ -269,11 +252,36 @@ ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t works
     a.y = p->y;
     a.h_final = p->h_final;
     a.disc = p->disc;
-    const size_t nch = (static_cast<size_t>(p->seqlen) + p->chunk_size - 1) / p->chunk_size;
-    const size_t states = static_cast<size_t>(p->batch) * p->nheads * nch * p->headdim * p->dstate *
-                          sizeof(float);
     a.ws_states = static_cast<float*>(workspace);
-    a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((states + 255) / 256) * 256);
+    a.ws_decay = nullptr;
+    return a;
+}
+
+size_t ssd_chunk_scan_workspace_size(const ssd_params* p) {
+    if (check_ssd_sizes(p) != SSM_OK) return 0;
+    return ssm::ssd_workspace_bytes(ssd_args(p, nullptr));
+}
+
+ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_ssd(p);
+    if (st != SSM_OK) return st;
+    ssm::SsdArgs a = ssd_args(p, workspace);
+    const size_t need = ssm::ssd_workspace_bytes(a);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    if (!ssm::ssd_tc_supported(a)) {
+        // CUDA-core path: chunk states, then per-chunk decay sums, in the workspace
+        const size_t nch = (static_cast<size_t>(p->seqlen) + p->chunk_size - 1) / p->chunk_size;
+        const size_t states = static_cast<size_t>(p->batch) * p->nheads * nch * p->headdim *
+                              p->dstate * sizeof(float);
+        a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              ((states + 255) / 256) * 256);
+    }
     cudaError_t e = ssm::ssd_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssd_chunk_scan_fwd launch");
     return SSM_OK;

@@ -53,6 +53,8 @@ unsigned int m1_tma_wait_timeouts();
 cudaError_t encode_tmap_2d(struct CUtensorMap_st* map, const void* base, int elem_bytes,
                            unsigned long long inner, unsigned long long rows, unsigned box_inner,
                            unsigned box_rows, bool swizzle128);
+cudaError_t encode_tmap_nd(struct CUtensorMap_st* map, const void* base, int elem_bytes, int rank,
+                           const unsigned long long* dims, const unsigned* box, bool swizzle128);
 
 // Decode-step arguments.
 struct StepArgs {
@@ -93,8 +95,14 @@ struct SsdArgs {
     float* ws_states;  // [batch, nheads, nchunks, headdim, dstate] chunk states, then h_in
     float* ws_decay;   // [batch, nheads, nchunks] exp(sum of Delta*A over the chunk)
 };
-size_t ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, int chunk);
+size_t ssd_workspace_bytes(const SsdArgs& a);
 cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
+
+// tensor-core SSD path (ssd_tc.cu)
+bool ssd_tc_supported(const SsdArgs& a);
+int ssd_tc_segments(const SsdArgs& a);
+size_t ssd_tc_workspace_bytes(const SsdArgs& a);
+cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s);
 
 // Records `msg` as this thread's ssm_last_error() text and returns `st`.
 ssm_status set_error(ssm_status st, const char* msg);

@@ -232,11 +232,16 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_out(SsdArgs a) {
     }
 }
 
-size_t ssd_workspace_bytes(int batch, int seqlen, int nheads, int headdim, int dstate, int chunk) {
-    const size_t nch = (static_cast<size_t>(seqlen) + chunk - 1) / chunk;
-    const size_t states = static_cast<size_t>(batch) * nheads * nch * headdim * dstate * sizeof(float);
-    const size_t decay = static_cast<size_t>(batch) * nheads * nch * sizeof(float);
+static size_t ssd_cuda_core_workspace_bytes(const SsdArgs& a) {
+    const size_t nch = (static_cast<size_t>(a.seqlen) + a.chunk - 1) / a.chunk;
+    const size_t states =
+        static_cast<size_t>(a.batch) * a.nheads * nch * a.headdim * a.dstate * sizeof(float);
+    const size_t decay = static_cast<size_t>(a.batch) * a.nheads * nch * sizeof(float);
     return ((states + 255) / 256) * 256 + ((decay + 255) / 256) * 256;
+}
+
+size_t ssd_workspace_bytes(const SsdArgs& a) {
+    return ssd_tc_supported(a) ? ssd_tc_workspace_bytes(a) : ssd_cuda_core_workspace_bytes(a);
 }
 
 template <typename Tin, typename Tout>
@@ -268,6 +273,7 @@ static cudaError_t ssd_launch_t(const SsdArgs& a, cudaStream_t s) {
 }
 
 cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s) {
+    if (ssd_tc_supported(a)) return ssd_tc_launch(a, a.ws_states, s);
     if (a.in_dtype == SSM_BF16)
         return a.out_dtype == SSM_BF16 ? ssd_launch_t<bf16_t, bf16_t>(a, s)
                                        : ssd_launch_t<bf16_t, float>(a, s);

@@ -1,0 +1,107 @@
+// tcgen05.cuh -- 5th-generation tensor core (tcgen05) and tensor-memory helpers, inline
+// PTX for sm_100-family GPUs (used on sm_103a).
+//
+// Shared-memory operand convention used throughout: K-major tiles in the 128-byte
+// swizzle layout (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B): rows of 128
+// bytes (64 bf16 along K), 16-byte chunk c of row r stored at chunk c ^ (r % 8), tiles
+// 1024-byte aligned, 8-row groups 1024 bytes apart.  K beyond 64 bf16 lives in further
+// "slabs" of the same shape.  Accumulators are fp32 in TMEM: for M = 128 row r is lane
+// r; for M = 64 row r is lane 32 * (r / 16) + r % 16.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tma.cuh"
+
+namespace ssm {
+namespace tc {
+
+// shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);        // start address >> 4
+    d |= static_cast<uint64_t>(1) << 16;                         // leading byte offset (unused)
+    d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;    // stride byte offset = 1024
+    d |= static_cast<uint64_t>(1) << 46;                         // descriptor version (sm_100)
+    d |= static_cast<uint64_t>(2) << 61;                         // swizzle mode: 128 B
+    return d;
+}
+
+// instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator, both K-major
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4)                                   // D format: f32
+           | (1u << 7) | (1u << 10)                    // A, B format: bf16
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// instruction descriptor, kind::f16 with fp16 A and B, fp32 accumulator, both K-major
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// kind::f16 MMA (A and B both bf16 or both fp16, as the descriptor says)
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// all previously issued MMAs of this thread arrive on `bar` when complete
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// generic-proxy shared-memory writes -> visible to the tensor core (async proxy)
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// warp-wide: allocate `ncols` TMEM columns, address written to *slot
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// warp-wide: 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// byte offset of element (row, k) of a bf16 K-major SW128 tile with `rows` rows per slab
+__device__ __forceinline__ int sw_bf16(int rows, int row, int k) {
+    const int slab = k >> 6, kk = k & 63;
+    return slab * rows * 128 + row * 128 + ((((kk >> 3) ^ (row & 7))) << 4) + ((kk & 7) << 1);
+}
+
+}  // namespace tc
+}  // namespace ssm

@@ -57,4 +57,30 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Row-major tensor of `rank` dimensions (dims[0] innermost), contiguous strides.
+cudaError_t encode_tmap_nd(CUtensorMap* map, const void* base, int elem_bytes, int rank,
+                           const unsigned long long* dims, const unsigned* box, bool swizzle128) {
+    EncodeTiledFn fn = nullptr;
+    cudaError_t e = encoder(&fn);
+    if (e != cudaSuccess) return e;
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+    const CUtensorMapDataType dt =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    unsigned long long stride = static_cast<unsigned long long>(elem_bytes);
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i > 0) gs[i - 1] = stride;
+        stride *= dims[i];
+    }
+    CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace ssm

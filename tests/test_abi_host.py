@@ -107,10 +107,10 @@ def test_ssd_rejects_bad_arguments(lib, field, value, status):
 
 
 def test_ssd_workspace_size_and_shortfall(lib):
-    p = ssd_params()
+    p = ssd_params(headdim=32)  # CUDA-core path: one fp32 state per chunk
     need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
     nch = 256 // 64
-    assert need >= 2 * 4 * nch * 64 * 128 * 4
+    assert need >= 2 * 4 * nch * 32 * 128 * 4
     rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, need - 1, None)
     assert rc == _lib.SSM_ERR_INVALID_ARG
     assert "workspace" in lib.ssm_last_error().decode()

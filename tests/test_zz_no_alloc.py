@@ -37,8 +37,9 @@ def test_oversized_problem_is_refused_on_the_host():
     """Refused before any GPU work: the size query alone decides."""
     lib, fn, cap = _noalloc_fn()
     p = _lib.SsdParams()
+    # headdim 32 runs on the CUDA-core path, which keeps one fp32 state per chunk
     p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = \
-        4, 4096, 24, 64, 128, 1, 64
+        4, 65536, 24, 32, 128, 1, 64
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
     fake = 0x7F0000000000
     for f in ("x", "dt", "A", "B", "C", "y"):
