@@ -11,23 +11,26 @@
 //
 // One CTA walks a run ("segment") of consecutive chunks of one (batch, head) and keeps
 // the state in fp32 registers.  Per chunk, TMA brings the x, B, C tiles (bf16, 128-byte
-// swizzle); the threads build the remaining operand tiles; one thread issues tcgen05.mma
-// (kind::f16, bf16 in, fp32 accumulators in TMEM):
-//   MMA1  CB   = C . B^T                    M=64  N=64 K=128   (exact bf16 operands)
-//   MMA2  Yd   = M_hi . X + M_lo . X        M=64  N=64 K=64    (M = CB o decay o w, split
-//                                                               into two bf16 parts)
-//   MMA3  Yo   = C . H^T                    M=64  N=64 K=128   (state rounded to bf16; the
-//                                                               exp(s_t) row scale is applied
-//                                                               in fp32 afterwards)
-//   MMA4  S    = B^T . (f o X)^T            M=128 N=64 K=64    (f_s = exp(s_end - s_s) w_s;
-//                                                               fp16 operands: B is exact in
-//                                                               fp16, f o X keeps 11 bits)
+// swizzle); the threads build the remaining operand tiles with 16-byte vector stores; one
+// thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulators in TMEM).  x and B are
+// used straight from the TMA tiles, as MN-major operands where the contraction runs over
+// their rows:
+//   MMA1  CB = C . B^T                        M=64  N=64 K=128  C, B K-major (exact bf16)
+//   MMA2  Yd = M_hi . X + M_lo . X            M=64  N=64 K=64   M = CB o decay o w, split
+//                                                               into two bf16 parts; X
+//                                                               MN-major
+//   MMA3  Yo = C . H^T                        M=64  N=64 K=128  state rounded to bf16, held
+//                                                               as [n][p] (MN-major); the
+//                                                               exp(s_t) row scale is
+//                                                               applied in fp32 afterwards
+//   MMA4  S  = B^T . F_hi + B^T . F_lo        M=128 N=64 K=64   B MN-major; F = f o X,
+//                                                               f_s = exp(s_end - s_s) w_s,
+//                                                               split into two bf16 parts
 // A first launch ("states" mode) runs the state part only over every segment but the
 // last and leaves each segment's local end state and total decay in the workspace; the
 // main launch then starts segment k from h0 combined with those (state passing), so
 // segments of the same sequence run in parallel.
 #include <cuda.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -48,22 +51,44 @@ struct SsdMaps {
     CUtensorMap x, b, c;
 };
 
-// shared-memory layout (bytes); every tile 1024-byte aligned
-constexpr int kOffX = 0;                 // [64 t][64 p] bf16 (TMA)
-constexpr int kOffB = kOffX + 8192;      // [64 s][128 n] bf16, 2 slabs (TMA)
-constexpr int kOffC = kOffB + 16384;     // [64 t][128 n] bf16, 2 slabs (TMA)
-constexpr int kOffXt = kOffC + 16384;    // [64 p][64 s] bf16: x transposed
-constexpr int kOffXs = kOffXt + 8192;    // [64 p][64 s] fp16: (f_s x_s) transposed
-constexpr int kOffMh = kOffXs + 8192;    // [64 t][64 s] bf16: masked decayed CB, high part
+// shared-memory layout (bytes); every tile 1024-byte aligned, rows of 128 bytes
+constexpr int kOffX = 0;                 // [64 s][64 p] bf16 (TMA)
+constexpr int kOffB = kOffX + 8192;      // [64 s][128 n] bf16, two 64-column slabs (TMA)
+constexpr int kOffC = kOffB + 16384;     // [64 t][128 n] bf16, two slabs (TMA)
+constexpr int kOffMh = kOffC + 16384;    // [64 t][64 s] bf16: masked decayed CB, high part
 constexpr int kOffMl = kOffMh + 8192;    // [64 t][64 s] bf16: low part
-constexpr int kOffBt = kOffMl + 8192;    // [128 n][64 s] fp16: B transposed
-constexpr int kOffHt = kOffBt + 16384;   // [64 p][128 n] bf16, 2 slabs: carried state
-constexpr int kOffArr = kOffHt + 16384;  // cum, w, f, e: 4 x 64 floats
+constexpr int kOffHm = kOffMl + 8192;    // [128 n][64 p] bf16: carried state
+constexpr int kOffFh = kOffHm + 16384;   // [64 s][64 p] bf16: f_s x_s, high part
+constexpr int kOffFl = kOffFh + 8192;    // [64 s][64 p] bf16: low part
+constexpr int kOffArr = kOffFl + 8192;   // cum, w, f, e: 4 x 64 floats
 constexpr int kOffBar = kOffArr + 4 * kQ * 4;
 constexpr int kSmemBytes = kOffBar + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr uint32_t kTxFull = 8192 + 2 * 16384;
 constexpr uint32_t kTxState = 8192 + 16384;
+
+// 16-byte chunk `cq` (8 bf16) of row `r` in a 128-byte-row swizzled tile
+__device__ __forceinline__ int chunk_off(int r, int cq) { return r * 128 + (((cq ^ (r & 7))) << 4); }
+
+// v = hi + lo with hi, lo bf16 (8 values -> two packed 16-byte chunks)
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        h[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        l[j] = pack_bf16x2(v[2 * j] - lo_bf16(h[j]), v[2 * j + 1] - hi_bf16(h[j]));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+__device__ __forceinline__ void unpack8(uint4 w, float* v) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = lo_bf16(a[j]);
+        v[2 * j + 1] = hi_bf16(a[j]);
+    }
+}
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, int c3, uint64_t* bar) {
@@ -75,8 +100,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-__device__ __forceinline__ uint16_t bf16_rn(float f) { return f32_to_bf16(f); }
-__device__ __forceinline__ uint16_t f16_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
 template <typename Tin, typename Tout, bool STATES>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -140,10 +163,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[i] = dec * h[i] + sl[static_cast<size_t>(32 * hf + i) * kNs + hn];
         }
-        // carried state as the bf16 B operand of MMA3: Ht[p][n]
+        // carried state as the bf16 operand of MMA3: row n of Hm holds h[., n]
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<uint16_t*>(sm + kOffHt + tc::sw_bf16(kP, 32 * hf + i, hn)) = bf16_rn(h[i]);
+        for (int j = 0; j < 4; ++j) {
+            const uint4 w = make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                       pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+            *reinterpret_cast<uint4*>(sm + kOffHm + chunk_off(hn, 4 * hf + j)) = w;
+        }
     }
 
     auto issue = [&](int c) {
@@ -163,29 +189,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float Dh = a.D ? a.D[hd] : 0.f;
     const Tin* Z = static_cast<const Tin*>(a.z);
 
+    // raw time steps of the next chunk, fetched one chunk ahead (warp 0, two per lane)
+    float dt_next[2] = {0.f, 0.f};
+    auto fetch_dt = [&](int c) {
+        const int t0 = c * kQ, q = min(kQ, L - t0);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int s = 2 * lane + j;
+            dt_next[j] = s < q ? to_f32(DT[(static_cast<size_t>(b) * L + t0 + s) * a.nheads + hd]) : 0.f;
+        }
+    };
+    if (warp == 0 && cb < ce) fetch_dt(cb);
+
     for (int c = cb; c < ce; ++c) {
         const int t0 = c * kQ;
         const int q = min(kQ, L - t0);
+        float dt_raw[2] = {dt_next[0], dt_next[1]};
+        if (warp == 0 && c + 1 < ce) fetch_dt(c + 1);
         mbar_wait(tma_bar, tma_phase);
         tma_phase ^= 1;
 
-        // (a) transposes that need no decay factors: Bt[n][s] = B[s][n] (to fp16);
-        //     Xt[p][s] = x[s][p]
-        {
-            const int n = tid & 127, s0 = (tid >> 7) * 32;
-#pragma unroll 8
-            for (int s = s0; s < s0 + 32; ++s)
-                *reinterpret_cast<uint16_t*>(sm + kOffBt + tc::sw_bf16(kNs, n, s)) = f16_rn(bf16_to_f32(
-                    *reinterpret_cast<const uint16_t*>(sm + kOffB + tc::sw_bf16(kQ, s, n))));
-        }
-        if (!STATES) {
-            const int p = tid & 63, s0 = (tid >> 6) * 16;
-#pragma unroll 8
-            for (int s = s0; s < s0 + 16; ++s)
-                *reinterpret_cast<uint16_t*>(sm + kOffXt + tc::sw_bf16(kP, p, s)) =
-                    *reinterpret_cast<const uint16_t*>(sm + kOffX + tc::sw_bf16(kQ, s, p));
-        }
-        // (b) Delta, running sums and weights of the chunk (warp 0: two steps per lane)
+        // (a) Delta, running sums and weights of the chunk (warp 0: two steps per lane)
         if (warp == 0) {
             float d2[2], w2[2], c2[2];
 #pragma unroll
@@ -193,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int s = 2 * lane + j;
                 float dt = 0.f;
                 if (s < q) {
-                    const float v = to_f32(DT[(static_cast<size_t>(b) * L + t0 + s) * a.nheads + hd]) + bias;
+                    const float v = dt_raw[j] + bias;
                     dt = a.dt_softplus ? softplus_accurate(v) : v;
                 }
                 d2[j] = dt * Ah;
@@ -222,6 +246,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncthreads();
 
+        // x values this thread needs in the output epilogue (row t, 32 columns), kept in
+        // registers so the stage can take the next chunk's tiles before the epilogue
+        uint4 xkeep[4];
+        if (!STATES) {
+            const int t = 16 * qd + (lane & 15);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                xkeep[j] = *reinterpret_cast<const uint4*>(sm + kOffX + chunk_off(t, 4 * hf + j));
+        }
+
         if (!STATES && tid == 0) {  // MMA1: CB = C . B^T
             tc::fence_after();
             const uint32_t sc = smem_u32(sm + kOffC), sb = smem_u32(sm + kOffB);
@@ -233,17 +267,26 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc::mma_commit(mma_bar);
         }
-        // (c) Xs[p][s] = fp16(f_s x_s[p])
+        // (b) F[s][p] = f_s x_s[p] as bf16 hi + lo (row s, 16 columns per thread)
         {
-            const int p = tid & 63, s0 = (tid >> 6) * 16;
-#pragma unroll 8
-            for (int s = s0; s < s0 + 16; ++s) {
-                const float xv = bf16_to_f32(*reinterpret_cast<const uint16_t*>(sm + kOffX + tc::sw_bf16(kQ, s, p)));
-                *reinterpret_cast<uint16_t*>(sm + kOffXs + tc::sw_bf16(kP, p, s)) = f16_rn(fv[s] * xv);
+            const int s = tid >> 2, pq = tid & 3;
+            const float f = fv[s];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int cq = 2 * pq + j;
+                float v[8];
+                unpack8(*reinterpret_cast<const uint4*>(sm + kOffX + chunk_off(s, cq)), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= f;
+                uint4 hi, lo;
+                split8(v, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kOffFh + chunk_off(s, cq)) = hi;
+                *reinterpret_cast<uint4*>(sm + kOffFl + chunk_off(s, cq)) = lo;
             }
         }
         if (!STATES) {
-            // (d) masked, decayed, weighted CB -> M_hi, M_lo (rows t = 16 qd + lane, lane < 16)
+            // (c) masked, decayed, weighted CB -> M_hi, M_lo (row t = 16 qd + lane for
+            //     lane < 16; columns s = 32 hf .. 32 hf + 31)
             mbar_wait(mma_bar, mma_phase);
             mma_phase ^= 1;
             tc::fence_after();
@@ -254,15 +297,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane < 16) {
                 const float ct = cum[t];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int s = 32 * hf + i;
-                    float m = 0.f;
-                    if (s <= t && t < q) m = cbv[i] * expf(ct - cum[s]) * wv[s];
-                    const uint16_t hi = bf16_rn(m);
-                    const uint16_t lo = bf16_rn(m - bf16_to_f32(hi));
-                    const int off = tc::sw_bf16(kQ, t, s);
-                    *reinterpret_cast<uint16_t*>(sm + kOffMh + off) = hi;
-                    *reinterpret_cast<uint16_t*>(sm + kOffMl + off) = lo;
+                for (int j = 0; j < 4; ++j) {
+                    float m[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int s = 32 * hf + 8 * j + e;
+                        m[e] = (s <= t && t < q) ? cbv[8 * j + e] * expf(ct - cum[s]) * wv[s] : 0.f;
+                    }
+                    uint4 hi, lo;
+                    split8(m, hi, lo);
+                    *reinterpret_cast<uint4*>(sm + kOffMh + chunk_off(t, 4 * hf + j)) = hi;
+                    *reinterpret_cast<uint4*>(sm + kOffMl + chunk_off(t, 4 * hf + j)) = lo;
                 }
             }
         }
@@ -272,37 +317,43 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         if (tid == 0) {
             tc::fence_after();
+            const uint32_t sx = smem_u32(sm + kOffX), sbm = smem_u32(sm + kOffB);
             if (!STATES) {
                 const uint32_t smh = smem_u32(sm + kOffMh), sml = smem_u32(sm + kOffMl);
-                const uint32_t sxt = smem_u32(sm + kOffXt);
+                const uint32_t idn = tc::idesc_bf16_mn(64, 64, false, true);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)  // MMA2: Yd = M_hi X
+                for (int k = 0; k < 4; ++k)  // MMA2: Yd = M_hi X + M_lo X
                     tc::mma_bf16(tmem + kColYd, tc::desc_sw128(smh + k * 32),
-                                 tc::desc_sw128(sxt + k * 32), tc::idesc_bf16(64, 64), k > 0);
+                                 tc::desc_sw128_mn(sx + k * 2048, 8192), idn, k > 0);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)  //        + M_lo X
+                for (int k = 0; k < 4; ++k)
                     tc::mma_bf16(tmem + kColYd, tc::desc_sw128(sml + k * 32),
-                                 tc::desc_sw128(sxt + k * 32), tc::idesc_bf16(64, 64), 1);
-                const uint32_t sc = smem_u32(sm + kOffC), sh = smem_u32(sm + kOffHt);
+                                 tc::desc_sw128_mn(sx + k * 2048, 8192), idn, 1);
+                const uint32_t sc = smem_u32(sm + kOffC), sh = smem_u32(sm + kOffHm);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {  // MMA3: Yo = C H^T
-                    const uint32_t off = (k >> 2) * 8192 + (k & 3) * 32;
-                    tc::mma_bf16(tmem + kColYo, tc::desc_sw128(sc + off), tc::desc_sw128(sh + off),
-                                 tc::idesc_bf16(64, 64), k > 0);
-                }
+                for (int k = 0; k < 8; ++k)  // MMA3: Yo = C H^T
+                    tc::mma_bf16(tmem + kColYo, tc::desc_sw128(sc + (k >> 2) * 8192 + (k & 3) * 32),
+                                 tc::desc_sw128_mn(sh + k * 2048, 16384), idn, k > 0);
             }
-            const uint32_t sbt = smem_u32(sm + kOffBt), sxs = smem_u32(sm + kOffXs);
+            const uint32_t sfh = smem_u32(sm + kOffFh), sfl = smem_u32(sm + kOffFl);
+            const uint32_t id4 = tc::idesc_bf16_mn(128, 64, true, true);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // MMA4: S = B^T (f o X)^T
-                tc::mma_bf16(tmem + kColS, tc::desc_sw128(sbt + k * 32), tc::desc_sw128(sxs + k * 32),
-                             tc::idesc_f16(128, 64), k > 0);
+            for (int k = 0; k < 4; ++k)  // MMA4: S = B^T F_hi + B^T F_lo
+                tc::mma_bf16(tmem + kColS, tc::desc_sw128_mn(sbm + k * 2048, 8192),
+                             tc::desc_sw128_mn(sfh + k * 2048, 8192), id4, k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                tc::mma_bf16(tmem + kColS, tc::desc_sw128_mn(sbm + k * 2048, 8192),
+                             tc::desc_sw128_mn(sfl + k * 2048, 8192), id4, 1);
             tc::mma_commit(mma_bar);
         }
         mbar_wait(mma_bar, mma_phase);
         mma_phase ^= 1;
         tc::fence_after();
+        // every read of the stage is done: bring in the next chunk while the epilogues run
+        if (tid == 0 && c + 1 < ce) issue(c + 1);
 
-        if (!STATES) {  // (e) outputs, rows t = 16 qd + lane (lane < 16), columns p in 32 hf..
+        if (!STATES) {  // (d) outputs: row t = 16 qd + lane (lane < 16), p = 32 hf .. + 31
             const int t = 16 * qd + (lane & 15);
             float yd[32], yo[32];
             tc::tmem_ld16(tlane + kColYd + 32 * hf, yd);
@@ -314,17 +365,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const size_t row = ((static_cast<size_t>(b) * L + t0 + t) * a.nheads + hd) * kP + 32 * hf;
                 float out[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int p = 32 * hf + i;
-                    const float xv = bf16_to_f32(*reinterpret_cast<const uint16_t*>(sm + kOffX + tc::sw_bf16(kQ, t, p)));
-                    float v = yd[i] + et * yo[i] + Dh * xv;
-                    if (Z) v *= silu_accurate(to_f32(Z[row + i]));
-                    out[i] = v;
+                for (int j = 0; j < 4; ++j) {
+                    float xv[8];
+                    unpack8(xkeep[j], xv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * j + e;
+                        float v = yd[i] + et * yo[i] + Dh * xv[e];
+                        if (Z) v *= silu_accurate(to_f32(Z[row + i]));
+                        out[i] = v;
+                    }
                 }
                 store_row<32>(static_cast<Tout*>(a.y) + row, out, 32);
             }
         }
-        {  // (f) state update from the chunk state, rows n = 32 qd + lane, columns p in 32 hf..
+        {  // (e) state update: row n = 32 qd + lane, p = 32 hf .. + 31
             float sv[32];
             tc::tmem_ld16(tlane + kColS + 32 * hf, sv);
             tc::tmem_ld16(tlane + kColS + 32 * hf + 16, sv + 16);
@@ -333,14 +388,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i < 32; ++i) h[i] = dec * h[i] + sv[i];
             if (!STATES) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    *reinterpret_cast<uint16_t*>(sm + kOffHt + tc::sw_bf16(kP, 32 * hf + i, hn)) = bf16_rn(h[i]);
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 w = make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                               pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+                    *reinterpret_cast<uint4*>(sm + kOffHm + chunk_off(hn, 4 * hf + j)) = w;
+                }
             }
         }
         tc::fence_async_smem();
         tc::fence_before();
         __syncthreads();
-        if (tid == 0 && c + 1 < ce) issue(c + 1);
     }
 
     if (STATES) {
@@ -375,7 +432,7 @@ int ssd_tc_segments(const SsdArgs& a) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int nch = (a.seqlen + kQ - 1) / kQ;
     const long long units = static_cast<long long>(a.batch) * a.nheads;
-    int S = static_cast<int>((2LL * sms + units - 1) / units);  // about two CTAs per SM
+    int S = static_cast<int>((2LL * sms) / units);  // one wave at two CTAs per SM
     if (S < 1) S = 1;
     if (S > nch) S = nch;
     if (S > 64) S = 64;

@@ -27,6 +27,27 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// shared-memory matrix descriptor, MN-major operand in the 128-byte swizzle layout: rows
+// of 128 bytes run along M (or N), one row per K index, 8-row groups 1024 B apart along
+// K; `mn_slab_bytes` is the distance between consecutive 64-element blocks along M/N.
+// Advancing K by 16 (bf16) moves the start address by 2048 bytes.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_slab_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((mn_slab_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+    d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;          // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator; a_mn / b_mn
+// select MN-major (transposed) operands
+__host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator, both K-major
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4)                                   // D format: f32
