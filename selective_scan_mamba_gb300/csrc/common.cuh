@@ -85,6 +85,22 @@ __device__ __forceinline__ void load_f32(const bf16_t* p, float* out) {
     }
 }
 
+// 4 consecutive elements (8-byte aligned for bf16, 16-byte for fp32), widened to fp32
+__device__ __forceinline__ void load4_f32(const float* p, float* out) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    out[0] = v.x;
+    out[1] = v.y;
+    out[2] = v.z;
+    out[3] = v.w;
+}
+__device__ __forceinline__ void load4_f32(const bf16_t* p, float* out) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    out[0] = lo_bf16(v.x);
+    out[1] = hi_bf16(v.x);
+    out[2] = lo_bf16(v.y);
+    out[3] = hi_bf16(v.y);
+}
+
 // Store CNT consecutive outputs; `room` = how many of them lie inside the row.  Whole
 // rows go out as 16-byte vectors (the destination is 16-byte aligned then), ragged
 // ends element by element.
