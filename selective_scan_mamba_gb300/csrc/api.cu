@@ -187,7 +187,9 @@ int ssm_abi_version(void) { return SSM_ABI_VERSION; }
 
 const char* ssm_last_error(void) { return g_err; }
 
-unsigned int ssm_wait_timeouts(void) { return ssm::m1_tma_wait_timeouts(); }
+unsigned int ssm_wait_timeouts(void) {
+    return ssm::m1_tma_wait_timeouts() + ssm::m1_tmem_wait_timeouts();
+}
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     (void)p;
@@ -214,7 +216,14 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
     }
     ssm::M1Args a = scan_args(p);
     ssm::M1Plan plan;
-    cudaError_t e = ssm::m1_tma_plan(a, &plan);
+    cudaError_t e = ssm::m1_tmem_plan(a, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd plan");
+    if (plan.kind == ssm::M1Plan::kTmem) {
+        e = ssm::m1_tmem_launch(a, plan, s);
+        if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
+        return SSM_OK;
+    }
+    e = ssm::m1_tma_plan(a, &plan);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd plan");
     if (plan.kind == ssm::M1Plan::kTma) {
         e = ssm::m1_tma_launch(a, plan, s);

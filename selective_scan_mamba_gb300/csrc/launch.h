@@ -31,11 +31,12 @@ struct M1Args {
 };
 
 struct M1Plan {
-    enum Kind { kGeneric = 0, kTiled = 1, kTma = 2 } kind;
+    enum Kind { kGeneric = 0, kTiled = 1, kTma = 2, kTmem = 3 } kind;
     int tpc;      // threads per channel (tiled path)
     int grid;     // CTAs (tiled path)
     int cpb_max;  // channels per CTA (tiled path)
     size_t smem;  // dynamic shared memory per CTA (tiled path)
+    int cps = 0;  // CTAs per (batch, group) (TMEM-broadcast path)
 };
 
 size_t m1_tiled_smem_bytes(int cpb, int N, int T, size_t elem_size);
@@ -48,6 +49,11 @@ size_t m1_tma_smem_bytes(int cpb);
 cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan);
 cudaError_t m1_tma_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
 unsigned int m1_tma_wait_timeouts();
+
+// bf16 fast path with B/C broadcast through tensor memory (scan_m1_tmem.cu)
+cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan);
+cudaError_t m1_tmem_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
+unsigned int m1_tmem_wait_timeouts();
 
 // TMA tensor map of a row-major [rows][inner] tensor (tmap.cu)
 cudaError_t encode_tmap_2d(struct CUtensorMap_st* map, const void* base, int elem_bytes,

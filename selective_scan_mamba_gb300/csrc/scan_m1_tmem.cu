@@ -1,0 +1,404 @@
+// scan_m1_tmem.cu -- Mamba-1 selective scan, bf16 fast path with B and C broadcast through
+// tensor memory (sm_103a).
+//
+// Same mathematics as scan_m1.cu ("From S4 to Mamba-3", 03/System, mamba_minimal.py):
+//   h_t[n] = exp(Delta_t A[d,n]) h_{t-1}[n] + Delta_t B_t[n] x_t,
+//   y_t = (C_t . h_t + D x_t) * SiLU(z_t),  Delta_t = softplus(delta_t + bias_d).
+//
+// B_t and C_t are shared by every channel of a (batch, group), and each thread needs the
+// values of its own four states at every step.  Read from shared memory that broadcast
+// costs a wavefront per 4 bytes per lane; read as bf16 it costs a widening per value.
+// Here the tensor core does both jobs: one tcgen05.mma with a one-hot A operand (row m
+// selects state group m % 4) copies, for 32 steps at a time, each lane's 8 values per
+// step (4 of B, 4 of C, exact in fp32) into that lane's row of TMEM, and the step loop
+// fetches them with one tcgen05.ld per 4 steps.
+//
+// Work split: CTAs never straddle a (batch, group): grid = pairs x CTAs-per-pair, each CTA
+// a contiguous, balanced range of that pair's channels for the whole sequence, one CTA
+// per SM (512 TMEM columns: two 32-step halves of a 64-step tile).  Four threads per
+// channel, states n = gi + 4 i.  Per tile: TMA (128-byte swizzle, double buffer) brings x,
+// delta, z rows and the pair's B, C rows; the B/C operand of the broadcast MMA is built
+// (8 bytes per row); (dt, dt*x) pairs are computed once per (b, d, t); the recurrence runs
+// with f32x2 arithmetic and one MUFU.EX2 per state update; partial outputs are
+// reduce-scattered by shuffles; skip, gate and 16-byte stores of y finish the tile.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kT = 64;          // steps per tile (128 bytes of bf16 per row)
+constexpr int kN = 16;          // dstate of this path
+constexpr int kTPC = 4;         // threads per channel
+constexpr int kNS = 4;          // states per thread
+constexpr int kStages = 2;
+constexpr int kRowB = kT * 2;   // bytes per staged row
+constexpr int kDtxS = kT + 1;   // float2 row stride of (dt, dt*x)
+constexpr int kMaxThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+
+struct TmaMaps {
+    CUtensorMap x, dl, z, b, c;
+};
+
+__host__ __device__ inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// shared-memory layout (bytes); TMA destinations and MMA operands 1024-byte aligned
+struct Layout {
+    int cb;  // staged rows per tensor (cpb rounded up to 8)
+    int x, dl, z, b, c, stage;
+    int dtx, onehot, bop, bars, total;
+    __host__ __device__ Layout(int cpb) {
+        cb = round_up(cpb, 8);
+        x = 0;
+        dl = x + cb * kRowB;
+        z = dl + cb * kRowB;
+        b = z + cb * kRowB;
+        c = b + kN * kRowB;
+        stage = round_up(c + kN * kRowB, 1024);
+        dtx = kStages * stage;
+        onehot = round_up(dtx + cpb * kDtxS * 8, 1024);
+        bop = onehot + 128 * 128;       // [128 rows][128 B]
+        bars = bop + 2 * 256 * 128;     // two [256 rows][128 B] operands
+        total = bars + 64;
+    }
+};
+
+__device__ __forceinline__ int dtx_col(int t) { return t ^ (((t >> 4) & 3) << 2); }
+
+__device__ __forceinline__ void load8(const unsigned char* tile, int row, int chunk, float* out) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + sw128(row, chunk * 16));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        out[2 * j] = lo_bf16(w[j]);
+        out[2 * j + 1] = hi_bf16(w[j]);
+    }
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_constant__ TmaMaps maps,
+                                                                M1Args a, int cps) {
+    constexpr int TO = kT / kTPC;
+    const int per_group = a.dim / a.ngroups;
+    const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
+    const int b = pair / a.ngroups, g = pair % a.ngroups;
+    const int l0 = static_cast<int>((static_cast<long long>(part_i) * per_group) / cps);
+    const int l1 = static_cast<int>((static_cast<long long>(part_i + 1) * per_group) / cps);
+    const int nch = l1 - l0;
+    const int c0 = b * a.dim + g * per_group + l0;  // first channel row
+    const Layout lay(a.cpb_max);
+    const bool has_z = a.z != nullptr;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    float2* dtx = reinterpret_cast<float2*>(smem + lay.dtx);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
+    uint64_t* mmab = full + kStages;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mmab + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int gi = tid % kTPC;
+    const bool active = tid / kTPC < nch;
+    const int c = active ? tid / kTPC : 0;
+    const int ch = c0 + c;
+    const int d = g * per_group + l0 + c;
+    const int L = a.seqlen;
+    const int ntiles = (L + kT - 1) / kT;
+    const uint32_t stage_tx = static_cast<uint32_t>(((has_z ? 3 : 2) * lay.cb + 2 * kN) * kRowB);
+
+    auto issue = [&](int k) {
+        unsigned char* st = smem + (k % kStages) * lay.stage;
+        uint64_t* bar = &full[k % kStages];
+        const int t0 = k * kT;
+        mbar_arrive_expect_tx(bar, stage_tx);
+        tma_load_2d(st + lay.x, &maps.x, t0, c0, bar);
+        tma_load_2d(st + lay.dl, &maps.dl, t0, c0, bar);
+        if (has_z) tma_load_2d(st + lay.z, &maps.z, t0, c0, bar);
+        tma_load_2d(st + lay.b, &maps.b, t0, pair * kN, bar);
+        tma_load_2d(st + lay.c, &maps.c, t0, pair * kN, bar);
+    };
+
+    if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (tid == 0) {
+        prefetch_tmap(&maps.x);
+        prefetch_tmap(&maps.dl);
+        if (has_z) prefetch_tmap(&maps.z);
+        prefetch_tmap(&maps.b);
+        prefetch_tmap(&maps.c);
+        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        mbar_init(&mmab[0], 1);
+        mbar_init(&mmab[1], 1);
+        mbar_fence_init();
+    }
+    // one-hot A operand: row m selects state group m % 4 (K = 16, first 32 bytes of a row);
+    // the B/C operands start all zero in their first 32 bytes
+    for (int m = tid; m < 128; m += blockDim.x) {
+        uint4 z0 = make_uint4(0, 0, 0, 0), z1 = z0;
+        uint32_t* w = &z0.x;
+        const int kk = m % 4;  // element kk of chunk 0 is 1.0 (bf16 0x3F80)
+        w[kk >> 1] = (kk & 1) ? 0x3F800000u : 0x00003F80u;
+        *reinterpret_cast<uint4*>(smem + lay.onehot + m * 128 + ((0 ^ (m & 7)) << 4)) = z0;
+        *reinterpret_cast<uint4*>(smem + lay.onehot + m * 128 + ((1 ^ (m & 7)) << 4)) = z1;
+    }
+    for (int j = tid; j < 2 * 256; j += blockDim.x) {
+        const int row = j % 256, hh = j / 256;
+        unsigned char* r = smem + lay.bop + hh * 256 * 128 + row * 128;
+        *reinterpret_cast<uint4*>(r + ((0 ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(r + ((1 ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    if (tid == 0)
+        for (int k = 0; k < kStages && k < ntiles; ++k) issue(k);
+
+    // thread gi owns states n = gi + 4 i; pairs (i = 2k, 2k+1)
+    float2 hp[kNS / 2], A2p[kNS / 2];
+#pragma unroll
+    for (int k = 0; k < kNS / 2; ++k) {
+        const int n0 = gi + kTPC * (2 * k), n1 = gi + kTPC * (2 * k + 1);
+        hp[k] = (active && a.h0) ? make_float2(a.h0[static_cast<size_t>(ch) * kN + n0],
+                                               a.h0[static_cast<size_t>(ch) * kN + n1])
+                                 : make_float2(0.f, 0.f);
+        A2p[k] = make_float2(a.A[static_cast<size_t>(d) * kN + n0] * SSM_LOG2E,
+                             a.A[static_cast<size_t>(d) * kN + n1] * SSM_LOG2E);
+    }
+    const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+    const float Dd = a.D ? a.D[d] : 0.f;
+
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % kStages;
+        const unsigned char* st = smem + s * lay.stage;
+        mbar_wait(&full[s], (k / kStages) & 1);
+        const int t0 = k * kT;
+        const int tb = gi * TO;
+
+        // (1) B/C operands of the broadcast MMA: row j = step * 8 + e of half hh holds, at
+        // K = 0..3, the value of state (K + 4 (e % 4)) of B (e < 4) or C (e >= 4)
+        for (int j = tid; j < 2 * 256; j += blockDim.x) {
+            const int hh = j >> 8, row = j & 255;
+            const int step = 32 * hh + (row >> 3), e = row & 7;
+            const unsigned char* tile = st + (e < 4 ? lay.b : lay.c);
+            const int n0 = 4 * (e & 3);
+            uint16_t v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[q] = *reinterpret_cast<const uint16_t*>(tile + sw128(n0 + q, step * 2));
+            *reinterpret_cast<uint2*>(smem + lay.bop + hh * 256 * 128 + row * 128 + ((0 ^ (row & 7)) << 4)) =
+                make_uint2(v[0] | (static_cast<uint32_t>(v[1]) << 16), v[2] | (static_cast<uint32_t>(v[3]) << 16));
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after();
+            const uint64_t ad = tc::desc_sw128(smem_u32(smem + lay.onehot));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                tc::mma_bf16(tmem + 256 * hh, ad, tc::desc_sw128(smem_u32(smem + lay.bop + hh * 256 * 128)),
+                             tc::idesc_bf16(128, 256), 0);
+                tc::mma_commit(&mmab[hh]);
+            }
+        }
+
+        // (2) (dt, dt*x) for this thread's steps of its channel
+        if (active) {
+#pragma unroll
+            for (int q = 0; q < TO / 8; ++q) {
+                float dv[8], xv[8];
+                load8(st + lay.dl, c, tb / 8 + q, dv);
+                load8(st + lay.x, c, tb / 8 + q, xv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int t = tb + 8 * q + i;
+                    const float v = dv[i] + bias;
+                    float dt = a.delta_softplus ? softplus_fast(v) : v;
+                    dt = (t0 + t < L) ? dt : 0.f;  // padded steps leave the state unchanged
+                    dtx[c * kDtxS + dtx_col(t)] = make_float2(dt, dt * xv[i]);
+                }
+            }
+        }
+        __syncthreads();
+
+        // (3) recurrence; B/C of 4 steps per tcgen05.ld, the next group's load in flight
+        float part[kT];
+        const float2* drow = dtx + c * kDtxS;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_wait(&mmab[hh], k & 1);
+            tc::fence_after();
+            uint32_t ra[32], rb[32];
+            tc::tmem_ld32_async(tl + 256 * hh, ra);
+            tc::tmem_wait();
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+                uint32_t* cur = (g4 & 1) ? rb : ra;
+                uint32_t* nxt = (g4 & 1) ? ra : rb;
+                if (g4 < 7) tc::tmem_ld32_async(tl + 256 * hh + 32 * (g4 + 1), nxt);
+                // decays of the group's 4 steps first (independent of the state)
+                float2 ddv[4], zz[4][kNS / 2];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ddv[j] = drow[dtx_col(32 * hh + 4 * g4 + j)];
+#pragma unroll
+                    for (int q = 0; q < kNS / 2; ++q) {
+                        const float2 e2 = mul2(make_float2(ddv[j].x, ddv[j].x), A2p[q]);
+                        zz[j][q] = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 dx2 = make_float2(ddv[j].y, ddv[j].y);
+                    const uint32_t* r = cur + 8 * j;
+                    const float2 b0 = make_float2(__uint_as_float(r[0]), __uint_as_float(r[1]));
+                    const float2 b1 = make_float2(__uint_as_float(r[2]), __uint_as_float(r[3]));
+                    const float2 c0v = make_float2(__uint_as_float(r[4]), __uint_as_float(r[5]));
+                    const float2 c1v = make_float2(__uint_as_float(r[6]), __uint_as_float(r[7]));
+                    hp[0] = fma2(zz[j][0], hp[0], mul2(dx2, b0));
+                    hp[1] = fma2(zz[j][1], hp[1], mul2(dx2, b1));
+                    const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
+                    part[32 * hh + 4 * g4 + j] = acc.x + acc.y;
+                }
+                if (g4 < 7) tc::tmem_wait();
+            }
+        }
+
+        // (4) reduce-scatter across the channel's 4 threads (kept half moves to the front)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int half = kT >> (r + 1);
+            const int bit = kTPC >> (r + 1);
+            const bool keep_lo = (gi & bit) == 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float lo = part[i], hi = part[i + half];
+                const float recv = __shfl_xor_sync(0xffffffffu, keep_lo ? hi : lo, bit);
+                part[i] = (keep_lo ? lo : hi) + recv;
+            }
+        }
+        if (active) {
+            float yv[TO];
+#pragma unroll
+            for (int q = 0; q < TO / 8; ++q) {
+                float xv[8], zv[8];
+                load8(st + lay.x, c, tb / 8 + q, xv);
+                if (has_z) load8(st + lay.z, c, tb / 8 + q, zv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float v = part[8 * q + i] + Dd * xv[i];
+                    if (has_z) v *= silu_fast(zv[i]);
+                    yv[8 * q + i] = v;
+                }
+            }
+            Tout* yrow = static_cast<Tout*>(a.y) + static_cast<size_t>(ch) * L + t0 + tb;
+            store_row<TO>(yrow, yv, L - (t0 + tb));
+        }
+        tc::fence_before();
+        __syncthreads();  // stage s, dtx, the B/C operands and TMEM are free again
+        if (tid == 0 && k + kStages < ntiles) issue(k + kStages);
+    }
+
+    if (active && a.h_final) {
+#pragma unroll
+        for (int k = 0; k < kNS / 2; ++k) {
+            a.h_final[static_cast<size_t>(ch) * kN + gi + kTPC * (2 * k)] = hp[k].x;
+            a.h_final[static_cast<size_t>(ch) * kN + gi + kTPC * (2 * k + 1)] = hp[k].y;
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+
+}  // namespace
+
+// Plan for the TMEM-broadcast path: bf16 inputs, dstate 16, exp-Euler, 16-byte rows.
+cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
+    plan->kind = M1Plan::kGeneric;
+    const size_t es_out = a.out_dtype == SSM_BF16 ? 2 : 4;
+    if (a.in_dtype != SSM_BF16 || a.dstate != kN || a.disc != SSM_DISC_EXP_EULER || a.seqlen <= 0 ||
+        (static_cast<size_t>(a.seqlen) * 2) % 16 != 0 ||
+        (static_cast<size_t>(a.seqlen) * es_out) % 16 != 0 || env_int("SSM_M1_NO_TMEM", 0))
+        return cudaSuccess;
+    int dev = 0, sms = 0, max_smem = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+        return e;
+    const int pairs = a.batch * a.ngroups;
+    const int per_group = a.dim / a.ngroups;
+    int cps = sms / pairs;
+    if (cps < 1) cps = 1;
+    if (cps > per_group) cps = per_group;
+    while ((per_group + cps - 1) / cps * kTPC > kMaxThreads) ++cps;
+    const int cpb = (per_group + cps - 1) / cps;
+    size_t smem = static_cast<size_t>(Layout(cpb).total) + 1024;
+    if (smem > static_cast<size_t>(max_smem)) return cudaSuccess;
+    // one CTA per SM: it allocates all 512 TMEM columns
+    const size_t one_per_sm = static_cast<size_t>(max_smem) / 2 + 1024;
+    if (smem < one_per_sm) smem = one_per_sm;
+    plan->kind = M1Plan::kTmem;
+    plan->tpc = kTPC;
+    plan->grid = pairs * cps;
+    plan->cpb_max = cpb;
+    plan->smem = smem;
+    plan->cps = cps;
+    return cudaSuccess;
+}
+
+cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, cudaStream_t s) {
+    M1Args a = a_in;
+    a.cpb_max = plan.cpb_max;
+    const Layout lay(plan.cpb_max);
+    const unsigned long long rows = static_cast<unsigned long long>(a.batch) * a.dim;
+    const unsigned long long bcrows = static_cast<unsigned long long>(a.batch) * a.ngroups * kN;
+    TmaMaps maps;
+    cudaError_t e;
+    if ((e = encode_tmap_2d(&maps.x, a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
+    if ((e = encode_tmap_2d(&maps.dl, a.delta, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
+    if ((e = encode_tmap_2d(&maps.z, a.z ? a.z : a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess)
+        return e;
+    if ((e = encode_tmap_2d(&maps.b, a.B, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
+    if ((e = encode_tmap_2d(&maps.c, a.C, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
+    const int threads = round_up(plan.cpb_max * kTPC, 32);
+    if (a.out_dtype == SSM_BF16) {
+        auto k = m1_scan_tmem<bf16_t>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem))) !=
+            cudaSuccess)
+            return e;
+        k<<<plan.grid, threads, plan.smem, s>>>(maps, a, plan.cps);
+    } else {
+        auto k = m1_scan_tmem<float>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem))) !=
+            cudaSuccess)
+            return e;
+        k<<<plan.grid, threads, plan.smem, s>>>(maps, a, plan.cps);
+    }
+    return cudaGetLastError();
+}
+
+unsigned int m1_tmem_wait_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace ssm
