@@ -288,8 +288,8 @@ def bench_ours(args, rank, world):
         "hbm_gbs": gbs,
         "hbm_frac": gbs / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("m1_scan_tiled"),
-                     "kernel": "m1_scan_tiled", "bytes_per_launch": set_bytes,
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("m1_scan_tmem"),
+                     "kernel": "m1_scan_tmem", "bytes_per_launch": set_bytes,
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)"},
         "e2e": {"value": updates * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
@@ -501,6 +501,50 @@ def bench_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """Runs one kernel workload --warmup + --steps times with no timing (for profiler
+    captures): m1 (130m layer), m1_long (790m, L 32768), ssd64 / ssd256 (130m SSD),
+    step (780m decode)."""
+    import torch
+    import selective_scan_mamba_gb300 as ssm
+    torch.cuda.set_device(0)
+    n = args.warmup + args.steps
+    if args.case in ("m1", "m1_long"):
+        cfg = synth.WORKLOADS["m1_130m_layer" if args.case == "m1" else "m1_790m_long"]
+        L = cfg["seqlen"] if args.case == "m1" else 32768
+        inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], L, dtype=cfg["dtype"],
+                           delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+        t = _dev(inp, torch)
+        y = torch.empty_like(t["x"])
+        for _ in range(n):
+            ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t.get("z"),
+                             delta_bias=t["delta_bias"], y=y)
+    elif args.case in ("ssd64", "ssd256"):
+        c4 = synth.WORKLOADS["ssd_130m"]
+        Q = 64 if args.case == "ssd64" else 256
+        inp = synth.ssd(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
+                        c4["ngroups"], dtype=c4["dtype"], delta_scale=c4["delta_scale"], seed=0)
+        t = _dev(inp, torch)
+        y = torch.empty_like(t["x"])
+        for _ in range(n):
+            ssm.ssd_chunk_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], Q, D=t["D"],
+                                   dt_bias=t["dt_bias"], y=y)
+    elif args.case == "step":
+        c5 = synth.WORKLOADS["step_780m"]
+        Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
+        par = _dev(synth.step_params(H, N, seed=0), torch)
+        states = [torch.from_numpy(synth.step_state(Bt, H, P, N, seed=k)).cuda() for k in range(4)]
+        tok = _dev(synth.step_tokens(Bt, H, P, N, G, step=0, seed=0), torch)
+        y = torch.empty((Bt, H, P), dtype=torch.bfloat16, device="cuda")
+        for i in range(n):
+            ssm.ssm_state_update(states[i % 4], tok["x"], tok["dt"], par["A"], tok["B"], tok["C"],
+                                 D=par["D"], z=tok["z"], dt_bias=par["dt_bias"], y=y)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    torch.cuda.synchronize()
+    print("done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,7 +555,12 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the SSD, decode and long-context measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step"],
+                    help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))
