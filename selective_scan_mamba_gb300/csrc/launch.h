@@ -106,7 +106,6 @@ cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
 
 // tensor-core SSD path (ssd_tc.cu)
 bool ssd_tc_supported(const SsdArgs& a);
-int ssd_tc_segments(const SsdArgs& a);
 size_t ssd_tc_workspace_bytes(const SsdArgs& a);
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s);
 

@@ -9,14 +9,21 @@
 //   S[n,p]      = sum_s B_s[n] exp(s_end - s_s) w_s x_s[p]                  (chunk state)
 //   h_out       = exp(s_end) h_in + S^T,   y = Y_diag + Y_off + D x, gated.
 //
-// One CTA walks a run ("segment") of consecutive chunks of one (batch, head) and keeps
-// the state in fp32 registers.  Per chunk, TMA brings the x, B, C tiles (bf16, 128-byte
-// swizzle); the threads build the remaining operand tiles with 16-byte vector stores; one
-// thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulators in TMEM).  x and B are
-// used straight from the TMA tiles, as MN-major operands where the contraction runs over
-// their rows:
+// Three launches.
+//  1. prep: per (batch, head, chunk) the running sums s_t (in log2 units) and the input
+//     weights w_t (Delta, or Delta*phi1 for ZOH) from the raw time steps, into the
+//     workspace (512 bytes per chunk, copied next to the chunk's tiles later).
+//  2. cuts: the (batch, head, chunk) units, taken head-major, are cut into one contiguous,
+//     equal range per SM.  For every range that stops inside a sequence, the local end
+//     state (from zero) over its chunks of that sequence, B^T (f o X) with
+//     f_s = exp(s_range_end - s_s) w_s accumulated in TMEM, and its total decay.
+//  3. main: each CTA walks its range in order with the state in fp32 registers; where the
+//     range starts inside a sequence the state there is h0 decayed through the cuts
+//     before it.  Per chunk, TMA brings x, B, C (bf16, 128-byte swizzle, 3-stage ring)
+//     and the step quantities; one warp issues tcgen05.mma (kind::f16, bf16 in, fp32
+//     accumulators in TMEM):
 //   MMA1  CB = C . B^T                        M=64  N=64 K=128  C, B K-major (exact bf16)
-//   MMA2  Yd = M_hi . X + M_lo . X            M=64  N=64 K=64   M = CB o decay o w, split
+//   MMA2  Yd = M_hi . X + M_lo . X            M=64  N=64 K=64   M = CB o decay o w split
 //                                                               into two bf16 parts; X
 //                                                               MN-major
 //   MMA3  Yo = C . H^T                        M=64  N=64 K=128  state rounded to bf16, held
@@ -26,10 +33,11 @@
 //   MMA4  S  = B^T . F_hi + B^T . F_lo        M=128 N=64 K=64   B MN-major; F = f o X,
 //                                                               f_s = exp(s_end - s_s) w_s,
 //                                                               split into two bf16 parts
-// A first launch ("states" mode) runs the state part only over every segment but the
-// last and leaves each segment's local end state and total decay in the workspace; the
-// main launch then starts segment k from h0 combined with those (state passing), so
-// segments of the same sequence run in parallel.
+// Warp roles (18 warps): 16 compute warps build M and F of chunk c and then finish the
+// outputs and the state update of chunk c-1; one warp issues the MMAs (MMA2-4 of chunk c
+// once the operands are built, MMA1 two chunks ahead); one warp issues the copies.
+// Hand-offs go through mbarriers; the MMAs of chunk c run while the compute warps build
+// chunk c+1.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,29 +51,46 @@ namespace ssm {
 namespace {
 
 constexpr int kQ = 64, kP = 64, kNs = 128;
-constexpr int kThreads = 256;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColYd = 0, kColYo = 64, kColS = 128, kColCB = 192;
+constexpr int kCompute = 16;                   // warps that build operands and finish outputs
+constexpr int kMmaWarp = kCompute;             // issues the tensor-core MMAs
+constexpr int kLoadWarp = kCompute + 1;        // issues the TMA copies
+constexpr int kThreads = (kCompute + 2) * 32;
+
+// main launch TMEM columns: two CB slots, Y_diag, Y_off, S
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColCB = 0, kColYd = 128, kColYo = 192, kColS = 256;
 
 struct SsdMaps {
     CUtensorMap x, b, c;
 };
 
-// shared-memory layout (bytes); every tile 1024-byte aligned, rows of 128 bytes
-constexpr int kOffX = 0;                 // [64 s][64 p] bf16 (TMA)
-constexpr int kOffB = kOffX + 8192;      // [64 s][128 n] bf16, two 64-column slabs (TMA)
-constexpr int kOffC = kOffB + 16384;     // [64 t][128 n] bf16, two slabs (TMA)
-constexpr int kOffMh = kOffC + 16384;    // [64 t][64 s] bf16: masked decayed CB, high part
-constexpr int kOffMl = kOffMh + 8192;    // [64 t][64 s] bf16: low part
-constexpr int kOffHm = kOffMl + 8192;    // [128 n][64 p] bf16: carried state
-constexpr int kOffFh = kOffHm + 16384;   // [64 s][64 p] bf16: f_s x_s, high part
-constexpr int kOffFl = kOffFh + 8192;    // [64 s][64 p] bf16: low part
-constexpr int kOffArr = kOffFl + 8192;   // cum, w, f, e: 4 x 64 floats
-constexpr int kOffBar = kOffArr + 4 * kQ * 4;
-constexpr int kSmemBytes = kOffBar + 64;
+// per-chunk step quantities, written by the prep launch
+struct ChunkArr {
+    float cum2[kQ];  // running sum of Delta*A inside the chunk, log2 units (flat past the end)
+    float w[kQ];     // input weight: Delta, or Delta*phi1(Delta*A) for ZOH (0 past the end)
+};
+constexpr int kArrBytes = static_cast<int>(sizeof(ChunkArr));  // 512
+
+// main launch shared memory (bytes); tiles 1024-byte aligned, rows of 128 bytes
+constexpr int kStages = 3;
+constexpr int kStX = 0, kStB = 8192, kStC = 24576, kStArr = 40960;  // x [s][p], B, C [s][n]
+constexpr int kStBytes = 41984;
+constexpr int kOffM = kStages * kStBytes;  // 2 x [64 t][64 s] bf16 masked decayed CB, hi then lo
+constexpr int kOffF = kOffM + 2 * 16384;   // 2 x [64 s][64 p] f_s x_s, hi then lo
+constexpr int kOffHm = kOffF + 2 * 16384;  // [128 n][64 p] bf16 carried state
+constexpr int kOffBar = kOffHm + 16384;
+constexpr int kSmemBytes = kOffBar + 128;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
-constexpr uint32_t kTxFull = 8192 + 2 * 16384;
-constexpr uint32_t kTxState = 8192 + 16384;
+constexpr uint32_t kTxMain = 40960 + kArrBytes;
+
+// cuts launch: 4-stage ring of x, B and the step quantities; two F buffers
+constexpr int kCStages = 4;
+constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
+constexpr int kCOffF = kCStages * kCStBytes;  // 2 x (F_hi, F_lo) = 2 x 16 KB
+constexpr int kCOffBar = kCOffF + 2 * 16384;
+constexpr int kCSmemBytes = kCOffBar + 128;
+constexpr int kCSmemAlloc = kCSmemBytes + 1024;
+constexpr uint32_t kTxCut = 24576 + kArrBytes;
 
 // 16-byte chunk `cq` (8 bf16) of row `r` in a 128-byte-row swizzled tile
 __device__ __forceinline__ int chunk_off(int r, int cq) { return r * 128 + (((cq ^ (r & 7))) << 4); }
@@ -99,315 +124,458 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
         "r"(smem_u32(bar))
         : "memory");
 }
+// contiguous bulk copy (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 
+// first unit of range i when `total` units are cut into `nct` equal ranges
+__host__ __device__ __forceinline__ long long range_begin(long long total, int nct, int i) {
+    return total * i / nct;
+}
 
-template <typename Tin, typename Tout, bool STATES>
-__global__ void __launch_bounds__(kThreads, 2)
-    ssd_tc_kernel(const __grid_constant__ SsdMaps maps, SsdArgs a, int nseg, float* seg_state,
-                  float* seg_decay) {
-    const int seg = blockIdx.x, hd = blockIdx.y, b = blockIdx.z;
-    const int L = a.seqlen;
+// ---------------------------------------------------------------------------------------
+// prep launch: one warp per (batch, head, chunk), two steps per lane
+// ---------------------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(256) ssd_tc_prep(SsdArgs a, ChunkArr* out) {
+    const int L = a.seqlen, H = a.nheads;
     const int nch = (L + kQ - 1) / kQ;
-    const int per = (nch + nseg - 1) / nseg;
-    const int cb = seg * per;
-    const int ce = min(nch, cb + per);
-    const int g = hd / (a.nheads / a.ngroups);
+    const long long units = static_cast<long long>(a.batch) * H * nch;
+    const long long u = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (u >= units) return;
+    const int lane = threadIdx.x & 31;
+    const int c = static_cast<int>(u % nch);
+    const int hd = static_cast<int>((u / nch) % H), b = static_cast<int>(u / (static_cast<long long>(nch) * H));
     const float Ah = a.A[hd];
     const float bias = a.dt_bias ? a.dt_bias[hd] : 0.f;
     const Tin* DT = static_cast<const Tin*>(a.dt);
+    const int t0 = c * kQ, qv = min(kQ, L - t0);
+    float d2[2], w2[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int s = 2 * lane + j;
+        float dt = 0.f;
+        if (s < qv) {
+            const float v = to_f32(DT[(static_cast<size_t>(b) * L + t0 + s) * H + hd]) + bias;
+            dt = a.dt_softplus ? softplus_accurate(v) : v;
+        }
+        d2[j] = dt * Ah;
+        w2[j] = a.disc == SSM_DISC_ZOH ? dt * phi1f(dt * Ah) : dt;
+    }
+    const float p1 = d2[0] + d2[1];
+    float run = p1;  // inclusive prefix of the lane pairs
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, run, off);
+        if (lane >= off) run += o;
+    }
+    const float excl = run - p1;
+    ChunkArr& A = out[u];
+    *reinterpret_cast<float2*>(&A.cum2[2 * lane]) =
+        make_float2((excl + d2[0]) * SSM_LOG2E, (excl + p1) * SSM_LOG2E);
+    *reinterpret_cast<float2*>(&A.w[2 * lane]) = make_float2(w2[0], w2[1]);
+}
+
+// ---------------------------------------------------------------------------------------
+// cuts launch: local end state (from zero) and total decay of every range that stops
+// inside a sequence, over the chunks of that range in that sequence (walked last to
+// first).  Warps 0-15 build F, warp 16 issues the MMAs, warp 17 the copies.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_tc_cuts(const __grid_constant__ SsdMaps maps, SsdArgs a, int nct, const ChunkArr* arrs,
+                float* cut_state, float* cut_decay) {
+    const int L = a.seqlen, H = a.nheads;
+    const int nch = (L + kQ - 1) / kQ;
+    const long long total = static_cast<long long>(a.batch) * H * nch;
+    const int ci = blockIdx.x;
+    const long long u0 = range_begin(total, nct, ci), u1 = range_begin(total, nct, ci + 1);
+    if (u1 <= u0) return;
+    const int wk = static_cast<int>((u1 - 1) / nch);
+    const long long wstart = static_cast<long long>(wk) * nch;
+    const int ce = static_cast<int>(u1 - wstart);
+    if (ce == nch) return;  // the range ends with its sequence: no cut
+    const int ca = static_cast<int>((u0 > wstart ? u0 : wstart) - wstart);
+    const int n = ce - ca;
+    const int b = wk / H, hd = wk % H, g = hd / (H / a.ngroups);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float* cum = reinterpret_cast<float*>(sm + kOffArr);
-    float* wv = cum + kQ;
-    float* fv = wv + kQ;
-    float* ev = fv + kQ;
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
-    uint64_t* mma_bar = tma_bar + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kCOffBar);  // [kCStages]
+    uint64_t* mma_bar = tma_bar + kCStages;                           // [2] MMA of step k done
+    uint64_t* done_bar = mma_bar + 2;                                 // [2] F of step k built
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(done_bar + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, hf = warp >> 2;
 
-    if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (warp == 0) tc::tmem_alloc(tslot, 64);
     if (tid == 0) {
         prefetch_tmap(&maps.x);
         prefetch_tmap(&maps.b);
-        if (!STATES) prefetch_tmap(&maps.c);
-        mbar_init(tma_bar, 1);
-        mbar_init(mma_bar, 1);
+        for (int s = 0; s < kCStages; ++s) mbar_init(&tma_bar[s], 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&mma_bar[j], 1);
+            mbar_init(&done_bar[j], kCompute);
+        }
         mbar_fence_init();
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
 
-    // state held by this thread: h[p][n] for n = 32 qd + lane, p = 32 hf .. 32 hf + 31
-    const int hn = 32 * qd + lane;
-    const size_t PN = static_cast<size_t>(kP) * kNs;
-    const size_t bh = static_cast<size_t>(b) * a.nheads + hd;
-    float h[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) h[i] = 0.f;
-    if (!STATES) {
-        if (a.h0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = a.h0[bh * PN + static_cast<size_t>(32 * hf + i) * kNs + hn];
+    if (warp == kLoadWarp) {
+        // step k of the walk handles chunk ce - 1 - k
+        auto issue = [&](int k) {
+            const int c = ce - 1 - k;
+            unsigned char* st = sm + (k % kCStages) * kCStBytes;
+            uint64_t* bar = &tma_bar[k % kCStages];
+            mbar_arrive_expect_tx(bar, kTxCut);
+            tma_load_4d(st + kCStX, &maps.x, 0, hd, c * kQ, b, bar);
+            tma_load_4d(st + kCStB, &maps.b, 0, g, c * kQ, b, bar);
+            tma_load_4d(st + kCStB + 8192, &maps.b, 64, g, c * kQ, b, bar);
+            bulk_load(st + kCStArr, arrs + wstart + c, kArrBytes, bar);
+        };
+        if (lane == 0)
+            for (int k = 0; k < kCStages && k < n; ++k) issue(k);
+        for (int k = 0; k < n; ++k) {
+            mbar_wait_warp(&done_bar[k & 1], (k >> 1) & 1);
+            // the stage of step k-2 is free: the compute warps saw its MMA complete
+            if (lane == 0 && k >= 2 && k + 2 < n) issue(k + 2);
         }
-        // state passing over the segments before this one
-        for (int j = 0; j < seg; ++j) {
-            const float dec = seg_decay[bh * (nseg - 1) + j];
-            const float* sl = seg_state + (bh * (nseg - 1) + j) * PN;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = dec * h[i] + sl[static_cast<size_t>(32 * hf + i) * kNs + hn];
-        }
-        // carried state as the bf16 operand of MMA3: row n of Hm holds h[., n]
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 w = make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
-                                       pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
-            *reinterpret_cast<uint4*>(sm + kOffHm + chunk_off(hn, 4 * hf + j)) = w;
-        }
-    }
-
-    auto issue = [&](int c) {
-        mbar_arrive_expect_tx(tma_bar, STATES ? kTxState : kTxFull);
-        tma_load_4d(sm + kOffX, &maps.x, 0, hd, c * kQ, b, tma_bar);
-        tma_load_4d(sm + kOffB, &maps.b, 0, g, c * kQ, b, tma_bar);
-        tma_load_4d(sm + kOffB + 8192, &maps.b, 64, g, c * kQ, b, tma_bar);
-        if (!STATES) {
-            tma_load_4d(sm + kOffC, &maps.c, 0, g, c * kQ, b, tma_bar);
-            tma_load_4d(sm + kOffC + 8192, &maps.c, 64, g, c * kQ, b, tma_bar);
-        }
-    };
-    if (tid == 0 && cb < ce) issue(cb);
-
-    uint32_t tma_phase = 0, mma_phase = 0;
-    float log_decay = 0.f;  // sum of Delta*A over the segment (states mode)
-    const float Dh = a.D ? a.D[hd] : 0.f;
-    const Tin* Z = static_cast<const Tin*>(a.z);
-
-    // raw time steps of the next chunk, fetched one chunk ahead (warp 0, two per lane)
-    float dt_next[2] = {0.f, 0.f};
-    auto fetch_dt = [&](int c) {
-        const int t0 = c * kQ, q = min(kQ, L - t0);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int s = 2 * lane + j;
-            dt_next[j] = s < q ? to_f32(DT[(static_cast<size_t>(b) * L + t0 + s) * a.nheads + hd]) : 0.f;
-        }
-    };
-    if (warp == 0 && cb < ce) fetch_dt(cb);
-
-    for (int c = cb; c < ce; ++c) {
-        const int t0 = c * kQ;
-        const int q = min(kQ, L - t0);
-        float dt_raw[2] = {dt_next[0], dt_next[1]};
-        if (warp == 0 && c + 1 < ce) fetch_dt(c + 1);
-        mbar_wait(tma_bar, tma_phase);
-        tma_phase ^= 1;
-
-        // (a) Delta, running sums and weights of the chunk (warp 0: two steps per lane)
-        if (warp == 0) {
-            float d2[2], w2[2], c2[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int s = 2 * lane + j;
-                float dt = 0.f;
-                if (s < q) {
-                    const float v = dt_raw[j] + bias;
-                    dt = a.dt_softplus ? softplus_accurate(v) : v;
-                }
-                d2[j] = dt * Ah;
-                w2[j] = a.disc == SSM_DISC_ZOH ? dt * phi1f(dt * Ah) : dt;
-            }
-            c2[0] = d2[0];
-            c2[1] = d2[0] + d2[1];
-            float run = c2[1];  // inclusive prefix of lane sums
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, run, off);
-                if (lane >= off) run += o;
-            }
-            const float excl = run - c2[1];
-            const float last = __shfl_sync(0xffffffffu, run, 31);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int s = 2 * lane + j;
-                const float cs = excl + c2[j];
-                cum[s] = cs;
-                wv[s] = w2[j];
-                fv[s] = expf(last - cs) * w2[j];
-                ev[s] = expf(cs);
-            }
-            if (lane == 0) log_decay += last;
-        }
-        __syncthreads();
-
-        // x values this thread needs in the output epilogue (row t, 32 columns), kept in
-        // registers so the stage can take the next chunk's tiles before the epilogue
-        uint4 xkeep[4];
-        if (!STATES) {
-            const int t = 16 * qd + (lane & 15);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                xkeep[j] = *reinterpret_cast<const uint4*>(sm + kOffX + chunk_off(t, 4 * hf + j));
-        }
-
-        if (!STATES && tid == 0) {  // MMA1: CB = C . B^T
+    } else if (warp == kMmaWarp) {
+        for (int k = 0; k < n; ++k) {
+            mbar_wait_warp(&done_bar[k & 1], (k >> 1) & 1);
+            mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);  // complete already
             tc::fence_after();
-            const uint32_t sc = smem_u32(sm + kOffC), sb = smem_u32(sm + kOffB);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (k >> 2) * 8192 + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColCB, tc::desc_sw128(sc + off), tc::desc_sw128(sb + off),
-                             tc::idesc_bf16(64, 64), k > 0);
-            }
-            tc::mma_commit(mma_bar);
-        }
-        // (b) F[s][p] = f_s x_s[p] as bf16 hi + lo (row s, 16 columns per thread)
-        {
-            const int s = tid >> 2, pq = tid & 3;
-            const float f = fv[s];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int cq = 2 * pq + j;
-                float v[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + kOffX + chunk_off(s, cq)), v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= f;
-                uint4 hi, lo;
-                split8(v, hi, lo);
-                *reinterpret_cast<uint4*>(sm + kOffFh + chunk_off(s, cq)) = hi;
-                *reinterpret_cast<uint4*>(sm + kOffFl + chunk_off(s, cq)) = lo;
-            }
-        }
-        if (!STATES) {
-            // (c) masked, decayed, weighted CB -> M_hi, M_lo (row t = 16 qd + lane for
-            //     lane < 16; columns s = 32 hf .. 32 hf + 31)
-            mbar_wait(mma_bar, mma_phase);
-            mma_phase ^= 1;
-            tc::fence_after();
-            const int t = 16 * qd + (lane & 15);
-            float cbv[32];
-            tc::tmem_ld16(tlane + kColCB + 32 * hf, cbv);
-            tc::tmem_ld16(tlane + kColCB + 32 * hf + 16, cbv + 16);
-            if (lane < 16) {
-                const float ct = cum[t];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float m[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int s = 32 * hf + 8 * j + e;
-                        m[e] = (s <= t && t < q) ? cbv[8 * j + e] * expf(ct - cum[s]) * wv[s] : 0.f;
-                    }
-                    uint4 hi, lo;
-                    split8(m, hi, lo);
-                    *reinterpret_cast<uint4*>(sm + kOffMh + chunk_off(t, 4 * hf + j)) = hi;
-                    *reinterpret_cast<uint4*>(sm + kOffMl + chunk_off(t, 4 * hf + j)) = lo;
-                }
-            }
-        }
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-
-        if (tid == 0) {
-            tc::fence_after();
-            const uint32_t sx = smem_u32(sm + kOffX), sbm = smem_u32(sm + kOffB);
-            if (!STATES) {
-                const uint32_t smh = smem_u32(sm + kOffMh), sml = smem_u32(sm + kOffMl);
-                const uint32_t idn = tc::idesc_bf16_mn(64, 64, false, true);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)  // MMA2: Yd = M_hi X + M_lo X
-                    tc::mma_bf16(tmem + kColYd, tc::desc_sw128(smh + k * 32),
-                                 tc::desc_sw128_mn(sx + k * 2048, 8192), idn, k > 0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tc::mma_bf16(tmem + kColYd, tc::desc_sw128(sml + k * 32),
-                                 tc::desc_sw128_mn(sx + k * 2048, 8192), idn, 1);
-                const uint32_t sc = smem_u32(sm + kOffC), sh = smem_u32(sm + kOffHm);
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // MMA3: Yo = C H^T
-                    tc::mma_bf16(tmem + kColYo, tc::desc_sw128(sc + (k >> 2) * 8192 + (k & 3) * 32),
-                                 tc::desc_sw128_mn(sh + k * 2048, 16384), idn, k > 0);
-            }
-            const uint32_t sfh = smem_u32(sm + kOffFh), sfl = smem_u32(sm + kOffFl);
+            const unsigned char* st = sm + (k % kCStages) * kCStBytes;
+            const uint32_t sbm = smem_u32(st + kCStB);
+            const uint32_t sf = smem_u32(sm + kCOffF + (k & 1) * 16384);
             const uint32_t id4 = tc::idesc_bf16_mn(128, 64, true, true);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // MMA4: S = B^T F_hi + B^T F_lo
-                tc::mma_bf16(tmem + kColS, tc::desc_sw128_mn(sbm + k * 2048, 8192),
-                             tc::desc_sw128_mn(sfh + k * 2048, 8192), id4, k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                tc::mma_bf16(tmem + kColS, tc::desc_sw128_mn(sbm + k * 2048, 8192),
-                             tc::desc_sw128_mn(sfl + k * 2048, 8192), id4, 1);
-            tc::mma_commit(mma_bar);
+            for (int kk = 0; kk < 4; ++kk) {
+                tc::mma_bf16_warp(tmem, tc::desc_sw128_mn(sbm + kk * 2048, 8192),
+                                  tc::desc_sw128_mn(sf + kk * 2048, 8192), id4, (k > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_bf16_warp(tmem, tc::desc_sw128_mn(sbm + kk * 2048, 8192),
+                                  tc::desc_sw128_mn(sf + 8192 + kk * 2048, 8192), id4, 1u);
+            }
+            tc::mma_commit_warp(&mma_bar[k & 1]);
+            __syncwarp();
         }
-        mbar_wait(mma_bar, mma_phase);
-        mma_phase ^= 1;
+    } else {
+        const int fs = tid >> 3, fp = (tid & 7) * 8;  // F element (s, p..p+7)
+        float tailf = 1.f;  // decay of the chunks already walked (later in time)
+        for (int k = 0; k < n; ++k) {
+            if (k >= 2) {  // MMA of step k-2 done: its F buffer is free
+                mbar_wait_warp(&mma_bar[k & 1], ((k - 2) >> 1) & 1);
+                tc::fence_after();
+            }
+            mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);
+            const unsigned char* st = sm + (k % kCStages) * kCStBytes;
+            const ChunkArr& A = *reinterpret_cast<const ChunkArr*>(st + kCStArr);
+            const float cend = A.cum2[kQ - 1];
+            const float f = tailf * ex2_approx(cend - A.cum2[fs]) * A.w[fs];
+            tailf *= ex2_approx(cend);
+            float v[8];
+            unpack8(*reinterpret_cast<const uint4*>(st + kCStX + chunk_off(fs, fp >> 3)), v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] *= f;
+            uint4 hi, lo;
+            split8(v, hi, lo);
+            unsigned char* F = sm + kCOffF + (k & 1) * 16384;
+            *reinterpret_cast<uint4*>(F + chunk_off(fs, fp >> 3)) = hi;
+            *reinterpret_cast<uint4*>(F + 8192 + chunk_off(fs, fp >> 3)) = lo;
+            tc::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&done_bar[k & 1]);
+        }
+        mbar_wait_warp(&mma_bar[(n - 1) & 1], ((n - 1) >> 1) & 1);
         tc::fence_after();
-        // every read of the stage is done: bring in the next chunk while the epilogues run
-        if (tid == 0 && c + 1 < ce) issue(c + 1);
+        const int q4 = warp & 3, cg = warp >> 2;
+        const int hn = 32 * q4 + lane, hp = 16 * cg;
+        uint32_t r[16];
+        tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + hp, r);
+        tc::tmem_wait();
+        float* dst = cut_state + static_cast<size_t>(ci) * kP * kNs;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]);
+        if (tid == 0) cut_decay[ci] = tailf;
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+}
 
-        if (!STATES) {  // (d) outputs: row t = 16 qd + lane (lane < 16), p = 32 hf .. + 31
-            const int t = 16 * qd + (lane & 15);
-            float yd[32], yo[32];
-            tc::tmem_ld16(tlane + kColYd + 32 * hf, yd);
-            tc::tmem_ld16(tlane + kColYd + 32 * hf + 16, yd + 16);
-            tc::tmem_ld16(tlane + kColYo + 32 * hf, yo);
-            tc::tmem_ld16(tlane + kColYo + 32 * hf + 16, yo + 16);
-            if (lane < 16 && t < q) {
-                const float et = ev[t];
-                const size_t row = ((static_cast<size_t>(b) * L + t0 + t) * a.nheads + hd) * kP + 32 * hf;
-                float out[32];
+// ---------------------------------------------------------------------------------------
+// main launch
+// ---------------------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_tc_main(const __grid_constant__ SsdMaps maps, SsdArgs a, int nct, const ChunkArr* arrs,
+                const float* cut_state, const float* cut_decay) {
+    const int L = a.seqlen, H = a.nheads;
+    const int nch = (L + kQ - 1) / kQ;
+    const long long total = static_cast<long long>(a.batch) * H * nch;
+    const int ci = blockIdx.x;
+    const long long u0 = range_begin(total, nct, ci), u1 = range_begin(total, nct, ci + 1);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kOffBar);  // [kStages]
+    uint64_t* bar_a = tma_bar + kStages;  // [2] MMA1 (C B^T) of a chunk done, by chunk parity
+    uint64_t* bar_b = bar_a + 2;          // MMA2-4 of a chunk done
+    uint64_t* done_bar = bar_b + 1;       // [2] the compute warps finished a step
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(done_bar + 2);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (tid == 0) {
+        prefetch_tmap(&maps.x);
+        prefetch_tmap(&maps.b);
+        prefetch_tmap(&maps.c);
+        for (int s = 0; s < kStages; ++s) mbar_init(&tma_bar[s], 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&bar_a[j], 1);
+            mbar_init(&done_bar[j], kCompute);
+        }
+        mbar_init(bar_b, 1);
+        mbar_fence_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+    const Tin* Z = static_cast<const Tin*>(a.z);
+    const size_t PN = static_cast<size_t>(kP) * kNs;
+
+    // Running chunk number G over the CTA's ranges: stage G % 3, CB slot and M/F buffers
+    // G & 1, bar_a[G & 1] with parity (G >> 1) & 1.  Steps (n + 1 per range) alternate
+    // between the two done barriers, so that no waiter can fall two phases behind.
+    uint32_t gseq = 0, dstep = 0, b_seq = 0;
+
+    for (long long u = u0; u < u1;) {
+        const int wk = static_cast<int>(u / nch);
+        const int c0 = static_cast<int>(u % nch);
+        const int n = static_cast<int>(min(static_cast<long long>(nch - c0), u1 - u));
+        const int b = wk / H, hd = wk % H, g = hd / (H / a.ngroups);
+        const size_t bh = static_cast<size_t>(b) * H + hd;
+        const uint32_t G0 = gseq;
+        auto stage_of = [&](int k) { return sm + ((G0 + k) % kStages) * kStBytes; };
+        auto tma_bar_of = [&](int k) { return &tma_bar[(G0 + k) % kStages]; };
+        auto tma_par = [&](int k) { return ((G0 + k) / kStages) & 1; };
+
+        if (warp == kLoadWarp) {
+            auto issue = [&](int k) {  // chunk c0 + k
+                const int c = c0 + k;
+                unsigned char* st = stage_of(k);
+                uint64_t* bar = tma_bar_of(k);
+                mbar_arrive_expect_tx(bar, kTxMain);
+                tma_load_4d(st + kStX, &maps.x, 0, hd, c * kQ, b, bar);
+                tma_load_4d(st + kStB, &maps.b, 0, g, c * kQ, b, bar);
+                tma_load_4d(st + kStB + 8192, &maps.b, 64, g, c * kQ, b, bar);
+                tma_load_4d(st + kStC, &maps.c, 0, g, c * kQ, b, bar);
+                tma_load_4d(st + kStC + 8192, &maps.c, 64, g, c * kQ, b, bar);
+                bulk_load(st + kStArr, arrs + static_cast<size_t>(wk) * nch + c, kArrBytes, bar);
+            };
+            if (lane == 0)
+                for (int k = 0; k < kStages && k < n; ++k) issue(k);
+            for (int k = 0; k <= n; ++k) {
+                mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);
+                ++dstep;
+                // the stage of chunk k-1 is free (its MMAs and outputs are done)
+                if (lane == 0 && k >= 1 && k + 2 < n) issue(k + 2);
+            }
+        } else if (warp == kMmaWarp) {
+            auto mma1 = [&](int k) {  // CB of chunk k into its slot, then commit
+                if (lane == 0) mbar_wait(tma_bar_of(k), tma_par(k));
+                __syncwarp();
+                const unsigned char* st = stage_of(k);
+                const uint32_t sc = smem_u32(st + kStC), sb = smem_u32(st + kStB);
+                const uint32_t slot = tmem + kColCB + 64 * ((G0 + k) & 1);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float xv[8];
-                    unpack8(xkeep[j], xv);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    tc::mma_bf16_warp(slot, tc::desc_sw128(sc + off), tc::desc_sw128(sb + off),
+                                      tc::idesc_bf16(64, 64), kk > 0);
+                }
+                tc::mma_commit_warp(&bar_a[(G0 + k) & 1]);
+            };
+            mma1(0);
+            if (n > 1) mma1(1);
+            for (int k = 0; k <= n; ++k) {
+                mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);  // compute warps finished step k
+                ++dstep;
+                tc::fence_after();
+                if (k < n) {
+                    const unsigned char* st = stage_of(k);
+                    const uint32_t sx = smem_u32(st + kStX), sb = smem_u32(st + kStB),
+                                   sc = smem_u32(st + kStC);
+                    const uint32_t smh = smem_u32(sm + kOffM + ((G0 + k) & 1) * 16384), sml = smh + 8192;
+                    const uint32_t sfh = smem_u32(sm + kOffF + ((G0 + k) & 1) * 16384), sfl = sfh + 8192;
+                    const uint32_t sh = smem_u32(sm + kOffHm);
+                    const uint32_t idn = tc::idesc_bf16_mn(64, 64, false, true);
+                    const uint32_t id4 = tc::idesc_bf16_mn(128, 64, true, true);
+                    // three independent accumulations, interleaved
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 8 * j + e;
-                        float v = yd[i] + et * yo[i] + Dh * xv[e];
-                        if (Z) v *= silu_accurate(to_f32(Z[row + i]));
-                        out[i] = v;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // MMA2: Yd = M_hi X + M_lo X
+                        const uint32_t sm2 = (kk < 4 ? smh : sml) + (kk & 3) * 32;
+                        tc::mma_bf16_warp(tmem + kColYd, tc::desc_sw128(sm2),
+                                          tc::desc_sw128_mn(sx + (kk & 3) * 2048, 8192), idn, kk > 0);
+                        // MMA4: S = B^T F_hi + B^T F_lo
+                        const uint32_t sf4 = (kk < 4 ? sfh : sfl) + (kk & 3) * 2048;
+                        tc::mma_bf16_warp(tmem + kColS, tc::desc_sw128_mn(sb + (kk & 3) * 2048, 8192),
+                                          tc::desc_sw128_mn(sf4, 8192), id4, kk > 0);
+                        // MMA3: Yo = C H^T (K = 128 over n)
+                        tc::mma_bf16_warp(tmem + kColYo, tc::desc_sw128(sc + (kk >> 2) * 8192 + (kk & 3) * 32),
+                                          tc::desc_sw128_mn(sh + kk * 2048, 16384), idn, kk > 0);
+                    }
+                    tc::mma_commit_warp(bar_b);
+                }
+                __syncwarp();
+                if (k + 2 < n) mma1(k + 2);  // its slot held CB of chunk k, read in step k
+            }
+        } else {
+            const int q4 = warp & 3, cg = warp >> 2;
+            const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+            const int tr = 16 * q4 + (lane & 15);        // row t (M build, outputs)
+            const int pc = 8 * cg + 32 * (lane >> 4);    // first of 8 columns (s in M, p in outputs)
+            const int hn = 32 * q4 + lane, hp = 16 * cg;  // state row n, first of 16 columns p
+            const int fs = tid >> 3, fp = (tid & 7) * 8;  // F element (s, p..p+7)
+            const float Dh = a.D ? a.D[hd] : 0.f;
+
+            // state at the start of the range in this sequence: h0, then the cuts before it
+            float h[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) h[j] = a.h0 ? a.h0[bh * PN + static_cast<size_t>(hp + j) * kNs + hn] : 0.f;
+            if (c0 > 0) {
+                const long long ws = static_cast<long long>(wk) * nch;
+                int j0 = ci - 1;
+                while (j0 > 0 && range_begin(total, nct, j0) > ws) --j0;
+                for (int j = j0; j < ci; ++j) {
+                    const float dec = cut_decay[j];
+                    const float* cs = cut_state + static_cast<size_t>(j) * PN;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) h[i] = dec * h[i] + cs[static_cast<size_t>(hp + i) * kNs + hn];
+                }
+            }
+            auto write_hm = [&]() {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    *reinterpret_cast<uint4*>(sm + kOffHm + chunk_off(hn, 2 * cg + j)) =
+                        make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                   pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+            };
+            write_hm();
+
+            for (int k = 0; k <= n; ++k) {
+                if (k < n) {
+                    const uint32_t G = G0 + k;
+                    mbar_wait_warp(&bar_a[G & 1], (G >> 1) & 1);  // CB of chunk k is in its slot
+                    tc::fence_after();
+                    uint32_t r[8];
+                    tc::tmem_ld_16x32bx2_x8(tlane + kColCB + 64 * (G & 1) + 8 * cg, r);
+                    mbar_wait_warp(tma_bar_of(k), tma_par(k));
+                    const unsigned char* st = stage_of(k);
+                    const ChunkArr& A = *reinterpret_cast<const ChunkArr*>(st + kStArr);
+                    unsigned char* Mb = sm + kOffM + (G & 1) * 16384;
+                    unsigned char* Fb = sm + kOffF + (G & 1) * 16384;
+                    const float cend = A.cum2[kQ - 1];
+                    // (2) F[s][p] = f_s x_s[p] as bf16 hi + lo, f_s = exp(s_end - s_s) w_s
+                    {
+                        const float f = ex2_approx(cend - A.cum2[fs]) * A.w[fs];
+                        float v[8];
+                        unpack8(*reinterpret_cast<const uint4*>(st + kStX + chunk_off(fs, fp >> 3)), v);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] *= f;
+                        uint4 hi, lo;
+                        split8(v, hi, lo);
+                        *reinterpret_cast<uint4*>(Fb + chunk_off(fs, fp >> 3)) = hi;
+                        *reinterpret_cast<uint4*>(Fb + 8192 + chunk_off(fs, fp >> 3)) = lo;
+                    }
+                    // (1) M[t][s] = CB[t][s] exp(s_t - s_s) w_s for s <= t, as bf16 hi + lo
+                    {
+                        const float ct = A.cum2[tr];
+                        float csa[8], wsa[8];
+                        *reinterpret_cast<float4*>(csa) = *reinterpret_cast<const float4*>(&A.cum2[pc]);
+                        *reinterpret_cast<float4*>(csa + 4) = *reinterpret_cast<const float4*>(&A.cum2[pc + 4]);
+                        *reinterpret_cast<float4*>(wsa) = *reinterpret_cast<const float4*>(&A.w[pc]);
+                        *reinterpret_cast<float4*>(wsa + 4) = *reinterpret_cast<const float4*>(&A.w[pc + 4]);
+                        tc::tmem_wait();
+                        float m[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float v = __uint_as_float(r[e]) * ex2_approx(ct - csa[e]) * wsa[e];
+                            m[e] = (pc + e <= tr) ? v : 0.f;
+                        }
+                        uint4 hi, lo;
+                        split8(m, hi, lo);
+                        *reinterpret_cast<uint4*>(Mb + chunk_off(tr, pc >> 3)) = hi;
+                        *reinterpret_cast<uint4*>(Mb + 8192 + chunk_off(tr, pc >> 3)) = lo;
                     }
                 }
-                store_row<32>(static_cast<Tout*>(a.y) + row, out, 32);
-            }
-        }
-        {  // (e) state update: row n = 32 qd + lane, p = 32 hf .. + 31
-            float sv[32];
-            tc::tmem_ld16(tlane + kColS + 32 * hf, sv);
-            tc::tmem_ld16(tlane + kColS + 32 * hf + 16, sv + 16);
-            const float dec = expf(cum[kQ - 1]);
+                if (k > 0) {
+                    const int kp = k - 1;
+                    mbar_wait_warp(bar_b, b_seq & 1);  // Y_diag, Y_off and S of chunk k-1
+                    ++b_seq;
+                    tc::fence_after();
+                    uint32_t yd[8], yo[8], sv[16];
+                    tc::tmem_ld_16x32bx2_x8(tlane + kColYd + 8 * cg, yd);
+                    tc::tmem_ld_16x32bx2_x8(tlane + kColYo + 8 * cg, yo);
+                    tc::tmem_ld_32x32b_x16(tlane + kColS + hp, sv);
+                    const unsigned char* st = stage_of(kp);
+                    const ChunkArr& A = *reinterpret_cast<const ChunkArr*>(st + kStArr);
+                    const int t0 = (c0 + kp) * kQ;
+                    const bool live = tr < L - t0;
+                    float xv[8];
+                    unpack8(*reinterpret_cast<const uint4*>(st + kStX + chunk_off(tr, pc >> 3)), xv);
+                    const float et = ex2_approx(A.cum2[tr]), dec = ex2_approx(A.cum2[kQ - 1]);
+                    const size_t row = ((static_cast<size_t>(b) * L + t0 + tr) * H + hd) * kP + pc;
+                    float zv[8];
+                    if (Z && live) unpack8(*reinterpret_cast<const uint4*>(Z + row), zv);
+                    tc::tmem_wait();
+                    // (4) state after chunk kp: row n = hn, columns p = hp .. hp + 15
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = dec * h[i] + sv[i];
-            if (!STATES) {
+                    for (int j = 0; j < 16; ++j) h[j] = dec * h[j] + __uint_as_float(sv[j]);
+                    write_hm();
+                    // (3) outputs of chunk kp: row t = tr, columns p = pc .. pc + 7
+                    if (live) {
+                        float out[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 w = make_uint4(pack_bf16x2(h[8 * j], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
-                                               pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
-                    *reinterpret_cast<uint4*>(sm + kOffHm + chunk_off(hn, 4 * hf + j)) = w;
+                        for (int e = 0; e < 8; ++e) {
+                            float v = __uint_as_float(yd[e]) + et * __uint_as_float(yo[e]) + Dh * xv[e];
+                            if (Z) v *= silu_accurate(zv[e]);
+                            out[e] = v;
+                        }
+                        Tout* yp = static_cast<Tout*>(a.y) + row;
+                        if constexpr (sizeof(Tout) == 2) {
+                            *reinterpret_cast<uint4*>(yp) =
+                                make_uint4(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]),
+                                           pack_bf16x2(out[4], out[5]), pack_bf16x2(out[6], out[7]));
+                        } else {
+                            reinterpret_cast<float4*>(yp)[0] = make_float4(out[0], out[1], out[2], out[3]);
+                            reinterpret_cast<float4*>(yp)[1] = make_float4(out[4], out[5], out[6], out[7]);
+                        }
+                    }
                 }
+                tc::fence_async_smem();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&done_bar[dstep & 1]);
+                ++dstep;
+            }
+            if (c0 + n == nch && a.h_final) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a.h_final[bh * PN + static_cast<size_t>(hp + j) * kNs + hn] = h[j];
             }
         }
-        tc::fence_async_smem();
-        tc::fence_before();
-        __syncthreads();
-    }
-
-    if (STATES) {
-        float* sl = seg_state + (bh * (nseg - 1) + seg) * PN;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sl[static_cast<size_t>(32 * hf + i) * kNs + hn] = h[i];
-        if (tid == 0) seg_decay[bh * (nseg - 1) + seg] = expf(log_decay);
-    } else if (a.h_final && seg == nseg - 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a.h_final[bh * PN + static_cast<size_t>(32 * hf + i) * kNs + hn] = h[i];
+        gseq += n;
+        u += n;
     }
     tc::fence_before();
     __syncthreads();
@@ -416,6 +584,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 cudaError_t encode_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                       uint64_t d3);
+
+long long tc_units(const SsdArgs& a) {
+    return static_cast<long long>(a.batch) * a.nheads * ((a.seqlen + kQ - 1) / kQ);
+}
+
+// one range per SM (fewer when there are fewer units)
+int tc_ctas(long long total) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return static_cast<int>(total < sms ? total : sms);
+}
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// workspace: cut states [nct][P][N] fp32, cut decays [nct], step quantities [units]
+struct TcWorkspace {
+    size_t off_decay, off_arr, bytes;
+    TcWorkspace(int nct, long long units) {
+        off_decay = round256(static_cast<size_t>(nct) * kP * kNs * sizeof(float));
+        off_arr = off_decay + round256(static_cast<size_t>(nct) * sizeof(float));
+        bytes = off_arr + round256(static_cast<size_t>(units) * kArrBytes);
+    }
+};
 
 }  // namespace
 
@@ -426,54 +618,50 @@ bool ssd_tc_supported(const SsdArgs& a) {
            a.seqlen > 0;
 }
 
-int ssd_tc_segments(const SsdArgs& a) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int nch = (a.seqlen + kQ - 1) / kQ;
-    const long long units = static_cast<long long>(a.batch) * a.nheads;
-    int S = static_cast<int>((2LL * sms) / units);  // one wave at two CTAs per SM
-    if (S < 1) S = 1;
-    if (S > nch) S = nch;
-    if (S > 64) S = 64;
-    return S;
-}
-
 size_t ssd_tc_workspace_bytes(const SsdArgs& a) {
-    const int S = ssd_tc_segments(a);
-    const size_t units = static_cast<size_t>(a.batch) * a.nheads * (S > 1 ? S - 1 : 0);
-    return ((units * kP * kNs * sizeof(float) + 255) / 256) * 256 + ((units * 4 + 255) / 256) * 256;
+    const long long units = tc_units(a);
+    return TcWorkspace(tc_ctas(units), units).bytes;
 }
 
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
-    const int S = ssd_tc_segments(a);
+    const long long total = tc_units(a);
+    const int nct = tc_ctas(total);
+    const TcWorkspace wl(nct, total);
     SsdMaps maps;
     cudaError_t e;
     const uint64_t H = a.nheads, G = a.ngroups, L = a.seqlen, Bt = a.batch;
     if ((e = encode_4d(&maps.x, a.x, kP, H, L, Bt)) != cudaSuccess) return e;
     if ((e = encode_4d(&maps.b, a.B, kNs, G, L, Bt)) != cudaSuccess) return e;
     if ((e = encode_4d(&maps.c, a.C, kNs, G, L, Bt)) != cudaSuccess) return e;
-    const size_t units = static_cast<size_t>(a.batch) * a.nheads * (S > 1 ? S - 1 : 0);
-    float* seg_state = static_cast<float*>(workspace);
-    float* seg_decay = reinterpret_cast<float*>(
-        static_cast<char*>(workspace) + ((units * kP * kNs * sizeof(float) + 255) / 256) * 256);
-    auto set = [](const void* fn) {
-        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    };
-    if (S > 1) {
-        auto k = ssd_tc_kernel<bf16_t, bf16_t, true>;
-        if ((e = set(reinterpret_cast<const void*>(k))) != cudaSuccess) return e;
-        k<<<dim3(S - 1, a.nheads, a.batch), kThreads, kSmemAlloc, s>>>(maps, a, S, seg_state, seg_decay);
+    char* ws = static_cast<char*>(workspace);
+    float* cut_state = reinterpret_cast<float*>(ws);
+    float* cut_decay = reinterpret_cast<float*>(ws + wl.off_decay);
+    ChunkArr* arrs = reinterpret_cast<ChunkArr*>(ws + wl.off_arr);
+    ssd_tc_prep<bf16_t><<<static_cast<unsigned>((total + 7) / 8), 256, 0, s>>>(a, arrs);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // a cut exists where a range boundary falls inside a sequence
+    const int nch = (a.seqlen + kQ - 1) / kQ;
+    bool cuts = false;
+    for (int i = 1; i < nct && !cuts; ++i) cuts = range_begin(total, nct, i) % nch != 0;
+    if (cuts) {
+        if ((e = cudaFuncSetAttribute(ssd_tc_cuts, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kCSmemAlloc)) != cudaSuccess)
+            return e;
+        ssd_tc_cuts<<<nct, kThreads, kCSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.out_dtype == SSM_BF16) {
-        auto k = ssd_tc_kernel<bf16_t, bf16_t, false>;
-        if ((e = set(reinterpret_cast<const void*>(k))) != cudaSuccess) return e;
-        k<<<dim3(S, a.nheads, a.batch), kThreads, kSmemAlloc, s>>>(maps, a, S, seg_state, seg_decay);
+        auto k = ssd_tc_main<bf16_t, bf16_t>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc)) !=
+            cudaSuccess)
+            return e;
+        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
     } else {
-        auto k = ssd_tc_kernel<bf16_t, float, false>;
-        if ((e = set(reinterpret_cast<const void*>(k))) != cudaSuccess) return e;
-        k<<<dim3(S, a.nheads, a.batch), kThreads, kSmemAlloc, s>>>(maps, a, S, seg_state, seg_decay);
+        auto k = ssd_tc_main<bf16_t, float>;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc)) !=
+            cudaSuccess)
+            return e;
+        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
     }
     return cudaGetLastError();
 }

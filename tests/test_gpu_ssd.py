@@ -98,6 +98,18 @@ def test_empty_sequence():
     assert np.array_equal(hf, inp.arrays["h0"].astype(np.float64))
 
 
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_ranges_cross_sequences(oracle_mod, out):
+    """Enough (batch, head, chunk) units that the per-SM ranges hold several chunks, start
+    and stop inside sequences and straddle sequence boundaries; ragged last chunk (4000 =
+    62 x 64 + 32), gate, initial state, two groups."""
+    inp = synth.ssd(2, 4000, 6, 64, 128, 2, dtype=synth.BF16, with_z=True, with_h0=True, seed=6)
+    y, hf = run_gpu(inp, 64, out_dtype=out)
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, out_bf16=(out == "bf16"), what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
 @pytest.mark.parametrize("chunk", [64, 256])
 def test_130m_full_size_sampled(oracle_mod, chunk):
     """Mamba-2 SSD 130m-shaped: batch 4, 24 heads x headdim 64, d_state 128, ngroups 1,
