@@ -30,12 +30,14 @@
 //                                                               as [n][p] (MN-major); the
 //                                                               exp(s_t) row scale is
 //                                                               applied in fp32 afterwards
-//   MMA4  S  = B^T . F_hi + B^T . F_lo        M=128 N=64 K=64   B MN-major; F = f o X,
+//   MMA4  S  = B^T . [F_hi | F_lo]            M=128 N=128 K=64  B MN-major; F = f o X,
 //                                                               f_s = exp(s_end - s_s) w_s,
 //                                                               split into two bf16 parts
+//                                                               side by side along N
 // Warp roles (18 warps): 16 compute warps build M and F of chunk c and then finish the
-// outputs and the state update of chunk c-1; one warp issues the MMAs (MMA2-4 of chunk c
-// once the operands are built, MMA1 two chunks ahead); one warp issues the copies.
+// outputs and the state update of chunk c-1.  Once chunk c is built, one warp issues
+// MMA2 of chunk c and then MMA1 two chunks ahead, another issues MMA3 and MMA4 of chunk
+// c and the TMA copies, so that the two issue streams run on different SM sub-partitions.
 // Hand-offs go through mbarriers; the MMAs of chunk c run while the compute warps build
 // chunk c+1.
 #include <cuda.h>
@@ -56,9 +58,13 @@ constexpr int kMmaWarp = kCompute;             // issues the tensor-core MMAs
 constexpr int kLoadWarp = kCompute + 1;        // issues the TMA copies
 constexpr int kThreads = (kCompute + 2) * 32;
 
-// main launch TMEM columns: two CB slots, Y_diag, Y_off, S
+// main launch TMEM columns: two CB slots, Y_diag, Y_off, S (high then low part)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColCB = 0, kColYd = 128, kColYo = 192, kColS = 256;
+
+// descriptor advanced by `bytes` along its start address (the address field holds
+// address >> 4 in its low 14 bits; shared-memory addresses stay below 2^18)
+__device__ __forceinline__ uint64_t dadv(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 struct SsdMaps {
     CUtensorMap x, b, c;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    if (warp == 0) tc::tmem_alloc(tslot, 64);
+    if (warp == 0) tc::tmem_alloc(tslot, 128);
     if (tid == 0) {
         prefetch_tmap(&maps.x);
         prefetch_tmap(&maps.b);
@@ -255,14 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
             const uint32_t sf = smem_u32(sm + kCOffF + (k & 1) * 16384);
-            const uint32_t id4 = tc::idesc_bf16_mn(128, 64, true, true);
+            // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts
+            const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
+            const uint64_t dB = tc::desc_sw128_mn(sbm, 8192), dF = tc::desc_sw128_mn(sf, 8192);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                tc::mma_bf16_warp(tmem, tc::desc_sw128_mn(sbm + kk * 2048, 8192),
-                                  tc::desc_sw128_mn(sf + kk * 2048, 8192), id4, (k > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_bf16_warp(tmem, tc::desc_sw128_mn(sbm + kk * 2048, 8192),
-                                  tc::desc_sw128_mn(sf + 8192 + kk * 2048, 8192), id4, 1u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                tc::mma_bf16_warp(tmem, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4, (k > 0 || kk > 0) ? 1u : 0u);
             tc::mma_commit_warp(&mma_bar[k & 1]);
             __syncwarp();
         }
@@ -297,17 +301,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after();
         const int q4 = warp & 3, cg = warp >> 2;
         const int hn = 32 * q4 + lane, hp = 16 * cg;
-        uint32_t r[16];
+        uint32_t r[16], r2[16];
         tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + hp, r);
+        tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + hp, r2);
         tc::tmem_wait();
         float* dst = cut_state + static_cast<size_t>(ci) * kP * kNs;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]);
+        for (int j = 0; j < 16; ++j)
+            dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
         if (tid == 0) cut_decay[ci] = tailf;
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_a[j], 1);
             mbar_init(&done_bar[j], kCompute);
         }
-        mbar_init(bar_b, 1);
+        mbar_init(bar_b, 2);  // one commit from each of the two issuing warps
         mbar_fence_init();
     }
     tc::fence_before();
@@ -384,24 +390,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             if (lane == 0)
                 for (int k = 0; k < kStages && k < n; ++k) issue(k);
+            const uint32_t id3 = tc::idesc_bf16_mn(64, 64, false, true);
+            const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
+            const uint64_t dH = tc::desc_sw128_mn(smem_u32(sm + kOffHm), 16384);
             for (int k = 0; k <= n; ++k) {
                 mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);
                 ++dstep;
+                tc::fence_after();
+                if (k < n) {  // MMA3 and MMA4 of chunk k (MMA2 comes from the MMA warp)
+                    const unsigned char* st = stage_of(k);
+                    const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC));
+                    const uint64_t dB = tc::desc_sw128_mn(smem_u32(st + kStB), 8192);
+                    const uint64_t dF = tc::desc_sw128_mn(smem_u32(sm + kOffF + ((G0 + k) & 1) * 16384), 8192);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        // Yo = C H^T (K = 128 over n)
+                        tc::mma_bf16_warp(tmem + kColYo, dadv(dC, (kk >> 2) * 8192 + (kk & 3) * 32),
+                                          dadv(dH, kk * 2048), id3, kk > 0);
+                        // S[n][p_hi | p_lo] = B^T [F_hi | F_lo] (N = 128, K = 64 over s)
+                        if (kk < 4)
+                            tc::mma_bf16_warp(tmem + kColS, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4, kk > 0);
+                    }
+                    tc::mma_commit_warp(bar_b);
+                }
+                __syncwarp();
                 // the stage of chunk k-1 is free (its MMAs and outputs are done)
                 if (lane == 0 && k >= 1 && k + 2 < n) issue(k + 2);
             }
         } else if (warp == kMmaWarp) {
+            const uint32_t id1 = tc::idesc_bf16(64, 64), id2 = tc::idesc_bf16_mn(64, 64, false, true);
             auto mma1 = [&](int k) {  // CB of chunk k into its slot, then commit
                 if (lane == 0) mbar_wait(tma_bar_of(k), tma_par(k));
                 __syncwarp();
                 const unsigned char* st = stage_of(k);
-                const uint32_t sc = smem_u32(st + kStC), sb = smem_u32(st + kStB);
+                const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC)), dB = tc::desc_sw128(smem_u32(st + kStB));
                 const uint32_t slot = tmem + kColCB + 64 * ((G0 + k) & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                    tc::mma_bf16_warp(slot, tc::desc_sw128(sc + off), tc::desc_sw128(sb + off),
-                                      tc::idesc_bf16(64, 64), kk > 0);
+                    tc::mma_bf16_warp(slot, dadv(dC, off), dadv(dB, off), id1, kk > 0);
                 }
                 tc::mma_commit_warp(&bar_a[(G0 + k) & 1]);
             };
@@ -411,30 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);  // compute warps finished step k
                 ++dstep;
                 tc::fence_after();
-                if (k < n) {
+                if (k < n) {  // MMA2 of chunk k: Yd = M_hi X + M_lo X
                     const unsigned char* st = stage_of(k);
-                    const uint32_t sx = smem_u32(st + kStX), sb = smem_u32(st + kStB),
-                                   sc = smem_u32(st + kStC);
-                    const uint32_t smh = smem_u32(sm + kOffM + ((G0 + k) & 1) * 16384), sml = smh + 8192;
-                    const uint32_t sfh = smem_u32(sm + kOffF + ((G0 + k) & 1) * 16384), sfl = sfh + 8192;
-                    const uint32_t sh = smem_u32(sm + kOffHm);
-                    const uint32_t idn = tc::idesc_bf16_mn(64, 64, false, true);
-                    const uint32_t id4 = tc::idesc_bf16_mn(128, 64, true, true);
-                    // three independent accumulations, interleaved
+                    const uint64_t dX = tc::desc_sw128_mn(smem_u32(st + kStX), 8192);
+                    const uint64_t dM = tc::desc_sw128(smem_u32(sm + kOffM + ((G0 + k) & 1) * 16384));
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // MMA2: Yd = M_hi X + M_lo X
-                        const uint32_t sm2 = (kk < 4 ? smh : sml) + (kk & 3) * 32;
-                        tc::mma_bf16_warp(tmem + kColYd, tc::desc_sw128(sm2),
-                                          tc::desc_sw128_mn(sx + (kk & 3) * 2048, 8192), idn, kk > 0);
-                        // MMA4: S = B^T F_hi + B^T F_lo
-                        const uint32_t sf4 = (kk < 4 ? sfh : sfl) + (kk & 3) * 2048;
-                        tc::mma_bf16_warp(tmem + kColS, tc::desc_sw128_mn(sb + (kk & 3) * 2048, 8192),
-                                          tc::desc_sw128_mn(sf4, 8192), id4, kk > 0);
-                        // MMA3: Yo = C H^T (K = 128 over n)
-                        tc::mma_bf16_warp(tmem + kColYo, tc::desc_sw128(sc + (kk >> 2) * 8192 + (kk & 3) * 32),
-                                          tc::desc_sw128_mn(sh + kk * 2048, 16384), idn, kk > 0);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_bf16_warp(tmem + kColYd, dadv(dM, (kk >> 2) * 8192 + (kk & 3) * 32),
+                                          dadv(dX, (kk & 3) * 2048), id2, kk > 0);
                     tc::mma_commit_warp(bar_b);
                 }
                 __syncwarp();
@@ -524,25 +535,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait_warp(bar_b, b_seq & 1);  // Y_diag, Y_off and S of chunk k-1
                     ++b_seq;
                     tc::fence_after();
-                    uint32_t yd[8], yo[8], sv[16];
-                    tc::tmem_ld_16x32bx2_x8(tlane + kColYd + 8 * cg, yd);
-                    tc::tmem_ld_16x32bx2_x8(tlane + kColYo + 8 * cg, yo);
+                    uint32_t sv[16], sl[16];
                     tc::tmem_ld_32x32b_x16(tlane + kColS + hp, sv);
+                    tc::tmem_ld_32x32b_x16(tlane + kColS + 64 + hp, sl);
                     const unsigned char* st = stage_of(kp);
                     const ChunkArr& A = *reinterpret_cast<const ChunkArr*>(st + kStArr);
+                    const float dec = ex2_approx(A.cum2[kQ - 1]);
+                    tc::tmem_wait();
+                    uint32_t yd[8], yo[8];  // in flight during the state update
+                    tc::tmem_ld_16x32bx2_x8(tlane + kColYd + 8 * cg, yd);
+                    tc::tmem_ld_16x32bx2_x8(tlane + kColYo + 8 * cg, yo);
+                    // (4) state after chunk kp: row n = hn, columns p = hp .. hp + 15
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        h[j] = dec * h[j] + (__uint_as_float(sv[j]) + __uint_as_float(sl[j]));
+                    write_hm();
                     const int t0 = (c0 + kp) * kQ;
                     const bool live = tr < L - t0;
                     float xv[8];
                     unpack8(*reinterpret_cast<const uint4*>(st + kStX + chunk_off(tr, pc >> 3)), xv);
-                    const float et = ex2_approx(A.cum2[tr]), dec = ex2_approx(A.cum2[kQ - 1]);
+                    const float et = ex2_approx(A.cum2[tr]);
                     const size_t row = ((static_cast<size_t>(b) * L + t0 + tr) * H + hd) * kP + pc;
                     float zv[8];
                     if (Z && live) unpack8(*reinterpret_cast<const uint4*>(Z + row), zv);
                     tc::tmem_wait();
-                    // (4) state after chunk kp: row n = hn, columns p = hp .. hp + 15
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) h[j] = dec * h[j] + __uint_as_float(sv[j]);
-                    write_hm();
                     // (3) outputs of chunk kp: row t = tr, columns p = pc .. pc + 7
                     if (live) {
                         float out[8];
