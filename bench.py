@@ -360,14 +360,19 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                                    dt_bias=s["dt_bias"], y=s["y"], h_final=s["hf"], workspace=ws)
         n = max(5, min(args.steps, 20))
         tsec = time_launches(torch, f, n, 3, stream)
+        # dense per-chunk products at chunk Q (the roofline's count) and the products the
+        # tensor-core kernels execute (64-step tiles for every Q)
         fl = ssd_flops(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
                        c4["ngroups"], Q)
+        fl_exec = ssd_flops(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"],
+                            c4["dstate"], c4["ngroups"], 64)
         t_roof = max(nb / (hbm * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
         upd = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
         out[f"ssd_130m_chunk{Q}"] = {
             "ms": tsec * 1e3, "state_updates_per_s": upd / tsec, "hbm_gbs": nb / tsec / 1e9,
-            "tflops": fl / tsec / 1e12, "roofline_s": t_roof, "roofline_frac": t_roof / tsec,
-            "bytes": nb, "flops": fl}
+            "tflops_executed": fl_exec / tsec / 1e12, "roofline_s": t_roof,
+            "roofline_frac": t_roof / tsec, "bytes": nb, "flops_dense_chunk": fl,
+            "flops_executed": fl_exec}
     del sets
     # decode step, 780m-shaped: 4 layers' states rotate (each 100.7 MB; together > L2)
     c5 = synth.WORKLOADS["step_780m"]

@@ -128,7 +128,11 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
  * Inside a chunk the output is a decayed-attention product and chunk states are
  * passed between chunks, so the result equals the sequential scan up to
  * rounding.  Limits: Q in {64, 128, 256}; P in {32, 64, 128}; N in {64, 128};
- * G divides H.
+ * G divides H.  With bf16 inputs, P = 64 and N = 128 the tensor-core kernels
+ * run every Q on 64-step tiles: for Q = 128 or 256 the decayed-attention block
+ * of two different tiles of one chunk is applied through the state carried
+ * between them, which is the same product regrouped (exact in real arithmetic),
+ * so the result does not depend on Q there.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
@@ -148,9 +152,9 @@ typedef struct {
     ssm_disc disc;
 } ssd_params;
 
-/* Device scratch needed by ssd_chunk_scan_fwd, in bytes (the float32 chunk
- * states and per-chunk decay sums).  Only the sizes in `p` are read; returns 0
- * when they are invalid or unsupported. */
+/* Device scratch needed by ssd_chunk_scan_fwd, in bytes (float32 chunk or
+ * range states, decays and per-chunk step sums).  Only the sizes in `p` are
+ * read; returns 0 when they are invalid or unsupported. */
 size_t ssd_chunk_scan_workspace_size(const ssd_params* p);
 
 /* Runs the chunked scan; `workspace` is a device buffer of at least

@@ -627,10 +627,15 @@ struct TcWorkspace {
 
 }  // namespace
 
-// The tensor-core path covers the Mamba-2 130m/780m layer shapes: chunk 64, headdim 64,
-// dstate 128, bf16 inputs; other shapes use the CUDA-core kernels in ssd.cu.
+// The tensor-core path covers the Mamba-2 130m/780m layer shapes: headdim 64, dstate 128,
+// bf16 inputs, chunk 64, 128 or 256; other shapes use the CUDA-core kernels in ssd.cu.
+// Every chunk size runs on 64-step tiles.  For a chunk of 128 or 256 steps the
+// decayed-attention block between two different tiles i > j of the chunk,
+//   sum_{s in j} (C_t . B_s) exp(s_t - s_s) w_s x_s  (t in tile i),
+// equals exp(s_t - s_{end of j}) C_t . (sum_{s in j} B_s exp(s_{end of j} - s_s) w_s x_s)
+// carried forward to tile i: the chunk-state product regrouped, exact in real arithmetic.
 bool ssd_tc_supported(const SsdArgs& a) {
-    return a.chunk == kQ && a.headdim == kP && a.dstate == kNs && a.in_dtype == SSM_BF16 &&
+    return a.chunk % kQ == 0 && a.headdim == kP && a.dstate == kNs && a.in_dtype == SSM_BF16 &&
            a.seqlen > 0;
 }
 
