@@ -162,11 +162,12 @@ __device__ __forceinline__ float softplus_accurate(float v) {
 // Fast variant for bfloat16 inputs: e = e^v by MUFU.EX2, then log1p(e) either by the
 // series e - e^2/2 + e^3/3 - e^4/4 (e < 2^-7, truncation below 2^-30 relative) or by
 // MUFU.LG2 of 1 + e (relative error below ~4e-5 there).
+// Branch-free, so that independent evaluations interleave.
 __device__ __forceinline__ float softplus_fast(float v) {
-    if (v > 20.f) return v;
-    float e = ex2_approx(v * SSM_LOG2E);
-    if (e < 0.0078125f) return e * (1.f - e * (0.5f - e * (0.33333334f - 0.25f * e)));
-    return lg2_approx(1.f + e) * SSM_LN2;
+    const float e = ex2_approx(v * SSM_LOG2E);
+    const float series = e * (1.f - e * (0.5f - e * (0.33333334f - 0.25f * e)));
+    const float r = e < 0.0078125f ? series : lg2_approx(1.f + e) * SSM_LN2;
+    return v > 20.f ? v : r;
 }
 __device__ __forceinline__ float silu_accurate(float v) { return v / (1.f + expf(-v)); }
 __device__ __forceinline__ float silu_fast(float v) {

@@ -41,7 +41,7 @@ constexpr int kNS = 4;          // states per thread
 constexpr int kStages = 2;
 constexpr int kRowB = kT * 2;   // bytes per staged row
 constexpr int kDtxS = kT + 1;   // float2 row stride of (dt, dt*x)
-constexpr int kMaxThreads = 384;
+constexpr int kMaxThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 
 struct TmaMaps {
@@ -231,11 +231,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         }
         __syncthreads();
 
-        // (3) recurrence; B/C of 4 steps per tcgen05.ld, the next group's load in flight
-        float part[kT];
+        // (3) recurrence, in two halves of 32 steps (one broadcast MMA each).  B/C of 4
+        // steps per tcgen05.ld with the next group's load in flight; the decays of the
+        // next group are computed before the state updates of the current one, so the
+        // MUFU work of one group overlaps the FMA chain of the other.
         const float2* drow = dtx + c * kDtxS;
+        auto decays = [&](int grp, float2* ddv, float2 (*zz)[kNS / 2]) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ddv[j] = drow[dtx_col(4 * grp + j)];
+#pragma unroll
+                for (int q = 0; q < kNS / 2; ++q) {
+                    const float2 e2 = mul2(make_float2(ddv[j].x, ddv[j].x), A2p[q]);
+                    zz[j][q] = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+                }
+            }
+        };
+        float2 ddv_c[4], zz_c[4][kNS / 2];
+        decays(0, ddv_c, zz_c);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
+            float part[kT / 2];
             mbar_wait(&mmab[hh], k & 1);
             tc::fence_after();
             uint32_t ra[32], rb[32];
@@ -243,66 +259,64 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
             tc::tmem_wait();
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
+                const int grp = 8 * hh + g4;
                 uint32_t* cur = (g4 & 1) ? rb : ra;
                 uint32_t* nxt = (g4 & 1) ? ra : rb;
                 if (g4 < 7) tc::tmem_ld32_async(tl + 256 * hh + 32 * (g4 + 1), nxt);
-                // decays of the group's 4 steps first (independent of the state)
-                float2 ddv[4], zz[4][kNS / 2];
+                float2 ddv_n[4], zz_n[4][kNS / 2];
+                if (grp < 15) decays(grp + 1, ddv_n, zz_n);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    ddv[j] = drow[dtx_col(32 * hh + 4 * g4 + j)];
-#pragma unroll
-                    for (int q = 0; q < kNS / 2; ++q) {
-                        const float2 e2 = mul2(make_float2(ddv[j].x, ddv[j].x), A2p[q]);
-                        zz[j][q] = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 dx2 = make_float2(ddv[j].y, ddv[j].y);
+                    const float2 dx2 = make_float2(ddv_c[j].y, ddv_c[j].y);
                     const uint32_t* r = cur + 8 * j;
                     const float2 b0 = make_float2(__uint_as_float(r[0]), __uint_as_float(r[1]));
                     const float2 b1 = make_float2(__uint_as_float(r[2]), __uint_as_float(r[3]));
                     const float2 c0v = make_float2(__uint_as_float(r[4]), __uint_as_float(r[5]));
                     const float2 c1v = make_float2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-                    hp[0] = fma2(zz[j][0], hp[0], mul2(dx2, b0));
-                    hp[1] = fma2(zz[j][1], hp[1], mul2(dx2, b1));
+                    hp[0] = fma2(zz_c[j][0], hp[0], mul2(dx2, b0));
+                    hp[1] = fma2(zz_c[j][1], hp[1], mul2(dx2, b1));
                     const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
-                    part[32 * hh + 4 * g4 + j] = acc.x + acc.y;
+                    part[4 * g4 + j] = acc.x + acc.y;
                 }
                 if (g4 < 7) tc::tmem_wait();
-            }
-        }
-
-        // (4) reduce-scatter across the channel's 4 threads (kept half moves to the front)
+                if (grp < 15) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int half = kT >> (r + 1);
-            const int bit = kTPC >> (r + 1);
-            const bool keep_lo = (gi & bit) == 0;
+                    for (int j = 0; j < 4; ++j) {
+                        ddv_c[j] = ddv_n[j];
 #pragma unroll
-            for (int i = 0; i < half; ++i) {
-                const float lo = part[i], hi = part[i + half];
-                const float recv = __shfl_xor_sync(0xffffffffu, keep_lo ? hi : lo, bit);
-                part[i] = (keep_lo ? lo : hi) + recv;
-            }
-        }
-        if (active) {
-            float yv[TO];
-#pragma unroll
-            for (int q = 0; q < TO / 8; ++q) {
-                float xv[8], zv[8];
-                load8(st + lay.x, c, tb / 8 + q, xv);
-                if (has_z) load8(st + lay.z, c, tb / 8 + q, zv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float v = part[8 * q + i] + Dd * xv[i];
-                    if (has_z) v *= silu_fast(zv[i]);
-                    yv[8 * q + i] = v;
+                        for (int q = 0; q < kNS / 2; ++q) zz_c[j][q] = zz_n[j][q];
+                    }
                 }
             }
-            Tout* yrow = static_cast<Tout*>(a.y) + static_cast<size_t>(ch) * L + t0 + tb;
-            store_row<TO>(yrow, yv, L - (t0 + tb));
+
+            // (4) reduce-scatter of this half across the channel's 4 threads (the kept half
+            // moves to the front): thread gi ends with steps 32 hh + 8 gi .. + 7
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int half = (kT / 2) >> (r + 1);
+                const int bit = kTPC >> (r + 1);
+                const bool keep_lo = (gi & bit) == 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float lo = part[i], hi = part[i + half];
+                    const float recv = __shfl_xor_sync(0xffffffffu, keep_lo ? hi : lo, bit);
+                    part[i] = (keep_lo ? lo : hi) + recv;
+                }
+            }
+            if (active) {
+                const int te = 32 * hh + 8 * gi;
+                float xv[8], zv[8], yv[8];
+                load8(st + lay.x, c, te / 8, xv);
+                if (has_z) load8(st + lay.z, c, te / 8, zv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float v = part[i] + Dd * xv[i];
+                    if (has_z) v *= silu_fast(zv[i]);
+                    yv[i] = v;
+                }
+                Tout* yrow = static_cast<Tout*>(a.y) + static_cast<size_t>(ch) * L + t0 + te;
+                store_row<8>(yrow, yv, L - (t0 + te));
+            }
         }
         tc::fence_before();
         __syncthreads();  // stage s, dtx, the B/C operands and TMEM are free again
