@@ -19,8 +19,14 @@ import ctypes
 from . import _lib
 from ._lib import SsmError  # noqa: F401
 
-__all__ = ["ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+__all__ = ["wait_timeouts", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
            "ssd_chunk_scan_workspace_size", "SsmError", "lib"]
+
+
+def wait_timeouts() -> int:
+    """Bounded device-side waits that gave up since the previous call (0 in correct
+    operation); synchronises with the device and clears the count."""
+    return int(_lib.load().ssm_wait_timeouts())
 
 
 def lib():

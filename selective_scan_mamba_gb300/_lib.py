@@ -89,6 +89,8 @@ def load(build_if_missing: bool = True):
             lib.ssm_last_error.argtypes = []
             lib.ssm_abi_version.restype = _i
             lib.ssm_abi_version.argtypes = []
+            lib.ssm_wait_timeouts.restype = ctypes.c_uint
+            lib.ssm_wait_timeouts.argtypes = []
             _lib = lib
         return _lib
 

@@ -188,7 +188,7 @@ int ssm_abi_version(void) { return SSM_ABI_VERSION; }
 const char* ssm_last_error(void) { return g_err; }
 
 unsigned int ssm_wait_timeouts(void) {
-    return ssm::m1_tma_wait_timeouts() + ssm::m1_tmem_wait_timeouts();
+    return ssm::m1_tma_wait_timeouts() + ssm::m1_tmem_wait_timeouts() + ssm::ssd_tc_wait_timeouts();
 }
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {

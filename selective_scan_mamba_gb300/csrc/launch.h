@@ -108,6 +108,7 @@ cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
 bool ssd_tc_supported(const SsdArgs& a);
 size_t ssd_tc_workspace_bytes(const SsdArgs& a);
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s);
+unsigned int ssd_tc_wait_timeouts();
 
 // Records `msg` as this thread's ssm_last_error() text and returns `st`.
 ssm_status set_error(ssm_status st, const char* msg);

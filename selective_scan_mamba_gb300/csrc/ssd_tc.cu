@@ -89,7 +89,9 @@ constexpr int kSmemBytes = kOffBar + 128;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr uint32_t kTxMain = 40960 + kArrBytes;
 
-// cuts launch: 4-stage ring of x, B and the step quantities; two F buffers
+// cuts launch: each cut is split into kCutParts parts (separate CTAs), each with a ring
+// of kCStages stages of x, B and the step quantities and two F buffers
+constexpr int kCutParts = 1;
 constexpr int kCStages = 4;
 constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
 constexpr int kCOffF = kCStages * kCStBytes;  // 2 x (F_hi, F_lo) = 2 x 16 KB
@@ -198,15 +200,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = a.seqlen, H = a.nheads;
     const int nch = (L + kQ - 1) / kQ;
     const long long total = static_cast<long long>(a.batch) * H * nch;
-    const int ci = blockIdx.x;
+    const int ci = blockIdx.x / kCutParts, part = blockIdx.x % kCutParts;
     const long long u0 = range_begin(total, nct, ci), u1 = range_begin(total, nct, ci + 1);
     if (u1 <= u0) return;
     const int wk = static_cast<int>((u1 - 1) / nch);
     const long long wstart = static_cast<long long>(wk) * nch;
-    const int ce = static_cast<int>(u1 - wstart);
-    if (ce == nch) return;  // the range ends with its sequence: no cut
-    const int ca = static_cast<int>((u0 > wstart ? u0 : wstart) - wstart);
+    const int cut_end = static_cast<int>(u1 - wstart);
+    if (cut_end == nch) return;  // the range ends with its sequence: no cut
+    const int cut_begin = static_cast<int>((u0 > wstart ? u0 : wstart) - wstart);
+    // this CTA's part of the cut: chunks [ca, ce)
+    const int ca = cut_begin + ((cut_end - cut_begin) * part) / kCutParts;
+    const int ce = cut_begin + ((cut_end - cut_begin) * (part + 1)) / kCutParts;
     const int n = ce - ca;
+    const int oi = ci * kCutParts + part;  // output slot
+    if (n == 0) {  // empty part: zero state, unit decay
+        float* dst = cut_state + static_cast<size_t>(oi) * kP * kNs;
+        for (int i = threadIdx.x; i < kP * kNs; i += blockDim.x) dst[i] = 0.f;
+        if (threadIdx.x == 0) cut_decay[oi] = 1.f;
+        return;
+    }
     const int b = wk / H, hd = wk % H, g = hd / (H / a.ngroups);
 
     extern __shared__ unsigned char smem_raw[];
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < n; ++k) {
             mbar_wait_warp(&done_bar[k & 1], (k >> 1) & 1);
             // the stage of step k-2 is free: the compute warps saw its MMA complete
-            if (lane == 0 && k >= 2 && k + 2 < n) issue(k + 2);
+            if (lane == 0 && k >= 2 && k + kCStages - 2 < n) issue(k + kCStages - 2);
         }
     } else if (warp == kMmaWarp) {
         for (int k = 0; k < n; ++k) {
@@ -305,11 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + hp, r);
         tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + hp, r2);
         tc::tmem_wait();
-        float* dst = cut_state + static_cast<size_t>(ci) * kP * kNs;
+        float* dst = cut_state + static_cast<size_t>(oi) * kP * kNs;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
-        if (tid == 0) cut_decay[ci] = tailf;
+        if (tid == 0) cut_decay[oi] = tailf;
     }
     tc::fence_before();
     __syncthreads();
@@ -420,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kMmaWarp) {
             const uint32_t id1 = tc::idesc_bf16(64, 64), id2 = tc::idesc_bf16_mn(64, 64, false, true);
             auto mma1 = [&](int k) {  // CB of chunk k into its slot, then commit
-                if (lane == 0) mbar_wait(tma_bar_of(k), tma_par(k));
-                __syncwarp();
+                mbar_wait_warp(tma_bar_of(k), tma_par(k));
                 const unsigned char* st = stage_of(k);
                 const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC)), dB = tc::desc_sw128(smem_u32(st + kStB));
                 const uint32_t slot = tmem + kColCB + 64 * ((G0 + k) & 1);
@@ -468,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long ws = static_cast<long long>(wk) * nch;
                 int j0 = ci - 1;
                 while (j0 > 0 && range_begin(total, nct, j0) > ws) --j0;
-                for (int j = j0; j < ci; ++j) {
+                for (int j = j0 * kCutParts; j < ci * kCutParts; ++j) {  // parts in time order
                     const float dec = cut_decay[j];
                     const float* cs = cut_state + static_cast<size_t>(j) * PN;
 #pragma unroll
@@ -615,7 +626,7 @@ int tc_ctas(long long total) {
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// workspace: cut states [nct][P][N] fp32, cut decays [nct], step quantities [units]
+// workspace: cut states [cuts][P][N] fp32, cut decays [cuts], step quantities [units]
 struct TcWorkspace {
     size_t off_decay, off_arr, bytes;
     TcWorkspace(int nct, long long units) {
@@ -641,13 +652,13 @@ bool ssd_tc_supported(const SsdArgs& a) {
 
 size_t ssd_tc_workspace_bytes(const SsdArgs& a) {
     const long long units = tc_units(a);
-    return TcWorkspace(tc_ctas(units), units).bytes;
+    return TcWorkspace(tc_ctas(units) * kCutParts, units).bytes;
 }
 
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     const long long total = tc_units(a);
     const int nct = tc_ctas(total);
-    const TcWorkspace wl(nct, total);
+    const TcWorkspace wl(nct * kCutParts, total);
     SsdMaps maps;
     cudaError_t e;
     const uint64_t H = a.nheads, G = a.ngroups, L = a.seqlen, Bt = a.batch;
@@ -668,7 +679,7 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
         if ((e = cudaFuncSetAttribute(ssd_tc_cuts, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       kCSmemAlloc)) != cudaSuccess)
             return e;
-        ssd_tc_cuts<<<nct, kThreads, kCSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
+        ssd_tc_cuts<<<nct * kCutParts, kThreads, kCSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.out_dtype == SSM_BF16) {
@@ -685,6 +696,13 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
         k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
     }
     return cudaGetLastError();
+}
+
+unsigned int ssd_tc_wait_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero));
+    return v;
 }
 
 namespace {

@@ -53,7 +53,8 @@ __device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity) {
 
 // mbar_wait polled by lane 0 alone; the other lanes wait at __syncwarp, which also makes
 // what lane 0 observed visible to them.  Keeps a large CTA's waiting warps off the issue
-// slots.  All 32 lanes must call it.
+// slots.  All 32 lanes must call it.  (A try_wait with a suspend-time hint measured
+// slower here: the sleeping thread wakes late.)
 __device__ __forceinline__ void mbar_wait_warp(uint64_t* bar, uint32_t parity) {
     if ((threadIdx.x & 31) == 0) mbar_wait(bar, parity);
     __syncwarp();

@@ -188,3 +188,8 @@ def test_790m_long_context_sampled(oracle_mod, L):
     yr, hr = run_oracle(oracle_mod, inp, h0=False, rows=rows)
     check(np.stack([y[b, d] for b, d in rows]), yr, TOL_BF16, out_bf16=True, what="y sampled")
     check(np.stack([hf[b, d] for b, d in rows]), hr, TOL_BF16, what="h_final sampled")
+
+
+def test_zz_no_device_wait_gave_up():
+    """Every bounded wait in the kernels above completed (timeout counter still zero)."""
+    assert ssm.wait_timeouts() == 0

@@ -124,3 +124,9 @@ def test_130m_full_size_sampled(oracle_mod, chunk):
     check(np.stack([y[b, :, h] for b, h in heads]), yr, TOL_BF16, out_bf16=True, what="y sampled")
     check(np.stack([hf[b, h] for b, h in heads]), hr, TOL_BF16, what="h_final sampled")
     assert np.all(np.isfinite(y))
+
+
+def test_zz_no_device_wait_gave_up():
+    """Every bounded wait in the kernels above (copies, MMAs, warp hand-offs) completed:
+    the library's timeout counter is still zero after this file's cases."""
+    assert ssm.wait_timeouts() == 0
