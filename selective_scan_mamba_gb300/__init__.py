@@ -112,12 +112,17 @@ def _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_f
     return p
 
 
-def ssm_scan_workspace_size(x, B) -> int:
-    """Scratch bytes ssm_scan_fwd needs for these shapes."""
+def ssm_scan_workspace_size(x, B, out_dtype=None, disc="exp_euler") -> int:
+    """Scratch bytes ssm_scan_fwd needs for these shapes and dtypes (y defaults to x's
+    dtype)."""
     p = _lib.ScanParams()
     p.batch, p.dim, p.seqlen = x.shape
     p.dstate = B.shape[-2]
     p.ngroups = 1 if B.dim() == 3 else B.shape[1]
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(x) if out_dtype is None else _dtype_code(
+        _torch().empty(0, dtype=out_dtype))
+    p.disc = _disc(disc)
     return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
 
 

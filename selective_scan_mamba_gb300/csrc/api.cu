@@ -55,6 +55,23 @@ bool injected_launch_fault() {
             return fail(SSM_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);   \
     } while (0)
 
+// sizes, dtypes and modes only (what the workspace query reads)
+ssm_status check_scan_sizes(const ssm_scan_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->batch >= 1 && p->dim >= 1 && p->dstate >= 1 && p->seqlen >= 0 && p->ngroups >= 1,
+            "bad sizes: batch=%d dim=%d dstate=%d seqlen=%d ngroups=%d", p->batch, p->dim,
+            p->dstate, p->seqlen, p->ngroups);
+    REQUIRE(p->dim % p->ngroups == 0, "ngroups=%d does not divide dim=%d", p->ngroups, p->dim);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(p->disc == SSM_DISC_EXP_EULER || p->disc == SSM_DISC_ZOH, "unknown discretisation");
+    REQUIRE(static_cast<long long>(p->batch) * p->dim * (p->seqlen > 0 ? p->seqlen : 1) < (1LL << 40),
+            "tensor too large");
+    if (p->dstate > 256) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 256", p->dstate);
+    if (static_cast<long long>(p->batch) * p->dim > (1LL << 31) - 1)
+        return fail(SSM_ERR_UNSUPPORTED, "batch*dim too large");
+    return SSM_OK;
+}
+
 ssm_status check_scan(const ssm_scan_params* p) {
     REQUIRE(p != nullptr, "params is NULL");
     REQUIRE(p->batch >= 1 && p->dim >= 1 && p->dstate >= 1 && p->seqlen >= 0 && p->ngroups >= 1,
@@ -192,14 +209,14 @@ unsigned int ssm_wait_timeouts(void) {
 }
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
-    (void)p;
-    return 0;
+    if (check_scan_sizes(p) != SSM_OK || p->seqlen == 0) return 0;
+    ssm::M1Plan plan;
+    if (ssm::m1_tmem_plan(scan_args(p), &plan) != cudaSuccess) return 0;
+    return plan.kind == ssm::M1Plan::kTmem ? plan.ws_bytes : 0;
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t workspace_bytes,
                         void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     g_err[0] = '\0';
     ssm_status st = check_scan(p);
     if (st != SSM_OK) return st;
@@ -219,7 +236,12 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
     cudaError_t e = ssm::m1_tmem_plan(a, &plan);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd plan");
     if (plan.kind == ssm::M1Plan::kTmem) {
-        e = ssm::m1_tmem_launch(a, plan, s);
+        if (workspace_bytes < plan.ws_bytes)
+            return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                        plan.ws_bytes);
+        if (plan.ws_bytes > 0 && (workspace == nullptr || !aligned16(workspace)))
+            return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+        e = ssm::m1_tmem_launch(a, plan, workspace, s);
         if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
         return SSM_OK;
     }

@@ -37,6 +37,10 @@ struct M1Plan {
     int cpb_max;  // channels per CTA (tiled path)
     size_t smem;  // dynamic shared memory per CTA (tiled path)
     int cps = 0;  // CTAs per (batch, group) (TMEM-broadcast path)
+    int segs = 1;         // time segments (TMEM-broadcast path)
+    int tps = 0;          // tiles per segment
+    size_t ws_state = 0;  // workspace offset of the segment sums of Delta
+    size_t ws_bytes = 0;  // workspace bytes
 };
 
 size_t m1_tiled_smem_bytes(int cpb, int N, int T, size_t elem_size);
@@ -52,7 +56,7 @@ unsigned int m1_tma_wait_timeouts();
 
 // bf16 fast path with B/C broadcast through tensor memory (scan_m1_tmem.cu)
 cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan);
-cudaError_t m1_tmem_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
+cudaError_t m1_tmem_launch(const M1Args& a, const M1Plan& plan, void* workspace, cudaStream_t s);
 unsigned int m1_tmem_wait_timeouts();
 
 // TMA tensor map of a row-major [rows][inner] tensor (tmap.cu)

@@ -15,7 +15,11 @@
 //
 // Work split: CTAs never straddle a (batch, group): grid = pairs x CTAs-per-pair, each CTA
 // a contiguous, balanced range of that pair's channels for the whole sequence, one CTA
-// per SM (512 TMEM columns: two 32-step halves of a 64-step tile).  Four threads per
+// per SM (512 TMEM columns: two 32-step halves of a 64-step tile).  When that leaves few
+// channels per CTA (a long sequence of one batch row), the sequence is split into
+// segments: a first launch runs segments 0 .. S-2 from a zero state and keeps their end
+// states and sums of Delta; the main launch starts each segment from h0 carried through
+// the segments before it (the decay over a segment is exp(A sum Delta)).  Four threads per
 // channel, states n = gi + 4 i.  Per tile: TMA (128-byte swizzle, double buffer) brings x,
 // delta, z rows and the pair's B, C rows; the B/C operand of the broadcast MMA is built
 // (8 bytes per row); (dt, dt*x) pairs are computed once per (b, d, t); the recurrence runs
@@ -83,12 +87,20 @@ __device__ __forceinline__ void load8(const unsigned char* tile, int row, int ch
     }
 }
 
-template <typename Tout>
+// STATES: the segment pass of a time-split scan.  Segment `seg` (of `nseg`) covers tiles
+// [seg * tps, (seg + 1) * tps); this pass runs segments 0 .. nseg-2 from a zero state and
+// writes their end states and sums of Delta to the workspace, without outputs.  The main
+// pass starts segment seg from h0 carried through those (h <- exp(A sum Delta) h + h_seg).
+template <typename Tout, bool STATES>
 __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_constant__ TmaMaps maps,
-                                                                M1Args a, int cps) {
+                                                                M1Args a, int cps, int nseg, int tps,
+                                                                float* seg_state, float* seg_dsum) {
     constexpr int TO = kT / kTPC;
     const int per_group = a.dim / a.ngroups;
-    const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
+    const int segs_here = STATES ? nseg - 1 : nseg;
+    const int seg = blockIdx.x % segs_here;
+    const int rest = blockIdx.x / segs_here;
+    const int pair = rest / cps, part_i = rest % cps;
     const int b = pair / a.ngroups, g = pair % a.ngroups;
     const int l0 = static_cast<int>((static_cast<long long>(part_i) * per_group) / cps);
     const int l1 = static_cast<int>((static_cast<long long>(part_i + 1) * per_group) / cps);
@@ -111,13 +123,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     const int ch = c0 + c;
     const int d = g * per_group + l0 + c;
     const int L = a.seqlen;
-    const int ntiles = (L + kT - 1) / kT;
+    const int ntiles_all = (L + kT - 1) / kT;
+    const int k0 = seg * tps;
+    const int k1 = min(ntiles_all, k0 + tps);
     const uint32_t stage_tx = static_cast<uint32_t>(((has_z ? 3 : 2) * lay.cb + 2 * kN) * kRowB);
 
-    auto issue = [&](int k) {
+    auto issue = [&](int k) {  // tile k0 + k
         unsigned char* st = smem + (k % kStages) * lay.stage;
         uint64_t* bar = &full[k % kStages];
-        const int t0 = k * kT;
+        const int t0 = (k0 + k) * kT;
         mbar_arrive_expect_tx(bar, stage_tx);
         tma_load_2d(st + lay.x, &maps.x, t0, c0, bar);
         tma_load_2d(st + lay.dl, &maps.dl, t0, c0, bar);
@@ -160,6 +174,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     tc::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const int ntiles = k1 - k0;  // tiles of this CTA
     if (tid == 0)
         for (int k = 0; k < kStages && k < ntiles; ++k) issue(k);
 
@@ -174,14 +189,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         A2p[k] = make_float2(a.A[static_cast<size_t>(d) * kN + n0] * SSM_LOG2E,
                              a.A[static_cast<size_t>(d) * kN + n1] * SSM_LOG2E);
     }
+    if (STATES) {
+#pragma unroll
+        for (int k = 0; k < kNS / 2; ++k) hp[k] = make_float2(0.f, 0.f);
+    } else if (active) {
+        const size_t rows = static_cast<size_t>(a.batch) * a.dim;
+        for (int j = 0; j < seg; ++j) {
+            const float ds = seg_dsum[j * rows + ch];
+            const float* hs = seg_state + (j * rows + ch) * kN;
+#pragma unroll
+            for (int k = 0; k < kNS / 2; ++k) {
+                const float2 dec = make_float2(ex2_approx(A2p[k].x * ds), ex2_approx(A2p[k].y * ds));
+                hp[k] = fma2(dec, hp[k], make_float2(hs[gi + kTPC * (2 * k)], hs[gi + kTPC * (2 * k + 1)]));
+            }
+        }
+    }
     const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
     const float Dd = a.D ? a.D[d] : 0.f;
+    float dsum = 0.f;  // sum of Delta over the segment (segment pass)
 
     for (int k = 0; k < ntiles; ++k) {
         const int s = k % kStages;
         const unsigned char* st = smem + s * lay.stage;
         mbar_wait(&full[s], (k / kStages) & 1);
-        const int t0 = k * kT;
+        const int t0 = (k0 + k) * kT;
         const int tb = gi * TO;
 
         // (1) B/C operands of the broadcast MMA: row j = step * 8 + e of half hh holds, at
@@ -225,6 +256,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                     const float v = dv[i] + bias;
                     float dt = a.delta_softplus ? softplus_fast(v) : v;
                     dt = (t0 + t < L) ? dt : 0.f;  // padded steps leave the state unchanged
+                    if (STATES) dsum += dt;
                     dtx[c * kDtxS + dtx_col(t)] = make_float2(dt, dt * xv[i]);
                 }
             }
@@ -275,8 +307,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                     const float2 c1v = make_float2(__uint_as_float(r[6]), __uint_as_float(r[7]));
                     hp[0] = fma2(zz_c[j][0], hp[0], mul2(dx2, b0));
                     hp[1] = fma2(zz_c[j][1], hp[1], mul2(dx2, b1));
-                    const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
-                    part[4 * g4 + j] = acc.x + acc.y;
+                    if (!STATES) {
+                        const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
+                        part[4 * g4 + j] = acc.x + acc.y;
+                    }
                 }
                 if (g4 < 7) tc::tmem_wait();
                 if (grp < 15) {
@@ -289,6 +323,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 }
             }
 
+            if (STATES) continue;
             // (4) reduce-scatter of this half across the channel's 4 threads (the kept half
             // moves to the front): thread gi ends with steps 32 hh + 8 gi .. + 7
 #pragma unroll
@@ -323,7 +358,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         if (tid == 0 && k + kStages < ntiles) issue(k + kStages);
     }
 
-    if (active && a.h_final) {
+    if (STATES) {
+        // the channel's sum of Delta over the segment, from its 4 threads
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
+        if (active) {
+            const size_t rows = static_cast<size_t>(a.batch) * a.dim;
+            float* hs = seg_state + (seg * rows + ch) * kN;
+#pragma unroll
+            for (int k = 0; k < kNS / 2; ++k) {
+                hs[gi + kTPC * (2 * k)] = hp[k].x;
+                hs[gi + kTPC * (2 * k + 1)] = hp[k].y;
+            }
+            if (gi == 0) seg_dsum[seg * rows + ch] = dsum;
+        }
+    } else if (active && a.h_final && seg == nseg - 1) {
 #pragma unroll
         for (int k = 0; k < kNS / 2; ++k) {
             a.h_final[static_cast<size_t>(ch) * kN + gi + kTPC * (2 * k)] = hp[k].x;
@@ -362,7 +411,24 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     if (cps < 1) cps = 1;
     if (cps > per_group) cps = per_group;
     while ((per_group + cps - 1) / cps * kTPC > kMaxThreads) ++cps;
-    const int cpb = (per_group + cps - 1) / cps;
+    int cpb = (per_group + cps - 1) / cps;
+    // Long sequences with few channels per SM: split the sequence into segments so that
+    // every CTA holds a full channel group (more warps per SM), at the cost of a segment
+    // pass over all but the last segment.
+    const int ntiles = (a.seqlen + kT - 1) / kT;
+    int segs = 1;
+    if (cpb < 48 && ntiles >= 16 && !env_int("SSM_M1_NO_SPLIT", 0)) {
+        const int cps_full = (per_group + kMaxThreads / kTPC - 1) / (kMaxThreads / kTPC);
+        int S = sms / (pairs * cps_full);
+        if (S > ntiles / 4) S = ntiles / 4;  // at least 4 tiles per segment
+        if (S >= 2) {
+            cps = cps_full;
+            cpb = (per_group + cps - 1) / cps;
+            segs = S;
+        }
+    }
+    const int tps = (ntiles + segs - 1) / segs;
+    segs = (ntiles + tps - 1) / tps;  // no empty segment
     size_t smem = static_cast<size_t>(Layout(cpb).total) + 1024;
     if (smem > static_cast<size_t>(max_smem)) return cudaSuccess;
     // one CTA per SM: it allocates all 512 TMEM columns
@@ -370,14 +436,20 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     if (smem < one_per_sm) smem = one_per_sm;
     plan->kind = M1Plan::kTmem;
     plan->tpc = kTPC;
-    plan->grid = pairs * cps;
+    plan->grid = pairs * cps * segs;
     plan->cpb_max = cpb;
     plan->smem = smem;
     plan->cps = cps;
+    plan->segs = segs;
+    plan->tps = tps;
+    // segment end states [segs-1][batch*dim][16] and sums of Delta [segs-1][batch*dim]
+    const size_t rows = static_cast<size_t>(a.batch) * a.dim;
+    plan->ws_state = (static_cast<size_t>(segs - 1) * rows * kN * sizeof(float) + 255) / 256 * 256;
+    plan->ws_bytes = plan->ws_state + (static_cast<size_t>(segs - 1) * rows * sizeof(float) + 255) / 256 * 256;
     return cudaSuccess;
 }
 
-cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, cudaStream_t s) {
+cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspace, cudaStream_t s) {
     M1Args a = a_in;
     a.cpb_max = plan.cpb_max;
     const Layout lay(plan.cpb_max);
@@ -392,20 +464,22 @@ cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, cudaStream_t 
     if ((e = encode_tmap_2d(&maps.b, a.B, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
     if ((e = encode_tmap_2d(&maps.c, a.C, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
     const int threads = round_up(plan.cpb_max * kTPC, 32);
-    if (a.out_dtype == SSM_BF16) {
-        auto k = m1_scan_tmem<bf16_t>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem))) !=
-            cudaSuccess)
-            return e;
-        k<<<plan.grid, threads, plan.smem, s>>>(maps, a, plan.cps);
-    } else {
-        auto k = m1_scan_tmem<float>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan.smem))) !=
-            cudaSuccess)
-            return e;
-        k<<<plan.grid, threads, plan.smem, s>>>(maps, a, plan.cps);
+    float* seg_state = static_cast<float*>(workspace);
+    float* seg_dsum = plan.segs > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.ws_state)
+                                    : nullptr;
+    const int ctas = plan.grid / plan.segs;  // CTAs per segment
+    auto run = [&](auto kern, int grid) -> cudaError_t {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(plan.smem));
+        if (err != cudaSuccess) return err;
+        kern<<<grid, threads, plan.smem, s>>>(maps, a, plan.cps, plan.segs, plan.tps, seg_state, seg_dsum);
+        return cudaGetLastError();
+    };
+    if (plan.segs > 1) {  // segment pass (outputs unused: instantiated for bf16 only)
+        if ((e = run(m1_scan_tmem<bf16_t, true>, ctas * (plan.segs - 1))) != cudaSuccess) return e;
     }
-    return cudaGetLastError();
+    return a.out_dtype == SSM_BF16 ? run(m1_scan_tmem<bf16_t, false>, plan.grid)
+                                   : run(m1_scan_tmem<float, false>, plan.grid);
 }
 
 unsigned int m1_tmem_wait_timeouts() {
