@@ -92,7 +92,7 @@ constexpr uint32_t kTxMain = 40960 + kArrBytes;
 // cuts launch: each cut is split into kCutParts parts (separate CTAs), each with a ring
 // of kCStages stages of x, B and the step quantities and two F buffers
 constexpr int kCutParts = 1;
-constexpr int kCStages = 4;
+constexpr int kCStages = 7;
 constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
 constexpr int kCOffF = kCStages * kCStBytes;  // 2 x (F_hi, F_lo) = 2 x 16 KB
 constexpr int kCOffBar = kCOffF + 2 * 16384;

@@ -190,6 +190,22 @@ def test_790m_long_context_sampled(oracle_mod, L):
     check(np.stack([hf[b, d] for b, d in rows]), hr, TOL_BF16, what="h_final sampled")
 
 
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_time_split_many_segments(oracle_mod, out):
+    """One batch row with few channels and a long sequence: the bf16 path splits the
+    sequence into many time segments (a segment pass, then each segment starts from h0
+    carried through the earlier ones).  Gate, initial state, non-uniform A, every channel
+    checked, ragged length."""
+    inp = synth.mamba1(1, 256, 16, 4096 - 64 + 16, dtype=synth.BF16, with_z=True,
+                       with_h0=True, seed=11)
+    inp.arrays["A"] = -np.exp(np.random.default_rng(12).uniform(-1.0, 2.5, (256, 16))
+                              ).astype(np.float32)
+    y, hf = run_gpu(inp, out_dtype=out)
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, out_bf16=(out == "bf16"), what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
 def test_zz_no_device_wait_gave_up():
     """Every bounded wait in the kernels above completed (timeout counter still zero)."""
     assert ssm.wait_timeouts() == 0
