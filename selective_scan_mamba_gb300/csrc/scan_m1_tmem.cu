@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         for (int j = tid; j < 2 * 256; j += blockDim.x) {
             const int hh = j >> 8, row = j & 255;
             const int step = 32 * hh + (row >> 3), e = row & 7;
+            if (STATES && e >= 4) continue;  // the segment pass reads B only
             const unsigned char* tile = st + (e < 4 ? lay.b : lay.c);
             const int n0 = 4 * (e & 3);
             uint16_t v[4];
@@ -279,6 +280,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 }
             }
         };
+        if constexpr (STATES) {
+            // segment pass: states only (no C, no outputs); one TMEM buffer, the group's
+            // decays computed while its load is in flight
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                mbar_wait(&mmab[hh], k & 1);
+                tc::fence_after();
+#pragma unroll 2
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    uint32_t r[32];
+                    tc::tmem_ld32_async(tl + 256 * hh + 32 * g4, r);
+                    float2 ddv[4], zz[4][kNS / 2];
+                    decays(8 * hh + g4, ddv, zz);
+                    tc::tmem_wait();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 dx2 = make_float2(ddv[j].y, ddv[j].y);
+                        const uint32_t* rr = r + 8 * j;
+                        hp[0] = fma2(zz[j][0], hp[0], mul2(dx2, make_float2(__uint_as_float(rr[0]), __uint_as_float(rr[1]))));
+                        hp[1] = fma2(zz[j][1], hp[1], mul2(dx2, make_float2(__uint_as_float(rr[2]), __uint_as_float(rr[3]))));
+                    }
+                }
+            }
+        } else {
         float2 ddv_c[4], zz_c[4][kNS / 2];
         decays(0, ddv_c, zz_c);
 #pragma unroll
@@ -307,10 +332,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                     const float2 c1v = make_float2(__uint_as_float(r[6]), __uint_as_float(r[7]));
                     hp[0] = fma2(zz_c[j][0], hp[0], mul2(dx2, b0));
                     hp[1] = fma2(zz_c[j][1], hp[1], mul2(dx2, b1));
-                    if (!STATES) {
-                        const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
-                        part[4 * g4 + j] = acc.x + acc.y;
-                    }
+                    const float2 acc = fma2(c1v, hp[1], mul2(c0v, hp[0]));
+                    part[4 * g4 + j] = acc.x + acc.y;
                 }
                 if (g4 < 7) tc::tmem_wait();
                 if (grp < 15) {
@@ -323,7 +346,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 }
             }
 
-            if (STATES) continue;
             // (4) reduce-scatter of this half across the channel's 4 threads (the kept half
             // moves to the front): thread gi ends with steps 32 hh + 8 gi .. + 7
 #pragma unroll
@@ -353,6 +375,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 store_row<8>(yrow, yv, L - (t0 + te));
             }
         }
+        }  // not the segment pass
         tc::fence_before();
         __syncthreads();  // stage s, dtx, the B/C operands and TMEM are free again
         if (tid == 0 && k + kStages < ntiles) issue(k + kStages);
