@@ -90,13 +90,15 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr uint32_t kTxMain = 40960 + kArrBytes;
 
 // cuts launch: each cut is split into kCutParts parts (separate CTAs), each with a ring
-// of kCStages stages of x, B and the step quantities and two F buffers
+// of kCStages stages of x, B and the step quantities and kCF F buffers (the F builders
+// run up to kCF chunks ahead of the MMAs)
 constexpr int kCutParts = 1;
-constexpr int kCStages = 7;
+constexpr int kCStages = 6;
+constexpr int kCF = 4;
 constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
-constexpr int kCOffF = kCStages * kCStBytes;  // 2 x (F_hi, F_lo) = 2 x 16 KB
-constexpr int kCOffBar = kCOffF + 2 * 16384;
-constexpr int kCSmemBytes = kCOffBar + 128;
+constexpr int kCOffF = kCStages * kCStBytes;  // kCF x (F_hi, F_lo) = kCF x 16 KB
+constexpr int kCOffBar = kCOffF + kCF * 16384;
+constexpr int kCSmemBytes = kCOffBar + 192;
 constexpr int kCSmemAlloc = kCSmemBytes + 1024;
 constexpr uint32_t kTxCut = 24576 + kArrBytes;
 
@@ -224,9 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kCOffBar);  // [kCStages]
-    uint64_t* mma_bar = tma_bar + kCStages;                           // [2] MMA of step k done
-    uint64_t* done_bar = mma_bar + 2;                                 // [2] F of step k built
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(done_bar + 2);
+    uint64_t* mma_bar = tma_bar + kCStages;  // [kCF] MMA of step k done (k % kCF)
+    uint64_t* done_bar = mma_bar + kCF;      // [4] F of step k built (k % 4): builders stay
+                                             // within 3 steps of each other
+    uint64_t* free_bar = done_bar + 4;       // [kCStages] the stage's MMA done (its reuse)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(free_bar + kCStages);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -235,10 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&maps.x);
         prefetch_tmap(&maps.b);
         for (int s = 0; s < kCStages; ++s) mbar_init(&tma_bar[s], 1);
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(&mma_bar[j], 1);
-            mbar_init(&done_bar[j], kCompute);
-        }
+        for (int j = 0; j < kCF; ++j) mbar_init(&mma_bar[j], 1);
+        for (int j = 0; j < 4; ++j) mbar_init(&done_bar[j], kCompute);
+        for (int j = 0; j < kCStages; ++j) mbar_init(&free_bar[j], 1);
         mbar_fence_init();
     }
     tc::fence_before();
@@ -260,34 +263,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (lane == 0)
             for (int k = 0; k < kCStages && k < n; ++k) issue(k);
-        for (int k = 0; k < n; ++k) {
-            mbar_wait_warp(&done_bar[k & 1], (k >> 1) & 1);
-            // the stage of step k-2 is free: the compute warps saw its MMA complete
-            if (lane == 0 && k >= 2 && k + kCStages - 2 < n) issue(k + kCStages - 2);
-        }
+        // step j + kCStages reuses the stage of step j once the MMA of step j is done
+        // (its F was built before that MMA was issued)
+        if (lane == 0)
+            for (int j = 0; j + kCStages < n; ++j) {
+                mbar_wait(&free_bar[j % kCStages], (j / kCStages) & 1);
+                issue(j + kCStages);
+            }
     } else if (warp == kMmaWarp) {
         for (int k = 0; k < n; ++k) {
-            mbar_wait_warp(&done_bar[k & 1], (k >> 1) & 1);
+            mbar_wait_warp(&done_bar[k & 3], (k >> 2) & 1);
             mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);  // complete already
             tc::fence_after();
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
-            const uint32_t sf = smem_u32(sm + kCOffF + (k & 1) * 16384);
+            const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * 16384);
             // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts
             const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
             const uint64_t dB = tc::desc_sw128_mn(sbm, 8192), dF = tc::desc_sw128_mn(sf, 8192);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 tc::mma_bf16_warp(tmem, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4, (k > 0 || kk > 0) ? 1u : 0u);
-            tc::mma_commit_warp(&mma_bar[k & 1]);
+            tc::mma_commit_warp(&mma_bar[k % kCF]);
+            tc::mma_commit_warp(&free_bar[k % kCStages]);
             __syncwarp();
         }
     } else {
         const int fs = tid >> 3, fp = (tid & 7) * 8;  // F element (s, p..p+7)
         float tailf = 1.f;  // decay of the chunks already walked (later in time)
         for (int k = 0; k < n; ++k) {
-            if (k >= 2) {  // MMA of step k-2 done: its F buffer is free
-                mbar_wait_warp(&mma_bar[k & 1], ((k - 2) >> 1) & 1);
+            if (k >= kCF) {  // MMA of step k-kCF done: its F buffer is free
+                mbar_wait_warp(&mma_bar[k % kCF], (k / kCF - 1) & 1);
                 tc::fence_after();
             }
             mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);
@@ -302,14 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) v[e] *= f;
             uint4 hi, lo;
             split8(v, hi, lo);
-            unsigned char* F = sm + kCOffF + (k & 1) * 16384;
+            unsigned char* F = sm + kCOffF + (k % kCF) * 16384;
             *reinterpret_cast<uint4*>(F + chunk_off(fs, fp >> 3)) = hi;
             *reinterpret_cast<uint4*>(F + 8192 + chunk_off(fs, fp >> 3)) = lo;
             tc::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&done_bar[k & 1]);
+            if (lane == 0) mbar_arrive(&done_bar[k & 3]);
         }
-        mbar_wait_warp(&mma_bar[(n - 1) & 1], ((n - 1) >> 1) & 1);
+        mbar_wait_warp(&mma_bar[(n - 1) % kCF], ((n - 1) / kCF) & 1);
         tc::fence_after();
         const int q4 = warp & 3, cg = warp >> 2;
         const int hn = 32 * q4 + lane, hp = 16 * cg;
