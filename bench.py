@@ -413,7 +413,26 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                           "state_updates_per_s": Bt * H * P * N / tstep,
                           "hbm_gbs": sb / tstep / 1e9, "hbm_frac": sb / tstep / 1e9 / hbm,
                           "bytes_per_step": sb, "note": "4 layer states rotate (403 MB > L2)"}
-    del states, graph
+    del graph
+    # multi-token decode: T tokens per call, the state read and written once per call
+    tok_runs = {}
+    for T in (4, 16):
+        stk = {n: torch.stack([toks[k % 8][n] for k in range(T)]) for n in ("x", "dt", "B", "C", "z")}
+        yT = torch.empty((T, Bt, H, P), dtype=torch.bfloat16, device="cuda")
+
+        def gt(i, stk=stk, yT=yT):
+            ssm.ssm_state_update_tokens(states[i % 4], stk["x"], stk["dt"], par["A"], stk["B"],
+                                        stk["C"], D=par["D"], z=stk["z"], dt_bias=par["dt_bias"],
+                                        y=yT)
+        tcall = time_launches(torch, gt, 32, 4, stream)
+        tb = 2 * Bt * H * P * N * 4 + T * (step_bytes(Bt, H, P, N, G) - 2 * Bt * H * P * N * 4)
+        tok_runs[str(T)] = {"us_per_call": tcall * 1e6, "us_per_token": tcall * 1e6 / T,
+                            "state_updates_per_s": T * Bt * H * P * N / tcall,
+                            "hbm_gbs": tb / tcall / 1e9, "hbm_frac": tb / tcall / 1e9 / hbm,
+                            "bytes_per_call": tb}
+    out["decode_780m_tokens"] = dict(tok_runs, note="T consecutive tokens per call; 4 layer "
+                                     "states rotate (403 MB > L2)")
+    del states
     # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
     c3 = synth.WORKLOADS["m1_790m_long"]
     sweep = {}

@@ -226,6 +226,20 @@ typedef struct {
 
 ssm_status ssm_state_update(const ssm_step_params* p, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Multi-token decode: `ntokens` consecutive steps of ssm_state_update in one call
+ *   (the pages' incremental step() applied T times; 03/System)
+ *
+ * The state is read once, advanced through the T tokens in registers and written
+ * once, so the HBM traffic per token falls from the whole state to the token data.
+ * Token-major layouts, each token's slice laid out as in ssm_state_update:
+ *   x, z, y : [T, Bt, H, P];   dt : [T, Bt, H];   B, C : [T, Bt, G, N]
+ *   state, A, D_skip, dt_bias: as in ssm_state_update.
+ * y[t] is the output after token t.  Limits: 1 <= ntokens <= 256, otherwise as
+ * ssm_state_update.  ntokens = 1 equals ssm_state_update.
+ * ------------------------------------------------------------------------- */
+ssm_status ssm_state_update_tokens(const ssm_step_params* p, int ntokens, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* ssm_last_error(void);
 

@@ -19,7 +19,7 @@ import ctypes
 from . import _lib
 from ._lib import SsmError  # noqa: F401
 
-__all__ = ["wait_timeouts", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+__all__ = ["wait_timeouts", "ssm_state_update_tokens", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
            "ssd_chunk_scan_workspace_size", "SsmError", "lib"]
 
 
@@ -245,4 +245,42 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_sof
     p.y = _ptr(y, "y", (batch, H, P))
     p.disc = _disc(disc)
     _lib.check(lib().ssm_state_update(ctypes.byref(p), _stream(stream)))
+    return y
+
+
+def ssm_state_update_tokens(state, x, dt, A, B, C, D=None, z=None, dt_bias=None,
+                            dt_softplus=True, *, y=None, out_dtype=None, disc="exp_euler",
+                            stream=None):
+    """T consecutive decode steps in one call, updating ``state`` [batch, H, P, N] float32
+    in place (read and written once).
+
+    Token-major inputs: x, z: [T, batch, H, P]; dt: [T, batch, H]; B, C: [T, batch, G, N];
+    A: [H] or [H, N]; D, dt_bias: [H].  Returns y [T, batch, H, P] (output after each
+    token).
+    """
+    torch = _torch()
+    batch, H, P, N = state.shape
+    T = x.shape[0]
+    G = B.shape[2]
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    f32 = torch.float32
+    p = _lib.StepParams()
+    p.batch, p.nheads, p.headdim, p.dstate, p.ngroups = batch, H, P, N, G
+    p.a_per_state = 1 if A.dim() == 2 else 0
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(y)
+    p.state = _ptr(state, "state", (batch, H, P, N), f32)
+    p.x = _ptr(x, "x", (T, batch, H, P))
+    p.dt = _ptr(dt, "dt", (T, batch, H), x.dtype)
+    p.dt_bias = _ptr(dt_bias, "dt_bias", (H,), f32)
+    p.dt_softplus = int(bool(dt_softplus))
+    p.A = _ptr(A, "A", (H, N) if A.dim() == 2 else (H,), f32)
+    p.B = _ptr(B, "B", (T, batch, G, N), x.dtype)
+    p.C = _ptr(C, "C", (T, batch, G, N), x.dtype)
+    p.D_skip = _ptr(D, "D", (H,), f32)
+    p.z = _ptr(z, "z", (T, batch, H, P), x.dtype)
+    p.y = _ptr(y, "y", (T, batch, H, P))
+    p.disc = _disc(disc)
+    _lib.check(lib().ssm_state_update_tokens(ctypes.byref(p), int(T), _stream(stream)))
     return y

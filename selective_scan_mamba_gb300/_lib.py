@@ -53,8 +53,8 @@ class StepParams(ctypes.Structure):
 
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssd_chunk_scan_fwd",
-           "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_last_error",
-           "ssm_abi_version")
+           "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
+           "ssm_last_error", "ssm_abi_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +85,8 @@ def load(build_if_missing: bool = True):
             lib.ssd_chunk_scan_workspace_size.argtypes = [ctypes.POINTER(SsdParams)]
             lib.ssm_state_update.restype = _i
             lib.ssm_state_update.argtypes = [ctypes.POINTER(StepParams), _vp]
+            lib.ssm_state_update_tokens.restype = _i
+            lib.ssm_state_update_tokens.argtypes = [ctypes.POINTER(StepParams), _i, _vp]
             lib.ssm_last_error.restype = ctypes.c_char_p
             lib.ssm_last_error.argtypes = []
             lib.ssm_abi_version.restype = _i

@@ -318,10 +318,11 @@ ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t works
     return SSM_OK;
 }
 
-ssm_status ssm_state_update(const ssm_step_params* p, void* stream) {
+static ssm_status state_update(const ssm_step_params* p, int ntokens, void* stream) {
     g_err[0] = '\0';
     ssm_status st = check_step(p);
     if (st != SSM_OK) return st;
+    REQUIRE(ntokens >= 1 && ntokens <= 256, "ntokens=%d (1..256)", ntokens);
     if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
     ssm::StepArgs a;
     a.batch = p->batch;
@@ -344,9 +345,18 @@ ssm_status ssm_state_update(const ssm_step_params* p, void* stream) {
     a.z = p->z;
     a.y = p->y;
     a.disc = p->disc;
+    a.ntok = ntokens;
     cudaError_t e = ssm::step_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_state_update launch");
     return SSM_OK;
+}
+
+ssm_status ssm_state_update(const ssm_step_params* p, void* stream) {
+    return state_update(p, 1, stream);
+}
+
+ssm_status ssm_state_update_tokens(const ssm_step_params* p, int ntokens, void* stream) {
+    return state_update(p, ntokens, stream);
 }
 
 }  // extern "C"

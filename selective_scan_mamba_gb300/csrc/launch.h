@@ -82,6 +82,7 @@ struct StepArgs {
     const void* z;
     void* y;
     ssm_disc disc;
+    int ntok = 1;  // consecutive tokens (token-major x, dt, B, C, z, y)
 };
 cudaError_t step_launch(const StepArgs& a, cudaStream_t s);
 

@@ -128,6 +128,13 @@ def step_params(**kw):
     return p
 
 
+@pytest.mark.parametrize("ntokens", [0, -1, 257])
+def test_step_tokens_rejects_bad_count(lib, ntokens):
+    p = step_params()
+    assert lib.ssm_state_update_tokens(ctypes.byref(p), ntokens, None) == _lib.SSM_ERR_INVALID_ARG
+    assert "ntokens" in lib.ssm_last_error().decode()
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("state", None, _lib.SSM_ERR_INVALID_ARG),
     ("a_per_state", 2, _lib.SSM_ERR_INVALID_ARG),

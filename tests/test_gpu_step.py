@@ -95,3 +95,66 @@ def test_780m_full_size_every_step_sampled(oracle_mod):
     cfg = synth.WORKLOADS["step_780m"]
     _steps(oracle_mod, cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"],
            cfg["ngroups"], cfg["steps"], cfg["dtype"], rows=[0, 37])
+
+
+def _tokens(oracle, batch, H, P, N, G, T, dtype, a_per_state=False, disc="exp_euler", seed=3,
+            calls=2):
+    """`calls` consecutive ssm_state_update_tokens calls of T tokens each (token-major
+    stacks of step_tokens) against T oracle steps each."""
+    import torch
+    par = synth.step_params(H, N, a_per_state=a_per_state, seed=seed)
+    tp = to_device(par)
+    st0 = synth.step_state(batch, H, P, N, seed=seed)
+    state = torch.from_numpy(st0).cuda()
+    ref_state = st0.astype(np.float64)
+    fp = par.f64
+    tol = TOL_F32 if dtype == synth.F32 else TOL_BF16
+    for call in range(calls):
+        toks = [synth.step_tokens(batch, H, P, N, G, step=call * T + k, dtype=dtype, seed=seed)
+                for k in range(T)]
+        stack = {n: np.stack([tk.arrays[n] for tk in toks]) for n in ("x", "dt", "B", "C", "z")}
+        if dtype == synth.BF16:  # exact bf16 values, as in tests.helpers.to_device
+            dev = {n: torch.from_numpy(synth.bf16_bits(v).view(np.int16).copy()).cuda()
+                   .view(torch.bfloat16) for n, v in stack.items()}
+        else:
+            dev = {n: torch.from_numpy(np.ascontiguousarray(v, np.float32)).cuda()
+                   for n, v in stack.items()}
+        y = ssm.ssm_state_update_tokens(state, dev["x"], dev["dt"], tp["A"], dev["B"], dev["C"],
+                                        D=tp["D"], z=dev["z"], dt_bias=tp["dt_bias"], disc=disc,
+                                        out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        yg = to_numpy(y)
+        for k, tk in enumerate(toks):
+            f = tk.f64
+            yr, ref_state = oracle.state_update(ref_state, f("x"), f("dt"), fp("A"), f("B"), f("C"),
+                                                D=fp("D"), z=f("z"), dt_bias=fp("dt_bias"),
+                                                disc=1 if disc == "zoh" else 0)
+            check(yg[k], yr, tol, what=f"y call {call} token {k}")
+        check(to_numpy(state), ref_state, tol, what=f"state after call {call}")
+
+
+@pytest.mark.parametrize("T", [1, 4, 17])
+@pytest.mark.parametrize("N", [128, 16, 24])
+def test_tokens_mamba2_form(oracle_mod, T, N):
+    """Multi-token decode: T tokens per call, state read and written once, equal to T
+    single steps (vector path for N = 16 and 128, scalar path for N = 24)."""
+    _tokens(oracle_mod, 3, 6, 16, N, 2, T, synth.BF16)
+
+
+def test_tokens_fp32_zoh(oracle_mod):
+    _tokens(oracle_mod, 2, 4, 8, 64, 1, 5, synth.F32, disc="zoh")
+
+
+def test_tokens_mamba1_form_large_table(oracle_mod):
+    """Mamba-1 form (headdim 1, A [channels, N]) with many tokens: the per-token table
+    does not fit in shared memory and the step quantities are computed where used."""
+    _tokens(oracle_mod, 2, 96, 1, 16, 1, 64, synth.F32, a_per_state=True, calls=1)
+
+
+@pytest.mark.parametrize("N,P,T", [(256, 48, 40), (64, 64, 33), (128, 100, 9), (128, 64, 70),
+                                   (256, 40, 12), (64, 24, 10)])
+def test_tokens_register_kernel_shapes(oracle_mod, N, P, T):
+    """The register-resident multi-token kernel (N in 64/128/256): heads that do not
+    divide the CTA span (P = 40, 48, 100), CTAs whose rows cross a group, several staged
+    token blocks (T > block) and a ragged last token group."""
+    _tokens(oracle_mod, 2, 4, P, N, 2, T, synth.BF16, calls=1)
