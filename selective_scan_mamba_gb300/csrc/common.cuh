@@ -159,15 +159,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float softplus_accurate(float v) {
     return v > 20.f ? v : log1pf(expf(v));
 }
-// Fast variant for bfloat16 inputs: e = e^v by MUFU.EX2, then log1p(e) either by the
-// series e - e^2/2 + e^3/3 - e^4/4 (e < 2^-7, truncation below 2^-30 relative) or by
-// MUFU.LG2 of 1 + e (relative error below ~4e-5 there).
-// Branch-free, so that independent evaluations interleave.
+// Fast variant for bfloat16 inputs, by the identity softplus(v) = max(v, 0) +
+// log(1 + e^-|v|): MUFU.EX2 of -|v|, MUFU.LG2 of 1 + that, one FMA; no branches, so
+// independent evaluations interleave.  The absolute error is ~1e-7 (lg2.approx near 1
+// and the rounding of 1 + e^-|v|); where softplus(v) < 1e-6 (v < -14) the result may be
+// 0, which changes Delta, e^(Delta A) and Delta B x by less than 1e-6 absolute.
 __device__ __forceinline__ float softplus_fast(float v) {
-    const float e = ex2_approx(v * SSM_LOG2E);
-    const float series = e * (1.f - e * (0.5f - e * (0.33333334f - 0.25f * e)));
-    const float r = e < 0.0078125f ? series : lg2_approx(1.f + e) * SSM_LN2;
-    return v > 20.f ? v : r;
+    const float t = ex2_approx(-fabsf(v) * SSM_LOG2E);
+    return fmaf(lg2_approx(1.f + t), SSM_LN2, fmaxf(v, 0.f));
 }
 __device__ __forceinline__ float silu_accurate(float v) { return v / (1.f + expf(-v)); }
 __device__ __forceinline__ float silu_fast(float v) {

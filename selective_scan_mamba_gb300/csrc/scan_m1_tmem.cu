@@ -208,20 +208,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     const float Dd = a.D ? a.D[d] : 0.f;
     float dsum = 0.f;  // sum of Delta over the segment (segment pass)
 
-    for (int k = 0; k < ntiles; ++k) {
-        const int s = k % kStages;
-        const unsigned char* st = smem + s * lay.stage;
-        mbar_wait(&full[s], (k / kStages) & 1);
-        const int t0 = (k0 + k) * kT;
-        const int tb = gi * TO;
-
-        // (1) B/C operands of the broadcast MMA: row j = step * 8 + e of half hh holds, at
-        // K = 0..3, the value of state (K + 4 (e % 4)) of B (e < 4) or C (e >= 4)
+    // (1) B/C operands of the broadcast MMA for tile kk: row j = step * 8 + e of half hh
+    // holds, at K = 0..3, the value of state (K + 4 (e % 4)) of B (e < 4) or C (e >= 4).
+    // Built one tile ahead, before the barrier that ends the previous tile, so that the
+    // MMAs go out right after that barrier.
+    auto build_bop = [&](int kk) {
+        const unsigned char* stb = smem + (kk % kStages) * lay.stage;
+        mbar_wait(&full[kk % kStages], (kk / kStages) & 1);
         for (int j = tid; j < 2 * 256; j += blockDim.x) {
             const int hh = j >> 8, row = j & 255;
             const int step = 32 * hh + (row >> 3), e = row & 7;
             if (STATES && e >= 4) continue;  // the segment pass reads B only
-            const unsigned char* tile = st + (e < 4 ? lay.b : lay.c);
+            const unsigned char* tile = stb + (e < 4 ? lay.b : lay.c);
             const int n0 = 4 * (e & 3);
             uint16_t v[4];
 #pragma unroll
@@ -231,18 +229,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 make_uint2(v[0] | (static_cast<uint32_t>(v[1]) << 16), v[2] | (static_cast<uint32_t>(v[3]) << 16));
         }
         tc::fence_async_smem();
+    };
+    auto issue_mma = [&]() {
+        tc::fence_after();
+        const uint64_t ad = tc::desc_sw128(smem_u32(smem + lay.onehot));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            tc::mma_bf16(tmem + 256 * hh, ad, tc::desc_sw128(smem_u32(smem + lay.bop + hh * 256 * 128)),
+                         tc::idesc_bf16(128, 256), 0);
+            tc::mma_commit(&mmab[hh]);
+        }
+    };
+    if (ntiles > 0) {
+        build_bop(0);
         tc::fence_before();
         __syncthreads();
-        if (tid == 0) {
-            tc::fence_after();
-            const uint64_t ad = tc::desc_sw128(smem_u32(smem + lay.onehot));
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                tc::mma_bf16(tmem + 256 * hh, ad, tc::desc_sw128(smem_u32(smem + lay.bop + hh * 256 * 128)),
-                             tc::idesc_bf16(128, 256), 0);
-                tc::mma_commit(&mmab[hh]);
-            }
-        }
+        if (tid == 0) issue_mma();
+    }
+
+    for (int k = 0; k < ntiles; ++k) {
+        const int s = k % kStages;
+        const unsigned char* st = smem + s * lay.stage;
+        mbar_wait(&full[s], (k / kStages) & 1);
+        const int t0 = (k0 + k) * kT;
+        const int tb = gi * TO;
 
         // (2) (dt, dt*x) for this thread's steps of its channel
         if (active) {
@@ -262,7 +272,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 }
             }
         }
-        __syncthreads();
+        __syncwarp();  // dtx rows are channel-local and a channel's 4 threads share a warp
 
         // (3) recurrence, in two halves of 32 steps (one broadcast MMA each).  B/C of 4
         // steps per tcgen05.ld with the next group's load in flight; the decays of the
@@ -321,9 +331,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
                 uint32_t* nxt = (g4 & 1) ? ra : rb;
                 if (g4 < 7) tc::tmem_ld32_async(tl + 256 * hh + 32 * (g4 + 1), nxt);
                 float2 ddv_n[4], zz_n[4][kNS / 2];
-                if (grp < 15) decays(grp + 1, ddv_n, zz_n);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    if (grp < 15) {
+                        ddv_n[j] = drow[dtx_col(4 * (grp + 1) + j)];
+#pragma unroll
+                        for (int q = 0; q < kNS / 2; ++q) {
+                            const float2 e2 = mul2(make_float2(ddv_n[j].x, ddv_n[j].x), A2p[q]);
+                            zz_n[j][q] = make_float2(ex2_approx(e2.x), ex2_approx(e2.y));
+                        }
+                    }
                     const float2 dx2 = make_float2(ddv_c[j].y, ddv_c[j].y);
                     const uint32_t* r = cur + 8 * j;
                     const float2 b0 = make_float2(__uint_as_float(r[0]), __uint_as_float(r[1]));
@@ -376,9 +393,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
             }
         }
         }  // not the segment pass
+        // every thread has waited for both MMAs of tile k in (3): the operands are free
+        if (k + 1 < ntiles) build_bop(k + 1);
         tc::fence_before();
-        __syncthreads();  // stage s, dtx, the B/C operands and TMEM are free again
-        if (tid == 0 && k + kStages < ntiles) issue(k + kStages);
+        __syncthreads();  // stage s, dtx and TMEM are free again; tile k+1's operands are built
+        if (tid == 0) {
+            if (k + 1 < ntiles) issue_mma();
+            if (k + kStages < ntiles) issue(k + kStages);
+        }
     }
 
     if (STATES) {

@@ -82,6 +82,22 @@ def test_bf16_tiled_multi_cta_ragged(oracle_mod, monkeypatch, tpc, out):
     check(hf, hr, TOL_BF16, what="h_final")
 
 
+@pytest.mark.parametrize("path", ["tmem", "tma", "tiled"])
+def test_bf16_softplus_extremes(oracle_mod, monkeypatch, path):
+    """delta + bias spread over about +-40: softplus in its linear range (v > 20), near 0
+    and vanishing (v < -14, where the fast form may return 0), on each bf16 kernel."""
+    if path != "tmem":
+        monkeypatch.setenv("SSM_M1_NO_TMEM", "1")
+    if path == "tiled":
+        monkeypatch.setenv("SSM_M1_NO_TMA", "1")
+    inp = synth.mamba1(2, 96, 16, 200, dtype=synth.BF16, delta_scale=14.0, with_z=True,
+                       with_h0=True, seed=11)
+    y, hf = run_gpu(inp, out_dtype="f32")
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
 @pytest.mark.parametrize("tpc", ["2", "4"])
 def test_fp32_tiled_with_gate_and_groups(oracle_mod, monkeypatch, tpc):
     monkeypatch.setenv("SSM_M1_TPC", tpc)
