@@ -78,6 +78,23 @@ def ssd_flops(batch, L, H, P, N, G, Q):
     return batch * nch * (H * per_bhc + G * per_bgc)
 
 
+# The Mamba-1 update h = exp(Delta A) h + (Delta x) B, y += C h needs at least one
+# exponential (MUFU.EX2) and four FP32 FMA-pipe operations (Delta A, (Delta x) B, the state
+# FMA, the C h FMA).  A GB300 SM retires 32 EX2 and 128 FP32 FMA lanes per clock (measured
+# by selective_scan_mamba_gb300/tools/alu_probe.cu; the f32x2 forms save issue slots, not
+# FP32 lanes), so both units cap the scan at 32 updates per SM clock.  At 1.99 updates per
+# algorithmic byte (130m layer) that is ~75% of the HBM copy bandwidth: the scan is bound
+# by arithmetic, not by HBM.
+EX2_PER_CLK_SM = 32
+FP32_LANES_PER_CLK_SM = 128
+FP32_OPS_PER_UPDATE = 4
+
+
+def alu_peak_updates(sms, sm_max_mhz):
+    per_clk = min(EX2_PER_CLK_SM / 1.0, FP32_LANES_PER_CLK_SM / FP32_OPS_PER_UPDATE)
+    return sms * sm_max_mhz * 1e6 * per_clk
+
+
 def step_bytes(batch, H, P, N, G, es=2, with_z=True):
     b = 2 * batch * H * P * N * 4  # state read + write
     b += batch * H * P * es * (2 + (1 if with_z else 0))  # x, z, y
@@ -246,6 +263,9 @@ def bench_ours(args, rank, world):
         t_step = float(tt.item())
     updates = Bt * L * D * N
     value = updates * world / t_step
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = clocks.get("sm_max_mhz") or 2070.0
+    alu_peak = alu_peak_updates(sms, sm_max)
     gbs = set_bytes / t_step / 1e9
 
     # end to end through the public API with host buffers: pinned inputs copied in,
@@ -287,10 +307,17 @@ def bench_ours(args, rank, world):
                    "parallelism": f"replicas x{world} (independent batches per GPU)"},
         "hbm_gbs": gbs,
         "hbm_frac": gbs / peaks["hbm_gbs"],
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("m1_scan_tmem"),
-                     "kernel": "m1_scan_tmem", "bytes_per_launch": set_bytes,
-                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)"},
+        "roofline": {"bound": "alu", "achieved": updates / t_step / 1e9, "peak": alu_peak / 1e9,
+                     "unit": "Gupd/s", "frac": updates / t_step / alu_peak,
+                     "traffic": recorded_traffic("m1_scan_tmem"),
+                     "kernel": "m1_scan_tmem", "updates_per_launch": updates,
+                     "bytes_per_launch": set_bytes,
+                     "peak_source": f"derived: {sms} SMs x {sm_max:.0f} MHz x 32 updates/clk/SM "
+                                    "(1 MUFU.EX2 + 4 FP32 FMA-pipe ops per update; 32 EX2 and "
+                                    "128 FP32 lanes per clk per SM)",
+                     "hbm": {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"],
+                             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}},
         "e2e": {"value": updates * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": args.steps,
@@ -308,7 +335,7 @@ def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
     current kernel source; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
-    src = _source_digest()
+    src = _source_digest(kernel)
     try:
         with open(path) as fh:
             for line in fh:
@@ -320,14 +347,23 @@ def recorded_traffic(kernel):
     return None
 
 
-def _source_digest():
+# the sources each recorded kernel is built from (its unit and the headers it includes)
+KERNEL_SOURCES = {
+    "m1_scan_tmem": ("scan_m1_tmem.cu", "common.cuh", "launch.h", "tcgen05.cuh", "tma.cuh",
+                     "ssmscan.h"),
+}
+
+
+def _source_digest(kernel="m1_scan_tmem"):
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "selective_scan_mamba_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + fh.read())
+    pkg = os.path.join(ROOT, "selective_scan_mamba_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        path = os.path.join(pkg, name)
+        if not os.path.exists(path):
+            path = os.path.join(ROOT, "include", name)
+        with open(path, "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -571,6 +607,18 @@ def run_case(args):
         for i in range(n):
             ssm.ssm_state_update(states[i % 4], tok["x"], tok["dt"], par["A"], tok["B"], tok["C"],
                                  D=par["D"], z=tok["z"], dt_bias=par["dt_bias"], y=y)
+    elif args.case == "tokens":  # 16 decode tokens per call, one state buffer
+        c5 = synth.WORKLOADS["step_780m"]
+        Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
+        T = 16
+        par = _dev(synth.step_params(H, N, seed=0), torch)
+        state = torch.from_numpy(synth.step_state(Bt, H, P, N, seed=0)).cuda()
+        toks = [_dev(synth.step_tokens(Bt, H, P, N, G, step=k, seed=0), torch) for k in range(T)]
+        stk = {n: torch.stack([tk[n] for tk in toks]) for n in ("x", "dt", "B", "C", "z")}
+        y = torch.empty((T, Bt, H, P), dtype=torch.bfloat16, device="cuda")
+        for _ in range(n):
+            ssm.ssm_state_update_tokens(state, stk["x"], stk["dt"], par["A"], stk["B"], stk["C"],
+                                        D=par["D"], z=stk["z"], dt_bias=par["dt_bias"], y=y)
     else:
         raise SystemExit(f"unknown case {args.case}")
     torch.cuda.synchronize()
@@ -587,7 +635,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the SSD, decode and long-context measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step"],
+    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:

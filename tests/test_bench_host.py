@@ -1,0 +1,42 @@
+"""Host-side logic of bench.py (no GPU): byte and roofline accounting, recorded traffic."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_alu_peak_is_32_updates_per_sm_clock():
+    # 152 SMs at 2070 MHz, 32 updates per SM clock
+    assert bench.alu_peak_updates(152, 2070.0) == pytest.approx(152 * 2070e6 * 32)
+    # the exponential unit and the FP32 lanes give the same cap for this update
+    assert bench.EX2_PER_CLK_SM == bench.FP32_LANES_PER_CLK_SM / bench.FP32_OPS_PER_UPDATE
+
+
+def test_m1_bytes_130m_layer():
+    # x, delta, z in and y out (bf16) per (b, d, t); B and C per (b, t, n); A, D, bias
+    b = bench.m1_bytes(8, 1536, 16, 2048)
+    assert b == 8 * 1536 * 2048 * 8 + 2 * 8 * 16 * 2048 * 2 + 1536 * 16 * 4 + 1536 * 8
+
+
+def test_step_bytes_780m():
+    b = bench.step_bytes(64, 48, 64, 128, 1)
+    assert b == 2 * 64 * 48 * 64 * 128 * 4 + 64 * 48 * 64 * 2 * 3 + 64 * 48 * 2 + 2 * 64 * 128 * 2
+
+
+def test_recorded_traffic_needs_matching_digest(tmp_path, monkeypatch):
+    digest = bench._source_digest("m1_scan_tmem")
+    assert len(digest) == 16
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.txt").write_text(f"# header\nm1_scan_tmem 123456 {digest}\n"
+                                      "m1_scan_tmem 999 0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the digest is taken from the sources under ROOT: point it back at the repo for them
+    monkeypatch.setattr(bench, "_source_digest", lambda kernel="m1_scan_tmem": digest)
+    assert bench.recorded_traffic("m1_scan_tmem") == 123456.0
+    (prof / "traffic.txt").write_text("m1_scan_tmem 999 0000000000000000\n")
+    assert bench.recorded_traffic("m1_scan_tmem") is None
