@@ -56,6 +56,8 @@ def _bind(path):
     lib.oracle_softplus.argtypes = [ctypes.c_double]
     lib.oracle_phi1.restype = ctypes.c_double
     lib.oracle_phi1.argtypes = [ctypes.c_double]
+    lib.oracle_mamba1_scan_bwd.restype = i
+    lib.oracle_mamba1_scan_bwd.argtypes = [i, i, i, i, i] + [dp] * 3 + [i] + [dp] * 17
     lib.oracle_mamba1_scan.restype = i
     lib.oracle_mamba1_scan.argtypes = [i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp, dp, i,
                                        dp, dp]
@@ -155,6 +157,46 @@ def mamba1_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
     if rc:
         raise ValueError("oracle_mamba1_scan: invalid arguments")
     return y, hf
+
+
+def mamba1_scan_bwd(x, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
+                    delta_softplus=True, h0=None, dh_final=None):
+    """Gradients of sum(dy * y) + sum(dh_final * h_final) for mamba1_scan
+    (exponential-Euler).  Shapes as mamba1_scan with B, C [batch, G, N, L].  Returns a
+    dict with dx, ddelta, dA, dB, dC and, for the inputs given, dD, dz, ddelta_bias,
+    dh0 (dh0 always)."""
+    x = _f64(x)
+    batch, dim, L = x.shape
+    A = _f64(A)
+    N = A.shape[1]
+    B = _f64(B)
+    G = B.shape[1]
+    B = _f64(B, (batch, G, N, L))
+    C = _f64(C, (batch, G, N, L))
+    delta = _f64(delta, (batch, dim, L))
+    dy = _f64(dy, (batch, dim, L))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim, L))
+    delta_bias = _f64(delta_bias, (dim,))
+    h0 = _f64(h0, (batch, dim, N))
+    dh_final = _f64(dh_final, (batch, dim, N))
+    out = {"dx": np.empty((batch, dim, L)), "ddelta": np.empty((batch, dim, L)),
+           "dA": np.empty((dim, N)), "dB": np.empty((batch, G, N, L)),
+           "dC": np.empty((batch, G, N, L)), "dh0": np.empty((batch, dim, N))}
+    if D is not None:
+        out["dD"] = np.empty(dim)
+    if z is not None:
+        out["dz"] = np.empty((batch, dim, L))
+    if delta_bias is not None:
+        out["ddelta_bias"] = np.empty(dim)
+    rc = _load().oracle_mamba1_scan_bwd(
+        batch, dim, N, L, G, _p(x), _p(delta), _p(delta_bias), int(bool(delta_softplus)), _p(A),
+        _p(B), _p(C), _p(D), _p(z), _p(h0), _p(dy), _p(dh_final), _p(out["dx"]),
+        _p(out["ddelta"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]), _p(out.get("dD")),
+        _p(out.get("dz")), _p(out.get("ddelta_bias")), _p(out["dh0"]))
+    if rc:
+        raise ValueError("oracle_mamba1_scan_bwd: invalid arguments")
+    return out
 
 
 def _ssd_args(x, dt, A, B, C, D, z, dt_bias, h0):

@@ -121,6 +121,103 @@ int oracle_mamba1_scan(int batch, int dim, int dstate, int seqlen, int ngroups,
     return 0;
 }
 
+/* Reverse-mode derivative of oracle_mamba1_scan (exponential-Euler only): given
+ * dy [batch, dim, L] and dh_final [batch, dim, N] (nullable = zero), the gradients
+ * of  sum_t dy_t y_t + sum_n dh_final[n] h_final[n]  with respect to every input.
+ * The pages train every model with this scan inside ("From S4 to Mamba-3",
+ * 03/System: one shared trainer; 05/Evaluation: per-model training-step latency),
+ * so the derivative of the recurrence is part of the path; it is the chain rule
+ * applied to the forward definition above, walked backwards in time:
+ *   G_t[n]   = g[n] + do_t C_t[n]          (dL/dh_t; g carries the later steps)
+ *   dC_t[n] += do_t h_t[n],  dB_t[n] += G_t[n] Delta_t x_t
+ *   dx_t    += sum_n G_t[n] Delta_t B_t[n] (+ do_t D)
+ *   dDelta_t = sum_n G_t[n] (B_t[n] x_t + h_{t-1}[n] E_t[n] A[n]),  E_t = exp(Delta_t A)
+ *   dA[n]   += G_t[n] h_{t-1}[n] E_t[n] Delta_t,   g[n] = G_t[n] E_t[n]
+ * with do_t = dy_t SiLU(z_t), dz_t = dy_t o_t SiLU'(z_t) where o_t is the pre-gate
+ * output, d(delta)_t = dDelta_t sigmoid(delta_t + bias) under softplus, and
+ * dh0 = g after step 0.  dA, dD and dbias are summed over the batch; dB and dC over
+ * the channels of a group.  Gradient pointers for absent inputs may be NULL. */
+int oracle_mamba1_scan_bwd(int batch, int dim, int dstate, int seqlen, int ngroups,
+                           const double* x, const double* delta, const double* delta_bias,
+                           int delta_softplus, const double* A, const double* B,
+                           const double* C, const double* Dskip, const double* z,
+                           const double* h0, const double* dy, const double* dh_final,
+                           double* dx, double* ddelta, double* dA, double* dB, double* dC,
+                           double* dD, double* dz, double* dbias, double* dh0) {
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0 || dim % ngroups)
+        return 1;
+    int per_group = dim / ngroups;
+    size_t L = (size_t)seqlen, N = (size_t)dstate;
+    memset(dA, 0, sizeof(double) * (size_t)dim * N);
+    memset(dB, 0, sizeof(double) * (size_t)batch * ngroups * N * L);
+    memset(dC, 0, sizeof(double) * (size_t)batch * ngroups * N * L);
+    if (dD) memset(dD, 0, sizeof(double) * (size_t)dim);
+    if (dbias) memset(dbias, 0, sizeof(double) * (size_t)dim);
+    double* hs = (double*)malloc(sizeof(double) * (L + 1) * N);  /* h_{t-1} for t = 0..L */
+    double* o = (double*)malloc(sizeof(double) * (L ? L : 1));
+    double* g = (double*)malloc(sizeof(double) * N);
+    for (int b = 0; b < batch; ++b) {
+        for (int d = 0; d < dim; ++d) {
+            int gr = d / per_group;
+            size_t row = ((size_t)b * dim + d) * L;
+            /* forward again, keeping every state and the pre-gate output */
+            for (size_t n = 0; n < N; ++n) hs[n] = h0 ? h0[((size_t)b * dim + d) * N + n] : 0.0;
+            for (size_t t = 0; t < L; ++t) {
+                double dt = step_delta(delta[row + t], delta_bias, d, delta_softplus);
+                double acc = 0.0;
+                for (size_t n = 0; n < N; ++n) {
+                    size_t bc = (((size_t)b * ngroups + gr) * N + n) * L + t;
+                    double a = A[(size_t)d * N + n];
+                    hs[(t + 1) * N + n] = exp(dt * a) * hs[t * N + n] + dt * B[bc] * x[row + t];
+                    acc += C[bc] * hs[(t + 1) * N + n];
+                }
+                if (Dskip) acc += Dskip[d] * x[row + t];
+                o[t] = acc;
+            }
+            /* backwards in time */
+            for (size_t n = 0; n < N; ++n) g[n] = dh_final ? dh_final[((size_t)b * dim + d) * N + n] : 0.0;
+            for (size_t tt = L; tt-- > 0;) {
+                double v = delta[row + tt] + (delta_bias ? delta_bias[d] : 0.0);
+                double dt = delta_softplus ? oracle_softplus(v) : v;
+                double xt = x[row + tt];
+                double dout = dy[row + tt];
+                if (z) {
+                    double zt = z[row + tt];
+                    double sg = 1.0 / (1.0 + exp(-zt));
+                    dz[row + tt] = dy[row + tt] * o[tt] * sg * (1.0 + zt * (1.0 - sg));
+                    dout = dy[row + tt] * silu(zt);
+                }
+                double dxt = Dskip ? dout * Dskip[d] : 0.0;
+                if (dD) dD[d] += dout * xt;
+                double ddt = 0.0;
+                for (size_t n = 0; n < N; ++n) {
+                    size_t bc = (((size_t)b * ngroups + gr) * N + n) * L + tt;
+                    double a = A[(size_t)d * N + n];
+                    double E = exp(dt * a);
+                    double Gt = g[n] + dout * C[bc];
+                    double hprev = hs[tt * N + n];
+                    dC[bc] += dout * hs[(tt + 1) * N + n];
+                    dB[bc] += Gt * dt * xt;
+                    dxt += Gt * dt * B[bc];
+                    ddt += Gt * (B[bc] * xt + hprev * E * a);
+                    dA[(size_t)d * N + n] += Gt * hprev * E * dt;
+                    g[n] = Gt * E;
+                }
+                dx[row + tt] = dxt;
+                double dv = delta_softplus ? ddt / (1.0 + exp(-v)) : ddt;
+                ddelta[row + tt] = dv;
+                if (dbias) dbias[d] += dv;
+            }
+            if (dh0)
+                for (size_t n = 0; n < N; ++n) dh0[((size_t)b * dim + d) * N + n] = g[n];
+        }
+    }
+    free(hs);
+    free(o);
+    free(g);
+    return 0;
+}
+
 /* Mamba-2 sequential scan, the reference the pages test the chunked form
  * against ("From S4 to Mamba-3", 03/System, mamba2_minimal.py): scalar A per
  * head, state h[p, n] per (batch, head):

@@ -32,6 +32,12 @@ MUTATIONS = [
     ("ssd_seq_B_index", "acc += Ct[n] * *hp;", "acc += Bt[n] * *hp;"),
     ("step_zoh_ignored", "hrow[n] = exp(d_t * a) * hrow[n] + input_weight(d_t, a, disc) * x[xi] * Bb[n];",
      "hrow[n] = exp(d_t * a) * hrow[n] + d_t * x[xi] * Bb[n];"),
+    ("bwd_carry_decay_dropped", "g[n] = Gt * E;", "g[n] = Gt;"),
+    ("bwd_dA_missing_delta", "dA[(size_t)d * N + n] += Gt * hprev * E * dt;",
+     "dA[(size_t)d * N + n] += Gt * hprev * E;"),
+    ("bwd_gate_derivative_sign", "(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
+    ("bwd_dC_uses_prev_state", "dC[bc] += dout * hs[(tt + 1) * N + n];", "dC[bc] += dout * hs[tt * N + n];"),
+    ("bwd_softplus_derivative", "ddt / (1.0 + exp(-v))", "ddt / (1.0 + exp(v))"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
 ]
@@ -50,6 +56,8 @@ PIN_CHECKS = [
     lambda o: pins.test_mamba1_decode_equals_scan(o),
     lambda o: pins.test_ssd_decode_equals_scan(o, False),
     lambda o: pins.test_ssd_decode_equals_scan(o, True),
+    lambda o: pins.check_mamba1_bwd_fd(o),
+    lambda o: pins.test_mamba1_bwd_one_step_closed_form(o),
 ]
 
 

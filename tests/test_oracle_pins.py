@@ -439,3 +439,91 @@ def test_golden_fixture_unchanged(oracle_mod):
     now = make_golden.compute(oracle_mod)
     for key, vals in stored["values"].items():
         assert rel_err(np.array(now[key]), np.array(vals)) < 1e-15, key
+
+
+# ----------------------------------------------------------------------------------------
+# Mamba-1 backward: the oracle's gradients against central finite differences of the
+# (separately pinned) forward oracle, one random direction per input
+# ----------------------------------------------------------------------------------------
+def _bwd_inputs(seed, gated, skip, bias, h0, batch=2, dim=4, N=3, L=7, G=2):
+    rng = np.random.default_rng(seed)
+    inp = {
+        "x": rng.standard_normal((batch, dim, L)),
+        "delta": 0.7 * rng.standard_normal((batch, dim, L)),
+        "A": -np.exp(0.5 * rng.standard_normal((dim, N))),
+        "B": rng.standard_normal((batch, G, N, L)),
+        "C": rng.standard_normal((batch, G, N, L)),
+        "D": rng.standard_normal(dim) if skip else None,
+        "z": rng.standard_normal((batch, dim, L)) if gated else None,
+        "delta_bias": 0.3 * rng.standard_normal(dim) if bias else None,
+        "h0": rng.standard_normal((batch, dim, N)) if h0 else None,
+    }
+    dy = rng.standard_normal((batch, dim, L))
+    dhf = rng.standard_normal((batch, dim, N))
+    return inp, dy, dhf
+
+
+GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+           "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
+
+
+@pytest.mark.parametrize("gated,skip,bias,h0,softplus", [
+    (True, True, True, True, True), (False, False, False, False, True),
+    (True, False, True, False, False), (False, True, False, True, False)])
+def test_mamba1_bwd_finite_differences(oracle_mod, gated, skip, bias, h0, softplus):
+    check_mamba1_bwd_fd(oracle_mod, gated, skip, bias, h0, softplus)
+
+
+def check_mamba1_bwd_fd(oracle_mod, gated=True, skip=True, bias=True, h0=True, softplus=True):
+    inp, dy, dhf = _bwd_inputs(5, gated, skip, bias, h0)
+    if not softplus:  # keep Delta positive without softplus
+        inp["delta"] = np.abs(inp["delta"]) + 0.05
+        if inp["delta_bias"] is not None:
+            inp["delta_bias"] = np.abs(inp["delta_bias"])
+
+    def loss(args):
+        y, hf = oracle_mod.mamba1_scan(**args, delta_softplus=softplus)
+        return float((dy * y).sum() + (dhf * hf).sum())
+
+    grads = oracle_mod.mamba1_scan_bwd(**inp, dy=dy, dh_final=dhf, delta_softplus=softplus)
+    rng = np.random.default_rng(7)
+    eps = 1e-6
+    for name, val in inp.items():
+        if val is None:
+            assert GRAD_OF[name] not in grads or name == "h0"
+            continue
+        v = rng.standard_normal(val.shape)
+        plus = dict(inp, **{name: val + eps * v})
+        minus = dict(inp, **{name: val - eps * v})
+        fd = (loss(plus) - loss(minus)) / (2 * eps)
+        an = float((grads[GRAD_OF[name]] * v).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_mamba1_bwd_empty_sequence(oracle_mod):
+    """L = 0: h_final = h0, so dh0 = dh_final and every other gradient is empty or zero."""
+    inp, _, dhf = _bwd_inputs(6, True, True, True, True, L=0)
+    dy = np.zeros((2, 4, 0))
+    g = oracle_mod.mamba1_scan_bwd(**inp, dy=dy, dh_final=dhf)
+    assert np.array_equal(g["dh0"], dhf)
+    assert np.all(g["dA"] == 0) and np.all(g["dD"] == 0) and np.all(g["ddelta_bias"] == 0)
+
+
+def test_mamba1_bwd_one_step_closed_form(oracle_mod):
+    """L = 1, one channel, one state, no gate: y = C (e^{Delta a} h0 + Delta B x) + D x with
+    Delta = softplus(delta + bias); the derivatives written out by hand."""
+    x, dl, a, Bv, Cv, Dv, bias, h0 = 0.8, -0.3, -1.1, 0.6, -0.9, 0.4, 0.2, 1.5
+    v = dl + bias
+    Dt = math.log1p(math.exp(v))
+    sig = 1.0 / (1.0 + math.exp(-v))
+    E = math.exp(Dt * a)
+    inp = {"x": np.full((1, 1, 1), x), "delta": np.full((1, 1, 1), dl), "A": np.full((1, 1), a),
+           "B": np.full((1, 1, 1, 1), Bv), "C": np.full((1, 1, 1, 1), Cv), "D": np.array([Dv]),
+           "delta_bias": np.array([bias]), "h0": np.full((1, 1, 1), h0)}
+    g = oracle_mod.mamba1_scan_bwd(**inp, dy=np.ones((1, 1, 1)))
+    dDt = Cv * (Bv * x + h0 * E * a)
+    want = {"dx": Cv * Dt * Bv + Dv, "ddelta": dDt * sig, "ddelta_bias": dDt * sig,
+            "dA": Cv * h0 * E * Dt, "dB": Cv * Dt * x, "dC": E * h0 + Dt * Bv * x, "dD": x,
+            "dh0": Cv * E}
+    for k, w in want.items():
+        assert abs(float(np.ravel(g[k])[0]) - w) <= 1e-14 * max(1.0, abs(w)), (k, g[k], w)
