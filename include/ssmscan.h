@@ -113,6 +113,59 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Mamba-1 selective scan, backward: the reverse-mode derivative of ssm_scan_fwd
+ *   (the pages train every model through the scan: "From S4 to Mamba-3", 03/System,
+ *    the shared trainer; 05/Evaluation, per-model training-step latency)
+ *
+ * Given dy and dh_final, computes the gradients of
+ *     sum_t dy_t * y_t + sum_n dh_final[n] * h_final[n]
+ * with respect to every input of ssm_scan_fwd for the same `fwd` parameters (its y and
+ * h_final pointers are ignored).  Walking the recurrence backwards in time with
+ * g = dL/dh_t carried from later steps, E_t = exp(Delta_t A):
+ *   G_t = g + do_t C_t,  do_t = dy_t SiLU(z_t),  dz_t = dy_t o_t SiLU'(z_t)
+ *   dC_t += do_t h_t,  dB_t += G_t Delta_t x_t,  dx_t = sum_n G_t Delta_t B_t + do_t D
+ *   dDelta_t = sum_n G_t (B_t x_t + h_{t-1} E_t A),  dA += G_t h_{t-1} E_t Delta_t,
+ *   g <- G_t E_t,  d(delta)_t = dDelta_t sigmoid(delta_t + bias) under softplus,
+ * where o_t is the pre-gate output; dh0 = g after step 0.
+ *
+ * Shapes as ssm_scan_fwd; every gradient is float32 and is written (not accumulated):
+ *   dy          : [Bt, D, L]    fwd.out_dtype
+ *   dh_final    : [Bt, D, N]    float32 (nullable: zero)
+ *   dx, ddelta  : [Bt, D, L]
+ *   dz          : [Bt, D, L]    (required exactly when fwd.z is given)
+ *   dA          : [D, N]        (summed over the batch)
+ *   dB, dC      : [Bt, G, N, L] (summed over the channels of the group)
+ *   dD_skip     : [D]           (required exactly when fwd.D_skip is given)
+ *   ddelta_bias : [D]           (required exactly when fwd.delta_bias is given)
+ *   dh0         : [Bt, D, N]    (nullable: not written)
+ * Limits: exponential-Euler only and dstate in {16, 32, 64} (else SSM_ERR_UNSUPPORTED).
+ * The result does not depend on launch order (partial sums are added in a fixed order).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    ssm_scan_params fwd;
+    const void* dy;
+    const float* dh_final;
+    float* dx;
+    float* ddelta;
+    float* dz;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD_skip;
+    float* ddelta_bias;
+    float* dh0;
+} ssm_scan_bwd_params;
+
+/* Device scratch for ssm_scan_bwd, in bytes (0 when the problem is invalid or
+ * unsupported): per-chunk state checkpoints and per-CTA partial sums. */
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p);
+
+/* Runs the backward pass.  `workspace`: at least ssm_scan_bwd_workspace_size(p) bytes,
+ * 16-byte aligned; its contents on entry do not matter. */
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
  * Mamba-2 chunked SSD scan (scalar A per head)
  *   ("From S4 to Mamba-3", 03/System, mamba2_minimal.py; 04/Approach)
  *

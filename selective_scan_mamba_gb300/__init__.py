@@ -153,6 +153,70 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
     return (y, h_final) if return_final_state else y
 
 
+def ssm_scan_bwd(x, delta, A, B, C, dy, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 h0=None, dh_final=None, *, return_dh0=True, workspace=None, stream=None):
+    """Backward of ssm_scan_fwd (exponential-Euler, dstate 16, 32 or 64).
+
+    Same inputs as the forward plus dy [batch, dim, L] (bfloat16 or float32) and the
+    optional dh_final [batch, dim, N] float32.  Returns a dict of float32 gradients of
+    sum(dy * y) + sum(dh_final * h_final): dx, ddelta [batch, dim, L], dA [dim, N],
+    dB, dC [batch, G, N, L], and dD, dz, ddelta_bias for the inputs given, dh0
+    [batch, dim, N] when ``return_dh0``.
+    """
+    torch = _torch()
+    if B.dim() == 3:
+        B = B.unsqueeze(1)
+        C = C.unsqueeze(1)
+    batch, dim, L = x.shape
+    G, N = B.shape[1], B.shape[2]
+    f32, dev = torch.float32, x.device
+    p = _lib.ScanBwdParams()
+    # the forward parameters; y is ignored by the backward, dy fixes its dtype
+    p.fwd = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, dy, None,
+                         "exp_euler")
+    out = {"dx": torch.empty((batch, dim, L), dtype=f32, device=dev),
+           "ddelta": torch.empty((batch, dim, L), dtype=f32, device=dev),
+           "dA": torch.empty((dim, N), dtype=f32, device=dev),
+           "dB": torch.empty((batch, G, N, L), dtype=f32, device=dev),
+           "dC": torch.empty((batch, G, N, L), dtype=f32, device=dev)}
+    if D is not None:
+        out["dD"] = torch.empty((dim,), dtype=f32, device=dev)
+    if z is not None:
+        out["dz"] = torch.empty((batch, dim, L), dtype=f32, device=dev)
+    if delta_bias is not None:
+        out["ddelta_bias"] = torch.empty((dim,), dtype=f32, device=dev)
+    if return_dh0:
+        out["dh0"] = torch.empty((batch, dim, N), dtype=f32, device=dev)
+    p.dy = _ptr(dy, "dy", (batch, dim, L))
+    p.dh_final = _ptr(dh_final, "dh_final", (batch, dim, N), f32)
+    for name, field in (("dx", "dx"), ("ddelta", "ddelta"), ("dz", "dz"), ("dA", "dA"),
+                        ("dB", "dB"), ("dC", "dC"), ("dD", "dD_skip"),
+                        ("ddelta_bias", "ddelta_bias"), ("dh0", "dh0")):
+        setattr(p, field, _ptr(out.get(name), name))
+    need = int(lib().ssm_scan_bwd_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    _lib.check(lib().ssm_scan_bwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def ssm_scan_bwd_workspace_size(x, B, dy_dtype=None) -> int:
+    """Scratch bytes ssm_scan_bwd needs for these shapes (0 if unsupported)."""
+    p = _lib.ScanBwdParams()
+    if B.dim() == 3:
+        B = B.unsqueeze(1)
+    p.fwd.batch, p.fwd.dim, p.fwd.seqlen = x.shape
+    p.fwd.ngroups, p.fwd.dstate = B.shape[1], B.shape[2]
+    p.fwd.in_dtype = _dtype_code(x)
+    p.fwd.out_dtype = (_lib.SSM_F32 if dy_dtype is not None and dy_dtype == _torch().float32
+                       else _lib.SSM_BF16)
+    p.fwd.disc = 0
+    return int(lib().ssm_scan_bwd_workspace_size(ctypes.byref(p)))
+
+
 def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h_final, disc):
     torch = _torch()
     batch, L, H, P = x.shape

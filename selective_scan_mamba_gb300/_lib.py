@@ -36,6 +36,12 @@ class ScanParams(ctypes.Structure):
                 ("y", _vp), ("h_final", _fp), ("disc", _i)]
 
 
+class ScanBwdParams(ctypes.Structure):
+    _fields_ = [("fwd", ScanParams), ("dy", _vp), ("dh_final", _fp), ("dx", _fp),
+                ("ddelta", _fp), ("dz", _fp), ("dA", _fp), ("dB", _fp), ("dC", _fp),
+                ("dD_skip", _fp), ("ddelta_bias", _fp), ("dh0", _fp)]
+
+
 class SsdParams(ctypes.Structure):
     _fields_ = [("batch", _i), ("seqlen", _i), ("nheads", _i), ("headdim", _i), ("dstate", _i),
                 ("ngroups", _i), ("chunk_size", _i), ("in_dtype", _i), ("out_dtype", _i),
@@ -52,7 +58,8 @@ class StepParams(ctypes.Structure):
                 ("disc", _i)]
 
 
-SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssd_chunk_scan_fwd",
+SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
+           "ssm_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version")
 
@@ -79,6 +86,10 @@ def load(build_if_missing: bool = True):
             lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp, sz, _vp]
             lib.ssm_scan_workspace_size.restype = sz
             lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+            lib.ssm_scan_bwd.restype = _i
+            lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), _vp, sz, _vp]
+            lib.ssm_scan_bwd_workspace_size.restype = sz
+            lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
             lib.ssd_chunk_scan_fwd.restype = _i
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp, sz, _vp]
             lib.ssd_chunk_scan_workspace_size.restype = sz

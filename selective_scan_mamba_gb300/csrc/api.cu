@@ -101,6 +101,51 @@ ssm_status check_scan(const ssm_scan_params* p) {
     return SSM_OK;
 }
 
+// sizes, modes and support of the backward (what its workspace query reads)
+ssm_status check_scan_bwd_sizes(const ssm_scan_bwd_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    ssm_status st = check_scan_sizes(&p->fwd);
+    if (st != SSM_OK) return st;
+    if (p->fwd.disc != SSM_DISC_EXP_EULER)
+        return fail(SSM_ERR_UNSUPPORTED, "backward: exponential-Euler only");
+    if (!ssm::m1_bwd_supported(*p))
+        return fail(SSM_ERR_UNSUPPORTED, "backward: dstate=%d (16, 32 or 64 supported)", p->fwd.dstate);
+    return SSM_OK;
+}
+
+ssm_status check_scan_bwd(const ssm_scan_bwd_params* p) {
+    ssm_status st = check_scan_bwd_sizes(p);
+    if (st != SSM_OK) return st;
+    const ssm_scan_params* f = &p->fwd;
+    REQUIRE_PTR(f->A, "A");
+    REQUIRE_PTR(p->dA, "dA");
+    OPTIONAL_PTR(f->h0, "h0");
+    OPTIONAL_PTR(p->dh_final, "dh_final");
+    OPTIONAL_PTR(p->dh0, "dh0");
+    REQUIRE((f->D_skip == nullptr) == (p->dD_skip == nullptr), "dD_skip must be given exactly when D_skip is");
+    REQUIRE((f->delta_bias == nullptr) == (p->ddelta_bias == nullptr),
+            "ddelta_bias must be given exactly when delta_bias is");
+    REQUIRE((f->z == nullptr) == (p->dz == nullptr), "dz must be given exactly when z is");
+    OPTIONAL_PTR(f->D_skip, "D_skip");
+    OPTIONAL_PTR(f->delta_bias, "delta_bias");
+    OPTIONAL_PTR(p->dD_skip, "dD_skip");
+    OPTIONAL_PTR(p->ddelta_bias, "ddelta_bias");
+    if (f->seqlen > 0) {
+        REQUIRE_PTR(f->x, "x");
+        REQUIRE_PTR(f->delta, "delta");
+        REQUIRE_PTR(f->B, "B");
+        REQUIRE_PTR(f->C, "C");
+        REQUIRE_PTR(p->dy, "dy");
+        REQUIRE_PTR(p->dx, "dx");
+        REQUIRE_PTR(p->ddelta, "ddelta");
+        REQUIRE_PTR(p->dB, "dB");
+        REQUIRE_PTR(p->dC, "dC");
+        OPTIONAL_PTR(f->z, "z");
+        OPTIONAL_PTR(p->dz, "dz");
+    }
+    return SSM_OK;
+}
+
 ssm::M1Args scan_args(const ssm_scan_params* p) {
     ssm::M1Args a;
     a.batch = p->batch;
@@ -213,6 +258,27 @@ size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     ssm::M1Plan plan;
     if (ssm::m1_tmem_plan(scan_args(p), &plan) != cudaSuccess) return 0;
     return plan.kind == ssm::M1Plan::kTmem ? plan.ws_bytes : 0;
+}
+
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p) {
+    if (check_scan_bwd_sizes(p) != SSM_OK) return 0;
+    return ssm::m1_bwd_workspace_size(*p);
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_scan_bwd(p);
+    if (st != SSM_OK) return st;
+    const size_t need = ssm::m1_bwd_workspace_size(*p);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaError_t e = ssm::m1_bwd_launch(*p, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_bwd launch");
+    return SSM_OK;
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t workspace_bytes,

@@ -30,6 +30,12 @@ struct M1Args {
     int cpb_max;  // channels per CTA (tiled path)
 };
 
+// backward of the Mamba-1 scan (scan_m1_bwd.cu)
+using M1BwdArgs = ssm_scan_bwd_params;
+bool m1_bwd_supported(const M1BwdArgs& a);
+size_t m1_bwd_workspace_size(const M1BwdArgs& a);
+cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s);
+
 struct M1Plan {
     enum Kind { kGeneric = 0, kTiled = 1, kTma = 2, kTmem = 3 } kind;
     int tpc;      // threads per channel (tiled path)

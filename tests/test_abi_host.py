@@ -165,3 +165,44 @@ def test_python_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         ssm.ssm_scan_fwd(x, x, torch.zeros(4, 16), torch.zeros(1, 16, 8, dtype=torch.bfloat16),
                          torch.zeros(1, 16, 8, dtype=torch.bfloat16))
+
+
+def scan_bwd_params(**kw):
+    p = _lib.ScanBwdParams()
+    p.fwd = scan_params()
+    for f in ("dy", "dx", "ddelta", "dA", "dB", "dC"):
+        setattr(p, f, FAKE)
+    for k, v in kw.items():
+        if k.startswith("fwd_"):
+            setattr(p.fwd, k[4:], v)
+        else:
+            setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"fwd_disc": _lib.SSM_DISC_ZOH}, _lib.SSM_ERR_UNSUPPORTED),
+    ({"fwd_dstate": 8}, _lib.SSM_ERR_UNSUPPORTED),
+    ({"fwd_dstate": 24}, _lib.SSM_ERR_UNSUPPORTED),
+    ({"dA": None}, _lib.SSM_ERR_INVALID_ARG),
+    ({"dy": None}, _lib.SSM_ERR_INVALID_ARG),
+    ({"dB": FAKE + 4}, _lib.SSM_ERR_INVALID_ARG),
+    ({"fwd_z": FAKE}, _lib.SSM_ERR_INVALID_ARG),            # z given, dz missing
+    ({"dD_skip": FAKE}, _lib.SSM_ERR_INVALID_ARG),          # dD given, D missing
+    ({"fwd_delta_bias": FAKE}, _lib.SSM_ERR_INVALID_ARG),   # bias given, dbias missing
+    ({"fwd_ngroups": 3}, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_scan_bwd_rejects_bad_arguments(lib, kw, status):
+    p = scan_bwd_params(**kw)
+    assert lib.ssm_scan_bwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssm_last_error()
+
+
+def test_scan_bwd_workspace_size_and_shortfall(lib):
+    p = scan_bwd_params()
+    need = lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
+    # checkpoints every 32 steps, per-CTA dB/dC partials, per-row dA, dD, dbias partials
+    assert need >= 2 * 32 * (64 // 32) * 16 * 4 + 2 * 32 * 16 * 4
+    assert lib.ssm_scan_bwd(ctypes.byref(p), FAKE, need - 1, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(scan_bwd_params(fwd_dstate=8))) == 0
+    assert lib.ssm_scan_bwd_workspace_size(None) == 0
