@@ -7,7 +7,8 @@ GB/s against the measured copy bandwidth.  One step = one ssm_scan_fwd call over
 batch; several input sets (together larger than L2) rotate between steps.
 
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
-the decode update (780m-shaped, 1024 steps) and the long-context Mamba-1 sweep.
+the decode update (780m-shaped, 1024 steps), multi-token decode, the Mamba-1 backward
+(130m layer) and the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -93,6 +94,16 @@ FP32_OPS_PER_UPDATE = 4
 def alu_peak_updates(sms, sm_max_mhz):
     per_clk = min(EX2_PER_CLK_SM / 1.0, FP32_LANES_PER_CLK_SM / FP32_OPS_PER_UPDATE)
     return sms * sm_max_mhz * 1e6 * per_clk
+
+
+def bwd_bytes(batch, dim, N, L, G=1):
+    """Backward of the Mamba-1 scan: x, delta, z, dy (bf16) and B, C read once; dx,
+    ddelta, dz (float32) and dB, dC (float32) written once; A, D, bias and their
+    gradients."""
+    b = batch * dim * L * (4 * 2 + 3 * 4)
+    b += batch * G * N * L * (2 * 2 + 2 * 4)
+    b += dim * N * 8 + dim * 16
+    return b
 
 
 def step_bytes(batch, H, P, N, G, es=2, with_z=True):
@@ -469,6 +480,31 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
     out["decode_780m_tokens"] = dict(tok_runs, note="T consecutive tokens per call; 4 layer "
                                      "states rotate (403 MB > L2)")
     del states
+    # Mamba-1 backward on the 130m layer: dy in, every gradient out (float32)
+    c1 = synth.WORKLOADS["m1_130m_layer"]
+    Bt1, D1, N1, L1 = c1["batch"], c1["dim"], c1["dstate"], c1["seqlen"]
+    bsets = []
+    for k in range(2):
+        inp = synth.mamba1(Bt1, D1, N1, L1, dtype=c1["dtype"], delta_scale=c1["delta_scale"],
+                           with_z=c1["with_z"], seed=20 + k)
+        s = _dev(inp, torch)
+        s["dy"] = torch.randn((Bt1, D1, L1), device="cuda").to(torch.bfloat16)
+        bsets.append(s)
+    bws = torch.empty(ssm.ssm_scan_bwd_workspace_size(bsets[0]["x"], bsets[0]["B"]),
+                      dtype=torch.uint8, device="cuda")
+
+    def fb(i):
+        s = bsets[i % 2]
+        ssm.ssm_scan_bwd(s["x"], s["delta"], s["A"], s["B"], s["C"], s["dy"], D=s["D"], z=s["z"],
+                         delta_bias=s["delta_bias"], workspace=bws)
+    tb = time_launches(torch, fb, max(3, min(args.steps, 10)), 2, stream)
+    nbwd = bwd_bytes(Bt1, D1, N1, L1)
+    out["m1_130m_bwd"] = {"ms": tb * 1e3, "state_updates_per_s": Bt1 * D1 * N1 * L1 / tb,
+                          "hbm_gbs": nbwd / tb / 1e9, "bytes": nbwd,
+                          "workspace_bytes": bws.numel(),
+                          "note": "x, delta, z, dy bf16 in; dx, ddelta, dz, dA, dB, dC, dD, "
+                                  "dbias float32 out; 2 input sets rotate"}
+    del bsets, bws
     # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
     c3 = synth.WORKLOADS["m1_790m_long"]
     sweep = {}
@@ -607,6 +643,15 @@ def run_case(args):
         for i in range(n):
             ssm.ssm_state_update(states[i % 4], tok["x"], tok["dt"], par["A"], tok["B"], tok["C"],
                                  D=par["D"], z=tok["z"], dt_bias=par["dt_bias"], y=y)
+    elif args.case == "bwd":  # Mamba-1 backward, 130m layer
+        cfg = synth.WORKLOADS["m1_130m_layer"]
+        inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
+                           delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+        t = _dev(inp, torch)
+        dy = torch.randn(t["x"].shape, device="cuda").to(torch.bfloat16)
+        for _ in range(n):
+            ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], dy, D=t["D"], z=t["z"],
+                             delta_bias=t["delta_bias"])
     elif args.case == "tokens":  # 16 decode tokens per call, one state buffer
         c5 = synth.WORKLOADS["step_780m"]
         Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
@@ -635,7 +680,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the SSD, decode and long-context measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens"],
+    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens", "bwd"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:

@@ -15,7 +15,7 @@
 // One launch computes everything per CTA, then a small launch sums the partials:
 //   - a CTA owns 256 / TPC channels of one (batch, group) (TPC threads per channel, four
 //     consecutive states per thread);
-//   - pass 1 runs the recurrence forwards and keeps h at the start of every 32-step chunk
+//   - pass 1 runs the recurrence forwards and keeps h at the start of every 16-step chunk
 //     (the checkpoints, in the workspace);
 //   - pass 2 walks the chunks last to first: it stages the chunk's inputs in shared
 //     memory, recomputes h_t over the chunk from its checkpoint into a shared buffer
@@ -34,16 +34,19 @@ namespace ssm {
 
 namespace {
 
-constexpr int kBT = 32;          // steps per chunk
-constexpr int kBThreads = 256;   // threads per CTA
+constexpr int kBT = 16;          // steps per chunk
+constexpr int kBThreads = 256;   // threads per CTA (two CTAs per SM)
 constexpr int kBS = 4;           // states per thread
 constexpr int kRow = kBT + 1;    // padded row of the per-(channel, step) tiles
 
-struct BwdLayout {  // float offsets into dynamic shared memory
-    int h, dl, dlx, xs, dout, o, sg, zz, gx, gd, bs, cs, total;
+struct BwdLayout {  // float offsets into dynamic shared memory (16-byte aligned blocks)
+    int h, bs, cs, red, dl, dlx, xs, dout, o, sg, zz, gx, gd, total;
     __host__ __device__ BwdLayout(int cpb, int n) {
         h = 0;                                  // [kBT][kBThreads][kBS]: h_t, then G_t
-        dl = h + kBT * kBThreads * kBS;         // [cpb][kRow] Delta
+        bs = h + kBT * kBThreads * kBS;         // [kBT][n] B
+        cs = bs + kBT * n;                      // [kBT][n] C
+        red = cs + kBT * n;                     // [kBThreads][4] partial sums over channels
+        dl = red + kBThreads * 4;               // [cpb][kRow] Delta
         dlx = dl + cpb * kRow;                  // Delta x
         xs = dlx + cpb * kRow;                  // x
         dout = xs + cpb * kRow;                 // dL/do
@@ -52,9 +55,7 @@ struct BwdLayout {  // float offsets into dynamic shared memory
         zz = sg + cpb * kRow;                   // z
         gx = zz + cpb * kRow;                   // dx
         gd = gx + cpb * kRow;                   // d(delta)
-        bs = gd + cpb * kRow;                   // [n][kRow] B
-        cs = bs + n * kRow;                     // [n][kRow] C
-        total = cs + n * kRow;
+        total = gd + cpb * kRow;
     }
 };
 
@@ -69,12 +70,16 @@ __device__ __forceinline__ float ldf(const T* p, size_t i) {
     return io<T>::load(p, i);
 }
 
+__device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.f + ex2_approx(-v * SSM_LOG2E)); }
+
 template <typename Tin, typename Tdy, int TPC>
-__global__ void __launch_bounds__(kBThreads, 1)
+__global__ void __launch_bounds__(kBThreads, 2)
     m1_scan_bwd(M1BwdArgs a, int cps, float* ckpt, float* part_bc, float* part_a, float* part_d,
                 float* part_bias) {
     constexpr int N = TPC * kBS;
     constexpr int CPB = kBThreads / TPC;
+    constexpr int NQ = kBT * N / 4;         // (step, 4 states) cells of a chunk
+    constexpr int SPLIT = kBThreads / NQ;   // channel slices summed in parallel per cell
     const int L = a.fwd.seqlen, Dm = a.fwd.dim, G = a.fwd.ngroups;
     const int per_group = Dm / G;
     const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
@@ -101,12 +106,16 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const Tdy* DY = static_cast<const Tdy*>(a.dy);
     const size_t bc_base = (static_cast<size_t>(b) * G + g) * N * static_cast<size_t>(L);
 
-    float Av[kBS];
+    float Av[kBS], A2[kBS];  // A, and A log2(e) for the exponentials
 #pragma unroll
-    for (int i = 0; i < kBS; ++i) Av[i] = a.fwd.A[static_cast<size_t>(d) * N + kBS * gi + i];
+    for (int i = 0; i < kBS; ++i) {
+        Av[i] = a.fwd.A[static_cast<size_t>(d) * N + kBS * gi + i];
+        A2[i] = Av[i] * SSM_LOG2E;
+    }
     const float Dd = a.fwd.D_skip ? a.fwd.D_skip[d] : 0.f;
 
-    // stage Delta (and Delta x, x, sigmoid) of the CTA's channels and B (C) for a chunk
+    // stage Delta (and Delta x, x, sigmoid, dL/do, z) of the CTA's channels and B (C)
+    // for a chunk
     auto stage = [&](int t0, int tl, bool full) {
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
             const int cc = j / kBT, t = j % kBT;
@@ -114,14 +123,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
             if (cc < nchan && t < tl) {
                 const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
                 const float v = ldf(DL, i) + (a.fwd.delta_bias ? a.fwd.delta_bias[d0 + cc] : 0.f);
-                dl = a.fwd.delta_softplus ? softplus_accurate(v) : v;
-                sgv = a.fwd.delta_softplus ? 1.f / (1.f + expf(-v)) : 1.f;
+                dl = a.fwd.delta_softplus ? softplus_fast(v) : v;
                 xv = ldf(X, i);
                 if (full) {
+                    sgv = a.fwd.delta_softplus ? sigmoid_fast(v) : 1.f;
                     dov = ldf(DY, i);
                     if (Z) {
                         zv = ldf(Z, i);
-                        dov *= silu_accurate(zv);
+                        dov *= silu_fast(zv);
                     }
                 }
             }
@@ -137,8 +146,46 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int j = tid; j < N * kBT; j += kBThreads) {
             const int n = j / kBT, t = j % kBT;
             const size_t i = bc_base + static_cast<size_t>(n) * L + t0 + t;
-            sm[lay.bs + n * kRow + t] = t < tl ? ldf(Bp, i) : 0.f;
-            if (full) sm[lay.cs + n * kRow + t] = t < tl ? ldf(Cp, i) : 0.f;
+            sm[lay.bs + t * N + n] = t < tl ? ldf(Bp, i) : 0.f;
+            if (full) sm[lay.cs + t * N + n] = t < tl ? ldf(Cp, i) : 0.f;
+        }
+    };
+    // sum over the CTA's channels of w[channel][t] * buf[t][channel][n] for every (t, n) of
+    // the chunk, into the partial row `dst` ([N][L] at column t0): cell q = (t, 4 states)
+    // per thread slice, SPLIT slices of the channels, then the slices added
+    auto channel_sum = [&](int wofs, float* dst, int t0, int tl) {
+        const int q = tid % NQ, sl = tid / NQ;
+        const int t = q / (N / 4), n4 = q % (N / 4);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < tl) {
+            for (int cc = sl; cc < nchan; cc += SPLIT) {
+                const float w = sm[wofs + cc * kRow + t];
+                const float4 v = *reinterpret_cast<const float4*>(hbuf + (t * kBThreads + cc * TPC + n4) * kBS);
+                s.x += w * v.x;
+                s.y += w * v.y;
+                s.z += w * v.z;
+                s.w += w * v.w;
+            }
+        }
+        if (SPLIT > 1) {
+            *reinterpret_cast<float4*>(sm + lay.red + tid * 4) = s;
+            __syncthreads();
+            if (sl == 0) {
+#pragma unroll
+                for (int k = 1; k < SPLIT; ++k) {
+                    const float4 o = *reinterpret_cast<const float4*>(sm + lay.red + (tid + k * NQ) * 4);
+                    s.x += o.x;
+                    s.y += o.y;
+                    s.z += o.z;
+                    s.w += o.w;
+                }
+            }
+        }
+        if (sl == 0 && t < tl) {
+            dst[static_cast<size_t>(4 * n4 + 0) * L + t0 + t] = s.x;
+            dst[static_cast<size_t>(4 * n4 + 1) * L + t0 + t] = s.y;
+            dst[static_cast<size_t>(4 * n4 + 2) * L + t0 + t] = s.z;
+            dst[static_cast<size_t>(4 * n4 + 3) * L + t0 + t] = s.w;
         }
     };
 
@@ -155,9 +202,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
         __syncthreads();
         for (int t = 0; t < tl; ++t) {
             const float dl = sm[lay.dl + c * kRow + t], dlx = sm[lay.dlx + c * kRow + t];
+            const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
+            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-            for (int i = 0; i < kBS; ++i)
-                h[i] = expf(dl * Av[i]) * h[i] + dlx * sm[lay.bs + (kBS * gi + i) * kRow + t];
+            for (int i = 0; i < kBS; ++i) h[i] = ex2_approx(dl * A2[i]) * h[i] + dlx * bb[i];
         }
     }
 
@@ -186,12 +234,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int i = 0; i < kBS; ++i) h[i] = hs[i];
         for (int t = 0; t < tl; ++t) {
             const float dl = sm[lay.dl + c * kRow + t], dlx = sm[lay.dlx + c * kRow + t];
+            const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
+            const float4 cv = *reinterpret_cast<const float4*>(sm + lay.cs + t * N + kBS * gi);
+            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w}, cb[kBS] = {cv.x, cv.y, cv.z, cv.w};
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < kBS; ++i) {
-                const int n = kBS * gi + i;
-                h[i] = expf(dl * Av[i]) * h[i] + dlx * sm[lay.bs + n * kRow + t];
-                acc += sm[lay.cs + n * kRow + t] * h[i];
+                h[i] = ex2_approx(dl * A2[i]) * h[i] + dlx * bb[i];
+                acc += cb[i] * h[i];
             }
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(h[0], h[1], h[2], h[3]);
 #pragma unroll
@@ -200,21 +250,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
         __syncthreads();
         // dC_t[n] = sum over the CTA's channels of do_t h_t[n]; dz from the pre-gate output
-        for (int j = tid; j < N * kBT; j += kBThreads) {
-            const int n = j / kBT, t = j % kBT;
-            if (t >= tl) continue;
-            float s = 0.f;
-            for (int cc = 0; cc < nchan; ++cc)
-                s += sm[lay.dout + cc * kRow + t] * hbuf[(t * kBThreads + cc * TPC + n / kBS) * kBS + n % kBS];
-            pbc[(static_cast<size_t>(N) + n) * L + t0 + t] = s;
-        }
+        channel_sum(lay.dout, pbc + static_cast<size_t>(N) * L, t0, tl);
         if (a.dz) {
             for (int j = tid; j < CPB * kBT; j += kBThreads) {
                 const int cc = j / kBT, t = j % kBT;
                 if (cc >= nchan || t >= tl) continue;
                 const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
                 const float zv = sm[lay.zz + cc * kRow + t];
-                const float sgz = 1.f / (1.f + expf(-zv));
+                const float sgz = sigmoid_fast(zv);
                 a.dz[i] = ldf(DY, i) * sm[lay.o + cc * kRow + t] * sgz * (1.f + zv * (1.f - sgz));
             }
         }
@@ -231,19 +274,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
             }
             const float dl = sm[lay.dl + c * kRow + t], xv = sm[lay.xs + c * kRow + t];
             const float dov = sm[lay.dout + c * kRow + t];
+            const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
+            const float4 cv = *reinterpret_cast<const float4*>(sm + lay.cs + t * N + kBS * gi);
+            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w}, cb[kBS] = {cv.x, cv.y, cv.z, cv.w};
             float gx = 0.f, gd = 0.f, Gt[kBS];
 #pragma unroll
             for (int i = 0; i < kBS; ++i) {
-                const int n = kBS * gi + i;
-                const float Bn = sm[lay.bs + n * kRow + t], Cn = sm[lay.cs + n * kRow + t];
-                const float E = expf(dl * Av[i]);
-                Gt[i] = gcar[i] + dov * Cn;
-                gx += Gt[i] * dl * Bn;
+                const float E = ex2_approx(dl * A2[i]);
+                Gt[i] = gcar[i] + dov * cb[i];
+                gx += Gt[i] * bb[i];
                 const float hE = hp[i] * E;
-                gd += Gt[i] * (Bn * xv + hE * Av[i]);
+                gd += Gt[i] * (bb[i] * xv + hE * Av[i]);
                 dAacc[i] += Gt[i] * hE * dl;
                 gcar[i] = Gt[i] * E;
             }
+            gx *= dl;
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(Gt[0], Gt[1], Gt[2], Gt[3]);
 #pragma unroll
             for (int off = 1; off < TPC; off <<= 1) {
@@ -260,14 +305,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
         __syncthreads();
         // dB_t[n] = sum over the CTA's channels of G_t[n] Delta_t x_t
-        for (int j = tid; j < N * kBT; j += kBThreads) {
-            const int n = j / kBT, t = j % kBT;
-            if (t >= tl) continue;
-            float s = 0.f;
-            for (int cc = 0; cc < nchan; ++cc)
-                s += sm[lay.dlx + cc * kRow + t] * hbuf[(t * kBThreads + cc * TPC + n / kBS) * kBS + n % kBS];
-            pbc[static_cast<size_t>(n) * L + t0 + t] = s;
-        }
+        channel_sum(lay.dlx, pbc, t0, tl);
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
             const int cc = j / kBT, t = j % kBT;
             if (cc >= nchan || t >= tl) continue;

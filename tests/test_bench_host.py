@@ -40,3 +40,9 @@ def test_recorded_traffic_needs_matching_digest(tmp_path, monkeypatch):
     assert bench.recorded_traffic("m1_scan_tmem") == 123456.0
     (prof / "traffic.txt").write_text("m1_scan_tmem 999 0000000000000000\n")
     assert bench.recorded_traffic("m1_scan_tmem") is None
+
+
+def test_bwd_bytes_130m_layer():
+    # 4 bf16 reads and 3 float32 writes per (b, d, t); B, C bf16 in and dB, dC float32 out
+    b = bench.bwd_bytes(8, 1536, 16, 2048)
+    assert b == 8 * 1536 * 2048 * 20 + 8 * 16 * 2048 * 12 + 1536 * 16 * 8 + 1536 * 16
