@@ -13,7 +13,7 @@
 //   dA[n] += G_t h_{t-1} E_t Delta_t,   g <- G_t E_t,   d(delta)_t = dDelta_t sigmoid(v_t).
 //
 // One launch computes everything per CTA, then a small launch sums the partials:
-//   - a CTA owns 256 / TPC channels of one (batch, group) (TPC threads per channel, four
+//   - a CTA owns 128 / TPC channels of one (batch, group) (TPC threads per channel, four
 //     consecutive states per thread);
 //   - pass 1 runs the recurrence forwards and keeps h at the start of every 16-step chunk
 //     (the checkpoints, in the workspace);
@@ -35,7 +35,7 @@ namespace ssm {
 namespace {
 
 constexpr int kBT = 16;          // steps per chunk
-constexpr int kBThreads = 256;   // threads per CTA (two CTAs per SM)
+constexpr int kBThreads = 128;   // threads per CTA (four CTAs per SM)
 constexpr int kBS = 4;           // states per thread
 constexpr int kRow = kBT + 1;    // padded row of the per-(channel, step) tiles
 
@@ -73,13 +73,14 @@ __device__ __forceinline__ float ldf(const T* p, size_t i) {
 __device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.f + ex2_approx(-v * SSM_LOG2E)); }
 
 template <typename Tin, typename Tdy, int TPC>
-__global__ void __launch_bounds__(kBThreads, 2)
+__global__ void __launch_bounds__(kBThreads, 4)
     m1_scan_bwd(M1BwdArgs a, int cps, float* ckpt, float* part_bc, float* part_a, float* part_d,
                 float* part_bias) {
     constexpr int N = TPC * kBS;
     constexpr int CPB = kBThreads / TPC;
     constexpr int NQ = kBT * N / 4;         // (step, 4 states) cells of a chunk
-    constexpr int SPLIT = kBThreads / NQ;   // channel slices summed in parallel per cell
+    // channel slices summed in parallel per cell (1: each thread sums whole cells)
+    constexpr int SPLIT = NQ < kBThreads ? kBThreads / NQ : 1;
     const int L = a.fwd.seqlen, Dm = a.fwd.dim, G = a.fwd.ngroups;
     const int per_group = Dm / G;
     const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
@@ -154,7 +155,8 @@ __global__ void __launch_bounds__(kBThreads, 2)
     // the chunk, into the partial row `dst` ([N][L] at column t0): cell q = (t, 4 states)
     // per thread slice, SPLIT slices of the channels, then the slices added
     auto channel_sum = [&](int wofs, float* dst, int t0, int tl) {
-        const int q = tid % NQ, sl = tid / NQ;
+      for (int q0 = 0; q0 < (NQ > kBThreads ? NQ : 1); q0 += kBThreads) {
+        const int q = NQ > kBThreads ? q0 + tid : tid % NQ, sl = NQ > kBThreads ? 0 : tid / NQ;
         const int t = q / (N / 4), n4 = q % (N / 4);
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < tl) {
@@ -187,6 +189,7 @@ __global__ void __launch_bounds__(kBThreads, 2)
             dst[static_cast<size_t>(4 * n4 + 2) * L + t0 + t] = s.z;
             dst[static_cast<size_t>(4 * n4 + 3) * L + t0 + t] = s.w;
         }
+      }
     };
 
     // pass 1: checkpoints h_{t0 - 1} of every chunk
