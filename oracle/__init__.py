@@ -56,6 +56,8 @@ def _bind(path):
     lib.oracle_softplus.argtypes = [ctypes.c_double]
     lib.oracle_phi1.restype = ctypes.c_double
     lib.oracle_phi1.argtypes = [ctypes.c_double]
+    lib.oracle_mamba3_scan.restype = i
+    lib.oracle_mamba3_scan.argtypes = [i, i, i, i, i] + [dp] * 3 + [i] + [dp] * 10
     lib.oracle_mamba1_scan_bwd.restype = i
     lib.oracle_mamba1_scan_bwd.argtypes = [i, i, i, i, i] + [dp] * 3 + [i] + [dp] * 17
     lib.oracle_mamba1_scan.restype = i
@@ -197,6 +199,40 @@ def mamba1_scan_bwd(x, delta, A, B, C, dy, D=None, z=None, delta_bias=None,
     if rc:
         raise ValueError("oracle_mamba1_scan_bwd: invalid arguments")
     return out
+
+
+def mamba3_scan(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_bias=None,
+                delta_softplus=True, h0=None):
+    """Mamba-3 scan (complex diagonal A = A_re + i A_im, exponential-trapezoidal rule with
+    weight lam [batch, dim, L]).  x, delta, z: [batch, dim, L]; B, C: [batch, G, N, L];
+    A_re, A_im: [dim, N]; h0: [batch, dim, N] complex (or None).  Returns (y [batch, dim,
+    L], h_final [batch, dim, N] complex128)."""
+    x = _f64(x)
+    batch, dim, L = x.shape
+    A_re = _f64(A_re)
+    N = A_re.shape[1]
+    B = _f64(B)
+    G = B.shape[1]
+    B = _f64(B, (batch, G, N, L))
+    C = _f64(C, (batch, G, N, L))
+    delta = _f64(delta, (batch, dim, L))
+    A_im = _f64(A_im, (dim, N))
+    lam = _f64(lam, (batch, dim, L))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim, L))
+    delta_bias = _f64(delta_bias, (dim,))
+    h0p = None
+    if h0 is not None:
+        h0c = np.asarray(h0, np.complex128).reshape(batch, dim, N)
+        h0p = np.ascontiguousarray(np.stack([h0c.real, h0c.imag], axis=-1))
+    y = np.empty((batch, dim, L), np.float64)
+    hf = np.empty((batch, dim, N, 2), np.float64)
+    rc = _load().oracle_mamba3_scan(batch, dim, N, L, G, _p(x), _p(delta), _p(delta_bias),
+                                    int(bool(delta_softplus)), _p(A_re), _p(A_im), _p(lam),
+                                    _p(B), _p(C), _p(D), _p(z), _p(h0p), _p(y), _p(hf))
+    if rc:
+        raise ValueError("oracle_mamba3_scan: invalid arguments")
+    return y, hf[..., 0] + 1j * hf[..., 1]
 
 
 def _ssd_args(x, dt, A, B, C, D, z, dt_bias, h0):

@@ -218,6 +218,76 @@ int oracle_mamba1_scan_bwd(int batch, int dim, int dstate, int seqlen, int ngrou
     return 0;
 }
 
+/* Mamba-3 scan ("From S4 to Mamba-3", 03/System, mamba3_minimal.py; 04/Approach,
+ * "Complex transitions for state tracking"): a complex diagonal transition
+ * A = A_re + i A_im per (channel, state) (A_re = -exp(a) < 0, A_im = theta) with a
+ * data-dependent exponential-trapezoidal rule.  The pages fix only that the rule blends
+ * the two ends of each step with a weight lambda_t and reduces to exponential-Euler at
+ * lambda = 1, theta = 0; the reading taken here is the trapezoid over [t-1, t] with the
+ * left end decayed by the step's transition:
+ *   Abar_t[n] = exp(Delta_t A[n])                       (complex)
+ *   h_t[n]    = Abar_t h_{t-1} + (1 - lambda_t) Delta_t Abar_t B_{t-1}[n] x_{t-1}
+ *               + lambda_t Delta_t B_t[n] x_t           (the t-1 term is 0 at t = 0)
+ *   y_t       = (Re sum_n C_t[n] h_t[n] + D x_t) * SiLU(z_t).
+ * States are complex, stored as (re, im) pairs: h0, h_final [batch, dim, N, 2].
+ * lambda: [batch, dim, L].  Other layouts as oracle_mamba1_scan. */
+int oracle_mamba3_scan(int batch, int dim, int dstate, int seqlen, int ngroups,
+                       const double* x, const double* delta, const double* delta_bias,
+                       int delta_softplus, const double* A_re, const double* A_im,
+                       const double* lam, const double* B, const double* C, const double* Dskip,
+                       const double* z, const double* h0, double* y, double* h_final) {
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0 || ngroups <= 0 || dim % ngroups)
+        return 1;
+    int per_group = dim / ngroups;
+    size_t N = (size_t)dstate, L = (size_t)seqlen;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int d = 0; d < dim; ++d) {
+            int g = d / per_group;
+            size_t row = ((size_t)b * dim + d) * L;
+            double* hr = (double*)malloc(sizeof(double) * N * 2);
+            double* hi = hr + N;
+            for (size_t n = 0; n < N; ++n) {
+                size_t k = (((size_t)b * dim + d) * N + n) * 2;
+                hr[n] = h0 ? h0[k] : 0.0;
+                hi[n] = h0 ? h0[k + 1] : 0.0;
+            }
+            for (size_t t = 0; t < L; ++t) {
+                double dt = step_delta(delta[row + t], delta_bias, d, delta_softplus);
+                double lt = lam[row + t];
+                double xt = x[row + t];
+                double xp = t > 0 ? x[row + t - 1] : 0.0;
+                double acc = 0.0;
+                for (size_t n = 0; n < N; ++n) {
+                    size_t bc = (((size_t)b * ngroups + g) * N + n) * L + t;
+                    double mag = exp(dt * A_re[(size_t)d * N + n]);
+                    double ang = dt * A_im[(size_t)d * N + n];
+                    double ar = mag * cos(ang), ai = mag * sin(ang);
+                    double up = t > 0 ? B[bc - 1] * xp : 0.0;   /* B_{t-1} x_{t-1} */
+                    double cur = B[bc] * xt;                   /* B_t x_t */
+                    /* Abar (h + (1 - lambda) Delta u_{t-1}) + lambda Delta u_t */
+                    double pr = hr[n] + (1.0 - lt) * dt * up;
+                    double pi = hi[n];
+                    hr[n] = ar * pr - ai * pi + lt * dt * cur;
+                    hi[n] = ar * pi + ai * pr;
+                    acc += C[bc] * hr[n];
+                }
+                if (Dskip) acc += Dskip[d] * xt;
+                if (z) acc *= silu(z[row + t]);
+                y[row + t] = acc;
+            }
+            if (h_final)
+                for (size_t n = 0; n < N; ++n) {
+                    size_t k = (((size_t)b * dim + d) * N + n) * 2;
+                    h_final[k] = hr[n];
+                    h_final[k + 1] = hi[n];
+                }
+            free(hr);
+        }
+    }
+    return 0;
+}
+
 /* Mamba-2 sequential scan, the reference the pages test the chunked form
  * against ("From S4 to Mamba-3", 03/System, mamba2_minimal.py): scalar A per
  * head, state h[p, n] per (batch, head):

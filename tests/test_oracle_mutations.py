@@ -38,6 +38,10 @@ MUTATIONS = [
     ("bwd_gate_derivative_sign", "(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
     ("bwd_dC_uses_prev_state", "dC[bc] += dout * hs[(tt + 1) * N + n];", "dC[bc] += dout * hs[tt * N + n];"),
     ("bwd_softplus_derivative", "ddt / (1.0 + exp(-v))", "ddt / (1.0 + exp(v))"),
+    ("m3_left_end_dropped", "double pr = hr[n] + (1.0 - lt) * dt * up;", "double pr = hr[n];"),
+    ("m3_rotation_sign", "hi[n] = ar * pi + ai * pr;", "hi[n] = ar * pi - ai * pr;"),
+    ("m3_left_end_current_input", "double up = t > 0 ? B[bc - 1] * xp : 0.0;", "double up = t > 0 ? B[bc] * xt : 0.0;"),
+    ("m3_lambda_on_wrong_end", "hr[n] = ar * pr - ai * pi + lt * dt * cur;", "hr[n] = ar * pr - ai * pi + (1.0 - lt) * dt * cur;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
 ]
@@ -57,6 +61,10 @@ PIN_CHECKS = [
     lambda o: pins.test_ssd_decode_equals_scan(o, False),
     lambda o: pins.test_ssd_decode_equals_scan(o, True),
     lambda o: pins.check_mamba1_bwd_fd(o),
+    lambda o: pins.test_mamba3_reduces_to_exp_euler(o),
+    lambda o: pins.test_mamba3_unrolled_sum(o),
+    lambda o: pins.test_mamba3_steady_state(o),
+    lambda o: pins.test_mamba3_pure_rotation(o),
     lambda o: pins.test_mamba1_bwd_one_step_closed_form(o),
 ]
 

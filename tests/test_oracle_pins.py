@@ -527,3 +527,110 @@ def test_mamba1_bwd_one_step_closed_form(oracle_mod):
             "dh0": Cv * E}
     for k, w in want.items():
         assert abs(float(np.ravel(g[k])[0]) - w) <= 1e-14 * max(1.0, abs(w)), (k, g[k], w)
+
+
+# ----------------------------------------------------------------------------------------
+# Mamba-3 scan: reduction to exponential-Euler, an unrolled complex sum, a steady state
+# and a pure rotation
+# ----------------------------------------------------------------------------------------
+def _m3_inputs(seed, batch=2, dim=3, N=4, L=9, G=1, gated=True):
+    rng = np.random.default_rng(seed)
+    return {
+        "x": rng.standard_normal((batch, dim, L)),
+        "delta": 0.6 * rng.standard_normal((batch, dim, L)),
+        "A_re": -np.exp(0.5 * rng.standard_normal((dim, N))),
+        "A_im": 2.0 * rng.standard_normal((dim, N)),
+        "lam": rng.uniform(0.0, 1.0, (batch, dim, L)),
+        "B": rng.standard_normal((batch, G, N, L)),
+        "C": rng.standard_normal((batch, G, N, L)),
+        "D": rng.standard_normal(dim),
+        "z": rng.standard_normal((batch, dim, L)) if gated else None,
+        "delta_bias": 0.2 * rng.standard_normal(dim),
+        "h0": rng.standard_normal((batch, dim, N)) + 1j * rng.standard_normal((batch, dim, N)),
+    }
+
+
+def test_mamba3_reduces_to_exp_euler(oracle_mod):
+    """The pages' reduction test (04/Approach): lambda = 1, theta = 0 is Mamba-1 with the
+    exponential-Euler rule, states real."""
+    inp = _m3_inputs(11, G=1)
+    inp["lam"] = np.ones_like(inp["lam"])
+    inp["A_im"] = np.zeros_like(inp["A_im"])
+    inp["h0"] = inp["h0"].real.astype(np.complex128)
+    y3, h3 = oracle_mod.mamba3_scan(**inp)
+    y1, h1 = oracle_mod.mamba1_scan(inp["x"], inp["delta"], inp["A_re"], inp["B"], inp["C"],
+                                    D=inp["D"], z=inp["z"], delta_bias=inp["delta_bias"],
+                                    h0=inp["h0"].real)
+    assert rel_err(y3, y1) < 1e-14
+    assert rel_err(h3.real, h1) < 1e-14 and np.all(h3.imag == 0)
+
+
+def _m3_unrolled(inp, softplus=True):
+    """h_t = P(0..t) h0 + sum_s P(s+1..t) c_s with P the product of the complex decays and
+    c_s = lambda_s Delta_s u_s + (1 - lambda_s) Delta_s Abar_s u_{s-1}: the recurrence
+    summed out, written independently of the oracle."""
+    x, dl, lam = inp["x"], inp["delta"], inp["lam"]
+    batch, dim, L = x.shape
+    N = inp["A_re"].shape[1]
+    y = np.zeros((batch, dim, L))
+    hf = np.zeros((batch, dim, N), np.complex128)
+    for b in range(batch):
+        for d in range(dim):
+            A = inp["A_re"][d] + 1j * inp["A_im"][d]
+            v = dl[b, d] + inp["delta_bias"][d]
+            Dt = np.log1p(np.exp(v)) if softplus else v
+            Ab = np.exp(Dt[:, None] * A[None, :])                      # [L, N]
+            u = inp["B"][b, 0].T * x[b, d][:, None]                    # [L, N]
+            c = (lam[b, d][:, None] * Dt[:, None] * u).astype(np.complex128)
+            c[1:] += (1 - lam[b, d][1:, None]) * Dt[1:, None] * Ab[1:] * u[:-1]
+            for t in range(L):
+                h = np.prod(Ab[:t + 1], axis=0) * inp["h0"][b, d]
+                for s_ in range(t + 1):
+                    h = h + np.prod(Ab[s_ + 1:t + 1], axis=0) * c[s_]
+                o = np.real(np.sum(inp["C"][b, 0, :, t] * h)) + inp["D"][d] * x[b, d, t]
+                zt = inp["z"][b, d, t]
+                y[b, d, t] = o * zt / (1 + np.exp(-zt))
+                hf[b, d] = h
+    return y, hf
+
+
+def test_mamba3_unrolled_sum(oracle_mod):
+    inp = _m3_inputs(12)
+    y, hf = oracle_mod.mamba3_scan(**inp)
+    yr, hr = _m3_unrolled(inp)
+    assert rel_err(y, yr) < 1e-12
+    assert np.max(np.abs(hf - hr)) < 1e-12 * np.max(np.abs(hr))
+
+
+def test_mamba3_steady_state(oracle_mod):
+    """Constant Delta, lambda, x and B from t = 1 on: the state converges to
+    h* = Delta (lambda + (1 - lambda) Abar) B x / (1 - Abar)."""
+    L, N = 400, 3
+    Dt, lam_v, xv = 0.4, 0.3, 1.7
+    A = np.array([-0.5 + 2.0j, -1.2 - 0.7j, -0.3 + 5.0j])
+    Bv = np.array([0.8, -1.1, 0.4])
+    inp = {"x": np.full((1, 1, L), xv), "delta": np.full((1, 1, L), Dt),
+           "A_re": A.real[None], "A_im": A.imag[None], "lam": np.full((1, 1, L), lam_v),
+           "B": np.broadcast_to(Bv[None, None, :, None], (1, 1, N, L)).copy(),
+           "C": np.zeros((1, 1, N, L))}
+    _, hf = oracle_mod.mamba3_scan(**inp, delta_softplus=False)
+    Ab = np.exp(Dt * A)
+    hstar = Dt * (lam_v + (1 - lam_v) * Ab) * Bv * xv / (1 - Ab)
+    assert np.max(np.abs(hf[0, 0] - hstar)) < 1e-12 * np.max(np.abs(hstar))
+
+
+def test_mamba3_pure_rotation(oracle_mod):
+    """A_re = 0, lambda = 1, an impulse at t = 0: h_t = Delta_0 B_0 x_0 exp(i theta
+    sum_{r=1..t} Delta_r), so Re(C h) traces a cosine of the accumulated phase."""
+    L, theta = 12, 0.9
+    rng = np.random.default_rng(3)
+    dts = rng.uniform(0.1, 0.5, L)
+    x = np.zeros((1, 1, L))
+    x[0, 0, 0] = 1.3
+    inp = {"x": x, "delta": dts[None, None], "A_re": np.zeros((1, 1)), "A_im": np.full((1, 1), theta),
+           "lam": np.ones((1, 1, L)), "B": np.full((1, 1, 1, L), 0.7), "C": np.ones((1, 1, 1, L))}
+    y, hf = oracle_mod.mamba3_scan(**inp, delta_softplus=False)
+    phase = theta * np.concatenate([[0.0], np.cumsum(dts[1:])])
+    want = dts[0] * 0.7 * 1.3 * np.cos(phase)
+    assert np.max(np.abs(y[0, 0] - want)) < 1e-14
+    assert abs(hf[0, 0, 0] - dts[0] * 0.7 * 1.3 * np.exp(1j * phase[-1])) < 1e-14
