@@ -8,7 +8,7 @@ batch; several input sets (together larger than L2) rotate between steps.
 
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
 the decode update (780m-shaped, 1024 steps), multi-token decode, the Mamba-1 backward
-(130m layer) and the long-context Mamba-1 sweep.
+(130m layer), the Mamba-3 scan (130m layer shape) and the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -505,6 +505,27 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                           "note": "x, delta, z, dy bf16 in; dx, ddelta, dz, dA, dB, dC, dD, "
                                   "dbias float32 out; 2 input sets rotate"}
     del bsets, bws
+    # Mamba-3 scan on the 130m layer shape (complex states, trapezoid weight lam)
+    m3sets = []
+    for k in range(2):
+        inp = synth.mamba1(Bt1, D1, N1, L1, dtype=c1["dtype"], delta_scale=c1["delta_scale"],
+                           with_z=c1["with_z"], seed=30 + k)
+        s = _dev(inp, torch)
+        s["A_im"] = 3.0 * torch.randn((D1, N1), device="cuda")
+        s["lam"] = torch.rand((Bt1, D1, L1), device="cuda").to(torch.bfloat16)
+        s["y"] = torch.empty_like(s["x"])
+        m3sets.append(s)
+
+    def fm3(i):
+        s = m3sets[i % 2]
+        ssm.ssm_mamba3_scan_fwd(s["x"], s["delta"], s["A"], s["A_im"], s["lam"], s["B"], s["C"],
+                                D=s["D"], z=s["z"], delta_bias=s["delta_bias"], y=s["y"])
+    tm3 = time_launches(torch, fm3, max(3, min(args.steps, 10)), 2, stream)
+    nm3 = m1_bytes(Bt1, D1, N1, L1) + Bt1 * D1 * L1 * 2 + D1 * N1 * 4  # + lam, A_im
+    out["m3_130m"] = {"ms": tm3 * 1e3, "state_updates_per_s": Bt1 * D1 * N1 * L1 / tm3,
+                      "hbm_gbs": nm3 / tm3 / 1e9, "bytes": nm3,
+                      "note": "complex states; x, delta, lam, z, B, C bf16; 2 input sets rotate"}
+    del m3sets
     # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
     c3 = synth.WORKLOADS["m1_790m_long"]
     sweep = {}

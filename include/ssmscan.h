@@ -166,6 +166,47 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace, size_t wo
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Mamba-3 scan: complex diagonal transition, exponential-trapezoidal rule
+ *   ("From S4 to Mamba-3", 03/System, mamba3_minimal.py; 04/Approach, "Complex
+ *    transitions for state tracking")
+ *
+ * Per channel d and state n, with A = A_re + i A_im (A_re = -exp(a) < 0, A_im = theta):
+ *   Abar_t = exp(Delta_t A)                                           (complex)
+ *   h_t    = Abar_t (h_{t-1} + (1 - lambda_t) Delta_t B_{t-1} x_{t-1})
+ *            + lambda_t Delta_t B_t x_t                               (no t-1 term at t = 0)
+ *   y_t    = (Re sum_n C_t[n] h_t[n] + D x_t) * SiLU(z_t)
+ * At lambda = 1 and A_im = 0 this is ssm_scan_fwd with SSM_DISC_EXP_EULER (the pages'
+ * reduction test).  The pages name the rule and that reduction only; this trapezoid
+ * (left end decayed by the step's transition) is the reading taken.
+ *
+ * Shapes as ssm_scan_fwd, plus:
+ *   A_re, A_im  : [D, N]        float32
+ *   lam         : [Bt, D, L]    in_dtype (the trapezoid weight, after the caller's sigmoid)
+ *   h0, h_final : [Bt, D, N, 2] float32 complex (re, im) pairs (nullable)
+ * Limits: dstate in {4, 8, 16, 32, 64} (else SSM_ERR_UNSUPPORTED); no workspace.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int batch, dim, dstate, seqlen, ngroups;
+    ssm_dtype in_dtype, out_dtype;
+    const void* x;
+    const void* delta;
+    const float* delta_bias;
+    int delta_softplus;
+    const float* A_re;
+    const float* A_im;
+    const void* lam;
+    const void* B;
+    const void* C;
+    const float* D_skip;
+    const void* z;
+    const float* h0;
+    void* y;
+    float* h_final;
+} ssm_mamba3_params;
+
+ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Mamba-2 chunked SSD scan (scalar A per head)
  *   ("From S4 to Mamba-3", 03/System, mamba2_minimal.py; 04/Approach)
  *

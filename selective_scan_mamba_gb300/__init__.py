@@ -217,6 +217,49 @@ def ssm_scan_bwd_workspace_size(x, B, dy_dtype=None) -> int:
     return int(lib().ssm_scan_bwd_workspace_size(ctypes.byref(p)))
 
 
+def ssm_mamba3_scan_fwd(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_bias=None,
+                        delta_softplus=True, h0=None, *, y=None, h_final=None, out_dtype=None,
+                        return_final_state=False, stream=None):
+    """Mamba-3 scan: complex diagonal A = A_re + i A_im, exponential-trapezoidal rule.
+
+    x, delta, lam, z: [batch, dim, L] (bfloat16 or float32); B, C: [batch, G, N, L];
+    A_re, A_im: [dim, N] float32; D, delta_bias: [dim] float32; h0: [batch, dim, N, 2]
+    float32 (re, im).  Returns y and, when ``return_final_state``, h_final [batch, dim,
+    N, 2] float32.
+    """
+    torch = _torch()
+    if B.dim() == 3:
+        B = B.unsqueeze(1)
+        C = C.unsqueeze(1)
+    batch, dim, L = x.shape
+    G, N = B.shape[1], B.shape[2]
+    f32 = torch.float32
+    if y is None:
+        y = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    if return_final_state and h_final is None:
+        h_final = torch.empty((batch, dim, N, 2), dtype=f32, device=x.device)
+    p = _lib.Mamba3Params()
+    p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = batch, dim, N, L, G
+    p.in_dtype = _dtype_code(x)
+    p.out_dtype = _dtype_code(y)
+    p.x = _ptr(x, "x")
+    p.delta = _ptr(delta, "delta", (batch, dim, L), x.dtype)
+    p.delta_bias = _ptr(delta_bias, "delta_bias", (dim,), f32)
+    p.delta_softplus = int(bool(delta_softplus))
+    p.A_re = _ptr(A_re, "A_re", (dim, N), f32)
+    p.A_im = _ptr(A_im, "A_im", (dim, N), f32)
+    p.lam = _ptr(lam, "lam", (batch, dim, L), x.dtype)
+    p.B = _ptr(B, "B", (batch, G, N, L), x.dtype)
+    p.C = _ptr(C, "C", (batch, G, N, L), x.dtype)
+    p.D_skip = _ptr(D, "D", (dim,), f32)
+    p.z = _ptr(z, "z", (batch, dim, L), x.dtype)
+    p.h0 = _ptr(h0, "h0", (batch, dim, N, 2), f32)
+    p.y = _ptr(y, "y", (batch, dim, L))
+    p.h_final = _ptr(h_final, "h_final", (batch, dim, N, 2), f32)
+    _lib.check(lib().ssm_mamba3_scan_fwd(ctypes.byref(p), _stream(stream)))
+    return (y, h_final) if return_final_state else y
+
+
 def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h_final, disc):
     torch = _torch()
     batch, L, H, P = x.shape

@@ -42,6 +42,14 @@ class ScanBwdParams(ctypes.Structure):
                 ("dD_skip", _fp), ("ddelta_bias", _fp), ("dh0", _fp)]
 
 
+class Mamba3Params(ctypes.Structure):
+    _fields_ = [("batch", _i), ("dim", _i), ("dstate", _i), ("seqlen", _i), ("ngroups", _i),
+                ("in_dtype", _i), ("out_dtype", _i),
+                ("x", _vp), ("delta", _vp), ("delta_bias", _fp), ("delta_softplus", _i),
+                ("A_re", _fp), ("A_im", _fp), ("lam", _vp), ("B", _vp), ("C", _vp),
+                ("D_skip", _fp), ("z", _vp), ("h0", _fp), ("y", _vp), ("h_final", _fp)]
+
+
 class SsdParams(ctypes.Structure):
     _fields_ = [("batch", _i), ("seqlen", _i), ("nheads", _i), ("headdim", _i), ("dstate", _i),
                 ("ngroups", _i), ("chunk_size", _i), ("in_dtype", _i), ("out_dtype", _i),
@@ -59,7 +67,7 @@ class StepParams(ctypes.Structure):
 
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
-           "ssm_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
+           "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version")
 
@@ -90,6 +98,8 @@ def load(build_if_missing: bool = True):
             lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), _vp, sz, _vp]
             lib.ssm_scan_bwd_workspace_size.restype = sz
             lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
+            lib.ssm_mamba3_scan_fwd.restype = _i
+            lib.ssm_mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Params), _vp]
             lib.ssd_chunk_scan_fwd.restype = _i
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp, sz, _vp]
             lib.ssd_chunk_scan_workspace_size.restype = sz

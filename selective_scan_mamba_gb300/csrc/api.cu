@@ -260,6 +260,49 @@ size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     return plan.kind == ssm::M1Plan::kTmem ? plan.ws_bytes : 0;
 }
 
+ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream) {
+    g_err[0] = '\0';
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->batch >= 1 && p->dim >= 1 && p->dstate >= 1 && p->seqlen >= 0 && p->ngroups >= 1,
+            "bad sizes: batch=%d dim=%d dstate=%d seqlen=%d ngroups=%d", p->batch, p->dim,
+            p->dstate, p->seqlen, p->ngroups);
+    REQUIRE(p->dim % p->ngroups == 0, "ngroups=%d does not divide dim=%d", p->ngroups, p->dim);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(static_cast<long long>(p->batch) * p->dim * (p->seqlen > 0 ? p->seqlen : 1) < (1LL << 40),
+            "tensor too large");
+    if (!ssm::m3_supported(p->dstate))
+        return fail(SSM_ERR_UNSUPPORTED, "mamba3: dstate=%d (4, 8, 16, 32 or 64 supported)", p->dstate);
+    REQUIRE_PTR(p->A_re, "A_re");
+    REQUIRE_PTR(p->A_im, "A_im");
+    OPTIONAL_PTR(p->delta_bias, "delta_bias");
+    OPTIONAL_PTR(p->D_skip, "D_skip");
+    OPTIONAL_PTR(p->h0, "h0");
+    OPTIONAL_PTR(p->h_final, "h_final");
+    if (p->seqlen > 0) {
+        REQUIRE_PTR(p->x, "x");
+        REQUIRE_PTR(p->delta, "delta");
+        REQUIRE_PTR(p->lam, "lam");
+        REQUIRE_PTR(p->B, "B");
+        REQUIRE_PTR(p->C, "C");
+        REQUIRE_PTR(p->y, "y");
+        OPTIONAL_PTR(p->z, "z");
+    }
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->seqlen == 0) {
+        if (p->h_final) {
+            const size_t bytes = static_cast<size_t>(p->batch) * p->dim * p->dstate * 2 * sizeof(float);
+            cudaError_t e = p->h0 ? cudaMemcpyAsync(p->h_final, p->h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(p->h_final, 0, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e, "ssm_mamba3_scan_fwd (empty sequence)");
+        }
+        return SSM_OK;
+    }
+    cudaError_t e = ssm::m3_launch(*p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_mamba3_scan_fwd launch");
+    return SSM_OK;
+}
+
 size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p) {
     if (check_scan_bwd_sizes(p) != SSM_OK) return 0;
     return ssm::m1_bwd_workspace_size(*p);

@@ -36,6 +36,10 @@ bool m1_bwd_supported(const M1BwdArgs& a);
 size_t m1_bwd_workspace_size(const M1BwdArgs& a);
 cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s);
 
+// Mamba-3 complex scan (scan_m3.cu)
+bool m3_supported(int dstate);
+cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s);
+
 struct M1Plan {
     enum Kind { kGeneric = 0, kTiled = 1, kTma = 2, kTmem = 3 } kind;
     int tpc;      // threads per channel (tiled path)

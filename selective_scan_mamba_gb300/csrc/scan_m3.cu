@@ -1,0 +1,200 @@
+// scan_m3.cu -- Mamba-3 scan: complex diagonal transition, exponential-trapezoidal rule.
+//
+// ("From S4 to Mamba-3", 03/System, mamba3_minimal.py; 04/Approach, "Complex transitions
+// for state tracking".)  Per channel d and state n, A = A_re + i A_im (A_re < 0):
+//   Abar_t = exp(Delta_t A)
+//   h_t    = Abar_t (h_{t-1} + (1 - lambda_t) Delta_t B_{t-1} x_{t-1}) + lambda_t Delta_t B_t x_t
+//   y_t    = (Re sum_n C_t h_t + D x_t) SiLU(z_t)
+// which is the exponential-Euler Mamba-1 scan at lambda = 1, A_im = 0.
+//
+// A CTA of 128 threads owns 128 / TPC channels of one (batch, group) (TPC threads per
+// channel, four complex states per thread, in registers for the whole sequence).  Per
+// 32-step chunk the CTA stages in shared memory, per (channel, step), Delta, the two input
+// weights p_t = (1 - lambda_t) Delta_t x_{t-1} and q_t = lambda_t Delta_t x_t, x and the
+// gate, and the B rows t0-1 .. t0+31 and C rows of the group; the recurrence then reads
+// shared memory only, sums Re(C h) over the channel's threads with shuffles, and the
+// chunk's outputs leave in coalesced rows.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kMT = 32;          // steps per chunk
+constexpr int kMThreads = 128;
+constexpr int kMS = 4;           // complex states per thread
+constexpr int kMRow = kMT + 1;
+
+struct M3Layout {  // float offsets
+    int dl, p, q, x, gate, y, bs, cs, total;
+    __host__ __device__ M3Layout(int cpb, int n) {
+        dl = 0;                      // [cpb][kMRow] Delta
+        p = dl + cpb * kMRow;        // (1 - lambda) Delta x_{t-1}
+        q = p + cpb * kMRow;         // lambda Delta x_t
+        x = q + cpb * kMRow;         // x
+        gate = x + cpb * kMRow;      // SiLU(z) or 1
+        y = gate + cpb * kMRow;      // outputs
+        bs = y + cpb * kMRow;        // [kMT + 1][n] B rows t0-1 .. t0+kMT-1
+        cs = bs + (kMT + 1) * n;     // [kMT][n] C rows
+        total = cs + kMT * n;
+    }
+};
+
+template <typename Tin, typename Tout, int TPC>
+__global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cps) {
+    constexpr int N = TPC * kMS;
+    constexpr int CPB = kMThreads / TPC;
+    const int L = a.seqlen, Dm = a.dim, G = a.ngroups;
+    const int per_group = Dm / G;
+    const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
+    const int b = pair / G, g = pair % G;
+    const int l0 = static_cast<int>((static_cast<long long>(part_i) * per_group) / cps);
+    const int l1 = static_cast<int>((static_cast<long long>(part_i + 1) * per_group) / cps);
+    const int nchan = l1 - l0;
+    const int d0 = g * per_group + l0;
+
+    extern __shared__ __align__(16) float sm[];
+    const M3Layout lay(CPB, N);
+    const int tid = threadIdx.x;
+    const int c = tid / TPC, gi = tid % TPC;
+    const bool active = c < nchan;
+    const int d = d0 + (active ? c : 0);
+    const size_t row = static_cast<size_t>(b) * Dm + d;
+    const Tin* X = static_cast<const Tin*>(a.x);
+    const Tin* DL = static_cast<const Tin*>(a.delta);
+    const Tin* LM = static_cast<const Tin*>(a.lam);
+    const Tin* Z = static_cast<const Tin*>(a.z);
+    const Tin* Bp = static_cast<const Tin*>(a.B);
+    const Tin* Cp = static_cast<const Tin*>(a.C);
+    const size_t bc_base = (static_cast<size_t>(b) * G + g) * N * static_cast<size_t>(L);
+
+    float are2[kMS], aim[kMS], hr[kMS], hi[kMS];
+#pragma unroll
+    for (int i = 0; i < kMS; ++i) {
+        const size_t k = static_cast<size_t>(d) * N + kMS * gi + i;
+        are2[i] = a.A_re[k] * SSM_LOG2E;
+        aim[i] = a.A_im[k];
+        const size_t hk = (row * N + kMS * gi + i) * 2;
+        hr[i] = (active && a.h0) ? a.h0[hk] : 0.f;
+        hi[i] = (active && a.h0) ? a.h0[hk + 1] : 0.f;
+    }
+    const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
+
+    for (int t0 = 0; t0 < L; t0 += kMT) {
+        const int tl = min(kMT, L - t0);
+        __syncthreads();  // the previous chunk's tiles and outputs are done with
+        for (int j = tid; j < CPB * kMT; j += kMThreads) {
+            const int cc = j / kMT, t = j % kMT;
+            float dl = 0.f, p = 0.f, q = 0.f, xv = 0.f, gv = 1.f;
+            if (cc < nchan && t < tl) {
+                const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
+                const float v = io<Tin>::load(DL, i) + (a.delta_bias ? a.delta_bias[d0 + cc] : 0.f);
+                dl = a.delta_softplus ? softplus_accurate(v) : v;
+                const float lm = io<Tin>::load(LM, i);
+                xv = io<Tin>::load(X, i);
+                const float xp = (t0 + t > 0) ? io<Tin>::load(X, i - 1) : 0.f;
+                p = (1.f - lm) * dl * xp;
+                q = lm * dl * xv;
+                if (Z) gv = silu_accurate(io<Tin>::load(Z, i));
+            }
+            sm[lay.dl + cc * kMRow + t] = dl;
+            sm[lay.p + cc * kMRow + t] = p;
+            sm[lay.q + cc * kMRow + t] = q;
+            sm[lay.x + cc * kMRow + t] = xv;
+            sm[lay.gate + cc * kMRow + t] = gv;
+        }
+        for (int j = tid; j < N * (kMT + 1); j += kMThreads) {
+            const int n = j / (kMT + 1), tt = j % (kMT + 1);  // B row t0 - 1 + tt
+            const int t = t0 - 1 + tt;
+            sm[lay.bs + tt * N + n] = (t >= 0 && tt <= tl) ? io<Tin>::load(Bp, bc_base + static_cast<size_t>(n) * L + t) : 0.f;
+            if (tt < kMT)
+                sm[lay.cs + tt * N + n] = tt < tl ? io<Tin>::load(Cp, bc_base + static_cast<size_t>(n) * L + t0 + tt) : 0.f;
+        }
+        __syncthreads();
+        for (int t = 0; t < tl; ++t) {
+            const float dl = sm[lay.dl + c * kMRow + t];
+            const float p = sm[lay.p + c * kMRow + t], q = sm[lay.q + c * kMRow + t];
+            const float4 bp = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kMS * gi);
+            const float4 bc = *reinterpret_cast<const float4*>(sm + lay.bs + (t + 1) * N + kMS * gi);
+            const float4 cv = *reinterpret_cast<const float4*>(sm + lay.cs + t * N + kMS * gi);
+            const float bpa[kMS] = {bp.x, bp.y, bp.z, bp.w}, bca[kMS] = {bc.x, bc.y, bc.z, bc.w};
+            const float cva[kMS] = {cv.x, cv.y, cv.z, cv.w};
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMS; ++i) {
+                const float mag = ex2_approx(dl * are2[i]);
+                float sn, cs;
+                sincosf(dl * aim[i], &sn, &cs);
+                const float ar = mag * cs, ai = mag * sn;
+                const float pr = hr[i] + p * bpa[i], pi = hi[i];
+                hr[i] = ar * pr - ai * pi + q * bca[i];
+                hi[i] = ar * pi + ai * pr;
+                acc += cva[i] * hr[i];
+            }
+#pragma unroll
+            for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (gi == 0)
+                sm[lay.y + c * kMRow + t] = (acc + Dd * sm[lay.x + c * kMRow + t]) * sm[lay.gate + c * kMRow + t];
+        }
+        __syncthreads();
+        for (int j = tid; j < CPB * kMT; j += kMThreads) {
+            const int cc = j / kMT, t = j % kMT;
+            if (cc >= nchan || t >= tl) continue;
+            const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
+            io<Tout>::store(static_cast<Tout*>(a.y), i, sm[lay.y + cc * kMRow + t]);
+        }
+    }
+    if (active && a.h_final) {
+#pragma unroll
+        for (int i = 0; i < kMS; ++i) {
+            const size_t hk = (row * N + kMS * gi + i) * 2;
+            a.h_final[hk] = hr[i];
+            a.h_final[hk + 1] = hi[i];
+        }
+    }
+}
+
+template <typename Tin, typename Tout, int TPC>
+cudaError_t launch_m3(const ssm_mamba3_params& a, cudaStream_t s) {
+    constexpr int CPB = kMThreads / TPC;
+    const int per_group = a.dim / a.ngroups;
+    const int cps = (per_group + CPB - 1) / CPB;
+    const M3Layout lay(CPB, TPC * kMS);
+    const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
+    auto k = m3_scan<Tin, Tout, TPC>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k<<<a.batch * a.ngroups * cps, kMThreads, smem, s>>>(a, cps);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t dispatch_m3(const ssm_mamba3_params& a, cudaStream_t s) {
+    switch (a.dstate) {
+        case 4: return launch_m3<Tin, Tout, 1>(a, s);
+        case 8: return launch_m3<Tin, Tout, 2>(a, s);
+        case 16: return launch_m3<Tin, Tout, 4>(a, s);
+        case 32: return launch_m3<Tin, Tout, 8>(a, s);
+        case 64: return launch_m3<Tin, Tout, 16>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool m3_supported(int dstate) {
+    return dstate == 4 || dstate == 8 || dstate == 16 || dstate == 32 || dstate == 64;
+}
+
+cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s) {
+    const bool ib = a.in_dtype == SSM_BF16, ob = a.out_dtype == SSM_BF16;
+    if (ib && ob) return dispatch_m3<bf16_t, bf16_t>(a, s);
+    if (ib) return dispatch_m3<bf16_t, float>(a, s);
+    if (ob) return dispatch_m3<float, bf16_t>(a, s);
+    return dispatch_m3<float, float>(a, s);
+}
+
+}  // namespace ssm

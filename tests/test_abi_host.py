@@ -206,3 +206,30 @@ def test_scan_bwd_workspace_size_and_shortfall(lib):
     assert lib.ssm_scan_bwd(ctypes.byref(p), FAKE, need - 1, None) == _lib.SSM_ERR_INVALID_ARG
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(scan_bwd_params(fwd_dstate=8))) == 0
     assert lib.ssm_scan_bwd_workspace_size(None) == 0
+
+
+def mamba3_params(**kw):
+    p = _lib.Mamba3Params()
+    p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = 2, 32, 16, 64, 1
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    for f in ("x", "delta", "A_re", "A_im", "lam", "B", "C", "y"):
+        setattr(p, f, FAKE)
+    p.delta_softplus = 1
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dstate", 12, _lib.SSM_ERR_UNSUPPORTED),
+    ("dstate", 128, _lib.SSM_ERR_UNSUPPORTED),
+    ("A_im", None, _lib.SSM_ERR_INVALID_ARG),
+    ("lam", None, _lib.SSM_ERR_INVALID_ARG),
+    ("lam", FAKE + 2, _lib.SSM_ERR_INVALID_ARG),
+    ("ngroups", 5, _lib.SSM_ERR_INVALID_ARG),
+    ("batch", 0, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_mamba3_rejects_bad_arguments(lib, field, value, status):
+    p = mamba3_params(**{field: value})
+    assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), None) == status
+    assert lib.ssm_last_error()
