@@ -43,6 +43,16 @@ struct M3Layout {  // float offsets
     }
 };
 
+// sin and cos of x: Cody-Waite reduction to r = x - k 2pi with 2pi split into a float
+// head and its tail (2pi - head, -1.748455531e-7), then the MUFU forms on |r| <= pi
+// (absolute error ~4e-7 there).  Exact for |x| well below 2^10.
+__device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
+    const float k = rintf(x * 0.15915494309189535f);
+    float r = fmaf(-k, 6.2831854820251465f, x);
+    r = fmaf(-k, -1.7484555314695172e-7f, r);
+    __sincosf(r, s, c);
+}
+
 template <typename Tin, typename Tout, int TPC>
 __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cps) {
     constexpr int N = TPC * kMS;
@@ -127,7 +137,7 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
             for (int i = 0; i < kMS; ++i) {
                 const float mag = ex2_approx(dl * are2[i]);
                 float sn, cs;
-                sincosf(dl * aim[i], &sn, &cs);
+                sincos_reduced(dl * aim[i], &sn, &cs);
                 const float ar = mag * cs, ai = mag * sn;
                 const float pr = hr[i] + p * bpa[i], pi = hi[i];
                 hr[i] = ar * pr - ai * pi + q * bca[i];
