@@ -56,6 +56,10 @@ def _bind(path):
     lib.oracle_softplus.argtypes = [ctypes.c_double]
     lib.oracle_phi1.restype = ctypes.c_double
     lib.oracle_phi1.argtypes = [ctypes.c_double]
+    lib.oracle_s4d_kernel.restype = i
+    lib.oracle_s4d_kernel.argtypes = [i, i, i] + [dp] * 5
+    lib.oracle_s4d_recurrent.restype = i
+    lib.oracle_s4d_recurrent.argtypes = [i, i, i, i] + [dp] * 9
     lib.oracle_mamba3_scan.restype = i
     lib.oracle_mamba3_scan.argtypes = [i, i, i, i, i] + [dp] * 3 + [i] + [dp] * 10
     lib.oracle_mamba1_scan_bwd.restype = i
@@ -233,6 +237,56 @@ def mamba3_scan(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_bias=None
     if rc:
         raise ValueError("oracle_mamba3_scan: invalid arguments")
     return y, hf[..., 0] + 1j * hf[..., 1]
+
+
+def _pairs(a, shape):
+    """complex array -> float64 (re, im) pairs of the given leading shape"""
+    a = np.asarray(a, np.complex128).reshape(shape)
+    return np.ascontiguousarray(np.stack([a.real, a.imag], axis=-1))
+
+
+def s4d_kernel(log_dt, A, B, C, L):
+    """S4D convolution kernel K [dim, L]: K_l = Re sum_n C Bbar Abar^l (exact ZOH).
+    log_dt [dim]; A, B, C complex [dim, N]."""
+    log_dt = _f64(log_dt)
+    dim = log_dt.shape[0]
+    N = np.asarray(A).shape[1]
+    K = np.empty((dim, L), np.float64)
+    rc = _load().oracle_s4d_kernel(dim, N, L, _p(log_dt), _p(_pairs(A, (dim, N))),
+                                   _p(_pairs(B, (dim, N))), _p(_pairs(C, (dim, N))), _p(K))
+    if rc:
+        raise ValueError("oracle_s4d_kernel: invalid arguments")
+    return K
+
+
+def s4d_recurrent(u, log_dt, A, B, C, D=None, h0=None):
+    """S4D recurrent form from h0 (complex [batch, dim, N], zeros when None).  u [batch,
+    dim, L].  Returns (y [batch, dim, L], h_final complex [batch, dim, N])."""
+    u = _f64(u)
+    batch, dim, L = u.shape
+    N = np.asarray(A).shape[1]
+    y = np.empty((batch, dim, L), np.float64)
+    hf = np.empty((batch, dim, N, 2), np.float64)
+    rc = _load().oracle_s4d_recurrent(batch, dim, N, L, _p(u), _p(_f64(log_dt, (dim,))),
+                                      _p(_pairs(A, (dim, N))), _p(_pairs(B, (dim, N))),
+                                      _p(_pairs(C, (dim, N))), _p(_f64(D, (dim,))),
+                                      _p(None if h0 is None else _pairs(h0, (batch, dim, N))),
+                                      _p(y), _p(hf))
+    if rc:
+        raise ValueError("oracle_s4d_recurrent: invalid arguments")
+    return y, hf[..., 0] + 1j * hf[..., 1]
+
+
+def s4d_fft_conv(u, log_dt, A, B, C, D=None):
+    """S4D convolution form: y = K * u (causal, by FFT of length 2L) + D u."""
+    u = _f64(u)
+    batch, dim, L = u.shape
+    K = s4d_kernel(log_dt, A, B, C, L)
+    n = 2 * L if L else 1
+    y = np.fft.irfft(np.fft.rfft(u, n=n) * np.fft.rfft(K, n=n)[None], n=n)[..., :L]
+    if D is not None:
+        y = y + _f64(D, (dim,))[None, :, None] * u
+    return y
 
 
 def _ssd_args(x, dt, A, B, C, D, z, dt_bias, h0):

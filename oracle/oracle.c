@@ -288,6 +288,98 @@ int oracle_mamba3_scan(int batch, int dim, int dstate, int seqlen, int ngroups,
     return 0;
 }
 
+/* S4D ("From S4 to Mamba-3", 03/System, s4_minimal.py; Likely questions Q01): a linear
+ * time-invariant SSM with a complex diagonal A per (channel, state), discretised by exact
+ * ZOH with Delta = exp(log_dt) per channel:
+ *   Abar[n] = exp(Delta A[n]),  Bbar[n] = Delta B[n] phi1(Delta A[n]),  phi1(z) = (e^z - 1)/z
+ * (the Taylor polynomial 1 + z/2 + z^2/6 for |z| < 1e-4, as the pages state), and
+ *   recurrent form:    h_t = Abar h_{t-1} + Bbar u_t,  y_t = Re sum_n C[n] h_t[n] + D u_t
+ *   convolution form:  y = K * u + D u,  K_l = Re sum_n C[n] Bbar[n] Abar[n]^l
+ * (equal from a zero state; the pages test one against the other).  A, B, C complex
+ * (re, im) pairs: A [dim, N, 2], B, C [dim, N, 2]; u, y [batch, dim, L]; h0, h_final
+ * [batch, dim, N, 2]. */
+static void s4d_discretise(double dt, double ar, double ai, double br, double bi,
+                           double* abr, double* abi, double* bbr, double* bbi) {
+    double zr = dt * ar, zi = dt * ai;
+    double ex = exp(zr);
+    *abr = ex * cos(zi);
+    *abi = ex * sin(zi);
+    double pr, pi;  /* phi1(z) */
+    if (sqrt(zr * zr + zi * zi) < 1e-4) {
+        /* 1 + z/2 + z^2/6 */
+        pr = 1.0 + zr / 2.0 + (zr * zr - zi * zi) / 6.0;
+        pi = zi / 2.0 + (2.0 * zr * zi) / 6.0;
+    } else {
+        /* (e^z - 1) / z with e^z - 1 = expm1(zr) cos(zi) - 2 sin^2(zi/2) + i e^zr sin(zi) */
+        double s2 = sin(zi / 2.0);
+        double nr = expm1(zr) * cos(zi) - 2.0 * s2 * s2;
+        double ni = ex * sin(zi);
+        double den = zr * zr + zi * zi;
+        pr = (nr * zr + ni * zi) / den;
+        pi = (ni * zr - nr * zi) / den;
+    }
+    /* Bbar = Delta B phi1 */
+    *bbr = dt * (br * pr - bi * pi);
+    *bbi = dt * (br * pi + bi * pr);
+}
+
+int oracle_s4d_kernel(int dim, int dstate, int seqlen, const double* log_dt, const double* A,
+                      const double* B, const double* C, double* K) {
+    if (dim <= 0 || dstate <= 0 || seqlen < 0) return 1;
+    size_t N = (size_t)dstate, L = (size_t)seqlen;
+    for (int d = 0; d < dim; ++d) {
+        double dt = exp(log_dt[d]);
+        for (size_t l = 0; l < L; ++l) K[(size_t)d * L + l] = 0.0;
+        for (size_t n = 0; n < N; ++n) {
+            size_t k = ((size_t)d * N + n) * 2;
+            double abr, abi, bbr, bbi;
+            s4d_discretise(dt, A[k], A[k + 1], B[k], B[k + 1], &abr, &abi, &bbr, &bbi);
+            /* w = C Bbar, then w Abar^l for l = 0, 1, ... */
+            double wr = C[k] * bbr - C[k + 1] * bbi, wi = C[k] * bbi + C[k + 1] * bbr;
+            for (size_t l = 0; l < L; ++l) {
+                K[(size_t)d * L + l] += wr;
+                double nr = wr * abr - wi * abi;
+                wi = wr * abi + wi * abr;
+                wr = nr;
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_s4d_recurrent(int batch, int dim, int dstate, int seqlen, const double* u,
+                         const double* log_dt, const double* A, const double* B, const double* C,
+                         const double* Dskip, const double* h0, double* y, double* h_final) {
+    if (batch < 0 || dim <= 0 || dstate <= 0 || seqlen < 0) return 1;
+    size_t N = (size_t)dstate, L = (size_t)seqlen;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < batch; ++b) {
+        for (int d = 0; d < dim; ++d) {
+            double dt = exp(log_dt[d]);
+            size_t row = ((size_t)b * dim + d) * L;
+            for (size_t t = 0; t < L; ++t) y[row + t] = Dskip ? Dskip[d] * u[row + t] : 0.0;
+            for (size_t n = 0; n < N; ++n) {
+                size_t k = ((size_t)d * N + n) * 2;
+                size_t hk = (((size_t)b * dim + d) * N + n) * 2;
+                double abr, abi, bbr, bbi;
+                s4d_discretise(dt, A[k], A[k + 1], B[k], B[k + 1], &abr, &abi, &bbr, &bbi);
+                double hr = h0 ? h0[hk] : 0.0, hi = h0 ? h0[hk + 1] : 0.0;
+                for (size_t t = 0; t < L; ++t) {
+                    double nr = abr * hr - abi * hi + bbr * u[row + t];
+                    hi = abr * hi + abi * hr + bbi * u[row + t];
+                    hr = nr;
+                    y[row + t] += C[k] * hr - C[k + 1] * hi;
+                }
+                if (h_final) {
+                    h_final[hk] = hr;
+                    h_final[hk + 1] = hi;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 /* Mamba-2 sequential scan, the reference the pages test the chunked form
  * against ("From S4 to Mamba-3", 03/System, mamba2_minimal.py): scalar A per
  * head, state h[p, n] per (batch, head):

@@ -42,6 +42,10 @@ MUTATIONS = [
     ("m3_rotation_sign", "hi[n] = ar * pi + ai * pr;", "hi[n] = ar * pi - ai * pr;"),
     ("m3_left_end_current_input", "double up = t > 0 ? B[bc - 1] * xp : 0.0;", "double up = t > 0 ? B[bc] * xt : 0.0;"),
     ("m3_lambda_on_wrong_end", "hr[n] = ar * pr - ai * pi + lt * dt * cur;", "hr[n] = ar * pr - ai * pi + (1.0 - lt) * dt * cur;"),
+    ("s4d_taylor_imag", "pi = zi / 2.0 + (2.0 * zr * zi) / 6.0;", "pi = zi / 2.0;"),
+    ("s4d_expm1_term_dropped", "double nr = expm1(zr) * cos(zi) - 2.0 * s2 * s2;", "double nr = expm1(zr) * cos(zi);"),
+    ("s4d_kernel_conjugate", "wi = wr * abi + wi * abr;", "wi = -wr * abi + wi * abr;"),
+    ("s4d_output_imag_sign", "y[row + t] += C[k] * hr - C[k + 1] * hi;", "y[row + t] += C[k] * hr + C[k + 1] * hi;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
 ]
@@ -65,6 +69,10 @@ PIN_CHECKS = [
     lambda o: pins.test_mamba3_unrolled_sum(o),
     lambda o: pins.test_mamba3_steady_state(o),
     lambda o: pins.test_mamba3_pure_rotation(o),
+    lambda o: pins.test_s4d_fft_conv_equals_recurrent(o, 64),
+    lambda o: pins.test_s4d_zoh_against_high_precision(o, 1e-3 + 0.5j),
+    lambda o: pins.test_s4d_zoh_against_high_precision(o, 3e-5 - 9e-5j),
+    lambda o: pins.test_s4d_dc_gain(o),
     lambda o: pins.test_mamba1_bwd_one_step_closed_form(o),
 ]
 

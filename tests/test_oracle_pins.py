@@ -634,3 +634,51 @@ def test_mamba3_pure_rotation(oracle_mod):
     want = dts[0] * 0.7 * 1.3 * np.cos(phase)
     assert np.max(np.abs(y[0, 0] - want)) < 1e-14
     assert abs(hf[0, 0, 0] - dts[0] * 0.7 * 1.3 * np.exp(1j * phase[-1])) < 1e-14
+
+
+# ----------------------------------------------------------------------------------------
+# S4D: convolution form equals recurrent form (the pages' test), ZOH against
+# high-precision arithmetic, the continuous-time DC gain
+# ----------------------------------------------------------------------------------------
+def _s4d_params(seed, dim=3, N=4):
+    rng = np.random.default_rng(seed)
+    n = np.arange(N)
+    A = np.broadcast_to(-0.5 + 1j * np.pi * n, (dim, N)).copy()          # S4D-Lin
+    log_dt = rng.uniform(np.log(1e-3), np.log(1e-1), dim)
+    B = np.ones((dim, N), np.complex128)
+    C = rng.standard_normal((dim, N)) + 1j * rng.standard_normal((dim, N))
+    D = rng.standard_normal(dim)
+    return log_dt, A, B, C, D
+
+
+@pytest.mark.parametrize("L", [1, 7, 64, 300])
+def test_s4d_fft_conv_equals_recurrent(oracle_mod, L):
+    log_dt, A, B, C, D = _s4d_params(21)
+    u = np.random.default_rng(22).standard_normal((2, 3, L))
+    yc = oracle_mod.s4d_fft_conv(u, log_dt, A, B, C, D=D)
+    yr, _ = oracle_mod.s4d_recurrent(u, log_dt, A, B, C, D=D)
+    assert rel_err(yc, yr) < 1e-12
+
+
+@pytest.mark.parametrize("z", [1e-6 + 2e-6j, 3e-5 - 9e-5j, 1e-3 + 0.5j, -0.8 + 3.0j, -2.5 - 40.0j])
+def test_s4d_zoh_against_high_precision(oracle_mod, z):
+    """K_0 = Re(C Bbar) with N = 1, B = 1: C = 1 gives Re(Bbar), C = -i gives Im(Bbar);
+    Bbar = Delta (e^z - 1)/z evaluated with 50 digits."""
+    dt = 0.05
+    A = np.array([[z / dt]])
+    Bb = mpmath.mpf(dt) * (mpmath.exp(mpmath.mpc(z.real, z.imag)) - 1) / mpmath.mpc(z.real, z.imag)
+    for Cv, want in ((1.0 + 0j, float(Bb.real)), (-1j, float(Bb.imag))):
+        K = oracle_mod.s4d_kernel(np.array([np.log(dt)]), A, np.ones((1, 1)), np.array([[Cv]]), 1)
+        # within the Taylor band the pages' polynomial is exact to O(z^3)
+        tol = 1e-15 + (abs(z) ** 3 * dt if abs(z) < 1e-4 else 0.0)
+        assert abs(K[0, 0] - want) <= tol * max(1.0, abs(want)) + 1e-18, (z, K[0, 0], want)
+
+
+def test_s4d_dc_gain(oracle_mod):
+    """A constant input settles at the continuous-time DC gain -C B / A, which ZOH
+    reproduces exactly (real A, N = 1)."""
+    a, dt = -0.7, 0.3
+    L = 400
+    y, _ = oracle_mod.s4d_recurrent(np.ones((1, 1, L)), np.array([np.log(dt)]), np.array([[a + 0j]]),
+                                    np.array([[2.0 + 0j]]), np.array([[1.5 + 0j]]))
+    assert abs(y[0, 0, -1] - (-1.5 * 2.0 / a)) < 1e-12
