@@ -8,7 +8,8 @@ batch; several input sets (together larger than L2) rotate between steps.
 
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
 the decode update (780m-shaped, 1024 steps), multi-token decode, the Mamba-1 backward
-(130m layer), the Mamba-3 scan (130m layer shape) and the long-context Mamba-1 sweep.
+(130m layer), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel) and
+the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -526,6 +527,32 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                       "hbm_gbs": nm3 / tm3 / 1e9, "bytes": nm3,
                       "note": "complex states; x, delta, lam, z, B, C bf16; 2 input sets rotate"}
     del m3sets
+    # S4D recurrent form and convolution kernel, the pages' efficiency-sweep shape
+    # (batch 8, d_model 256), 32 complex states, L 4096
+    Bs, Ds, Ns, Ls = 8, 256, 32, 4096
+    g = torch.Generator(device="cuda").manual_seed(40)
+    s4 = {"log_dt": torch.empty(Ds, device="cuda").uniform_(float(np.log(1e-3)), float(np.log(1e-1)),
+                                                              generator=g),
+          "A": torch.stack([torch.full((Ds, Ns), -0.5, device="cuda"),
+                            (np.pi * torch.arange(Ns, device="cuda", dtype=torch.float32)).expand(Ds, Ns)],
+                           dim=-1).contiguous(),
+          "B": torch.stack([torch.ones(Ds, Ns, device="cuda"), torch.zeros(Ds, Ns, device="cuda")],
+                           dim=-1).contiguous(),
+          "C": torch.randn(Ds, Ns, 2, device="cuda", generator=g),
+          "D": torch.randn(Ds, device="cuda", generator=g)}
+    us = [torch.randn(Bs, Ds, Ls, device="cuda", generator=g).to(torch.bfloat16) for _ in range(2)]
+    ys = torch.empty_like(us[0])
+
+    def fs(i):
+        ssm.ssm_s4d_scan_fwd(us[i % 2], s4["log_dt"], s4["A"], s4["B"], s4["C"], D=s4["D"], y=ys)
+    ts = time_launches(torch, fs, max(3, min(args.steps, 10)), 2, stream)
+    Kbuf = torch.empty((Ds, Ls), dtype=torch.float32, device="cuda")
+    tk = time_launches(torch, lambda i: ssm.ssm_s4d_kernel(s4["log_dt"], s4["A"], s4["B"], s4["C"],
+                                                           Ls, out=Kbuf), 3, 1, stream)
+    out["s4d_256"] = {"scan_ms": ts * 1e3, "state_updates_per_s": Bs * Ds * Ns * Ls / ts,
+                      "scan_hbm_gbs": Bs * Ds * Ls * 4 / ts / 1e9, "kernel_ms": tk * 1e3,
+                      "shape": f"batch {Bs}, dim {Ds}, N {Ns} complex, L {Ls}; bf16 u, y"}
+    del us, ys, Kbuf
     # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
     c3 = synth.WORKLOADS["m1_790m_long"]
     sweep = {}

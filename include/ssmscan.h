@@ -207,6 +207,45 @@ typedef struct {
 ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * S4D: linear time-invariant SSM, complex diagonal A, exact ZOH
+ *   ("From S4 to Mamba-3", 03/System, s4_minimal.py; Likely questions Q01)
+ *
+ * Per channel d and state n, Delta = exp(log_dt[d]) and z = Delta A[d,n]:
+ *   Abar = e^z,  Bbar = Delta B (e^z - 1)/z  (1 + z/2 + z^2/6 for |z| < 1e-4)
+ *   recurrent form:    h_t = Abar h_{t-1} + Bbar u_t,  y_t = Re sum_n C h_t + D u_t
+ *   convolution form:  K_l = Re sum_n C Bbar Abar^l,   y = K * u + D u
+ * The two are equal from a zero state (the pages' equivalence test).
+ *
+ * Shapes (Bt = batch, D = dim, N = dstate complex states, L = seqlen):
+ *   u, y          : [Bt, D, L]     in_dtype / out_dtype
+ *   log_dt        : [D]            float32
+ *   A, B, C       : [D, N, 2]      float32 complex (re, im)
+ *   D_skip        : [D]            float32 (nullable)
+ *   h0, h_final   : [Bt, D, N, 2]  float32 complex (nullable)
+ * Limits: dstate in {4, 8, 16, 32, 64} (else SSM_ERR_UNSUPPORTED).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int batch, dim, dstate, seqlen;
+    ssm_dtype in_dtype, out_dtype;
+    const void* u;
+    const float* log_dt;
+    const float* A;
+    const float* B;
+    const float* C;
+    const float* D_skip;
+    const float* h0;
+    void* y;
+    float* h_final;
+} ssm_s4d_params;
+
+/* The recurrent form over the whole sequence (batch, u, y, h0, h_final are used). */
+ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* stream);
+
+/* The convolution kernel K [dim, kernel_len] float32 (device pointer), from dim, dstate,
+ * log_dt, A, B and C of `p` (the other fields are ignored). */
+ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Mamba-2 chunked SSD scan (scalar A per head)
  *   ("From S4 to Mamba-3", 03/System, mamba2_minimal.py; 04/Approach)
  *

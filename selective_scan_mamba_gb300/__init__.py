@@ -260,6 +260,74 @@ def ssm_mamba3_scan_fwd(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_b
     return (y, h_final) if return_final_state else y
 
 
+def _complex_pairs(t, name, shape):
+    """float32 [..., 2] (re, im) view of a complex64 tensor, or a float32 [..., 2] tensor"""
+    torch = _torch()
+    if t is None:
+        return None
+    if t.is_complex():
+        t = torch.view_as_real(t.to(torch.complex64)).contiguous()
+    _ptr(t, name, tuple(shape) + (2,), torch.float32)
+    return t
+
+
+def _s4d_params(log_dt, A, B, C, D=None):
+    torch = _torch()
+    dim = log_dt.shape[0]
+    A_ = _complex_pairs(A, "A", (dim, A.shape[1]))
+    N = A_.shape[1]
+    p = _lib.S4dParams()
+    p.dim, p.dstate = dim, N
+    keep = [A_, _complex_pairs(B, "B", (dim, N)), _complex_pairs(C, "C", (dim, N))]
+    p.log_dt = _ptr(log_dt, "log_dt", (dim,), torch.float32)
+    p.A, p.B, p.C = (_ptr(k, n) for k, n in zip(keep, ("A", "B", "C")))
+    p.D_skip = _ptr(D, "D", (dim,), torch.float32)
+    return p, keep
+
+
+def ssm_s4d_scan_fwd(u, log_dt, A, B, C, D=None, h0=None, *, y=None, h_final=None,
+                     out_dtype=None, return_final_state=False, stream=None):
+    """S4D recurrent form (exact ZOH, Delta = exp(log_dt)).
+
+    u: [batch, dim, L] (bfloat16 or float32); log_dt: [dim] float32; A, B, C: [dim, N]
+    complex64 or [dim, N, 2] float32; D: [dim]; h0: [batch, dim, N] complex64 or
+    [batch, dim, N, 2] float32.  Returns y [batch, dim, L] and, when
+    ``return_final_state``, h_final [batch, dim, N, 2] float32.
+    """
+    torch = _torch()
+    batch, dim, L = u.shape
+    p, keep = _s4d_params(log_dt, A, B, C, D)
+    N = p.dstate
+    if y is None:
+        y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
+    if return_final_state and h_final is None:
+        h_final = torch.empty((batch, dim, N, 2), dtype=torch.float32, device=u.device)
+    h0_ = _complex_pairs(h0, "h0", (batch, dim, N))
+    p.batch, p.seqlen = batch, L
+    p.in_dtype = _dtype_code(u)
+    p.out_dtype = _dtype_code(y)
+    p.u = _ptr(u, "u")
+    p.h0 = _ptr(h0_, "h0")
+    p.y = _ptr(y, "y", (batch, dim, L))
+    p.h_final = _ptr(h_final, "h_final", (batch, dim, N, 2), torch.float32)
+    _lib.check(lib().ssm_s4d_scan_fwd(ctypes.byref(p), _stream(stream)))
+    del keep, h0_
+    return (y, h_final) if return_final_state else y
+
+
+def ssm_s4d_kernel(log_dt, A, B, C, kernel_len, *, out=None, stream=None):
+    """S4D convolution kernel K [dim, kernel_len] float32: K_l = Re sum_n C Bbar Abar^l."""
+    torch = _torch()
+    p, keep = _s4d_params(log_dt, A, B, C)
+    if out is None:
+        out = torch.empty((p.dim, int(kernel_len)), dtype=torch.float32, device=log_dt.device)
+    _lib.check(lib().ssm_s4d_kernel(ctypes.byref(p), _ptr(out, "K", (p.dim, int(kernel_len)),
+                                                         torch.float32), int(kernel_len),
+                                    _stream(stream)))
+    del keep
+    return out
+
+
 def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h_final, disc):
     torch = _torch()
     batch, L, H, P = x.shape

@@ -50,6 +50,12 @@ class Mamba3Params(ctypes.Structure):
                 ("D_skip", _fp), ("z", _vp), ("h0", _fp), ("y", _vp), ("h_final", _fp)]
 
 
+class S4dParams(ctypes.Structure):
+    _fields_ = [("batch", _i), ("dim", _i), ("dstate", _i), ("seqlen", _i), ("in_dtype", _i),
+                ("out_dtype", _i), ("u", _vp), ("log_dt", _fp), ("A", _fp), ("B", _fp),
+                ("C", _fp), ("D_skip", _fp), ("h0", _fp), ("y", _vp), ("h_final", _fp)]
+
+
 class SsdParams(ctypes.Structure):
     _fields_ = [("batch", _i), ("seqlen", _i), ("nheads", _i), ("headdim", _i), ("dstate", _i),
                 ("ngroups", _i), ("chunk_size", _i), ("in_dtype", _i), ("out_dtype", _i),
@@ -67,7 +73,8 @@ class StepParams(ctypes.Structure):
 
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
-           "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssd_chunk_scan_fwd",
+           "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd",
+           "ssm_s4d_kernel", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version")
 
@@ -100,6 +107,10 @@ def load(build_if_missing: bool = True):
             lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
             lib.ssm_mamba3_scan_fwd.restype = _i
             lib.ssm_mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Params), _vp]
+            lib.ssm_s4d_scan_fwd.restype = _i
+            lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp]
+            lib.ssm_s4d_kernel.restype = _i
+            lib.ssm_s4d_kernel.argtypes = [ctypes.POINTER(S4dParams), _vp, _i, _vp]
             lib.ssd_chunk_scan_fwd.restype = _i
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp, sz, _vp]
             lib.ssd_chunk_scan_workspace_size.restype = sz

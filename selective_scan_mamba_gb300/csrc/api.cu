@@ -146,6 +146,30 @@ ssm_status check_scan_bwd(const ssm_scan_bwd_params* p) {
     return SSM_OK;
 }
 
+ssm_status check_s4d_params(const ssm_s4d_params* p, bool scan) {
+    REQUIRE(p != nullptr, "params is NULL");
+    REQUIRE(p->dim >= 1 && p->dstate >= 1, "bad sizes: dim=%d dstate=%d", p->dim, p->dstate);
+    if (!ssm::s4d_supported(p->dstate))
+        return fail(SSM_ERR_UNSUPPORTED, "s4d: dstate=%d (4, 8, 16, 32 or 64 supported)", p->dstate);
+    REQUIRE_PTR(p->log_dt, "log_dt");
+    REQUIRE_PTR(p->A, "A");
+    REQUIRE_PTR(p->B, "B");
+    REQUIRE_PTR(p->C, "C");
+    if (!scan) return SSM_OK;
+    REQUIRE(p->batch >= 1 && p->seqlen >= 0, "bad sizes: batch=%d seqlen=%d", p->batch, p->seqlen);
+    REQUIRE(dtype_ok(p->in_dtype) && dtype_ok(p->out_dtype), "unknown dtype");
+    REQUIRE(static_cast<long long>(p->batch) * p->dim * (p->seqlen > 0 ? p->seqlen : 1) < (1LL << 40),
+            "tensor too large");
+    OPTIONAL_PTR(p->D_skip, "D_skip");
+    OPTIONAL_PTR(p->h0, "h0");
+    OPTIONAL_PTR(p->h_final, "h_final");
+    if (p->seqlen > 0) {
+        REQUIRE_PTR(p->u, "u");
+        REQUIRE_PTR(p->y, "y");
+    }
+    return SSM_OK;
+}
+
 ssm::M1Args scan_args(const ssm_scan_params* p) {
     ssm::M1Args a;
     a.batch = p->batch;
@@ -300,6 +324,40 @@ ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream) {
     }
     cudaError_t e = ssm::m3_launch(*p, s);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_mamba3_scan_fwd launch");
+    return SSM_OK;
+}
+
+
+ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_s4d_params(p, true);
+    if (st != SSM_OK) return st;
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->seqlen == 0) {
+        if (p->h_final) {
+            const size_t bytes = static_cast<size_t>(p->batch) * p->dim * p->dstate * 2 * sizeof(float);
+            cudaError_t e = p->h0 ? cudaMemcpyAsync(p->h_final, p->h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(p->h_final, 0, bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_scan_fwd (empty sequence)");
+        }
+        return SSM_OK;
+    }
+    cudaError_t e = ssm::s4d_launch(*p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_scan_fwd launch");
+    return SSM_OK;
+}
+
+ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_s4d_params(p, false);
+    if (st != SSM_OK) return st;
+    REQUIRE(kernel_len >= 0, "kernel_len=%d", kernel_len);
+    if (p->dim > 65535) return fail(SSM_ERR_UNSUPPORTED, "s4d kernel: dim=%d > 65535", p->dim);
+    if (kernel_len > 0) REQUIRE_PTR(K, "K");
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaError_t e = ssm::s4d_kernel_launch(*p, K, kernel_len, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_kernel launch");
     return SSM_OK;
 }
 

@@ -40,6 +40,11 @@ cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s);
 bool m3_supported(int dstate);
 cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s);
 
+// S4D (s4d.cu)
+bool s4d_supported(int dstate);
+cudaError_t s4d_launch(const ssm_s4d_params& a, cudaStream_t s);
+cudaError_t s4d_kernel_launch(const ssm_s4d_params& a, float* K, int L, cudaStream_t s);
+
 struct M1Plan {
     enum Kind { kGeneric = 0, kTiled = 1, kTma = 2, kTmem = 3 } kind;
     int tpc;      // threads per channel (tiled path)

@@ -233,3 +233,22 @@ def test_mamba3_rejects_bad_arguments(lib, field, value, status):
     p = mamba3_params(**{field: value})
     assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), None) == status
     assert lib.ssm_last_error()
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dstate", 6, _lib.SSM_ERR_UNSUPPORTED),
+    ("log_dt", None, _lib.SSM_ERR_INVALID_ARG),
+    ("C", FAKE + 8, _lib.SSM_ERR_INVALID_ARG),
+    ("u", None, _lib.SSM_ERR_INVALID_ARG),
+    ("batch", 0, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_s4d_rejects_bad_arguments(lib, field, value, status):
+    p = _lib.S4dParams()
+    p.batch, p.dim, p.dstate, p.seqlen = 2, 16, 32, 64
+    p.in_dtype = p.out_dtype = _lib.SSM_BF16
+    for f in ("u", "log_dt", "A", "B", "C", "y"):
+        setattr(p, f, FAKE)
+    setattr(p, field, value)
+    assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), None) == status
+    if field in ("dstate", "log_dt", "C"):
+        assert lib.ssm_s4d_kernel(ctypes.byref(p), FAKE, 16, None) == status

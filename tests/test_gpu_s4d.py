@@ -1,0 +1,116 @@
+"""GPU parity of S4D (ssm_s4d_scan_fwd, ssm_s4d_kernel) against the float64 oracle, whose
+recurrent and FFT-convolution forms are pinned equal.
+
+Tolerances: the kernel K is computed in double precision per element and rounded, so it
+is held to 1e-6 of max|K|.  The recurrence runs in float32 with Abar rounded to float32;
+its relative error grows with the memory length ~1/(Delta |Re A|) of the slowest state
+(up to 2000 steps at Delta = 1e-3, Re A = -1/2), so float32 inputs are held to 1e-4 and
+bfloat16 inputs to 2e-3 of max|y|."""
+import numpy as np
+import pytest
+
+import selective_scan_mamba_gb300 as ssm
+from selective_scan_mamba_gb300 import synth
+from tests.helpers import TOL_BF16, check, to_numpy
+
+pytestmark = pytest.mark.gpu
+TOL_S4D_F32 = 1e-4
+
+
+@pytest.fixture(autouse=True)
+def _needs_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def _params(dim, N, seed):
+    """S4D-Lin: A_n = -1/2 + i pi n, log Delta uniform on [ln 1e-3, ln 1e-1], B = 1,
+    C complex normal, D normal."""
+    rng = np.random.default_rng(seed)
+    A = np.broadcast_to(-0.5 + 1j * np.pi * np.arange(N), (dim, N)).astype(np.complex128)
+    log_dt = rng.uniform(np.log(1e-3), np.log(1e-1), dim)
+    B = np.ones((dim, N), np.complex128)
+    C = rng.standard_normal((dim, N)) + 1j * rng.standard_normal((dim, N))
+    D = rng.standard_normal(dim)
+    return log_dt, A, B, C, D
+
+
+def _dev_params(log_dt, A, B, C, D):
+    import torch
+
+    def pairs(a):
+        return torch.from_numpy(np.ascontiguousarray(np.stack([a.real, a.imag], -1), np.float32)).cuda()
+    return (torch.from_numpy(log_dt.astype(np.float32)).cuda(), pairs(A), pairs(B), pairs(C),
+            torch.from_numpy(D.astype(np.float32)).cuda())
+
+
+def _run(oracle, batch, dim, N, L, bf16, h0=True, seed=0):
+    import torch
+    log_dt, A, B, C, D = _params(dim, N, seed)
+    # the device sees float32 parameters: the oracle reads the same rounded values
+    log_dt, D = log_dt.astype(np.float32).astype(np.float64), D.astype(np.float32).astype(np.float64)
+    C = C.astype(np.complex64).astype(np.complex128)
+    A = A.astype(np.complex64).astype(np.complex128)
+    rng = np.random.default_rng(seed + 1)
+    u = rng.standard_normal((batch, dim, L)).astype(np.float32)
+    if bf16:
+        bits = synth.bf16_bits(u)
+        u = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+        ut = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    else:
+        ut = torch.from_numpy(u).cuda()
+    h0c = (rng.standard_normal((batch, dim, N)) + 1j * rng.standard_normal((batch, dim, N))
+           ).astype(np.complex64) if h0 else None
+    dl, dA, dB, dC, dD = _dev_params(log_dt, A, B, C, D)
+    y, hf = ssm.ssm_s4d_scan_fwd(ut, dl, dA, dB, dC, D=dD,
+                                 h0=None if h0c is None else torch.from_numpy(h0c).cuda(),
+                                 out_dtype=torch.float32, return_final_state=True)
+    torch.cuda.synchronize()
+    yr, hr = oracle.s4d_recurrent(u.astype(np.float64), log_dt, A, B, C, D=D,
+                                  h0=None if h0c is None else h0c.astype(np.complex128))
+    tol = TOL_BF16 if bf16 else TOL_S4D_F32
+    check(to_numpy(y), yr, tol, what="y")
+    hf = to_numpy(hf)
+    check(np.stack([hf[..., 0], hf[..., 1]]), np.stack([hr.real, hr.imag]), tol, what="h_final")
+    return u, (log_dt, A, B, C, D), to_numpy(y)
+
+
+@pytest.mark.parametrize("N", [4, 16, 64])
+def test_recurrent_fp32(oracle_mod, N):
+    _run(oracle_mod, 2, 40 if N < 64 else 20, N, 300, False)
+
+
+def test_recurrent_bf16_long(oracle_mod):
+    _run(oracle_mod, 1, 64, 32, 1500, True, seed=3)
+
+
+def test_recurrent_equals_fft_convolution(oracle_mod):
+    """From a zero state the GPU recurrence equals the oracle's FFT convolution form."""
+    u, (log_dt, A, B, C, D), y = _run(oracle_mod, 2, 16, 32, 257, False, h0=False, seed=5)
+    yc = oracle_mod.s4d_fft_conv(u.astype(np.float64), log_dt, A, B, C, D=D)
+    check(y, yc, TOL_S4D_F32, what="y vs FFT convolution")
+
+
+@pytest.mark.parametrize("L", [1, 100, 4096])
+def test_kernel(oracle_mod, L):
+    import torch
+    log_dt, A, B, C, D = _params(24, 32, 7)
+    log_dt = log_dt.astype(np.float32).astype(np.float64)
+    C = C.astype(np.complex64).astype(np.complex128)
+    dl, dA, dB, dC, _ = _dev_params(log_dt, A, B, C, D)
+    K = ssm.ssm_s4d_kernel(dl, dA, dB, dC, L)
+    torch.cuda.synchronize()
+    Kr = oracle_mod.s4d_kernel(log_dt, A.astype(np.complex64).astype(np.complex128), B, C, L)
+    check(to_numpy(K), Kr, 1e-6, what="K")
+
+
+def test_empty_sequence_copies_state():
+    import torch
+    log_dt, A, B, C, D = _params(8, 16, 1)
+    dl, dA, dB, dC, dD = _dev_params(log_dt, A, B, C, D)
+    h0 = torch.randn(2, 8, 16, 2, device="cuda")
+    u = torch.empty((2, 8, 0), device="cuda")
+    _, hf = ssm.ssm_s4d_scan_fwd(u, dl, dA, dB, dC, D=dD, h0=h0, return_final_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(hf, h0)
