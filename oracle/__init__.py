@@ -321,6 +321,49 @@ def ssd_sequential(x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=Tru
     return y, hf
 
 
+def ssd_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
+            dh_final=None):
+    """Gradients of sum(dy * y) + sum(dh_final * h_final) for ssd_sequential
+    (exponential-Euler).  With a scalar A per head the Mamba-2 recurrence is the Mamba-1
+    scan over the H*P channels of the heads, A tied across each head's channels and
+    states and Delta shared by a head's P channels ("From S4 to Mamba-3", 03/System,
+    mamba2_minimal.py), so its derivative is mamba1_scan_bwd on that view with the tied
+    gradients summed.  Layouts as ssd_sequential; returns dx, ddt [batch, L, H], dA [H],
+    dB, dC [batch, L, G, N], dh0 [batch, H, P, N] and dD, dz, ddt_bias for the inputs
+    given."""
+    x, dt, A, B, C, D, z, dt_bias, h0, (batch, L, H, P, G, N) = _ssd_args(
+        x, dt, A, B, C, D, z, dt_bias, h0)
+    dy = _f64(dy, (batch, L, H, P))
+    dh_final = _f64(dh_final, (batch, H, P, N))
+
+    def chan(a):  # [batch, L, H, P] -> [batch, H*P, L]
+        return None if a is None else np.ascontiguousarray(a.reshape(batch, L, H * P).transpose(0, 2, 1))
+    rep = lambda v: None if v is None else np.repeat(v, P)  # noqa: E731  [H] -> [H*P]
+    g = mamba1_scan_bwd(
+        chan(x), np.ascontiguousarray(np.repeat(dt, P, axis=2).transpose(0, 2, 1)),
+        np.repeat(A[:, None], P * N).reshape(H * P, N),
+        np.ascontiguousarray(B.transpose(0, 2, 3, 1)), np.ascontiguousarray(C.transpose(0, 2, 3, 1)),
+        chan(dy), D=rep(D), z=chan(z), delta_bias=rep(dt_bias), delta_softplus=dt_softplus,
+        h0=None if h0 is None else h0.reshape(batch, H * P, N),
+        dh_final=None if dh_final is None else dh_final.reshape(batch, H * P, N))
+
+    def back(a):  # [batch, H*P, L] -> [batch, L, H, P]
+        return np.ascontiguousarray(a.transpose(0, 2, 1).reshape(batch, L, H, P))
+    out = {"dx": back(g["dx"]),
+           "ddt": g["ddelta"].reshape(batch, H, P, L).sum(axis=2).transpose(0, 2, 1).copy(),
+           "dA": g["dA"].reshape(H, P * N).sum(axis=1),
+           "dB": np.ascontiguousarray(g["dB"].transpose(0, 3, 1, 2)),
+           "dC": np.ascontiguousarray(g["dC"].transpose(0, 3, 1, 2)),
+           "dh0": g["dh0"].reshape(batch, H, P, N)}
+    if D is not None:
+        out["dD"] = g["dD"].reshape(H, P).sum(axis=1)
+    if z is not None:
+        out["dz"] = back(g["dz"])
+    if dt_bias is not None:
+        out["ddt_bias"] = g["ddelta_bias"].reshape(H, P).sum(axis=1)
+    return out
+
+
 def ssd_chunked(x, dt, A, B, C, chunk, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
                 disc=DISC_EXP_EULER):
     """Mamba-2 chunked SSD with chunk size ``chunk``; same layouts as ssd_sequential."""

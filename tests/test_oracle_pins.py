@@ -682,3 +682,39 @@ def test_s4d_dc_gain(oracle_mod):
     y, _ = oracle_mod.s4d_recurrent(np.ones((1, 1, L)), np.array([np.log(dt)]), np.array([[a + 0j]]),
                                     np.array([[2.0 + 0j]]), np.array([[1.5 + 0j]]))
     assert abs(y[0, 0, -1] - (-1.5 * 2.0 / a)) < 1e-12
+
+
+# ----------------------------------------------------------------------------------------
+# SSD backward: finite differences of the sequential SSD oracle (a separate C routine)
+# ----------------------------------------------------------------------------------------
+SSD_GRAD_OF = {"x": "dx", "dt": "ddt", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+               "dt_bias": "ddt_bias", "h0": "dh0"}
+
+
+@pytest.mark.parametrize("gated,softplus", [(True, True), (False, False)])
+def test_ssd_bwd_finite_differences(oracle_mod, gated, softplus):
+    rng = np.random.default_rng(31)
+    batch, L, H, P, G, N = 2, 6, 4, 3, 2, 5
+    inp = {"x": rng.standard_normal((batch, L, H, P)),
+           "dt": (np.abs(rng.standard_normal((batch, L, H))) * 0.5 + 0.05) if not softplus
+           else 0.7 * rng.standard_normal((batch, L, H)),
+           "A": -np.exp(0.5 * rng.standard_normal(H)),
+           "B": rng.standard_normal((batch, L, G, N)), "C": rng.standard_normal((batch, L, G, N)),
+           "D": rng.standard_normal(H), "z": rng.standard_normal((batch, L, H, P)) if gated else None,
+           "dt_bias": np.abs(0.3 * rng.standard_normal(H)), "h0": rng.standard_normal((batch, H, P, N))}
+    dy = rng.standard_normal((batch, L, H, P))
+    dhf = rng.standard_normal((batch, H, P, N))
+
+    def loss(args):
+        y, hf = oracle_mod.ssd_sequential(**args, dt_softplus=softplus)
+        return float((dy * y).sum() + (dhf * hf).sum())
+
+    grads = oracle_mod.ssd_bwd(**inp, dy=dy, dh_final=dhf, dt_softplus=softplus)
+    eps = 1e-6
+    for name, val in inp.items():
+        if val is None:
+            continue
+        v = rng.standard_normal(val.shape)
+        fd = (loss(dict(inp, **{name: val + eps * v})) - loss(dict(inp, **{name: val - eps * v}))) / (2 * eps)
+        an = float((grads[SSD_GRAD_OF[name]] * v).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
