@@ -138,7 +138,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t worksp
  *   dD_skip     : [D]           (required exactly when fwd.D_skip is given)
  *   ddelta_bias : [D]           (required exactly when fwd.delta_bias is given)
  *   dh0         : [Bt, D, N]    (nullable: not written)
- * Limits: exponential-Euler only and dstate in {16, 32, 64} (else SSM_ERR_UNSUPPORTED).
+ * Limits: exponential-Euler only and dstate in {16, 32, 64, 128} (else SSM_ERR_UNSUPPORTED).
  * The result does not depend on launch order (partial sums are added in a fixed order).
  * ------------------------------------------------------------------------- */
 typedef struct {
@@ -372,6 +372,51 @@ ssm_status ssm_state_update(const ssm_step_params* p, void* stream);
  * ssm_state_update.  ntokens = 1 equals ssm_state_update.
  * ------------------------------------------------------------------------- */
 ssm_status ssm_state_update_tokens(const ssm_step_params* p, int ntokens, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Mamba-2 SSD backward: the reverse-mode derivative of the SSD scan
+ *   (same passages as ssm_scan_bwd; mamba2_minimal.py for the scalar-A form)
+ *
+ * With a scalar A per head the SSD recurrence is the Mamba-1 scan over the H*P channels
+ * of the heads, A tied across a head's channels and states and Delta, D and dt_bias
+ * shared by its P channels; the gradients are those of ssm_scan_bwd on that view, the
+ * tied ones summed (dA over the batch, the head's channels and the states; ddt over the
+ * head's channels).  The derivative is of the recurrence, so it does not depend on the
+ * chunk size of the forward call (fwd.chunk_size, y and h_final are ignored).
+ *
+ * Shapes as ssd_chunk_scan_fwd; every gradient is float32 and is written:
+ *   dy          : [Bt, L, H, P]  fwd.out_dtype
+ *   dh_final    : [Bt, H, P, N]  (nullable: zero)
+ *   dx          : [Bt, L, H, P]
+ *   ddt         : [Bt, L, H]
+ *   dz          : [Bt, L, H, P]  (required exactly when fwd.z is given)
+ *   dA          : [H]
+ *   dB, dC      : [Bt, L, G, N]
+ *   dD_skip     : [H]            (required exactly when fwd.D_skip is given)
+ *   ddt_bias    : [H]            (required exactly when fwd.dt_bias is given)
+ *   dh0         : [Bt, H, P, N]  (nullable: not written)
+ * Limits: exponential-Euler only, dstate in {16, 32, 64, 128}.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    ssd_params fwd;
+    const void* dy;
+    const float* dh_final;
+    float* dx;
+    float* ddt;
+    float* dz;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD_skip;
+    float* ddt_bias;
+    float* dh0;
+} ssd_bwd_params;
+
+/* Device scratch for ssd_scan_bwd in bytes (0 when invalid or unsupported). */
+size_t ssd_scan_bwd_workspace_size(const ssd_bwd_params* p);
+
+ssm_status ssd_scan_bwd(const ssd_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* ssm_last_error(void);

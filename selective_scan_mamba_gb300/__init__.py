@@ -354,6 +354,50 @@ def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h
     return p
 
 
+def ssd_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
+                 dh_final=None, *, return_dh0=True, workspace=None, stream=None):
+    """Backward of the SSD scan (exponential-Euler, dstate 16, 32, 64 or 128).
+
+    Same inputs as ssd_chunk_scan_fwd plus dy [batch, L, H, P] and the optional dh_final
+    [batch, H, P, N] float32.  Returns a dict of float32 gradients: dx [batch, L, H, P],
+    ddt [batch, L, H], dA [H], dB, dC [batch, L, G, N], and dD, dz, ddt_bias for the
+    inputs given, dh0 [batch, H, P, N] when ``return_dh0``.
+    """
+    torch = _torch()
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    f32, dev = torch.float32, x.device
+    p = _lib.SsdBwdParams()
+    # forward parameters; chunk size, y and h_final are ignored by the backward
+    p.fwd = _ssd_params(x, dt, A, B, C, 64, D, z, dt_bias, dt_softplus, h0, dy, None, "exp_euler")
+    out = {"dx": torch.empty((batch, L, H, P), dtype=f32, device=dev),
+           "ddt": torch.empty((batch, L, H), dtype=f32, device=dev),
+           "dA": torch.empty((H,), dtype=f32, device=dev),
+           "dB": torch.empty((batch, L, G, N), dtype=f32, device=dev),
+           "dC": torch.empty((batch, L, G, N), dtype=f32, device=dev)}
+    if D is not None:
+        out["dD"] = torch.empty((H,), dtype=f32, device=dev)
+    if z is not None:
+        out["dz"] = torch.empty((batch, L, H, P), dtype=f32, device=dev)
+    if dt_bias is not None:
+        out["ddt_bias"] = torch.empty((H,), dtype=f32, device=dev)
+    if return_dh0:
+        out["dh0"] = torch.empty((batch, H, P, N), dtype=f32, device=dev)
+    p.dy = _ptr(dy, "dy", (batch, L, H, P))
+    p.dh_final = _ptr(dh_final, "dh_final", (batch, H, P, N), f32)
+    for name, field in (("dx", "dx"), ("ddt", "ddt"), ("dz", "dz"), ("dA", "dA"), ("dB", "dB"),
+                        ("dC", "dC"), ("dD", "dD_skip"), ("ddt_bias", "ddt_bias"), ("dh0", "dh0")):
+        setattr(p, field, _ptr(out.get(name), name))
+    need = int(lib().ssd_scan_bwd_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    _lib.check(lib().ssd_scan_bwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
 def ssd_chunk_scan_workspace_size(x, B, chunk_size) -> int:
     """Scratch bytes ssd_chunk_scan_fwd needs for these shapes and chunk size."""
     p = _lib.SsdParams()

@@ -64,6 +64,12 @@ class SsdParams(ctypes.Structure):
                 ("h_final", _fp), ("disc", _i)]
 
 
+class SsdBwdParams(ctypes.Structure):
+    _fields_ = [("fwd", SsdParams), ("dy", _vp), ("dh_final", _fp), ("dx", _fp), ("ddt", _fp),
+                ("dz", _fp), ("dA", _fp), ("dB", _fp), ("dC", _fp), ("dD_skip", _fp),
+                ("ddt_bias", _fp), ("dh0", _fp)]
+
+
 class StepParams(ctypes.Structure):
     _fields_ = [("batch", _i), ("nheads", _i), ("headdim", _i), ("dstate", _i), ("ngroups", _i),
                 ("a_per_state", _i), ("in_dtype", _i), ("out_dtype", _i),
@@ -74,7 +80,7 @@ class StepParams(ctypes.Structure):
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
            "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd",
-           "ssm_s4d_kernel", "ssd_chunk_scan_fwd",
+           "ssm_s4d_kernel", "ssd_scan_bwd", "ssd_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version")
 
@@ -111,6 +117,10 @@ def load(build_if_missing: bool = True):
             lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp]
             lib.ssm_s4d_kernel.restype = _i
             lib.ssm_s4d_kernel.argtypes = [ctypes.POINTER(S4dParams), _vp, _i, _vp]
+            lib.ssd_scan_bwd.restype = _i
+            lib.ssd_scan_bwd.argtypes = [ctypes.POINTER(SsdBwdParams), _vp, sz, _vp]
+            lib.ssd_scan_bwd_workspace_size.restype = sz
+            lib.ssd_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(SsdBwdParams)]
             lib.ssd_chunk_scan_fwd.restype = _i
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SsdParams), _vp, sz, _vp]
             lib.ssd_chunk_scan_workspace_size.restype = sz

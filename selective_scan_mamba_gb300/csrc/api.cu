@@ -109,7 +109,7 @@ ssm_status check_scan_bwd_sizes(const ssm_scan_bwd_params* p) {
     if (p->fwd.disc != SSM_DISC_EXP_EULER)
         return fail(SSM_ERR_UNSUPPORTED, "backward: exponential-Euler only");
     if (!ssm::m1_bwd_supported(*p))
-        return fail(SSM_ERR_UNSUPPORTED, "backward: dstate=%d (16, 32 or 64 supported)", p->fwd.dstate);
+        return fail(SSM_ERR_UNSUPPORTED, "backward: dstate=%d (16, 32, 64 or 128 supported)", p->fwd.dstate);
     return SSM_OK;
 }
 
@@ -166,6 +166,57 @@ ssm_status check_s4d_params(const ssm_s4d_params* p, bool scan) {
     if (p->seqlen > 0) {
         REQUIRE_PTR(p->u, "u");
         REQUIRE_PTR(p->y, "y");
+    }
+    return SSM_OK;
+}
+
+ssm_status check_ssd_bwd_sizes(const ssd_bwd_params* p) {
+    REQUIRE(p != nullptr, "params is NULL");
+    const ssd_params* f = &p->fwd;
+    REQUIRE(f->batch >= 1 && f->seqlen >= 0 && f->nheads >= 1 && f->headdim >= 1 && f->dstate >= 1 &&
+                f->ngroups >= 1,
+            "bad sizes: batch=%d seqlen=%d nheads=%d headdim=%d dstate=%d ngroups=%d", f->batch,
+            f->seqlen, f->nheads, f->headdim, f->dstate, f->ngroups);
+    REQUIRE(f->nheads % f->ngroups == 0, "ngroups=%d does not divide nheads=%d", f->ngroups, f->nheads);
+    REQUIRE(dtype_ok(f->in_dtype) && dtype_ok(f->out_dtype), "unknown dtype");
+    REQUIRE(static_cast<long long>(f->batch) * f->seqlen * f->nheads * f->headdim < (1LL << 40),
+            "tensor too large");
+    if (static_cast<long long>(f->nheads) * f->headdim > (1 << 24))
+        return fail(SSM_ERR_UNSUPPORTED, "nheads*headdim too large");
+    if (f->disc != SSM_DISC_EXP_EULER) return fail(SSM_ERR_UNSUPPORTED, "backward: exponential-Euler only");
+    if (!ssm::ssd_bwd_supported(*p))
+        return fail(SSM_ERR_UNSUPPORTED, "backward: dstate=%d (16, 32, 64 or 128 supported)", f->dstate);
+    return SSM_OK;
+}
+
+ssm_status check_ssd_bwd(const ssd_bwd_params* p) {
+    ssm_status st = check_ssd_bwd_sizes(p);
+    if (st != SSM_OK) return st;
+    const ssd_params* f = &p->fwd;
+    REQUIRE_PTR(f->A, "A");
+    REQUIRE_PTR(p->dA, "dA");
+    OPTIONAL_PTR(f->h0, "h0");
+    OPTIONAL_PTR(p->dh_final, "dh_final");
+    OPTIONAL_PTR(p->dh0, "dh0");
+    REQUIRE((f->D_skip == nullptr) == (p->dD_skip == nullptr), "dD_skip must be given exactly when D_skip is");
+    REQUIRE((f->dt_bias == nullptr) == (p->ddt_bias == nullptr), "ddt_bias must be given exactly when dt_bias is");
+    REQUIRE((f->z == nullptr) == (p->dz == nullptr), "dz must be given exactly when z is");
+    OPTIONAL_PTR(f->D_skip, "D_skip");
+    OPTIONAL_PTR(f->dt_bias, "dt_bias");
+    OPTIONAL_PTR(p->dD_skip, "dD_skip");
+    OPTIONAL_PTR(p->ddt_bias, "ddt_bias");
+    if (f->seqlen > 0) {
+        REQUIRE_PTR(f->x, "x");
+        REQUIRE_PTR(f->dt, "dt");
+        REQUIRE_PTR(f->B, "B");
+        REQUIRE_PTR(f->C, "C");
+        REQUIRE_PTR(p->dy, "dy");
+        REQUIRE_PTR(p->dx, "dx");
+        REQUIRE_PTR(p->ddt, "ddt");
+        REQUIRE_PTR(p->dB, "dB");
+        REQUIRE_PTR(p->dC, "dC");
+        OPTIONAL_PTR(f->z, "z");
+        OPTIONAL_PTR(p->dz, "dz");
     }
     return SSM_OK;
 }
@@ -358,6 +409,27 @@ ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, voi
     if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
     cudaError_t e = ssm::s4d_kernel_launch(*p, K, kernel_len, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_kernel launch");
+    return SSM_OK;
+}
+
+size_t ssd_scan_bwd_workspace_size(const ssd_bwd_params* p) {
+    if (check_ssd_bwd_sizes(p) != SSM_OK) return 0;
+    return ssm::ssd_bwd_workspace_size(*p);
+}
+
+ssm_status ssd_scan_bwd(const ssd_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    g_err[0] = '\0';
+    ssm_status st = check_ssd_bwd(p);
+    if (st != SSM_OK) return st;
+    const size_t need = ssm::ssd_bwd_workspace_size(*p);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    cudaError_t e = ssm::ssd_bwd_launch(*p, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssd_scan_bwd launch");
     return SSM_OK;
 }
 

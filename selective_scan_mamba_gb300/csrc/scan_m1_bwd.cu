@@ -25,6 +25,12 @@
 //   - dB, dC partial sums per CTA and dA, dD, dbias partial sums per batch row go to the
 //     workspace; the second launch adds them up, so the result does not depend on the
 //     order in which CTAs run.
+// The same kernels serve the Mamba-2 SSD backward: with a scalar A per head its
+// recurrence is this scan over the H*P channels of the heads, A tied over a head's
+// channels and states and Delta, D and the bias shared by its P channels.  A BwdView
+// carries the element strides of either layout and `hp`, the channels per head; with
+// hp > 1 the per-channel d(delta) goes to the workspace and the second launch sums each
+// head's P channels (and A over the states too).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -60,7 +66,7 @@ struct BwdLayout {  // float offsets into dynamic shared memory (16-byte aligned
 };
 
 struct BwdWs {  // byte offsets into the workspace
-    size_t ckpt, part_bc, part_a, part_d, part_bias, bytes;
+    size_t ckpt, part_bc, part_a, part_d, part_bias, dd_chan, bytes;
 };
 
 __host__ __device__ inline int bwd_cpb(int tpc) { return kBThreads / tpc; }
@@ -72,16 +78,35 @@ __device__ __forceinline__ float ldf(const T* p, size_t i) {
 
 __device__ __forceinline__ float sigmoid_fast(float v) { return rcp_approx(1.f + ex2_approx(-v * SSM_LOG2E)); }
 
+}  // namespace
+
+// Operands of one backward call in either layout (element strides; see the file comment).
+struct BwdView {
+    const void *x, *delta, *z, *B, *C, *dy;
+    const float *delta_bias, *A, *D_skip, *h0, *dh_final;
+    float *dx, *ddelta, *dz, *dh0;             // per (b, channel, t) / per state outputs
+    float *dA, *dB, *dC, *dD, *dbias;          // reduced outputs
+    int batch, dim, dstate, seqlen, ngroups, softplus;
+    ssm_dtype in_dtype, dy_dtype;
+    int hp;                                    // channels per head (1: Mamba-1)
+    long long sxb, sxd, sxt;                   // x, z, dy, dx, dz: batch, channel, step
+    long long sdb, sdh, sdt;                   // delta and its gradient: batch, head, step
+    long long sbb, sbg, sbn, sbt;              // B, C, dB, dC: batch, group, state, step
+    long long sah, san;                        // A: head, state (san = 0: one A per head)
+};
+
+namespace {
+
 template <typename Tin, typename Tdy, int TPC>
 __global__ void __launch_bounds__(kBThreads, 4)
-    m1_scan_bwd(M1BwdArgs a, int cps, float* ckpt, float* part_bc, float* part_a, float* part_d,
-                float* part_bias) {
+    m1_scan_bwd(BwdView a, int cps, float* ckpt, float* part_bc, float* part_a, float* part_d,
+                float* part_bias, float* dd_chan) {
     constexpr int N = TPC * kBS;
     constexpr int CPB = kBThreads / TPC;
     constexpr int NQ = kBT * N / 4;         // (step, 4 states) cells of a chunk
     // channel slices summed in parallel per cell (1: each thread sums whole cells)
     constexpr int SPLIT = NQ < kBThreads ? kBThreads / NQ : 1;
-    const int L = a.fwd.seqlen, Dm = a.fwd.dim, G = a.fwd.ngroups;
+    const int L = a.seqlen, Dm = a.dim, G = a.ngroups;
     const int per_group = Dm / G;
     const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
     const int b = pair / G, g = pair % G;
@@ -99,35 +124,40 @@ __global__ void __launch_bounds__(kBThreads, 4)
     const bool active = c < nchan;
     const int d = d0 + (active ? c : 0);
     const size_t row = static_cast<size_t>(b) * Dm + d;  // (b, d)
-    const Tin* X = static_cast<const Tin*>(a.fwd.x);
-    const Tin* DL = static_cast<const Tin*>(a.fwd.delta);
-    const Tin* Z = static_cast<const Tin*>(a.fwd.z);
-    const Tin* Bp = static_cast<const Tin*>(a.fwd.B);
-    const Tin* Cp = static_cast<const Tin*>(a.fwd.C);
+    const Tin* X = static_cast<const Tin*>(a.x);
+    const Tin* DL = static_cast<const Tin*>(a.delta);
+    const Tin* Z = static_cast<const Tin*>(a.z);
+    const Tin* Bp = static_cast<const Tin*>(a.B);
+    const Tin* Cp = static_cast<const Tin*>(a.C);
     const Tdy* DY = static_cast<const Tdy*>(a.dy);
-    const size_t bc_base = (static_cast<size_t>(b) * G + g) * N * static_cast<size_t>(L);
+    const long long bc_base = b * a.sbb + g * a.sbg;
+    // element (b, channel cc of the CTA, step t) of x, z, dy, dx, dz and of delta
+    auto xi = [&](int cc, int t) { return b * a.sxb + (d0 + cc) * a.sxd + t * a.sxt; };
+    auto di = [&](int cc, int t) { return b * a.sdb + ((d0 + cc) / a.hp) * a.sdh + t * a.sdt; };
+    // staging order: consecutive threads take consecutive addresses of the layout
+    const bool tfast = a.sxt == 1, bt_fast = a.sbt == 1;
 
     float Av[kBS], A2[kBS];  // A, and A log2(e) for the exponentials
 #pragma unroll
     for (int i = 0; i < kBS; ++i) {
-        Av[i] = a.fwd.A[static_cast<size_t>(d) * N + kBS * gi + i];
+        Av[i] = a.A[(d / a.hp) * a.sah + (kBS * gi + i) * a.san];
         A2[i] = Av[i] * SSM_LOG2E;
     }
-    const float Dd = a.fwd.D_skip ? a.fwd.D_skip[d] : 0.f;
+    const float Dd = a.D_skip ? a.D_skip[d / a.hp] : 0.f;
 
     // stage Delta (and Delta x, x, sigmoid, dL/do, z) of the CTA's channels and B (C)
     // for a chunk
     auto stage = [&](int t0, int tl, bool full) {
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
-            const int cc = j / kBT, t = j % kBT;
+            const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
             float dl = 0.f, xv = 0.f, sgv = 1.f, dov = 0.f, zv = 0.f;
             if (cc < nchan && t < tl) {
-                const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
-                const float v = ldf(DL, i) + (a.fwd.delta_bias ? a.fwd.delta_bias[d0 + cc] : 0.f);
-                dl = a.fwd.delta_softplus ? softplus_fast(v) : v;
+                const long long i = xi(cc, t0 + t);
+                const float v = ldf(DL, di(cc, t0 + t)) + (a.delta_bias ? a.delta_bias[(d0 + cc) / a.hp] : 0.f);
+                dl = a.softplus ? softplus_fast(v) : v;
                 xv = ldf(X, i);
                 if (full) {
-                    sgv = a.fwd.delta_softplus ? sigmoid_fast(v) : 1.f;
+                    sgv = a.softplus ? sigmoid_fast(v) : 1.f;
                     dov = ldf(DY, i);
                     if (Z) {
                         zv = ldf(Z, i);
@@ -145,8 +175,8 @@ __global__ void __launch_bounds__(kBThreads, 4)
             }
         }
         for (int j = tid; j < N * kBT; j += kBThreads) {
-            const int n = j / kBT, t = j % kBT;
-            const size_t i = bc_base + static_cast<size_t>(n) * L + t0 + t;
+            const int n = bt_fast ? j / kBT : j % N, t = bt_fast ? j % kBT : j / N;
+            const long long i = bc_base + n * a.sbn + (t0 + t) * a.sbt;
             sm[lay.bs + t * N + n] = t < tl ? ldf(Bp, i) : 0.f;
             if (full) sm[lay.cs + t * N + n] = t < tl ? ldf(Cp, i) : 0.f;
         }
@@ -195,7 +225,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
     // pass 1: checkpoints h_{t0 - 1} of every chunk
     float h[kBS];
 #pragma unroll
-    for (int i = 0; i < kBS; ++i) h[i] = (active && a.fwd.h0) ? a.fwd.h0[row * N + kBS * gi + i] : 0.f;
+    for (int i = 0; i < kBS; ++i) h[i] = (active && a.h0) ? a.h0[row * N + kBS * gi + i] : 0.f;
     for (int ch = 0; ch < nch; ++ch) {
         const int t0 = ch * kBT, tl = min(kBT, L - t0);
         if (active)
@@ -256,9 +286,9 @@ __global__ void __launch_bounds__(kBThreads, 4)
         channel_sum(lay.dout, pbc + static_cast<size_t>(N) * L, t0, tl);
         if (a.dz) {
             for (int j = tid; j < CPB * kBT; j += kBThreads) {
-                const int cc = j / kBT, t = j % kBT;
+                const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
                 if (cc >= nchan || t >= tl) continue;
-                const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
+                const long long i = xi(cc, t0 + t);
                 const float zv = sm[lay.zz + cc * kRow + t];
                 const float sgz = sigmoid_fast(zv);
                 a.dz[i] = ldf(DY, i) * sm[lay.o + cc * kRow + t] * sgz * (1.f + zv * (1.f - sgz));
@@ -310,11 +340,15 @@ __global__ void __launch_bounds__(kBThreads, 4)
         // dB_t[n] = sum over the CTA's channels of G_t[n] Delta_t x_t
         channel_sum(lay.dlx, pbc, t0, tl);
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
-            const int cc = j / kBT, t = j % kBT;
+            const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
             if (cc >= nchan || t >= tl) continue;
-            const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
-            a.dx[i] = sm[lay.gx + cc * kRow + t];
-            a.ddelta[i] = sm[lay.gd + cc * kRow + t];
+            a.dx[xi(cc, t0 + t)] = sm[lay.gx + cc * kRow + t];
+            // one channel per head: the gradient of delta directly; else per channel,
+            // summed over the head by the second launch
+            if (a.hp == 1)
+                a.ddelta[di(cc, t0 + t)] = sm[lay.gd + cc * kRow + t];
+            else
+                dd_chan[(static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t] = sm[lay.gd + cc * kRow + t];
         }
     }
     if (active) {
@@ -328,38 +362,59 @@ __global__ void __launch_bounds__(kBThreads, 4)
     }
 }
 
-// dB, dC: sum of the per-CTA partials of each (batch, group); dA, dD, dbias: sum over the
-// batch.  One thread per output element.
-__global__ void m1_scan_bwd_reduce(M1BwdArgs a, int cps, const float* part_bc, const float* part_a,
-                                   const float* part_d, const float* part_bias) {
-    const int L = a.fwd.seqlen, Dm = a.fwd.dim, G = a.fwd.ngroups, N = a.fwd.dstate, Bt = a.fwd.batch;
+// dB, dC: sum of the per-CTA partials of each (batch, group), written in the caller's
+// layout; dA, dD, dbias: sums over the batch (and over a head's channels and, for A,
+// states when hp > 1); the gradient of the shared delta (hp > 1): sum over a head's
+// channels.  One thread per output element, fixed summation order.
+__global__ void m1_scan_bwd_reduce(BwdView a, int cps, const float* part_bc, const float* part_a,
+                                   const float* part_d, const float* part_bias, const float* dd_chan) {
+    const int L = a.seqlen, Dm = a.dim, G = a.ngroups, N = a.dstate, Bt = a.batch, hp = a.hp;
+    const int heads = Dm / hp;
     const size_t nbc = static_cast<size_t>(Bt) * G * N * L;
-    const size_t na = static_cast<size_t>(Dm) * N;
-    const size_t total = 2 * nbc + na + 2 * static_cast<size_t>(Dm);
+    const size_t na = a.san ? static_cast<size_t>(Dm) * N : static_cast<size_t>(heads);
+    const size_t ndt = hp > 1 ? static_cast<size_t>(Bt) * heads * L : 0;
+    const size_t total = 2 * nbc + na + 2 * static_cast<size_t>(heads) + ndt;
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
         if (i < 2 * nbc) {
             const int which = i < nbc ? 0 : 1;  // 0: dB, 1: dC
             const size_t e = i % nbc;           // (pair, n, t)
             const size_t pair = e / (static_cast<size_t>(N) * L), nt = e % (static_cast<size_t>(N) * L);
-            float s = 0.f;
+            float sum = 0.f;
             for (int p = 0; p < cps; ++p)
-                s += part_bc[((pair * cps + p) * 2 + which) * N * static_cast<size_t>(L) + nt];
-            (which ? a.dC : a.dB)[e] = s;
+                sum += part_bc[((pair * cps + p) * 2 + which) * N * static_cast<size_t>(L) + nt];
+            const long long bb = static_cast<long long>(pair / G), gg = static_cast<long long>(pair % G);
+            const long long n = static_cast<long long>(nt / L), t = static_cast<long long>(nt % L);
+            (which ? a.dC : a.dB)[bb * a.sbb + gg * a.sbg + n * a.sbn + t * a.sbt] = sum;
         } else if (i < 2 * nbc + na) {
-            const size_t e = i - 2 * nbc;  // (d, n)
-            float s = 0.f;
-            for (int bb = 0; bb < Bt; ++bb) s += part_a[static_cast<size_t>(bb) * na + e];
-            a.dA[e] = s;
-        } else {
+            const size_t e = i - 2 * nbc;  // (d, n), or the head
+            float sum = 0.f;
+            if (a.san) {
+                for (int bb = 0; bb < Bt; ++bb) sum += part_a[static_cast<size_t>(bb) * Dm * N + e];
+            } else {
+                for (int bb = 0; bb < Bt; ++bb)
+                    for (int q = 0; q < hp * N; ++q)
+                        sum += part_a[(static_cast<size_t>(bb) * Dm + e * hp) * N + q];
+            }
+            a.dA[e] = sum;
+        } else if (i < 2 * nbc + na + 2 * static_cast<size_t>(heads)) {
             const size_t e = i - 2 * nbc - na;
-            const int dd = static_cast<int>(e % Dm);
-            const float* src = e < static_cast<size_t>(Dm) ? part_d : part_bias;
-            float* dst = e < static_cast<size_t>(Dm) ? a.dD_skip : a.ddelta_bias;
+            const int hh = static_cast<int>(e % heads);
+            const float* src = e < static_cast<size_t>(heads) ? part_d : part_bias;
+            float* dst = e < static_cast<size_t>(heads) ? a.dD : a.dbias;
             if (!dst) continue;
-            float s = 0.f;
-            for (int bb = 0; bb < Bt; ++bb) s += src[static_cast<size_t>(bb) * Dm + dd];
-            dst[dd] = s;
+            float sum = 0.f;
+            for (int bb = 0; bb < Bt; ++bb)
+                for (int q = 0; q < hp; ++q) sum += src[static_cast<size_t>(bb) * Dm + hh * hp + q];
+            dst[hh] = sum;
+        } else {
+            const size_t e = i - 2 * nbc - na - 2 * static_cast<size_t>(heads);  // (b, head, t)
+            const int bb = static_cast<int>(e / (static_cast<size_t>(heads) * L));
+            const int hh = static_cast<int>((e / L) % heads), t = static_cast<int>(e % L);
+            float sum = 0.f;
+            for (int q = 0; q < hp; ++q)
+                sum += dd_chan[(static_cast<size_t>(bb) * Dm + hh * hp + q) * L + t];
+            a.ddelta[bb * a.sdb + hh * a.sdh + static_cast<long long>(t) * a.sdt] = sum;
         }
     }
 }
@@ -371,35 +426,35 @@ int bwd_tpc(int n) {
         case 16: return 4;
         case 32: return 8;
         case 64: return 16;
+        case 128: return 32;
         default: return 0;
     }
 }
 
-BwdWs bwd_ws(const M1BwdArgs& a, int cps) {
-    const ssm_scan_params& f = a.fwd;
-    const size_t rows = static_cast<size_t>(f.batch) * f.dim;
-    const size_t nch = (static_cast<size_t>(f.seqlen) + kBT - 1) / kBT;
-    const size_t pairs = static_cast<size_t>(f.batch) * f.ngroups;
+BwdWs bwd_ws(const BwdView& a, int cps) {
+    const size_t rows = static_cast<size_t>(a.batch) * a.dim;
+    const size_t nch = (static_cast<size_t>(a.seqlen) + kBT - 1) / kBT;
+    const size_t pairs = static_cast<size_t>(a.batch) * a.ngroups;
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
     BwdWs w;
     w.ckpt = 0;
-    w.part_bc = r256(rows * nch * f.dstate * 4);
-    w.part_a = w.part_bc + r256(pairs * cps * 2 * f.dstate * static_cast<size_t>(f.seqlen) * 4);
-    w.part_d = w.part_a + r256(rows * f.dstate * 4);
+    w.part_bc = r256(rows * nch * a.dstate * 4);
+    w.part_a = w.part_bc + r256(pairs * cps * 2 * a.dstate * static_cast<size_t>(a.seqlen) * 4);
+    w.part_d = w.part_a + r256(rows * a.dstate * 4);
     w.part_bias = w.part_d + r256(rows * 4);
-    w.bytes = w.part_bias + r256(rows * 4);
+    w.dd_chan = w.part_bias + r256(rows * 4);
+    w.bytes = w.dd_chan + (a.hp > 1 ? r256(rows * static_cast<size_t>(a.seqlen) * 4) : 0);
     return w;
 }
 
-int bwd_cps(const M1BwdArgs& a) {
-    const int tpc = bwd_tpc(a.fwd.dstate);
-    const int cpb = bwd_cpb(tpc);
-    const int per_group = a.fwd.dim / a.fwd.ngroups;
+int bwd_cps(const BwdView& a) {
+    const int cpb = bwd_cpb(bwd_tpc(a.dstate));
+    const int per_group = a.dim / a.ngroups;
     return (per_group + cpb - 1) / cpb;
 }
 
 template <typename Tin, typename Tdy, int TPC>
-cudaError_t launch_bwd(const M1BwdArgs& a, void* ws, cudaStream_t s) {
+cudaError_t launch_bwd(const BwdView& a, void* ws, cudaStream_t s) {
     const int cps = bwd_cps(a);
     const BwdWs w = bwd_ws(a, cps);
     unsigned char* base = static_cast<unsigned char*>(ws);
@@ -408,28 +463,77 @@ cudaError_t launch_bwd(const M1BwdArgs& a, void* ws, cudaStream_t s) {
     auto k = m1_scan_bwd<Tin, Tdy, TPC>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int grid = a.fwd.batch * a.fwd.ngroups * cps;
+    const int grid = a.batch * a.ngroups * cps;
     float* part_bc = reinterpret_cast<float*>(base + w.part_bc);
     float* part_a = reinterpret_cast<float*>(base + w.part_a);
     float* part_d = reinterpret_cast<float*>(base + w.part_d);
     float* part_bias = reinterpret_cast<float*>(base + w.part_bias);
+    float* dd_chan = reinterpret_cast<float*>(base + w.dd_chan);
     if (grid > 0)
         k<<<grid, kBThreads, smem, s>>>(a, cps, reinterpret_cast<float*>(base + w.ckpt), part_bc, part_a,
-                                        part_d, part_bias);
+                                        part_d, part_bias, dd_chan);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    m1_scan_bwd_reduce<<<2 * 152, 256, 0, s>>>(a, cps, part_bc, part_a, part_d, part_bias);
+    m1_scan_bwd_reduce<<<2 * 152, 256, 0, s>>>(a, cps, part_bc, part_a, part_d, part_bias, dd_chan);
     return cudaGetLastError();
 }
 
 template <typename Tin, typename Tdy>
-cudaError_t dispatch_tpc(const M1BwdArgs& a, void* ws, cudaStream_t s) {
-    switch (bwd_tpc(a.fwd.dstate)) {
+cudaError_t dispatch_tpc(const BwdView& a, void* ws, cudaStream_t s) {
+    switch (bwd_tpc(a.dstate)) {
         case 4: return launch_bwd<Tin, Tdy, 4>(a, ws, s);
         case 8: return launch_bwd<Tin, Tdy, 8>(a, ws, s);
         case 16: return launch_bwd<Tin, Tdy, 16>(a, ws, s);
+        case 32: return launch_bwd<Tin, Tdy, 32>(a, ws, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t bwd_launch(const BwdView& a, void* workspace, cudaStream_t s) {
+    const bool in_bf = a.in_dtype == SSM_BF16, dy_bf = a.dy_dtype == SSM_BF16;
+    if (in_bf && dy_bf) return dispatch_tpc<bf16_t, bf16_t>(a, workspace, s);
+    if (in_bf) return dispatch_tpc<bf16_t, float>(a, workspace, s);
+    if (dy_bf) return dispatch_tpc<float, bf16_t>(a, workspace, s);
+    return dispatch_tpc<float, float>(a, workspace, s);
+}
+
+// Mamba-1 layouts: x, z, dy, delta [Bt, D, L]; B, C [Bt, G, N, L]; A [D, N]
+BwdView view_m1(const M1BwdArgs& a) {
+    const ssm_scan_params& f = a.fwd;
+    BwdView v{};
+    v.x = f.x; v.delta = f.delta; v.z = f.z; v.B = f.B; v.C = f.C; v.dy = a.dy;
+    v.delta_bias = f.delta_bias; v.A = f.A; v.D_skip = f.D_skip; v.h0 = f.h0; v.dh_final = a.dh_final;
+    v.dx = a.dx; v.ddelta = a.ddelta; v.dz = a.dz; v.dh0 = a.dh0;
+    v.dA = a.dA; v.dB = a.dB; v.dC = a.dC; v.dD = a.dD_skip; v.dbias = a.ddelta_bias;
+    v.batch = f.batch; v.dim = f.dim; v.dstate = f.dstate; v.seqlen = f.seqlen; v.ngroups = f.ngroups;
+    v.softplus = f.delta_softplus; v.in_dtype = f.in_dtype; v.dy_dtype = f.out_dtype;
+    const long long L = f.seqlen, D = f.dim, N = f.dstate, G = f.ngroups;
+    v.hp = 1;
+    v.sxb = D * L; v.sxd = L; v.sxt = 1;
+    v.sdb = D * L; v.sdh = L; v.sdt = 1;
+    v.sbb = G * N * L; v.sbg = N * L; v.sbn = L; v.sbt = 1;
+    v.sah = N; v.san = 1;
+    return v;
+}
+
+// SSD layouts: x, z, dy [Bt, L, H, P] (channel d = h P + p); dt [Bt, L, H]; B, C
+// [Bt, L, G, N]; A, D, dt_bias [H]
+BwdView view_ssd(const ssd_bwd_params& a) {
+    const ssd_params& f = a.fwd;
+    BwdView v{};
+    v.x = f.x; v.delta = f.dt; v.z = f.z; v.B = f.B; v.C = f.C; v.dy = a.dy;
+    v.delta_bias = f.dt_bias; v.A = f.A; v.D_skip = f.D_skip; v.h0 = f.h0; v.dh_final = a.dh_final;
+    v.dx = a.dx; v.ddelta = a.ddt; v.dz = a.dz; v.dh0 = a.dh0;
+    v.dA = a.dA; v.dB = a.dB; v.dC = a.dC; v.dD = a.dD_skip; v.dbias = a.ddt_bias;
+    const long long L = f.seqlen, H = f.nheads, P = f.headdim, N = f.dstate, G = f.ngroups;
+    v.batch = f.batch; v.dim = static_cast<int>(H * P); v.dstate = f.dstate; v.seqlen = f.seqlen;
+    v.ngroups = f.ngroups; v.softplus = f.dt_softplus; v.in_dtype = f.in_dtype; v.dy_dtype = f.out_dtype;
+    v.hp = f.headdim;
+    v.sxb = L * H * P; v.sxd = 1; v.sxt = H * P;
+    v.sdb = L * H; v.sdh = 1; v.sdt = H;
+    v.sbb = L * G * N; v.sbg = N; v.sbn = 1; v.sbt = G * N;
+    v.sah = 1; v.san = 0;
+    return v;
 }
 
 }  // namespace
@@ -440,15 +544,26 @@ bool m1_bwd_supported(const M1BwdArgs& a) {
 
 size_t m1_bwd_workspace_size(const M1BwdArgs& a) {
     if (!m1_bwd_supported(a)) return 0;
-    return bwd_ws(a, bwd_cps(a)).bytes;
+    const BwdView v = view_m1(a);
+    return bwd_ws(v, bwd_cps(v)).bytes;
 }
 
 cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s) {
-    const bool in_bf = a.fwd.in_dtype == SSM_BF16, dy_bf = a.fwd.out_dtype == SSM_BF16;
-    if (in_bf && dy_bf) return dispatch_tpc<bf16_t, bf16_t>(a, workspace, s);
-    if (in_bf) return dispatch_tpc<bf16_t, float>(a, workspace, s);
-    if (dy_bf) return dispatch_tpc<float, bf16_t>(a, workspace, s);
-    return dispatch_tpc<float, float>(a, workspace, s);
+    return bwd_launch(view_m1(a), workspace, s);
+}
+
+bool ssd_bwd_supported(const ssd_bwd_params& a) {
+    return a.fwd.disc == SSM_DISC_EXP_EULER && bwd_tpc(a.fwd.dstate) > 0;
+}
+
+size_t ssd_bwd_workspace_size(const ssd_bwd_params& a) {
+    if (!ssd_bwd_supported(a)) return 0;
+    const BwdView v = view_ssd(a);
+    return bwd_ws(v, bwd_cps(v)).bytes;
+}
+
+cudaError_t ssd_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_t s) {
+    return bwd_launch(view_ssd(a), workspace, s);
 }
 
 }  // namespace ssm

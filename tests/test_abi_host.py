@@ -252,3 +252,43 @@ def test_s4d_rejects_bad_arguments(lib, field, value, status):
     assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), None) == status
     if field in ("dstate", "log_dt", "C"):
         assert lib.ssm_s4d_kernel(ctypes.byref(p), FAKE, 16, None) == status
+
+
+def ssd_bwd_params(**kw):
+    p = _lib.SsdBwdParams()
+    f = p.fwd
+    f.batch, f.seqlen, f.nheads, f.headdim, f.dstate, f.ngroups, f.chunk_size = 2, 64, 4, 64, 128, 1, 64
+    f.in_dtype = f.out_dtype = _lib.SSM_BF16
+    for n in ("x", "dt", "A", "B", "C"):
+        setattr(f, n, FAKE)
+    f.dt_softplus = 1
+    for n in ("dy", "dx", "ddt", "dA", "dB", "dC"):
+        setattr(p, n, FAKE)
+    for k, v in kw.items():
+        if k.startswith("fwd_"):
+            setattr(p.fwd, k[4:], v)
+        else:
+            setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"fwd_disc": _lib.SSM_DISC_ZOH}, _lib.SSM_ERR_UNSUPPORTED),
+    ({"fwd_dstate": 96}, _lib.SSM_ERR_UNSUPPORTED),
+    ({"ddt": None}, _lib.SSM_ERR_INVALID_ARG),
+    ({"fwd_z": FAKE}, _lib.SSM_ERR_INVALID_ARG),
+    ({"fwd_dt_bias": FAKE}, _lib.SSM_ERR_INVALID_ARG),
+    ({"dB": FAKE + 4}, _lib.SSM_ERR_INVALID_ARG),
+])
+def test_ssd_bwd_rejects_bad_arguments(lib, kw, status):
+    p = ssd_bwd_params(**kw)
+    assert lib.ssd_scan_bwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssm_last_error()
+
+
+def test_ssd_bwd_workspace_size(lib):
+    p = ssd_bwd_params()
+    need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
+    # includes the per-channel d(dt) buffer: batch * H * P * L floats
+    assert need >= 2 * 4 * 64 * 64 * 4
+    assert lib.ssd_scan_bwd(ctypes.byref(p), FAKE, need - 1, None) == _lib.SSM_ERR_INVALID_ARG
