@@ -8,7 +8,7 @@ batch; several input sets (together larger than L2) rotate between steps.
 
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
 the decode update (780m-shaped, 1024 steps), multi-token decode, the Mamba-1 backward
-(130m layer), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel) and
+(130m layer), the SSD backward (130m SSD shape), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel) and
 the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -506,6 +506,24 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                           "note": "x, delta, z, dy bf16 in; dx, ddelta, dz, dA, dB, dC, dD, "
                                   "dbias float32 out; 2 input sets rotate"}
     del bsets, bws
+    # SSD backward on the 130m SSD shape (batch 4, L 4096, 24 heads x 64, dstate 128)
+    c4 = synth.WORKLOADS["ssd_130m"]
+    sb_inp = synth.ssd(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
+                       c4["ngroups"], dtype=c4["dtype"], delta_scale=c4["delta_scale"], seed=60)
+    sb = _dev(sb_inp, torch)
+    sb_dy = torch.randn(sb["x"].shape, device="cuda").to(torch.bfloat16)
+    sbws = torch.empty(max(1, ssm.ssd_scan_bwd_workspace_size(sb["x"], sb["B"])), dtype=torch.uint8,
+                       device="cuda")
+
+    def fsb(i):
+        ssm.ssd_scan_bwd(sb["x"], sb["dt"], sb["A"], sb["B"], sb["C"], sb_dy, D=sb["D"],
+                         dt_bias=sb["dt_bias"], workspace=sbws)
+    tsb = time_launches(torch, fsb, 3, 1, stream)
+    upd_sb = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
+    out["ssd_130m_bwd"] = {"ms": tsb * 1e3, "state_updates_per_s": upd_sb / tsb,
+                           "workspace_bytes": sbws.numel(),
+                           "note": "x, dt, B, C, dy bf16 in; every gradient float32 out"}
+    del sb, sb_dy, sbws
     # Mamba-3 scan on the 130m layer shape (complex states, trapezoid weight lam)
     m3sets = []
     for k in range(2):
@@ -700,6 +718,28 @@ def run_case(args):
         for _ in range(n):
             ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], dy, D=t["D"], z=t["z"],
                              delta_bias=t["delta_bias"])
+    elif args.case == "m3":  # Mamba-3 scan, 130m layer shape
+        cfg = synth.WORKLOADS["m1_130m_layer"]
+        inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
+                           delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+        t = _dev(inp, torch)
+        A_im = 3.0 * torch.randn(t["A"].shape, device="cuda")
+        lam = torch.rand(t["x"].shape, device="cuda").to(torch.bfloat16)
+        for _ in range(n):
+            ssm.ssm_mamba3_scan_fwd(t["x"], t["delta"], t["A"], A_im, lam, t["B"], t["C"], D=t["D"],
+                                    z=t["z"], delta_bias=t["delta_bias"])
+    elif args.case == "s4d":  # S4D recurrent form, batch 8, d_model 256, 32 states, L 4096
+        Ds, Ns = 256, 32
+        log_dt = torch.empty(Ds, device="cuda").uniform_(float(np.log(1e-3)), float(np.log(1e-1)))
+        A = torch.stack([torch.full((Ds, Ns), -0.5, device="cuda"),
+                         (np.pi * torch.arange(Ns, device="cuda", dtype=torch.float32)).expand(Ds, Ns)],
+                        dim=-1).contiguous()
+        Bm = torch.stack([torch.ones(Ds, Ns, device="cuda"), torch.zeros(Ds, Ns, device="cuda")],
+                         dim=-1).contiguous()
+        Cm = torch.randn(Ds, Ns, 2, device="cuda")
+        u = torch.randn(8, Ds, 4096, device="cuda").to(torch.bfloat16)
+        for _ in range(n):
+            ssm.ssm_s4d_scan_fwd(u, log_dt, A, Bm, Cm)
     elif args.case == "tokens":  # 16 decode tokens per call, one state buffer
         c5 = synth.WORKLOADS["step_780m"]
         Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
@@ -728,7 +768,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the SSD, decode and long-context measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens", "bwd"],
+    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens", "bwd",
+                                       "m3", "s4d"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:

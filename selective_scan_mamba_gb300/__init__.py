@@ -398,6 +398,18 @@ def ssd_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, dt_softplus=T
     return out
 
 
+def ssd_scan_bwd_workspace_size(x, B, dy_dtype=None) -> int:
+    """Scratch bytes ssd_scan_bwd needs for these shapes (0 if unsupported)."""
+    p = _lib.SsdBwdParams()
+    p.fwd.batch, p.fwd.seqlen, p.fwd.nheads, p.fwd.headdim = x.shape
+    p.fwd.ngroups, p.fwd.dstate = B.shape[2], B.shape[3]
+    p.fwd.chunk_size = 64
+    p.fwd.in_dtype = _dtype_code(x)
+    p.fwd.out_dtype = (_lib.SSM_F32 if dy_dtype is not None and dy_dtype == _torch().float32
+                       else _lib.SSM_BF16)
+    return int(lib().ssd_scan_bwd_workspace_size(ctypes.byref(p)))
+
+
 def ssd_chunk_scan_workspace_size(x, B, chunk_size) -> int:
     """Scratch bytes ssd_chunk_scan_fwd needs for these shapes and chunk size."""
     p = _lib.SsdParams()

@@ -8,7 +8,7 @@
 //
 // Two kernels:
 //   - s4d_scan runs the recurrent form (the O(1)-state form, equal to the convolution from
-//     a zero state): a CTA of 128 threads owns 128 / TPC channels of one batch row, four
+//     a zero state): a CTA of 128 threads owns 128 / TPC channels of one batch row, two
 //     complex states per thread; Abar, Bbar and C sit in registers (Abar and Bbar computed
 //     once per state in double precision, then rounded), u and y pass through shared
 //     memory in 32-step chunks so that global accesses are coalesced rows;
@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kST = 32;
 constexpr int kSThreads = 128;
-constexpr int kSS = 4;
+constexpr int kSS = 2;           // complex states per thread (more threads: L is sequential)
 constexpr int kSRow = kST + 1;
 
 // Abar = e^z and Bbar = Delta B phi1(z) for one state, in double precision
@@ -184,11 +184,11 @@ cudaError_t launch_s4d(const ssm_s4d_params& a, cudaStream_t s) {
 template <typename Tin, typename Tout>
 cudaError_t dispatch_s4d(const ssm_s4d_params& a, cudaStream_t s) {
     switch (a.dstate) {
-        case 4: return launch_s4d<Tin, Tout, 1>(a, s);
-        case 8: return launch_s4d<Tin, Tout, 2>(a, s);
-        case 16: return launch_s4d<Tin, Tout, 4>(a, s);
-        case 32: return launch_s4d<Tin, Tout, 8>(a, s);
-        case 64: return launch_s4d<Tin, Tout, 16>(a, s);
+        case 4: return launch_s4d<Tin, Tout, 4 / kSS>(a, s);
+        case 8: return launch_s4d<Tin, Tout, 8 / kSS>(a, s);
+        case 16: return launch_s4d<Tin, Tout, 16 / kSS>(a, s);
+        case 32: return launch_s4d<Tin, Tout, 32 / kSS>(a, s);
+        case 64: return launch_s4d<Tin, Tout, 64 / kSS>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }

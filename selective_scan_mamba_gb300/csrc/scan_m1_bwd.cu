@@ -132,8 +132,12 @@ __global__ void __launch_bounds__(kBThreads, 4)
     const Tdy* DY = static_cast<const Tdy*>(a.dy);
     const long long bc_base = b * a.sbb + g * a.sbg;
     // element (b, channel cc of the CTA, step t) of x, z, dy, dx, dz and of delta
+    // head of each of the CTA's channels (the channel itself when hp = 1), once
+    __shared__ int s_head[CPB];
+    for (int cc = tid; cc < CPB; cc += kBThreads) s_head[cc] = (d0 + cc) / a.hp;
+    __syncthreads();
     auto xi = [&](int cc, int t) { return b * a.sxb + (d0 + cc) * a.sxd + t * a.sxt; };
-    auto di = [&](int cc, int t) { return b * a.sdb + ((d0 + cc) / a.hp) * a.sdh + t * a.sdt; };
+    auto di = [&](int cc, int t) { return b * a.sdb + s_head[cc] * a.sdh + t * a.sdt; };
     // staging order: consecutive threads take consecutive addresses of the layout
     const bool tfast = a.sxt == 1, bt_fast = a.sbt == 1;
 
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
             float dl = 0.f, xv = 0.f, sgv = 1.f, dov = 0.f, zv = 0.f;
             if (cc < nchan && t < tl) {
                 const long long i = xi(cc, t0 + t);
-                const float v = ldf(DL, di(cc, t0 + t)) + (a.delta_bias ? a.delta_bias[(d0 + cc) / a.hp] : 0.f);
+                const float v = ldf(DL, di(cc, t0 + t)) + (a.delta_bias ? a.delta_bias[s_head[cc]] : 0.f);
                 dl = a.softplus ? softplus_fast(v) : v;
                 xv = ldf(X, i);
                 if (full) {
