@@ -214,6 +214,23 @@ def time_launches(torch, fn, n, warmup, stream):
     return e0.elapsed_time(e1) / 1e3 / n
 
 
+def max_over_ranks(dist, value, device):
+    """The largest of the ranks' values (the job's time is its slowest rank's); the value
+    itself when there is no process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, t_max):
+    """Weak scaling: every rank processes `units_per_rank` (its own batch); the job's rate
+    is all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / t_max
+
+
 def bench_ours(args, rank, world):
     import torch
     import selective_scan_mamba_gb300 as ssm
@@ -269,12 +286,9 @@ def bench_ours(args, rank, world):
             dist.barrier()
         t_step = e0.elapsed_time(e1) / 1e3 / args.steps
     clocks = clk.summary()
-    if dist:
-        tt = torch.tensor([t_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step = float(tt.item())
+    t_step = max_over_ranks(dist, t_step, "cuda")
     updates = Bt * L * D * N
-    value = updates * world / t_step
+    value = whole_job_rate(updates, world, t_step)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sm_max = clocks.get("sm_max_mhz") or 2070.0
     alu_peak = alu_peak_updates(sms, sm_max)
@@ -298,10 +312,7 @@ def bench_ours(args, rank, world):
 
     e2e_steps = max(3, min(args.steps, 20))
     t_e2e = time_launches(torch, e2e_step, e2e_steps, 2, stream)
-    if dist:
-        tt = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = max_over_ranks(dist, t_e2e, "cuda")
 
     paths = {}
     if rank == 0 and not args.headline_only:
@@ -330,7 +341,7 @@ def bench_ours(args, rank, world):
                      "hbm": {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"],
                              "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}},
-        "e2e": {"value": updates * world / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(updates, world, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
         "gpu_launches": args.steps,
         "clocks": clocks,
