@@ -238,8 +238,14 @@ typedef struct {
     float* h_final;
 } ssm_s4d_params;
 
-/* The recurrent form over the whole sequence (batch, u, y, h0, h_final are used). */
-ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* stream);
+/* Device scratch ssm_s4d_scan_fwd needs, in bytes: 0 unless the sequence is split into
+ * segments (few channels, long L), then the segments' end states. */
+size_t ssm_s4d_scan_workspace_size(const ssm_s4d_params* p);
+
+/* The recurrent form over the whole sequence (batch, u, y, h0, h_final are used).
+ * `workspace`: at least ssm_s4d_scan_workspace_size(p) bytes (may be NULL when 0). */
+ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /* The convolution kernel K [dim, kernel_len] float32 (device pointer), from dim, dstate,
  * log_dt, A, B and C of `p` (the other fields are ignored). */

@@ -286,7 +286,7 @@ def _s4d_params(log_dt, A, B, C, D=None):
 
 
 def ssm_s4d_scan_fwd(u, log_dt, A, B, C, D=None, h0=None, *, y=None, h_final=None,
-                     out_dtype=None, return_final_state=False, stream=None):
+                     out_dtype=None, return_final_state=False, workspace=None, stream=None):
     """S4D recurrent form (exact ZOH, Delta = exp(log_dt)).
 
     u: [batch, dim, L] (bfloat16 or float32); log_dt: [dim] float32; A, B, C: [dim, N]
@@ -310,7 +310,13 @@ def ssm_s4d_scan_fwd(u, log_dt, A, B, C, D=None, h0=None, *, y=None, h_final=Non
     p.h0 = _ptr(h0_, "h0")
     p.y = _ptr(y, "y", (batch, dim, L))
     p.h_final = _ptr(h_final, "h_final", (batch, dim, N, 2), torch.float32)
-    _lib.check(lib().ssm_s4d_scan_fwd(ctypes.byref(p), _stream(stream)))
+    need = int(lib().ssm_s4d_scan_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    _lib.check(lib().ssm_s4d_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
     del keep, h0_
     return (y, h_final) if return_final_state else y
 

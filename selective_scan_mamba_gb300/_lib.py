@@ -80,6 +80,7 @@ class StepParams(ctypes.Structure):
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
            "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd",
+           "ssm_s4d_scan_workspace_size",
            "ssm_s4d_kernel", "ssd_scan_bwd", "ssd_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version")
@@ -114,7 +115,9 @@ def load(build_if_missing: bool = True):
             lib.ssm_mamba3_scan_fwd.restype = _i
             lib.ssm_mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Params), _vp]
             lib.ssm_s4d_scan_fwd.restype = _i
-            lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp]
+            lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp, sz, _vp]
+            lib.ssm_s4d_scan_workspace_size.restype = sz
+            lib.ssm_s4d_scan_workspace_size.argtypes = [ctypes.POINTER(S4dParams)]
             lib.ssm_s4d_kernel.restype = _i
             lib.ssm_s4d_kernel.argtypes = [ctypes.POINTER(S4dParams), _vp, _i, _vp]
             lib.ssd_scan_bwd.restype = _i

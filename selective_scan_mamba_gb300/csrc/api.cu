@@ -379,10 +379,22 @@ ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream) {
 }
 
 
-ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* stream) {
+size_t ssm_s4d_scan_workspace_size(const ssm_s4d_params* p) {
+    if (p == nullptr || p->batch < 1 || p->dim < 1 || p->seqlen < 0 || !ssm::s4d_supported(p->dstate))
+        return 0;
+    return ssm::s4d_workspace_size(*p);
+}
+
+ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* workspace, size_t workspace_bytes,
+                            void* stream) {
     g_err[0] = '\0';
     ssm_status st = check_s4d_params(p, true);
     if (st != SSM_OK) return st;
+    const size_t need = ssm::s4d_workspace_size(*p);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
     if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->seqlen == 0) {
@@ -394,7 +406,7 @@ ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* stream) {
         }
         return SSM_OK;
     }
-    cudaError_t e = ssm::s4d_launch(*p, s);
+    cudaError_t e = ssm::s4d_launch(*p, workspace, s);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_scan_fwd launch");
     return SSM_OK;
 }

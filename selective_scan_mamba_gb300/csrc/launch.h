@@ -45,7 +45,8 @@ cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s);
 
 // S4D (s4d.cu)
 bool s4d_supported(int dstate);
-cudaError_t s4d_launch(const ssm_s4d_params& a, cudaStream_t s);
+size_t s4d_workspace_size(const ssm_s4d_params& a);
+cudaError_t s4d_launch(const ssm_s4d_params& a, void* workspace, cudaStream_t s);
 cudaError_t s4d_kernel_launch(const ssm_s4d_params& a, float* K, int L, cudaStream_t s);
 
 struct M1Plan {

@@ -11,7 +11,9 @@
 //     a zero state): a CTA of 128 threads owns 128 / TPC channels of one batch row, two
 //     complex states per thread; Abar, Bbar and C sit in registers (Abar and Bbar computed
 //     once per state in double precision, then rounded), u and y pass through shared
-//     memory in 32-step chunks so that global accesses are coalesced rows;
+//     memory in 32-step chunks so that global accesses are coalesced rows; when that
+//     leaves few CTAs the sequence is cut into segments (a states-only pass over all but
+//     the last, then every segment from the state carried through the ones before it);
 //   - s4d_kernel_gen writes the convolution kernel K [dim, L]: per channel the states'
 //     C Bbar and z once, then per step l the sum of Re(C Bbar exp(l z)) with the phase
 //     l Im z reduced modulo 2 pi in double precision (it reaches 1e5 rad at long L).
@@ -54,12 +56,23 @@ __device__ void s4d_disc(double dt, double ar, double ai, double br, double bi, 
     *bbi = dt * (br * pi + bi * pr);
 }
 
-template <typename Tin, typename Tout, int TPC>
-__global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps) {
+// STATES: the segment pass of a time-split scan.  Segment `seg` covers steps
+// [seg * seg_len, (seg + 1) * seg_len); this pass runs segments 0 .. nseg-2 from a zero
+// state and writes their end states (no outputs).  The main pass starts segment seg from
+// h0 carried through those: h <- Abar^seg_len h + h_end(j) for j < seg (Abar^seg_len in
+// double precision).
+template <typename Tin, typename Tout, int TPC, bool STATES>
+__global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps, int nseg, int seg_len,
+                                                      float* seg_state) {
     constexpr int N = TPC * kSS;
     constexpr int CPB = kSThreads / TPC;
-    const int L = a.seqlen, Dm = a.dim;
-    const int b = blockIdx.x / cps, part_i = blockIdx.x % cps;
+    const int Dm = a.dim;
+    const int segs_here = STATES ? nseg - 1 : nseg;
+    const int seg = blockIdx.x % segs_here;
+    const int rest = blockIdx.x / segs_here;
+    const int b = rest / cps, part_i = rest % cps;
+    const int tbeg = seg * seg_len, tend = min(a.seqlen, tbeg + seg_len);
+    const int L = a.seqlen;
     const int l0 = static_cast<int>((static_cast<long long>(part_i) * Dm) / cps);
     const int l1 = static_cast<int>((static_cast<long long>(part_i + 1) * Dm) / cps);
     const int nchan = l1 - l0;
@@ -74,6 +87,7 @@ __global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps)
 
     float abr[kSS], abi[kSS], bbr[kSS], bbi[kSS], cr[kSS], ci[kSS], hr[kSS], hi[kSS];
     const double dt = exp(static_cast<double>(a.log_dt[d]));
+    const size_t rows = static_cast<size_t>(a.batch) * Dm;
 #pragma unroll
     for (int i = 0; i < kSS; ++i) {
         const size_t k = (static_cast<size_t>(d) * N + kSS * gi + i) * 2;
@@ -86,14 +100,30 @@ __global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps)
         cr[i] = a.C[k];
         ci[i] = a.C[k + 1];
         const size_t hk = (row * N + kSS * gi + i) * 2;
-        hr[i] = (active && a.h0) ? a.h0[hk] : 0.f;
-        hi[i] = (active && a.h0) ? a.h0[hk + 1] : 0.f;
+        double h_r = (!STATES && active && a.h0) ? a.h0[hk] : 0.0;
+        double h_i = (!STATES && active && a.h0) ? a.h0[hk + 1] : 0.0;
+        if (!STATES && seg > 0) {
+            // carry through the earlier segments: h <- Abar^seg_len h + h_end(j)
+            const double zr = dt * a.A[k] * seg_len, zi = dt * a.A[k + 1] * seg_len;
+            const double mag = exp(zr);
+            double sn, cs;
+            sincos(fmod(zi, 6.283185307179586), &sn, &cs);
+            const double pr = mag * cs, pi = mag * sn;
+            for (int j = 0; j < seg; ++j) {
+                const float* hs = seg_state + ((j * rows + row) * N + kSS * gi + i) * 2;
+                const double nr = pr * h_r - pi * h_i + hs[0];
+                h_i = pr * h_i + pi * h_r + hs[1];
+                h_r = nr;
+            }
+        }
+        hr[i] = static_cast<float>(h_r);
+        hi[i] = static_cast<float>(h_i);
     }
     const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
     const Tin* U = static_cast<const Tin*>(a.u);
 
-    for (int t0 = 0; t0 < L; t0 += kST) {
-        const int tl = min(kST, L - t0);
+    for (int t0 = tbeg; t0 < tend; t0 += kST) {
+        const int tl = min(kST, tend - t0);
         __syncthreads();
         for (int j = tid; j < CPB * kST; j += kSThreads) {
             const int cc = j / kST, t = j % kST;
@@ -110,12 +140,15 @@ __global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps)
                 const float nr = fmaf(abr[i], hr[i], fmaf(-abi[i], hi[i], bbr[i] * u));
                 hi[i] = fmaf(abr[i], hi[i], fmaf(abi[i], hr[i], bbi[i] * u));
                 hr[i] = nr;
-                acc = fmaf(cr[i], hr[i], fmaf(-ci[i], hi[i], acc));
+                if (!STATES) acc = fmaf(cr[i], hr[i], fmaf(-ci[i], hi[i], acc));
             }
+            if (!STATES) {
 #pragma unroll
-            for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (gi == 0) s_y[c * kSRow + t] = acc + Dd * u;
+                for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (gi == 0) s_y[c * kSRow + t] = acc + Dd * u;
+            }
         }
+        if (STATES) continue;
         __syncthreads();
         for (int j = tid; j < CPB * kST; j += kSThreads) {
             const int cc = j / kST, t = j % kST;
@@ -124,7 +157,16 @@ __global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps)
                             s_y[cc * kSRow + t]);
         }
     }
-    if (active && a.h_final) {
+    if (STATES) {
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < kSS; ++i) {
+                float* hs = seg_state + ((seg * rows + row) * N + kSS * gi + i) * 2;
+                hs[0] = hr[i];
+                hs[1] = hi[i];
+            }
+        }
+    } else if (active && a.h_final && seg == nseg - 1) {
 #pragma unroll
         for (int i = 0; i < kSS; ++i) {
             const size_t hk = (row * N + kSS * gi + i) * 2;
@@ -173,22 +215,59 @@ __global__ void __launch_bounds__(kKThreads) s4d_kernel_gen(ssm_s4d_params a, fl
     }
 }
 
+// Time split: with few channel blocks the sequence is cut into segments so that about
+// four CTAs per SM run (measured: three segments 0.415 ms, eight 0.490 ms on the
+// 8 x 256 x 32-state shape: the states-only pass grows with the count); each segment at least 256 steps and a whole number of chunks.
+struct S4dPlan {
+    int cps, nseg, seg_len;
+    size_t ws_bytes;
+};
+S4dPlan s4d_plan(const ssm_s4d_params& a) {
+    const int tpc = a.dstate / kSS;
+    const int cpb = kSThreads / tpc;
+    S4dPlan p;
+    p.cps = (a.dim + cpb - 1) / cpb;
+    const long long base = static_cast<long long>(a.batch) * p.cps;
+    int sms = 148, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long want = (4LL * sms + base - 1) / base;
+    const long long by_len = a.seqlen / 256;
+    if (want > by_len) want = by_len;
+    if (want > 64) want = 64;
+    p.nseg = want < 1 ? 1 : static_cast<int>(want);
+    const int chunks = (a.seqlen + kST - 1) / kST;
+    p.seg_len = ((chunks + p.nseg - 1) / p.nseg) * kST;
+    if (p.seg_len == 0) p.seg_len = kST;
+    p.nseg = (a.seqlen + p.seg_len - 1) / p.seg_len;
+    if (p.nseg < 1) p.nseg = 1;
+    p.ws_bytes = static_cast<size_t>(p.nseg - 1) * a.batch * a.dim * a.dstate * 2 * sizeof(float);
+    return p;
+}
+
 template <typename Tin, typename Tout, int TPC>
-cudaError_t launch_s4d(const ssm_s4d_params& a, cudaStream_t s) {
-    constexpr int CPB = kSThreads / TPC;
-    const int cps = (a.dim + CPB - 1) / CPB;
-    s4d_scan<Tin, Tout, TPC><<<a.batch * cps, kSThreads, 0, s>>>(a, cps);
+cudaError_t launch_s4d(const ssm_s4d_params& a, void* ws, cudaStream_t s) {
+    const S4dPlan p = s4d_plan(a);
+    float* seg_state = static_cast<float*>(ws);
+    const int base = a.batch * p.cps;
+    if (p.nseg > 1) {
+        s4d_scan<Tin, Tout, TPC, true><<<base * (p.nseg - 1), kSThreads, 0, s>>>(a, p.cps, p.nseg, p.seg_len,
+                                                                                 seg_state);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    s4d_scan<Tin, Tout, TPC, false><<<base * p.nseg, kSThreads, 0, s>>>(a, p.cps, p.nseg, p.seg_len, seg_state);
     return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-cudaError_t dispatch_s4d(const ssm_s4d_params& a, cudaStream_t s) {
+cudaError_t dispatch_s4d(const ssm_s4d_params& a, void* ws, cudaStream_t s) {
     switch (a.dstate) {
-        case 4: return launch_s4d<Tin, Tout, 4 / kSS>(a, s);
-        case 8: return launch_s4d<Tin, Tout, 8 / kSS>(a, s);
-        case 16: return launch_s4d<Tin, Tout, 16 / kSS>(a, s);
-        case 32: return launch_s4d<Tin, Tout, 32 / kSS>(a, s);
-        case 64: return launch_s4d<Tin, Tout, 64 / kSS>(a, s);
+        case 4: return launch_s4d<Tin, Tout, 4 / kSS>(a, ws, s);
+        case 8: return launch_s4d<Tin, Tout, 8 / kSS>(a, ws, s);
+        case 16: return launch_s4d<Tin, Tout, 16 / kSS>(a, ws, s);
+        case 32: return launch_s4d<Tin, Tout, 32 / kSS>(a, ws, s);
+        case 64: return launch_s4d<Tin, Tout, 64 / kSS>(a, ws, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -199,12 +278,17 @@ bool s4d_supported(int dstate) {
     return dstate == 4 || dstate == 8 || dstate == 16 || dstate == 32 || dstate == 64;
 }
 
-cudaError_t s4d_launch(const ssm_s4d_params& a, cudaStream_t s) {
+size_t s4d_workspace_size(const ssm_s4d_params& a) {
+    if (a.seqlen <= 0) return 0;
+    return s4d_plan(a).ws_bytes;
+}
+
+cudaError_t s4d_launch(const ssm_s4d_params& a, void* workspace, cudaStream_t s) {
     const bool ib = a.in_dtype == SSM_BF16, ob = a.out_dtype == SSM_BF16;
-    if (ib && ob) return dispatch_s4d<bf16_t, bf16_t>(a, s);
-    if (ib) return dispatch_s4d<bf16_t, float>(a, s);
-    if (ob) return dispatch_s4d<float, bf16_t>(a, s);
-    return dispatch_s4d<float, float>(a, s);
+    if (ib && ob) return dispatch_s4d<bf16_t, bf16_t>(a, workspace, s);
+    if (ib) return dispatch_s4d<bf16_t, float>(a, workspace, s);
+    if (ob) return dispatch_s4d<float, bf16_t>(a, workspace, s);
+    return dispatch_s4d<float, float>(a, workspace, s);
 }
 
 cudaError_t s4d_kernel_launch(const ssm_s4d_params& a, float* K, int L, cudaStream_t s) {

@@ -249,7 +249,7 @@ def test_s4d_rejects_bad_arguments(lib, field, value, status):
     for f in ("u", "log_dt", "A", "B", "C", "y"):
         setattr(p, f, FAKE)
     setattr(p, field, value)
-    assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), None) == status
+    assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
     if field in ("dstate", "log_dt", "C"):
         assert lib.ssm_s4d_kernel(ctypes.byref(p), FAKE, 16, None) == status
 

@@ -114,3 +114,10 @@ def test_empty_sequence_copies_state():
     _, hf = ssm.ssm_s4d_scan_fwd(u, dl, dA, dB, dC, D=dD, h0=h0, return_final_state=True)
     torch.cuda.synchronize()
     assert torch.equal(hf, h0)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_time_split_long_sequence(oracle_mod, bf16):
+    """Few channels and a long sequence: the plan cuts the sequence into segments (a
+    states-only pass, then each segment from the carried state); h0 and h_final."""
+    _run(oracle_mod, 1, 8, 16, 3000, bf16, seed=11)
