@@ -240,9 +240,13 @@ __global__ void __launch_bounds__(kBThreads, 4)
         for (int t = 0; t < tl; ++t) {
             const float dl = sm[lay.dl + c * kRow + t], dlx = sm[lay.dlx + c * kRow + t];
             const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
-            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-            for (int i = 0; i < kBS; ++i) h[i] = ex2_approx(dl * A2[i]) * h[i] + dlx * bb[i];
+            const float2 dl2 = make_float2(dl, dl), dx2 = make_float2(dlx, dlx);
+            const float2 b01 = make_float2(bv.x, bv.y), b23 = make_float2(bv.z, bv.w);
+            const float2 e01 = mul2(dl2, make_float2(A2[0], A2[1])), e23 = mul2(dl2, make_float2(A2[2], A2[3]));
+            float2 h01 = make_float2(h[0], h[1]), h23 = make_float2(h[2], h[3]);
+            h01 = fma2(make_float2(ex2_approx(e01.x), ex2_approx(e01.y)), h01, mul2(dx2, b01));
+            h23 = fma2(make_float2(ex2_approx(e23.x), ex2_approx(e23.y)), h23, mul2(dx2, b23));
+            h[0] = h01.x; h[1] = h01.y; h[2] = h23.x; h[3] = h23.y;
         }
     }
 
@@ -273,13 +277,14 @@ __global__ void __launch_bounds__(kBThreads, 4)
             const float dl = sm[lay.dl + c * kRow + t], dlx = sm[lay.dlx + c * kRow + t];
             const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
             const float4 cv = *reinterpret_cast<const float4*>(sm + lay.cs + t * N + kBS * gi);
-            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w}, cb[kBS] = {cv.x, cv.y, cv.z, cv.w};
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < kBS; ++i) {
-                h[i] = ex2_approx(dl * A2[i]) * h[i] + dlx * bb[i];
-                acc += cb[i] * h[i];
-            }
+            const float2 dl2 = make_float2(dl, dl), dx2 = make_float2(dlx, dlx);
+            const float2 e01 = mul2(dl2, make_float2(A2[0], A2[1])), e23 = mul2(dl2, make_float2(A2[2], A2[3]));
+            float2 h01 = make_float2(h[0], h[1]), h23 = make_float2(h[2], h[3]);
+            h01 = fma2(make_float2(ex2_approx(e01.x), ex2_approx(e01.y)), h01, mul2(dx2, make_float2(bv.x, bv.y)));
+            h23 = fma2(make_float2(ex2_approx(e23.x), ex2_approx(e23.y)), h23, mul2(dx2, make_float2(bv.z, bv.w)));
+            h[0] = h01.x; h[1] = h01.y; h[2] = h23.x; h[3] = h23.y;
+            const float2 ac = fma2(make_float2(cv.z, cv.w), h23, mul2(make_float2(cv.x, cv.y), h01));
+            float acc = ac.x + ac.y;
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(h[0], h[1], h[2], h[3]);
 #pragma unroll
             for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -313,19 +318,30 @@ __global__ void __launch_bounds__(kBThreads, 4)
             const float dov = sm[lay.dout + c * kRow + t];
             const float4 bv = *reinterpret_cast<const float4*>(sm + lay.bs + t * N + kBS * gi);
             const float4 cv = *reinterpret_cast<const float4*>(sm + lay.cs + t * N + kBS * gi);
-            const float bb[kBS] = {bv.x, bv.y, bv.z, bv.w}, cb[kBS] = {cv.x, cv.y, cv.z, cv.w};
-            float gx = 0.f, gd = 0.f, Gt[kBS];
+            // states in pairs (f32x2): E = exp(Delta A), G = g + do C, dx += G B,
+            // dDelta += G (B x + h_{t-1} E A), dA += G h_{t-1} E Delta, g <- G E
+            const float2 dl2 = make_float2(dl, dl), do2 = make_float2(dov, dov), xv2 = make_float2(xv, xv);
+            float2 gx2 = make_float2(0.f, 0.f), gd2 = make_float2(0.f, 0.f), G2[2];
 #pragma unroll
-            for (int i = 0; i < kBS; ++i) {
-                const float E = ex2_approx(dl * A2[i]);
-                Gt[i] = gcar[i] + dov * cb[i];
-                gx += Gt[i] * bb[i];
-                const float hE = hp[i] * E;
-                gd += Gt[i] * (bb[i] * xv + hE * Av[i]);
-                dAacc[i] += Gt[i] * hE * dl;
-                gcar[i] = Gt[i] * E;
+            for (int q = 0; q < 2; ++q) {
+                const float2 bq = q ? make_float2(bv.z, bv.w) : make_float2(bv.x, bv.y);
+                const float2 cq = q ? make_float2(cv.z, cv.w) : make_float2(cv.x, cv.y);
+                const float2 ea = mul2(dl2, make_float2(A2[2 * q], A2[2 * q + 1]));
+                const float2 E = make_float2(ex2_approx(ea.x), ex2_approx(ea.y));
+                const float2 G = fma2(do2, cq, make_float2(gcar[2 * q], gcar[2 * q + 1]));
+                gx2 = fma2(G, bq, gx2);
+                const float2 hE = mul2(make_float2(hp[2 * q], hp[2 * q + 1]), E);
+                gd2 = fma2(G, fma2(hE, make_float2(Av[2 * q], Av[2 * q + 1]), mul2(bq, xv2)), gd2);
+                const float2 da = fma2(mul2(G, hE), dl2, make_float2(dAacc[2 * q], dAacc[2 * q + 1]));
+                dAacc[2 * q] = da.x;
+                dAacc[2 * q + 1] = da.y;
+                const float2 gn = mul2(G, E);
+                gcar[2 * q] = gn.x;
+                gcar[2 * q + 1] = gn.y;
+                G2[q] = G;
             }
-            gx *= dl;
+            float gx = (gx2.x + gx2.y) * dl, gd = gd2.x + gd2.y;
+            const float Gt[kBS] = {G2[0].x, G2[0].y, G2[1].x, G2[1].y};
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(Gt[0], Gt[1], Gt[2], Gt[3]);
 #pragma unroll
             for (int off = 1; off < TPC; off <<= 1) {
