@@ -183,7 +183,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace, size_t wo
  *   A_re, A_im  : [D, N]        float32
  *   lam         : [Bt, D, L]    in_dtype (the trapezoid weight, after the caller's sigmoid)
  *   h0, h_final : [Bt, D, N, 2] float32 complex (re, im) pairs (nullable)
- * Limits: dstate in {4, 8, 16, 32, 64} (else SSM_ERR_UNSUPPORTED); no workspace.
+ * Limits: dstate in {4, 8, 16, 32, 64} (else SSM_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------- */
 typedef struct {
     int batch, dim, dstate, seqlen, ngroups;
@@ -204,7 +204,14 @@ typedef struct {
     float* h_final;
 } ssm_mamba3_params;
 
-ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream);
+/* Device scratch ssm_mamba3_scan_fwd needs, in bytes: 0 unless the sequence is split
+ * into time segments (few channels, long L), then the segments' end states and sums of
+ * Delta. */
+size_t ssm_mamba3_scan_workspace_size(const ssm_mamba3_params* p);
+
+/* `workspace`: at least ssm_mamba3_scan_workspace_size(p) bytes (may be NULL when 0). */
+ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * S4D: linear time-invariant SSM, complex diagonal A, exact ZOH

@@ -219,7 +219,7 @@ def ssm_scan_bwd_workspace_size(x, B, dy_dtype=None) -> int:
 
 def ssm_mamba3_scan_fwd(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_bias=None,
                         delta_softplus=True, h0=None, *, y=None, h_final=None, out_dtype=None,
-                        return_final_state=False, stream=None):
+                        return_final_state=False, workspace=None, stream=None):
     """Mamba-3 scan: complex diagonal A = A_re + i A_im, exponential-trapezoidal rule.
 
     x, delta, lam, z: [batch, dim, L] (bfloat16 or float32); B, C: [batch, G, N, L];
@@ -256,7 +256,13 @@ def ssm_mamba3_scan_fwd(x, delta, A_re, A_im, lam, B, C, D=None, z=None, delta_b
     p.h0 = _ptr(h0, "h0", (batch, dim, N, 2), f32)
     p.y = _ptr(y, "y", (batch, dim, L))
     p.h_final = _ptr(h_final, "h_final", (batch, dim, N, 2), f32)
-    _lib.check(lib().ssm_mamba3_scan_fwd(ctypes.byref(p), _stream(stream)))
+    need = int(lib().ssm_mamba3_scan_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    _lib.check(lib().ssm_mamba3_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
     return (y, h_final) if return_final_state else y
 
 

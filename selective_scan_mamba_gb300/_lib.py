@@ -79,7 +79,7 @@ class StepParams(ctypes.Structure):
 
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
-           "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd",
+           "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_mamba3_scan_workspace_size", "ssm_s4d_scan_fwd",
            "ssm_s4d_scan_workspace_size",
            "ssm_s4d_kernel", "ssd_scan_bwd", "ssd_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
@@ -113,7 +113,9 @@ def load(build_if_missing: bool = True):
             lib.ssm_scan_bwd_workspace_size.restype = sz
             lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
             lib.ssm_mamba3_scan_fwd.restype = _i
-            lib.ssm_mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Params), _vp]
+            lib.ssm_mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Params), _vp, sz, _vp]
+            lib.ssm_mamba3_scan_workspace_size.restype = sz
+            lib.ssm_mamba3_scan_workspace_size.argtypes = [ctypes.POINTER(Mamba3Params)]
             lib.ssm_s4d_scan_fwd.restype = _i
             lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp, sz, _vp]
             lib.ssm_s4d_scan_workspace_size.restype = sz

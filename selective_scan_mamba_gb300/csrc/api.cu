@@ -335,7 +335,15 @@ size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
     return plan.kind == ssm::M1Plan::kTmem ? plan.ws_bytes : 0;
 }
 
-ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream) {
+size_t ssm_mamba3_scan_workspace_size(const ssm_mamba3_params* p) {
+    if (p == nullptr || p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->ngroups < 1 ||
+        p->dim % p->ngroups != 0 || !ssm::m3_supported(p->dstate))
+        return 0;
+    return ssm::m3_workspace_size(*p);
+}
+
+ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* workspace, size_t workspace_bytes,
+                               void* stream) {
     g_err[0] = '\0';
     REQUIRE(p != nullptr, "params is NULL");
     REQUIRE(p->batch >= 1 && p->dim >= 1 && p->dstate >= 1 && p->seqlen >= 0 && p->ngroups >= 1,
@@ -373,7 +381,12 @@ ssm_status ssm_mamba3_scan_fwd(const ssm_mamba3_params* p, void* stream) {
         }
         return SSM_OK;
     }
-    cudaError_t e = ssm::m3_launch(*p, s);
+    const size_t need = ssm::m3_workspace_size(*p);
+    if (workspace_bytes < need)
+        return fail(SSM_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace)))
+        return fail(SSM_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+    cudaError_t e = ssm::m3_launch(*p, workspace, s);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_mamba3_scan_fwd launch");
     return SSM_OK;
 }

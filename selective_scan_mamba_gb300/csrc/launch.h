@@ -41,7 +41,8 @@ cudaError_t ssd_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_
 
 // Mamba-3 complex scan (scan_m3.cu)
 bool m3_supported(int dstate);
-cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s);
+size_t m3_workspace_size(const ssm_mamba3_params& a);
+cudaError_t m3_launch(const ssm_mamba3_params& a, void* workspace, cudaStream_t s);
 
 // S4D (s4d.cu)
 bool s4d_supported(int dstate);

@@ -13,7 +13,9 @@
 // weights p_t = (1 - lambda_t) Delta_t x_{t-1} and q_t = lambda_t Delta_t x_t, x and the
 // gate, and the B rows t0-1 .. t0+31 and C rows of the group; the recurrence then reads
 // shared memory only, sums Re(C h) over the channel's threads with shuffles, and the
-// chunk's outputs leave in coalesced rows.
+// chunk's outputs leave in coalesced rows.  When that leaves few CTAs, the sequence is
+// cut into time segments (a states-only pass over all but the last, then every segment
+// from the state carried through the ones before it).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -53,13 +55,24 @@ __device__ __forceinline__ void sincos_reduced(float x, float* s, float* c) {
     __sincosf(r, s, c);
 }
 
-template <typename Tin, typename Tout, int TPC>
-__global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cps) {
+// STATES: the segment pass of a time-split scan.  Segment `seg` covers steps
+// [seg * seg_len, (seg + 1) * seg_len); this pass runs segments 0 .. nseg-2 from a zero
+// state and writes their end states and sums of Delta (no outputs).  The main pass starts
+// segment seg from h0 carried through those: h <- exp(A sum Delta_j) h + h_end(j).  The
+// trapezoid's left-end term at a segment's first step reads x and B of the step before,
+// so each segment (in both passes) adds it as an input from a zero-state start.
+template <typename Tin, typename Tout, int TPC, bool STATES>
+__global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cps, int nseg, int seg_len,
+                                                     float* seg_state, float* seg_dsum) {
     constexpr int N = TPC * kMS;
     constexpr int CPB = kMThreads / TPC;
     const int L = a.seqlen, Dm = a.dim, G = a.ngroups;
     const int per_group = Dm / G;
-    const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
+    const int segs_here = STATES ? nseg - 1 : nseg;
+    const int seg = blockIdx.x % segs_here;
+    const int rest = blockIdx.x / segs_here;
+    const int tbeg = seg * seg_len, tend = min(L, tbeg + seg_len);
+    const int pair = rest / cps, part_i = rest % cps;
     const int b = pair / G, g = pair % G;
     const int l0 = static_cast<int>((static_cast<long long>(part_i) * per_group) / cps);
     const int l1 = static_cast<int>((static_cast<long long>(part_i + 1) * per_group) / cps);
@@ -81,6 +94,7 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
     const Tin* Cp = static_cast<const Tin*>(a.C);
     const size_t bc_base = (static_cast<size_t>(b) * G + g) * N * static_cast<size_t>(L);
 
+    const size_t rows = static_cast<size_t>(a.batch) * Dm;
     float are2[kMS], aim[kMS], hr[kMS], hi[kMS];
 #pragma unroll
     for (int i = 0; i < kMS; ++i) {
@@ -88,13 +102,28 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
         are2[i] = a.A_re[k] * SSM_LOG2E;
         aim[i] = a.A_im[k];
         const size_t hk = (row * N + kMS * gi + i) * 2;
-        hr[i] = (active && a.h0) ? a.h0[hk] : 0.f;
-        hi[i] = (active && a.h0) ? a.h0[hk + 1] : 0.f;
+        hr[i] = (!STATES && active && a.h0) ? a.h0[hk] : 0.f;
+        hi[i] = (!STATES && active && a.h0) ? a.h0[hk + 1] : 0.f;
+        if (!STATES && active) {
+            // carry through the earlier segments: h <- exp(A sum Delta_j) h + h_end(j)
+            for (int j = 0; j < seg; ++j) {
+                const float ds = seg_dsum[j * rows + row];
+                const float mag = expf(a.A_re[k] * ds);
+                float sn, cs;
+                sincosf(aim[i] * ds, &sn, &cs);
+                const float ar = mag * cs, ai = mag * sn;
+                const float* hs = seg_state + ((j * rows + row) * N + kMS * gi + i) * 2;
+                const float nr = ar * hr[i] - ai * hi[i] + hs[0];
+                hi[i] = ar * hi[i] + ai * hr[i] + hs[1];
+                hr[i] = nr;
+            }
+        }
     }
     const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
+    float dsum = 0.f;  // sum of Delta over the segment (segment pass)
 
-    for (int t0 = 0; t0 < L; t0 += kMT) {
-        const int tl = min(kMT, L - t0);
+    for (int t0 = tbeg; t0 < tend; t0 += kMT) {
+        const int tl = min(kMT, tend - t0);
         __syncthreads();  // the previous chunk's tiles and outputs are done with
         for (int j = tid; j < CPB * kMT; j += kMThreads) {
             const int cc = j / kMT, t = j % kMT;
@@ -133,6 +162,7 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
             const float bpa[kMS] = {bp.x, bp.y, bp.z, bp.w}, bca[kMS] = {bc.x, bc.y, bc.z, bc.w};
             const float cva[kMS] = {cv.x, cv.y, cv.z, cv.w};
             float acc = 0.f;
+            if (STATES) dsum += dl;
 #pragma unroll
             for (int i = 0; i < kMS; ++i) {
                 const float mag = ex2_approx(dl * are2[i]);
@@ -142,13 +172,16 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
                 const float pr = hr[i] + p * bpa[i], pi = hi[i];
                 hr[i] = ar * pr - ai * pi + q * bca[i];
                 hi[i] = ar * pi + ai * pr;
-                acc += cva[i] * hr[i];
+                if (!STATES) acc += cva[i] * hr[i];
             }
+            if (!STATES) {
 #pragma unroll
-            for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (gi == 0)
-                sm[lay.y + c * kMRow + t] = (acc + Dd * sm[lay.x + c * kMRow + t]) * sm[lay.gate + c * kMRow + t];
+                for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (gi == 0)
+                    sm[lay.y + c * kMRow + t] = (acc + Dd * sm[lay.x + c * kMRow + t]) * sm[lay.gate + c * kMRow + t];
+            }
         }
+        if (STATES) continue;
         __syncthreads();
         for (int j = tid; j < CPB * kMT; j += kMThreads) {
             const int cc = j / kMT, t = j % kMT;
@@ -157,7 +190,17 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
             io<Tout>::store(static_cast<Tout*>(a.y), i, sm[lay.y + cc * kMRow + t]);
         }
     }
-    if (active && a.h_final) {
+    if (STATES) {
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < kMS; ++i) {
+                float* hs = seg_state + ((seg * rows + row) * N + kMS * gi + i) * 2;
+                hs[0] = hr[i];
+                hs[1] = hi[i];
+            }
+            if (gi == 0) seg_dsum[seg * rows + row] = dsum;
+        }
+    } else if (active && a.h_final && seg == nseg - 1) {
 #pragma unroll
         for (int i = 0; i < kMS; ++i) {
             const size_t hk = (row * N + kMS * gi + i) * 2;
@@ -167,28 +210,77 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
     }
 }
 
-template <typename Tin, typename Tout, int TPC>
-cudaError_t launch_m3(const ssm_mamba3_params& a, cudaStream_t s) {
-    constexpr int CPB = kMThreads / TPC;
+// Time split: when the channel blocks fill fewer than two CTAs per SM, the sequence is
+// cut into segments so that about two run; each segment at least 256 steps and a whole
+// number of chunks.  (The states-only pass costs about as much as the extra occupancy
+// gains at 2.5 CTAs per SM: 1.08 ms unsplit against ~1.12 ms in two segments on the
+// 8 x 1536-channel layer.)
+struct M3Plan {
+    int cps, nseg, seg_len;
+    size_t off_dsum, ws_bytes;
+};
+M3Plan m3_plan(const ssm_mamba3_params& a) {
+    const int tpc = a.dstate / kMS;
+    const int cpb = kMThreads / tpc;
     const int per_group = a.dim / a.ngroups;
-    const int cps = (per_group + CPB - 1) / CPB;
+    M3Plan p;
+    p.cps = (per_group + cpb - 1) / cpb;
+    const long long base = static_cast<long long>(a.batch) * a.ngroups * p.cps;
+    int sms = 148, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long want = (2LL * sms + base - 1) / base;
+    const long long by_len = a.seqlen / 256;
+    if (want > by_len) want = by_len;
+    if (want > 64) want = 64;
+    p.nseg = want < 1 ? 1 : static_cast<int>(want);
+    const int chunks = (a.seqlen + kMT - 1) / kMT;
+    p.seg_len = ((chunks + p.nseg - 1) / p.nseg) * kMT;
+    if (p.seg_len == 0) p.seg_len = kMT;
+    p.nseg = (a.seqlen + p.seg_len - 1) / p.seg_len;
+    if (p.nseg < 1) p.nseg = 1;
+    const size_t rows = static_cast<size_t>(a.batch) * a.dim;
+    const size_t st = static_cast<size_t>(p.nseg - 1) * rows * a.dstate * 2 * sizeof(float);
+    p.off_dsum = (st + 255) / 256 * 256;
+    p.ws_bytes = p.nseg > 1 ? p.off_dsum + static_cast<size_t>(p.nseg - 1) * rows * sizeof(float) : 0;
+    return p;
+}
+
+template <typename Tin, typename Tout, int TPC, bool STATES>
+cudaError_t launch_m3_pass(const ssm_mamba3_params& a, const M3Plan& p, int grid, float* st, float* ds,
+                           cudaStream_t s) {
+    constexpr int CPB = kMThreads / TPC;
     const M3Layout lay(CPB, TPC * kMS);
     const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
-    auto k = m3_scan<Tin, Tout, TPC>;
+    auto k = m3_scan<Tin, Tout, TPC, STATES>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k<<<a.batch * a.ngroups * cps, kMThreads, smem, s>>>(a, cps);
+    k<<<grid, kMThreads, smem, s>>>(a, p.cps, p.nseg, p.seg_len, st, ds);
     return cudaGetLastError();
 }
 
+template <typename Tin, typename Tout, int TPC>
+cudaError_t launch_m3(const ssm_mamba3_params& a, void* ws, cudaStream_t s) {
+    const M3Plan p = m3_plan(a);
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    float* st = reinterpret_cast<float*>(base);
+    float* ds = base ? reinterpret_cast<float*>(base + p.off_dsum) : nullptr;
+    const int grid1 = a.batch * a.ngroups * p.cps;
+    if (p.nseg > 1) {
+        cudaError_t e = launch_m3_pass<Tin, Tout, TPC, true>(a, p, grid1 * (p.nseg - 1), st, ds, s);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_m3_pass<Tin, Tout, TPC, false>(a, p, grid1 * p.nseg, st, ds, s);
+}
+
 template <typename Tin, typename Tout>
-cudaError_t dispatch_m3(const ssm_mamba3_params& a, cudaStream_t s) {
+cudaError_t dispatch_m3(const ssm_mamba3_params& a, void* ws, cudaStream_t s) {
     switch (a.dstate) {
-        case 4: return launch_m3<Tin, Tout, 1>(a, s);
-        case 8: return launch_m3<Tin, Tout, 2>(a, s);
-        case 16: return launch_m3<Tin, Tout, 4>(a, s);
-        case 32: return launch_m3<Tin, Tout, 8>(a, s);
-        case 64: return launch_m3<Tin, Tout, 16>(a, s);
+        case 4: return launch_m3<Tin, Tout, 1>(a, ws, s);
+        case 8: return launch_m3<Tin, Tout, 2>(a, ws, s);
+        case 16: return launch_m3<Tin, Tout, 4>(a, ws, s);
+        case 32: return launch_m3<Tin, Tout, 8>(a, ws, s);
+        case 64: return launch_m3<Tin, Tout, 16>(a, ws, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -199,12 +291,17 @@ bool m3_supported(int dstate) {
     return dstate == 4 || dstate == 8 || dstate == 16 || dstate == 32 || dstate == 64;
 }
 
-cudaError_t m3_launch(const ssm_mamba3_params& a, cudaStream_t s) {
+size_t m3_workspace_size(const ssm_mamba3_params& a) {
+    if (a.seqlen <= 0) return 0;
+    return m3_plan(a).ws_bytes;
+}
+
+cudaError_t m3_launch(const ssm_mamba3_params& a, void* workspace, cudaStream_t s) {
     const bool ib = a.in_dtype == SSM_BF16, ob = a.out_dtype == SSM_BF16;
-    if (ib && ob) return dispatch_m3<bf16_t, bf16_t>(a, s);
-    if (ib) return dispatch_m3<bf16_t, float>(a, s);
-    if (ob) return dispatch_m3<float, bf16_t>(a, s);
-    return dispatch_m3<float, float>(a, s);
+    if (ib && ob) return dispatch_m3<bf16_t, bf16_t>(a, workspace, s);
+    if (ib) return dispatch_m3<bf16_t, float>(a, workspace, s);
+    if (ob) return dispatch_m3<float, bf16_t>(a, workspace, s);
+    return dispatch_m3<float, float>(a, workspace, s);
 }
 
 }  // namespace ssm

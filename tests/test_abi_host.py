@@ -231,7 +231,7 @@ def mamba3_params(**kw):
 ])
 def test_mamba3_rejects_bad_arguments(lib, field, value, status):
     p = mamba3_params(**{field: value})
-    assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), None) == status
+    assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
     assert lib.ssm_last_error()
 
 

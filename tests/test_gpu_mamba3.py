@@ -102,3 +102,12 @@ def test_one_step_and_empty(oracle_mod):
 def test_130m_layer_shape(oracle_mod):
     """The 130m layer's channel count and dstate, 512 steps, every output compared."""
     _case(oracle_mod, 1, 1536, 16, 512, 1, synth.BF16, seed=4)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_time_split_long_sequence(oracle_mod, out):
+    """Few channels and a long sequence: the plan cuts the sequence into segments (a
+    states-only pass, then each segment from the carried state), including the
+    trapezoid's left-end term at every segment boundary; complex h0 and h_final."""
+    _case(oracle_mod, 1, 16, 16, 2600, 1, synth.F32 if out == "f32" else synth.BF16, seed=13,
+          out=out)
