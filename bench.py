@@ -214,6 +214,56 @@ def time_launches(torch, fn, n, warmup, stream):
     return e0.elapsed_time(e1) / 1e3 / n
 
 
+def host_link_peak(torch, h_in, d_in, d_out, h_out, in_streams, out_stream, stream, reps):
+    """Rate of the host link for one end-to-end step's transfers, the e2e leg's roofline.
+
+    Copies the given pinned host tensors to device buffers, each on its own stream, while
+    a device buffer of the output's size goes back to pinned host memory on another, and
+    times `reps` repetitions with CUDA events.  `floor_ms` is the time one step's bytes
+    need on this link with both directions busy at once; `h2d_gbs` and `d2h_gbs` are the
+    one-direction rates."""
+    def run(h2d, d2h):
+        start = torch.cuda.Event()
+        start.record(stream)
+        evs = []
+        if h2d:
+            for cs, src, dst in zip(in_streams, h_in, d_in.values()):
+                cs.wait_event(start)
+                with torch.cuda.stream(cs):
+                    dst.copy_(src, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                evs.append(ev)
+        if d2h:
+            out_stream.wait_event(start)
+            with torch.cuda.stream(out_stream):
+                h_out.copy_(d_out, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(out_stream)
+            evs.append(ev)
+        for ev in evs:
+            stream.wait_event(ev)
+
+    def timed(h2d, d2h):
+        run(h2d, d2h)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            run(h2d, d2h)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = h_out.numel() * h_out.element_size()
+    t_both, t_in, t_out = timed(True, True), timed(True, False), timed(False, True)
+    return {"floor_ms": t_both * 1e3, "both_gbs": (bi + bo) / t_both / 1e9,
+            "h2d_gbs": bi / t_in / 1e9, "d2h_gbs": bo / t_out / 1e9,
+            "source": "pinned host <-> device copies of one step's bytes, timed in this run"}
+
+
 def max_over_ranks(dist, value, device):
     """The largest of the ranks' values (the job's time is its slowest rank's); the value
     itself when there is no process group."""
@@ -296,20 +346,22 @@ def bench_ours(args, rank, world):
 
     # end to end through the public API with host buffers: every step copies its inputs
     # in from pinned host memory and its y back, inside the timed region.  Each input has
-    # its own copy stream (concurrent host-to-device copies) and the device buffers
-    # alternate between two sets, so the copies of step i+1 overlap the scan of step i;
-    # a copy into a set waits for the scan (and y read-back) that last used it.
+    # its own copy stream (concurrent host-to-device copies), y goes back on a stream of
+    # its own (so the next scan does not queue behind the read-back), and the device
+    # buffers rotate through --e2e-sets sets, so the copies of step i+1 overlap the scan and
+    # read-back of step i; a copy into a set waits for the read-back that last used it.
     host = {n: t.cpu().pin_memory() for n, t in sets[0].items() if n in ("x", "delta", "z", "B", "C")}
-    dbufs = [{n: torch.empty_like(sets[0][n]) for n in host} for _ in range(2)]
-    ybufs = [torch.empty_like(sets[0]["y"]) for _ in range(2)]
-    y_hosts = [torch.empty(sets[0]["y"].shape, dtype=sets[0]["y"].dtype).pin_memory() for _ in range(2)]
+    nbuf = max(2, args.e2e_sets)
+    dbufs = [{n: torch.empty_like(sets[0][n]) for n in host} for _ in range(nbuf)]
+    ybufs = [torch.empty_like(sets[0]["y"]) for _ in range(nbuf)]
+    y_hosts = [torch.empty(sets[0]["y"].shape, dtype=sets[0]["y"].dtype).pin_memory() for _ in range(nbuf)]
     copy_streams = [torch.cuda.Stream() for _ in host]
+    d2h_stream = torch.cuda.Stream()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = y_hosts[0].numel() * y_hosts[0].element_size()
-    last_use = [None, None]
+    last_use = [None] * nbuf
 
-    def e2e_step(i, start=None):
-        k = i % 2
+    def h2d_copies(k, start):
         buf, evs = dbufs[k], []
         for cs, (n, t) in zip(copy_streams, host.items()):
             if start is not None:
@@ -321,29 +373,43 @@ def bench_ours(args, rank, world):
                 ev = torch.cuda.Event()
                 ev.record(cs)
             evs.append(ev)
+        return buf, evs
+
+    def e2e_step(i, start=None):
+        k = i % nbuf
+        buf, evs = h2d_copies(k, start)
         for ev in evs:
             stream.wait_event(ev)
+        if last_use[k] is not None:
+            stream.wait_event(last_use[k])  # ybufs[k] is free once its read-back is done
         s = sets[0]
         y = ssm.ssm_scan_fwd(buf["x"], buf["delta"], s["A"], buf["B"], buf["C"], D=s["D"],
                              z=buf["z"], delta_bias=s["delta_bias"], y=ybufs[k])
-        y_hosts[k].copy_(y, non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(stream)
+        scanned = torch.cuda.Event()
+        scanned.record(stream)
+        d2h_stream.wait_event(scanned)
+        with torch.cuda.stream(d2h_stream):
+            y_hosts[k].copy_(y, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(d2h_stream)
         last_use[k] = done
 
     e2e_steps = max(3, min(args.steps, 20))
-    for i in range(2):
+    for i in range(nbuf):
         e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(e2e_steps):
-        e2e_step(i, start=e0 if i < 2 else None)
+        e2e_step(i, start=e0 if i < nbuf else None)
+    for ev in last_use:
+        stream.wait_event(ev)  # the timed region ends after the last read-back
     e1.record(stream)
     torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3 / e2e_steps
-    t_e2e = max_over_ranks(dist, t_e2e, "cuda")
+    t_e2e = max_over_ranks(dist, e0.elapsed_time(e1) / 1e3 / e2e_steps, "cuda")
+    link = host_link_peak(torch, list(host.values()), dbufs[0], ybufs[0], y_hosts[0],
+                          copy_streams, d2h_stream, stream, e2e_steps)
 
     paths = {}
     if rank == 0 and not args.headline_only:
@@ -373,7 +439,9 @@ def bench_ours(args, rank, world):
                              "frac": gbs / peaks["hbm_gbs"],
                              "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}},
         "e2e": {"value": whole_job_rate(updates, world, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+                "link_gbs": (h2d + d2h) / t_e2e / 1e9,
+                "link_peak": link, "link_frac": link["floor_ms"] / (t_e2e * 1e3), "buffer_sets": nbuf},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "paths": paths,
@@ -810,6 +878,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the SSD, decode and long-context measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-sets", type=int, default=3,
+                    help="device buffer sets the end-to-end leg rotates through (>= 2)")
     ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens", "bwd",
                                        "m3", "s4d"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
