@@ -591,6 +591,54 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
     out["decode_780m_tokens"] = dict(tok_runs, note="T consecutive tokens per call; 4 layer "
                                      "states rotate (403 MB > L2)")
     del states
+    # serving loop over a hybrid stack: Mamba-1-form layers (790m-shaped: 3072 channels,
+    # 16 states, A per state) alternate with Mamba-2-form layers (780m-shaped); one CUDA
+    # graph of 256 tokens through all four layers, 8 token sets rotating
+    c3 = synth.WORKLOADS["m1_790m_long"]
+    stack = [(c3["dim"], 1, c3["dstate"], 1, True), (H, P, N, G, False)] * 2
+    lays = []
+    for li, (Hl, Pl, Nl, Gl, m1) in enumerate(stack):
+        lays.append(dict(
+            par=_dev(synth.step_params(Hl, Nl, a_per_state=m1, seed=li), torch),
+            state=torch.from_numpy(synth.step_state(Bt, Hl, Pl, Nl, seed=li)).cuda(),
+            toks=[_dev(synth.step_tokens(Bt, Hl, Pl, Nl, Gl, step=k, seed=li), torch)
+                  for k in range(8)],
+            y=torch.empty((Bt, Hl, Pl), dtype=torch.bfloat16, device="cuda")))
+
+    def mixed_token(i):
+        for lay in lays:
+            tk, pr = lay["toks"][i % 8], lay["par"]
+            ssm.ssm_state_update(lay["state"], tk["x"], tk["dt"], pr["A"], tk["B"], tk["C"],
+                                 D=pr["D"], z=tk["z"], dt_bias=pr["dt_bias"], y=lay["y"])
+    ntok = 256
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        for i in range(2):
+            mixed_token(i)
+    stream.wait_stream(gs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(ntok):
+            mixed_token(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ttok = e0.elapsed_time(e1) / 1e3 / ntok
+    mb = sum(step_bytes(Bt, Hl, Pl, Nl, Gl) for Hl, Pl, Nl, Gl, _ in stack)
+    mupd = sum(Bt * Hl * Pl * Nl for Hl, Pl, Nl, Gl, _ in stack)
+    out["decode_mixed_stack"] = {
+        "us_per_token": ttok * 1e6, "tokens": ntok, "layers": len(stack),
+        "state_updates_per_s": mupd / ttok, "hbm_gbs": mb / ttok / 1e9,
+        "hbm_frac": mb / ttok / 1e9 / hbm, "bytes_per_token": mb,
+        "note": f"batch {Bt}; Mamba-1 form {c3['dim']} channels x {c3['dstate']} states and "
+                f"Mamba-2 form {H} x {P} x {N}, alternating; one CUDA graph of {ntok} tokens"}
+    del graph, lays
     # Mamba-1 backward on the 130m layer: dy in, every gradient out (float32)
     c1 = synth.WORKLOADS["m1_130m_layer"]
     Bt1, D1, N1, L1 = c1["batch"], c1["dim"], c1["dstate"], c1["seqlen"]

@@ -158,3 +158,62 @@ def test_tokens_register_kernel_shapes(oracle_mod, N, P, T):
     divide the CTA span (P = 40, 48, 100), CTAs whose rows cross a group, several staged
     token blocks (T > block) and a ragged last token group."""
     _tokens(oracle_mod, 2, 4, P, N, 2, T, synth.BF16, calls=1)
+
+
+# A hybrid stack for the serving loop: (heads, headdim, dstate, groups, Mamba-1 form).  The
+# Mamba-1 form has one channel per head (P = 1) and A per (channel, state).
+MIXED_STACK = [
+    (96, 1, 16, 1, True),
+    (4, 16, 64, 2, False),
+    (48, 1, 16, 1, True),
+    (6, 8, 128, 1, False),
+]
+
+
+def test_mixed_stack_cuda_graph_serving_loop(oracle_mod):
+    """A decode serving loop captured once as a CUDA graph: T tokens, each through a stack
+    whose layers alternate the Mamba-1 form and the Mamba-2 form (scalar A per head, two
+    groups in one layer).  The graph is replayed twice, every layer's state carried from
+    one replay to the next; each y and each state is checked against the oracle stepping
+    the same layers in the same order."""
+    import torch
+    batch, T = 4, 5
+    layers = []
+    for li, (H, P, N, G, m1) in enumerate(MIXED_STACK):
+        par = synth.step_params(H, N, a_per_state=m1, seed=40 + li)
+        st0 = synth.step_state(batch, H, P, N, seed=40 + li)
+        toks = [synth.step_tokens(batch, H, P, N, G, step=k, seed=40 + li) for k in range(T)]
+        layers.append(dict(
+            par=par, tp=to_device(par), st0=st0, state=torch.from_numpy(st0).cuda(), toks=toks,
+            tt=[to_device(tk) for tk in toks],
+            ys=[torch.empty((batch, H, P), dtype=torch.float32, device="cuda") for _ in range(T)]))
+
+    def loop(states):
+        for k in range(T):
+            for lay, st in zip(layers, states):
+                tt, tp = lay["tt"][k], lay["tp"]
+                ssm.ssm_state_update(st, tt["x"], tt["dt"], tp["A"], tt["B"], tt["C"], D=tp["D"],
+                                     z=tt["z"], dt_bias=tp["dt_bias"], y=lay["ys"][k])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        loop([lay["state"].clone() for lay in layers])  # first launches outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        loop([lay["state"] for lay in layers])
+    ref = [lay["st0"].astype(np.float64) for lay in layers]
+    for rep in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        for li, lay in enumerate(layers):
+            fp = lay["par"].f64
+            for k in range(T):
+                f = lay["toks"][k].f64
+                yr, ref[li] = oracle_mod.state_update(ref[li], f("x"), f("dt"), fp("A"), f("B"),
+                                                      f("C"), D=fp("D"), z=f("z"),
+                                                      dt_bias=fp("dt_bias"))
+                check(to_numpy(lay["ys"][k]), yr, TOL_BF16, what=f"replay {rep} layer {li} token {k}")
+            check(to_numpy(lay["state"]), ref[li], TOL_BF16, what=f"replay {rep} layer {li} state")
