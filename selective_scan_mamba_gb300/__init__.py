@@ -1,16 +1,22 @@
-"""selective_scan_mamba_gb300 -- GB300-native selective state-space scan.
+"""selective_scan_mamba_gb300 -- GB300-native selective state-space scans.
 
-A thin Python binding over libssmscan's C ABI (include/ssmscan.h).  The three entry
-points keep the C names:
+A thin Python binding over libssmscan's C ABI (include/ssmscan.h).  The functions keep
+the C names:
 
-  * ssm_scan_fwd        -- Mamba-1 selective scan (diagonal A per channel)
-  * ssd_chunk_scan_fwd  -- Mamba-2 chunked SSD scan (scalar A per head)
-  * ssm_state_update    -- one decode step, in place on the state
+  * ssm_scan_fwd, ssm_scan_bwd          -- Mamba-1 selective scan (diagonal A per channel)
+                                           and its gradients
+  * ssd_chunk_scan_fwd, ssd_scan_bwd    -- Mamba-2 chunked SSD scan (scalar A per head)
+                                           and its gradients
+  * ssm_state_update, ssm_state_update_tokens
+                                        -- decode: one token or T tokens, in place on the
+                                           state
+  * ssm_mamba3_scan_fwd                 -- Mamba-3 complex-diagonal scan
+  * ssm_s4d_scan_fwd, ssm_s4d_kernel    -- S4D recurrent form and convolution kernel
 
-Each takes CUDA torch tensors in the library's layouts, checks them, fills the C
-parameter struct and calls the library on the current torch stream.  Every step of
-the computation runs in the library's CUDA kernels; there is no CPU or PyTorch
-fallback, and a missing GPU or library raises.
+Each takes CUDA torch tensors of the current device in the library's layouts, checks
+them, fills the C parameter struct and calls the library on the current torch stream
+(or the one given).  Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and a missing GPU or library raises.
 """
 from __future__ import annotations
 
@@ -19,8 +25,13 @@ import ctypes
 from . import _lib
 from ._lib import SsmError  # noqa: F401
 
-__all__ = ["wait_timeouts", "ssm_state_update_tokens", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
-           "ssd_chunk_scan_workspace_size", "SsmError", "lib"]
+__all__ = [
+    "ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
+    "ssd_chunk_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_scan_bwd",
+    "ssd_scan_bwd_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
+    "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd", "ssm_s4d_kernel", "wait_timeouts", "SsmError",
+    "lib",
+]
 
 
 def wait_timeouts() -> int:
@@ -61,6 +72,9 @@ def _ptr(t, name, shape=None, dtype=None):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the call runs on the current device "
+                         f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -80,8 +94,12 @@ def _disc(disc):
 
 def _stream(stream):
     torch = _torch()
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {stream.device}, but the call runs on the current "
+                         f"device cuda:{torch.cuda.current_device()}")
+    return ctypes.c_void_p(stream.cuda_stream)
 
 
 def _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final, disc):

@@ -167,6 +167,46 @@ def test_python_binding_refuses_cpu_tensors():
                          torch.zeros(1, 16, 8, dtype=torch.bfloat16))
 
 
+def _tensor_on_cuda1(shape):
+    """A CPU tensor that reports itself as living on cuda:1, to reach the binding's
+    device check without a GPU."""
+    import torch
+
+    class OnCuda1(torch.Tensor):
+        @property
+        def is_cuda(self):
+            return True
+
+        @property
+        def device(self):
+            return torch.device("cuda", 1)
+
+    return torch.Tensor._make_subclass(OnCuda1, torch.zeros(shape))
+
+
+def test_python_binding_refuses_tensor_of_another_device(monkeypatch):
+    import torch
+    import selective_scan_mamba_gb300 as ssm
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="current device"):
+        ssm._ptr(_tensor_on_cuda1((4,)), "x")
+
+
+def test_python_binding_refuses_stream_of_another_device(monkeypatch):
+    import torch
+    import selective_scan_mamba_gb300 as ssm
+
+    class Stream1:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="current device"):
+        ssm._stream(Stream1())
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    assert ssm._stream(Stream1()).value in (None, 0)
+
+
 def scan_bwd_params(**kw):
     p = _lib.ScanBwdParams()
     p.fwd = scan_params()
