@@ -265,6 +265,9 @@ ssm_status check_ssd_sizes(const ssd_params* p) {
         return fail(SSM_ERR_UNSUPPORTED, "dstate=%d (supported: 64, 128)", p->dstate);
     if (p->headdim * p->dstate > 8192)
         return fail(SSM_ERR_UNSUPPORTED, "headdim*dstate=%d > 8192", p->headdim * p->dstate);
+    REQUIRE(static_cast<long long>(p->batch) * (p->seqlen > 0 ? p->seqlen : 1) * p->nheads * p->headdim <
+                (1LL << 40),
+            "tensor too large");
     return SSM_OK;
 }
 
@@ -299,6 +302,12 @@ ssm_status check_step(const ssm_step_params* p) {
     REQUIRE(p->disc == SSM_DISC_EXP_EULER || p->disc == SSM_DISC_ZOH, "unknown discretisation");
     REQUIRE(p->a_per_state == 0 || p->a_per_state == 1, "a_per_state must be 0 or 1");
     if (p->dstate > 4096) return fail(SSM_ERR_UNSUPPORTED, "dstate=%d > 4096", p->dstate);
+    REQUIRE(static_cast<long long>(p->batch) * p->nheads * p->headdim * p->dstate < (1LL << 40),
+            "state too large");
+    // the kernels keep (batch, head) indices and B/C row offsets in 32 bits
+    if (static_cast<long long>(p->batch) * p->nheads > (1LL << 31) - 1 ||
+        static_cast<long long>(p->batch) * p->ngroups * p->dstate > (1LL << 31) - 1)
+        return fail(SSM_ERR_UNSUPPORTED, "batch*nheads or batch*ngroups*dstate too large");
     REQUIRE_PTR(p->state, "state");
     REQUIRE_PTR(p->x, "x");
     REQUIRE_PTR(p->dt, "dt");

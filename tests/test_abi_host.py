@@ -167,6 +167,19 @@ def test_python_binding_refuses_cpu_tensors():
                          torch.zeros(1, 16, 8, dtype=torch.bfloat16))
 
 
+def test_size_ceilings_refuse_before_any_launch(lib):
+    """Problems past the index ranges the kernels use are refused, not wrapped."""
+    p = ssd_params(batch=4, seqlen=2**31 - 1)
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert "too large" in lib.ssm_last_error().decode()
+    p = step_params(batch=2**28)  # 2^41 state elements
+    assert lib.ssm_state_update(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
+    assert "too large" in lib.ssm_last_error().decode()
+    p = step_params(batch=2**26)  # B/C rows of 2^32 elements
+    assert lib.ssm_state_update(ctypes.byref(p), None) == _lib.SSM_ERR_UNSUPPORTED
+    assert "too large" in lib.ssm_last_error().decode()
+
+
 def _tensor_on_cuda1(shape):
     """A CPU tensor that reports itself as living on cuda:1, to reach the binding's
     device check without a GPU."""
