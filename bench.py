@@ -6,10 +6,15 @@ state updates per second (batch * L * d_inner * d_state / time) and as achieved 
 GB/s against the measured copy bandwidth.  One step = one ssm_scan_fwd call over one
 batch; several input sets (together larger than L2) rotate between steps.
 
+The end-to-end figure ("e2e") runs the same scan through the public API with pinned host
+buffers: every step copies its inputs in and y back inside the timed region, and the
+host link's own rate for those bytes is measured beside it ("e2e.link_peak").
+
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
-the decode update (780m-shaped, 1024 steps), multi-token decode, the Mamba-1 backward
-(130m layer), the SSD backward (130m SSD shape), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel) and
-the long-context Mamba-1 sweep.
+the decode update (780m-shaped, 1024 steps), multi-token decode, a decode serving loop
+over a hybrid Mamba-1/Mamba-2 stack, the Mamba-1 backward (130m layer), the SSD backward
+(130m SSD shape), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel)
+and the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
