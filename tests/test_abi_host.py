@@ -180,6 +180,49 @@ def test_size_ceilings_refuse_before_any_launch(lib):
     assert "too large" in lib.ssm_last_error().decode()
 
 
+# ctypes mirrors of the C parameter structs, by the header's typedef names
+C_STRUCTS = {
+    "ssm_scan_params": _lib.ScanParams,
+    "ssm_scan_bwd_params": _lib.ScanBwdParams,
+    "ssm_mamba3_params": _lib.Mamba3Params,
+    "ssm_s4d_params": _lib.S4dParams,
+    "ssd_params": _lib.SsdParams,
+    "ssd_bwd_params": _lib.SsdBwdParams,
+    "ssm_step_params": _lib.StepParams,
+}
+
+
+def test_ctypes_structs_match_the_header_layout(tmp_path):
+    """Every field offset and every struct size of the Python binding's ctypes mirrors
+    equals what a C compiler makes of include/ssmscan.h, so no argument lands in another
+    field's slot."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ssmscan.h"', 'int main(void) {']
+    for cname, cls in C_STRUCTS.items():
+        lines.append(f'    printf("{cname} . %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'    printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ['    return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    seen = 0
+    for line in out.splitlines():
+        cname, fname, value = line.split()
+        cls = C_STRUCTS[cname]
+        want = ctypes.sizeof(cls) if fname == "." else getattr(cls, fname).offset
+        assert int(value) == want, f"{cname}.{fname}: C says {value}, ctypes says {want}"
+        seen += 1
+    assert seen == sum(len(c._fields_) + 1 for c in C_STRUCTS.values())
+
+
 def _tensor_on_cuda1(shape):
     """A CPU tensor that reports itself as living on cuda:1, to reach the binding's
     device check without a GPU."""
