@@ -223,6 +223,49 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
     assert seen == sum(len(c._fields_) + 1 for c in C_STRUCTS.values())
 
 
+def _header_prototypes():
+    """(return type, name, [parameter types]) of every function include/ssmscan.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "ssmscan.h")).read(),
+                  flags=re.S)
+    out = []
+    for ret, name, args in re.findall(
+            r"^\s*(ssm_status|size_t|int|const char\s*\*|unsigned int)\s+(\w+)\s*\(([^)]*)\)\s*;",
+            text, re.M | re.S):
+        params = [] if args.strip() == "void" else [
+            " ".join(a.split()).rsplit(" ", 1)[0] if not a.strip().endswith("*") else a.strip()
+            for a in args.split(",")]
+        out.append((" ".join(ret.split()), name, params))
+    return out
+
+
+def _ctype_of(c_type):
+    """The ctypes type the binding must declare for a C parameter or return type."""
+    t = c_type.replace("const ", "").replace(" *", "*").strip()
+    if t.endswith("_params*"):
+        return ctypes.POINTER(C_STRUCTS[t[:-1]])
+    return {"void*": ctypes.c_void_p, "float*": ctypes.c_void_p, "size_t": ctypes.c_size_t,
+            "int": ctypes.c_int, "ssm_status": ctypes.c_int, "char*": ctypes.c_char_p,
+            "unsigned int": ctypes.c_uint}[t]
+
+
+def test_ctypes_signatures_match_the_header(lib):
+    """Every function the loader declares has the header's parameter count, parameter
+    types and return type; every symbol the binding calls is declared."""
+    protos = _header_prototypes()
+    assert {n for _, n, _ in protos} >= set(_lib.SYMBOLS) | {"ssm_wait_timeouts"}
+    checked = 0
+    for ret, name, params in protos:
+        fn = getattr(lib, name)
+        if fn.argtypes is None:  # not used by the binding (declared by its own test)
+            assert name not in _lib.SYMBOLS, name
+            continue
+        want = [_ctype_of(p) for p in params]
+        assert list(fn.argtypes) == want, f"{name}: argtypes {fn.argtypes} != header {params}"
+        assert fn.restype == _ctype_of(ret), f"{name}: restype {fn.restype} != header {ret}"
+        checked += 1
+    assert checked >= len(_lib.SYMBOLS)
+
+
 def _tensor_on_cuda1(shape):
     """A CPU tensor that reports itself as living on cuda:1, to reach the binding's
     device check without a GPU."""
