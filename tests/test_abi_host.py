@@ -192,10 +192,14 @@ C_STRUCTS = {
 }
 
 
+ENUM_CONSTANTS = ("SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA",
+                  "SSM_ERR_TIMEOUT", "SSM_F32", "SSM_BF16", "SSM_DISC_EXP_EULER", "SSM_DISC_ZOH")
+
+
 def test_ctypes_structs_match_the_header_layout(tmp_path):
-    """Every field offset and every struct size of the Python binding's ctypes mirrors
-    equals what a C compiler makes of include/ssmscan.h, so no argument lands in another
-    field's slot."""
+    """Every field offset and every struct size of the Python binding's ctypes mirrors,
+    and every enum constant it uses, equals what a C compiler makes of include/ssmscan.h,
+    so no argument lands in another field's slot."""
     import shutil
     import subprocess
     cc = shutil.which("gcc") or shutil.which("cc")
@@ -206,6 +210,8 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
         lines.append(f'    printf("{cname} . %zu\\n", sizeof({cname}));')
         for fname, _ in cls._fields_:
             lines.append(f'    printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    for const in ENUM_CONSTANTS:
+        lines.append(f'    printf("enum {const} %d\\n", (int){const});')
     lines += ['    return 0;', '}']
     src = tmp_path / "layout.c"
     src.write_text("\n".join(lines) + "\n")
@@ -216,11 +222,15 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
     seen = 0
     for line in out.splitlines():
         cname, fname, value = line.split()
+        if cname == "enum":
+            assert int(value) == getattr(_lib, fname), f"{fname}: C says {value}"
+            seen += 1
+            continue
         cls = C_STRUCTS[cname]
         want = ctypes.sizeof(cls) if fname == "." else getattr(cls, fname).offset
         assert int(value) == want, f"{cname}.{fname}: C says {value}, ctypes says {want}"
         seen += 1
-    assert seen == sum(len(c._fields_) + 1 for c in C_STRUCTS.values())
+    assert seen == sum(len(c._fields_) + 1 for c in C_STRUCTS.values()) + len(ENUM_CONSTANTS)
 
 
 def _header_prototypes():
