@@ -48,6 +48,13 @@ MUTATIONS = [
     ("s4d_output_imag_sign", "y[row + t] += C[k] * hr - C[k + 1] * hi;", "y[row + t] += C[k] * hr + C[k + 1] * hi;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
+    ("step_per_state_A_transposed", "double a = a_per_state ? A[(size_t)hd * dstate + n] : A[hd];",
+     "double a = a_per_state ? A[(size_t)n * nheads + hd] : A[hd];"),
+    ("step_y_before_update",
+     "hrow[n] = exp(d_t * a) * hrow[n] + input_weight(d_t, a, disc) * x[xi] * Bb[n];\n"
+     "                    acc += Cb[n] * hrow[n];",
+     "acc += Cb[n] * hrow[n];\n"
+     "                    hrow[n] = exp(d_t * a) * hrow[n] + input_weight(d_t, a, disc) * x[xi] * Bb[n];"),
 ]
 
 PIN_CHECKS = [
