@@ -48,6 +48,11 @@ MUTATIONS = [
     ("s4d_output_imag_sign", "y[row + t] += C[k] * hr - C[k + 1] * hi;", "y[row + t] += C[k] * hr + C[k + 1] * hi;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
+    ("ssd_causal_mask_drops_diagonal", "for (int j = 0; j <= i; ++j) {        /* decayed attention */",
+     "for (int j = 0; j < i; ++j) {        /* decayed attention */"),
+    ("ssd_exclusive_cumsum", "run += d_t * A[hd];\n                    cum[i] = run;",
+     "cum[i] = run;\n                    run += d_t * A[hd];"),
+    ("ssd_ragged_chunk_decay", "double chunk_decay = exp(cum[q - 1]);", "double chunk_decay = exp(cum[chunk - 1]);"),
     ("step_per_state_A_transposed", "double a = a_per_state ? A[(size_t)hd * dstate + n] : A[hd];",
      "double a = a_per_state ? A[(size_t)n * nheads + hd] : A[hd];"),
     ("step_y_before_update",
