@@ -48,6 +48,8 @@ MUTATIONS = [
     ("s4d_output_imag_sign", "y[row + t] += C[k] * hr - C[k + 1] * hi;", "y[row + t] += C[k] * hr + C[k + 1] * hi;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
+    ("zoh_phi1_of_A_not_DeltaA", "return delta * oracle_phi1(delta * a);", "return delta * oracle_phi1(a);"),
+    ("phi1_taylor_branch_inverted", "if (fabs(z) < 1e-4) return", "if (fabs(z) > 1e-4) return"),
     ("ssd_causal_mask_drops_diagonal", "for (int j = 0; j <= i; ++j) {        /* decayed attention */",
      "for (int j = 0; j < i; ++j) {        /* decayed attention */"),
     ("ssd_exclusive_cumsum", "run += d_t * A[hd];\n                    cum[i] = run;",
