@@ -38,6 +38,9 @@ MUTATIONS = [
     ("bwd_gate_derivative_sign", "(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
     ("bwd_dC_uses_prev_state", "dC[bc] += dout * hs[(tt + 1) * N + n];", "dC[bc] += dout * hs[tt * N + n];"),
     ("bwd_softplus_derivative", "ddt / (1.0 + exp(-v))", "ddt / (1.0 + exp(v))"),
+    ("bwd_dD_ignores_gate", "if (dD) dD[d] += dout * xt;", "if (dD) dD[d] += dy[row + tt] * xt;"),
+    ("bwd_dx_skip_term_dropped", "double dxt = Dskip ? dout * Dskip[d] : 0.0;", "double dxt = 0.0;"),
+    ("bwd_ddelta_decay_term_dropped", "ddt += Gt * (B[bc] * xt + hprev * E * a);", "ddt += Gt * B[bc] * xt;"),
     ("m3_left_end_dropped", "double pr = hr[n] + (1.0 - lt) * dt * up;", "double pr = hr[n];"),
     ("m3_rotation_sign", "hi[n] = ar * pi + ai * pr;", "hi[n] = ar * pi - ai * pr;"),
     ("m3_left_end_current_input", "double up = t > 0 ? B[bc - 1] * xp : 0.0;", "double up = t > 0 ? B[bc] * xt : 0.0;"),
