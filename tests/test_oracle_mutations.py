@@ -45,9 +45,20 @@ MUTATIONS = [
     ("m3_rotation_sign", "hi[n] = ar * pi + ai * pr;", "hi[n] = ar * pi - ai * pr;"),
     ("m3_left_end_current_input", "double up = t > 0 ? B[bc - 1] * xp : 0.0;", "double up = t > 0 ? B[bc] * xt : 0.0;"),
     ("m3_lambda_on_wrong_end", "hr[n] = ar * pr - ai * pi + lt * dt * cur;", "hr[n] = ar * pr - ai * pi + (1.0 - lt) * dt * cur;"),
+    ("m3_angle_without_delta", "double ang = dt * A_im[(size_t)d * N + n];", "double ang = A_im[(size_t)d * N + n];"),
+    ("m3_magnitude_sign", "double mag = exp(dt * A_re[(size_t)d * N + n]);", "double mag = exp(-dt * A_re[(size_t)d * N + n]);"),
     ("s4d_taylor_imag", "pi = zi / 2.0 + (2.0 * zr * zi) / 6.0;", "pi = zi / 2.0;"),
     ("s4d_expm1_term_dropped", "double nr = expm1(zr) * cos(zi) - 2.0 * s2 * s2;", "double nr = expm1(zr) * cos(zi);"),
     ("s4d_kernel_conjugate", "wi = wr * abi + wi * abr;", "wi = -wr * abi + wi * abr;"),
+    ("s4d_phi1_division_conjugate", "pi = (ni * zr - nr * zi) / den;", "pi = (ni * zr + nr * zi) / den;"),
+    ("s4d_in_place_complex_update",
+     "double nr = abr * hr - abi * hi + bbr * u[row + t];\n"
+     "                    hi = abr * hi + abi * hr + bbi * u[row + t];\n"
+     "                    hr = nr;",
+     "hr = abr * hr - abi * hi + bbr * u[row + t];\n"
+     "                    hi = abr * hi + abi * hr + bbi * u[row + t];"),
+    ("s4d_kernel_log_dt_as_dt", "double dt = exp(log_dt[d]);\n        for (size_t l = 0;",
+     "double dt = log_dt[d];\n        for (size_t l = 0;"),
     ("s4d_output_imag_sign", "y[row + t] += C[k] * hr - C[k + 1] * hi;", "y[row + t] += C[k] * hr + C[k + 1] * hi;"),
     ("step_skip_dropped", "if (Dskip) acc += Dskip[hd] * x[xi];\n                if (z) acc *= silu(z[xi]);\n                y[xi] = acc;",
      "if (z) acc *= silu(z[xi]);\n                y[xi] = acc;"),
