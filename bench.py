@@ -872,6 +872,17 @@ def run_case(args):
         for i in range(n):
             ssm.ssm_state_update(states[i % 4], tok["x"], tok["dt"], par["A"], tok["B"], tok["C"],
                                  D=par["D"], z=tok["z"], dt_bias=par["dt_bias"], y=y)
+    elif args.case == "step_m1":  # Mamba-1-form decode: batch 64, 3072 channels x 16 states
+        c5 = synth.WORKLOADS["step_780m"]
+        c3 = synth.WORKLOADS["m1_790m_long"]
+        Bt, H, N = c5["batch"], c3["dim"], c3["dstate"]
+        par = _dev(synth.step_params(H, N, a_per_state=True, seed=0), torch)
+        states = [torch.from_numpy(synth.step_state(Bt, H, 1, N, seed=k)).cuda() for k in range(4)]
+        tok = _dev(synth.step_tokens(Bt, H, 1, N, 1, step=0, seed=0), torch)
+        y = torch.empty((Bt, H, 1), dtype=torch.bfloat16, device="cuda")
+        for i in range(n):
+            ssm.ssm_state_update(states[i % 4], tok["x"], tok["dt"], par["A"], tok["B"], tok["C"],
+                                 D=par["D"], z=tok["z"], dt_bias=par["dt_bias"], y=y)
     elif args.case == "bwd":  # Mamba-1 backward, 130m layer
         cfg = synth.WORKLOADS["m1_130m_layer"]
         inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
@@ -933,8 +944,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--e2e-sets", type=int, default=3,
                     help="device buffer sets the end-to-end leg rotates through (>= 2)")
-    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "tokens", "bwd",
-                                       "m3", "s4d"],
+    ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "step_m1", "tokens",
+                                       "bwd", "m3", "s4d"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:
