@@ -380,11 +380,18 @@ def ssd_chunked(x, dt, A, B, C, chunk, D=None, z=None, dt_bias=None, dt_softplus
 
 
 def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True,
-                 disc=DISC_EXP_EULER):
-    """One decode step.  state: [batch, H, P, N] (a new array is returned, the
-    input is not modified); x, z: [batch, H, P]; dt: [batch, H]; B, C: [batch, G, N];
-    A: [H] or [H, N].  Returns (y [batch, H, P], new_state)."""
-    st = np.array(state, dtype=np.float64, copy=True, order="C")
+                 disc=DISC_EXP_EULER, inplace=False):
+    """One decode step.  state: [batch, H, P, N] (a new array is returned and the input is
+    not modified, unless ``inplace``: then ``state``, a C-contiguous float64 array, is
+    advanced in place and returned); x, z: [batch, H, P]; dt: [batch, H]; B, C:
+    [batch, G, N]; A: [H] or [H, N].  Returns (y [batch, H, P], new_state)."""
+    if inplace:
+        if not (isinstance(state, np.ndarray) and state.dtype == np.float64
+                and state.flags.c_contiguous):
+            raise ValueError("oracle: an in-place state must be a C-contiguous float64 array")
+        st = state
+    else:
+        st = np.array(state, dtype=np.float64, copy=True, order="C")
     batch, H, P, N = st.shape
     B = _f64(B)
     G = B.shape[1]

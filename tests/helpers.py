@@ -48,20 +48,56 @@ TOL_F32 = 1e-5
 TOL_BF16 = 2e-3
 
 
+def _as_f64(a, device):
+    """float64 torch tensor on ``device`` (no copy for a float64 numpy array on the CPU)."""
+    import torch
+    if isinstance(a, torch.Tensor):
+        return a.detach().to(device=device, dtype=torch.float64)
+    return torch.from_numpy(np.ascontiguousarray(a, np.float64)).to(device)
+
+
 def check(got, ref, tol, out_bf16=False, what=""):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    if ref.size == 0:
+    """Element-by-element parity: every |got - ref| <= tol * max|ref| (plus half a
+    bfloat16 ulp of ref for a bfloat16 output).  ``got`` and ``ref`` are numpy arrays or
+    torch tensors; the comparison runs in float64 on got's device (the GPU when got is a
+    CUDA tensor), so whole tensors of 10^8 elements check in well under a second."""
+    import torch
+    dev = got.device if isinstance(got, torch.Tensor) else "cpu"
+    g = _as_f64(got, dev)
+    r = _as_f64(ref, dev)
+    assert tuple(g.shape) == tuple(r.shape), f"{what}: shape {tuple(g.shape)} vs {tuple(r.shape)}"
+    if r.numel() == 0:
         return
-    assert np.all(np.isfinite(ref)), f"{what}: reference has non-finite values"
-    assert np.all(np.isfinite(got)), f"{what}: {int((~np.isfinite(got)).sum())} non-finite outputs"
-    scale = np.max(np.abs(ref))
-    allowed = tol * scale + (bf16_half_ulp(ref) if out_bf16 else 0.0)
-    err = np.abs(got - ref)
-    bad = err > allowed
-    if np.any(bad):
-        i = np.unravel_index(np.argmax(err - allowed), err.shape)
+    assert bool(torch.isfinite(r).all()), f"{what}: reference has non-finite values"
+    nonfinite = int((~torch.isfinite(g)).sum())
+    assert nonfinite == 0, f"{what}: {nonfinite} non-finite outputs"
+    scale = float(r.abs().max())
+    err = (g - r).abs_()
+    if out_bf16:
+        # half a bfloat16 ulp of |ref|: 2^(floor(log2|ref|) - 8); frexp gives |ref| = m 2^e
+        # with m in [0.5, 1), so floor(log2|ref|) = e - 1
+        _, e = torch.frexp(r.abs().clamp_min(1e-38))
+        allowed = torch.ldexp(torch.ones_like(r), (e - 9).to(r.dtype)).add_(tol * scale)
+        excess = err - allowed
+    else:
+        excess = err - tol * scale
+    worst = float(excess.max())
+    if worst > 0:
+        bad = int((excess > 0).sum())
+        i = np.unravel_index(int(excess.argmax()), tuple(r.shape))
+        gi, ri = float(g[i]), float(r[i])
         raise AssertionError(
-            f"{what}: {int(bad.sum())} of {err.size} outside tolerance; worst at {i}: got "
-            f"{got[i]!r} ref {ref[i]!r} (tol {tol} * max|ref| {scale:.4g}); "
-            f"max rel err {max_rel_err(got, ref):.3g}")
+            f"{what}: {bad} of {r.numel()} outside tolerance; worst at {i}: got {gi!r} ref "
+            f"{ri!r} (tol {tol} * max|ref| {scale:.4g}); max rel err "
+            f"{float(err.max()) / scale if scale else float(err.max()):.3g}")
+
+
+def rel_err(got, ref):
+    """max |got - ref| / max |ref| in float64 on got's device (for reports)."""
+    import torch
+    dev = got.device if isinstance(got, torch.Tensor) else "cpu"
+    g = _as_f64(got, dev)
+    r = _as_f64(ref, dev)
+    scale = float(r.abs().max()) if r.numel() else 0.0
+    e = float((g - r).abs().max()) if r.numel() else 0.0
+    return e / scale if scale else e

@@ -88,13 +88,38 @@ def test_decode_equals_scan_on_gpu():
     check(to_numpy(state.view(batch, dim, N)), to_numpy(hf), TOL_F32, what="decode vs scan h")
 
 
-def test_780m_full_size_every_step_sampled(oracle_mod):
+def test_780m_full_size_every_step(oracle_mod):
     """Decode state update, Mamba2-780m-shaped: batch 64, 48 heads x headdim 64, d_state
-    128, 1024 consecutive steps on the GPU; y and state of two batch rows checked against
-    the oracle after every step."""
+    128, 1024 consecutive steps on the GPU.  Two GPU states advance in lockstep from the
+    same start, one writing y in float32 and one in bfloat16; after every step each y and
+    each whole state is checked against the float64 oracle stepping the same inputs
+    (float32 y at the bare 2e-3 max|ref| bound, bfloat16 y with half a bfloat16 ulp)."""
+    import torch
     cfg = synth.WORKLOADS["step_780m"]
-    _steps(oracle_mod, cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"],
-           cfg["ngroups"], cfg["steps"], cfg["dtype"], rows=[0, 37])
+    batch, H, P, N, G = cfg["batch"], cfg["nheads"], cfg["headdim"], cfg["dstate"], cfg["ngroups"]
+    par = synth.step_params(H, N, seed=0)
+    tp = to_device(par)
+    fp = par.f64
+    st0 = synth.step_state(batch, H, P, N, seed=0)
+    states = {od: torch.from_numpy(st0).cuda() for od in (torch.float32, torch.bfloat16)}
+    ref_state = st0.astype(np.float64)
+    for k in range(cfg["steps"]):
+        tok = synth.step_tokens(batch, H, P, N, G, step=k, dtype=cfg["dtype"],
+                                delta_scale=cfg["delta_scale"], with_z=cfg["with_z"], seed=0)
+        tt = to_device(tok)
+        ys = {od: ssm.ssm_state_update(st, tt["x"], tt["dt"], tp["A"], tt["B"], tt["C"],
+                                       D=tp["D"], z=tt["z"], dt_bias=tp["dt_bias"], out_dtype=od)
+              for od, st in states.items()}
+        f = tok.f64
+        yr, _ = oracle_mod.state_update(ref_state, f("x"), f("dt"), fp("A"), f("B"), f("C"),
+                                        D=fp("D"), z=f("z"), dt_bias=fp("dt_bias"), inplace=True)
+        torch.cuda.synchronize()
+        ref_dev = torch.from_numpy(ref_state).cuda()
+        for od in states:
+            bf = od == torch.bfloat16
+            tag = "bf16" if bf else "f32"
+            check(ys[od], yr, TOL_BF16, out_bf16=bf, what=f"y step {k} ({tag} out)")
+            check(states[od], ref_dev, TOL_BF16, what=f"state step {k} ({tag} out)")
 
 
 def _tokens(oracle, batch, H, P, N, G, T, dtype, a_per_state=False, disc="exp_euler", seed=3,

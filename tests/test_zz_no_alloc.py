@@ -4,17 +4,17 @@ memory, or a serving loop that may not allocate once running).  It keeps its scr
 in the library's own fixed device array instead of a caller workspace.
 
 Checked here through the C ABI: two calls in a row match the regular entry point
-(which gets a caller workspace) within the parity tolerance, and a problem too big
-for the fixed array is refused with a clear message.  The file name makes pytest
+(which gets a caller workspace) and the float64 oracle within the parity tolerance, on
+the tensor-core and the CUDA-core paths, and a problem too big for the fixed array is
+refused with a clear message.  The file name makes pytest
 collect it last."""
 import ctypes
 
-import numpy as np
 import pytest
 
 import selective_scan_mamba_gb300 as ssm
 from selective_scan_mamba_gb300 import _lib, synth
-from tests.helpers import TOL_BF16, check, to_device, to_numpy
+from tests.helpers import TOL_BF16, TOL_F32, check, to_device
 
 
 def _noalloc_fn():
@@ -50,29 +50,45 @@ def test_oversized_problem_is_refused_on_the_host():
     assert "fixed" in msg and "scratch" in msg
 
 
+# (P, N, in dtype): the tensor-core path (headdim 64, dstate 128, bf16) and the CUDA-core
+# path (headdim 32; float32 inputs), which keeps its chunk decays at an offset inside the
+# same scratch
+NOALLOC_CASES = [(64, 128, synth.BF16, 64), (64, 128, synth.BF16, 256), (32, 64, synth.BF16, 64),
+                 (64, 64, synth.F32, 128)]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("chunk", [64, 256])
-def test_noalloc_matches_workspace_entry_point_twice(chunk):
+@pytest.mark.parametrize("P,N,dtype,chunk", NOALLOC_CASES)
+def test_noalloc_matches_workspace_entry_point_and_oracle_twice(oracle_mod, P, N, dtype, chunk):
+    """Two calls in a row through the C ABI: each matches the regular entry point (given a
+    caller workspace) and the float64 sequential oracle, within the parity tolerance.
+    Ragged length, two groups, gate, skip and initial state."""
     import torch
     if not torch.cuda.is_available():
         pytest.fail("CUDA device required for -m gpu tests")
     lib, fn, cap = _noalloc_fn()
-    inp = synth.ssd(2, 1000, 8, 64, 128, 2, dtype=synth.BF16, with_z=True, with_h0=True, seed=21)
+    inp = synth.ssd(2, 1000, 8, P, N, 2, dtype=dtype, with_z=True, with_h0=True, seed=21)
     t = to_device(inp)
     assert ssm.ssd_chunk_scan_workspace_size(t["x"], t["B"], chunk) <= cap
     y_ref, h_ref = ssm.ssd_chunk_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk,
                                           D=t["D"], z=t["z"], dt_bias=t["dt_bias"], h0=t["h0"],
                                           return_final_state=True)
     torch.cuda.synchronize()
-    y_ref, h_ref = to_numpy(y_ref), to_numpy(h_ref)
+    f = inp.f64
+    y_or, h_or = oracle_mod.ssd_sequential(f("x"), f("dt"), f("A"), f("B"), f("C"), D=f("D"),
+                                           z=f("z"), dt_bias=f("dt_bias"), h0=f("h0"))
+    tol = TOL_BF16 if dtype == synth.BF16 else TOL_F32
+    out_bf16 = dtype == synth.BF16
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         y = torch.full_like(t["x"], float("nan"))
-        hf = torch.full((2, 8, 64, 128), float("nan"), dtype=torch.float32, device="cuda")
+        hf = torch.full((2, 8, P, N), float("nan"), dtype=torch.float32, device="cuda")
         p = ssm._ssd_params(t["x"], t["dt"], t["A"], t["B"], t["C"], chunk, t["D"], t["z"],
                             t["dt_bias"], True, t["h0"], y, hf, "exp_euler")
         rc = fn(ctypes.byref(p), stream)
         assert rc == _lib.SSM_OK, lib.ssm_last_error().decode()
         torch.cuda.synchronize()
-        check(to_numpy(y), y_ref, TOL_BF16, out_bf16=True, what=f"y, call {call}")
-        check(to_numpy(hf), h_ref, TOL_BF16, what=f"h_final, call {call}")
+        check(y, y_ref, tol, out_bf16=out_bf16, what=f"y vs workspace entry point, call {call}")
+        check(hf, h_ref, tol, what=f"h_final vs workspace entry point, call {call}")
+        check(y, y_or, tol, out_bf16=out_bf16, what=f"y vs oracle, call {call}")
+        check(hf, h_or, tol, what=f"h_final vs oracle, call {call}")
