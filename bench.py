@@ -85,13 +85,14 @@ def ssd_flops(batch, L, H, P, N, G, Q):
     return batch * nch * (H * per_bhc + G * per_bgc)
 
 
-# The Mamba-1 update h = exp(Delta A) h + (Delta x) B, y += C h needs at least one
+# The roofline of the scan is HBM bandwidth: algorithmic bytes (each input read once, each
+# output written once) over the measured copy rate.  Its arithmetic ceiling is reported
+# beside it: the update h = exp(Delta A) h + (Delta x) B, y += C h needs at least one
 # exponential (MUFU.EX2) and four FP32 FMA-pipe operations (Delta A, (Delta x) B, the state
 # FMA, the C h FMA).  A GB300 SM retires 32 EX2 and 128 FP32 FMA lanes per clock (measured
-# by selective_scan_mamba_gb300/tools/alu_probe.cu; the f32x2 forms save issue slots, not
-# FP32 lanes), so both units cap the scan at 32 updates per SM clock.  At 1.99 updates per
-# algorithmic byte (130m layer) that is ~75% of the HBM copy bandwidth: the scan is bound
-# by arithmetic, not by HBM.
+# with a microbenchmark of independent ex2 / FFMA chains; the f32x2 forms save issue slots,
+# not FP32 lanes), so both units cap the scan at 32 updates per SM clock.  At 1.99 updates
+# per algorithmic byte (130m layer) that is ~75% of the HBM copy rate.
 EX2_PER_CLK_SM = 32
 FP32_LANES_PER_CLK_SM = 128
 FP32_OPS_PER_UPDATE = 4
@@ -330,16 +331,18 @@ def bench_ours(args, rank, world):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        # one event between consecutive steps: the region from the first to the last is
+        # exactly the K steps, and the gaps give the per-step times
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        evs[0].record(stream)
         for i in range(args.steps):
             step(i)
-        e1.record(stream)
+            evs[i + 1].record(stream)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-        t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+        t_step = evs[0].elapsed_time(evs[-1]) / 1e3 / args.steps
+        per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
     clocks = clk.summary()
     t_step = max_over_ranks(dist, t_step, "cuda")
     updates = Bt * L * D * N
@@ -348,6 +351,7 @@ def bench_ours(args, rank, world):
     sm_max = clocks.get("sm_max_mhz") or 2070.0
     alu_peak = alu_peak_updates(sms, sm_max)
     gbs = set_bytes / t_step / 1e9
+    launches_per_step = 2 if ssm.ssm_scan_workspace_size(sets[0]["x"], sets[0]["B"]) else 1
 
     # end to end through the public API with host buffers: every step copies its inputs
     # in from pinned host memory and its y back, inside the timed region.  Each input has
@@ -430,32 +434,117 @@ def bench_ours(args, rank, world):
                    "l2": f"{nsets} rotating input sets, {nsets * set_bytes / 1e6:.0f} MB > "
                          f"L2 {l2 / 1e6:.0f} MB",
                    "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "ms_median": statistics.median(per_step),
+        "ms_p95": percentile(per_step, 95),
         "hbm_gbs": gbs,
         "hbm_frac": gbs / peaks["hbm_gbs"],
-        "roofline": {"bound": "alu", "achieved": updates / t_step / 1e9, "peak": alu_peak / 1e9,
-                     "unit": "Gupd/s", "frac": updates / t_step / alu_peak,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"],
                      "traffic": recorded_traffic("m1_scan_tmem"),
-                     "kernel": "m1_scan_tmem", "updates_per_launch": updates,
-                     "bytes_per_launch": set_bytes,
-                     "peak_source": f"derived: {sms} SMs x {sm_max:.0f} MHz x 32 updates/clk/SM "
-                                    "(1 MUFU.EX2 + 4 FP32 FMA-pipe ops per update; 32 EX2 and "
-                                    "128 FP32 lanes per clk per SM)",
-                     "hbm": {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"],
-                             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}},
+                     "kernel": "m1_scan_tmem", "bytes_per_launch": set_bytes,
+                     "updates_per_launch": updates,
+                     "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "alu": {"achieved": updates / t_step / 1e9, "peak": alu_peak / 1e9,
+                             "unit": "Gupd/s", "frac": updates / t_step / alu_peak,
+                             "peak_source": f"derived: {sms} SMs x {sm_max:.0f} MHz x 32 updates/clk/SM "
+                                            "(1 MUFU.EX2 + 4 FP32 FMA-pipe ops per update; 32 EX2 "
+                                            "and 128 FP32 lanes per clk per SM, measured)"},
+                     "paths": {}},
         "e2e": {"value": whole_job_rate(updates, world, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
                 "link_gbs": (h2d + d2h) / t_e2e / 1e9,
                 "link_peak": link, "link_frac": link["floor_ms"] / (t_e2e * 1e3), "buffer_sets": nbuf},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
+        "meta": run_metadata(torch, dev, seed=rank),
         "paths": paths,
     }
+    result["roofline"]["paths"] = path_rooflines(paths)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_seconds)
     if dist:
         dist.destroy_process_group()
     return result
+
+
+def percentile(xs, q):
+    """The q-th percentile of xs by linear interpolation between order statistics."""
+    v = sorted(xs)
+    if not v:
+        return None
+    pos = (len(v) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (pos - lo)
+
+
+def _run(cmd):
+    try:
+        return subprocess.run(cmd, capture_output=True, text=True, timeout=20,
+                              cwd=ROOT).stdout.strip() or None
+    except Exception:
+        return None
+
+
+def sources_digest():
+    """sha256 (16 hex digits) of the library, oracle and bench sources: identifies the code
+    a result was measured on where no git history is available (the GPU machine gets a copy of
+    the tree without .git)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "selective_scan_mamba_gb300", "csrc", "*")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")) +
+                   glob.glob(os.path.join(ROOT, "oracle", "*.[ch]")) +
+                   glob.glob(os.path.join(ROOT, "selective_scan_mamba_gb300", "*.py")) +
+                   [os.path.abspath(__file__)])
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.relpath(f, ROOT).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def run_metadata(torch, dev, seed):
+    """The environment block that goes with every result: GPU, driver, CUDA, torch, seed,
+    command, time, host and the code it ran."""
+    import datetime
+    import platform
+    props = torch.cuda.get_device_properties(dev)
+    drv = _run(["nvidia-smi", "-i", str(dev), "--query-gpu=driver_version", "--format=csv,noheader"])
+    cpu = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    cpu = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"gpu": props.name, "sms": props.multi_processor_count, "driver": drv,
+            "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
+            "seed": seed, "command": " ".join([os.path.basename(sys.executable)] + sys.argv),
+            "utc": datetime.datetime.now(datetime.timezone.utc).strftime("%Y-%m-%dT%H:%M:%SZ"),
+            "host": {"machine": platform.machine(), "cpu": cpu, "cores": os.cpu_count()},
+            "git": _run(["git", "rev-parse", "--short=12", "HEAD"]),
+            "sources_sha256": sources_digest()}
+
+
+def path_rooflines(paths):
+    """One roofline fraction per measured path (the SSD against max(HBM, bf16 tensor) time,
+    the others against HBM), compact, so that the line's head carries them."""
+    out = {}
+    for q in ("64", "256"):
+        r = paths.get(f"ssd_130m_chunk{q}")
+        if r:
+            out[f"ssd_130m_chunk{q}"] = {"bound": r["roofline_bound"], "frac": r["roofline_frac"],
+                                         "ms": r["ms"]}
+    r = paths.get("decode_780m")
+    if r:
+        out["decode_780m"] = {"bound": "hbm", "frac": r["hbm_frac"], "us": r["us_per_step"]}
+    for L, r in paths.get("m1_790m_long", {}).items():
+        out[f"m1_790m_L{L}"] = {"bound": "hbm", "frac": r["hbm_frac"], "ms": r["ms"],
+                                "alu_frac": r.get("alu_frac")}
+    return out
 
 
 def recorded_traffic(kernel):
@@ -497,6 +586,7 @@ def _source_digest(kernel="m1_scan_tmem"):
 def other_paths(args, torch, ssm, peaks, stream, l2):
     out = {}
     hbm = peaks["hbm_gbs"]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     # Mamba-2 chunked SSD, 130m-shaped
     c4 = synth.WORKLOADS["ssd_130m"]
     s_inp = synth.ssd(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"],
@@ -529,12 +619,14 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                        c4["ngroups"], Q)
         fl_exec = ssd_flops(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"],
                             c4["dstate"], c4["ngroups"], 64)
-        t_roof = max(nb / (hbm * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+        t_hbm, t_tc = nb / (hbm * 1e9), fl / (peaks["bf16_tflops"] * 1e12)
+        t_roof = max(t_hbm, t_tc)
         upd = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
         out[f"ssd_130m_chunk{Q}"] = {
             "ms": tsec * 1e3, "state_updates_per_s": upd / tsec, "hbm_gbs": nb / tsec / 1e9,
             "tflops_executed": fl_exec / tsec / 1e12, "roofline_s": t_roof,
-            "roofline_frac": t_roof / tsec, "bytes": nb, "flops_dense_chunk": fl,
+            "roofline_frac": t_roof / tsec, "roofline_bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "bytes": nb, "flops_dense_chunk": fl,
             "flops_executed": fl_exec}
     del sets
     # decode step, 780m-shaped: 4 layers' states rotate (each 100.7 MB; together > L2)
@@ -756,9 +848,10 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
             ssm.ssm_scan_fwd(tt["x"], tt["delta"], tt["A"], tt["B"], tt["C"], D=tt["D"],
                              delta_bias=tt["delta_bias"], y=yb, h_final=hf, workspace=ws)
         tsec = time_launches(torch, m, max(5, nsets), 2, stream)
-        sweep[str(L)] = {"ms": tsec * 1e3,
-                         "state_updates_per_s": c3["dim"] * c3["dstate"] * L / tsec,
+        upd3 = c3["dim"] * c3["dstate"] * L
+        sweep[str(L)] = {"ms": tsec * 1e3, "state_updates_per_s": upd3 / tsec,
                          "hbm_gbs": nbytes / tsec / 1e9, "hbm_frac": nbytes / tsec / 1e9 / hbm,
+                         "alu_frac": upd3 / tsec / alu_peak_updates(sms, 2070.0),
                          "input_sets": nsets, "workspace_bytes": wsb}
         del t0, sets, yb, hf, ws
     out["m1_790m_long"] = sweep
@@ -793,10 +886,27 @@ def cpu_baseline(inp, budget_s=10.0):
         total += run(nb)
         reps += 1
     upd = reps * nb * D * L * N
+    # the same oracle on one thread, on a sample of channels of one batch row (about a
+    # third of the budget)
+    oracle.set_num_threads(1)
+    try:
+        def run1(nch):
+            t0 = time.perf_counter()
+            oracle.mamba1_scan(x[:1, :nch], dl[:1, :nch], A[:nch], B[:1], C[:1], D=Dv[:nch],
+                               z=None if z is None else z[:1, :nch], delta_bias=bias[:nch])
+            return time.perf_counter() - t0
+        t8 = run1(8)
+        nch = max(8, min(D, int(budget_s / 3 / max(t8, 1e-4) * 8)))
+        t1 = run1(nch)
+    finally:
+        oracle.set_num_threads(0)
     return {"value": upd / total, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{reps} x {nb} batch rows ({nb * D} channels x {L} steps x {N} states), "
-                      f"float64 sequential oracle, {total:.1f} s"}
+                      f"float64 sequential oracle, {total:.1f} s",
+            "single_thread": {"value": nch * L * N / t1, "unit": UNIT, "cores": 1,
+                              "sample": f"{nch} channels of one batch row x {L} steps x {N} "
+                                        f"states, {t1:.1f} s"}}
 
 
 def bench_reference(args, rank, world):

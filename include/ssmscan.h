@@ -30,16 +30,22 @@
  *   - Pointers: every tensor pointer is a DEVICE pointer of the current CUDA
  *     device; tensors are dense, row-major (last index fastest), and 16-byte
  *     aligned.  Optional tensors (marked "nullable") may be NULL.
- *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
- *     default stream).  Every call is asynchronous on that stream; results are
- *     ready when the stream reaches that point.
+ *   - Streams: `stream` is a cudaStream_t of the current device passed as void*
+ *     (NULL = the legacy default stream).  Every call is asynchronous on that
+ *     stream; results are ready when the stream reaches that point.
  *   - Errors: arguments are validated before anything is launched.  Bad
  *     arguments return SSM_ERR_INVALID_ARG, shapes outside what the kernels
  *     support return SSM_ERR_UNSUPPORTED, and a failed launch returns
  *     SSM_ERR_CUDA; in each case ssm_last_error() describes the problem and
  *     nothing has been written.  There is no CPU fallback.
- *   - Aliasing: outputs must not overlap inputs, except the decode state, which
- *     is updated in place by design.
+ *   - Device-side waits: kernels that wait for their own asynchronous copies and
+ *     tensor-core operations bound every wait.  A wait that runs out makes its
+ *     block stop issuing work and finish; the call's outputs are then not valid.
+ *     Calls are asynchronous, so this is reported afterwards: ssm_device_status()
+ *     returns SSM_ERR_TIMEOUT until the event has been read.
+ *   - Aliasing: outputs (and the workspace) must not overlap inputs or each
+ *     other, except the decode state, which is updated in place by design.
+ *     Overlaps are checked from the shapes and refused with SSM_ERR_INVALID_ARG.
  *   - Precision: inputs are bfloat16 or float32; A, D, biases and all states are
  *     float32; every accumulation is float32.
  */
@@ -52,14 +58,14 @@
 extern "C" {
 #endif
 
-#define SSM_ABI_VERSION 1
+#define SSM_ABI_VERSION 2
 
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = 1,  /* null required pointer, bad size, misaligned pointer */
     SSM_ERR_UNSUPPORTED = 2,  /* valid, but outside the shapes the kernels implement */
     SSM_ERR_CUDA = 3,         /* a CUDA call or launch failed */
-    SSM_ERR_TIMEOUT = 4       /* reserved: a bounded device-side wait gave up */
+    SSM_ERR_TIMEOUT = 4       /* a bounded device-side wait gave up (ssm_device_status) */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -101,16 +107,50 @@ typedef struct {
     ssm_disc disc;
 } ssm_scan_params;
 
-/* Device scratch the scan needs for this problem, in bytes (0 for most shapes:
- * long sequences with few channels are split in time and carry their segment
- * states through this buffer). */
-size_t ssm_scan_workspace_size(const ssm_scan_params* p);
+/* Runs the scan.  Needs no scratch memory: every problem runs in one pass over
+ * the sequence (see ssm_scan_fwd_ex for the time-split plan of long sequences
+ * with few channels, which carries segment states through a workspace). */
+ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* stream);
 
-/* Runs the scan.  `workspace` is a device buffer of at least
- * ssm_scan_workspace_size(p) bytes (may be NULL when that is 0); its contents
- * on entry do not matter. */
-ssm_status ssm_scan_fwd(const ssm_scan_params* p, void* workspace, size_t workspace_bytes,
-                        void* stream);
+/* Kernel choice for ssm_scan_fwd_ex.  AUTO takes the fastest kernel that supports
+ * the problem; naming one that does not returns SSM_ERR_UNSUPPORTED. */
+typedef enum {
+    SSM_SCAN_KERNEL_AUTO = 0,
+    SSM_SCAN_KERNEL_TMEM = 1,     /* bf16 in, dstate 16, exp-Euler, L*2 and L*out a
+                                     multiple of 16 bytes: TMA tiles, B/C broadcast
+                                     through tensor memory, optional time split */
+    SSM_SCAN_KERNEL_TMA = 2,      /* same inputs: TMA tiles, B/C read from shared memory */
+    SSM_SCAN_KERNEL_TILED = 3,    /* dstate 16, exp-Euler, bf16 or fp32 in, 16-byte rows:
+                                     cp.async-staged tiles */
+    SSM_SCAN_KERNEL_GENERIC = 4   /* any supported shape, either discretisation */
+} ssm_scan_kernel;
+
+/* Options of ssm_scan_fwd_ex; a zero-filled struct (or NULL) means automatic. */
+typedef struct {
+    ssm_scan_kernel kernel;
+    int threads_per_channel;  /* 0 = the kernel's own; TMEM: 4; TMA: 2 or 4;
+                                 TILED: 1 (bf16 in only), 2 or 4 */
+    int max_segments;         /* time segments of the TMEM kernel's split for long
+                                 sequences with few channels: 0 = automatic,
+                                 1 = never split, n = at most n */
+    unsigned int wait_limit;  /* polls before a device-side wait gives up; 0 = the
+                                 default (2^24, seconds) */
+    int fault_test;           /* testing only, 0 = off.  1: the TMEM kernel never copies
+                                 the inputs of its second 64-step tile, so every wait
+                                 for them runs out after wait_limit polls and the call
+                                 is reported by ssm_device_status() as SSM_ERR_TIMEOUT.
+                                 Needs a problem of at least two tiles. */
+} ssm_scan_opts;
+
+/* Device scratch ssm_scan_fwd_ex needs for this problem and these options (NULL =
+ * automatic), in bytes; 0 for most shapes and whenever max_segments is 1. */
+size_t ssm_scan_workspace_size(const ssm_scan_params* p, const ssm_scan_opts* opts);
+
+/* ssm_scan_fwd with explicit options.  `workspace` is a device buffer of at least
+ * ssm_scan_workspace_size(p, opts) bytes, 16-byte aligned (may be NULL when that
+ * is 0); its contents on entry do not matter. */
+ssm_status ssm_scan_fwd_ex(const ssm_scan_params* p, const ssm_scan_opts* opts,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Mamba-1 selective scan, backward: the reverse-mode derivative of ssm_scan_fwd
@@ -324,7 +364,11 @@ ssm_status ssd_chunk_scan_fwd(const ssd_params* p, void* workspace, size_t works
  *     are rejected with SSM_ERR_INVALID_ARG and a message saying so.
  *   - The first call on each device looks up the array's device address with
  *     cudaGetSymbolAddress (that device must be current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is valid in the
+ *     CUDA context it was looked up in; a call under another context (after
+ *     cudaDeviceReset, say) looks it up again.
+ *   - `stream` must belong to the current device (the scratch size depends on
+ *     that device); a stream of another device is refused.
  *   - All calls share the array: calls whose GPU work may overlap (other
  *     streams, other host threads) race on it; the caller must order them.
  *     The array keeps the last call's contents, and no part of it needs to
@@ -434,9 +478,17 @@ ssm_status ssd_scan_bwd(const ssd_bwd_params* p, void* workspace, size_t workspa
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* ssm_last_error(void);
 
-/* Diagnostics: how many bounded device-side waits (a kernel waiting for its own
- * asynchronous copies) gave up since the previous call, on the current device;
- * 0 in correct operation.  Reading it synchronises with the device and clears it. */
+/* Status of the work launched on the current device: waits for the device
+ * (cudaDeviceSynchronize, so not inside a stream capture), then returns
+ * SSM_ERR_TIMEOUT if a bounded device-side wait gave up since the previous call
+ * (ssm_last_error() names the kernels; the outputs of the calls in between are
+ * not valid), SSM_ERR_CUDA if the device reports an error, else SSM_OK.  Reading
+ * clears the record. */
+ssm_status ssm_device_status(void);
+
+/* The same record as a count: how many bounded device-side waits gave up since
+ * the previous read (0 in correct operation, and 0 after a CUDA error).  Waits
+ * for the device and clears the record. */
 unsigned int ssm_wait_timeouts(void);
 
 /* SSM_ABI_VERSION of the loaded library. */

@@ -78,6 +78,8 @@ def _bind(path):
                                         i, dp]
     lib.oracle_num_threads.restype = i
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads.argtypes = [i]
     return lib
 
 
@@ -133,6 +135,13 @@ def phi1(zv: float) -> float:
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the OpenMP loops over independent rows use (n < 1: all cores).  Timing
+    only: every row is still computed sequentially by one thread, so results do not
+    change."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def mamba1_scan(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,

@@ -571,3 +571,16 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Sets the number of OpenMP threads the parallel regions here use (timing harness only:
+ * the results do not depend on it, every row is computed by one thread in order).
+ * n < 1 restores the default.  Without OpenMP this does nothing. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    extern int omp_get_num_procs(void);
+    omp_set_num_threads(n >= 1 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}

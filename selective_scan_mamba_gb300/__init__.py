@@ -29,8 +29,8 @@ __all__ = [
     "ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
     "ssd_chunk_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_scan_bwd",
     "ssd_scan_bwd_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
-    "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd", "ssm_s4d_kernel", "wait_timeouts", "SsmError",
-    "lib",
+    "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd", "ssm_s4d_kernel", "wait_timeouts",
+    "device_status", "SsmError", "lib",
 ]
 
 
@@ -38,6 +38,14 @@ def wait_timeouts() -> int:
     """Bounded device-side waits that gave up since the previous call (0 in correct
     operation); synchronises with the device and clears the count."""
     return int(_lib.load().ssm_wait_timeouts())
+
+
+def device_status() -> None:
+    """Waits for the current device and raises SsmError (status SSM_ERR_TIMEOUT) if a
+    bounded device-side wait gave up since the previous check, which means the outputs
+    of the calls in between are not valid, or SSM_ERR_CUDA if the device reports an
+    error.  Clears the record."""
+    _lib.check(_lib.load().ssm_device_status())
 
 
 def lib():
@@ -130,9 +138,28 @@ def _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_f
     return p
 
 
-def ssm_scan_workspace_size(x, B, out_dtype=None, disc="exp_euler") -> int:
-    """Scratch bytes ssm_scan_fwd needs for these shapes and dtypes (y defaults to x's
-    dtype)."""
+_KERNELS = {"auto": _lib.SSM_SCAN_KERNEL_AUTO, "tmem": _lib.SSM_SCAN_KERNEL_TMEM,
+            "tma": _lib.SSM_SCAN_KERNEL_TMA, "tiled": _lib.SSM_SCAN_KERNEL_TILED,
+            "generic": _lib.SSM_SCAN_KERNEL_GENERIC}
+
+
+def scan_opts(kernel="auto", threads_per_channel=0, max_segments=0, wait_limit=0,
+              fault_test=0):
+    """The C options struct of ssm_scan_fwd_ex (see include/ssmscan.h)."""
+    o = _lib.ScanOpts()
+    if kernel not in _KERNELS:
+        raise ValueError(f"unknown kernel {kernel!r} ({', '.join(_KERNELS)})")
+    o.kernel = _KERNELS[kernel]
+    o.threads_per_channel = int(threads_per_channel)
+    o.max_segments = int(max_segments)
+    o.wait_limit = int(wait_limit)
+    o.fault_test = int(fault_test)
+    return o
+
+
+def ssm_scan_workspace_size(x, B, out_dtype=None, disc="exp_euler", **opts) -> int:
+    """Scratch bytes ssm_scan_fwd needs for these shapes, dtypes and options (y defaults
+    to x's dtype); the options are those of :func:`scan_opts`."""
     p = _lib.ScanParams()
     p.batch, p.dim, p.seqlen = x.shape
     p.dstate = B.shape[-2]
@@ -141,18 +168,24 @@ def ssm_scan_workspace_size(x, B, out_dtype=None, disc="exp_euler") -> int:
     p.out_dtype = _dtype_code(x) if out_dtype is None else _dtype_code(
         _torch().empty(0, dtype=out_dtype))
     p.disc = _disc(disc)
-    return int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
+    o = scan_opts(**opts)
+    return int(lib().ssm_scan_workspace_size(ctypes.byref(p), ctypes.byref(o)))
 
 
 def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
                  h0=None, *, y=None, h_final=None, out_dtype=None, return_final_state=False,
-                 disc="exp_euler", workspace=None, stream=None):
+                 disc="exp_euler", workspace=None, stream=None, **opts):
     """Mamba-1 selective scan.
 
     x, delta, z: [batch, dim, L] (bfloat16 or float32); B, C: [batch, G, N, L] or
     [batch, N, L]; A: [dim, N] float32; D, delta_bias: [dim] float32; h0: [batch, dim, N]
     float32.  Returns y [batch, dim, L] (dtype ``out_dtype``, default x's), and the final
     state [batch, dim, N] float32 when ``return_final_state``.
+
+    Runs ssm_scan_fwd_ex with the options of :func:`scan_opts` given as keywords (kernel,
+    threads_per_channel, max_segments, ...; all automatic by default).  When the plan
+    splits a long sequence in time it needs scratch: ``workspace`` (a uint8 CUDA tensor of
+    at least ssm_scan_workspace_size bytes) or, if None, a tensor allocated here.
     """
     torch = _torch()
     if y is None:
@@ -161,13 +194,15 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softp
         h_final = torch.empty((x.shape[0], x.shape[1], A.shape[1]), dtype=torch.float32,
                               device=x.device)
     p = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final, disc)
-    need = int(lib().ssm_scan_workspace_size(ctypes.byref(p)))
+    o = scan_opts(**opts)
+    need = int(lib().ssm_scan_workspace_size(ctypes.byref(p), ctypes.byref(o)))
     ws_ptr, ws_bytes = None, 0
     if need:
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    _lib.check(lib().ssm_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+        ws_ptr, ws_bytes = _ptr(workspace, "workspace"), workspace.numel()
+    _lib.check(lib().ssm_scan_fwd_ex(ctypes.byref(p), ctypes.byref(o), ws_ptr, ws_bytes,
+                                     _stream(stream)))
     return (y, h_final) if return_final_state else y
 
 

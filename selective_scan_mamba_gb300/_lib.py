@@ -23,6 +23,14 @@ SSM_BF16 = 1
 SSM_DISC_EXP_EULER = 0
 SSM_DISC_ZOH = 1
 
+SSM_SCAN_KERNEL_AUTO = 0
+SSM_SCAN_KERNEL_TMEM = 1
+SSM_SCAN_KERNEL_TMA = 2
+SSM_SCAN_KERNEL_TILED = 3
+SSM_SCAN_KERNEL_GENERIC = 4
+
+ABI_VERSION = 2
+
 _vp = ctypes.c_void_p
 _fp = ctypes.c_void_p  # float* passed as an address
 _i = ctypes.c_int
@@ -34,6 +42,11 @@ class ScanParams(ctypes.Structure):
                 ("x", _vp), ("delta", _vp), ("delta_bias", _fp), ("delta_softplus", _i),
                 ("A", _fp), ("B", _vp), ("C", _vp), ("D_skip", _fp), ("z", _vp), ("h0", _fp),
                 ("y", _vp), ("h_final", _fp), ("disc", _i)]
+
+
+class ScanOpts(ctypes.Structure):
+    _fields_ = [("kernel", _i), ("threads_per_channel", _i), ("max_segments", _i),
+                ("wait_limit", ctypes.c_uint), ("fault_test", _i)]
 
 
 class ScanBwdParams(ctypes.Structure):
@@ -78,12 +91,12 @@ class StepParams(ctypes.Structure):
                 ("disc", _i)]
 
 
-SYMBOLS = ("ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd",
+SYMBOLS = ("ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_workspace_size", "ssm_scan_bwd",
            "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_mamba3_scan_workspace_size", "ssm_s4d_scan_fwd",
            "ssm_s4d_scan_workspace_size",
            "ssm_s4d_kernel", "ssd_scan_bwd", "ssd_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
-           "ssm_last_error", "ssm_abi_version")
+           "ssm_last_error", "ssm_abi_version", "ssm_device_status", "ssm_wait_timeouts")
 
 _lock = threading.Lock()
 _lib = None
@@ -105,9 +118,13 @@ def load(build_if_missing: bool = True):
             lib = ctypes.CDLL(_build.LIB)
             sz = ctypes.c_size_t
             lib.ssm_scan_fwd.restype = _i
-            lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp, sz, _vp]
+            lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp]
+            lib.ssm_scan_fwd_ex.restype = _i
+            lib.ssm_scan_fwd_ex.argtypes = [ctypes.POINTER(ScanParams), ctypes.POINTER(ScanOpts),
+                                            _vp, sz, _vp]
             lib.ssm_scan_workspace_size.restype = sz
-            lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+            lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams),
+                                                    ctypes.POINTER(ScanOpts)]
             lib.ssm_scan_bwd.restype = _i
             lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), _vp, sz, _vp]
             lib.ssm_scan_bwd_workspace_size.restype = sz
@@ -140,6 +157,11 @@ def load(build_if_missing: bool = True):
             lib.ssm_abi_version.argtypes = []
             lib.ssm_wait_timeouts.restype = ctypes.c_uint
             lib.ssm_wait_timeouts.argtypes = []
+            lib.ssm_device_status.restype = _i
+            lib.ssm_device_status.argtypes = []
+            if lib.ssm_abi_version() != ABI_VERSION:
+                raise RuntimeError(f"libssmscan ABI version {lib.ssm_abi_version()}, this "
+                                   f"binding expects {ABI_VERSION}: rebuild the library")
             _lib = lib
         return _lib
 

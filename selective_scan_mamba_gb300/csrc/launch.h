@@ -28,6 +28,12 @@ struct M1Args {
     float* h_final;
     ssm_disc disc;
     int cpb_max;  // channels per CTA (tiled path)
+    // choices of ssm_scan_opts (0 = automatic)
+    int kernel;               // ssm_scan_kernel
+    int tpc;                  // threads per channel
+    int max_segments;         // time segments
+    unsigned int wait_limit;  // polls before a device-side wait gives up (0 = default)
+    int fault_test;           // testing: skip one tile's input copy (see ssmscan.h)
 };
 
 // backward of the Mamba-1 scan (scan_m1_bwd.cu)
@@ -72,12 +78,12 @@ cudaError_t m1_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
 size_t m1_tma_smem_bytes(int cpb);
 cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan);
 cudaError_t m1_tma_launch(const M1Args& a, const M1Plan& plan, cudaStream_t s);
-unsigned int m1_tma_wait_timeouts();
+cudaError_t m1_tma_take_wait_timeouts(unsigned int* count);  // reads and clears
 
 // bf16 fast path with B/C broadcast through tensor memory (scan_m1_tmem.cu)
 cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan);
 cudaError_t m1_tmem_launch(const M1Args& a, const M1Plan& plan, void* workspace, cudaStream_t s);
-unsigned int m1_tmem_wait_timeouts();
+cudaError_t m1_tmem_take_wait_timeouts(unsigned int* count);  // reads and clears
 
 // TMA tensor map of a row-major [rows][inner] tensor (tmap.cu)
 cudaError_t encode_tmap_2d(struct CUtensorMap_st* map, const void* base, int elem_bytes,
@@ -133,7 +139,7 @@ cudaError_t ssd_launch(const SsdArgs& a, cudaStream_t s);
 bool ssd_tc_supported(const SsdArgs& a);
 size_t ssd_tc_workspace_bytes(const SsdArgs& a);
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s);
-unsigned int ssd_tc_wait_timeouts();
+cudaError_t ssd_tc_take_wait_timeouts(unsigned int* count);  // reads and clears
 
 // Records `msg` as this thread's ssm_last_error() text and returns `st`.
 ssm_status set_error(ssm_status st, const char* msg);

@@ -391,10 +391,6 @@ static cudaError_t dispatch_tiled(const M1Args& a, int tpc, F&& f) {
     return cudaErrorInvalidValue;
 }
 
-static int env_int(const char* name, int dflt) {
-    const char* v = getenv(name);
-    return (v && *v) ? atoi(v) : dflt;
-}
 
 // Chooses the kernel and its launch.  The tiled path needs dstate = 16, the default
 // discretisation, 16-byte aligned rows and at most kM1MaxPairs B/C rows per CTA; it runs
@@ -412,7 +408,7 @@ cudaError_t m1_plan(const M1Args& a, M1Plan* plan) {
     const bool aligned = (static_cast<size_t>(a.seqlen) * es) % 16 == 0 &&
                          (static_cast<size_t>(a.seqlen) * es_out) % 16 == 0;
     if (a.dstate != 16 || a.disc != SSM_DISC_EXP_EULER || !aligned || a.seqlen == 0 ||
-        env_int("SSM_M1_FORCE_GENERIC", 0))
+        (a.kernel != SSM_SCAN_KERNEL_AUTO && a.kernel != SSM_SCAN_KERNEL_TILED))
         return cudaSuccess;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -421,9 +417,9 @@ cudaError_t m1_plan(const M1Args& a, M1Plan* plan) {
     if (e != cudaSuccess) return e;
     const int nch = a.batch * a.dim;
     const int T = m1_tile_steps(a.in_dtype);
-    int tpc = env_int("SSM_M1_TPC", a.in_dtype == SSM_BF16 ? 2 : 4);
+    int tpc = a.tpc ? a.tpc : (a.in_dtype == SSM_BF16 ? 2 : 4);
     if (a.in_dtype != SSM_BF16 && tpc == 1) tpc = 2;
-    int per_sm = env_int("SSM_M1_CTAS_PER_SM", 2);
+    int per_sm = 2;
     const int per_group = a.dim / a.ngroups;
     for (; per_sm >= 1; --per_sm) {
         int grid = per_sm * sms;

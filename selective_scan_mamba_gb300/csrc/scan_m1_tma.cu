@@ -137,10 +137,15 @@ __global__ void __launch_bounds__(kM1MaxThreads) m1_scan_tma(const __grid_consta
         prefetch_tmap(&maps.c);
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         mbar_fence_init();
+        wait_setup(a.wait_limit);
     }
     __syncthreads();
+    int last_issued = -1;  // thread 0: the last tile whose copy went out
     if (tid == 0)
-        for (int k = 0; k < kStages && k < ntiles; ++k) issue(k);
+        for (int k = 0; k < kStages && k < ntiles; ++k) {
+            issue(k);
+            last_issued = k;
+        }
 
     // per-thread constants
     // Thread gi owns states n = gi + TPC * i (i < NS): strided, so that the B/C chunk rows
@@ -279,8 +284,13 @@ __global__ void __launch_bounds__(kM1MaxThreads) m1_scan_tma(const __grid_consta
             store_row<TO>(yrow, yv, L - (t0 + tb));
         }
         __syncthreads();  // stage s and the (dt, dt*x) buffer are free again
-        if (tid == 0 && k + kStages < ntiles) issue(k + kStages);
+        if (tid == 0 && k + kStages < ntiles && !wait_aborted()) {
+            issue(k + kStages);
+            last_issued = k + kStages;
+        }
     }
+    // a CTA whose waits gave up lets its copies in flight land before it exits
+    if (tid == 0 && wait_aborted()) drain_ring(full, kStages, last_issued);
 
     if (active && a.h_final) {
 #pragma unroll
@@ -309,10 +319,6 @@ cudaError_t dispatch(ssm_dtype out, int tpc, F&& f) {
     return cudaErrorInvalidValue;
 }
 
-int env_int(const char* name, int dflt) {
-    const char* v = getenv(name);
-    return (v && *v) ? atoi(v) : dflt;
-}
 
 }  // namespace
 
@@ -325,7 +331,8 @@ cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan) {
     const size_t es_out = a.out_dtype == SSM_BF16 ? 2 : 4;
     if (a.in_dtype != SSM_BF16 || a.dstate != kN || a.disc != SSM_DISC_EXP_EULER || a.seqlen <= 0 ||
         (static_cast<size_t>(a.seqlen) * 2) % 16 != 0 ||
-        (static_cast<size_t>(a.seqlen) * es_out) % 16 != 0 || env_int("SSM_M1_NO_TMA", 0))
+        (static_cast<size_t>(a.seqlen) * es_out) % 16 != 0 ||
+        (a.kernel != SSM_SCAN_KERNEL_AUTO && a.kernel != SSM_SCAN_KERNEL_TMA))
         return cudaSuccess;
     int dev = 0, sms = 0, max_smem = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -336,10 +343,10 @@ cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan) {
         cudaSuccess)
         return e;
     const int nch = a.batch * a.dim;
-    const int tpc = env_int("SSM_M1_TPC", 4);
+    const int tpc = a.tpc ? a.tpc : 4;
     if (tpc != 2 && tpc != 4) return cudaSuccess;  // built for 2 or 4 threads per channel
     const int per_group = a.dim / a.ngroups;
-    for (int per_sm = env_int("SSM_M1_CTAS_PER_SM", 2); per_sm >= 1; --per_sm) {
+    for (int per_sm = 2; per_sm >= 1; --per_sm) {
         int grid = per_sm * sms;
         if (grid > nch) grid = nch;
         const int cpb = (nch + grid - 1) / grid;
@@ -395,11 +402,8 @@ cudaError_t m1_tma_launch(const M1Args& a_in, const M1Plan& plan, cudaStream_t s
     return cudaGetLastError();
 }
 
-unsigned int m1_tma_wait_timeouts() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-    cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero));
-    return v;
+cudaError_t m1_tma_take_wait_timeouts(unsigned int* count) {
+    return take_wait_timeouts(count);
 }
 
 }  // namespace ssm

@@ -27,7 +27,6 @@
 // reduce-scattered by shuffles; skip, gate and 16-byte stores of y finish the tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -115,6 +114,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
     uint64_t* mmab = full + kStages;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mmab + 2);
+    uint64_t* drain_bar = mmab + 3;  // after an abort: the issued MMAs are done
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int gi = tid % kTPC;
@@ -128,7 +128,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     const int k1 = min(ntiles_all, k0 + tps);
     const uint32_t stage_tx = static_cast<uint32_t>(((has_z ? 3 : 2) * lay.cb + 2 * kN) * kRowB);
 
+    int last_issued = -1;  // thread 0: the last tile whose copy went out
     auto issue = [&](int k) {  // tile k0 + k
+        if (wait_aborted()) return;
+        // testing hook: the second tile's copy is never issued, so nothing arrives on its
+        // barrier and every wait for it runs out (no copy or MMA is in flight then)
+        if (a.fault_test && k == 1) return;
+        last_issued = k;
         unsigned char* st = smem + (k % kStages) * lay.stage;
         uint64_t* bar = &full[k % kStages];
         const int t0 = (k0 + k) * kT;
@@ -150,7 +156,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
         mbar_init(&mmab[0], 1);
         mbar_init(&mmab[1], 1);
+        mbar_init(drain_bar, 1);
         mbar_fence_init();
+        wait_setup(a.wait_limit);
     }
     // one-hot A operand: row m selects state group m % 4 (K = 16, first 32 bytes of a row);
     // the B/C operands start all zero in their first 32 bytes
@@ -231,6 +239,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         tc::fence_async_smem();
     };
     auto issue_mma = [&]() {
+        if (wait_aborted()) return;
         tc::fence_after();
         const uint64_t ad = tc::desc_sw128(smem_u32(smem + lay.onehot));
 #pragma unroll
@@ -424,14 +433,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
             a.h_final[static_cast<size_t>(ch) * kN + gi + kTPC * (2 * k + 1)] = hp[k].y;
         }
     }
+    if (tid == 0 && wait_aborted()) {
+        // a CTA whose waits gave up lets its copies and MMAs in flight finish before the
+        // shared and tensor memory they write is released
+        drain_ring(full, kStages, last_issued);
+        tc::mma_commit(drain_bar);  // arrives once every MMA this thread issued is done
+        mbar_drain(drain_bar, 0);
+    }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
-}
-
-int env_int(const char* name, int dflt) {
-    const char* v = getenv(name);
-    return (v && *v) ? atoi(v) : dflt;
 }
 
 }  // namespace
@@ -442,7 +453,9 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     const size_t es_out = a.out_dtype == SSM_BF16 ? 2 : 4;
     if (a.in_dtype != SSM_BF16 || a.dstate != kN || a.disc != SSM_DISC_EXP_EULER || a.seqlen <= 0 ||
         (static_cast<size_t>(a.seqlen) * 2) % 16 != 0 ||
-        (static_cast<size_t>(a.seqlen) * es_out) % 16 != 0 || env_int("SSM_M1_NO_TMEM", 0))
+        (static_cast<size_t>(a.seqlen) * es_out) % 16 != 0 ||
+        (a.kernel != SSM_SCAN_KERNEL_AUTO && a.kernel != SSM_SCAN_KERNEL_TMEM) ||
+        (a.tpc != 0 && a.tpc != kTPC))
         return cudaSuccess;
     int dev = 0, sms = 0, max_smem = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -462,10 +475,11 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     // pass over all but the last segment.
     const int ntiles = (a.seqlen + kT - 1) / kT;
     int segs = 1;
-    if (cpb < 48 && ntiles >= 16 && !env_int("SSM_M1_NO_SPLIT", 0)) {
+    if (cpb < 48 && ntiles >= 16 && a.max_segments != 1) {
         const int cps_full = (per_group + kMaxThreads / kTPC - 1) / (kMaxThreads / kTPC);
         int S = sms / (pairs * cps_full);
         if (S > ntiles / 4) S = ntiles / 4;  // at least 4 tiles per segment
+        if (a.max_segments > 1 && S > a.max_segments) S = a.max_segments;
         if (S >= 2) {
             cps = cps_full;
             cpb = (per_group + cps - 1) / cps;
@@ -527,11 +541,8 @@ cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspa
                                    : run(m1_scan_tmem<float, false>, plan.grid);
 }
 
-unsigned int m1_tmem_wait_timeouts() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-    cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero));
-    return v;
+cudaError_t m1_tmem_take_wait_timeouts(unsigned int* count) {
+    return take_wait_timeouts(count);
 }
 
 }  // namespace ssm

@@ -231,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              // within 3 steps of each other
     uint64_t* free_bar = done_bar + 4;       // [kCStages] the stage's MMA done (its reuse)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(free_bar + kCStages);
+    uint64_t* drain_bar = free_bar + kCStages + 1;  // after an abort: the issued MMAs are done
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -242,16 +243,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kCF; ++j) mbar_init(&mma_bar[j], 1);
         for (int j = 0; j < 4; ++j) mbar_init(&done_bar[j], kCompute);
         for (int j = 0; j < kCStages; ++j) mbar_init(&free_bar[j], 1);
+        mbar_init(drain_bar, 1);
         mbar_fence_init();
+        wait_setup(0);
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
 
+    int last_issued = -1;  // load warp, lane 0: the last step whose copy went out
     if (warp == kLoadWarp) {
         // step k of the walk handles chunk ce - 1 - k
         auto issue = [&](int k) {
+            if (wait_aborted()) return;
+            last_issued = k;
             const int c = ce - 1 - k;
             unsigned char* st = sm + (k % kCStages) * kCStBytes;
             uint64_t* bar = &tma_bar[k % kCStages];
@@ -275,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_warp(&done_bar[k & 3], (k >> 2) & 1);
             mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);  // complete already
             tc::fence_after();
+            if (wait_aborted_warp()) continue;  // issue nothing more
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
             const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * 16384);
@@ -329,6 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
         if (tid == 0) cut_decay[oi] = tailf;
     }
+    // a CTA whose waits gave up lets its copies and MMAs in flight finish before the
+    // shared and tensor memory they write is released
+    if (warp == kLoadWarp && lane == 0 && wait_aborted()) drain_ring(tma_bar, kCStages, last_issued);
+    if (warp == kMmaWarp && wait_aborted_warp()) {
+        tc::mma_commit_warp(drain_bar);  // the issuing lane's MMAs
+        if (lane == 0) mbar_drain(drain_bar, 0);
+        __syncwarp();
+    }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 128);
@@ -354,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar_b = bar_a + 2;          // MMA2-4 of a chunk done
     uint64_t* done_bar = bar_b + 1;       // [2] the compute warps finished a step
     uint32_t* tslot = reinterpret_cast<uint32_t*>(done_bar + 2);
+    uint64_t* drain_bar = done_bar + 3;   // [2] after an abort: each issuing warp's MMAs done
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -368,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&done_bar[j], kCompute);
         }
         mbar_init(bar_b, 2);  // one commit from each of the two issuing warps
+        mbar_init(&drain_bar[0], 1);
+        mbar_init(&drain_bar[1], 1);
         mbar_fence_init();
+        wait_setup(0);
     }
     tc::fence_before();
     __syncthreads();
@@ -381,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // G & 1, bar_a[G & 1] with parity (G >> 1) & 1.  Steps (n + 1 per range) alternate
     // between the two done barriers, so that no waiter can fall two phases behind.
     uint32_t gseq = 0, dstep = 0, b_seq = 0;
+    long long last_g = -1;  // load warp, lane 0: running number of the last chunk copied
 
     for (long long u = u0; u < u1;) {
         const int wk = static_cast<int>(u / nch);
@@ -395,6 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (warp == kLoadWarp) {
             auto issue = [&](int k) {  // chunk c0 + k
+                if (wait_aborted()) return;
+                last_g = static_cast<long long>(G0) + k;
                 const int c = c0 + k;
                 unsigned char* st = stage_of(k);
                 uint64_t* bar = tma_bar_of(k);
@@ -415,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);
                 ++dstep;
                 tc::fence_after();
-                if (k < n) {  // MMA3 and MMA4 of chunk k (MMA2 comes from the MMA warp)
+                if (k < n && !wait_aborted_warp()) {  // MMA3 and MMA4 of chunk k (MMA2: the MMA warp)
                     const unsigned char* st = stage_of(k);
                     const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC));
                     const uint64_t dB = tc::desc_sw128_mn(smem_u32(st + kStB), 8192);
@@ -439,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id1 = tc::idesc_bf16(64, 64), id2 = tc::idesc_bf16_mn(64, 64, false, true);
             auto mma1 = [&](int k) {  // CB of chunk k into its slot, then commit
                 mbar_wait_warp(tma_bar_of(k), tma_par(k));
+                if (wait_aborted_warp()) return;
                 const unsigned char* st = stage_of(k);
                 const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC)), dB = tc::desc_sw128(smem_u32(st + kStB));
                 const uint32_t slot = tmem + kColCB + 64 * ((G0 + k) & 1);
@@ -455,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);  // compute warps finished step k
                 ++dstep;
                 tc::fence_after();
-                if (k < n) {  // MMA2 of chunk k: Yd = M_hi X + M_lo X
+                if (k < n && !wait_aborted_warp()) {  // MMA2 of chunk k: Yd = M_hi X + M_lo X
                     const unsigned char* st = stage_of(k);
                     const uint64_t dX = tc::desc_sw128_mn(smem_u32(st + kStX), 8192);
                     const uint64_t dM = tc::desc_sw128(smem_u32(sm + kOffM + ((G0 + k) & 1) * 16384));
@@ -610,6 +633,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         gseq += n;
         u += n;
     }
+    // a CTA whose waits gave up lets its copies and MMAs in flight finish before the
+    // shared and tensor memory they write is released
+    if (warp == kLoadWarp || warp == kMmaWarp) {
+        if (wait_aborted_warp()) {
+            if (warp == kLoadWarp && lane == 0) drain_ring(tma_bar, kStages, last_g);
+            uint64_t* db = &drain_bar[warp == kLoadWarp ? 0 : 1];
+            tc::mma_commit_warp(db);  // the issuing lane's MMAs
+            if (lane == 0) mbar_drain(db, 0);
+            __syncwarp();
+        }
+    }
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -704,11 +738,8 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-unsigned int ssd_tc_wait_timeouts() {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-    cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero));
-    return v;
+cudaError_t ssd_tc_take_wait_timeouts(unsigned int* count) {
+    return take_wait_timeouts(count);
 }
 
 namespace {

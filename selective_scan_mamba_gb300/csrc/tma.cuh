@@ -38,17 +38,87 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Device-side count of waits that gave up, one counter per translation unit (each unit
-// that waits reads and clears its own; see ssm_wait_timeouts()).  A bounded wait never
-// hangs the GPU.
+// ---------------------------------------------------------------------------------------
+// Bounded waits.  A kernel that waits on mbarriers calls wait_setup() from thread 0 before
+// its first __syncthreads.  A wait polls its barrier up to the CTA's limit (default 2^24
+// polls, far longer than any copy or MMA takes).  If the limit runs out, the wait counts
+// the event in a device counter that the host reads and clears (ssm_device_status and
+// ssm_wait_timeouts), marks the CTA as aborted and returns false.  From then on every wait
+// in the CTA returns false at once.  The kernel keeps to its normal control flow and meets
+// every block barrier, but its threads issue no further copies or MMAs.  Before the CTA
+// frees its tensor memory and exits, the threads that issued asynchronous work wait
+// (mbar_drain, with the default limit and ignoring the abort) for what they issued.  The
+// outputs of an aborted call are not valid; the host learns of it through the counter.
+// ---------------------------------------------------------------------------------------
+
+// One counter per translation unit; ssm_device_status reads and clears each of them.
 static __device__ unsigned int g_ssm_wait_timeouts = 0;
 
-// Waits for phase `parity` of the barrier; gives up after ~2^24 polls (far longer than
-// any copy takes), counting the event instead of hanging.
-__device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < (1u << 24); ++i)
-        if (mbar_try_wait(bar, parity)) return;
+// Host side: reads this translation unit's counter into *count and clears it.  Waits for
+// the device first, so that the kernels launched before it have finished.
+static inline cudaError_t take_wait_timeouts(unsigned int* count) {
+    *count = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    unsigned int v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_ssm_wait_timeouts, sizeof(v))) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_ssm_wait_timeouts, &zero, sizeof(zero))) != cudaSuccess) return e;
+    *count = v;
+    return cudaSuccess;
+}
+
+constexpr uint32_t kWaitPolls = 1u << 24;
+
+static __shared__ uint32_t s_wait_abort;  // nonzero once a wait in this CTA gave up
+static __shared__ uint32_t s_wait_limit;  // polls before a wait gives up
+
+// Thread 0, before the kernel's first __syncthreads.  limit 0 = kWaitPolls.
+__device__ __forceinline__ void wait_setup(uint32_t limit) {
+    s_wait_abort = 0;
+    s_wait_limit = limit ? limit : kWaitPolls;
+}
+
+__device__ __forceinline__ bool wait_aborted() {
+    return *reinterpret_cast<volatile uint32_t*>(&s_wait_abort) != 0;
+}
+
+// The same, one answer for the whole warp (all 32 lanes must call it): for decisions that
+// guard warp-collective instructions such as an elected-lane MMA issue.
+__device__ __forceinline__ bool wait_aborted_warp() {
+    return __any_sync(0xffffffffu, wait_aborted());
+}
+
+// Waits for phase `parity` of the barrier.  Returns false if the CTA has aborted or the
+// limit ran out (which aborts it); the caller then skips issuing further work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t limit = *reinterpret_cast<volatile uint32_t*>(&s_wait_limit);
+    for (uint32_t i = 1; i < limit; ++i) {
+        if (wait_aborted()) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+    *reinterpret_cast<volatile uint32_t*>(&s_wait_abort) = 1u;
     atomicAdd(&g_ssm_wait_timeouts, 1u);
+    return false;
+}
+
+// Waits for work this thread issued before the CTA exits: polls up to kWaitPolls whether
+// or not the CTA has aborted (a copy or MMA still in flight must land before the shared
+// and tensor memory it writes is released).  Counts a failure like mbar_wait.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicAdd(&g_ssm_wait_timeouts, 1u);
+    return false;
+}
+
+// After an abort, by the thread that issued the copies of a ring of `stages` barriers:
+// copy number j (0, 1, 2, ... in issue order) completed on bars[j % stages] in phase
+// (j / stages) & 1, and `last` is the number of the last copy issued (-1: none).  Phases
+// of one barrier complete in order, so the last `stages` copies are the ones to wait for.
+__device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, long long last) {
+    for (long long j = last - stages + 1; j <= last; ++j)
+        if (j >= 0) mbar_drain(&bars[j % stages], static_cast<uint32_t>((j / stages) & 1));
 }
 
 // mbar_wait polled by lane 0 alone; the other lanes wait at __syncwarp, which also makes

@@ -19,8 +19,8 @@ def lib():
 
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "ssmscan.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:ssm_status|size_t|int|const char\*)\s+(\w+)\s*\(",
-                                 text, re.M)))
+    return sorted(set(re.findall(
+        r"^\s*(?:ssm_status|size_t|int|unsigned int|const char\*)\s+(\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_three_entry_points():
@@ -36,19 +36,29 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.ssm_abi_version() == 1
+    assert lib.ssm_abi_version() == 2 == _lib.ABI_VERSION
 
 
 
 FAKE = 0x7F0000000000  # a 16-byte aligned address; never dereferenced by these calls
 
 
+def fake(i):
+    """The i-th of a set of far-apart aligned fake addresses (distinct tensors, so that the
+    overlap checks pass); never dereferenced by these calls."""
+    return FAKE + (i << 36)
+
+
+def set_fakes(p, fields):
+    for i, f in enumerate(fields):
+        setattr(p, f, fake(i + 1))
+
+
 def scan_params(**kw):
     p = _lib.ScanParams()
     p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = 2, 32, 16, 64, 1
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
-    for f in ("x", "delta", "A", "B", "C", "y"):
-        setattr(p, f, FAKE)
+    set_fakes(p, ("x", "delta", "A", "B", "C", "y"))
     p.delta_softplus = 1
     for k, v in kw.items():
         setattr(p, k, v)
@@ -70,21 +80,67 @@ def scan_params(**kw):
 ])
 def test_scan_rejects_bad_arguments(lib, field, value, status):
     p = scan_params(**{field: value})
-    rc = lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None)
+    rc = lib.ssm_scan_fwd(ctypes.byref(p), None)
     assert rc == status
     assert lib.ssm_last_error().decode()
+    o = _lib.ScanOpts()
+    assert lib.ssm_scan_fwd_ex(ctypes.byref(p), ctypes.byref(o), fake(30), 1 << 30, None) == status
 
 
 def test_scan_null_params(lib):
-    assert lib.ssm_scan_fwd(None, None, 0, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_fwd(None, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_fwd_ex(None, None, None, 0, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_workspace_size(None, None) == 0
+
+
+@pytest.mark.parametrize("field,value", [("kernel", 9), ("threads_per_channel", 3),
+                                         ("max_segments", -1), ("fault_test", 2)])
+def test_scan_rejects_bad_options(lib, field, value):
+    o = _lib.ScanOpts()
+    setattr(o, field, value)
+    assert lib.ssm_scan_fwd_ex(ctypes.byref(scan_params()), ctypes.byref(o), None, 0, None) == \
+        _lib.SSM_ERR_INVALID_ARG
+    assert field in lib.ssm_last_error().decode()
+    assert lib.ssm_scan_workspace_size(ctypes.byref(scan_params()), ctypes.byref(o)) == 0
+
+
+def test_scan_kernel_that_cannot_run_the_problem_is_unsupported(lib):
+    """Naming a kernel that does not take the problem (the TMEM kernel needs bf16 inputs
+    and dstate 16) is refused on the host."""
+    o = _lib.ScanOpts()
+    o.kernel = _lib.SSM_SCAN_KERNEL_TMEM
+    p = scan_params(dstate=8)
+    assert lib.ssm_scan_fwd_ex(ctypes.byref(p), ctypes.byref(o), None, 0, None) == \
+        _lib.SSM_ERR_UNSUPPORTED
+    assert "TMEM" in lib.ssm_last_error().decode()
+
+
+@pytest.mark.parametrize("out,inp", [("y", "x"), ("y", "B"), ("h_final", "h0"), ("y", "h_final")])
+def test_scan_refuses_overlapping_outputs(lib, out, inp):
+    """An output that overlaps an input (or another output) is refused before any launch."""
+    p = scan_params(h0=fake(20), h_final=fake(21))
+    setattr(p, out, getattr(p, inp) + 64)  # inside the other tensor
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
+    assert "overlaps" in lib.ssm_last_error().decode()
+
+
+@pytest.mark.gpu
+def test_workspace_overlapping_an_input_is_refused(lib):
+    """The time-split plan's workspace must not overlap the tensors (one batch row, few
+    channels, long sequence: the automatic plan splits it)."""
+    p = scan_params(batch=1, dim=256, seqlen=4096)
+    o = _lib.ScanOpts()
+    need = lib.ssm_scan_workspace_size(ctypes.byref(p), ctypes.byref(o))
+    assert need > 0
+    assert lib.ssm_scan_fwd_ex(ctypes.byref(p), ctypes.byref(o), p.x, need, None) == \
+        _lib.SSM_ERR_INVALID_ARG
 
 
 def ssd_params(**kw):
     p = _lib.SsdParams()
     p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = 2, 256, 4, 64, 128, 1, 64
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
-    for f in ("x", "dt", "A", "B", "C", "y"):
-        setattr(p, f, FAKE)
+    set_fakes(p, ("x", "dt", "A", "B", "C", "y"))
     for k, v in kw.items():
         setattr(p, k, v)
     return p
@@ -102,8 +158,19 @@ def ssd_params(**kw):
 def test_ssd_rejects_bad_arguments(lib, field, value, status):
     p = ssd_params(**{field: value})
     need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
-    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, max(need, 1 << 30), None)
+    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), fake(30), max(need, 1 << 30), None)
     assert rc == status
+
+
+def test_ssd_refuses_overlaps(lib):
+    p = ssd_params()
+    need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
+    p.y = p.x
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), fake(30), need, None) == _lib.SSM_ERR_INVALID_ARG
+    assert "overlaps" in lib.ssm_last_error().decode()
+    p = ssd_params()
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), p.C, need, None) == _lib.SSM_ERR_INVALID_ARG
+    assert "workspace" in lib.ssm_last_error().decode()
 
 
 def test_ssd_workspace_size_and_shortfall(lib):
@@ -111,7 +178,7 @@ def test_ssd_workspace_size_and_shortfall(lib):
     need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
     nch = 256 // 64
     assert need >= 2 * 4 * nch * 32 * 128 * 4
-    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, need - 1, None)
+    rc = lib.ssd_chunk_scan_fwd(ctypes.byref(p), fake(30), need - 1, None)
     assert rc == _lib.SSM_ERR_INVALID_ARG
     assert "workspace" in lib.ssm_last_error().decode()
     assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(ssd_params(chunk_size=7))) == 0
@@ -121,11 +188,21 @@ def step_params(**kw):
     p = _lib.StepParams()
     p.batch, p.nheads, p.headdim, p.dstate, p.ngroups = 4, 8, 16, 64, 1
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
-    for f in ("state", "x", "dt", "A", "B", "C", "y"):
-        setattr(p, f, FAKE)
+    set_fakes(p, ("state", "x", "dt", "A", "B", "C", "y"))
     for k, v in kw.items():
         setattr(p, k, v)
     return p
+
+
+def test_step_refuses_y_inside_the_state(lib):
+    """The state is updated in place by design, but y may not overlap it or an input."""
+    p = step_params()
+    p.y = p.state + 256
+    assert lib.ssm_state_update(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
+    assert "overlaps" in lib.ssm_last_error().decode()
+    p = step_params()
+    p.state = p.B
+    assert lib.ssm_state_update(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("ntokens", [0, -1, 257])
@@ -152,10 +229,10 @@ def test_injected_launch_fault_reports_cuda_error(lib, monkeypatch):
     monkeypatch.setenv("SSM_FAULT_INJECT", "launch")
     assert lib.ssm_state_update(ctypes.byref(step_params()), None) == _lib.SSM_ERR_CUDA
     assert "injected" in lib.ssm_last_error().decode()
-    assert lib.ssm_scan_fwd(ctypes.byref(scan_params()), None, 0, None) == _lib.SSM_ERR_CUDA
+    assert lib.ssm_scan_fwd(ctypes.byref(scan_params()), None) == _lib.SSM_ERR_CUDA
     p = ssd_params()
     need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
-    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, need, None) == _lib.SSM_ERR_CUDA
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), fake(30), need, None) == _lib.SSM_ERR_CUDA
 
 
 def test_python_binding_refuses_cpu_tensors():
@@ -170,7 +247,7 @@ def test_python_binding_refuses_cpu_tensors():
 def test_size_ceilings_refuse_before_any_launch(lib):
     """Problems past the index ranges the kernels use are refused, not wrapped."""
     p = ssd_params(batch=4, seqlen=2**31 - 1)
-    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), fake(30), 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
     assert "too large" in lib.ssm_last_error().decode()
     p = step_params(batch=2**28)  # 2^41 state elements
     assert lib.ssm_state_update(ctypes.byref(p), None) == _lib.SSM_ERR_INVALID_ARG
@@ -189,11 +266,14 @@ C_STRUCTS = {
     "ssd_params": _lib.SsdParams,
     "ssd_bwd_params": _lib.SsdBwdParams,
     "ssm_step_params": _lib.StepParams,
+    "ssm_scan_opts": _lib.ScanOpts,
 }
 
 
 ENUM_CONSTANTS = ("SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA",
-                  "SSM_ERR_TIMEOUT", "SSM_F32", "SSM_BF16", "SSM_DISC_EXP_EULER", "SSM_DISC_ZOH")
+                  "SSM_ERR_TIMEOUT", "SSM_F32", "SSM_BF16", "SSM_DISC_EXP_EULER", "SSM_DISC_ZOH",
+                  "SSM_SCAN_KERNEL_AUTO", "SSM_SCAN_KERNEL_TMEM", "SSM_SCAN_KERNEL_TMA",
+                  "SSM_SCAN_KERNEL_TILED", "SSM_SCAN_KERNEL_GENERIC")
 
 
 def test_ctypes_structs_match_the_header_layout(tmp_path):
@@ -251,7 +331,7 @@ def _header_prototypes():
 def _ctype_of(c_type):
     """The ctypes type the binding must declare for a C parameter or return type."""
     t = c_type.replace("const ", "").replace(" *", "*").strip()
-    if t.endswith("_params*"):
+    if t.endswith("_params*") or t.endswith("_opts*"):
         return ctypes.POINTER(C_STRUCTS[t[:-1]])
     return {"void*": ctypes.c_void_p, "float*": ctypes.c_void_p, "size_t": ctypes.c_size_t,
             "int": ctypes.c_int, "ssm_status": ctypes.c_int, "char*": ctypes.c_char_p,
@@ -319,8 +399,8 @@ def test_python_binding_refuses_stream_of_another_device(monkeypatch):
 def scan_bwd_params(**kw):
     p = _lib.ScanBwdParams()
     p.fwd = scan_params()
-    for f in ("dy", "dx", "ddelta", "dA", "dB", "dC"):
-        setattr(p, f, FAKE)
+    for i, f in enumerate(("dy", "dx", "ddelta", "dA", "dB", "dC")):
+        setattr(p, f, fake(10 + i))
     for k, v in kw.items():
         if k.startswith("fwd_"):
             setattr(p.fwd, k[4:], v)
@@ -336,14 +416,15 @@ def scan_bwd_params(**kw):
     ({"dA": None}, _lib.SSM_ERR_INVALID_ARG),
     ({"dy": None}, _lib.SSM_ERR_INVALID_ARG),
     ({"dB": FAKE + 4}, _lib.SSM_ERR_INVALID_ARG),
-    ({"fwd_z": FAKE}, _lib.SSM_ERR_INVALID_ARG),            # z given, dz missing
-    ({"dD_skip": FAKE}, _lib.SSM_ERR_INVALID_ARG),          # dD given, D missing
-    ({"fwd_delta_bias": FAKE}, _lib.SSM_ERR_INVALID_ARG),   # bias given, dbias missing
+    ({"fwd_z": fake(20)}, _lib.SSM_ERR_INVALID_ARG),            # z given, dz missing
+    ({"dD_skip": fake(20)}, _lib.SSM_ERR_INVALID_ARG),          # dD given, D missing
+    ({"fwd_delta_bias": fake(20)}, _lib.SSM_ERR_INVALID_ARG),   # bias given, dbias missing
+    ({"dx": fake(1)}, _lib.SSM_ERR_INVALID_ARG),                # dx is x
     ({"fwd_ngroups": 3}, _lib.SSM_ERR_INVALID_ARG),
 ])
 def test_scan_bwd_rejects_bad_arguments(lib, kw, status):
     p = scan_bwd_params(**kw)
-    assert lib.ssm_scan_bwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssm_scan_bwd(ctypes.byref(p), fake(30), 1 << 40, None) == status
     assert lib.ssm_last_error()
 
 
@@ -352,7 +433,7 @@ def test_scan_bwd_workspace_size_and_shortfall(lib):
     need = lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
     # checkpoints every 32 steps, per-CTA dB/dC partials, per-row dA, dD, dbias partials
     assert need >= 2 * 32 * (64 // 32) * 16 * 4 + 2 * 32 * 16 * 4
-    assert lib.ssm_scan_bwd(ctypes.byref(p), FAKE, need - 1, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_bwd(ctypes.byref(p), fake(30), need - 1, None) == _lib.SSM_ERR_INVALID_ARG
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(scan_bwd_params(fwd_dstate=8))) == 0
     assert lib.ssm_scan_bwd_workspace_size(None) == 0
 
@@ -361,8 +442,7 @@ def mamba3_params(**kw):
     p = _lib.Mamba3Params()
     p.batch, p.dim, p.dstate, p.seqlen, p.ngroups = 2, 32, 16, 64, 1
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
-    for f in ("x", "delta", "A_re", "A_im", "lam", "B", "C", "y"):
-        setattr(p, f, FAKE)
+    set_fakes(p, ("x", "delta", "A_re", "A_im", "lam", "B", "C", "y"))
     p.delta_softplus = 1
     for k, v in kw.items():
         setattr(p, k, v)
@@ -380,7 +460,7 @@ def mamba3_params(**kw):
 ])
 def test_mamba3_rejects_bad_arguments(lib, field, value, status):
     p = mamba3_params(**{field: value})
-    assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssm_mamba3_scan_fwd(ctypes.byref(p), fake(30), 1 << 40, None) == status
     assert lib.ssm_last_error()
 
 
@@ -395,12 +475,11 @@ def test_s4d_rejects_bad_arguments(lib, field, value, status):
     p = _lib.S4dParams()
     p.batch, p.dim, p.dstate, p.seqlen = 2, 16, 32, 64
     p.in_dtype = p.out_dtype = _lib.SSM_BF16
-    for f in ("u", "log_dt", "A", "B", "C", "y"):
-        setattr(p, f, FAKE)
+    set_fakes(p, ("u", "log_dt", "A", "B", "C", "y"))
     setattr(p, field, value)
-    assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssm_s4d_scan_fwd(ctypes.byref(p), fake(30), 1 << 40, None) == status
     if field in ("dstate", "log_dt", "C"):
-        assert lib.ssm_s4d_kernel(ctypes.byref(p), FAKE, 16, None) == status
+        assert lib.ssm_s4d_kernel(ctypes.byref(p), fake(31), 16, None) == status
 
 
 def ssd_bwd_params(**kw):
@@ -408,11 +487,10 @@ def ssd_bwd_params(**kw):
     f = p.fwd
     f.batch, f.seqlen, f.nheads, f.headdim, f.dstate, f.ngroups, f.chunk_size = 2, 64, 4, 64, 128, 1, 64
     f.in_dtype = f.out_dtype = _lib.SSM_BF16
-    for n in ("x", "dt", "A", "B", "C"):
-        setattr(f, n, FAKE)
+    set_fakes(f, ("x", "dt", "A", "B", "C"))
     f.dt_softplus = 1
-    for n in ("dy", "dx", "ddt", "dA", "dB", "dC"):
-        setattr(p, n, FAKE)
+    for i, n in enumerate(("dy", "dx", "ddt", "dA", "dB", "dC")):
+        setattr(p, n, fake(10 + i))
     for k, v in kw.items():
         if k.startswith("fwd_"):
             setattr(p.fwd, k[4:], v)
@@ -425,13 +503,13 @@ def ssd_bwd_params(**kw):
     ({"fwd_disc": _lib.SSM_DISC_ZOH}, _lib.SSM_ERR_UNSUPPORTED),
     ({"fwd_dstate": 96}, _lib.SSM_ERR_UNSUPPORTED),
     ({"ddt": None}, _lib.SSM_ERR_INVALID_ARG),
-    ({"fwd_z": FAKE}, _lib.SSM_ERR_INVALID_ARG),
-    ({"fwd_dt_bias": FAKE}, _lib.SSM_ERR_INVALID_ARG),
+    ({"fwd_z": fake(20)}, _lib.SSM_ERR_INVALID_ARG),
+    ({"fwd_dt_bias": fake(20)}, _lib.SSM_ERR_INVALID_ARG),
     ({"dB": FAKE + 4}, _lib.SSM_ERR_INVALID_ARG),
 ])
 def test_ssd_bwd_rejects_bad_arguments(lib, kw, status):
     p = ssd_bwd_params(**kw)
-    assert lib.ssd_scan_bwd(ctypes.byref(p), FAKE, 1 << 40, None) == status
+    assert lib.ssd_scan_bwd(ctypes.byref(p), fake(30), 1 << 40, None) == status
     assert lib.ssm_last_error()
 
 
@@ -440,4 +518,4 @@ def test_ssd_bwd_workspace_size(lib):
     need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
     # includes the per-channel d(dt) buffer: batch * H * P * L floats
     assert need >= 2 * 4 * 64 * 64 * 4
-    assert lib.ssd_scan_bwd(ctypes.byref(p), FAKE, need - 1, None) == _lib.SSM_ERR_INVALID_ARG
+    assert lib.ssd_scan_bwd(ctypes.byref(p), fake(30), need - 1, None) == _lib.SSM_ERR_INVALID_ARG

@@ -46,3 +46,28 @@ def test_bwd_bytes_130m_layer():
     # 4 bf16 reads and 3 float32 writes per (b, d, t); B, C bf16 in and dB, dC float32 out
     b = bench.bwd_bytes(8, 1536, 16, 2048)
     assert b == 8 * 1536 * 2048 * 20 + 8 * 16 * 2048 * 12 + 1536 * 16 * 8 + 1536 * 16
+
+
+def test_percentile_interpolates_order_statistics():
+    xs = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.percentile(xs, 0) == 1.0
+    assert bench.percentile(xs, 50) == 3.0
+    assert bench.percentile(xs, 100) == 5.0
+    assert bench.percentile(xs, 95) == pytest.approx(4.8)
+    assert bench.percentile([], 95) is None
+
+
+def test_path_rooflines_carry_every_measured_path():
+    paths = {"ssd_130m_chunk64": {"roofline_bound": "hbm", "roofline_frac": 0.2, "ms": 0.08},
+             "decode_780m": {"hbm_frac": 0.75, "us_per_step": 40.0},
+             "m1_790m_long": {"4096": {"hbm_frac": 0.3, "ms": 0.05, "alu_frac": 0.5}}}
+    r = bench.path_rooflines(paths)
+    assert r["ssd_130m_chunk64"] == {"bound": "hbm", "frac": 0.2, "ms": 0.08}
+    assert r["decode_780m"]["frac"] == 0.75 and r["decode_780m"]["bound"] == "hbm"
+    assert r["m1_790m_L4096"]["frac"] == 0.3 and r["m1_790m_L4096"]["alu_frac"] == 0.5
+    assert bench.path_rooflines({}) == {}
+
+
+def test_sources_digest_is_stable():
+    d = bench.sources_digest()
+    assert len(d) == 16 and d == bench.sources_digest()

@@ -5,8 +5,6 @@ tolerance is max|y_gpu - y_ref| <= 1e-5 max|y_ref| for float32 inputs and
 2e-3 max|y_ref| for bfloat16 inputs with float32 state (the same for h_final); a
 bfloat16 output may in addition differ by the half-ulp of its own rounding.
 """
-import os
-
 import numpy as np
 import pytest
 
@@ -24,14 +22,14 @@ def _needs_gpu():
         pytest.fail("CUDA device required for -m gpu tests")
 
 
-def run_gpu(inp, out_dtype=None, disc="exp_euler", final=True, h0=True, softplus=True):
+def run_gpu(inp, out_dtype=None, disc="exp_euler", final=True, h0=True, softplus=True, **opts):
     import torch
     t = to_device(inp)
     od = {"bf16": torch.bfloat16, "f32": torch.float32}[out_dtype] if out_dtype else None
     y, hf = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t.get("D"),
                              z=t.get("z"), delta_bias=t["delta_bias"], delta_softplus=softplus,
                              h0=t.get("h0") if h0 else None, out_dtype=od,
-                             return_final_state=True, disc=disc)
+                             return_final_state=True, disc=disc, **opts)
     torch.cuda.synchronize()
     return to_numpy(y), to_numpy(hf)
 
@@ -69,41 +67,39 @@ def test_tiny_fp32_config(oracle_mod):
     check(hf, hr, TOL_F32, what="h_final")
 
 
-@pytest.mark.parametrize("tpc", ["1", "2", "4"])
+BF16_KERNELS = [("tmem", 4), ("tma", 2), ("tma", 4), ("tiled", 1), ("tiled", 2), ("tiled", 4)]
+
+
+@pytest.mark.parametrize("kernel,tpc", BF16_KERNELS)
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_bf16_tiled_multi_cta_ragged(oracle_mod, monkeypatch, tpc, out):
-    """Several CTAs, CTAs spanning a batch boundary, a ragged last tile, z, D, h0."""
-    monkeypatch.setenv("SSM_M1_TPC", tpc)
+def test_bf16_kernels_multi_cta_ragged(oracle_mod, kernel, tpc, out):
+    """Each bf16 kernel and threads-per-channel choice (named through ssm_scan_fwd_ex's
+    options): several CTAs, CTAs spanning a batch boundary, a ragged last tile, z, D, h0."""
     inp = synth.mamba1(3, 200, 16, 136, dtype=synth.BF16, delta_scale=1.0, with_z=True,
                        with_h0=True, seed=1)
-    y, hf = run_gpu(inp, out_dtype=out)
+    y, hf = run_gpu(inp, out_dtype=out, kernel=kernel, threads_per_channel=tpc)
     yr, hr = run_oracle(oracle_mod, inp)
     check(y, yr, TOL_BF16, out_bf16=(out == "bf16"), what="y")
     check(hf, hr, TOL_BF16, what="h_final")
 
 
 @pytest.mark.parametrize("path", ["tmem", "tma", "tiled"])
-def test_bf16_softplus_extremes(oracle_mod, monkeypatch, path):
+def test_bf16_softplus_extremes(oracle_mod, path):
     """delta + bias spread over about +-40: softplus in its linear range (v > 20), near 0
     and vanishing (v < -14, where the fast form may return 0), on each bf16 kernel."""
-    if path != "tmem":
-        monkeypatch.setenv("SSM_M1_NO_TMEM", "1")
-    if path == "tiled":
-        monkeypatch.setenv("SSM_M1_NO_TMA", "1")
     inp = synth.mamba1(2, 96, 16, 200, dtype=synth.BF16, delta_scale=14.0, with_z=True,
                        with_h0=True, seed=11)
-    y, hf = run_gpu(inp, out_dtype="f32")
+    y, hf = run_gpu(inp, out_dtype="f32", kernel=path)
     yr, hr = run_oracle(oracle_mod, inp)
     check(y, yr, TOL_BF16, what="y")
     check(hf, hr, TOL_BF16, what="h_final")
 
 
-@pytest.mark.parametrize("tpc", ["2", "4"])
-def test_fp32_tiled_with_gate_and_groups(oracle_mod, monkeypatch, tpc):
-    monkeypatch.setenv("SSM_M1_TPC", tpc)
+@pytest.mark.parametrize("tpc", [2, 4])
+def test_fp32_tiled_with_gate_and_groups(oracle_mod, tpc):
     inp = synth.mamba1(2, 320, 16, 100, dtype=synth.F32, with_z=True, with_h0=True, ngroups=2,
                        seed=2)
-    y, hf = run_gpu(inp, out_dtype="f32")
+    y, hf = run_gpu(inp, out_dtype="f32", kernel="tiled", threads_per_channel=tpc)
     yr, hr = run_oracle(oracle_mod, inp)
     check(y, yr, TOL_F32, what="y")
     check(hf, hr, TOL_F32, what="h_final")
@@ -220,6 +216,29 @@ def test_time_split_many_segments(oracle_mod, out):
     y, hf = run_gpu(inp, out_dtype=out)
     yr, hr = run_oracle(oracle_mod, inp)
     check(y, yr, TOL_BF16, out_bf16=(out == "bf16"), what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
+def test_plain_entry_point_needs_no_scratch(oracle_mod):
+    """ssm_scan_fwd(p, stream), called through the C ABI: one batch row with few channels
+    and a long sequence, a shape that ssm_scan_fwd_ex splits in time through a workspace,
+    runs in one pass without scratch and matches the oracle."""
+    import ctypes
+    import torch
+    from selective_scan_mamba_gb300 import _lib
+    inp = synth.mamba1(1, 256, 16, 4096, dtype=synth.BF16, with_z=True, with_h0=True, seed=13)
+    t = to_device(inp)
+    assert ssm.ssm_scan_workspace_size(t["x"], t["B"]) > 0  # the _ex plan would split
+    y = torch.empty_like(t["x"])
+    hf = torch.empty((1, 256, 16), dtype=torch.float32, device="cuda")
+    p = ssm._scan_params(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                         t["delta_bias"], True, t["h0"], y, hf, "exp_euler")
+    lib = _lib.load()
+    rc = lib.ssm_scan_fwd(ctypes.byref(p), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == _lib.SSM_OK, lib.ssm_last_error().decode()
+    torch.cuda.synchronize()
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, out_bf16=True, what="y")
     check(hf, hr, TOL_BF16, what="h_final")
 
 
