@@ -133,8 +133,8 @@ typedef struct {
     int max_segments;         /* time segments of the TMEM kernel's split for long
                                  sequences with few channels: 0 = automatic,
                                  1 = never split, n = at most n */
-    unsigned int wait_limit;  /* polls before a device-side wait gives up; 0 = the
-                                 default (2^24, seconds) */
+    unsigned int wait_limit;  /* polls before a device-side wait gives up, in whole
+                                 blocks of 1024; 0 = the default (2^24, seconds) */
     int fault_test;           /* testing only, 0 = off.  1: the TMEM kernel never copies
                                  the inputs of its second 64-step tile, so every wait
                                  for them runs out after wait_limit polls and the call

@@ -253,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tslot;
 
     int last_issued = -1;  // load warp, lane 0: the last step whose copy went out
+    bool live = true;      // MMA warp: no wait has failed yet
     if (warp == kLoadWarp) {
         // step k of the walk handles chunk ce - 1 - k
         auto issue = [&](int k) {
-            if (wait_aborted()) return;
             last_issued = k;
             const int c = ce - 1 - k;
             unsigned char* st = sm + (k % kCStages) * kCStBytes;
@@ -273,15 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (its F was built before that MMA was issued)
         if (lane == 0)
             for (int j = 0; j + kCStages < n; ++j) {
-                mbar_wait(&free_bar[j % kCStages], (j / kCStages) & 1);
+                if (!mbar_wait_lane(&free_bar[j % kCStages], (j / kCStages) & 1)) break;
                 issue(j + kCStages);
             }
     } else if (warp == kMmaWarp) {
         for (int k = 0; k < n; ++k) {
-            mbar_wait_warp(&done_bar[k & 3], (k >> 2) & 1);
-            mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);  // complete already
+            const bool built = mbar_wait_warp_ok(&done_bar[k & 3], (k >> 2) & 1);
+            const bool landed = mbar_wait_warp_ok(&tma_bar[k % kCStages], (k / kCStages) & 1);
             tc::fence_after();
-            if (wait_aborted_warp()) continue;  // issue nothing more
+            live = built && landed && live;
+            if (!live) continue;  // the CTA has aborted: issue nothing more
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
             const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * 16384);
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // between the two done barriers, so that no waiter can fall two phases behind.
     uint32_t gseq = 0, dstep = 0, b_seq = 0;
     long long last_g = -1;  // load warp, lane 0: running number of the last chunk copied
+    bool live = true;       // issuing warps: no wait has failed yet
 
     for (long long u = u0; u < u1;) {
         const int wk = static_cast<int>(u / nch);
@@ -415,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (warp == kLoadWarp) {
             auto issue = [&](int k) {  // chunk c0 + k
-                if (wait_aborted()) return;
                 last_g = static_cast<long long>(G0) + k;
                 const int c = c0 + k;
                 unsigned char* st = stage_of(k);
@@ -434,10 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
             const uint64_t dH = tc::desc_sw128_mn(smem_u32(sm + kOffHm), 16384);
             for (int k = 0; k <= n; ++k) {
-                mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);
+                // once a wait has failed (the CTA aborted) this warp issues nothing more
+                live = mbar_wait_warp_ok(&done_bar[dstep & 1], (dstep >> 1) & 1) && live;
                 ++dstep;
                 tc::fence_after();
-                if (k < n && !wait_aborted_warp()) {  // MMA3 and MMA4 of chunk k (MMA2: the MMA warp)
+                if (k < n && live) {  // MMA3 and MMA4 of chunk k (MMA2: the MMA warp)
                     const unsigned char* st = stage_of(k);
                     const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC));
                     const uint64_t dB = tc::desc_sw128_mn(smem_u32(st + kStB), 8192);
@@ -455,13 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 // the stage of chunk k-1 is free (its MMAs and outputs are done)
-                if (lane == 0 && k >= 1 && k + 2 < n) issue(k + 2);
+                if (lane == 0 && live && k >= 1 && k + 2 < n) issue(k + 2);
             }
         } else if (warp == kMmaWarp) {
             const uint32_t id1 = tc::idesc_bf16(64, 64), id2 = tc::idesc_bf16_mn(64, 64, false, true);
             auto mma1 = [&](int k) {  // CB of chunk k into its slot, then commit
-                mbar_wait_warp(tma_bar_of(k), tma_par(k));
-                if (wait_aborted_warp()) return;
+                live = mbar_wait_warp_ok(tma_bar_of(k), tma_par(k)) && live;
+                if (!live) return;
                 const unsigned char* st = stage_of(k);
                 const uint64_t dC = tc::desc_sw128(smem_u32(st + kStC)), dB = tc::desc_sw128(smem_u32(st + kStB));
                 const uint32_t slot = tmem + kColCB + 64 * ((G0 + k) & 1);
@@ -475,10 +477,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma1(0);
             if (n > 1) mma1(1);
             for (int k = 0; k <= n; ++k) {
-                mbar_wait_warp(&done_bar[dstep & 1], (dstep >> 1) & 1);  // compute warps finished step k
+                // the compute warps finished step k
+                live = mbar_wait_warp_ok(&done_bar[dstep & 1], (dstep >> 1) & 1) && live;
                 ++dstep;
                 tc::fence_after();
-                if (k < n && !wait_aborted_warp()) {  // MMA2 of chunk k: Yd = M_hi X + M_lo X
+                if (k < n && live) {  // MMA2 of chunk k: Yd = M_hi X + M_lo X
                     const unsigned char* st = stage_of(k);
                     const uint64_t dX = tc::desc_sw128_mn(smem_u32(st + kStX), 8192);
                     const uint64_t dM = tc::desc_sw128(smem_u32(sm + kOffM + ((G0 + k) & 1) * 16384));
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_commit_warp(bar_b);
                 }
                 __syncwarp();
-                if (k + 2 < n) mma1(k + 2);  // its slot held CB of chunk k, read in step k
+                if (live && k + 2 < n) mma1(k + 2);  // its slot held CB of chunk k, read in step k
             }
         } else {
             const int q4 = warp & 3, cg = warp >> 2;

@@ -44,7 +44,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // polls, far longer than any copy or MMA takes).  If the limit runs out, the wait counts
 // the event in a device counter that the host reads and clears (ssm_device_status and
 // ssm_wait_timeouts), marks the CTA as aborted and returns false.  From then on every wait
-// in the CTA returns false at once.  The kernel keeps to its normal control flow and meets
+// in the CTA returns false within 1024 polls.  The kernel keeps to its normal control flow and meets
 // every block barrier, but its threads issue no further copies or MMAs.  Before the CTA
 // frees its tensor memory and exits, the threads that issued asynchronous work wait
 // (mbar_drain, with the default limit and ignoring the abort) for what they issued.  The
@@ -72,7 +72,8 @@ constexpr uint32_t kWaitPolls = 1u << 24;
 static __shared__ uint32_t s_wait_abort;  // nonzero once a wait in this CTA gave up
 static __shared__ uint32_t s_wait_limit;  // polls before a wait gives up
 
-// Thread 0, before the kernel's first __syncthreads.  limit 0 = kWaitPolls.
+// Thread 0, before the kernel's first __syncthreads.  limit 0 = kWaitPolls; the limit is
+// counted in whole blocks of 1024 polls (at least one block).
 __device__ __forceinline__ void wait_setup(uint32_t limit) {
     s_wait_abort = 0;
     s_wait_limit = limit ? limit : kWaitPolls;
@@ -88,24 +89,47 @@ __device__ __forceinline__ bool wait_aborted_warp() {
     return __any_sync(0xffffffffu, wait_aborted());
 }
 
-// Waits for phase `parity` of the barrier.  Returns false if the CTA has aborted or the
-// limit ran out (which aborts it); the caller then skips issuing further work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint32_t limit = *reinterpret_cast<volatile uint32_t*>(&s_wait_limit);
-    for (uint32_t i = 1; i < limit; ++i) {
+// Slow path of the waits, taken after 1024 unsuccessful polls: polls on, reading the abort
+// flag and the limit once per 1024 polls.
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 1024;; i += 1024) {
         if (wait_aborted()) return false;
-        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= *reinterpret_cast<volatile uint32_t*>(&s_wait_limit)) break;
+        for (uint32_t j = 0; j < 1024; ++j)
+            if (mbar_try_wait(bar, parity)) return true;
     }
     *reinterpret_cast<volatile uint32_t*>(&s_wait_abort) = 1u;
     atomicAdd(&g_ssm_wait_timeouts, 1u);
     return false;
+}
+static __device__ __noinline__ bool mbar_wait_slow_call(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_slow(bar, parity);
+}
+
+// Waits for phase `parity` of the barrier.  Returns false if the CTA has aborted or the
+// limit ran out (which aborts it); the caller then skips issuing further work.  The first
+// 1024 polls are a bare loop of constant length, with the abort flag and the limit read
+// only on the slow path: loops that read them on every pass made the waiting threads take
+// issue slots from the working ones (the SSD walk measured 1.7x slower).  The exact form
+// was chosen by measurement: for waits by every thread (the Mamba-1 kernels) the slow path
+// is inlined; for waits by one lane of a warp (mbar_wait_lane, the SSD walk's hand-offs)
+// it is a call.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < 1024u; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity);
+}
+__device__ __forceinline__ bool mbar_wait_lane(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < 1024u; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow_call(bar, parity);
 }
 
 // Waits for work this thread issued before the CTA exits: polls up to kWaitPolls whether
 // or not the CTA has aborted (a copy or MMA still in flight must land before the shared
 // and tensor memory it writes is released).  Counts a failure like mbar_wait.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+#pragma unroll 1
     for (uint32_t i = 0; i < kWaitPolls; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     atomicAdd(&g_ssm_wait_timeouts, 1u);
@@ -126,8 +150,18 @@ __device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, long long
 // slots.  All 32 lanes must call it.  (A try_wait with a suspend-time hint measured
 // slower here: the sleeping thread wakes late.)
 __device__ __forceinline__ void mbar_wait_warp(uint64_t* bar, uint32_t parity) {
-    if ((threadIdx.x & 31) == 0) mbar_wait(bar, parity);
+    if ((threadIdx.x & 31) == 0) mbar_wait_lane(bar, parity);
     __syncwarp();
+}
+
+// mbar_wait_warp that also tells the whole warp whether the wait succeeded (false: the CTA
+// has aborted).  For the warps that issue copies or MMAs: they issue only after a wait
+// that succeeded, so they need no separate read of the abort flag on their critical path.
+__device__ __forceinline__ bool mbar_wait_warp_ok(uint64_t* bar, uint32_t parity) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_lane(bar, parity) ? 1 : 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // 2-D tiled bulk tensor load: box at (x = inner element index, y = row) into smem,
