@@ -13,8 +13,8 @@ host link's own rate for those bytes is measured beside it ("e2e.link_peak").
 Also reported (in "paths"): the Mamba-2 chunked SSD (130m-shaped, chunk 64 and 256),
 the decode update (780m-shaped, 1024 steps), multi-token decode, a decode serving loop
 over a hybrid Mamba-1/Mamba-2 stack, the Mamba-1 backward (130m layer), the SSD backward
-(130m SSD shape), the Mamba-3 scan (130m layer shape), S4D (recurrent form and kernel)
-and the long-context Mamba-1 sweep.
+(130m SSD shape), the Mamba-3 scan (130m layer shape), S4D (recurrent form, FFT
+convolution form and kernel) and the long-context Mamba-1 sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -541,6 +541,9 @@ def path_rooflines(paths):
     r = paths.get("decode_780m")
     if r:
         out["decode_780m"] = {"bound": "hbm", "frac": r["hbm_frac"], "us": r["us_per_step"]}
+    r = paths.get("s4d_256")
+    if r and "conv_hbm_frac" in r:
+        out["s4d_256_conv"] = {"bound": "hbm", "frac": r["conv_hbm_frac"], "ms": r["conv_ms"]}
     for L, r in paths.get("m1_790m_long", {}).items():
         out[f"m1_790m_L{L}"] = {"bound": "hbm", "frac": r["hbm_frac"], "ms": r["ms"],
                                 "alu_frac": r.get("alu_frac")}
@@ -822,8 +825,20 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
     Kbuf = torch.empty((Ds, Ls), dtype=torch.float32, device="cuda")
     tk = time_launches(torch, lambda i: ssm.ssm_s4d_kernel(s4["log_dt"], s4["A"], s4["B"], s4["C"],
                                                            Ls, out=Kbuf), 3, 1, stream)
+    # the convolution form: K, its spectrum and the FFT convolution (three launches)
+    cws = torch.empty(ssm.ssm_s4d_conv_workspace_size(us[0], s4["log_dt"], s4["A"], s4["B"], s4["C"]),
+                      dtype=torch.uint8, device="cuda")
+    tc_ = time_launches(torch, lambda i: ssm.ssm_s4d_conv_fwd(us[i % 2], s4["log_dt"], s4["A"], s4["B"],
+                                                              s4["C"], D=s4["D"], y=ys, workspace=cws),
+                        max(3, min(args.steps, 10)), 2, stream)
+    # algorithmic bytes of the convolution call: u in, y out (bf16), K and its spectrum
+    # written and read once (float32, complex64 of the padded length)
+    nfft = 1 << (2 * Ls - 1).bit_length()
+    cbytes = 2 * Bs * Ds * Ls * 2 + Ds * Ls * 4 * 2 + Ds * nfft * 8 * 2
     out["s4d_256"] = {"scan_ms": ts * 1e3, "state_updates_per_s": Bs * Ds * Ns * Ls / ts,
                       "scan_hbm_gbs": Bs * Ds * Ls * 4 / ts / 1e9, "kernel_ms": tk * 1e3,
+                      "conv_ms": tc_ * 1e3, "conv_hbm_gbs": cbytes / tc_ / 1e9,
+                      "conv_hbm_frac": cbytes / tc_ / 1e9 / hbm,
                       "shape": f"batch {Bs}, dim {Ds}, N {Ns} complex, L {Ls}; bf16 u, y"}
     del us, ys, Kbuf
     # long-context Mamba-1 sweep, 790m-shaped (batch 1, d_inner 3072, no z, h_final out)
@@ -1012,7 +1027,7 @@ def run_case(args):
         for _ in range(n):
             ssm.ssm_mamba3_scan_fwd(t["x"], t["delta"], t["A"], A_im, lam, t["B"], t["C"], D=t["D"],
                                     z=t["z"], delta_bias=t["delta_bias"])
-    elif args.case == "s4d":  # S4D recurrent form, batch 8, d_model 256, 32 states, L 4096
+    elif args.case in ("s4d", "s4d_conv"):  # S4D, batch 8, d_model 256, 32 states, L 4096
         Ds, Ns = 256, 32
         log_dt = torch.empty(Ds, device="cuda").uniform_(float(np.log(1e-3)), float(np.log(1e-1)))
         A = torch.stack([torch.full((Ds, Ns), -0.5, device="cuda"),
@@ -1023,7 +1038,10 @@ def run_case(args):
         Cm = torch.randn(Ds, Ns, 2, device="cuda")
         u = torch.randn(8, Ds, 4096, device="cuda").to(torch.bfloat16)
         for _ in range(n):
-            ssm.ssm_s4d_scan_fwd(u, log_dt, A, Bm, Cm)
+            if args.case == "s4d":  # recurrent form
+                ssm.ssm_s4d_scan_fwd(u, log_dt, A, Bm, Cm)
+            else:  # FFT convolution form
+                ssm.ssm_s4d_conv_fwd(u, log_dt, A, Bm, Cm)
     elif args.case == "tokens":  # 16 decode tokens per call, one state buffer
         c5 = synth.WORKLOADS["step_780m"]
         Bt, H, P, N, G = c5["batch"], c5["nheads"], c5["headdim"], c5["dstate"], c5["ngroups"]
@@ -1055,7 +1073,7 @@ def main():
     ap.add_argument("--e2e-sets", type=int, default=3,
                     help="device buffer sets the end-to-end leg rotates through (>= 2)")
     ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "step_m1", "tokens",
-                                       "bwd", "m3", "s4d"],
+                                       "bwd", "m3", "s4d", "s4d_conv"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:

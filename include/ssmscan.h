@@ -298,6 +298,20 @@ ssm_status ssm_s4d_scan_fwd(const ssm_s4d_params* p, void* workspace, size_t wor
  * log_dt, A, B and C of `p` (the other fields are ignored). */
 ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, void* stream);
 
+/* The convolution form on the GPU: y = K * u + D u, K_l as above for l < L, from a zero
+ * state ("From S4 to Mamba-3", 03/System: S4D trains as one FFT convolution).  The causal
+ * convolution is the first L points of the cyclic one of length N = 2^ceil(log2 2L):
+ * y = IFFT(FFT(K) . FFT(u)), computed in float32 (FFT error ~1e-6 of max|y|).  Uses batch,
+ * dim, dstate, seqlen, dtypes, u, log_dt, A, B, C, D_skip and y of `p`; h0 and h_final
+ * must be NULL (use ssm_s4d_scan_fwd for a carried state).
+ * `workspace`: ssm_s4d_conv_workspace_size(p) bytes, 16-byte aligned, contents on entry
+ * irrelevant (the kernel K [dim, L] and its spectrum [dim, N] complex).
+ * Limits: 1 <= L <= 8192 for the workspace query (N <= 16384 fits in shared memory; L = 0
+ * is accepted by the call and does nothing), dim <= 65535, dstate as ssm_s4d_scan_fwd. */
+size_t ssm_s4d_conv_workspace_size(const ssm_s4d_params* p);
+ssm_status ssm_s4d_conv_fwd(const ssm_s4d_params* p, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* ---------------------------------------------------------------------------
  * Mamba-2 chunked SSD scan (scalar A per head)
  *   ("From S4 to Mamba-3", 03/System, mamba2_minimal.py; 04/Approach)

@@ -11,7 +11,9 @@ the C names:
                                         -- decode: one token or T tokens, in place on the
                                            state
   * ssm_mamba3_scan_fwd                 -- Mamba-3 complex-diagonal scan
-  * ssm_s4d_scan_fwd, ssm_s4d_kernel    -- S4D recurrent form and convolution kernel
+  * ssm_s4d_scan_fwd, ssm_s4d_conv_fwd, ssm_s4d_kernel
+                                        -- S4D recurrent form, FFT convolution form and
+                                           convolution kernel
 
 Each takes CUDA torch tensors of the current device in the library's layouts, checks
 them, fills the C parameter struct and calls the library on the current torch stream
@@ -29,7 +31,8 @@ __all__ = [
     "ssm_scan_fwd", "ssm_scan_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
     "ssd_chunk_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_scan_bwd",
     "ssd_scan_bwd_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
-    "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd", "ssm_s4d_kernel", "wait_timeouts",
+    "ssm_mamba3_scan_fwd", "ssm_s4d_scan_fwd", "ssm_s4d_conv_fwd", "ssm_s4d_conv_workspace_size",
+    "ssm_s4d_kernel", "wait_timeouts",
     "device_status", "SsmError", "lib",
 ]
 
@@ -378,6 +381,44 @@ def ssm_s4d_scan_fwd(u, log_dt, A, B, C, D=None, h0=None, *, y=None, h_final=Non
     _lib.check(lib().ssm_s4d_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
     del keep, h0_
     return (y, h_final) if return_final_state else y
+
+
+def ssm_s4d_conv_fwd(u, log_dt, A, B, C, D=None, *, y=None, out_dtype=None, workspace=None,
+                     stream=None):
+    """S4D convolution form by FFT on the GPU: y = K * u + D u from a zero state (L <= 8192).
+
+    Same arguments as :func:`ssm_s4d_scan_fwd` without a state.  ``workspace``: a uint8
+    CUDA tensor of at least ssm_s4d_conv_workspace_size bytes (allocated here if None).
+    Returns y [batch, dim, L]."""
+    torch = _torch()
+    batch, dim, L = u.shape
+    p, keep = _s4d_params(log_dt, A, B, C, D)
+    if y is None:
+        y = torch.empty(u.shape, dtype=out_dtype or u.dtype, device=u.device)
+    p.batch, p.seqlen = batch, L
+    p.in_dtype = _dtype_code(u)
+    p.out_dtype = _dtype_code(y)
+    p.u = _ptr(u, "u")
+    p.y = _ptr(y, "y", (batch, dim, L))
+    need = int(lib().ssm_s4d_conv_workspace_size(ctypes.byref(p)))
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+        ws_ptr, ws_bytes = _ptr(workspace, "workspace"), workspace.numel()
+    _lib.check(lib().ssm_s4d_conv_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    del keep
+    return y
+
+
+def ssm_s4d_conv_workspace_size(u, log_dt, A, B, C) -> int:
+    """Scratch bytes ssm_s4d_conv_fwd needs for u's shape (0 if unsupported)."""
+    p, keep = _s4d_params(log_dt, A, B, C)
+    p.batch, _, p.seqlen = u.shape
+    p.in_dtype = p.out_dtype = _dtype_code(u)
+    n = int(lib().ssm_s4d_conv_workspace_size(ctypes.byref(p)))
+    del keep
+    return n
 
 
 def ssm_s4d_kernel(log_dt, A, B, C, kernel_len, *, out=None, stream=None):

@@ -93,7 +93,7 @@ class StepParams(ctypes.Structure):
 
 SYMBOLS = ("ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_workspace_size", "ssm_scan_bwd",
            "ssm_scan_bwd_workspace_size", "ssm_mamba3_scan_fwd", "ssm_mamba3_scan_workspace_size", "ssm_s4d_scan_fwd",
-           "ssm_s4d_scan_workspace_size",
+           "ssm_s4d_scan_workspace_size", "ssm_s4d_conv_fwd", "ssm_s4d_conv_workspace_size",
            "ssm_s4d_kernel", "ssd_scan_bwd", "ssd_scan_bwd_workspace_size", "ssd_chunk_scan_fwd",
            "ssd_chunk_scan_workspace_size", "ssm_state_update", "ssm_state_update_tokens",
            "ssm_last_error", "ssm_abi_version", "ssm_device_status", "ssm_wait_timeouts")
@@ -137,6 +137,10 @@ def load(build_if_missing: bool = True):
             lib.ssm_s4d_scan_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp, sz, _vp]
             lib.ssm_s4d_scan_workspace_size.restype = sz
             lib.ssm_s4d_scan_workspace_size.argtypes = [ctypes.POINTER(S4dParams)]
+            lib.ssm_s4d_conv_fwd.restype = _i
+            lib.ssm_s4d_conv_fwd.argtypes = [ctypes.POINTER(S4dParams), _vp, sz, _vp]
+            lib.ssm_s4d_conv_workspace_size.restype = sz
+            lib.ssm_s4d_conv_workspace_size.argtypes = [ctypes.POINTER(S4dParams)]
             lib.ssm_s4d_kernel.restype = _i
             lib.ssm_s4d_kernel.argtypes = [ctypes.POINTER(S4dParams), _vp, _i, _vp]
             lib.ssd_scan_bwd.restype = _i

@@ -772,6 +772,35 @@ ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, voi
     return SSM_OK;
 }
 
+size_t ssm_s4d_conv_workspace_size(const ssm_s4d_params* p) {
+    if (p == nullptr || p->batch < 1 || p->dim < 1 || p->dim > 65535 || p->seqlen < 1) return 0;
+    return ssm::s4d_conv_workspace_size(*p);
+}
+
+ssm_status ssm_s4d_conv_fwd(const ssm_s4d_params* p, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    g_err[0] = '\0';
+    RETURN_IF_FAILED(check_s4d(p, true));
+    REQUIRE(p->h0 == nullptr && p->h_final == nullptr,
+            "the convolution form starts from a zero state and gives no final state: h0 and "
+            "h_final must be NULL (use ssm_s4d_scan_fwd for either)");
+    if (p->dim > 65535) return fail(SSM_ERR_UNSUPPORTED, "s4d convolution: dim=%d > 65535", p->dim);
+    if (p->seqlen > 0 && !ssm::s4d_conv_supported(*p))
+        return fail(SSM_ERR_UNSUPPORTED, "s4d convolution: seqlen=%d > 8192 (the FFT of length "
+                    "2^ceil(log2 2L) must fit in shared memory; use ssm_s4d_scan_fwd)", p->seqlen);
+    const size_t need = p->seqlen > 0 ? ssm::s4d_conv_workspace_size(*p) : 0;
+    RETURN_IF_FAILED(check_workspace(workspace, workspace_bytes, need));
+    const S4dSizes s(*p);
+    RETURN_IF_FAILED(check_disjoint({{p->y, s.y, "y"}, {workspace, need, "workspace"}},
+                                    {{p->u, s.u, "u"}, {p->log_dt, s.dt, "log_dt"}, {p->A, s.abc, "A"},
+                                     {p->B, s.abc, "B"}, {p->C, s.abc, "C"}, {p->D_skip, s.dt, "D_skip"}}));
+    if (injected_launch_fault()) return fail(SSM_ERR_CUDA, "injected launch fault");
+    if (p->seqlen == 0) return SSM_OK;
+    cudaError_t e = ssm::s4d_conv_launch(*p, workspace, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_s4d_conv_fwd launch");
+    return SSM_OK;
+}
+
 size_t ssd_chunk_scan_workspace_size(const ssd_params* p) {
     if (check_ssd(p, false) != SSM_OK) return 0;
     return ssm::ssd_workspace_bytes(ssd_args(p, nullptr));

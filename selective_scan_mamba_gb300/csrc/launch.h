@@ -55,6 +55,10 @@ bool s4d_supported(int dstate);
 size_t s4d_workspace_size(const ssm_s4d_params& a);
 cudaError_t s4d_launch(const ssm_s4d_params& a, void* workspace, cudaStream_t s);
 cudaError_t s4d_kernel_launch(const ssm_s4d_params& a, float* K, int L, cudaStream_t s);
+// S4D convolution form by FFT (s4d_conv.cu)
+bool s4d_conv_supported(const ssm_s4d_params& a);
+size_t s4d_conv_workspace_size(const ssm_s4d_params& a);
+cudaError_t s4d_conv_launch(const ssm_s4d_params& a, void* workspace, cudaStream_t s);
 
 struct M1Plan {
     enum Kind { kGeneric = 0, kTiled = 1, kTma = 2, kTmem = 3 } kind;

@@ -121,3 +121,66 @@ def test_time_split_long_sequence(oracle_mod, bf16):
     """Few channels and a long sequence: the plan cuts the sequence into segments (a
     states-only pass, then each segment from the carried state); h0 and h_final."""
     _run(oracle_mod, 1, 8, 16, 3000, bf16, seed=11)
+
+
+def _conv(oracle, batch, dim, N, L, bf16, out_bf16=False, seed=0):
+    """The FFT convolution form on the GPU against both float64 oracle forms (the FFT
+    convolution and the recurrence from a zero state), which the oracle pins equal."""
+    import torch
+    log_dt, A, B, C, D = _params(dim, N, seed)
+    log_dt, D = log_dt.astype(np.float32).astype(np.float64), D.astype(np.float32).astype(np.float64)
+    C = C.astype(np.complex64).astype(np.complex128)
+    A = A.astype(np.complex64).astype(np.complex128)
+    rng = np.random.default_rng(seed + 1)
+    u = rng.standard_normal((batch, dim, L)).astype(np.float32)
+    if bf16:
+        bits = synth.bf16_bits(u)
+        u = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+        ut = torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    else:
+        ut = torch.from_numpy(u).cuda()
+    dl, dA, dB, dC, dD = _dev_params(log_dt, A, B, C, D)
+    y = ssm.ssm_s4d_conv_fwd(ut, dl, dA, dB, dC, D=dD,
+                             out_dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    torch.cuda.synchronize()
+    u64 = u.astype(np.float64)
+    yc = oracle.s4d_fft_conv(u64, log_dt, A, B, C, D=D)
+    yr, _ = oracle.s4d_recurrent(u64, log_dt, A, B, C, D=D)
+    tol = TOL_BF16 if bf16 else TOL_S4D_F32
+    check(y, yc, tol, out_bf16=out_bf16, what="y vs the oracle's FFT convolution")
+    check(y, yr, tol, out_bf16=out_bf16, what="y vs the oracle's recurrence")
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_convolution_form_efficiency_sweep_shape(oracle_mod, bf16):
+    """The pages' efficiency-sweep shape: batch 8, d_model 256, 32 complex states, L 4096."""
+    _conv(oracle_mod, 8, 256, 32, 4096, bf16, out_bf16=bf16)
+
+
+@pytest.mark.parametrize("batch,L,N", [(3, 1000, 16), (1, 1, 8), (2, 8192, 4), (5, 257, 64)])
+def test_convolution_form_ragged_and_limits(oracle_mod, batch, L, N):
+    """An odd batch (the last transform carries one row), lengths that are not powers of
+    two, one step, and the longest sequence the shared-memory transform takes (8192)."""
+    _conv(oracle_mod, batch, 6, N, L, False, seed=batch)
+
+
+def test_convolution_form_refusals():
+    import torch
+    log_dt, A, B, C, D = _params(4, 8, 2)
+    dl, dA, dB, dC, dD = _dev_params(log_dt, A, B, C, D)
+    u = torch.randn(1, 4, 8193, device="cuda")
+    assert ssm.ssm_s4d_conv_workspace_size(u, dl, dA, dB, dC) == 0
+    with pytest.raises(ssm.SsmError) as err:
+        ssm.ssm_s4d_conv_fwd(u, dl, dA, dB, dC, D=dD)
+    assert err.value.status == 2 and "8192" in err.value.message
+    # the convolution form carries no state
+    from selective_scan_mamba_gb300 import _lib
+    import ctypes
+    p, keep = ssm._s4d_params(dl, dA, dB, dC, dD)
+    u = torch.randn(1, 4, 64, device="cuda")
+    y = torch.empty_like(u)
+    h0 = torch.zeros(1, 4, 8, 2, device="cuda")
+    p.batch, p.seqlen = 1, 64
+    p.u, p.y, p.h0 = u.data_ptr(), y.data_ptr(), h0.data_ptr()
+    assert _lib.load().ssm_s4d_conv_fwd(ctypes.byref(p), None, 0, None) == _lib.SSM_ERR_INVALID_ARG
+    del keep
