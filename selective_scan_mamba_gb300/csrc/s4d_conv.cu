@@ -7,26 +7,31 @@
 // to N = 2^ceil(log2 2L): y = IFFT(FFT(K) . FFT(u)) restricted to t < L.
 //
 // Two launches:
-//   1. s4d_kspec, one CTA per channel: K_l = Re sum_n w_n z_n^l (w = C Bbar, z = Abar)
-//      for l < L, with z^l = z^(64 q) z^i (l = 64 q + i): each power's phase l Im z is
-//      formed and reduced modulo 2 pi in double, then evaluated in float; w is folded
-//      into the first power, so each (l, n) costs two FMAs.  Then
-//      Khat = FFT(K zero-padded) / N into the workspace, [dim, N] complex.
+//   1. s4d_kspec, one CTA per channel: K_l = Re sum_n w_n z_n^l (w = C Bbar, z = Delta A)
+//      for l < L, with e^(l z) = e^(64 q z) e^(i z) (l = 64 q + i) from two small power
+//      tables per state, so each (l, n) costs two FMAs.  A power's phase l Im z is taken
+//      as a 64-bit fixed-point fraction of a turn, l times frac(Im z / 2 pi) modulo 2^64
+//      (exact integer wrap-around; Delta and that fraction are formed in double), then
+//      evaluated in float.  Then Khat = FFT(K zero-padded) / N into the workspace,
+//      [dim, N] complex; CTA 0 also stores the twiddle tables there.
 //   2. s4d_conv, per channel and pair of batch rows (b, b + 1): one complex sequence
 //      u_b + i u_{b+1} (zero-padded) is transformed, multiplied by Khat and transformed
 //      back.  K is real, so Khat is Hermitian and IFFT(Khat FFT(u_b + i u_{b+1})) =
 //      y_b + i y_{b+1}: two rows per transform pair.  The inverse is conj(FFT(conj(.))),
-//      so one forward routine serves both.  Then D u is added.
+//      so one forward routine serves both.  The first pass reads u from global memory,
+//      the last forward pass multiplies by Khat as it stores, and the last inverse pass
+//      adds D u and writes y: the sequence goes through shared memory only between passes.
 // The transforms run in shared memory, one CTA of N / 16 threads per sequence: a Stockham
 // (autosort) FFT, natural order in and out, in passes of radix 16 (and one of radix 2, 4
-// or 8 for the remaining bits).  In a pass each thread loads its butterfly's 16 points
-// into registers, the block syncs, each thread twiddles, transforms and stores them, and
-// the block syncs again, so one buffer serves in place (one pad slot per 16 elements
-// keeps the strided stores off a single bank).  Twiddles exp(-2 pi i k / N), k < N/2,
-// are computed once per CTA with sincospif (the argument -2k/N is exact in float32); the
-// radix-16 butterflies use the 16th roots of unity as constants.  N is at most 16384
-// (L <= 8192): the sequence and the twiddles take 192 KB of shared memory (204 KB with
-// the power tables of the spectrum kernel).
+// or 8 for the remaining bits).  In a pass each thread loads its butterfly's points into
+// registers, the block syncs, each thread twiddles, transforms and stores them, and the
+// block syncs again, so one buffer serves in place (one pad slot per 16 elements keeps
+// the strided stores off a single bank).  Pass p (after the first) twiddles point r of
+// butterfly k by w^(r k), w = exp(-2 pi i / (Ns R)): w^k is read from that pass's own
+// table (consecutive k, so no bank conflicts) and its powers are formed by repeated
+// multiplication.  Input points past N / 2 are zero and output points past N / 2 are
+// never read (L <= N / 2), so the first forward and last inverse passes skip them.
+// N is at most 16384 (L <= 8192).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -41,16 +46,28 @@ constexpr int kMaxThreads = (1 << kMaxLog2N) / 16;  // N / 16 threads: one radix
 constexpr int kPowChunk = 64;  // l = 64 q + i in the kernel generator
 constexpr int kGroup = 8;      // states per power-table round
 constexpr int kMaxSteps = 8;   // steps l < L per thread: L <= N / 2 = 8 x threads
-constexpr int kTableFloat2 = kGroup * ((1 << (kMaxLog2N - 1)) / kPowChunk + kPowChunk);
+constexpr int kMaxStates = 64;
 
 // threads of a block for an N = 2^m point transform
 __host__ __device__ inline int fft_threads(int m) { return m >= 9 ? (1 << m) / 16 : 32; }
+// passes of an N = 2^m transform: radix 16 while four bits remain, then radix 2, 4 or 8
+__host__ __device__ inline int n_passes(int m) { return m / 4 + (m % 4 != 0); }
+__host__ __device__ inline int pass_log2_radix(int m, int p) { return p < m / 4 ? 4 : m % 4; }
+// pass p >= 1 has Ns = 16^p; its table of Ns twiddles starts at sum_{i=1}^{p-1} 16^i
+__host__ __device__ inline int twiddle_offset(int p) { return ((1 << (4 * p)) - 16) / 15; }
+__host__ __device__ inline int twiddle_len(int m) { return n_passes(m) > 1 ? twiddle_offset(n_passes(m)) : 0; }
 
 // Shared-memory position of element i: one pad slot per 16 elements, so that the
 // stride-16 stores of the first pass (and the stride-Ns ones after it) spread over the
 // banks instead of all landing on one.
 __device__ __forceinline__ int pad(int i) { return i + (i >> 4); }
 __host__ __device__ inline int padded_len(int n) { return n + (n >> 4); }
+// the spectrum kernel's sequence region also holds its power tables first
+__host__ __device__ inline int power_chunks(int L) { return (L + kPowChunk - 1) / kPowChunk; }
+__host__ __device__ inline int kspec_x_len(int m, int L) {
+    const int t = kGroup * (power_chunks(L) + kPowChunk), x = padded_len(1 << m);
+    return t > x ? t : x;
+}
 
 __device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
 __device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
@@ -111,132 +128,203 @@ __device__ __forceinline__ void dft_reg(float2* v) {
     }
 }
 
-// W[k] = exp(-2 pi i k / N), k < N / 2
+// The twiddle tables of every pass after the first: pass p's entry k is
+// exp(-2 pi i k / (Ns R)), k < Ns = 16^p (the argument -2k / (Ns R) is exact in float).
 __device__ void make_twiddles(float2* W, int m) {
-    const int N = 1 << m;
-    for (int k = threadIdx.x; k < N / 2; k += blockDim.x) {
-        float s, c;
-        sincospif(-2.0f * static_cast<float>(k) / static_cast<float>(N), &s, &c);
-        W[k] = make_float2(c, s);
+    for (int p = 1; p < n_passes(m); ++p) {
+        const int ns_log2 = 4 * p, Ns = 1 << ns_log2;
+        const float inv = 1.0f / static_cast<float>(Ns << pass_log2_radix(m, p));
+        float2* T = W + twiddle_offset(p);
+        for (int k = threadIdx.x; k < Ns; k += blockDim.x) {
+            float s, c;
+            sincospif(-2.0f * static_cast<float>(k) * inv, &s, &c);
+            T[k] = make_float2(c, s);
+        }
     }
 }
-// exp(-2 pi i k / N) for k < N from the half table
-__device__ __forceinline__ float2 twiddle(const float2* W, int k, int half) {
-    if (k < half) return W[k];
-    const float2 w = W[k - half];
-    return make_float2(-w.x, -w.y);
-}
 
-// One Stockham pass of radix R over N = 2^m points in place, Ns = product of the
-// radices of the passes before it (BPT = butterflies per thread, upper bound).
-template <int R, int BPT>
-__device__ __forceinline__ void stockham_pass(float2* X, const float2* W, int m, int ns_log2) {
-    constexpr int LR = R == 2 ? 1 : R == 4 ? 2 : R == 8 ? 3 : 4;
-    const int N = 1 << m, nb = N >> LR, Ns = 1 << ns_log2;
-    const int tw_shift = m - ns_log2 - LR;  // N / (Ns R) = 2^tw_shift
+// One Stockham pass of radix 2^LR over N = 2^m points, Ns = 2^ns_log2 (the product of
+// the radices before it), at most BPT butterflies per thread.  load(t) gives point t of
+// the pass input, store(t, v) takes point t of its output; with SYNC the block syncs
+// between the loads and the stores (both in the same shared buffer).  HALF_IN: input
+// points t >= N / 2 are zero and not loaded; HALF_OUT: output points t >= N / 2 are not
+// formed (only for a last pass, where they are r >= R / 2).  tw: this pass's table.
+template <int LR, int BPT, bool HALF_IN, bool HALF_OUT, bool SYNC, class Load, class Store>
+__device__ __forceinline__ void fft_pass(const float2* tw, int m, int ns_log2, Load load, Store store) {
+    constexpr int R = 1 << LR;
+    const int nb = 1 << (m - LR), Ns = 1 << ns_log2;
     float2 v[BPT][R];
 #pragma unroll
     for (int q = 0; q < BPT; ++q) {
         const int j = threadIdx.x + q * blockDim.x;
         if (j < nb) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[q][r] = X[pad(j + r * nb)];
+            for (int r = 0; r < R; ++r) v[q][r] = HALF_IN && r >= R / 2 ? make_float2(0.f, 0.f) : load(j + r * nb);
         }
     }
-    __syncthreads();
+    if (SYNC) __syncthreads();
 #pragma unroll
     for (int q = 0; q < BPT; ++q) {
         const int j = threadIdx.x + q * blockDim.x;
         if (j < nb) {
             const int k = j & (Ns - 1);
-            if (Ns > 1) {
+            if (ns_log2 > 0) {
+                const float2 w = tw[k];
+                float2 wr = w;
 #pragma unroll
-                for (int r = 1; r < R; ++r) v[q][r] = cmul(v[q][r], twiddle(W, (r * k) << tw_shift, N >> 1));
+                for (int r = 1; r < R; ++r) {
+                    v[q][r] = cmul(v[q][r], wr);
+                    if (r + 1 < R) wr = cmul(wr, w);
+                }
             }
             dft_reg<R>(v[q]);
             const int base = ((j - k) << LR) + k;  // (j / Ns) Ns R + k
 #pragma unroll
-            for (int r = 0; r < R; ++r) X[pad(base + r * Ns)] = v[q][r];
+            for (int r = 0; r < (HALF_OUT ? R / 2 : R); ++r) store(base + r * Ns, v[q][r]);
         }
     }
+}
+
+// pass p of an N = 2^m transform with its radix chosen at run time
+template <bool HALF_IN, bool HALF_OUT, bool SYNC, class Load, class Store>
+__device__ __forceinline__ void fft_pass_any(const float2* W, int m, int p, Load load, Store store) {
+    const float2* tw = W + (p > 0 ? twiddle_offset(p) : 0);
+    const int ns_log2 = 4 * p;
+    switch (pass_log2_radix(m, p)) {
+        case 4: fft_pass<4, 1, HALF_IN, HALF_OUT, SYNC>(tw, m, ns_log2, load, store); break;
+        case 3: fft_pass<3, 2, HALF_IN, HALF_OUT, SYNC>(tw, m, ns_log2, load, store); break;
+        case 2: fft_pass<2, 4, HALF_IN, HALF_OUT, SYNC>(tw, m, ns_log2, load, store); break;
+        default: fft_pass<1, 8, HALF_IN, HALF_OUT, SYNC>(tw, m, ns_log2, load, store); break;
+    }
+}
+
+// point loaders and storers of a pass
+struct LoadX {
+    const float2* X;
+    __device__ __forceinline__ float2 operator()(int t) const { return X[pad(t)]; }
+};
+struct StoreX {
+    float2* X;
+    __device__ __forceinline__ void operator()(int t, float2 v) const { X[pad(t)] = v; }
+};
+
+// Forward FFT of N = 2^m points whose second half is zero: the first pass takes its
+// input from first(t) (t < N / 2; FIRST_SYNC if that reads X) and stores into X; the
+// middle passes run in X; the last pass hands its natural-order output to last(t, v).
+// The block syncs after every pass but the last (last may write X: the caller syncs).
+template <bool FIRST_SYNC, class First, class Last>
+__device__ __forceinline__ void fft_forward(float2* X, const float2* W, int m, First first, Last last) {
+    const LoadX ld{X};
+    const StoreX st{X};
+    const int P = n_passes(m);
+    if (P == 1) {
+        fft_pass_any<true, false, FIRST_SYNC>(W, m, 0, first, last);
+        return;
+    }
+    // every pass but the last has radix 16
+    fft_pass<4, 1, true, false, FIRST_SYNC>(W, m, 0, first, st);
     __syncthreads();
+    for (int p = 1; p + 1 < P; ++p) {
+        fft_pass<4, 1, false, false, true>(W + twiddle_offset(p), m, 4 * p, ld, st);
+        __syncthreads();
+    }
+    fft_pass_any<false, false, true>(W, m, P - 1, ld, last);
 }
 
-// Forward FFT of N = 2^m (1 <= m <= 14) points in X (padded positions), natural order in
-// and out, by a block of fft_threads(m) threads: passes of radix 16, then one of radix 2,
-// 4 or 8 if m % 4 != 0.  With N / 16 threads a radix-R pass has 16 / R butterflies per
-// thread.
-__device__ void fft_stockham(float2* X, const float2* W, int m) {
-    int done = 0;
-    while (m - done >= 4) {
-        stockham_pass<16, 1>(X, W, m, done);
-        done += 4;
+// FFT of the N = 2^m points in X of which only outputs t < N / 2 are wanted, handed to
+// last(t, v); X is overwritten.
+template <class Last>
+__device__ __forceinline__ void fft_half_out(float2* X, const float2* W, int m, Last last) {
+    const LoadX ld{X};
+    const StoreX st{X};
+    const int P = n_passes(m);
+    for (int p = 0; p + 1 < P; ++p) {
+        fft_pass<4, 1, false, false, true>(W + (p > 0 ? twiddle_offset(p) : 0), m, 4 * p, ld, st);
+        __syncthreads();
     }
-    switch (m - done) {
-        case 1: stockham_pass<2, 8>(X, W, m, done); break;
-        case 2: stockham_pass<4, 4>(X, W, m, done); break;
-        case 3: stockham_pass<8, 2>(X, W, m, done); break;
-        default: break;
-    }
+    fft_pass_any<false, true, false>(W, m, P - 1, ld, last);
 }
 
-// one state's w = C Bbar and z = e^(Delta A), the latter as magnitude log and phase (double)
-__device__ void s4d_wz(const ssm_s4d_params& a, int d, int n, double* wr, double* wi, double* zr,
-                       double* zi) {
-    const double dt = exp(static_cast<double>(a.log_dt[d]));
+// One state's w = C Bbar / N (float), Re z = Delta Re A (float) and frac(Im z / 2 pi) as a
+// 64-bit fixed-point fraction of a turn, z = Delta A.  Delta and Im z are formed in double:
+// the phase l Im z reaches 1e5 rad at long L, so its turn fraction must hold that many
+// more bits than a float does.  Bbar = (e^z - 1) / z Delta B (zero-order hold).
+struct StateWZ {
+    float2 w;
+    float zr;
+    unsigned long long turn;
+};
+struct StoreKhat {
+    float2* kh;
+    __device__ __forceinline__ void operator()(int t, float2 v) const { kh[t] = v; }
+};
+
+__device__ StateWZ s4d_wz(const ssm_s4d_params& a, int d, int n, double dt, float inv_n) {
     const size_t k = (static_cast<size_t>(d) * a.dstate + n) * 2;
-    const double ar = a.A[k], ai = a.A[k + 1], br = a.B[k], bi = a.B[k + 1];
-    const double pr0 = dt * ar, pi0 = dt * ai;  // z = Delta A
-    const double ex = exp(pr0);
-    double sn, cs;
-    sincos(pi0, &sn, &cs);
-    double pr, pi;  // phi1(z) = (e^z - 1) / z, Taylor 1 + z/2 + z^2/6 near 0
-    if (sqrt(pr0 * pr0 + pi0 * pi0) < 1e-4) {
-        pr = 1.0 + pr0 / 2.0 + (pr0 * pr0 - pi0 * pi0) / 6.0;
-        pi = pi0 / 2.0 + (2.0 * pr0 * pi0) / 6.0;
+    const double zi = dt * static_cast<double>(a.A[k + 1]);
+    const double x = zi * 0.15915494309189535;  // turns
+    const double f = x - floor(x);                // [0, 1)
+    StateWZ s;
+    // f 2^64 as an integer: f 2^32 splits into high word and remainder (both exact)
+    const double hi = floor(f * 4294967296.0);
+    const double lo = (f * 4294967296.0 - hi) * 4294967296.0;
+    s.turn = (static_cast<unsigned long long>(hi) << 32) + static_cast<unsigned long long>(lo);
+    const float dtf = static_cast<float>(dt);
+    const float pr0 = dtf * a.A[k], pi0 = static_cast<float>(zi);
+    s.zr = pr0;
+    float sn, cs;
+    sincosf(pi0, &sn, &cs);
+    float pr, pi;  // phi1(z) = (e^z - 1) / z, Taylor 1 + z/2 + z^2/6 near 0
+    const float den = pr0 * pr0 + pi0 * pi0;
+    if (den < 1e-6f) {
+        pr = 1.0f + pr0 / 2.0f + (pr0 * pr0 - pi0 * pi0) / 6.0f;
+        pi = pi0 / 2.0f + (2.0f * pr0 * pi0) / 6.0f;
     } else {
-        const double s2 = sin(pi0 / 2.0);
-        const double nr = expm1(pr0) * cs - 2.0 * s2 * s2;
-        const double ni = ex * sn;
-        const double den = pr0 * pr0 + pi0 * pi0;
+        const float s2 = sinf(pi0 / 2.0f);
+        const float nr = expm1f(pr0) * cs - 2.0f * s2 * s2;  // Re e^z - 1
+        const float ni = expf(pr0) * sn;
         pr = (nr * pr0 + ni * pi0) / den;
         pi = (ni * pr0 - nr * pi0) / den;
     }
-    const double bbr = dt * (br * pr - bi * pi), bbi = dt * (br * pi + bi * pr);
-    const double cr = a.C[k], ci = a.C[k + 1];
-    *wr = cr * bbr - ci * bbi;
-    *wi = cr * bbi + ci * bbr;
-    *zr = pr0;
-    *zi = pi0;
+    const float br = a.B[k], bi = a.B[k + 1];
+    const float bbr = dtf * (br * pr - bi * pi), bbi = dtf * (br * pi + bi * pr);
+    const float cr = a.C[k], ci = a.C[k + 1];
+    s.w = make_float2((cr * bbr - ci * bbi) * inv_n, (cr * bbi + ci * bbr) * inv_n);
+    return s;
 }
 
-// e^(l z) in float: the phase l Im z is formed and reduced modulo 2 pi in double (it
-// reaches 1e5 rad at long L), then sine, cosine and the magnitude e^(l Re z) in float
-__device__ __forceinline__ float2 pow_z(double zr, double zi, double l) {
-    const double inv_two_pi = 0.15915494309189535, two_pi = 6.283185307179586;
-    const double x = l * zi;
-    const float ph = static_cast<float>(x - two_pi * floor(x * inv_two_pi));
+// e^(l z) for an integer l >= 0 in float: the phase from the turn fraction l frac(Im z /
+// 2 pi) modulo 1 (exact in 64 bits, then its top 32 bits as a signed turn in [-1/2, 1/2)),
+// the magnitude e^(l Re z)
+__device__ __forceinline__ float2 pow_z(const StateWZ& s, unsigned int l) {
+    const unsigned long long ph = s.turn * static_cast<unsigned long long>(l);
+    const int top = static_cast<int>(static_cast<unsigned int>(ph >> 32));
     float sn, cs;
-    sincosf(ph, &sn, &cs);
-    const float mag = expf(static_cast<float>(l * zr));
+    sincospif(static_cast<float>(top) * 4.656612873077393e-10f, &sn, &cs);  // top / 2^31
+    const float mag = expf(static_cast<float>(l) * s.zr);
     return make_float2(mag * cs, mag * sn);
 }
 
 // Khat[d] = FFT(K[d] zero-padded to N) / N, K computed here (see the file comment): each
-// state's w and z once (double), then the power tables of kGroup states at a time in a
-// small region T; each thread keeps the sums of its steps l = tid + threads k in registers.
-__global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float2* Khat, int m) {
+// state's w and z once, then the power tables of kGroup states at a time (in the space of
+// X, which is filled only afterwards); each thread keeps the sums of its steps
+// l = tid + threads k in registers.  CTA 0 also stores the twiddle tables for s4d_conv.
+__global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float2* Khat, float2* Wg, int m) {
     extern __shared__ float2 sm[];
-    __shared__ double s_w[64][4];  // per state: Re w, Im w, Re z, Im z
+    __shared__ StateWZ s_wz[kMaxStates];
     const int N = 1 << m, L = a.seqlen, Ns = a.dstate, nt = blockDim.x;
     float2* X = sm;
-    float2* W = sm + padded_len(N);
-    float2* T = W + N / 2;  // [kGroup][nq + kPowChunk]: w z^(64 q) / N, then z^i
+    float2* W = sm + kspec_x_len(m, L);
+    float2* T = X;  // [kGroup][nq + kPowChunk]: w z^(64 q) / N, then z^i
     const int d = blockIdx.x;
-    const int nq = (L + kPowChunk - 1) / kPowChunk;
+    const int nq = power_chunks(L);
     const int row = nq + kPowChunk;
-    const float inv_n = 1.0f / static_cast<float>(N);  // a power of two: exact
-    for (int n = threadIdx.x; n < Ns; n += nt) s4d_wz(a, d, n, &s_w[n][0], &s_w[n][1], &s_w[n][2], &s_w[n][3]);
+    make_twiddles(W, m);
+    {
+        const double dt = exp(static_cast<double>(a.log_dt[d]));
+        const float inv_n = 1.0f / static_cast<float>(N);  // a power of two: exact
+        for (int n = threadIdx.x; n < Ns; n += nt) s_wz[n] = s4d_wz(a, d, n, dt, inv_n);
+    }
     __syncthreads();
     float acc[kMaxSteps];
 #pragma unroll
@@ -245,13 +333,11 @@ __global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float
         const int ng = min(kGroup, Ns - n0);
         for (int e = threadIdx.x; e < ng * row; e += nt) {
             const int g = e / row, r = e % row;
-            const double* wz = s_w[n0 + g];
+            const StateWZ& s = s_wz[n0 + g];
             if (r < nq) {
-                const float2 p = pow_z(wz[2], wz[3], static_cast<double>(r) * kPowChunk);
-                const float wr = static_cast<float>(wz[0]) * inv_n, wi = static_cast<float>(wz[1]) * inv_n;
-                T[e] = make_float2(wr * p.x - wi * p.y, wr * p.y + wi * p.x);
+                T[e] = cmul(s.w, pow_z(s, static_cast<unsigned int>(r * kPowChunk)));
             } else {
-                T[e] = pow_z(wz[2], wz[3], static_cast<double>(r - nq));
+                T[e] = pow_z(s, static_cast<unsigned int>(r - nq));
             }
         }
         __syncthreads();
@@ -268,56 +354,83 @@ __global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float
         }
         __syncthreads();
     }
+    // K into X (the first pass reads only t < N / 2, the rest is zero by HALF_IN)
 #pragma unroll
-    for (int k = 0; k < 2 * kMaxSteps; ++k) {
+    for (int k = 0; k < kMaxSteps; ++k) {
         const int l = threadIdx.x + k * nt;
-        if (l < N) X[pad(l)] = make_float2(k < kMaxSteps && l < L ? acc[k < kMaxSteps ? k : 0] : 0.f, 0.f);
+        if (l < N / 2) X[pad(l)] = make_float2(l < L ? acc[k] : 0.f, 0.f);
     }
-    make_twiddles(W, m);
+    if (d == 0) {
+        for (int k = threadIdx.x; k < twiddle_len(m); k += nt) Wg[k] = W[k];
+    }
     __syncthreads();
-    fft_stockham(X, W, m);
-    for (int k = threadIdx.x; k < N; k += nt) Khat[static_cast<size_t>(d) * N + k] = X[pad(k)];
+    fft_forward<true>(X, W, m, LoadX{X}, StoreKhat{Khat + static_cast<size_t>(d) * N});
 }
 
+// u_b + i u_{b+1}, zero past L
+template <typename Tin>
+struct LoadRows {
+    const Tin* u0;
+    const Tin* u1;
+    int L;
+    bool has_b1;
+    __device__ __forceinline__ float2 operator()(int t) const {
+        float re = 0.f, im = 0.f;
+        if (t < L) {
+            re = to_f32(u0[t]);
+            if (has_b1) im = to_f32(u1[t]);
+        }
+        return make_float2(re, im);
+    }
+};
+// Y = X Khat (Khat holds 1/N), stored conjugated for the inverse
+struct StoreTimesKhat {
+    float2* X;
+    const float2* kh;
+    __device__ __forceinline__ void operator()(int t, float2 v) const {
+        const float2 y = cmul(v, __ldg(kh + t));
+        X[pad(t)] = make_float2(y.x, -y.y);
+    }
+};
+// the conjugate of the inverse is y_b0 + i y_b1 with D u added; t < L only
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kMaxThreads) s4d_conv(ssm_s4d_params a, const float2* Khat, int m) {
+struct StoreRows {
+    const Tin* u0;
+    const Tin* u1;
+    Tout* y0;
+    Tout* y1;
+    float Dd;
+    int L;
+    bool has_b1;
+    __device__ __forceinline__ void operator()(int t, float2 v) const {
+        if (t < L) {
+            io<Tout>::store(y0, t, v.x + Dd * to_f32(u0[t]));
+            if (has_b1) io<Tout>::store(y1, t, -v.y + Dd * to_f32(u1[t]));
+        }
+    }
+};
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kMaxThreads) s4d_conv(ssm_s4d_params a, const float2* Khat, const float2* Wg,
+                                                       int m) {
     extern __shared__ float2 sm[];
     const int N = 1 << m;
     float2* X = sm;
     float2* W = sm + padded_len(N);
     const int d = blockIdx.y;
-    const int b0 = 2 * blockIdx.x, b1 = b0 + 1;
-    const bool has_b1 = b1 < a.batch;
+    const int b0 = 2 * blockIdx.x;
+    const bool has_b1 = b0 + 1 < a.batch;
     const int L = a.seqlen;
-    const Tin* u = static_cast<const Tin*>(a.u);
-    const size_t r0 = (static_cast<size_t>(b0) * a.dim + d) * L;
-    const size_t r1 = (static_cast<size_t>(b1) * a.dim + d) * L;
-    make_twiddles(W, m);
-    for (int t = threadIdx.x; t < N; t += blockDim.x) {
-        float re = 0.f, im = 0.f;
-        if (t < L) {
-            re = to_f32(u[r0 + t]);
-            if (has_b1) im = to_f32(u[r1 + t]);
-        }
-        X[pad(t)] = make_float2(re, im);
-    }
+    const Tin* u0 = static_cast<const Tin*>(a.u) + (static_cast<size_t>(b0) * a.dim + d) * L;
+    const Tin* u1 = u0 + static_cast<size_t>(a.dim) * L;  // row b0 + 1 (read only if has_b1)
+    for (int k = threadIdx.x; k < twiddle_len(m); k += blockDim.x) W[k] = Wg[k];
+    // the first pass stores no twiddles' reader: the sync after it publishes W too
+    fft_forward<false>(X, W, m, LoadRows<Tin>{u0, u1, L, has_b1},
+                       StoreTimesKhat{X, Khat + static_cast<size_t>(d) * N});
     __syncthreads();
-    fft_stockham(X, W, m);
-    // Y = X Khat (Khat holds 1/N); the inverse is conj(FFT(conj(Y)))
-    const float2* kh = Khat + static_cast<size_t>(d) * N;
-    for (int k = threadIdx.x; k < N; k += blockDim.x) {
-        const float2 y = cmul(X[pad(k)], kh[k]);
-        X[pad(k)] = make_float2(y.x, -y.y);
-    }
-    __syncthreads();
-    fft_stockham(X, W, m);
-    const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
-    Tout* y = static_cast<Tout*>(a.y);
-    for (int t = threadIdx.x; t < L; t += blockDim.x) {
-        const float2 v = X[pad(t)];  // conj of the inverse: y_b0 = v.x, y_b1 = -v.y
-        io<Tout>::store(y, r0 + t, v.x + Dd * to_f32(u[r0 + t]));
-        if (has_b1) io<Tout>::store(y, r1 + t, -v.y + Dd * to_f32(u[r1 + t]));
-    }
+    Tout* y0 = static_cast<Tout*>(a.y) + (static_cast<size_t>(b0) * a.dim + d) * L;
+    fft_half_out(X, W, m, StoreRows<Tin, Tout>{u0, u1, y0, y0 + static_cast<size_t>(a.dim) * L,
+                                               a.D_skip ? a.D_skip[d] : 0.f, L, has_b1});
 }
 
 int log2_fft(int L) {
@@ -327,44 +440,49 @@ int log2_fft(int L) {
 }
 
 size_t smem_bytes(int m) {
-    return static_cast<size_t>(padded_len(1 << m) + (1 << (m - 1))) * sizeof(float2);
+    return static_cast<size_t>(padded_len(1 << m) + twiddle_len(m)) * sizeof(float2);
 }
-size_t kspec_smem_bytes(int m) { return smem_bytes(m) + kTableFloat2 * sizeof(float2); }
+size_t kspec_smem_bytes(int m, int L) {
+    return static_cast<size_t>(kspec_x_len(m, L) + twiddle_len(m)) * sizeof(float2);
+}
 
 template <typename Tin, typename Tout>
-cudaError_t launch_conv(const ssm_s4d_params& a, const float2* Khat, int m, cudaStream_t s) {
+cudaError_t launch_conv(const ssm_s4d_params& a, const float2* Khat, const float2* Wg, int m, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(s4d_conv<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes(m)));
     if (e != cudaSuccess) return e;
     const dim3 grid((a.batch + 1) / 2, a.dim);
-    s4d_conv<Tin, Tout><<<grid, fft_threads(m), smem_bytes(m), s>>>(a, Khat, m);
+    s4d_conv<Tin, Tout><<<grid, fft_threads(m), smem_bytes(m), s>>>(a, Khat, Wg, m);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool s4d_conv_supported(const ssm_s4d_params& a) {
-    return s4d_supported(a.dstate) && a.seqlen >= 1 && log2_fft(a.seqlen) <= kMaxLog2N;
+    return s4d_supported(a.dstate) && a.dstate <= kMaxStates && a.seqlen >= 1 && log2_fft(a.seqlen) <= kMaxLog2N;
 }
 
+// [dim, N] complex Khat, then the twiddle tables
 size_t s4d_conv_workspace_size(const ssm_s4d_params& a) {
     if (!s4d_conv_supported(a)) return 0;
-    return static_cast<size_t>(a.dim) * (static_cast<size_t>(1) << log2_fft(a.seqlen)) * sizeof(float2);
+    const int m = log2_fft(a.seqlen);
+    return (static_cast<size_t>(a.dim) * (static_cast<size_t>(1) << m) + twiddle_len(m)) * sizeof(float2);
 }
 
 cudaError_t s4d_conv_launch(const ssm_s4d_params& a, void* workspace, cudaStream_t s) {
     const int m = log2_fft(a.seqlen);
     float2* Khat = static_cast<float2*>(workspace);
-    cudaError_t e = cudaFuncSetAttribute(s4d_kspec, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kspec_smem_bytes(m)));
+    float2* Wg = Khat + static_cast<size_t>(a.dim) * (static_cast<size_t>(1) << m);
+    const size_t ks = kspec_smem_bytes(m, a.seqlen);
+    cudaError_t e = cudaFuncSetAttribute(s4d_kspec, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ks));
     if (e != cudaSuccess) return e;
-    s4d_kspec<<<a.dim, fft_threads(m), kspec_smem_bytes(m), s>>>(a, Khat, m);
+    s4d_kspec<<<a.dim, fft_threads(m), ks, s>>>(a, Khat, Wg, m);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool ib = a.in_dtype == SSM_BF16, ob = a.out_dtype == SSM_BF16;
-    if (ib && ob) return launch_conv<bf16_t, bf16_t>(a, Khat, m, s);
-    if (ib) return launch_conv<bf16_t, float>(a, Khat, m, s);
-    if (ob) return launch_conv<float, bf16_t>(a, Khat, m, s);
-    return launch_conv<float, float>(a, Khat, m, s);
+    if (ib && ob) return launch_conv<bf16_t, bf16_t>(a, Khat, Wg, m, s);
+    if (ib) return launch_conv<bf16_t, float>(a, Khat, Wg, m, s);
+    if (ob) return launch_conv<float, bf16_t>(a, Khat, Wg, m, s);
+    return launch_conv<float, float>(a, Khat, Wg, m, s);
 }
 
 }  // namespace ssm
