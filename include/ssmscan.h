@@ -179,7 +179,10 @@ ssm_status ssm_scan_fwd_ex(const ssm_scan_params* p, const ssm_scan_opts* opts,
  *   ddelta_bias : [D]           (required exactly when fwd.delta_bias is given)
  *   dh0         : [Bt, D, N]    (nullable: not written)
  * Limits: exponential-Euler only and dstate in {16, 32, 64, 128} (else SSM_ERR_UNSUPPORTED).
- * The result does not depend on launch order (partial sums are added in a fixed order).
+ * dA, dD_skip and ddelta_bias are summed in a fixed order and do not depend on launch
+ * order.  dB and dC are sums over the channels of the group that the kernel adds up
+ * with float32 atomic adds, so their last bits can differ between runs (each is within
+ * rounding of the exact sum either way).
  * ------------------------------------------------------------------------- */
 typedef struct {
     ssm_scan_params fwd;
@@ -197,7 +200,8 @@ typedef struct {
 } ssm_scan_bwd_params;
 
 /* Device scratch for ssm_scan_bwd, in bytes (0 when the problem is invalid or
- * unsupported): per-chunk state checkpoints and per-CTA partial sums. */
+ * unsupported): state checkpoints at two levels, about 2 sqrt(L / 16) states per
+ * channel, and per-(batch, channel) partial sums of dA, dD_skip, ddelta_bias. */
 size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p);
 
 /* Runs the backward pass.  `workspace`: at least ssm_scan_bwd_workspace_size(p) bytes,
@@ -483,7 +487,9 @@ typedef struct {
     float* dh0;
 } ssd_bwd_params;
 
-/* Device scratch for ssd_scan_bwd in bytes (0 when invalid or unsupported). */
+/* Device scratch for ssd_scan_bwd in bytes (0 when invalid or unsupported): as for
+ * ssm_scan_bwd.  ddt, like dB and dC, is a sum over channels (the head's P) added up
+ * with float32 atomic adds; dA, dD_skip, ddt_bias are summed in a fixed order. */
 size_t ssd_scan_bwd_workspace_size(const ssd_bwd_params* p);
 
 ssm_status ssd_scan_bwd(const ssd_bwd_params* p, void* workspace, size_t workspace_bytes,

@@ -12,25 +12,35 @@
 //   dx_t = sum_n G_t Delta_t B_t + do_t D,   dDelta_t = sum_n G_t (B_t x_t + h_{t-1} E_t A)
 //   dA[n] += G_t h_{t-1} E_t Delta_t,   g <- G_t E_t,   d(delta)_t = dDelta_t sigmoid(v_t).
 //
-// One launch computes everything per CTA, then a small launch sums the partials:
+// One launch computes everything per CTA, then a small launch sums the per-row partials:
 //   - a CTA owns 128 / TPC channels of one (batch, group) (TPC threads per channel, four
 //     consecutive states per thread);
-//   - pass 1 runs the recurrence forwards and keeps h at the start of every 16-step chunk
-//     (the checkpoints, in the workspace);
-//   - pass 2 walks the chunks last to first: it stages the chunk's inputs in shared
-//     memory, recomputes h_t over the chunk from its checkpoint into a shared buffer
-//     (with the pre-gate output o_t), sums dC over the CTA's channels from that buffer,
-//     walks the chunk backwards overwriting h_t by G_t (h_t is dead once step t+1 has
-//     used it), then sums dB over the channels from the same buffer;
-//   - dB, dC partial sums per CTA and dA, dD, dbias partial sums per batch row go to the
-//     workspace; the second launch adds them up, so the result does not depend on the
-//     order in which CTAs run.
+//   - the sequence is cut into 16-step chunks and the chunks into blocks of K chunks:
+//     K = 1 while a checkpoint per chunk takes no more room than x and dy (N <= 16 in
+//     bf16), else K ~ sqrt(chunks); pass 1 runs the recurrence forwards and keeps h at
+//     the start of every block (coarse checkpoints, in the workspace);
+//   - pass 2 takes the blocks last to first: when K > 1 it reruns the block forwards
+//     from its checkpoint, keeping h at the start of each of its chunks (fine
+//     checkpoints, one block's worth in the workspace), then walks the block's chunks
+//     last to first: it
+//     stages the chunk's inputs in shared memory, recomputes h_t over the chunk from its
+//     checkpoint into a shared buffer (with the pre-gate output o_t), sums dC over the
+//     CTA's channels from that buffer, walks the chunk backwards overwriting h_t by G_t
+//     (h_t is dead once step t+1 has used it), then sums dB over the channels from the
+//     same buffer;
+//   - the CTA adds its dB, dC sums into the outputs (zeroed before the launch) with
+//     float32 atomic adds, so their last bits depend on the order in which CTAs arrive;
+//     dA, dD, dbias partial sums per batch row go to the workspace and the second
+//     launch adds them in a fixed order.
+// So the workspace is at most x plus dy in size, or two sets of checkpoints of about
+// sqrt(L / 16) states per channel each, for one extra forward pass.
 // The same kernels serve the Mamba-2 SSD backward: with a scalar A per head its
 // recurrence is this scan over the H*P channels of the heads, A tied over a head's
 // channels and states and Delta, D and the bias shared by its P channels.  A BwdView
 // carries the element strides of either layout and `hp`, the channels per head; with
-// hp > 1 the per-channel d(delta) goes to the workspace and the second launch sums each
-// head's P channels (and A over the states too).
+// hp > 1 the per-channel d(delta) is added into the head's ddt (zeroed before the
+// launch) with atomic adds, and the second launch sums A over the head's channels and
+// states.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -66,8 +76,34 @@ struct BwdLayout {  // float offsets into dynamic shared memory (16-byte aligned
 };
 
 struct BwdWs {  // byte offsets into the workspace
-    size_t ckpt, part_bc, part_a, part_d, part_bias, dd_chan, bytes;
+    size_t ckpt, fine, part_a, part_d, part_bias, bytes;
 };
+
+// chunks per checkpoint block: one (a checkpoint per chunk, no rerun) while those
+// checkpoints, N floats per 16 steps and channel, take no more room than x and dy;
+// else about the square root of the chunk count, which keeps the coarse ([row][blocks]
+// [N]) and fine ([row][K][N]) checkpoints together smallest
+inline int bwd_block_chunks(int nch, int N, int L, int in_bytes, int dy_bytes) {
+    if (static_cast<long long>(nch) * N * 4 <= static_cast<long long>(L) * (in_bytes + dy_bytes)) return 1;
+    int k = 1;
+    while (k * k < nch) ++k;
+    return k;
+}
+
+// float32 atomic adds into dB / dC: four consecutive states as one vector add when they
+// are contiguous (16-byte aligned there: N % 4 == 0 and 16-byte aligned outputs)
+__device__ __forceinline__ void red_add4(float* p, long long stride, float4 v) {
+    if (stride == 1) {
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                     "f"(v.w)
+                     : "memory");
+    } else {
+        atomicAdd(p, v.x);
+        atomicAdd(p + stride, v.y);
+        atomicAdd(p + 2 * stride, v.z);
+        atomicAdd(p + 3 * stride, v.w);
+    }
+}
 
 __host__ __device__ inline int bwd_cpb(int tpc) { return kBThreads / tpc; }
 
@@ -99,8 +135,8 @@ namespace {
 
 template <typename Tin, typename Tdy, int TPC>
 __global__ void __launch_bounds__(kBThreads, 4)
-    m1_scan_bwd(BwdView a, int cps, float* ckpt, float* part_bc, float* part_a, float* part_d,
-                float* part_bias, float* dd_chan) {
+    m1_scan_bwd(BwdView a, int cps, int kb, float* ckpt, float* fine, float* part_a, float* part_d,
+                float* part_bias) {
     constexpr int N = TPC * kBS;
     constexpr int CPB = kBThreads / TPC;
     constexpr int NQ = kBT * N / 4;         // (step, 4 states) cells of a chunk
@@ -115,6 +151,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
     const int nchan = l1 - l0;
     const int d0 = g * per_group + l0;
     const int nch = (L + kBT - 1) / kBT;
+    const int nblk = (nch + kb - 1) / kb;  // kb: chunks per checkpoint block
 
     extern __shared__ __align__(16) float sm[];
     const BwdLayout lay(CPB, N);
@@ -186,8 +223,8 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
     };
     // sum over the CTA's channels of w[channel][t] * buf[t][channel][n] for every (t, n) of
-    // the chunk, into the partial row `dst` ([N][L] at column t0): cell q = (t, 4 states)
-    // per thread slice, SPLIT slices of the channels, then the slices added
+    // the chunk, added into dst (dB or dC) at step t0 + t: cell q = (t, 4 states) per
+    // thread slice, SPLIT slices of the channels, then the slices added
     auto channel_sum = [&](int wofs, float* dst, int t0, int tl) {
       for (int q0 = 0; q0 < (NQ > kBThreads ? NQ : 1); q0 += kBThreads) {
         const int q = NQ > kBThreads ? q0 + tid : tid % NQ, sl = NQ > kBThreads ? 0 : tid / NQ;
@@ -217,23 +254,19 @@ __global__ void __launch_bounds__(kBThreads, 4)
                 }
             }
         }
-        if (sl == 0 && t < tl) {
-            dst[static_cast<size_t>(4 * n4 + 0) * L + t0 + t] = s.x;
-            dst[static_cast<size_t>(4 * n4 + 1) * L + t0 + t] = s.y;
-            dst[static_cast<size_t>(4 * n4 + 2) * L + t0 + t] = s.z;
-            dst[static_cast<size_t>(4 * n4 + 3) * L + t0 + t] = s.w;
-        }
+        if (sl == 0 && t < tl) red_add4(dst + bc_base + 4 * n4 * a.sbn + (t0 + t) * a.sbt, a.sbn, s);
       }
     };
 
-    // pass 1: checkpoints h_{t0 - 1} of every chunk
+    // forward over chunks [c0, c1) from h, storing h at the start of chunk ch in
+    // dst + (ch - c0) * every N when (ch - c0) % every == 0, dst rows [row][.][N]
     float h[kBS];
-#pragma unroll
-    for (int i = 0; i < kBS; ++i) h[i] = (active && a.h0) ? a.h0[row * N + kBS * gi + i] : 0.f;
-    for (int ch = 0; ch < nch; ++ch) {
+    auto forward = [&](int c0, int c1, float* dst, int per_row, int every) {
+      for (int ch = c0; ch < c1; ++ch) {
         const int t0 = ch * kBT, tl = min(kBT, L - t0);
-        if (active)
-            *reinterpret_cast<float4*>(ckpt + (row * nch + ch) * N + kBS * gi) = make_float4(h[0], h[1], h[2], h[3]);
+        if (active && (ch - c0) % every == 0)
+            *reinterpret_cast<float4*>(dst + (row * per_row + (ch - c0) / every) * N + kBS * gi) =
+                make_float4(h[0], h[1], h[2], h[3]);
         __syncthreads();
         stage(t0, tl, false);
         __syncthreads();
@@ -248,9 +281,14 @@ __global__ void __launch_bounds__(kBThreads, 4)
             h23 = fma2(make_float2(ex2_approx(e23.x), ex2_approx(e23.y)), h23, mul2(dx2, b23));
             h[0] = h01.x; h[1] = h01.y; h[2] = h23.x; h[3] = h23.y;
         }
-    }
+      }
+    };
+    // pass 1: coarse checkpoints, h at the start of every block
+#pragma unroll
+    for (int i = 0; i < kBS; ++i) h[i] = (active && a.h0) ? a.h0[row * N + kBS * gi + i] : 0.f;
+    forward(0, nch, ckpt, nblk, kb);
 
-    // pass 2: chunks last to first
+    // pass 2: blocks last to first, and in each the chunks last to first
     float gcar[kBS], dAacc[kBS];
 #pragma unroll
     for (int i = 0; i < kBS; ++i) {
@@ -258,16 +296,26 @@ __global__ void __launch_bounds__(kBThreads, 4)
         dAacc[i] = 0.f;
     }
     float dDacc = 0.f, dbacc = 0.f;
-    float* pbc = part_bc + (static_cast<size_t>(pair) * cps + part_i) * 2 * N * static_cast<size_t>(L);
-    for (int ch = nch - 1; ch >= 0; --ch) {
+    for (int blk = nblk - 1; blk >= 0; --blk) {
+      const int cb0 = blk * kb, cb1 = min(nch, cb0 + kb);
+      {  // fine checkpoints of the block, from its coarse one
+          const float4 v = active ? *reinterpret_cast<const float4*>(ckpt + (row * nblk + blk) * N + kBS * gi)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+          h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+      }
+      if (kb > 1) forward(cb0, cb1, fine, kb, 1);  // one chunk: its coarse checkpoint is h
+      for (int ch = cb1 - 1; ch >= cb0; --ch) {
         const int t0 = ch * kBT, tl = min(kBT, L - t0);
         __syncthreads();  // the previous chunk's tiles are no longer read
         stage(t0, tl, true);
         float hs[kBS];
-        {
-            const float4 v = active ? *reinterpret_cast<const float4*>(ckpt + (row * nch + ch) * N + kBS * gi)
+        if (kb > 1) {  // written by this thread in forward(): program order suffices
+            const float4 v = active ? *reinterpret_cast<const float4*>(fine + (row * kb + (ch - cb0)) * N + kBS * gi)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
             hs[0] = v.x; hs[1] = v.y; hs[2] = v.z; hs[3] = v.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kBS; ++i) hs[i] = h[i];
         }
         __syncthreads();
         // recompute h_t over the chunk, and the pre-gate output
@@ -292,7 +340,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
         __syncthreads();
         // dC_t[n] = sum over the CTA's channels of do_t h_t[n]; dz from the pre-gate output
-        channel_sum(lay.dout, pbc + static_cast<size_t>(N) * L, t0, tl);
+        channel_sum(lay.dout, a.dC, t0, tl);
         if (a.dz) {
             for (int j = tid; j < CPB * kBT; j += kBThreads) {
                 const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
@@ -358,18 +406,19 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
         __syncthreads();
         // dB_t[n] = sum over the CTA's channels of G_t[n] Delta_t x_t
-        channel_sum(lay.dlx, pbc, t0, tl);
+        channel_sum(lay.dlx, a.dB, t0, tl);
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
             const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
             if (cc >= nchan || t >= tl) continue;
             a.dx[xi(cc, t0 + t)] = sm[lay.gx + cc * kRow + t];
-            // one channel per head: the gradient of delta directly; else per channel,
-            // summed over the head by the second launch
+            // one channel per head: the gradient of delta directly; else the channel's
+            // share added into the head's (zeroed before the launch)
             if (a.hp == 1)
                 a.ddelta[di(cc, t0 + t)] = sm[lay.gd + cc * kRow + t];
             else
-                dd_chan[(static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t] = sm[lay.gd + cc * kRow + t];
+                atomicAdd(a.ddelta + di(cc, t0 + t), sm[lay.gd + cc * kRow + t]);
         }
+      }
     }
     if (active) {
         if (a.dh0)
@@ -382,32 +431,17 @@ __global__ void __launch_bounds__(kBThreads, 4)
     }
 }
 
-// dB, dC: sum of the per-CTA partials of each (batch, group), written in the caller's
-// layout; dA, dD, dbias: sums over the batch (and over a head's channels and, for A,
-// states when hp > 1); the gradient of the shared delta (hp > 1): sum over a head's
-// channels.  One thread per output element, fixed summation order.
-__global__ void m1_scan_bwd_reduce(BwdView a, int cps, const float* part_bc, const float* part_a,
-                                   const float* part_d, const float* part_bias, const float* dd_chan) {
-    const int L = a.seqlen, Dm = a.dim, G = a.ngroups, N = a.dstate, Bt = a.batch, hp = a.hp;
+// dA, dD, dbias: sums over the batch (and over a head's channels and, for A, states when
+// hp > 1).  One thread per output element, fixed summation order.
+__global__ void m1_scan_bwd_reduce(BwdView a, const float* part_a, const float* part_d, const float* part_bias) {
+    const int Dm = a.dim, N = a.dstate, Bt = a.batch, hp = a.hp;
     const int heads = Dm / hp;
-    const size_t nbc = static_cast<size_t>(Bt) * G * N * L;
     const size_t na = a.san ? static_cast<size_t>(Dm) * N : static_cast<size_t>(heads);
-    const size_t ndt = hp > 1 ? static_cast<size_t>(Bt) * heads * L : 0;
-    const size_t total = 2 * nbc + na + 2 * static_cast<size_t>(heads) + ndt;
+    const size_t total = na + 2 * static_cast<size_t>(heads);
     for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-        if (i < 2 * nbc) {
-            const int which = i < nbc ? 0 : 1;  // 0: dB, 1: dC
-            const size_t e = i % nbc;           // (pair, n, t)
-            const size_t pair = e / (static_cast<size_t>(N) * L), nt = e % (static_cast<size_t>(N) * L);
-            float sum = 0.f;
-            for (int p = 0; p < cps; ++p)
-                sum += part_bc[((pair * cps + p) * 2 + which) * N * static_cast<size_t>(L) + nt];
-            const long long bb = static_cast<long long>(pair / G), gg = static_cast<long long>(pair % G);
-            const long long n = static_cast<long long>(nt / L), t = static_cast<long long>(nt % L);
-            (which ? a.dC : a.dB)[bb * a.sbb + gg * a.sbg + n * a.sbn + t * a.sbt] = sum;
-        } else if (i < 2 * nbc + na) {
-            const size_t e = i - 2 * nbc;  // (d, n), or the head
+        if (i < na) {
+            const size_t e = i;  // (d, n), or the head
             float sum = 0.f;
             if (a.san) {
                 for (int bb = 0; bb < Bt; ++bb) sum += part_a[static_cast<size_t>(bb) * Dm * N + e];
@@ -417,8 +451,8 @@ __global__ void m1_scan_bwd_reduce(BwdView a, int cps, const float* part_bc, con
                         sum += part_a[(static_cast<size_t>(bb) * Dm + e * hp) * N + q];
             }
             a.dA[e] = sum;
-        } else if (i < 2 * nbc + na + 2 * static_cast<size_t>(heads)) {
-            const size_t e = i - 2 * nbc - na;
+        } else {
+            const size_t e = i - na;
             const int hh = static_cast<int>(e % heads);
             const float* src = e < static_cast<size_t>(heads) ? part_d : part_bias;
             float* dst = e < static_cast<size_t>(heads) ? a.dD : a.dbias;
@@ -427,14 +461,6 @@ __global__ void m1_scan_bwd_reduce(BwdView a, int cps, const float* part_bc, con
             for (int bb = 0; bb < Bt; ++bb)
                 for (int q = 0; q < hp; ++q) sum += src[static_cast<size_t>(bb) * Dm + hh * hp + q];
             dst[hh] = sum;
-        } else {
-            const size_t e = i - 2 * nbc - na - 2 * static_cast<size_t>(heads);  // (b, head, t)
-            const int bb = static_cast<int>(e / (static_cast<size_t>(heads) * L));
-            const int hh = static_cast<int>((e / L) % heads), t = static_cast<int>(e % L);
-            float sum = 0.f;
-            for (int q = 0; q < hp; ++q)
-                sum += dd_chan[(static_cast<size_t>(bb) * Dm + hh * hp + q) * L + t];
-            a.ddelta[bb * a.sdb + hh * a.sdh + static_cast<long long>(t) * a.sdt] = sum;
         }
     }
 }
@@ -451,19 +477,24 @@ int bwd_tpc(int n) {
     }
 }
 
-BwdWs bwd_ws(const BwdView& a, int cps) {
+int bwd_kb(const BwdView& a) {
+    const int nch = (a.seqlen + kBT - 1) / kBT;
+    return bwd_block_chunks(nch, a.dstate, a.seqlen, a.in_dtype == SSM_BF16 ? 2 : 4, a.dy_dtype == SSM_BF16 ? 2 : 4);
+}
+
+BwdWs bwd_ws(const BwdView& a) {
     const size_t rows = static_cast<size_t>(a.batch) * a.dim;
-    const size_t nch = (static_cast<size_t>(a.seqlen) + kBT - 1) / kBT;
-    const size_t pairs = static_cast<size_t>(a.batch) * a.ngroups;
+    const int nch = (a.seqlen + kBT - 1) / kBT;
+    const int kb = bwd_kb(a);
+    const size_t nblk = (static_cast<size_t>(nch) + kb - 1) / kb;
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
     BwdWs w;
     w.ckpt = 0;
-    w.part_bc = r256(rows * nch * a.dstate * 4);
-    w.part_a = w.part_bc + r256(pairs * cps * 2 * a.dstate * static_cast<size_t>(a.seqlen) * 4);
+    w.fine = r256(rows * nblk * a.dstate * 4);
+    w.part_a = w.fine + (kb > 1 ? r256(rows * static_cast<size_t>(kb) * a.dstate * 4) : 0);
     w.part_d = w.part_a + r256(rows * a.dstate * 4);
     w.part_bias = w.part_d + r256(rows * 4);
-    w.dd_chan = w.part_bias + r256(rows * 4);
-    w.bytes = w.dd_chan + (a.hp > 1 ? r256(rows * static_cast<size_t>(a.seqlen) * 4) : 0);
+    w.bytes = w.part_bias + r256(rows * 4);
     return w;
 }
 
@@ -476,25 +507,32 @@ int bwd_cps(const BwdView& a) {
 template <typename Tin, typename Tdy, int TPC>
 cudaError_t launch_bwd(const BwdView& a, void* ws, cudaStream_t s) {
     const int cps = bwd_cps(a);
-    const BwdWs w = bwd_ws(a, cps);
+    const BwdWs w = bwd_ws(a);
     unsigned char* base = static_cast<unsigned char*>(ws);
     const BwdLayout lay(bwd_cpb(TPC), TPC * kBS);
     const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
     auto k = m1_scan_bwd<Tin, Tdy, TPC>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    // the atomic sums start from zero: dB, dC (dense in either layout) and, with shared
+    // delta, the head's gradient
+    const size_t nbc = static_cast<size_t>(a.batch) * a.ngroups * a.dstate * a.seqlen;
+    if ((e = cudaMemsetAsync(a.dB, 0, nbc * sizeof(float), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.dC, 0, nbc * sizeof(float), s)) != cudaSuccess) return e;
+    if (a.hp > 1) {
+        const size_t ndt = static_cast<size_t>(a.batch) * (a.dim / a.hp) * a.seqlen;
+        if ((e = cudaMemsetAsync(a.ddelta, 0, ndt * sizeof(float), s)) != cudaSuccess) return e;
+    }
     const int grid = a.batch * a.ngroups * cps;
-    float* part_bc = reinterpret_cast<float*>(base + w.part_bc);
     float* part_a = reinterpret_cast<float*>(base + w.part_a);
     float* part_d = reinterpret_cast<float*>(base + w.part_d);
     float* part_bias = reinterpret_cast<float*>(base + w.part_bias);
-    float* dd_chan = reinterpret_cast<float*>(base + w.dd_chan);
     if (grid > 0)
-        k<<<grid, kBThreads, smem, s>>>(a, cps, reinterpret_cast<float*>(base + w.ckpt), part_bc, part_a,
-                                        part_d, part_bias, dd_chan);
+        k<<<grid, kBThreads, smem, s>>>(a, cps, bwd_kb(a), reinterpret_cast<float*>(base + w.ckpt),
+                                        reinterpret_cast<float*>(base + w.fine), part_a, part_d, part_bias);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    m1_scan_bwd_reduce<<<2 * 152, 256, 0, s>>>(a, cps, part_bc, part_a, part_d, part_bias, dd_chan);
+    m1_scan_bwd_reduce<<<2 * 152, 256, 0, s>>>(a, part_a, part_d, part_bias);
     return cudaGetLastError();
 }
 
@@ -564,8 +602,7 @@ bool m1_bwd_supported(const M1BwdArgs& a) {
 
 size_t m1_bwd_workspace_size(const M1BwdArgs& a) {
     if (!m1_bwd_supported(a)) return 0;
-    const BwdView v = view_m1(a);
-    return bwd_ws(v, bwd_cps(v)).bytes;
+    return bwd_ws(view_m1(a)).bytes;
 }
 
 cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s) {
@@ -578,8 +615,7 @@ bool ssd_bwd_supported(const ssd_bwd_params& a) {
 
 size_t ssd_bwd_workspace_size(const ssd_bwd_params& a) {
     if (!ssd_bwd_supported(a)) return 0;
-    const BwdView v = view_ssd(a);
-    return bwd_ws(v, bwd_cps(v)).bytes;
+    return bwd_ws(view_ssd(a)).bytes;
 }
 
 cudaError_t ssd_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_t s) {

@@ -428,11 +428,26 @@ def test_scan_bwd_rejects_bad_arguments(lib, kw, status):
     assert lib.ssm_last_error()
 
 
+def bwd_workspace_bytes(rows, N, L, in_bytes=2, dy_bytes=2):
+    """The backward's scratch: coarse checkpoints (one per block of K 16-step chunks:
+    K = 1 while N floats per chunk fit in the bytes of x and dy per 16 steps, else
+    ceil(sqrt(chunks))), one block's fine checkpoints when K > 1, per-row dA, dD, dbias
+    sums; each part rounded up to 256 bytes."""
+    r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    nch = -(-L // 16)
+    kb = 1
+    if nch * N * 4 > L * (in_bytes + dy_bytes):
+        while kb * kb < nch:
+            kb += 1
+    nblk = -(-nch // kb)
+    fine = r256(rows * kb * N * 4) if kb > 1 else 0
+    return r256(rows * nblk * N * 4) + fine + r256(rows * N * 4) + 2 * r256(rows * 4)
+
+
 def test_scan_bwd_workspace_size_and_shortfall(lib):
     p = scan_bwd_params()
     need = lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
-    # checkpoints every 32 steps, per-CTA dB/dC partials, per-row dA, dD, dbias partials
-    assert need >= 2 * 32 * (64 // 32) * 16 * 4 + 2 * 32 * 16 * 4
+    assert need == bwd_workspace_bytes(2 * 32, 16, 64)
     assert lib.ssm_scan_bwd(ctypes.byref(p), fake(30), need - 1, None) == _lib.SSM_ERR_INVALID_ARG
     assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(scan_bwd_params(fwd_dstate=8))) == 0
     assert lib.ssm_scan_bwd_workspace_size(None) == 0
@@ -516,6 +531,28 @@ def test_ssd_bwd_rejects_bad_arguments(lib, kw, status):
 def test_ssd_bwd_workspace_size(lib):
     p = ssd_bwd_params()
     need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
-    # includes the per-channel d(dt) buffer: batch * H * P * L floats
-    assert need >= 2 * 4 * 64 * 64 * 4
+    assert need == bwd_workspace_bytes(2 * 4 * 64, 128, 64)
     assert lib.ssd_scan_bwd(ctypes.byref(p), fake(30), need - 1, None) == _lib.SSM_ERR_INVALID_ARG
+
+
+def test_backward_workspace_at_most_the_inputs(lib):
+    """At the benchmark shapes the backward's scratch is no larger than its inputs
+    (x, delta, B, C, dy, z where present)."""
+    # SSD 130m: batch 4, L 4096, 24 heads x 64, dstate 128, bf16, no z
+    p = ssd_bwd_params(fwd_batch=4, fwd_seqlen=4096, fwd_nheads=24, fwd_headdim=64)
+    L, HP, N = 4096, 24 * 64, 128
+    inputs = 4 * L * HP * 2 * 2 + 4 * L * 24 * 2 + 2 * 4 * L * N * 2
+    need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
+    assert 0 < need <= inputs
+    # Mamba-1 130m layer: batch 8, d_inner 1536, dstate 16, L 2048, bf16, z
+    p = scan_bwd_params(fwd_batch=8, fwd_dim=1536, fwd_seqlen=2048, fwd_z=fake(20), dz=fake(21))
+    inputs = 4 * 8 * 1536 * 2048 * 2 + 2 * 8 * 16 * 2048 * 2
+    need = lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
+    assert 0 < need <= inputs
+    # Mamba-1 790m, one row of 32768 steps
+    p = scan_bwd_params(fwd_batch=1, fwd_dim=3072, fwd_seqlen=32768)
+    inputs = 3 * 3072 * 32768 * 2 + 2 * 16 * 32768 * 2
+    need = lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
+    assert 0 < need <= inputs
+
+

@@ -86,3 +86,10 @@ def test_130m_layer_shape(oracle_mod):
     """The 130m layer's channel count and dstate on a shorter sequence (256 steps), the
     full backward compared element by element."""
     _run(oracle_mod, 1, 1536, 16, 256, 1, synth.BF16, seed=3)
+
+
+@pytest.mark.parametrize("N", [16, 32])
+def test_long_sequence_checkpoint_blocks(oracle_mod, N):
+    """1500 steps, 94 chunks: with N = 16 a checkpoint per chunk; with N = 32 blocks of
+    10 chunks (the last one short) rerun forwards from their checkpoints."""
+    _run(oracle_mod, 2, 40, N, 1500, 1, synth.BF16, seed=5)

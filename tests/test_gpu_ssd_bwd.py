@@ -57,3 +57,9 @@ def test_fp32_no_gate(oracle_mod):
 def test_130m_heads_short_sequence(oracle_mod):
     """The 130m SSD's 24 heads x 64 and dstate 128 on 192 steps, every gradient compared."""
     _run(oracle_mod, 1, 192, 24, 64, 128, 1, synth.BF16, seed=2)
+
+
+def test_long_sequence_checkpoint_blocks(oracle_mod):
+    """1000 steps: 63 chunks in 8 checkpoint blocks of 8, the last one short; dstate 128
+    with two heads sharing one group."""
+    _run(oracle_mod, 1, 1000, 2, 16, 128, 1, synth.BF16, seed=4)
