@@ -309,7 +309,7 @@ ssm_status ssm_s4d_kernel(const ssm_s4d_params* p, float* K, int kernel_len, voi
  * dim, dstate, seqlen, dtypes, u, log_dt, A, B, C, D_skip and y of `p`; h0 and h_final
  * must be NULL (use ssm_s4d_scan_fwd for a carried state).
  * `workspace`: ssm_s4d_conv_workspace_size(p) bytes, 16-byte aligned, contents on entry
- * irrelevant (the kernel K [dim, L] and its spectrum [dim, N] complex).
+ * irrelevant (the spectrum of K, [dim, N] complex, and the transform's twiddle tables).
  * Limits: 1 <= L <= 8192 for the workspace query (N <= 16384 fits in shared memory; L = 0
  * is accepted by the call and does nothing), dim <= 65535, dstate as ssm_s4d_scan_fwd. */
 size_t ssm_s4d_conv_workspace_size(const ssm_s4d_params* p);
