@@ -69,6 +69,9 @@ struct M1Plan {
     int cps = 0;  // CTAs per (batch, group) (TMEM-broadcast path)
     int segs = 1;         // time segments (TMEM-broadcast path)
     int tps = 0;          // tiles per segment
+    int cps_st = 0;       // CTAs per (batch, group) of the segment pass
+    int cpb_st = 0;       // channels per CTA of the segment pass
+    size_t smem_st = 0;   // dynamic shared memory per CTA of the segment pass
     size_t ws_state = 0;  // workspace offset of the segment sums of Delta
     size_t ws_bytes = 0;  // workspace bytes
 };

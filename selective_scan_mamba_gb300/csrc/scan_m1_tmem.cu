@@ -472,18 +472,23 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     int cpb = (per_group + cps - 1) / cps;
     // Long sequences with few channels per SM: split the sequence into segments so that
     // every CTA holds a full channel group (more warps per SM), at the cost of a segment
-    // pass over all but the last segment.
+    // pass over all but the last segment.  Each launch then spreads its (segment, channel
+    // block) units over as many SMs as it can: the main pass over S segments, the segment
+    // pass over S - 1, each with channel blocks sized to fill the SMs.
     const int ntiles = (a.seqlen + kT - 1) / kT;
-    int segs = 1;
+    int segs = 1, cps_st = 0;
     if (cpb < 48 && ntiles >= 16 && a.max_segments != 1) {
         const int cps_full = (per_group + kMaxThreads / kTPC - 1) / (kMaxThreads / kTPC);
         int S = sms / (pairs * cps_full);
         if (S > ntiles / 4) S = ntiles / 4;  // at least 4 tiles per segment
         if (a.max_segments > 1 && S > a.max_segments) S = a.max_segments;
         if (S >= 2) {
-            cps = cps_full;
+            cps = sms / (pairs * S);  // >= cps_full
+            if (cps > per_group) cps = per_group;
             cpb = (per_group + cps - 1) / cps;
             segs = S;
+            cps_st = sms / (pairs * (S - 1));
+            if (cps_st > per_group) cps_st = per_group;
         }
     }
     const int tps = (ntiles + segs - 1) / segs;
@@ -501,6 +506,12 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     plan->cps = cps;
     plan->segs = segs;
     plan->tps = tps;
+    if (segs > 1) {
+        plan->cps_st = cps_st;
+        plan->cpb_st = (per_group + cps_st - 1) / cps_st;
+        plan->smem_st = static_cast<size_t>(Layout(plan->cpb_st).total) + 1024;
+        if (plan->smem_st < one_per_sm) plan->smem_st = one_per_sm;
+    }
     // segment end states [segs-1][batch*dim][16] and sums of Delta [segs-1][batch*dim]
     const size_t rows = static_cast<size_t>(a.batch) * a.dim;
     plan->ws_state = (static_cast<size_t>(segs - 1) * rows * kN * sizeof(float) + 255) / 256 * 256;
@@ -508,37 +519,46 @@ cudaError_t m1_tmem_plan(const M1Args& a, M1Plan* plan) {
     return cudaSuccess;
 }
 
-cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspace, cudaStream_t s) {
-    M1Args a = a_in;
-    a.cpb_max = plan.cpb_max;
-    const Layout lay(plan.cpb_max);
+// tensor maps of one launch: box rows = the staged rows of its channel blocks
+static cudaError_t encode_maps(const M1Args& a, int cpb, TmaMaps* maps) {
+    const Layout lay(cpb);
     const unsigned long long rows = static_cast<unsigned long long>(a.batch) * a.dim;
     const unsigned long long bcrows = static_cast<unsigned long long>(a.batch) * a.ngroups * kN;
-    TmaMaps maps;
     cudaError_t e;
-    if ((e = encode_tmap_2d(&maps.x, a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
-    if ((e = encode_tmap_2d(&maps.dl, a.delta, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
-    if ((e = encode_tmap_2d(&maps.z, a.z ? a.z : a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess)
+    if ((e = encode_tmap_2d(&maps->x, a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
+    if ((e = encode_tmap_2d(&maps->dl, a.delta, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess) return e;
+    if ((e = encode_tmap_2d(&maps->z, a.z ? a.z : a.x, 2, a.seqlen, rows, kT, lay.cb, true)) != cudaSuccess)
         return e;
-    if ((e = encode_tmap_2d(&maps.b, a.B, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
-    if ((e = encode_tmap_2d(&maps.c, a.C, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
-    const int threads = round_up(plan.cpb_max * kTPC, 32);
+    if ((e = encode_tmap_2d(&maps->b, a.B, 2, a.seqlen, bcrows, kT, kN, true)) != cudaSuccess) return e;
+    return encode_tmap_2d(&maps->c, a.C, 2, a.seqlen, bcrows, kT, kN, true);
+}
+
+cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspace, cudaStream_t s) {
     float* seg_state = static_cast<float*>(workspace);
     float* seg_dsum = plan.segs > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.ws_state)
                                     : nullptr;
-    const int ctas = plan.grid / plan.segs;  // CTAs per segment
-    auto run = [&](auto kern, int grid) -> cudaError_t {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(plan.smem));
+    // one launch: cpb channels per CTA, cps CTAs per (batch, group) and segment
+    auto run = [&](auto kern, int cpb, int cps, size_t smem, int grid) -> cudaError_t {
+        M1Args a = a_in;
+        a.cpb_max = cpb;
+        TmaMaps maps;
+        cudaError_t err = encode_maps(a, cpb, &maps);
         if (err != cudaSuccess) return err;
-        kern<<<grid, threads, plan.smem, s>>>(maps, a, plan.cps, plan.segs, plan.tps, seg_state, seg_dsum);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        kern<<<grid, round_up(cpb * kTPC, 32), smem, s>>>(maps, a, cps, plan.segs, plan.tps, seg_state, seg_dsum);
         return cudaGetLastError();
     };
+    const int pairs = a_in.batch * a_in.ngroups;
+    cudaError_t e;
     if (plan.segs > 1) {  // segment pass (outputs unused: instantiated for bf16 only)
-        if ((e = run(m1_scan_tmem<bf16_t, true>, ctas * (plan.segs - 1))) != cudaSuccess) return e;
+        if ((e = run(m1_scan_tmem<bf16_t, true>, plan.cpb_st, plan.cps_st, plan.smem_st,
+                     pairs * plan.cps_st * (plan.segs - 1))) != cudaSuccess)
+            return e;
     }
-    return a.out_dtype == SSM_BF16 ? run(m1_scan_tmem<bf16_t, false>, plan.grid)
-                                   : run(m1_scan_tmem<float, false>, plan.grid);
+    return a_in.out_dtype == SSM_BF16
+               ? run(m1_scan_tmem<bf16_t, false>, plan.cpb_max, plan.cps, plan.smem, plan.grid)
+               : run(m1_scan_tmem<float, false>, plan.cpb_max, plan.cps, plan.smem, plan.grid);
 }
 
 cudaError_t m1_tmem_take_wait_timeouts(unsigned int* count) {
