@@ -242,3 +242,9 @@ def test_mixed_stack_cuda_graph_serving_loop(oracle_mod):
                                                       dt_bias=fp("dt_bias"))
                 check(to_numpy(lay["ys"][k]), yr, TOL_BF16, what=f"replay {rep} layer {li} token {k}")
             check(to_numpy(lay["state"]), ref[li], TOL_BF16, what=f"replay {rep} layer {li} state")
+
+
+def test_mamba1_form_bf16_zoh_ragged(oracle_mod):
+    """Mamba-1 decode in bf16 with ZOH and dstate 32; 3 x 37 rows do not fill the last
+    warp's row slots."""
+    _steps(oracle_mod, 3, 37, 1, 32, 1, 4, synth.BF16, a_per_state=True, disc="zoh")
