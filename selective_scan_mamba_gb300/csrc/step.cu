@@ -56,26 +56,6 @@ __global__ void __launch_bounds__(kStepThreads) step_vec1(StepArgs a, int rows_p
     int* s_h = s_bc + nbh;                          // head index
     const int per_group = a.nheads / a.ngroups;
     const Tin* DT = static_cast<const Tin*>(a.dt);
-    const int lane = threadIdx.x & 31;
-    const int sub = lane / LPR, li = lane % LPR;
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    // the first pass's state rows are requested before the prologue, so that the two
-    // round trips to memory (the per-head table, the rows) overlap
-    float4 hv[UNROLL][NV];
-    long long rr[UNROLL];
-    const long long base0 = r0 + static_cast<long long>(warp) * RPW * UNROLL;
-    auto load_rows = [&](long long base) {
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            rr[u] = base + u * RPW + sub;
-            if (rr[u] < r1) {
-                const float4* sp = reinterpret_cast<const float4*>(a.state + rr[u] * N);
-#pragma unroll
-                for (int v = 0; v < NV; ++v) hv[u][v] = __ldcs(sp + li + v * LPR);
-            }
-        }
-    };
-    load_rows(base0);
     for (int i = threadIdx.x; i < nbh; i += blockDim.x) {
         const long long bh = bh0 + i;
         const int hd = static_cast<int>(bh % a.nheads);
@@ -94,13 +74,27 @@ __global__ void __launch_bounds__(kStepThreads) step_vec1(StepArgs a, int rows_p
     }
     __syncthreads();
 
+    const int lane = threadIdx.x & 31;
+    const int sub = lane / LPR, li = lane % LPR;
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const Tin* X = static_cast<const Tin*>(a.x);
     const Tin* Z = static_cast<const Tin*>(a.z);
     const Tin* Bp = static_cast<const Tin*>(a.B);
     const Tin* Cp = static_cast<const Tin*>(a.C);
 
-    for (long long base = base0; base < r1; base += static_cast<long long>(nwarps) * RPW * UNROLL) {
-        if (base != base0) load_rows(base);
+    for (long long base = r0 + static_cast<long long>(warp) * RPW * UNROLL; base < r1;
+         base += static_cast<long long>(nwarps) * RPW * UNROLL) {
+        float4 hv[UNROLL][NV];
+        long long rr[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            rr[u] = base + u * RPW + sub;
+            if (rr[u] < r1) {
+                const float4* sp = reinterpret_cast<const float4*>(a.state + rr[u] * N);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) hv[u][v] = __ldcs(sp + li + v * LPR);
+            }
+        }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const long long r = rr[u] < r1 ? rr[u] : r1 - 1;
@@ -118,8 +112,7 @@ __global__ void __launch_bounds__(kStepThreads) step_vec1(StepArgs a, int rows_p
                 float2 da01, da23;
                 float wdx01, wdx23, wdx2, wdx3;
                 if (PER_STATE) {
-                    const float4 A4 = __ldg(reinterpret_cast<const float4*>(a.A + static_cast<size_t>(s_h[i]) * N + n0));
-                    const float Ah[4] = {A4.x, A4.y, A4.z, A4.w};
+                    const float* Ah = a.A + static_cast<size_t>(s_h[i]) * N + n0;
                     float ww[4], dd[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -597,11 +590,8 @@ __global__ void __launch_bounds__(128) step_scalar(StepArgs a) {
 
 template <typename Tin, typename Tout, int NV, int LPR, int UNROLL>
 static cudaError_t launch_vec(const StepArgs& a, long long rows, cudaStream_t s) {
-    // rows per CTA: enough for every warp to run two passes of UNROLL rows; one pass for
-    // the Mamba-1 form's short rows (its whole grid is then resident at once, and every
-    // state load goes out before the per-head prologue)
-    const int passes = (a.ntok == 1 && a.a_per_state) ? 1 : 2;
-    const int rows_per_cta = (kStepThreads / 32) * (32 / LPR) * UNROLL * passes;
+    // rows per CTA: enough for every warp to run two passes of UNROLL rows
+    const int rows_per_cta = (kStepThreads / 32) * (32 / LPR) * UNROLL * 2;
     const long long grid = (rows + rows_per_cta - 1) / rows_per_cta;
     int log2p = -1;
     if ((a.headdim & (a.headdim - 1)) == 0) {
