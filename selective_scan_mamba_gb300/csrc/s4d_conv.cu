@@ -34,6 +34,8 @@
 // N is at most 16384 (L <= 8192).
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -143,6 +145,34 @@ __device__ void make_twiddles(float2* W, int m) {
     }
 }
 
+// point loaders and storers of a pass.  Those of the shared sequence X also take a
+// padded address directly (put / the X member), so that a pass can address its points
+// as one padded base plus constant strides.
+struct LoadX {
+    const float2* X;
+    __device__ __forceinline__ float2 operator()(int t) const { return X[pad(t)]; }
+};
+struct StoreX {
+    float2* X;
+    __device__ __forceinline__ void operator()(int t, float2 v) const { X[pad(t)] = v; }
+    __device__ __forceinline__ void put(float2* p, int, float2 v) const { *p = v; }
+};
+// Y = X Khat (Khat holds 1/N), stored conjugated for the inverse
+struct StoreTimesKhat {
+    float2* X;
+    const float2* kh;
+    __device__ __forceinline__ void operator()(int t, float2 v) const { put(X + pad(t), t, v); }
+    __device__ __forceinline__ void put(float2* p, int t, float2 v) const {
+        const float2 y = cmul(v, __ldg(kh + t));
+        *p = make_float2(y.x, -y.y);
+    }
+};
+template <class F> struct padded_load : std::false_type {};
+template <> struct padded_load<LoadX> : std::true_type {};
+template <class F> struct padded_store : std::false_type {};
+template <> struct padded_store<StoreX> : std::true_type {};
+template <> struct padded_store<StoreTimesKhat> : std::true_type {};
+
 // One Stockham pass of radix 2^LR over N = 2^m points, Ns = 2^ns_log2 (the product of
 // the radices before it), at most BPT butterflies per thread.  load(t) gives point t of
 // the pass input, store(t, v) takes point t of its output; with SYNC the block syncs
@@ -158,8 +188,22 @@ __device__ __forceinline__ void fft_pass(const float2* tw, int m, int ns_log2, L
     for (int q = 0; q < BPT; ++q) {
         const int j = threadIdx.x + q * blockDim.x;
         if (j < nb) {
+            bool done = false;
+            if constexpr (padded_load<Load>::value) {
+                if (nb % 16 == 0) {  // pad(j + r nb) = pad(j) + r (nb + nb / 16)
+                    const float2* xb = load.X + pad(j);
+                    const int pnb = nb + (nb >> 4);
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[q][r] = HALF_IN && r >= R / 2 ? make_float2(0.f, 0.f) : load(j + r * nb);
+                    for (int r = 0; r < R; ++r)
+                        v[q][r] = HALF_IN && r >= R / 2 ? make_float2(0.f, 0.f) : xb[r * pnb];
+                    done = true;
+                }
+            }
+            if (!done) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    v[q][r] = HALF_IN && r >= R / 2 ? make_float2(0.f, 0.f) : load(j + r * nb);
+            }
         }
     }
     if (SYNC) __syncthreads();
@@ -179,8 +223,22 @@ __device__ __forceinline__ void fft_pass(const float2* tw, int m, int ns_log2, L
             }
             dft_reg<R>(v[q]);
             const int base = ((j - k) << LR) + k;  // (j / Ns) Ns R + k
+            bool done = false;
+            if constexpr (padded_store<Store>::value) {
+                if (Ns % 16 == 0 || (Ns == 1 && R == 16)) {
+                    // pad(base + r Ns) = pad(base) + r (Ns + Ns / 16) when 16 divides Ns, and
+                    // pad(base) + r when Ns = 1 (base = 16 j)
+                    float2* xb = store.X + pad(base);
+                    const int pns = Ns == 1 ? 1 : Ns + (Ns >> 4);
 #pragma unroll
-            for (int r = 0; r < (HALF_OUT ? R / 2 : R); ++r) store(base + r * Ns, v[q][r]);
+                    for (int r = 0; r < (HALF_OUT ? R / 2 : R); ++r) store.put(xb + r * pns, base + r * Ns, v[q][r]);
+                    done = true;
+                }
+            }
+            if (!done) {
+#pragma unroll
+                for (int r = 0; r < (HALF_OUT ? R / 2 : R); ++r) store(base + r * Ns, v[q][r]);
+            }
         }
     }
 }
@@ -198,15 +256,6 @@ __device__ __forceinline__ void fft_pass_any(const float2* W, int m, int p, Load
     }
 }
 
-// point loaders and storers of a pass
-struct LoadX {
-    const float2* X;
-    __device__ __forceinline__ float2 operator()(int t) const { return X[pad(t)]; }
-};
-struct StoreX {
-    float2* X;
-    __device__ __forceinline__ void operator()(int t, float2 v) const { X[pad(t)] = v; }
-};
 
 // Forward FFT of N = 2^m points whose second half is zero: the first pass takes its
 // input from first(t) (t < N / 2; FIRST_SYNC if that reads X) and stores into X; the
@@ -224,6 +273,7 @@ __device__ __forceinline__ void fft_forward(float2* X, const float2* W, int m, F
     // every pass but the last has radix 16
     fft_pass<4, 1, true, false, FIRST_SYNC>(W, m, 0, first, st);
     __syncthreads();
+#pragma unroll
     for (int p = 1; p + 1 < P; ++p) {
         fft_pass<4, 1, false, false, true>(W + twiddle_offset(p), m, 4 * p, ld, st);
         __syncthreads();
@@ -238,6 +288,7 @@ __device__ __forceinline__ void fft_half_out(float2* X, const float2* W, int m, 
     const LoadX ld{X};
     const StoreX st{X};
     const int P = n_passes(m);
+#pragma unroll
     for (int p = 0; p + 1 < P; ++p) {
         fft_pass<4, 1, false, false, true>(W + (p > 0 ? twiddle_offset(p) : 0), m, 4 * p, ld, st);
         __syncthreads();
@@ -309,7 +360,9 @@ __device__ __forceinline__ float2 pow_z(const StateWZ& s, unsigned int l) {
 // state's w and z once, then the power tables of kGroup states at a time (in the space of
 // X, which is filled only afterwards); each thread keeps the sums of its steps
 // l = tid + threads k in registers.  CTA 0 also stores the twiddle tables for s4d_conv.
-__global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float2* Khat, float2* Wg, int m) {
+template <int MT>
+__global__ void __launch_bounds__(kMaxThreads) s4d_kspec(ssm_s4d_params a, float2* Khat, float2* Wg, int m_arg) {
+    const int m = MT ? MT : m_arg;  // MT: the transform size known when compiled
     extern __shared__ float2 sm[];
     __shared__ StateWZ s_wz[kMaxStates];
     const int N = 1 << m, L = a.seqlen, Ns = a.dstate, nt = blockDim.x;
@@ -383,15 +436,6 @@ struct LoadRows {
         return make_float2(re, im);
     }
 };
-// Y = X Khat (Khat holds 1/N), stored conjugated for the inverse
-struct StoreTimesKhat {
-    float2* X;
-    const float2* kh;
-    __device__ __forceinline__ void operator()(int t, float2 v) const {
-        const float2 y = cmul(v, __ldg(kh + t));
-        X[pad(t)] = make_float2(y.x, -y.y);
-    }
-};
 // the conjugate of the inverse is y_b0 + i y_b1 with D u added; t < L only
 template <typename Tin, typename Tout>
 struct StoreRows {
@@ -410,9 +454,10 @@ struct StoreRows {
     }
 };
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, int MT>
 __global__ void __launch_bounds__(kMaxThreads) s4d_conv(ssm_s4d_params a, const float2* Khat, const float2* Wg,
-                                                       int m) {
+                                                       int m_arg) {
+    const int m = MT ? MT : m_arg;  // MT: the transform size known when compiled
     extern __shared__ float2 sm[];
     const int N = 1 << m;
     float2* X = sm;
@@ -446,14 +491,29 @@ size_t kspec_smem_bytes(int m, int L) {
     return static_cast<size_t>(kspec_x_len(m, L) + twiddle_len(m)) * sizeof(float2);
 }
 
+// the kernels of an N = 2^m transform: compiled for each m of 9 .. 14 (N / 16 threads,
+// every stride a constant), one runtime-m kernel for the short ones
+template <int MT, typename F>
+cudaError_t with_m(int m, F&& f) {
+    if constexpr (MT > kMaxLog2N) {
+        return f(std::integral_constant<int, 0>{});
+    } else {
+        if (m == MT) return f(std::integral_constant<int, MT>{});
+        return with_m<MT + 1>(m, f);
+    }
+}
+
 template <typename Tin, typename Tout>
 cudaError_t launch_conv(const ssm_s4d_params& a, const float2* Khat, const float2* Wg, int m, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(s4d_conv<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes(m)));
-    if (e != cudaSuccess) return e;
-    const dim3 grid((a.batch + 1) / 2, a.dim);
-    s4d_conv<Tin, Tout><<<grid, fft_threads(m), smem_bytes(m), s>>>(a, Khat, Wg, m);
-    return cudaGetLastError();
+    return with_m<9>(m, [&](auto mt) -> cudaError_t {
+        auto k = s4d_conv<Tin, Tout, decltype(mt)::value>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_bytes(m)));
+        if (e != cudaSuccess) return e;
+        const dim3 grid((a.batch + 1) / 2, a.dim);
+        k<<<grid, fft_threads(m), smem_bytes(m), s>>>(a, Khat, Wg, m);
+        return cudaGetLastError();
+    });
 }
 
 }  // namespace
@@ -474,10 +534,14 @@ cudaError_t s4d_conv_launch(const ssm_s4d_params& a, void* workspace, cudaStream
     float2* Khat = static_cast<float2*>(workspace);
     float2* Wg = Khat + static_cast<size_t>(a.dim) * (static_cast<size_t>(1) << m);
     const size_t ks = kspec_smem_bytes(m, a.seqlen);
-    cudaError_t e = cudaFuncSetAttribute(s4d_kspec, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ks));
+    cudaError_t e = with_m<9>(m, [&](auto mt) -> cudaError_t {
+        auto k = s4d_kspec<decltype(mt)::value>;
+        cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ks));
+        if (r != cudaSuccess) return r;
+        k<<<a.dim, fft_threads(m), ks, s>>>(a, Khat, Wg, m);
+        return cudaGetLastError();
+    });
     if (e != cudaSuccess) return e;
-    s4d_kspec<<<a.dim, fft_threads(m), ks, s>>>(a, Khat, Wg, m);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const bool ib = a.in_dtype == SSM_BF16, ob = a.out_dtype == SSM_BF16;
     if (ib && ob) return launch_conv<bf16_t, bf16_t>(a, Khat, Wg, m, s);
     if (ib) return launch_conv<bf16_t, float>(a, Khat, Wg, m, s);
