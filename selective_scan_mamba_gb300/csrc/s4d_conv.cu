@@ -507,8 +507,7 @@ template <typename Tin, typename Tout>
 cudaError_t launch_conv(const ssm_s4d_params& a, const float2* Khat, const float2* Wg, int m, cudaStream_t s) {
     return with_m<9>(m, [&](auto mt) -> cudaError_t {
         auto k = s4d_conv<Tin, Tout, decltype(mt)::value>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_bytes(m)));
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem_bytes(m)));
         if (e != cudaSuccess) return e;
         const dim3 grid((a.batch + 1) / 2, a.dim);
         k<<<grid, fft_threads(m), smem_bytes(m), s>>>(a, Khat, Wg, m);
@@ -536,7 +535,7 @@ cudaError_t s4d_conv_launch(const ssm_s4d_params& a, void* workspace, cudaStream
     const size_t ks = kspec_smem_bytes(m, a.seqlen);
     cudaError_t e = with_m<9>(m, [&](auto mt) -> cudaError_t {
         auto k = s4d_kspec<decltype(mt)::value>;
-        cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ks));
+        cudaError_t r = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(ks));
         if (r != cudaSuccess) return r;
         k<<<a.dim, fft_threads(m), ks, s>>>(a, Khat, Wg, m);
         return cudaGetLastError();

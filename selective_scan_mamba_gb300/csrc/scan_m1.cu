@@ -439,8 +439,7 @@ cudaError_t m1_plan(const M1Args& a, M1Plan* plan) {
         M1Args dummy = a;
         e = dispatch_tiled(dummy, tpc, [&](auto k) -> cudaError_t {
             using K = decltype(k);
-            cudaError_t r = cudaFuncSetAttribute(K::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
+            cudaError_t r = set_smem_attr(reinterpret_cast<const void*>(K::fn()), static_cast<int>(smem));
             if (r != cudaSuccess) return r;
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &resident, K::fn(), ((cpb * tpc + 31) / 32) * 32, smem);

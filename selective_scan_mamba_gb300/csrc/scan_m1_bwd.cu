@@ -512,7 +512,7 @@ cudaError_t launch_bwd(const BwdView& a, void* ws, cudaStream_t s) {
     const BwdLayout lay(bwd_cpb(TPC), TPC * kBS);
     const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
     auto k = m1_scan_bwd<Tin, Tdy, TPC>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // the atomic sums start from zero: dB, dC (dense in either layout) and, with shared
     // delta, the head's gradient

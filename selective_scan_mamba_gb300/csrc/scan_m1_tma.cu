@@ -356,9 +356,7 @@ cudaError_t m1_tma_plan(const M1Args& a, M1Plan* plan) {
         int resident = 0;
         const int threads = round_up(cpb * tpc, 32);
         e = dispatch(a.out_dtype, tpc, [&](auto k) -> cudaError_t {
-            cudaError_t r = cudaFuncSetAttribute(decltype(k)::fn(),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
+            cudaError_t r = set_smem_attr(reinterpret_cast<const void*>(decltype(k)::fn()), static_cast<int>(smem));
             if (r != cudaSuccess) return r;
             return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, decltype(k)::fn(),
                                                                  threads, smem);

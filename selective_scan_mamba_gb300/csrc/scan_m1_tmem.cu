@@ -544,7 +544,7 @@ cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspa
         TmaMaps maps;
         cudaError_t err = encode_maps(a, cpb, &maps);
         if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        err = set_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
         if (err != cudaSuccess) return err;
         kern<<<grid, round_up(cpb * kTPC, 32), smem, s>>>(maps, a, cps, plan.segs, plan.tps, seg_state, seg_dsum);
         return cudaGetLastError();

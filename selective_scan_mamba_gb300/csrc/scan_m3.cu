@@ -253,7 +253,7 @@ cudaError_t launch_m3_pass(const ssm_mamba3_params& a, const M3Plan& p, int grid
     const M3Layout lay(CPB, TPC * kMS);
     const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
     auto k = m3_scan<Tin, Tout, TPC, STATES>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     k<<<grid, kMThreads, smem, s>>>(a, p.cps, p.nseg, p.seg_len, st, ds);
     return cudaGetLastError();

@@ -251,9 +251,7 @@ static cudaError_t ssd_launch_t(const SsdArgs& a, cudaStream_t s) {
     if (nch > 0) {
         const dim3 grid(nch, a.nheads, a.batch);
         const size_t sm_a = (3 * Q + kSub * P + kSub * N) * sizeof(float);
-        cudaError_t e = cudaFuncSetAttribute(ssd_chunk_state<Tin>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(sm_a));
+        cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(ssd_chunk_state<Tin>), static_cast<int>(sm_a));
         if (e != cudaSuccess) return e;
         ssd_chunk_state<Tin><<<grid, kSsdThreads, sm_a, s>>>(a);
         e = cudaGetLastError();
@@ -265,8 +263,7 @@ static cudaError_t ssd_launch_t(const SsdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess || nch == 0) return e;
     const size_t sm_c = (3 * Q + P * (N + 1) + kSub * N + kSub * (N + 1) + kSub * P + kSub * kSub) *
                         sizeof(float);
-    e = cudaFuncSetAttribute(ssd_chunk_out<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sm_c));
+    e = set_smem_attr(reinterpret_cast<const void*>(ssd_chunk_out<Tin, Tout>), static_cast<int>(sm_c));
     if (e != cudaSuccess) return e;
     ssd_chunk_out<Tin, Tout><<<dim3(nch, a.nheads, a.batch), kSsdThreads, sm_c, s>>>(a);
     return cudaGetLastError();

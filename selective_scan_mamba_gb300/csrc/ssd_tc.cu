@@ -719,21 +719,20 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     bool cuts = false;
     for (int i = 1; i < nct && !cuts; ++i) cuts = range_begin(total, nct, i) % nch != 0;
     if (cuts) {
-        if ((e = cudaFuncSetAttribute(ssd_tc_cuts, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kCSmemAlloc)) != cudaSuccess)
+        if ((e = set_smem_attr(reinterpret_cast<const void*>(ssd_tc_cuts), kCSmemAlloc)) != cudaSuccess)
             return e;
         ssd_tc_cuts<<<nct * kCutParts, kThreads, kCSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.out_dtype == SSM_BF16) {
         auto k = ssd_tc_main<bf16_t, bf16_t>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc)) !=
+        if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
         k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
     } else {
         auto k = ssd_tc_main<bf16_t, float>;
-        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc)) !=
+        if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
         k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);

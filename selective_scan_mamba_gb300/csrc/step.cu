@@ -527,7 +527,7 @@ static cudaError_t launch_tok_k(const StepArgs& a, long long rows, int log2p, cu
     while (tb > 1 && tok_smem(nbh_max, nbg_max, tb, N, ROWS).total > budget) --tb;
     const size_t smem = static_cast<size_t>(tok_smem(nbh_max, nbg_max, tb, N, ROWS).total) * sizeof(float);
     auto k = step_tok<Tin, Tout, NV, SHARED>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const long long grid = (rows + ROWS - 1) / ROWS;
     k<<<static_cast<unsigned>(grid), kTokThreads, smem, s>>>(a, log2p, nbh_max, nbg_max, tb);

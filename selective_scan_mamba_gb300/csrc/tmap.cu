@@ -1,8 +1,13 @@
 // tmap.cu -- host-side encoding of TMA tensor maps.  The driver entry point
 // cuTensorMapEncodeTiled is fetched through the runtime, so the library needs no
-// link-time dependency on libcuda.
+// link-time dependency on libcuda.  A map is a pure function of its arguments (address,
+// element type, shape, box, swizzle), so the last kMapCache encodings are kept and a
+// repeated call (a training or decode loop over the same buffers) copies the cached map
+// instead of encoding it again.  The shared-memory attribute of a kernel is likewise set
+// once per (device, kernel, size).
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cstring>
 #include <mutex>
 
 #include "launch.h"
@@ -18,6 +23,61 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
+
+struct MapKey {
+    const void* base;
+    int kind, elem_bytes, rank, swizzle;  // kind: 2-D or n-D encoder
+    unsigned long long dims[5];
+    unsigned box[5];
+    bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+constexpr int kMapCache = 64;
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    unsigned long long used;  // 0: empty
+};
+MapEntry g_maps[kMapCache];
+unsigned long long g_tick = 0;
+
+MapKey make_key(int kind, const void* base, int elem_bytes, int rank, const unsigned long long* dims,
+                const unsigned* box, bool swizzle128) {
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));  // padding too: keys compare as bytes
+    k.kind = kind;
+    k.base = base;
+    k.elem_bytes = elem_bytes;
+    k.rank = rank;
+    k.swizzle = swizzle128 ? 1 : 0;
+    for (int i = 0; i < rank && i < 5; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+    }
+    return k;
+}
+
+bool cached_map(const MapKey& k, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (MapEntry& e : g_maps) {
+        if (e.used != 0 && e.key == k) {
+            e.used = ++g_tick;
+            *out = e.map;
+            return true;
+        }
+    }
+    return false;
+}
+
+void keep_map(const MapKey& k, const CUtensorMap& m) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    MapEntry* victim = &g_maps[0];
+    for (MapEntry& e : g_maps) {
+        if (e.used < victim->used) victim = &e;
+    }
+    victim->key = k;
+    victim->map = m;
+    victim->used = ++g_tick;
+}
 
 cudaError_t encoder(EncodeTiledFn* out) {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -41,6 +101,10 @@ cudaError_t encoder(EncodeTiledFn* out) {
 cudaError_t encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes,
                            unsigned long long inner, unsigned long long rows, unsigned box_inner,
                            unsigned box_rows, bool swizzle128) {
+    const unsigned long long kd[2] = {inner, rows};
+    const unsigned kb[2] = {box_inner, box_rows};
+    const MapKey key = make_key(2, base, elem_bytes, 2, kd, kb, swizzle128);
+    if (cached_map(key, map)) return cudaSuccess;
     EncodeTiledFn fn = nullptr;
     cudaError_t e = encoder(&fn);
     if (e != cudaSuccess) return e;
@@ -54,16 +118,20 @@ cudaError_t encode_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    keep_map(key, *map);
+    return cudaSuccess;
 }
 
 // Row-major tensor of `rank` dimensions (dims[0] innermost), contiguous strides.
 cudaError_t encode_tmap_nd(CUtensorMap* map, const void* base, int elem_bytes, int rank,
                            const unsigned long long* dims, const unsigned* box, bool swizzle128) {
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+    const MapKey key = make_key(0, base, elem_bytes, rank, dims, box, swizzle128);
+    if (cached_map(key, map)) return cudaSuccess;
     EncodeTiledFn fn = nullptr;
     cudaError_t e = encoder(&fn);
     if (e != cudaSuccess) return e;
-    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
     const CUtensorMapDataType dt =
         elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     cuuint64_t gd[5], gs[4];
@@ -80,7 +148,35 @@ cudaError_t encode_tmap_nd(CUtensorMap* map, const void* base, int elem_bytes, i
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    keep_map(key, *map);
+    return cudaSuccess;
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel, bytes): the
+// last kAttrCache settings are remembered
+cudaError_t set_smem_attr(const void* kernel, int bytes) {
+    constexpr int kAttrCache = 128;
+    struct Entry {
+        const void* fn;
+        int dev, bytes;
+    };
+    static Entry seen[kAttrCache];
+    static int next = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (const Entry& s : seen)
+            if (s.fn == kernel && s.dev == dev && s.bytes == bytes) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    seen[next] = Entry{kernel, dev, bytes};
+    next = (next + 1) % kAttrCache;
+    return cudaSuccess;
 }
 
 }  // namespace ssm
