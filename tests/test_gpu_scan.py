@@ -242,6 +242,31 @@ def test_plain_entry_point_needs_no_scratch(oracle_mod):
     check(hf, hr, TOL_BF16, what="h_final")
 
 
+def test_same_buffers_with_another_shape(oracle_mod):
+    """Tensor maps are cached by address, shape and box: the same allocations read as
+    another (batch, dim, L) must not reuse a map of the first shape."""
+    import torch
+    first = synth.mamba1(2, 96, 16, 512, dtype=synth.BF16, delta_scale=0.8, with_z=True, with_h0=True,
+                         seed=41)
+    second = synth.mamba1(3, 40, 16, 768, dtype=synth.BF16, delta_scale=0.8, with_z=True, seed=42)
+    pools = {}
+    for inp in (first, second):
+        t = to_device(inp)
+        for k, v in t.items():
+            flat = v.reshape(-1)
+            if k not in pools or pools[k].numel() < flat.numel():
+                pools[k] = torch.empty(max(flat.numel(), 4096), dtype=v.dtype, device="cuda")
+    for inp in (first, second, first):
+        t = {k: pools[k][:v.numel()].view(v.shape).copy_(v) for k, v in to_device(inp).items()}
+        y, hf = ssm.ssm_scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], D=t["D"], z=t["z"],
+                                 delta_bias=t["delta_bias"], h0=t.get("h0"), out_dtype=torch.float32,
+                                 return_final_state=True)
+        torch.cuda.synchronize()
+        yr, hr = run_oracle(oracle_mod, inp)
+        check(to_numpy(y), yr, TOL_BF16, what="y")
+        check(to_numpy(hf), hr, TOL_BF16, what="h_final")
+
+
 def test_zz_no_device_wait_gave_up():
     """Every bounded wait in the kernels above completed (timeout counter still zero)."""
     assert ssm.wait_timeouts() == 0
