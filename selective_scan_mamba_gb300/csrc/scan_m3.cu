@@ -122,9 +122,81 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
     const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
     float dsum = 0.f;  // sum of Delta over the segment (segment pass)
 
+    // Prefetch: the next chunk's inputs are loaded into registers before the current
+    // chunk's recurrence runs and written to shared memory after it, so the loads' latency
+    // hides behind the recurrence (for TPC >= 4, where a thread stages at most 8
+    // (channel, step) cells and a few B, C values).
+    constexpr int KS = (CPB * kMT + kMThreads - 1) / kMThreads;
+    constexpr int KB = (N * (kMT + 1) + kMThreads - 1) / kMThreads;
+    constexpr bool PREF = KS <= 8;
+    constexpr int RS = PREF ? KS : 1, RB = PREF ? KB : 1;
+    float r_dl[RS], r_lm[RS], r_x[RS], r_xp[RS], r_z[RS], r_b[RB], r_c[RB];
+    auto fetch = [&](int t0) {
+        const int tl = min(kMT, tend - t0);
+#pragma unroll
+        for (int k = 0; k < RS; ++k) {
+            const int j = tid + k * kMThreads;
+            const int cc = j / kMT, t = j % kMT;
+            r_dl[k] = r_lm[k] = r_x[k] = r_xp[k] = r_z[k] = 0.f;
+            if (j < CPB * kMT && cc < nchan && t < tl) {
+                const size_t i = (static_cast<size_t>(b) * Dm + d0 + cc) * L + t0 + t;
+                r_dl[k] = io<Tin>::load(DL, i) + (a.delta_bias ? a.delta_bias[d0 + cc] : 0.f);
+                r_lm[k] = io<Tin>::load(LM, i);
+                r_x[k] = io<Tin>::load(X, i);
+                r_xp[k] = (t0 + t > 0) ? io<Tin>::load(X, i - 1) : 0.f;
+                if (Z) r_z[k] = io<Tin>::load(Z, i);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            const int j = tid + k * kMThreads;
+            const int n = j / (kMT + 1), tt = j % (kMT + 1);  // B row t0 - 1 + tt
+            const int t = t0 - 1 + tt;
+            r_b[k] = r_c[k] = 0.f;
+            if (j < N * (kMT + 1)) {
+                if (t >= 0 && tt <= tl) r_b[k] = io<Tin>::load(Bp, bc_base + static_cast<size_t>(n) * L + t);
+                if (tt < tl) r_c[k] = io<Tin>::load(Cp, bc_base + static_cast<size_t>(n) * L + t0 + tt);
+            }
+        }
+    };
+    auto put = [&](int t0) {
+        const int tl = min(kMT, tend - t0);
+#pragma unroll
+        for (int k = 0; k < RS; ++k) {
+            const int j = tid + k * kMThreads;
+            if (j >= CPB * kMT) continue;
+            const int cc = j / kMT, t = j % kMT;
+            float dl = 0.f, p = 0.f, q = 0.f, xv = 0.f, gv = 1.f;
+            if (cc < nchan && t < tl) {
+                dl = a.delta_softplus ? softplus_accurate(r_dl[k]) : r_dl[k];
+                xv = r_x[k];
+                p = (1.f - r_lm[k]) * dl * r_xp[k];
+                q = r_lm[k] * dl * xv;
+                if (Z) gv = silu_accurate(r_z[k]);
+            }
+            sm[lay.dl + cc * kMRow + t] = dl;
+            sm[lay.p + cc * kMRow + t] = p;
+            sm[lay.q + cc * kMRow + t] = q;
+            sm[lay.x + cc * kMRow + t] = xv;
+            sm[lay.gate + cc * kMRow + t] = gv;
+        }
+#pragma unroll
+        for (int k = 0; k < RB; ++k) {
+            const int j = tid + k * kMThreads;
+            if (j >= N * (kMT + 1)) continue;
+            const int n = j / (kMT + 1), tt = j % (kMT + 1);
+            sm[lay.bs + tt * N + n] = r_b[k];
+            if (tt < kMT) sm[lay.cs + tt * N + n] = r_c[k];
+        }
+    };
+    if (PREF && tbeg < tend) fetch(tbeg);
+
     for (int t0 = tbeg; t0 < tend; t0 += kMT) {
         const int tl = min(kMT, tend - t0);
         __syncthreads();  // the previous chunk's tiles and outputs are done with
+        if constexpr (PREF) {
+            put(t0);
+        } else {
         for (int j = tid; j < CPB * kMT; j += kMThreads) {
             const int cc = j / kMT, t = j % kMT;
             float dl = 0.f, p = 0.f, q = 0.f, xv = 0.f, gv = 1.f;
@@ -152,7 +224,9 @@ __global__ void __launch_bounds__(kMThreads) m3_scan(ssm_mamba3_params a, int cp
             if (tt < kMT)
                 sm[lay.cs + tt * N + n] = tt < tl ? io<Tin>::load(Cp, bc_base + static_cast<size_t>(n) * L + t0 + tt) : 0.f;
         }
+        }  // not prefetched
         __syncthreads();
+        if (PREF && t0 + kMT < tend) fetch(t0 + kMT);
         for (int t = 0; t < tl; ++t) {
             const float dl = sm[lay.dl + c * kMRow + t];
             const float p = sm[lay.p + c * kMRow + t], q = sm[lay.q + c * kMRow + t];
