@@ -122,16 +122,32 @@ __global__ void __launch_bounds__(kSThreads) s4d_scan(ssm_s4d_params a, int cps,
     const float Dd = a.D_skip ? a.D_skip[d] : 0.f;
     const Tin* U = static_cast<const Tin*>(a.u);
 
+    // the next chunk's u is loaded into registers before the current chunk's recurrence
+    // and stored to shared memory after it, so its latency hides behind the recurrence
+    constexpr int KU = (CPB * kST + kSThreads - 1) / kSThreads;
+    float r_u[KU];
+    auto fetch = [&](int t0) {
+        const int tl = min(kST, tend - t0);
+#pragma unroll
+        for (int k = 0; k < KU; ++k) {
+            const int j = tid + k * kSThreads;
+            const int cc = j / kST, t = j % kST;
+            r_u[k] = (j < CPB * kST && cc < nchan && t < tl)
+                         ? io<Tin>::load(U, (static_cast<size_t>(b) * Dm + l0 + cc) * L + t0 + t)
+                         : 0.f;
+        }
+    };
+    if (tbeg < tend) fetch(tbeg);
     for (int t0 = tbeg; t0 < tend; t0 += kST) {
         const int tl = min(kST, tend - t0);
         __syncthreads();
-        for (int j = tid; j < CPB * kST; j += kSThreads) {
-            const int cc = j / kST, t = j % kST;
-            s_u[cc * kSRow + t] = (cc < nchan && t < tl)
-                                      ? io<Tin>::load(U, (static_cast<size_t>(b) * Dm + l0 + cc) * L + t0 + t)
-                                      : 0.f;
+#pragma unroll
+        for (int k = 0; k < KU; ++k) {
+            const int j = tid + k * kSThreads;
+            if (j < CPB * kST) s_u[(j / kST) * kSRow + j % kST] = r_u[k];
         }
         __syncthreads();
+        if (t0 + kST < tend) fetch(t0 + kST);
         for (int t = 0; t < tl; ++t) {
             const float u = s_u[c * kSRow + t];
             float acc = 0.f;
