@@ -98,8 +98,8 @@ cudaError_t encode_tmap_2d(struct CUtensorMap_st* map, const void* base, int ele
                            unsigned box_rows, bool swizzle128);
 cudaError_t encode_tmap_nd(struct CUtensorMap_st* map, const void* base, int elem_bytes, int rank,
                            const unsigned long long* dims, const unsigned* box, bool swizzle128);
-// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes), once per (device,
-// kernel, bytes)
+// raises the kernel's MaxDynamicSharedMemorySize on the current device to at least bytes
+// (a driver call only when the limit set so far is smaller)
 cudaError_t set_smem_attr(const void* kernel, int bytes);
 
 // Decode-step arguments.

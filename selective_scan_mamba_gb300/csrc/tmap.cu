@@ -153,10 +153,12 @@ cudaError_t encode_tmap_nd(CUtensorMap* map, const void* base, int elem_bytes, i
     return cudaSuccess;
 }
 
-// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel, bytes): the
-// last kAttrCache settings are remembered
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) only when a launch needs more than the
+// kernel's limit already set on this device: the attribute is an upper bound, so the
+// largest value set so far serves every smaller launch.  The last kAttrCache (device,
+// kernel) pairs are remembered.
 cudaError_t set_smem_attr(const void* kernel, int bytes) {
-    constexpr int kAttrCache = 128;
+    constexpr int kAttrCache = 256;
     struct Entry {
         const void* fn;
         int dev, bytes;
@@ -169,11 +171,17 @@ cudaError_t set_smem_attr(const void* kernel, int bytes) {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         for (const Entry& s : seen)
-            if (s.fn == kernel && s.dev == dev && s.bytes == bytes) return cudaSuccess;
+            if (s.fn == kernel && s.dev == dev && s.bytes >= bytes) return cudaSuccess;
     }
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_mu);
+    for (Entry& s : seen) {
+        if (s.fn == kernel && s.dev == dev) {  // raise the remembered limit
+            if (bytes > s.bytes) s.bytes = bytes;
+            return cudaSuccess;
+        }
+    }
     seen[next] = Entry{kernel, dev, bytes};
     next = (next + 1) % kAttrCache;
     return cudaSuccess;

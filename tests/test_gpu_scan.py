@@ -267,6 +267,19 @@ def test_same_buffers_with_another_shape(oracle_mod):
         check(to_numpy(hf), hr, TOL_BF16, what="h_final")
 
 
+def test_large_small_large_shared_memory(oracle_mod):
+    """The TMEM kernel's shared memory grows with its channels per CTA: a large problem,
+    a small one, then the large one again must each launch (the kernel's shared-memory
+    limit is only ever raised) and match the oracle."""
+    big = synth.mamba1(8, 1536, 16, 128, dtype=synth.BF16, delta_scale=0.8, with_z=True, seed=51)
+    small = synth.mamba1(1, 256, 16, 128, dtype=synth.BF16, delta_scale=0.8, with_z=True, seed=52)
+    for inp in (big, small, big):
+        y, hf = run_gpu(inp, out_dtype="f32", h0=False, kernel="tmem")
+        yr, hr = run_oracle(oracle_mod, inp, h0=False)
+        check(y, yr, TOL_BF16, what="y")
+        check(hf, hr, TOL_BF16, what="h_final")
+
+
 def test_zz_no_device_wait_gave_up():
     """Every bounded wait in the kernels above completed (timeout counter still zero)."""
     assert ssm.wait_timeouts() == 0
