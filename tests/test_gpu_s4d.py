@@ -157,10 +157,13 @@ def test_convolution_form_efficiency_sweep_shape(oracle_mod, bf16):
     _conv(oracle_mod, 8, 256, 32, 4096, bf16, out_bf16=bf16)
 
 
-@pytest.mark.parametrize("batch,L,N", [(3, 1000, 16), (1, 1, 8), (2, 8192, 4), (5, 257, 64)])
+@pytest.mark.parametrize("batch,L,N", [(3, 1000, 16), (1, 1, 8), (2, 8192, 4), (5, 257, 64), (2, 200, 32),
+                                       (1, 1500, 16), (2, 100, 8), (1, 2048, 32)])
 def test_convolution_form_ragged_and_limits(oracle_mod, batch, L, N):
     """An odd batch (the last transform carries one row), lengths that are not powers of
-    two, one step, and the longest sequence the shared-memory transform takes (8192)."""
+    two, one step, the longest sequence the shared-memory transform takes (8192), and a
+    length for every transform size N = 2^m (m = 1 and 8 run the kernel compiled for any
+    size, m = 9 .. 14 the ones compiled for theirs)."""
     _conv(oracle_mod, batch, 6, N, L, False, seed=batch)
 
 
