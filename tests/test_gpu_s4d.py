@@ -187,3 +187,15 @@ def test_convolution_form_refusals():
     p.u, p.y, p.h0 = u.data_ptr(), y.data_ptr(), h0.data_ptr()
     assert _lib.load().ssm_s4d_conv_fwd(ctypes.byref(p), None, 0, None) == _lib.SSM_ERR_INVALID_ARG
     del keep
+
+
+def test_convolution_form_empty_sequence():
+    """L = 0: nothing to convolve; the call succeeds without scratch and writes nothing."""
+    import torch
+    log_dt, A, B, C, D = _params(4, 8, 3)
+    dl, dA, dB, dC, dD = _dev_params(log_dt, A, B, C, D)
+    u = torch.empty((2, 4, 0), device="cuda")
+    assert ssm.ssm_s4d_conv_workspace_size(u, dl, dA, dB, dC) == 0
+    y = ssm.ssm_s4d_conv_fwd(u, dl, dA, dB, dC, D=dD)
+    torch.cuda.synchronize()
+    assert y.shape == (2, 4, 0)
