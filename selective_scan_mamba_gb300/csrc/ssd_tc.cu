@@ -89,10 +89,8 @@ constexpr int kSmemBytes = kOffBar + 128;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr uint32_t kTxMain = 40960 + kArrBytes;
 
-// cuts launch: each cut is split into kCutParts parts (separate CTAs), each with a ring
-// of kCStages stages of x, B and the step quantities and kCF F buffers (the F builders
-// run up to kCF chunks ahead of the MMAs)
-constexpr int kCutParts = 1;
+// cuts launch: a ring of kCStages stages of x, B and the step quantities and kCF F
+// buffers (the F builders run up to kCF chunks ahead of the MMAs)
 constexpr int kCStages = 6;
 constexpr int kCF = 4;
 constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
@@ -192,36 +190,83 @@ __global__ void __launch_bounds__(256) ssd_tc_prep(SsdArgs a, ChunkArr* out) {
 }
 
 // ---------------------------------------------------------------------------------------
-// cuts launch: local end state (from zero) and total decay of every range that stops
-// inside a sequence, over the chunks of that range in that sequence (walked last to
-// first).  Warps 0-15 build F, warp 16 issues the MMAs, warp 17 the copies.
+// Cuts.  Range i's cut is its chunks in its last sequence when that sequence goes on past
+// the range end: the local end state (from zero) and the total decay of those chunks are
+// what the next range of the sequence starts from.  The cut chunks of all ranges, cut
+// after cut, are dealt out in equal contiguous shares to the cuts launch's CTAs (cuts are
+// 0 to ~40 chunks long, so one CTA per cut would leave most SMs waiting for the longest).
+// The share of one CTA inside one cut is a piece; folding a cut's pieces in time order,
+// h = decay * h + S, gives the same state as the whole cut.
 // ---------------------------------------------------------------------------------------
+constexpr int kMaxRanges = 160;  // ranges (CTAs of the main launch) at most
+
+// One piece: chunks [ca, ce) of sequence wk (= batch * nheads + head).  Its state and
+// decay go to slot = its index in `piece`.
+struct CutPiece {
+    int wk, ca, ce;
+};
+// Built on the host (a few microseconds) and passed by value: no device set-up work.
+struct CutPlan {
+    int ncta;                          // CTAs of the cuts launch
+    int cta_first[kMaxRanges + 1];     // pieces of CTA q: [cta_first[q], cta_first[q + 1])
+    int cut_first[kMaxRanges + 1];     // pieces of range i's cut: [cut_first[i], cut_first[i + 1])
+    CutPiece piece[2 * kMaxRanges];    // in time order within each cut, cut after cut
+};
+// the piece slots of the ranges, for the main launch
+struct CutSlots {
+    int cut_first[kMaxRanges + 1];
+};
+
+// Range i's cut: units [beg, beg + len), len = 0 when the range ends with its sequence.
+void range_cut(long long total, int nct, int nch, int i, long long* beg, long long* len) {
+    const long long u0 = range_begin(total, nct, i), u1 = range_begin(total, nct, i + 1);
+    const long long ws = ((u1 - 1) / nch) * nch;
+    *beg = u0 > ws ? u0 : ws;
+    *len = (u1 <= u0 || u1 - ws == nch) ? 0 : u1 - *beg;
+}
+
+// The cut chunks of all ranges, cut after cut, form one list of T chunks; CTA q of the
+// cuts launch takes [q T / n, (q + 1) T / n) of it, n = min(nct, T), so no share is empty.
+// Returns the number of pieces (0: no cuts).
+int build_cut_plan(long long total, int nct, int nch, CutPlan* P) {
+    long long T = 0, beg, len;
+    for (int i = 0; i < nct; ++i) {
+        range_cut(total, nct, nch, i, &beg, &len);
+        T += len;
+    }
+    const int n = static_cast<int>(T < nct ? T : nct);
+    P->ncta = n;
+    int np = 0, next_q = 0;
+    long long F = 0;  // flat position of the cut's first chunk
+    for (int i = 0; i < nct; ++i) {
+        P->cut_first[i] = np;
+        range_cut(total, nct, nch, i, &beg, &len);
+        if (len == 0) continue;
+        const long long wk = beg / nch, off = beg - wk * nch;
+        // CTA of flat position f: the q with floor(q T / n) <= f < floor((q + 1) T / n)
+        const int qa = static_cast<int>(((F + 1) * n - 1) / T), qb = static_cast<int>(((F + len) * n - 1) / T);
+        for (int q = qa; q <= qb; ++q) {
+            const long long fa = static_cast<long long>(q) * T / n, fb = static_cast<long long>(q + 1) * T / n;
+            const long long lo = (fa > F ? fa : F) - F, hi = (fb < F + len ? fb : F + len) - F;
+            while (next_q <= q) P->cta_first[next_q++] = np;
+            P->piece[np++] = CutPiece{static_cast<int>(wk), static_cast<int>(off + lo), static_cast<int>(off + hi)};
+        }
+        F += len;
+    }
+    P->cut_first[nct] = np;
+    while (next_q <= n) P->cta_first[next_q++] = np;
+    return np;
+}
+
+// cuts launch: each CTA walks its pieces, each piece last chunk to first, accumulating
+// B^T (f x) in TMEM.  Warps 0-15 build F and read each piece's state out, warp 16 issues
+// the MMAs, warp 17 the copies.  Steps run on over the pieces, so the copy ring and the
+// F buffers stay full across piece boundaries.
 __global__ void __launch_bounds__(kThreads, 1)
-    ssd_tc_cuts(const __grid_constant__ SsdMaps maps, SsdArgs a, int nct, const ChunkArr* arrs,
-                float* cut_state, float* cut_decay) {
+    ssd_tc_cuts(const __grid_constant__ SsdMaps maps, SsdArgs a, const __grid_constant__ CutPlan plan,
+                const ChunkArr* arrs, float* cut_state, float* cut_decay) {
     const int L = a.seqlen, H = a.nheads;
     const int nch = (L + kQ - 1) / kQ;
-    const long long total = static_cast<long long>(a.batch) * H * nch;
-    const int ci = blockIdx.x / kCutParts, part = blockIdx.x % kCutParts;
-    const long long u0 = range_begin(total, nct, ci), u1 = range_begin(total, nct, ci + 1);
-    if (u1 <= u0) return;
-    const int wk = static_cast<int>((u1 - 1) / nch);
-    const long long wstart = static_cast<long long>(wk) * nch;
-    const int cut_end = static_cast<int>(u1 - wstart);
-    if (cut_end == nch) return;  // the range ends with its sequence: no cut
-    const int cut_begin = static_cast<int>((u0 > wstart ? u0 : wstart) - wstart);
-    // this CTA's part of the cut: chunks [ca, ce)
-    const int ca = cut_begin + ((cut_end - cut_begin) * part) / kCutParts;
-    const int ce = cut_begin + ((cut_end - cut_begin) * (part + 1)) / kCutParts;
-    const int n = ce - ca;
-    const int oi = ci * kCutParts + part;  // output slot
-    if (n == 0) {  // empty part: zero state, unit decay
-        float* dst = cut_state + static_cast<size_t>(oi) * kP * kNs;
-        for (int i = threadIdx.x; i < kP * kNs; i += blockDim.x) dst[i] = 0.f;
-        if (threadIdx.x == 0) cut_decay[oi] = 1.f;
-        return;
-    }
-    const int b = wk / H, hd = wk % H, g = hd / (H / a.ngroups);
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -232,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* free_bar = done_bar + 4;       // [kCStages] the stage's MMA done (its reuse)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(free_bar + kCStages);
     uint64_t* drain_bar = free_bar + kCStages + 1;  // after an abort: the issued MMAs are done
+    const CutPiece* pieces = plan.piece;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -251,55 +297,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
+    // this CTA's pieces [p0, p1), walked one after another: nsteps chunks in all
+    const int p0 = plan.cta_first[blockIdx.x], p1 = plan.cta_first[blockIdx.x + 1];
+    int nsteps = 0;
+    for (int p = p0; p < p1; ++p) nsteps += pieces[p].ce - pieces[p].ca;
 
     int last_issued = -1;  // load warp, lane 0: the last step whose copy went out
     bool live = true;      // MMA warp: no wait has failed yet
     if (warp == kLoadWarp) {
-        // step k of the walk handles chunk ce - 1 - k
-        auto issue = [&](int k) {
-            last_issued = k;
-            const int c = ce - 1 - k;
-            unsigned char* st = sm + (k % kCStages) * kCStBytes;
-            uint64_t* bar = &tma_bar[k % kCStages];
-            mbar_arrive_expect_tx(bar, kTxCut);
-            tma_load_4d(st + kCStX, &maps.x, 0, hd, c * kQ, b, bar);
-            tma_load_4d(st + kCStB, &maps.b, 0, g, c * kQ, b, bar);
-            tma_load_4d(st + kCStB + 8192, &maps.b, 64, g, c * kQ, b, bar);
-            bulk_load(st + kCStArr, arrs + wstart + c, kArrBytes, bar);
-        };
-        if (lane == 0)
-            for (int k = 0; k < kCStages && k < n; ++k) issue(k);
-        // step j + kCStages reuses the stage of step j once the MMA of step j is done
-        // (its F was built before that MMA was issued)
-        if (lane == 0)
-            for (int j = 0; j + kCStages < n; ++j) {
-                if (!mbar_wait_lane(&free_bar[j % kCStages], (j / kCStages) & 1)) break;
-                issue(j + kCStages);
+        if (lane == 0) {
+            // step k is piece p's local step kl: chunk pieces[p].ce - 1 - kl
+            int p = p0, kl = 0;
+            for (int k = 0; k < nsteps; ++k) {
+                while (kl == pieces[p].ce - pieces[p].ca) {
+                    ++p;
+                    kl = 0;
+                }
+                // step k reuses the stage of step k - kCStages once that step's MMA is done
+                if (k >= kCStages && !mbar_wait_lane(&free_bar[k % kCStages], ((k - kCStages) / kCStages) & 1))
+                    break;
+                last_issued = k;
+                const CutPiece& pc = pieces[p];
+                const int c = pc.ce - 1 - kl;
+                const int b = pc.wk / H, hd = pc.wk % H, g = hd / (H / a.ngroups);
+                unsigned char* st = sm + (k % kCStages) * kCStBytes;
+                uint64_t* bar = &tma_bar[k % kCStages];
+                mbar_arrive_expect_tx(bar, kTxCut);
+                tma_load_4d(st + kCStX, &maps.x, 0, hd, c * kQ, b, bar);
+                tma_load_4d(st + kCStB, &maps.b, 0, g, c * kQ, b, bar);
+                tma_load_4d(st + kCStB + 8192, &maps.b, 64, g, c * kQ, b, bar);
+                bulk_load(st + kCStArr, arrs + static_cast<size_t>(pc.wk) * nch + c, kArrBytes, bar);
+                ++kl;
             }
+        }
     } else if (warp == kMmaWarp) {
-        for (int k = 0; k < n; ++k) {
+        int p = p0, kl = 0;
+        for (int k = 0; k < nsteps; ++k) {
+            while (kl == pieces[p].ce - pieces[p].ca) {
+                ++p;
+                kl = 0;
+            }
             const bool built = mbar_wait_warp_ok(&done_bar[k & 3], (k >> 2) & 1);
             const bool landed = mbar_wait_warp_ok(&tma_bar[k % kCStages], (k / kCStages) & 1);
             tc::fence_after();
             live = built && landed && live;
+            ++kl;
             if (!live) continue;  // the CTA has aborted: issue nothing more
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
             const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * 16384);
-            // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts
+            // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts;
+            // a piece's first step starts the accumulator afresh
             const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
             const uint64_t dB = tc::desc_sw128_mn(sbm, 8192), dF = tc::desc_sw128_mn(sf, 8192);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                tc::mma_bf16_warp(tmem, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4, (k > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_bf16_warp(tmem, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4,
+                                  (kl > 1 || kk > 0) ? 1u : 0u);
             tc::mma_commit_warp(&mma_bar[k % kCF]);
             tc::mma_commit_warp(&free_bar[k % kCStages]);
             __syncwarp();
         }
     } else {
         const int fs = tid >> 3, fp = (tid & 7) * 8;  // F element (s, p..p+7)
-        float tailf = 1.f;  // decay of the chunks already walked (later in time)
-        for (int k = 0; k < n; ++k) {
+        const int q4 = warp & 3, cg = warp >> 2;
+        const int hn = 32 * q4 + lane, hp = 16 * cg;
+        int p = p0, kl = 0;
+        float tailf = 1.f;  // decay of the piece's chunks already walked (later in time)
+        for (int k = 0; k < nsteps; ++k) {
             if (k >= kCF) {  // MMA of step k-kCF done: its F buffer is free
                 mbar_wait_warp(&mma_bar[k % kCF], (k / kCF - 1) & 1);
                 tc::fence_after();
@@ -322,20 +387,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&done_bar[k & 3]);
-        }
-        mbar_wait_warp(&mma_bar[(n - 1) % kCF], ((n - 1) / kCF) & 1);
-        tc::fence_after();
-        const int q4 = warp & 3, cg = warp >> 2;
-        const int hn = 32 * q4 + lane, hp = 16 * cg;
-        uint32_t r[16], r2[16];
-        tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + hp, r);
-        tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + hp, r2);
-        tc::tmem_wait();
-        float* dst = cut_state + static_cast<size_t>(oi) * kP * kNs;
+            if (++kl == pieces[p].ce - pieces[p].ca) {
+                // the piece's last step: once its MMA is done, read the state out (the next
+                // piece's first MMA waits for F built after this read)
+                mbar_wait_warp(&mma_bar[k % kCF], (k / kCF) & 1);
+                tc::fence_after();
+                uint32_t r[16], r2[16];
+                tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + hp, r);
+                tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + hp, r2);
+                tc::tmem_wait();
+                tc::fence_before();
+                const int slot = p;
+                float* dst = cut_state + static_cast<size_t>(slot) * kP * kNs;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
-        if (tid == 0) cut_decay[oi] = tailf;
+                for (int j = 0; j < 16; ++j)
+                    dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
+                if (tid == 0) cut_decay[slot] = tailf;
+                ++p;
+                kl = 0;
+                tailf = 1.f;
+            }
+        }
     }
     // a CTA whose waits gave up lets its copies and MMAs in flight finish before the
     // shared and tensor memory they write is released
@@ -355,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
-    ssd_tc_main(const __grid_constant__ SsdMaps maps, SsdArgs a, int nct, const ChunkArr* arrs,
-                const float* cut_state, const float* cut_decay) {
+    ssd_tc_main(const __grid_constant__ SsdMaps maps, SsdArgs a, int nct, const __grid_constant__ CutSlots slots,
+                const ChunkArr* arrs, const float* cut_state, const float* cut_decay) {
     const int L = a.seqlen, H = a.nheads;
     const int nch = (L + kQ - 1) / kQ;
     const long long total = static_cast<long long>(a.batch) * H * nch;
@@ -511,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long ws = static_cast<long long>(wk) * nch;
                 int j0 = ci - 1;
                 while (j0 > 0 && range_begin(total, nct, j0) > ws) --j0;
-                for (int j = j0 * kCutParts; j < ci * kCutParts; ++j) {  // parts in time order
+                // the pieces of the cuts of ranges j0 .. ci-1, in time order
+                for (int j = slots.cut_first[j0]; j < slots.cut_first[ci]; ++j) {
                     const float dec = cut_decay[j];
                     const float* cs = cut_state + static_cast<size_t>(j) * PN;
 #pragma unroll
@@ -664,17 +737,20 @@ int tc_ctas(long long total) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms > kMaxRanges) sms = kMaxRanges;
     return static_cast<int>(total < sms ? total : sms);
 }
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// workspace: cut states [cuts][P][N] fp32, cut decays [cuts], step quantities [units]
+// workspace: piece states [pieces][P][N] fp32, piece decays [pieces], step quantities
+// [units]; nct ranges give at most 2 nct - 1 pieces
 struct TcWorkspace {
     size_t off_decay, off_arr, bytes;
     TcWorkspace(int nct, long long units) {
-        off_decay = round256(static_cast<size_t>(nct) * kP * kNs * sizeof(float));
-        off_arr = off_decay + round256(static_cast<size_t>(nct) * sizeof(float));
+        const size_t np = 2 * static_cast<size_t>(nct);
+        off_decay = round256(np * kP * kNs * sizeof(float));
+        off_arr = off_decay + round256(np * sizeof(float));
         bytes = off_arr + round256(static_cast<size_t>(units) * kArrBytes);
     }
 };
@@ -695,13 +771,13 @@ bool ssd_tc_supported(const SsdArgs& a) {
 
 size_t ssd_tc_workspace_bytes(const SsdArgs& a) {
     const long long units = tc_units(a);
-    return TcWorkspace(tc_ctas(units) * kCutParts, units).bytes;
+    return TcWorkspace(tc_ctas(units), units).bytes;
 }
 
 cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     const long long total = tc_units(a);
     const int nct = tc_ctas(total);
-    const TcWorkspace wl(nct * kCutParts, total);
+    const TcWorkspace wl(nct, total);
     SsdMaps maps;
     cudaError_t e;
     const uint64_t H = a.nheads, G = a.ngroups, L = a.seqlen, Bt = a.batch;
@@ -716,26 +792,27 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // a cut exists where a range boundary falls inside a sequence
     const int nch = (a.seqlen + kQ - 1) / kQ;
-    bool cuts = false;
-    for (int i = 1; i < nct && !cuts; ++i) cuts = range_begin(total, nct, i) % nch != 0;
-    if (cuts) {
+    CutPlan plan;
+    CutSlots slots;
+    if (build_cut_plan(total, nct, nch, &plan) > 0) {
         if ((e = set_smem_attr(reinterpret_cast<const void*>(ssd_tc_cuts), kCSmemAlloc)) != cudaSuccess)
             return e;
-        ssd_tc_cuts<<<nct * kCutParts, kThreads, kCSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
+        ssd_tc_cuts<<<plan.ncta, kThreads, kCSmemAlloc, s>>>(maps, a, plan, arrs, cut_state, cut_decay);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    for (int i = 0; i <= nct; ++i) slots.cut_first[i] = plan.cut_first[i];
     if (a.out_dtype == SSM_BF16) {
         auto k = ssd_tc_main<bf16_t, bf16_t>;
         if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
-        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
+        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, slots, arrs, cut_state, cut_decay);
     } else {
         auto k = ssd_tc_main<bf16_t, float>;
         if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
-        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, arrs, cut_state, cut_decay);
+        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, slots, arrs, cut_state, cut_decay);
     }
     return cudaGetLastError();
 }

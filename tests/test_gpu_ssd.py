@@ -110,6 +110,20 @@ def test_ranges_cross_sequences(oracle_mod, out):
     check(hf, hr, TOL_BF16, what="h_final")
 
 
+@pytest.mark.parametrize("batch,L,heads", [(1, 640, 3), (1, 12000, 1), (3, 2000, 5), (8, 1100, 4)],
+                         ids=["fewer_cut_chunks_than_sms", "one_sequence", "mixed", "many_short_cuts"])
+def test_cut_pieces(oracle_mod, batch, L, heads):
+    """Range ends inside sequences in several arrangements, so that the cut chunks are dealt
+    out in shares that split cuts across CTAs (pieces folded back in time order): fewer cut
+    chunks than SMs (one chunk per range), one sequence cut at every range, and mixes of
+    long and short cuts; initial state, gate, ragged last chunk."""
+    inp = synth.ssd(batch, L, heads, 64, 128, 1, dtype=synth.BF16, with_z=True, with_h0=True, seed=7)
+    y, hf = run_gpu(inp, 64, out_dtype="f32")
+    yr, hr = run_oracle(oracle_mod, inp)
+    check(y, yr, TOL_BF16, what="y")
+    check(hf, hr, TOL_BF16, what="h_final")
+
+
 _SSD_130M_REF = {}
 
 
