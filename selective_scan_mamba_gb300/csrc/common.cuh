@@ -185,6 +185,16 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched by launch_dependent() may start while
+// the kernel before it in the stream is still running: it calls grid_dep_wait() before it
+// reads what that kernel writes or writes what it reads (the wait returns once the earlier
+// grid has completed and its writes are visible).  grid_dep_launch() lets the next such
+// kernel be scheduled before this one ends.  Both do nothing in an ordinary launch.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------
 // asynchronous global->shared copies (16 bytes, zero-filled past src_bytes)
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {

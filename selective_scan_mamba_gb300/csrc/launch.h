@@ -102,6 +102,25 @@ cudaError_t encode_tmap_nd(struct CUtensorMap_st* map, const void* base, int ele
 // (a driver call only when the limit set so far is smaller)
 cudaError_t set_smem_attr(const void* kernel, int bytes);
 
+// Launches `kernel` so that it may start before the kernel ahead of it in stream `s` has
+// finished (programmatic stream serialisation); the kernel must call grid_dep_wait()
+// before it touches memory the earlier kernel uses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Decode-step arguments.
 struct StepArgs {
     int batch, nheads, headdim, dstate, ngroups, a_per_state;

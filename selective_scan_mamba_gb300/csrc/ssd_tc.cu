@@ -151,6 +151,7 @@ __host__ __device__ __forceinline__ long long range_begin(long long total, int n
 // ---------------------------------------------------------------------------------------
 template <typename Tin>
 __global__ void __launch_bounds__(256) ssd_tc_prep(SsdArgs a, ChunkArr* out) {
+    grid_dep_launch();  // the next launch may set itself up meanwhile
     const int L = a.seqlen, H = a.nheads;
     const int nch = (L + kQ - 1) / kQ;
     const long long units = static_cast<long long>(a.batch) * H * nch;
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    grid_dep_launch();
     if (warp == 0) tc::tmem_alloc(tslot, 128);
     if (tid == 0) {
         prefetch_tmap(&maps.x);
@@ -296,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    grid_dep_wait();  // the step quantities written by the launch before
     const uint32_t tmem = *tslot;
     // this CTA's pieces [p0, p1), walked one after another: nsteps chunks in all
     const int p0 = plan.cta_first[blockIdx.x], p1 = plan.cta_first[blockIdx.x + 1];
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    grid_dep_wait();  // the step quantities and cut states of the launches before
     const uint32_t tmem = *tslot;
     const Tin* Z = static_cast<const Tin*>(a.z);
     const size_t PN = static_cast<size_t>(kP) * kNs;
@@ -797,8 +801,9 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     if (build_cut_plan(total, nct, nch, &plan) > 0) {
         if ((e = set_smem_attr(reinterpret_cast<const void*>(ssd_tc_cuts), kCSmemAlloc)) != cudaSuccess)
             return e;
-        ssd_tc_cuts<<<plan.ncta, kThreads, kCSmemAlloc, s>>>(maps, a, plan, arrs, cut_state, cut_decay);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_dependent(ssd_tc_cuts, plan.ncta, kThreads, kCSmemAlloc, s, maps, a, plan, arrs, cut_state,
+                                  cut_decay)) != cudaSuccess)
+            return e;
     }
     for (int i = 0; i <= nct; ++i) slots.cut_first[i] = plan.cut_first[i];
     if (a.out_dtype == SSM_BF16) {
@@ -806,15 +811,15 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
         if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
-        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, slots, arrs, cut_state, cut_decay);
+        e = launch_dependent(k, nct, kThreads, kSmemAlloc, s, maps, a, nct, slots, arrs, cut_state, cut_decay);
     } else {
         auto k = ssd_tc_main<bf16_t, float>;
         if ((e = set_smem_attr(reinterpret_cast<const void*>(k), kSmemAlloc)) !=
             cudaSuccess)
             return e;
-        k<<<nct, kThreads, kSmemAlloc, s>>>(maps, a, nct, slots, arrs, cut_state, cut_decay);
+        e = launch_dependent(k, nct, kThreads, kSmemAlloc, s, maps, a, nct, slots, arrs, cut_state, cut_decay);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t ssd_tc_take_wait_timeouts(unsigned int* count) {
