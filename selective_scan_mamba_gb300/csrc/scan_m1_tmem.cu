@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
         tma_load_2d(st + lay.c, &maps.c, t0, pair * kN, bar);
     };
 
+    grid_dep_launch();  // the next launch may set itself up while this one runs
     if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
     if (tid == 0) {
         prefetch_tmap(&maps.x);
@@ -180,6 +181,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) m1_scan_tmem(const __grid_cons
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    // everything above touched only this CTA's own memory; from here on global memory,
+    // which the launch before this one may still be reading or writing
+    grid_dep_wait();
     const uint32_t tmem = *tslot;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const int ntiles = k1 - k0;  // tiles of this CTA
@@ -546,8 +550,9 @@ cudaError_t m1_tmem_launch(const M1Args& a_in, const M1Plan& plan, void* workspa
         if (err != cudaSuccess) return err;
         err = set_smem_attr(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
         if (err != cudaSuccess) return err;
-        kern<<<grid, round_up(cpb * kTPC, 32), smem, s>>>(maps, a, cps, plan.segs, plan.tps, seg_state, seg_dsum);
-        return cudaGetLastError();
+        err = launch_dependent(kern, grid, round_up(cpb * kTPC, 32), smem, s, maps, a, cps, plan.segs, plan.tps,
+                               seg_state, seg_dsum);
+        return err != cudaSuccess ? err : cudaGetLastError();
     };
     const int pairs = a_in.batch * a_in.ngroups;
     cudaError_t e;
