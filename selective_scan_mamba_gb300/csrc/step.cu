@@ -588,6 +588,76 @@ __global__ void __launch_bounds__(128) step_scalar(StepArgs a) {
     }
 }
 
+// Mamba-1 form, one token (A per state, P = 1, N = 16): every row is one (batch, channel)
+// with its own Delta, so there is no per-head work to share through a prologue.  Four
+// lanes per row (four states each, one float4), eight rows per warp per pass, UNROLL
+// passes per warp; every load of a pass (state, A, B, C, Delta, x, z, bias, D) is issued
+// before any of them is used, so a warp waits for one memory round trip per pass.
+template <typename Tin, typename Tout, int UNROLL>
+__global__ void __launch_bounds__(kStepThreads, 2) step_m1row(StepArgs a, unsigned rows) {
+    constexpr int N = 16;
+    const int lane = threadIdx.x & 31, sub = lane >> 2, li = lane & 3;
+    const unsigned H = static_cast<unsigned>(a.nheads);
+    const unsigned per_group = H / static_cast<unsigned>(a.ngroups);
+    const Tin* X = static_cast<const Tin*>(a.x);
+    const Tin* Z = static_cast<const Tin*>(a.z);
+    const Tin* DT = static_cast<const Tin*>(a.dt);
+    const Tin* Bp = static_cast<const Tin*>(a.B);
+    const Tin* Cp = static_cast<const Tin*>(a.C);
+    const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
+    const unsigned per_pass = 8u * UNROLL;
+    for (unsigned base = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * per_pass; base < rows;
+         base += nwarps * per_pass) {
+        float4 hv[UNROLL], av[UNROLL];
+        float bv[UNROLL][4], cv[UNROLL][4];
+        float dtr[UNROLL], xr[UNROLL], zr[UNROLL], bias[UNROLL], dsk[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const unsigned r0 = base + u * 8u + sub;
+            const unsigned r = r0 < rows ? r0 : rows - 1;  // past the end: reread the last row
+            const unsigned b = r / H, hd = r - b * H;
+            hv[u] = __ldcs(reinterpret_cast<const float4*>(a.state + static_cast<size_t>(r) * N) + li);
+            av[u] = __ldg(reinterpret_cast<const float4*>(a.A + static_cast<size_t>(hd) * N) + li);
+            const size_t bc = (static_cast<size_t>(b) * a.ngroups + hd / per_group) * N + 4 * li;
+            load4_f32(Bp + bc, bv[u]);
+            load4_f32(Cp + bc, cv[u]);
+            dtr[u] = to_f32(DT[r]);
+            xr[u] = to_f32(X[r]);
+            zr[u] = Z ? to_f32(Z[r]) : 0.f;
+            bias[u] = a.dt_bias ? a.dt_bias[hd] : 0.f;
+            dsk[u] = a.D ? a.D[hd] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const unsigned r = base + u * 8u + sub;
+            const float v = dtr[u] + bias[u];
+            const float dt = a.dt_softplus ? softplus_accurate(v) : v;
+            const float dx = dt * xr[u];
+            const float A4[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
+            float h4[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float za = dt * A4[j];
+                const float w = a.disc == SSM_DISC_ZOH ? phi1f(za) : 1.f;
+                h4[j] = expf(za) * h4[j] + (w * dx) * bv[u][j];
+                acc = fmaf(cv[u][j], h4[j], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (r < rows) {
+                __stcs(reinterpret_cast<float4*>(a.state + static_cast<size_t>(r) * N) + li,
+                       make_float4(h4[0], h4[1], h4[2], h4[3]));
+                if (li == 0) {
+                    float yv = acc + dsk[u] * xr[u];
+                    if (Z) yv *= silu_accurate(zr[u]);
+                    io<Tout>::store(static_cast<Tout*>(a.y), r, yv);
+                }
+            }
+        }
+    }
+}
+
 template <typename Tin, typename Tout, int NV, int LPR, int UNROLL>
 static cudaError_t launch_vec(const StepArgs& a, long long rows, cudaStream_t s) {
     // rows per CTA: enough for every warp to run two passes of UNROLL rows
@@ -635,6 +705,17 @@ static cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
             case 256: return launch_tok<Tin, Tout, 8>(a, rows, s);
             default: break;
         }
+    }
+    if (a.ntok == 1 && a.a_per_state && a.headdim == 1 && a.dstate == 16 && rows < (1LL << 31)) {
+        constexpr int kU = 4;
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const long long warps = (rows + 8 * kU - 1) / (8 * kU);
+        const long long want = (warps + kStepThreads / 32 - 1) / (kStepThreads / 32);
+        const long long grid = want < 2LL * sms ? want : 2LL * sms;  // 2 CTAs per SM resident
+        step_m1row<Tin, Tout, kU><<<static_cast<unsigned>(grid), kStepThreads, 0, s>>>(a, static_cast<unsigned>(rows));
+        return cudaGetLastError();
     }
     switch (a.dstate) {
         case 16: return launch_vec<Tin, Tout, 1, 4, 4>(a, rows, s);

@@ -248,3 +248,15 @@ def test_mamba1_form_bf16_zoh_ragged(oracle_mod):
     """Mamba-1 decode in bf16 with ZOH and dstate 32; 3 x 37 rows do not fill the last
     warp's row slots."""
     _steps(oracle_mod, 3, 37, 1, 32, 1, 4, synth.BF16, a_per_state=True, disc="zoh")
+
+
+@pytest.mark.parametrize("batch,H,G,dtype,disc,with_z", [
+    (3, 37, 1, synth.BF16, "zoh", True),
+    (2, 38, 2, synth.F32, "exp_euler", False),
+    (64, 3072, 1, synth.BF16, "exp_euler", True),
+], ids=["bf16_zoh_ragged", "fp32_two_groups_no_gate", "batch64_3072_channels"])
+def test_mamba1_form_dstate16_row_kernel(oracle_mod, batch, H, G, dtype, disc, with_z):
+    """Mamba-1 decode at dstate 16 (one row per (batch, channel), four lanes per row):
+    rows that do not fill the last warp's slots, two groups of channels sharing B/C, no
+    gate, and the hybrid stack's full layer (196,608 rows, several passes per warp)."""
+    _steps(oracle_mod, batch, H, 1, 16, G, 3, dtype, a_per_state=True, disc=disc, with_z=with_z)
