@@ -37,6 +37,10 @@ constexpr int kStepThreads = 256;
 template <typename Tin, typename Tout, int NV, int LPR, int UNROLL, bool PER_STATE>
 __global__ void __launch_bounds__(kStepThreads) step_vec1(StepArgs a, int rows_per_cta,
                                                          int log2p) {
+    // dependent launch: let the next launch be scheduled, then wait for the one before
+    // (its writes, for instance this layer's input) before touching global memory
+    grid_dep_launch();
+    grid_dep_wait();
     constexpr int RPW = 32 / LPR;  // rows per warp per pass
     const int N = a.dstate;
     const long long rows = static_cast<long long>(a.batch) * a.nheads * a.headdim;
@@ -160,6 +164,10 @@ __global__ void __launch_bounds__(kStepThreads) step_vec1(StepArgs a, int rows_p
 template <typename Tin, typename Tout, int NV, int LPR, int UNROLL, bool PER_STATE>
 __global__ void __launch_bounds__(kStepThreads) step_vec(StepArgs a, int rows_per_cta,
                                                          int log2p, int tab) {
+    // dependent launch: let the next launch be scheduled, then wait for the one before
+    // (its writes, for instance this layer's input) before touching global memory
+    grid_dep_launch();
+    grid_dep_wait();
     constexpr int RPW = 32 / LPR;  // rows per warp per pass
     const int N = a.dstate;
     const int T = a.ntok;
@@ -348,6 +356,10 @@ struct TokShape {
 template <typename Tin, typename Tout, int NV, bool SHARED>
 __global__ void __launch_bounds__(kTokThreads) step_tok(StepArgs a, int log2p, int nbh_max,
                                                         int nbg_max, int tb_max) {
+    // dependent launch: let the next launch be scheduled, then wait for the one before
+    // (its writes, for instance this layer's input) before touching global memory
+    grid_dep_launch();
+    grid_dep_wait();
     constexpr int LPR = 8, RPW = 4;
     constexpr int UNR = TokShape<NV>::UNR, TG = TokShape<NV>::TG, ROWS = TokShape<NV>::ROWS;
     constexpr int N = 32 * NV;
@@ -530,8 +542,7 @@ static cudaError_t launch_tok_k(const StepArgs& a, long long rows, int log2p, cu
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const long long grid = (rows + ROWS - 1) / ROWS;
-    k<<<static_cast<unsigned>(grid), kTokThreads, smem, s>>>(a, log2p, nbh_max, nbg_max, tb);
-    return cudaGetLastError();
+    return launch_dependent(k, static_cast<unsigned>(grid), kTokThreads, smem, s, a, log2p, nbh_max, nbg_max, tb);
 }
 
 template <typename Tin, typename Tout, int NV>
@@ -552,6 +563,10 @@ static cudaError_t launch_tok(const StepArgs& a, long long rows, cudaStream_t s)
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(128) step_scalar(StepArgs a) {
+    // dependent launch: let the next launch be scheduled, then wait for the one before
+    // (its writes, for instance this layer's input) before touching global memory
+    grid_dep_launch();
+    grid_dep_wait();
     const long long rows = static_cast<long long>(a.batch) * a.nheads * a.headdim;
     const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= rows) return;
@@ -595,6 +610,10 @@ __global__ void __launch_bounds__(128) step_scalar(StepArgs a) {
 // before any of them is used, so a warp waits for one memory round trip per pass.
 template <typename Tin, typename Tout, int UNROLL>
 __global__ void __launch_bounds__(kStepThreads, 2) step_m1row(StepArgs a, unsigned rows) {
+    // dependent launch: let the next launch be scheduled, then wait for the one before
+    // (its writes, for instance this layer's input) before touching global memory
+    grid_dep_launch();
+    grid_dep_wait();
     constexpr int N = 16;
     const int lane = threadIdx.x & 31, sub = lane >> 2, li = lane & 3;
     const unsigned H = static_cast<unsigned>(a.nheads);
@@ -672,12 +691,10 @@ static cudaError_t launch_vec(const StepArgs& a, long long rows, cudaStream_t s)
     if (a.ntok == 1) {
         const size_t smem1 = static_cast<size_t>(nbh_max) * 6 * sizeof(float);
         if (a.a_per_state)
-            step_vec1<Tin, Tout, NV, LPR, UNROLL, true>
-                <<<static_cast<unsigned>(grid), kStepThreads, smem1, s>>>(a, rows_per_cta, log2p);
-        else
-            step_vec1<Tin, Tout, NV, LPR, UNROLL, false>
-                <<<static_cast<unsigned>(grid), kStepThreads, smem1, s>>>(a, rows_per_cta, log2p);
-        return cudaGetLastError();
+            return launch_dependent(step_vec1<Tin, Tout, NV, LPR, UNROLL, true>, static_cast<unsigned>(grid),
+                                    kStepThreads, smem1, s, a, rows_per_cta, log2p);
+        return launch_dependent(step_vec1<Tin, Tout, NV, LPR, UNROLL, false>, static_cast<unsigned>(grid),
+                                kStepThreads, smem1, s, a, rows_per_cta, log2p);
     }
     // several tokens: per-CTA (batch, head) table, plus the per-token step quantities when
     // they fit in 48 KB
@@ -686,12 +703,10 @@ static cudaError_t launch_vec(const StepArgs& a, long long rows, cudaStream_t s)
     const int tab = base + tabb <= 48 * 1024 ? 1 : 0;
     const size_t smem = base + (tab ? tabb : 0);
     if (a.a_per_state)
-        step_vec<Tin, Tout, NV, LPR, UNROLL, true>
-            <<<static_cast<unsigned>(grid), kStepThreads, smem, s>>>(a, rows_per_cta, log2p, tab);
-    else
-        step_vec<Tin, Tout, NV, LPR, UNROLL, false>
-            <<<static_cast<unsigned>(grid), kStepThreads, smem, s>>>(a, rows_per_cta, log2p, tab);
-    return cudaGetLastError();
+        return launch_dependent(step_vec<Tin, Tout, NV, LPR, UNROLL, true>, static_cast<unsigned>(grid),
+                                kStepThreads, smem, s, a, rows_per_cta, log2p, tab);
+    return launch_dependent(step_vec<Tin, Tout, NV, LPR, UNROLL, false>, static_cast<unsigned>(grid),
+                            kStepThreads, smem, s, a, rows_per_cta, log2p, tab);
 }
 
 template <typename Tin, typename Tout>
@@ -714,8 +729,8 @@ static cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
         const long long warps = (rows + 8 * kU - 1) / (8 * kU);
         const long long want = (warps + kStepThreads / 32 - 1) / (kStepThreads / 32);
         const long long grid = want < 2LL * sms ? want : 2LL * sms;  // 2 CTAs per SM resident
-        step_m1row<Tin, Tout, kU><<<static_cast<unsigned>(grid), kStepThreads, 0, s>>>(a, static_cast<unsigned>(rows));
-        return cudaGetLastError();
+        return launch_dependent(step_m1row<Tin, Tout, kU>, static_cast<unsigned>(grid), kStepThreads, 0, s, a,
+                                static_cast<unsigned>(rows));
     }
     switch (a.dstate) {
         case 16: return launch_vec<Tin, Tout, 1, 4, 4>(a, rows, s);
@@ -725,8 +740,7 @@ static cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
         case 256: return launch_vec<Tin, Tout, 2, 32, 4>(a, rows, s);
         default: {
             const unsigned blocks = static_cast<unsigned>((rows + 127) / 128);
-            step_scalar<Tin, Tout><<<blocks, 128, 0, s>>>(a);
-            return cudaGetLastError();
+            return launch_dependent(step_scalar<Tin, Tout>, blocks, 128, 0, s, a);
         }
     }
 }
