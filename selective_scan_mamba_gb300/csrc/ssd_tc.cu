@@ -89,16 +89,19 @@ constexpr int kSmemBytes = kOffBar + 128;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr uint32_t kTxMain = 40960 + kArrBytes;
 
-// cuts launch: a ring of kCStages stages of x, B and the step quantities and kCF F
-// buffers (the F builders run up to kCF chunks ahead of the MMAs)
-constexpr int kCStages = 6;
-constexpr int kCF = 4;
-constexpr int kCStX = 0, kCStB = 8192, kCStArr = 24576, kCStBytes = 25600;
-constexpr int kCOffF = kCStages * kCStBytes;  // kCF x (F_hi, F_lo) = kCF x 16 KB
-constexpr int kCOffBar = kCOffF + kCF * 16384;
+// cuts launch: each step takes two chunks (128 steps of x and B, two chunks' step
+// quantities); a ring of kCStages such stages and kCF F buffers (the F builders run up to
+// kCF steps ahead of the MMAs)
+constexpr int kCStages = 3;
+constexpr int kCF = 2;
+constexpr int kCRows = 2 * kQ;  // s rows per step
+constexpr int kCStX = 0, kCStB = 16384, kCStArr = 49152, kCStBytes = 50176;  // x [s][p], B [s][n]
+constexpr int kCFBytes = 32768;  // F_hi then F_lo, [128 s][64 p] each
+constexpr int kCOffF = kCStages * kCStBytes;
+constexpr int kCOffBar = kCOffF + kCF * kCFBytes;
 constexpr int kCSmemBytes = kCOffBar + 192;
 constexpr int kCSmemAlloc = kCSmemBytes + 1024;
-constexpr uint32_t kTxCut = 24576 + kArrBytes;
+constexpr uint32_t kTxCutTiles = 16384 + 32768;  // x and B of two chunks
 
 // 16-byte chunk `cq` (8 bf16) of row `r` in a 128-byte-row swizzled tile
 __device__ __forceinline__ int chunk_off(int r, int cq) { return r * 128 + (((cq ^ (r & 7))) << 4); }
@@ -259,10 +262,26 @@ int build_cut_plan(long long total, int nct, int nch, CutPlan* P) {
     return np;
 }
 
-// cuts launch: each CTA walks its pieces, each piece last chunk to first, accumulating
-// B^T (f x) in TMEM.  Warps 0-15 build F and read each piece's state out, warp 16 issues
-// the MMAs, warp 17 the copies.  Steps run on over the pieces, so the copy ring and the
-// F buffers stay full across piece boundaries.
+// cuts launch: each CTA walks its pieces, each piece last chunk to first, two chunks per
+// step (hi = the later, lo = the one before it; a piece of odd length ends with a step
+// whose lo half lies outside the piece and is built as zeros), accumulating B^T (f x) in
+// TMEM with K = 128 per step.  Warps 0-15 build F and read each piece's state out, warp
+// 16 issues the MMAs, warp 17 the copies.  Steps run on over the pieces, so the copy ring
+// and the F buffers stay full across piece boundaries.
+struct CutSteps {  // the step sequence of one CTA: piece p, its local step j
+    const CutPiece* pieces;
+    int p = 0, j = 0;
+    __device__ int steps_of(int q) const { return (pieces[q].ce - pieces[q].ca + 1) >> 1; }
+    __device__ void next() {
+        if (++j == steps_of(p)) {
+            ++p;
+            j = 0;
+        }
+    }
+    __device__ int hi() const { return pieces[p].ce - 1 - 2 * j; }  // chunk of the later half
+    __device__ bool lo_ok() const { return hi() - 1 >= pieces[p].ca; }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_tc_cuts(const __grid_constant__ SsdMaps maps, SsdArgs a, const __grid_constant__ CutPlan plan,
                 const ChunkArr* arrs, float* cut_state, float* cut_decay) {
@@ -278,7 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* free_bar = done_bar + 4;       // [kCStages] the stage's MMA done (its reuse)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(free_bar + kCStages);
     uint64_t* drain_bar = free_bar + kCStages + 1;  // after an abort: the issued MMAs are done
-    const CutPiece* pieces = plan.piece;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -300,72 +318,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     grid_dep_wait();  // the step quantities written by the launch before
     const uint32_t tmem = *tslot;
-    // this CTA's pieces [p0, p1), walked one after another: nsteps chunks in all
+    // this CTA's pieces [p0, p1), walked one after another: nsteps steps in all
     const int p0 = plan.cta_first[blockIdx.x], p1 = plan.cta_first[blockIdx.x + 1];
+    CutSteps walk{plan.piece, p0, 0};
     int nsteps = 0;
-    for (int p = p0; p < p1; ++p) nsteps += pieces[p].ce - pieces[p].ca;
+    for (int p = p0; p < p1; ++p) nsteps += walk.steps_of(p);
 
     int last_issued = -1;  // load warp, lane 0: the last step whose copy went out
     bool live = true;      // MMA warp: no wait has failed yet
     if (warp == kLoadWarp) {
         if (lane == 0) {
-            // step k is piece p's local step kl: chunk pieces[p].ce - 1 - kl
-            int p = p0, kl = 0;
-            for (int k = 0; k < nsteps; ++k) {
-                while (kl == pieces[p].ce - pieces[p].ca) {
-                    ++p;
-                    kl = 0;
-                }
+            for (int k = 0; k < nsteps; ++k, walk.next()) {
                 // step k reuses the stage of step k - kCStages once that step's MMA is done
                 if (k >= kCStages && !mbar_wait_lane(&free_bar[k % kCStages], ((k - kCStages) / kCStages) & 1))
                     break;
                 last_issued = k;
-                const CutPiece& pc = pieces[p];
-                const int c = pc.ce - 1 - kl;
-                const int b = pc.wk / H, hd = pc.wk % H, g = hd / (H / a.ngroups);
+                const int wk = plan.piece[walk.p].wk, hi = walk.hi();
+                const bool lo_ok = walk.lo_ok();
+                const int b = wk / H, hd = wk % H, g = hd / (H / a.ngroups);
                 unsigned char* st = sm + (k % kCStages) * kCStBytes;
                 uint64_t* bar = &tma_bar[k % kCStages];
-                mbar_arrive_expect_tx(bar, kTxCut);
-                tma_load_4d(st + kCStX, &maps.x, 0, hd, c * kQ, b, bar);
-                tma_load_4d(st + kCStB, &maps.b, 0, g, c * kQ, b, bar);
-                tma_load_4d(st + kCStB + 8192, &maps.b, 64, g, c * kQ, b, bar);
-                bulk_load(st + kCStArr, arrs + static_cast<size_t>(pc.wk) * nch + c, kArrBytes, bar);
-                ++kl;
+                mbar_arrive_expect_tx(bar, kTxCutTiles + (lo_ok ? 2 : 1) * kArrBytes);
+                // rows (hi - 1) * 64 .. hi * 64 + 63; before the sequence start (hi = 0)
+                // the copy reads zeros
+                tma_load_4d(st + kCStX, &maps.x, 0, hd, (hi - 1) * kQ, b, bar);
+                tma_load_4d(st + kCStB, &maps.b, 0, g, (hi - 1) * kQ, b, bar);
+                tma_load_4d(st + kCStB + 16384, &maps.b, 64, g, (hi - 1) * kQ, b, bar);
+                const ChunkArr* ar = arrs + static_cast<size_t>(wk) * nch;
+                if (lo_ok) bulk_load(st + kCStArr, ar + hi - 1, kArrBytes, bar);
+                bulk_load(st + kCStArr + kArrBytes, ar + hi, kArrBytes, bar);
             }
         }
     } else if (warp == kMmaWarp) {
-        int p = p0, kl = 0;
-        for (int k = 0; k < nsteps; ++k) {
-            while (kl == pieces[p].ce - pieces[p].ca) {
-                ++p;
-                kl = 0;
-            }
+        for (int k = 0; k < nsteps; ++k, walk.next()) {
             const bool built = mbar_wait_warp_ok(&done_bar[k & 3], (k >> 2) & 1);
             const bool landed = mbar_wait_warp_ok(&tma_bar[k % kCStages], (k / kCStages) & 1);
             tc::fence_after();
             live = built && landed && live;
-            ++kl;
             if (!live) continue;  // the CTA has aborted: issue nothing more
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
             const uint32_t sbm = smem_u32(st + kCStB);
-            const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * 16384);
-            // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts;
-            // a piece's first step starts the accumulator afresh
+            const uint32_t sf = smem_u32(sm + kCOffF + (k % kCF) * kCFBytes);
+            // S[n][p_hi | p_lo] += B^T [F_hi | F_lo]: N = 128 over the two adjacent parts,
+            // K = 128 over the two chunks; a piece's first step starts the accumulator afresh
             const uint32_t id4 = tc::idesc_bf16_mn(128, 128, true, true);
-            const uint64_t dB = tc::desc_sw128_mn(sbm, 8192), dF = tc::desc_sw128_mn(sf, 8192);
+            const uint64_t dB = tc::desc_sw128_mn(sbm, 16384), dF = tc::desc_sw128_mn(sf, 16384);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_warp(tmem, dadv(dB, kk * 2048), dadv(dF, kk * 2048), id4,
-                                  (kl > 1 || kk > 0) ? 1u : 0u);
+                                  (walk.j > 0 || kk > 0) ? 1u : 0u);
             tc::mma_commit_warp(&mma_bar[k % kCF]);
             tc::mma_commit_warp(&free_bar[k % kCStages]);
             __syncwarp();
         }
     } else {
-        const int fs = tid >> 3, fp = (tid & 7) * 8;  // F element (s, p..p+7)
+        const int fs = tid >> 2, fp = (tid & 3) * 16;  // F elements (s, p..p+15), s over both chunks
+        const bool in_hi = fs >= kQ;                   // row of the later chunk
+        const int s_in = fs & (kQ - 1);
         const int q4 = warp & 3, cg = warp >> 2;
         const int hn = 32 * q4 + lane, hp = 16 * cg;
-        int p = p0, kl = 0;
         float tailf = 1.f;  // decay of the piece's chunks already walked (later in time)
         for (int k = 0; k < nsteps; ++k) {
             if (k >= kCF) {  // MMA of step k-kCF done: its F buffer is free
@@ -374,23 +385,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_wait_warp(&tma_bar[k % kCStages], (k / kCStages) & 1);
             const unsigned char* st = sm + (k % kCStages) * kCStBytes;
-            const ChunkArr& A = *reinterpret_cast<const ChunkArr*>(st + kCStArr);
-            const float cend = A.cum2[kQ - 1];
-            const float f = tailf * ex2_approx(cend - A.cum2[fs]) * A.w[fs];
-            tailf *= ex2_approx(cend);
-            float v[8];
-            unpack8(*reinterpret_cast<const uint4*>(st + kCStX + chunk_off(fs, fp >> 3)), v);
+            const ChunkArr& Ah = *reinterpret_cast<const ChunkArr*>(st + kCStArr + kArrBytes);
+            const ChunkArr& Al = *reinterpret_cast<const ChunkArr*>(st + kCStArr);
+            const bool lo_ok = walk.lo_ok();
+            const float dec_hi = ex2_approx(Ah.cum2[kQ - 1]);
+            // f_s = exp(s_end - s_s) w_s relative to the end of the piece's later chunks
+            float f;
+            if (in_hi) {
+                f = tailf * ex2_approx(Ah.cum2[kQ - 1] - Ah.cum2[s_in]) * Ah.w[s_in];
+            } else {
+                f = lo_ok ? tailf * dec_hi * ex2_approx(Al.cum2[kQ - 1] - Al.cum2[s_in]) * Al.w[s_in] : 0.f;
+            }
+            tailf *= lo_ok ? dec_hi * ex2_approx(Al.cum2[kQ - 1]) : dec_hi;
+            unsigned char* F = sm + kCOffF + (k % kCF) * kCFBytes;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] *= f;
-            uint4 hi, lo;
-            split8(v, hi, lo);
-            unsigned char* F = sm + kCOffF + (k % kCF) * 16384;
-            *reinterpret_cast<uint4*>(F + chunk_off(fs, fp >> 3)) = hi;
-            *reinterpret_cast<uint4*>(F + 8192 + chunk_off(fs, fp >> 3)) = lo;
+            for (int q = 0; q < 2; ++q) {
+                uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
+                if (in_hi || lo_ok) {  // outside the piece: zeros, whatever x holds there
+                    float v[8];
+                    unpack8(*reinterpret_cast<const uint4*>(st + kCStX + chunk_off(fs, (fp >> 3) + q)), v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] *= f;
+                    split8(v, hi, lo);
+                }
+                *reinterpret_cast<uint4*>(F + chunk_off(fs, (fp >> 3) + q)) = hi;
+                *reinterpret_cast<uint4*>(F + 16384 + chunk_off(fs, (fp >> 3) + q)) = lo;
+            }
             tc::fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&done_bar[k & 3]);
-            if (++kl == pieces[p].ce - pieces[p].ca) {
+            if (walk.j + 1 == walk.steps_of(walk.p)) {
                 // the piece's last step: once its MMA is done, read the state out (the next
                 // piece's first MMA waits for F built after this read)
                 mbar_wait_warp(&mma_bar[k % kCF], (k / kCF) & 1);
@@ -400,16 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 + hp, r2);
                 tc::tmem_wait();
                 tc::fence_before();
-                const int slot = p;
+                const int slot = walk.p;
                 float* dst = cut_state + static_cast<size_t>(slot) * kP * kNs;
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     dst[static_cast<size_t>(hp + j) * kNs + hn] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
                 if (tid == 0) cut_decay[slot] = tailf;
-                ++p;
-                kl = 0;
                 tailf = 1.f;
             }
+            walk.next();
         }
     }
     // a CTA whose waits gave up lets its copies and MMAs in flight finish before the
@@ -730,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 cudaError_t encode_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                      uint64_t d3);
+                      uint64_t d3, unsigned rows = kQ);
 
 long long tc_units(const SsdArgs& a) {
     return static_cast<long long>(a.batch) * a.nheads * ((a.seqlen + kQ - 1) / kQ);
@@ -799,9 +822,13 @@ cudaError_t ssd_tc_launch(const SsdArgs& a, void* workspace, cudaStream_t s) {
     CutPlan plan;
     CutSlots slots;
     if (build_cut_plan(total, nct, nch, &plan) > 0) {
+        SsdMaps cmaps;  // 128-row boxes: two chunks per copy
+        if ((e = encode_4d(&cmaps.x, a.x, kP, H, L, Bt, kCRows)) != cudaSuccess) return e;
+        if ((e = encode_4d(&cmaps.b, a.B, kNs, G, L, Bt, kCRows)) != cudaSuccess) return e;
+        cmaps.c = maps.c;  // (not read by the cuts launch)
         if ((e = set_smem_attr(reinterpret_cast<const void*>(ssd_tc_cuts), kCSmemAlloc)) != cudaSuccess)
             return e;
-        if ((e = launch_dependent(ssd_tc_cuts, plan.ncta, kThreads, kCSmemAlloc, s, maps, a, plan, arrs, cut_state,
+        if ((e = launch_dependent(ssd_tc_cuts, plan.ncta, kThreads, kCSmemAlloc, s, cmaps, a, plan, arrs, cut_state,
                                   cut_decay)) != cudaSuccess)
             return e;
     }
@@ -828,10 +855,10 @@ cudaError_t ssd_tc_take_wait_timeouts(unsigned int* count) {
 
 namespace {
 cudaError_t encode_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                      uint64_t d3) {
-    // [d3][d2][d1][d0] bf16, box {64, 1, 64, 1}, 128-byte swizzle
+                      uint64_t d3, unsigned rows) {
+    // [d3][d2][d1][d0] bf16, box {64, 1, rows, 1}, 128-byte swizzle
     const unsigned long long dims[4] = {d0, d1, d2, d3};
-    const unsigned box[4] = {64, 1, 64, 1};
+    const unsigned box[4] = {64, 1, rows, 1};
     return encode_tmap_nd(map, base, 2, 4, dims, box, true);
 }
 }  // namespace
