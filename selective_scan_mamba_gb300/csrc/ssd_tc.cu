@@ -16,10 +16,11 @@
 //  2. cuts: the (batch, head, chunk) units, taken head-major, are cut into one contiguous,
 //     equal range per SM.  For every range that stops inside a sequence, the local end
 //     state (from zero) over its chunks of that sequence, B^T (f o X) with
-//     f_s = exp(s_range_end - s_s) w_s accumulated in TMEM, and its total decay.
+//     f_s = exp(s_range_end - s_s) w_s accumulated in TMEM, and its total decay; these
+//     cut chunks are dealt out to the CTAs in equal shares (pieces), two chunks a step.
 //  3. main: each CTA walks its range in order with the state in fp32 registers; where the
-//     range starts inside a sequence the state there is h0 decayed through the cuts
-//     before it.  Per chunk, TMA brings x, B, C (bf16, 128-byte swizzle, 3-stage ring)
+//     range starts inside a sequence the state there is h0 folded through the pieces of
+//     the cuts before it.  Per chunk, TMA brings x, B, C (bf16, 128-byte swizzle, 3-stage ring)
 //     and the step quantities; one warp issues tcgen05.mma (kind::f16, bf16 in, fp32
 //     accumulators in TMEM):
 //   MMA1  CB = C . B^T                        M=64  N=64 K=128  C, B K-major (exact bf16)
