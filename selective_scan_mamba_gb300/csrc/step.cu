@@ -604,18 +604,18 @@ __global__ void __launch_bounds__(128) step_scalar(StepArgs a) {
 }
 
 // Mamba-1 form, one token (A per state, P = 1, N = 16): every row is one (batch, channel)
-// with its own Delta, so there is no per-head work to share through a prologue.  Four
-// lanes per row (four states each, one float4), eight rows per warp per pass, UNROLL
-// passes per warp; every load of a pass (state, A, B, C, Delta, x, z, bias, D) is issued
-// before any of them is used, so a warp waits for one memory round trip per pass.
-template <typename Tin, typename Tout, int UNROLL>
+// with its own Delta, so there is no per-head work to share through a prologue.  LPR
+// lanes per row (16 / LPR states each, in float4 groups), 32 / LPR rows per warp per pass,
+// UNROLL passes per warp; every load of a pass (state, A, B, C, Delta, x, z, bias, D) is
+// issued before any of them is used, so a warp waits for one memory round trip per pass.
+template <typename Tin, typename Tout, int LPR, int UNROLL>
 __global__ void __launch_bounds__(kStepThreads, 2) step_m1row(StepArgs a, unsigned rows) {
     // dependent launch: let the next launch be scheduled, then wait for the one before
     // (its writes, for instance this layer's input) before touching global memory
     grid_dep_launch();
     grid_dep_wait();
-    constexpr int N = 16;
-    const int lane = threadIdx.x & 31, sub = lane >> 2, li = lane & 3;
+    constexpr int N = 16, NV = N / LPR / 4, RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
     const unsigned H = static_cast<unsigned>(a.nheads);
     const unsigned per_group = H / static_cast<unsigned>(a.ngroups);
     const Tin* X = static_cast<const Tin*>(a.x);
@@ -624,22 +624,26 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_m1row(StepArgs a, unsign
     const Tin* Bp = static_cast<const Tin*>(a.B);
     const Tin* Cp = static_cast<const Tin*>(a.C);
     const unsigned nwarps = (gridDim.x * blockDim.x) >> 5;
-    const unsigned per_pass = 8u * UNROLL;
+    const unsigned per_pass = RPW * UNROLL;
     for (unsigned base = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * per_pass; base < rows;
          base += nwarps * per_pass) {
-        float4 hv[UNROLL], av[UNROLL];
-        float bv[UNROLL][4], cv[UNROLL][4];
+        float4 hv[UNROLL][NV], av[UNROLL][NV];
+        float bv[UNROLL][NV][4], cv[UNROLL][NV][4];
         float dtr[UNROLL], xr[UNROLL], zr[UNROLL], bias[UNROLL], dsk[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const unsigned r0 = base + u * 8u + sub;
+            const unsigned r0 = base + u * RPW + sub;
             const unsigned r = r0 < rows ? r0 : rows - 1;  // past the end: reread the last row
             const unsigned b = r / H, hd = r - b * H;
-            hv[u] = __ldcs(reinterpret_cast<const float4*>(a.state + static_cast<size_t>(r) * N) + li);
-            av[u] = __ldg(reinterpret_cast<const float4*>(a.A + static_cast<size_t>(hd) * N) + li);
-            const size_t bc = (static_cast<size_t>(b) * a.ngroups + hd / per_group) * N + 4 * li;
-            load4_f32(Bp + bc, bv[u]);
-            load4_f32(Cp + bc, cv[u]);
+            const size_t bc = (static_cast<size_t>(b) * a.ngroups + hd / per_group) * N;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int q = li + v * LPR;  // float4 group of the row: states 4q .. 4q + 3
+                hv[u][v] = __ldcs(reinterpret_cast<const float4*>(a.state + static_cast<size_t>(r) * N) + q);
+                av[u][v] = __ldg(reinterpret_cast<const float4*>(a.A + static_cast<size_t>(hd) * N) + q);
+                load4_f32(Bp + bc + 4 * q, bv[u][v]);
+                load4_f32(Cp + bc + 4 * q, cv[u][v]);
+            }
             dtr[u] = to_f32(DT[r]);
             xr[u] = to_f32(X[r]);
             zr[u] = Z ? to_f32(Z[r]) : 0.f;
@@ -648,25 +652,30 @@ __global__ void __launch_bounds__(kStepThreads, 2) step_m1row(StepArgs a, unsign
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const unsigned r = base + u * 8u + sub;
+            const unsigned r = base + u * RPW + sub;
             const float v = dtr[u] + bias[u];
             const float dt = a.dt_softplus ? softplus_accurate(v) : v;
             const float dx = dt * xr[u];
-            const float A4[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
-            float h4[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
             float acc = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float za = dt * A4[j];
-                const float w = a.disc == SSM_DISC_ZOH ? phi1f(za) : 1.f;
-                h4[j] = expf(za) * h4[j] + (w * dx) * bv[u][j];
-                acc = fmaf(cv[u][j], h4[j], acc);
+            for (int g = 0; g < NV; ++g) {
+                const float A4[4] = {av[u][g].x, av[u][g].y, av[u][g].z, av[u][g].w};
+                float h4[4] = {hv[u][g].x, hv[u][g].y, hv[u][g].z, hv[u][g].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float za = dt * A4[j];
+                    const float w = a.disc == SSM_DISC_ZOH ? phi1f(za) : 1.f;
+                    h4[j] = expf(za) * h4[j] + (w * dx) * bv[u][g][j];
+                    acc = fmaf(cv[u][g][j], h4[j], acc);
+                }
+                hv[u][g] = make_float4(h4[0], h4[1], h4[2], h4[3]);
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (r < rows) {
-                __stcs(reinterpret_cast<float4*>(a.state + static_cast<size_t>(r) * N) + li,
-                       make_float4(h4[0], h4[1], h4[2], h4[3]));
+#pragma unroll
+                for (int g = 0; g < NV; ++g)
+                    __stcs(reinterpret_cast<float4*>(a.state + static_cast<size_t>(r) * N) + li + g * LPR, hv[u][g]);
                 if (li == 0) {
                     float yv = acc + dsk[u] * xr[u];
                     if (Z) yv *= silu_accurate(zr[u]);
@@ -722,15 +731,15 @@ static cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
         }
     }
     if (a.ntok == 1 && a.a_per_state && a.headdim == 1 && a.dstate == 16 && rows < (1LL << 31)) {
-        constexpr int kU = 4;
+        constexpr int kL = 2, kU = 3, kRows = 32 / kL * kU;  // lanes per row, passes, rows per warp
         int dev = 0, sms = 148;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const long long warps = (rows + 8 * kU - 1) / (8 * kU);
+        const long long warps = (rows + kRows - 1) / kRows;
         const long long want = (warps + kStepThreads / 32 - 1) / (kStepThreads / 32);
         const long long grid = want < 2LL * sms ? want : 2LL * sms;  // 2 CTAs per SM resident
-        return launch_dependent(step_m1row<Tin, Tout, kU>, static_cast<unsigned>(grid), kStepThreads, 0, s, a,
-                                static_cast<unsigned>(rows));
+        return launch_dependent(step_m1row<Tin, Tout, kL, kU>, static_cast<unsigned>(grid), kStepThreads, 0, s,
+                                a, static_cast<unsigned>(rows));
     }
     switch (a.dstate) {
         case 16: return launch_vec<Tin, Tout, 1, 4, 4>(a, rows, s);
