@@ -743,9 +743,9 @@ static cudaError_t launch_step_t(const StepArgs& a, cudaStream_t s) {
     }
     switch (a.dstate) {
         case 16: return launch_vec<Tin, Tout, 1, 4, 4>(a, rows, s);
-        case 32: return launch_vec<Tin, Tout, 1, 8, 4>(a, rows, s);
-        case 64: return launch_vec<Tin, Tout, 1, 16, 4>(a, rows, s);
-        case 128: return launch_vec<Tin, Tout, 1, 32, 4>(a, rows, s);
+        case 32: return launch_vec<Tin, Tout, 2, 4, 4>(a, rows, s);
+        case 64: return launch_vec<Tin, Tout, 2, 8, 4>(a, rows, s);
+        case 128: return launch_vec<Tin, Tout, 4, 8, 4>(a, rows, s);
         case 256: return launch_vec<Tin, Tout, 2, 32, 4>(a, rows, s);
         default: {
             const unsigned blocks = static_cast<unsigned>((rows + 127) / 128);
