@@ -334,11 +334,32 @@ __global__ void __launch_bounds__(kBThreads, 4)
             const float2 ac = fma2(make_float2(cv.z, cv.w), h23, mul2(make_float2(cv.x, cv.y), h01));
             float acc = ac.x + ac.y;
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(h[0], h[1], h[2], h[3]);
+            if constexpr (TPC >= 8) {
+                // two butterfly rounds here, the rest summed once per chunk below: the
+                // step loop does not wait on a 32-lane reduction tree every step
+                if (gi == 0) acc += Dd * sm[lay.xs + c * kRow + t];
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if ((gi & 3) == 0) sm[lay.red + (c * kBT + t) * (TPC / 4) + (gi >> 2)] = acc;
+            } else {
 #pragma unroll
-            for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (gi == 0) sm[lay.o + c * kRow + t] = acc + Dd * sm[lay.xs + c * kRow + t];
+                for (int off = 1; off < TPC; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if (gi == 0) sm[lay.o + c * kRow + t] = acc + Dd * sm[lay.xs + c * kRow + t];
+            }
         }
         __syncthreads();
+        if constexpr (TPC >= 8) {  // o_t of every (channel, step) from its TPC / 4 partial sums
+            for (int j = tid; j < CPB * kBT; j += kBThreads) {
+                const int cc = j / kBT, t = j % kBT;
+                if (t >= tl) continue;
+                const float* pr = sm + lay.red + j * (TPC / 4);
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < TPC / 4; ++q) sum += pr[q];
+                sm[lay.o + cc * kRow + t] = sum;
+            }
+            __syncthreads();
+        }
         // dC_t[n] = sum over the CTA's channels of do_t h_t[n]; dz from the pre-gate output
         channel_sum(lay.dout, a.dC, t0, tl);
         if (a.dz) {
@@ -391,20 +412,54 @@ __global__ void __launch_bounds__(kBThreads, 4)
             float gx = (gx2.x + gx2.y) * dl, gd = gd2.x + gd2.y;
             const float Gt[kBS] = {G2[0].x, G2[0].y, G2[1].x, G2[1].y};
             *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(Gt[0], Gt[1], Gt[2], Gt[3]);
+            if constexpr (TPC >= 8) {
+                // three butterfly rounds here, the rest summed once per chunk below
+                if (gi == 0) gx += dov * Dd;
 #pragma unroll
-            for (int off = 1; off < TPC; off <<= 1) {
-                gx += __shfl_xor_sync(0xffffffffu, gx, off);
-                gd += __shfl_xor_sync(0xffffffffu, gd, off);
-            }
-            if (gi == 0) {
-                const float dv = gd * sm[lay.sg + c * kRow + t];
-                sm[lay.gx + c * kRow + t] = gx + dov * Dd;
-                sm[lay.gd + c * kRow + t] = dv;
-                dDacc += dov * xv;
-                dbacc += dv;
+                for (int off = 1; off < 8; off <<= 1) {
+                    gx += __shfl_xor_sync(0xffffffffu, gx, off);
+                    gd += __shfl_xor_sync(0xffffffffu, gd, off);
+                }
+                if ((gi & 7) == 0)
+                    *reinterpret_cast<float2*>(sm + lay.red + ((c * kBT + t) * (TPC / 8) + (gi >> 3)) * 2) =
+                        make_float2(gx, gd);
+            } else {
+#pragma unroll
+                for (int off = 1; off < TPC; off <<= 1) {
+                    gx += __shfl_xor_sync(0xffffffffu, gx, off);
+                    gd += __shfl_xor_sync(0xffffffffu, gd, off);
+                }
+                if (gi == 0) {
+                    const float dv = gd * sm[lay.sg + c * kRow + t];
+                    sm[lay.gx + c * kRow + t] = gx + dov * Dd;
+                    sm[lay.gd + c * kRow + t] = dv;
+                    dDacc += dov * xv;
+                    dbacc += dv;
+                }
             }
         }
         __syncthreads();
+        if constexpr (TPC >= 8) {  // dx and d(delta) of every (channel, step) from the partials
+            for (int j = tid; j < CPB * kBT; j += kBThreads) {
+                const int cc = j / kBT, t = j % kBT;
+                if (t >= tl) continue;
+                const float2* pr = reinterpret_cast<const float2*>(sm + lay.red) + j * (TPC / 8);
+                float sx = 0.f, sd = 0.f;
+#pragma unroll
+                for (int q = 0; q < TPC / 8; ++q) {
+                    sx += pr[q].x;
+                    sd += pr[q].y;
+                }
+                sm[lay.gx + cc * kRow + t] = sx;
+                sm[lay.gd + cc * kRow + t] = sd * sm[lay.sg + cc * kRow + t];
+            }
+            __syncthreads();
+            if (gi == 0)  // the channel's dD and d(bias) terms of this chunk
+                for (int t = 0; t < tl; ++t) {
+                    dDacc += sm[lay.dout + c * kRow + t] * sm[lay.xs + c * kRow + t];
+                    dbacc += sm[lay.gd + c * kRow + t];
+                }
+        }
         // dB_t[n] = sum over the CTA's channels of G_t[n] Delta_t x_t
         channel_sum(lay.dlx, a.dB, t0, tl);
         for (int j = tid; j < CPB * kBT; j += kBThreads) {
