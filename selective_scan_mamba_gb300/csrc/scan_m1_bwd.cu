@@ -51,18 +51,20 @@ namespace ssm {
 namespace {
 
 constexpr int kBT = 16;          // steps per chunk
-constexpr int kBThreads = 128;   // threads per CTA (four CTAs per SM)
+// threads per CTA: 128 (four CTAs per SM); 256 at 32 threads per channel (the SSD view at
+// dstate 128), where each CTA's dB/dC atomic adds then cover twice the channels
+__host__ __device__ constexpr int bwd_threads(int tpc) { return tpc == 32 ? 256 : 128; }
 constexpr int kBS = 4;           // states per thread
 constexpr int kRow = kBT + 1;    // padded row of the per-(channel, step) tiles
 
 struct BwdLayout {  // float offsets into dynamic shared memory (16-byte aligned blocks)
     int h, bs, cs, red, dl, dlx, xs, dout, o, sg, zz, gx, gd, total;
-    __host__ __device__ BwdLayout(int cpb, int n) {
-        h = 0;                                  // [kBT][kBThreads][kBS]: h_t, then G_t
-        bs = h + kBT * kBThreads * kBS;         // [kBT][n] B
+    __host__ __device__ BwdLayout(int cpb, int n, int nt) {
+        h = 0;                                  // [kBT][nt][kBS]: h_t, then G_t
+        bs = h + kBT * nt * kBS;                // [kBT][n] B
         cs = bs + kBT * n;                      // [kBT][n] C
-        red = cs + kBT * n;                     // [kBThreads][4] partial sums over channels
-        dl = red + kBThreads * 4;               // [cpb][kRow] Delta
+        red = cs + kBT * n;                     // [nt][4] partial sums over channels
+        dl = red + nt * 4;                      // [cpb][kRow] Delta
         dlx = dl + cpb * kRow;                  // Delta x
         xs = dlx + cpb * kRow;                  // x
         dout = xs + cpb * kRow;                 // dL/do
@@ -105,7 +107,7 @@ __device__ __forceinline__ void red_add4(float* p, long long stride, float4 v) {
     }
 }
 
-__host__ __device__ inline int bwd_cpb(int tpc) { return kBThreads / tpc; }
+__host__ __device__ inline int bwd_cpb(int tpc) { return bwd_threads(tpc) / tpc; }
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p, size_t i) {
@@ -133,15 +135,15 @@ struct BwdView {
 
 namespace {
 
-template <typename Tin, typename Tdy, int TPC>
-__global__ void __launch_bounds__(kBThreads, 4)
+template <typename Tin, typename Tdy, int TPC, int NT = bwd_threads(TPC)>
+__global__ void __launch_bounds__(NT, 512 / NT)
     m1_scan_bwd(BwdView a, int cps, int kb, float* ckpt, float* fine, float* part_a, float* part_d,
                 float* part_bias) {
     constexpr int N = TPC * kBS;
-    constexpr int CPB = kBThreads / TPC;
+    constexpr int CPB = NT / TPC;
     constexpr int NQ = kBT * N / 4;         // (step, 4 states) cells of a chunk
     // channel slices summed in parallel per cell (1: each thread sums whole cells)
-    constexpr int SPLIT = NQ < kBThreads ? kBThreads / NQ : 1;
+    constexpr int SPLIT = NQ < NT ? NT / NQ : 1;
     const int L = a.seqlen, Dm = a.dim, G = a.ngroups;
     const int per_group = Dm / G;
     const int pair = blockIdx.x / cps, part_i = blockIdx.x % cps;
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
     const int nblk = (nch + kb - 1) / kb;  // kb: chunks per checkpoint block
 
     extern __shared__ __align__(16) float sm[];
-    const BwdLayout lay(CPB, N);
+    const BwdLayout lay(CPB, N, NT);
     float* hbuf = sm + lay.h;
     const int tid = threadIdx.x;
     const int c = tid / TPC, gi = tid % TPC;
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
     // element (b, channel cc of the CTA, step t) of x, z, dy, dx, dz and of delta
     // head of each of the CTA's channels (the channel itself when hp = 1), once
     __shared__ int s_head[CPB];
-    for (int cc = tid; cc < CPB; cc += kBThreads) s_head[cc] = (d0 + cc) / a.hp;
+    for (int cc = tid; cc < CPB; cc += NT) s_head[cc] = (d0 + cc) / a.hp;
     __syncthreads();
     auto xi = [&](int cc, int t) { return b * a.sxb + (d0 + cc) * a.sxd + t * a.sxt; };
     auto di = [&](int cc, int t) { return b * a.sdb + s_head[cc] * a.sdh + t * a.sdt; };
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
     // stage Delta (and Delta x, x, sigmoid, dL/do, z) of the CTA's channels and B (C)
     // for a chunk
     auto stage = [&](int t0, int tl, bool full) {
-        for (int j = tid; j < CPB * kBT; j += kBThreads) {
+        for (int j = tid; j < CPB * kBT; j += NT) {
             const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
             float dl = 0.f, xv = 0.f, sgv = 1.f, dov = 0.f, zv = 0.f;
             if (cc < nchan && t < tl) {
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
                 sm[lay.zz + cc * kRow + t] = zv;
             }
         }
-        for (int j = tid; j < N * kBT; j += kBThreads) {
+        for (int j = tid; j < N * kBT; j += NT) {
             const int n = bt_fast ? j / kBT : j % N, t = bt_fast ? j % kBT : j / N;
             const long long i = bc_base + n * a.sbn + (t0 + t) * a.sbt;
             sm[lay.bs + t * N + n] = t < tl ? ldf(Bp, i) : 0.f;
@@ -226,14 +228,14 @@ __global__ void __launch_bounds__(kBThreads, 4)
     // the chunk, added into dst (dB or dC) at step t0 + t: cell q = (t, 4 states) per
     // thread slice, SPLIT slices of the channels, then the slices added
     auto channel_sum = [&](int wofs, float* dst, int t0, int tl) {
-      for (int q0 = 0; q0 < (NQ > kBThreads ? NQ : 1); q0 += kBThreads) {
-        const int q = NQ > kBThreads ? q0 + tid : tid % NQ, sl = NQ > kBThreads ? 0 : tid / NQ;
+      for (int q0 = 0; q0 < (NQ > NT ? NQ : 1); q0 += NT) {
+        const int q = NQ > NT ? q0 + tid : tid % NQ, sl = NQ > NT ? 0 : tid / NQ;
         const int t = q / (N / 4), n4 = q % (N / 4);
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < tl) {
             for (int cc = sl; cc < nchan; cc += SPLIT) {
                 const float w = sm[wofs + cc * kRow + t];
-                const float4 v = *reinterpret_cast<const float4*>(hbuf + (t * kBThreads + cc * TPC + n4) * kBS);
+                const float4 v = *reinterpret_cast<const float4*>(hbuf + (t * NT + cc * TPC + n4) * kBS);
                 s.x += w * v.x;
                 s.y += w * v.y;
                 s.z += w * v.z;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
             h[0] = h01.x; h[1] = h01.y; h[2] = h23.x; h[3] = h23.y;
             const float2 ac = fma2(make_float2(cv.z, cv.w), h23, mul2(make_float2(cv.x, cv.y), h01));
             float acc = ac.x + ac.y;
-            *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4*>(hbuf + (t * NT + tid) * kBS) = make_float4(h[0], h[1], h[2], h[3]);
             if constexpr (TPC >= 8) {
                 // two butterfly rounds here, the rest summed once per chunk below: the
                 // step loop does not wait on a 32-lane reduction tree every step
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
         __syncthreads();
         if constexpr (TPC >= 8) {  // o_t of every (channel, step) from its TPC / 4 partial sums
-            for (int j = tid; j < CPB * kBT; j += kBThreads) {
+            for (int j = tid; j < CPB * kBT; j += NT) {
                 const int cc = j / kBT, t = j % kBT;
                 if (t >= tl) continue;
                 const float* pr = sm + lay.red + j * (TPC / 4);
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         // dC_t[n] = sum over the CTA's channels of do_t h_t[n]; dz from the pre-gate output
         channel_sum(lay.dout, a.dC, t0, tl);
         if (a.dz) {
-            for (int j = tid; j < CPB * kBT; j += kBThreads) {
+            for (int j = tid; j < CPB * kBT; j += NT) {
                 const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
                 if (cc >= nchan || t >= tl) continue;
                 const long long i = xi(cc, t0 + t);
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         for (int t = tl - 1; t >= 0; --t) {
             float hp[kBS];
             if (t > 0) {
-                const float4 v = *reinterpret_cast<const float4*>(hbuf + ((t - 1) * kBThreads + tid) * kBS);
+                const float4 v = *reinterpret_cast<const float4*>(hbuf + ((t - 1) * NT + tid) * kBS);
                 hp[0] = v.x; hp[1] = v.y; hp[2] = v.z; hp[3] = v.w;
             } else {
 #pragma unroll
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
             }
             float gx = (gx2.x + gx2.y) * dl, gd = gd2.x + gd2.y;
             const float Gt[kBS] = {G2[0].x, G2[0].y, G2[1].x, G2[1].y};
-            *reinterpret_cast<float4*>(hbuf + (t * kBThreads + tid) * kBS) = make_float4(Gt[0], Gt[1], Gt[2], Gt[3]);
+            *reinterpret_cast<float4*>(hbuf + (t * NT + tid) * kBS) = make_float4(Gt[0], Gt[1], Gt[2], Gt[3]);
             if constexpr (TPC >= 8) {
                 // three butterfly rounds here, the rest summed once per chunk below
                 if (gi == 0) gx += dov * Dd;
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
         __syncthreads();
         if constexpr (TPC >= 8) {  // dx and d(delta) of every (channel, step) from the partials
-            for (int j = tid; j < CPB * kBT; j += kBThreads) {
+            for (int j = tid; j < CPB * kBT; j += NT) {
                 const int cc = j / kBT, t = j % kBT;
                 if (t >= tl) continue;
                 const float2* pr = reinterpret_cast<const float2*>(sm + lay.red) + j * (TPC / 8);
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
         }
         // dB_t[n] = sum over the CTA's channels of G_t[n] Delta_t x_t
         channel_sum(lay.dlx, a.dB, t0, tl);
-        for (int j = tid; j < CPB * kBT; j += kBThreads) {
+        for (int j = tid; j < CPB * kBT; j += NT) {
             const int cc = tfast ? j / kBT : j % CPB, t = tfast ? j % kBT : j / CPB;
             if (cc >= nchan || t >= tl) continue;
             a.dx[xi(cc, t0 + t)] = sm[lay.gx + cc * kRow + t];
@@ -564,7 +566,7 @@ cudaError_t launch_bwd(const BwdView& a, void* ws, cudaStream_t s) {
     const int cps = bwd_cps(a);
     const BwdWs w = bwd_ws(a);
     unsigned char* base = static_cast<unsigned char*>(ws);
-    const BwdLayout lay(bwd_cpb(TPC), TPC * kBS);
+    const BwdLayout lay(bwd_cpb(TPC), TPC * kBS, bwd_threads(TPC));
     const size_t smem = static_cast<size_t>(lay.total) * sizeof(float);
     auto k = m1_scan_bwd<Tin, Tdy, TPC>;
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(k), static_cast<int>(smem));
@@ -583,7 +585,7 @@ cudaError_t launch_bwd(const BwdView& a, void* ws, cudaStream_t s) {
     float* part_d = reinterpret_cast<float*>(base + w.part_d);
     float* part_bias = reinterpret_cast<float*>(base + w.part_bias);
     if (grid > 0)
-        k<<<grid, kBThreads, smem, s>>>(a, cps, bwd_kb(a), reinterpret_cast<float*>(base + w.ckpt),
+        k<<<grid, bwd_threads(TPC), smem, s>>>(a, cps, bwd_kb(a), reinterpret_cast<float*>(base + w.ckpt),
                                         reinterpret_cast<float*>(base + w.fine), part_a, part_d, part_bias);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
