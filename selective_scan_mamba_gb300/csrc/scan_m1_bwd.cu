@@ -13,7 +13,8 @@
 //   dA[n] += G_t h_{t-1} E_t Delta_t,   g <- G_t E_t,   d(delta)_t = dDelta_t sigmoid(v_t).
 //
 // One launch computes everything per CTA, then a small launch sums the per-row partials:
-//   - a CTA owns NT / TPC channels of one (batch, group) (TPC threads per channel, four
+//   - a CTA of NT threads (128; 256 at 32 threads per channel) owns NT / TPC channels of one
+//     (batch, group) (TPC threads per channel, four
 //     consecutive states per thread);
 //   - the sequence is cut into 16-step chunks and the chunks into blocks of K chunks:
 //     K = 1 while a checkpoint per chunk takes no more room than x and dy (N <= 16 in
