@@ -44,6 +44,10 @@ cudaError_t m1_bwd_launch(const M1BwdArgs& a, void* workspace, cudaStream_t s);
 bool ssd_bwd_supported(const ssd_bwd_params& a);
 size_t ssd_bwd_workspace_size(const ssd_bwd_params& a);
 cudaError_t ssd_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_t s);
+// the same derivative in chunked form (ssd_bwd.cu), for the shapes it covers
+bool ssd_chunked_bwd_supported(const ssd_bwd_params& a);
+size_t ssd_chunked_bwd_workspace_size(const ssd_bwd_params& a);
+cudaError_t ssd_chunked_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_t s);
 
 // Mamba-3 complex scan (scan_m3.cu)
 bool m3_supported(int dstate);

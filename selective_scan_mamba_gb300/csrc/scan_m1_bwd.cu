@@ -671,12 +671,15 @@ bool ssd_bwd_supported(const ssd_bwd_params& a) {
     return a.fwd.disc == SSM_DISC_EXP_EULER && bwd_tpc(a.fwd.dstate) > 0;
 }
 
+// The chunked form (ssd_bwd.cu) where it covers the shape, else the tied recurrence.
 size_t ssd_bwd_workspace_size(const ssd_bwd_params& a) {
     if (!ssd_bwd_supported(a)) return 0;
+    if (ssd_chunked_bwd_supported(a)) return ssd_chunked_bwd_workspace_size(a);
     return bwd_ws(view_ssd(a)).bytes;
 }
 
 cudaError_t ssd_bwd_launch(const ssd_bwd_params& a, void* workspace, cudaStream_t s) {
+    if (ssd_chunked_bwd_supported(a)) return ssd_chunked_bwd_launch(a, workspace, s);
     return bwd_launch(view_ssd(a), workspace, s);
 }
 

@@ -528,11 +528,31 @@ def test_ssd_bwd_rejects_bad_arguments(lib, kw, status):
     assert lib.ssm_last_error()
 
 
+def chunked_bwd_workspace_bytes(batch, L, H, P, N, es=2):
+    """The chunked SSD backward's scratch: chunk states and adjoints ([P][N] float32 per
+    64-step chunk) for one slice of (batch, head) sequences, the slice as large as fits
+    in the bytes of x and dy and then evened out over the slices; a chunk sum of dt A and
+    three per-chunk partial sums for every sequence; each part rounded up to 256 bytes."""
+    r256 = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    nch, seqs = -(-L // 64), batch * H
+    nq = min(seqs, max(1, (2 * batch * L * H * P * es) // (2 * nch * P * N * 4)))
+    slices = -(-seqs // nq)
+    nq = -(-seqs // slices)
+    return 2 * r256(nq * nch * P * N * 4) + r256(seqs * nch * 4) + r256(3 * seqs * nch * 4)
+
+
 def test_ssd_bwd_workspace_size(lib):
-    p = ssd_bwd_params()
+    p = ssd_bwd_params()  # dstate 128, headdim 64: the chunked form
     need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
-    assert need == bwd_workspace_bytes(2 * 4 * 64, 128, 64)
+    assert need == chunked_bwd_workspace_bytes(2, 64, 4, 64, 128)
     assert lib.ssd_scan_bwd(ctypes.byref(p), fake(30), need - 1, None) == _lib.SSM_ERR_INVALID_ARG
+    p = ssd_bwd_params(fwd_headdim=16)  # outside the chunked form's shapes: the tied recurrence
+    need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
+    assert need == bwd_workspace_bytes(2 * 4 * 16, 128, 64)
+    p = ssd_bwd_params(fwd_batch=3, fwd_seqlen=1000, fwd_nheads=5, fwd_in_dtype=_lib.SSM_F32,
+                       fwd_out_dtype=_lib.SSM_F32)
+    need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
+    assert need == chunked_bwd_workspace_bytes(3, 1000, 5, 64, 128, es=4)
 
 
 def test_backward_workspace_at_most_the_inputs(lib):

@@ -63,3 +63,21 @@ def test_long_sequence_checkpoint_blocks(oracle_mod):
     """1000 steps: 63 chunks in 8 checkpoint blocks of 8, the last one short; dstate 128
     with two heads sharing one group."""
     _run(oracle_mod, 1, 1000, 2, 16, 128, 1, synth.BF16, seed=4)
+
+
+def test_chunked_form_ragged_groups(oracle_mod):
+    """The chunked form (dstate 128, headdim 64): 1000 steps (15 full chunks and a ragged
+    one), two groups of two heads, h0 and dh_final, the (batch, head) sequences spread
+    over several slices of the workspace."""
+    _run(oracle_mod, 2, 1000, 4, 64, 128, 2, synth.BF16, seed=5)
+
+
+@pytest.mark.parametrize("N,P", [(64, 64), (128, 32)])
+def test_chunked_form_fp32_gated(oracle_mod, N, P):
+    """float32 inputs and dy through the chunked form, with the gate and a short tail."""
+    _run(oracle_mod, 2, 300, 3, P, N, 1, synth.F32, seed=6)
+
+
+def test_chunked_form_single_step(oracle_mod):
+    """One step: a chunk with 63 padded steps."""
+    _run(oracle_mod, 1, 1, 2, 64, 64, 1, synth.BF16, seed=7)
