@@ -780,7 +780,8 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
     upd_sb = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
     out["ssd_130m_bwd"] = {"ms": tsb * 1e3, "state_updates_per_s": upd_sb / tsb,
                            "workspace_bytes": sbws.numel(),
-                           "note": "x, dt, B, C, dy bf16 in; every gradient float32 out"}
+                           "note": "x, dt, B, C, dy bf16 in; every gradient float32 out; "
+                                   "chunked form (64-step chunks, float32 products)"}
     del sb, sb_dy, sbws
     # Mamba-3 scan on the 130m layer shape (complex states, trapezoid weight lam)
     m3sets = []
@@ -962,7 +963,8 @@ def bench_reference(args, rank, world):
 def run_case(args):
     """Runs one kernel workload --warmup + --steps times with no timing (for profiler
     captures): m1 (130m layer), m1_long (790m, L 32768), ssd64 / ssd256 (130m SSD),
-    step (780m decode)."""
+    step (780m decode), bwd / ssd_bwd (the backwards on the 130m shapes) and the others
+    named in --case."""
     import torch
     import selective_scan_mamba_gb300 as ssm
     torch.cuda.set_device(0)
@@ -1017,6 +1019,14 @@ def run_case(args):
         for _ in range(n):
             ssm.ssm_scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], dy, D=t["D"], z=t["z"],
                              delta_bias=t["delta_bias"])
+    elif args.case == "ssd_bwd":  # SSD backward, 130m SSD shape
+        cfg = synth.WORKLOADS["ssd_130m"]
+        inp = synth.ssd(cfg["batch"], cfg["seqlen"], cfg["nheads"], cfg["headdim"], cfg["dstate"],
+                        cfg["ngroups"], dtype=cfg["dtype"], delta_scale=cfg["delta_scale"], seed=60)
+        t = _dev(inp, torch)
+        dy = torch.randn(t["x"].shape, device="cuda").to(torch.bfloat16)
+        for _ in range(n):
+            ssm.ssd_scan_bwd(t["x"], t["dt"], t["A"], t["B"], t["C"], dy, D=t["D"], dt_bias=t["dt_bias"])
     elif args.case == "m3":  # Mamba-3 scan, 130m layer shape
         cfg = synth.WORKLOADS["m1_130m_layer"]
         inp = synth.mamba1(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["seqlen"], dtype=cfg["dtype"],
@@ -1073,7 +1083,7 @@ def main():
     ap.add_argument("--e2e-sets", type=int, default=3,
                     help="device buffer sets the end-to-end leg rotates through (>= 2)")
     ap.add_argument("--case", choices=["m1", "m1_long", "ssd64", "ssd256", "step", "step_m1", "tokens",
-                                       "bwd", "m3", "s4d", "s4d_conv"],
+                                       "bwd", "ssd_bwd", "m3", "s4d", "s4d_conv"],
                     help="run one kernel workload untimed (for profiler captures) and exit")
     args = ap.parse_args()
     if args.case:

@@ -459,6 +459,11 @@ ssm_status ssm_state_update_tokens(const ssm_step_params* p, int ntokens, void* 
  * head's channels).  The derivative is of the recurrence, so it does not depend on the
  * chunk size of the forward call (fwd.chunk_size, y and h_final are ignored).
  *
+ * For (dstate, headdim) in {(128, 64), (64, 64), (128, 32), (64, 32)} with in_dtype ==
+ * out_dtype the library computes it in chunked form (64-step chunks, the pages' chunked
+ * SSD differentiated product by product, float32 arithmetic); other shapes run the
+ * tied recurrence.  Both give the same gradients to float32 rounding.
+ *
  * Shapes as ssd_chunk_scan_fwd; every gradient is float32 and is written:
  *   dy          : [Bt, L, H, P]  fwd.out_dtype
  *   dh_final    : [Bt, H, P, N]  (nullable: zero)
@@ -487,9 +492,13 @@ typedef struct {
     float* dh0;
 } ssd_bwd_params;
 
-/* Device scratch for ssd_scan_bwd in bytes (0 when invalid or unsupported): as for
- * ssm_scan_bwd.  ddt, like dB and dC, is a sum over channels (the head's P) added up
- * with float32 atomic adds; dA, dD_skip, ddt_bias are summed in a fixed order. */
+/* Device scratch for ssd_scan_bwd in bytes (0 when invalid or unsupported).  Chunked
+ * form: the chunk states and adjoints of a slice of (batch, head) sequences, the slice
+ * no larger than x and dy together, plus a few floats per chunk; dB and dC are sums over
+ * a group's heads added up with float32 atomic adds, ddt is written once.  Tied
+ * recurrence: as for ssm_scan_bwd, and ddt, like dB and dC, is a sum over channels (the
+ * head's P) added up with atomic adds.  dA, dD_skip, ddt_bias are summed in a fixed
+ * order in both. */
 size_t ssd_scan_bwd_workspace_size(const ssd_bwd_params* p);
 
 ssm_status ssd_scan_bwd(const ssd_bwd_params* p, void* workspace, size_t workspace_bytes,

@@ -462,7 +462,9 @@ def _ssd_params(x, dt, A, B, C, chunk_size, D, z, dt_bias, dt_softplus, h0, y, h
 
 def ssd_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, dt_softplus=True, h0=None,
                  dh_final=None, *, return_dh0=True, workspace=None, stream=None):
-    """Backward of the SSD scan (exponential-Euler, dstate 16, 32, 64 or 128).
+    """Backward of the SSD scan (exponential-Euler, dstate 16, 32, 64 or 128; in chunked
+    form for (dstate, headdim) in {(128, 64), (64, 64), (128, 32), (64, 32)} when dy has
+    x's dtype, else as the tied recurrence).
 
     Same inputs as ssd_chunk_scan_fwd plus dy [batch, L, H, P] and the optional dh_final
     [batch, H, P, N] float32.  Returns a dict of float32 gradients: dx [batch, L, H, P],
@@ -505,14 +507,17 @@ def ssd_scan_bwd(x, dt, A, B, C, dy, D=None, z=None, dt_bias=None, dt_softplus=T
 
 
 def ssd_scan_bwd_workspace_size(x, B, dy_dtype=None) -> int:
-    """Scratch bytes ssd_scan_bwd needs for these shapes (0 if unsupported)."""
+    """Scratch bytes ssd_scan_bwd needs for these shapes (0 if unsupported); dy_dtype
+    defaults to x's dtype."""
     p = _lib.SsdBwdParams()
     p.fwd.batch, p.fwd.seqlen, p.fwd.nheads, p.fwd.headdim = x.shape
     p.fwd.ngroups, p.fwd.dstate = B.shape[2], B.shape[3]
     p.fwd.chunk_size = 64
     p.fwd.in_dtype = _dtype_code(x)
-    p.fwd.out_dtype = (_lib.SSM_F32 if dy_dtype is not None and dy_dtype == _torch().float32
-                       else _lib.SSM_BF16)
+    if dy_dtype is None:
+        p.fwd.out_dtype = p.fwd.in_dtype
+    else:
+        p.fwd.out_dtype = _lib.SSM_F32 if dy_dtype == _torch().float32 else _lib.SSM_BF16
     return int(lib().ssd_scan_bwd_workspace_size(ctypes.byref(p)))
 
 

@@ -47,7 +47,14 @@ namespace ssm {
 namespace {
 
 constexpr int kQ = 64;     // steps per chunk
-constexpr int kNT = 256;   // threads per CTA of the chunk launches
+#ifndef SSD_BWD_THREADS
+#define SSD_BWD_THREADS 256
+#endif
+#ifndef SSD_BWD_UNROLL
+#define SSD_BWD_UNROLL 8
+#endif
+constexpr int kNT = SSD_BWD_THREADS;  // threads per CTA of the chunk launches
+constexpr int kUnroll = SSD_BWD_UNROLL;  // unrolling of the products' inner loop
 constexpr int kSQ = kQ + 1;
 
 struct CkArgs {
@@ -143,7 +150,7 @@ template <int I, int J, int K, typename FA, typename FB>
 __device__ __forceinline__ void mac(const Tile<I, J>& t, float (&acc)[Tile<I, J>::TI][Tile<I, J>::TJ], FA a,
                                     FB b) {
     constexpr int TI = Tile<I, J>::TI, TJ = Tile<I, J>::TJ;
-#pragma unroll 4
+#pragma unroll kUnroll
     for (int k = 0; k < K; ++k) {
         float av[TI], bv[TJ];
 #pragma unroll
