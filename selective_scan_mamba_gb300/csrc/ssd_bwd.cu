@@ -34,9 +34,11 @@
 //      and dx are written once, dA, dD and ddt_bias per-chunk partials go to the
 //      workspace; after the last slice a small launch sums them in a fixed order.
 // Each chunk launch runs one CTA of 256 threads per chunk with the chunk's operands in
-// shared memory as float32 (rows padded to an odd length so that row and column walks
-// are free of bank conflicts); a product of an I x K by a K x J operand gives each thread
-// a tile of I J / 256 outputs.
+// shared memory as float32.  Each product is laid out so that both of its operands are
+// read with 16-byte loads: every operand is stored with either the contraction index or
+// the output index contiguous, whichever the product needs (C is kept both ways in the
+// gradient launch); a thread computes a 4 x TJ tile (4 x 8 lanes per warp) and takes four
+// steps of the contraction per load.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -55,7 +57,7 @@ constexpr int kQ = 64;     // steps per chunk
 #endif
 constexpr int kNT = SSD_BWD_THREADS;  // threads per CTA of the chunk launches
 constexpr int kUnroll = SSD_BWD_UNROLL;  // unrolling of the products' inner loop
-constexpr int kSQ = kQ + 1;
+constexpr int kLQ = kQ + 4;  // row length of the Q x Q operands
 
 struct CkArgs {
     int batch, seqlen, nheads, hpg, ngroups, nch;  // hpg: heads per group
@@ -129,57 +131,208 @@ __device__ __forceinline__ void chunk_steps(const CkArgs& a, int b, int hd, int 
     scum[lane + 32] = first + v[1];
 }
 
-// A thread's share of an I x J product: rows i0 .. i0 + TI - 1, columns j0 + q NJ
-// (q < TJ), so that the threads of a warp cover consecutive columns.
-template <int I, int J>
-struct Tile {
-    static constexpr int C = I * J / kNT;
-    static constexpr int TI = C >= 4 ? 4 : C;
-    static constexpr int TJ = C / TI;
-    static constexpr int NJ = J / TJ;
-    static_assert(I * J % kNT == 0 && C >= 1 && I % TI == 0 && J % TJ == 0 && (I / TI) * NJ == kNT,
-                  "tile shape");
-    int i0, j0;
-    __device__ __forceinline__ Tile() : i0((static_cast<int>(threadIdx.x) / NJ) * TI), j0(threadIdx.x % NJ) {}
-    __device__ __forceinline__ int row(int r) const { return i0 + r; }
-    __device__ __forceinline__ int col(int q) const { return j0 + q * NJ; }
+// Operand layouts in shared memory, rows padded to width + 4 floats (16-byte aligned, and
+// successive rows start four banks apart):
+//   KC: the contraction index k is contiguous (element (x, k) at x * ld + k);
+//   XC: the other index is contiguous (element (x, k) at k * ld + x).
+enum Lay { KC = 0, XC = 1 };
+
+// A thread's share of an I x J product.  Warp w covers rows 16 (w / WJ) .. + 15 and
+// columns 8 TJ (w % WJ) .. + 8 TJ - 1; lane 8 ti + tj holds 4 rows and TJ columns, spread
+// so that every 16-byte load of a warp touches each bank at most once: rows ti + 4 r (A
+// in KC) or 4 ti + r (A in XC), columns tj + 8 q (B in KC) or 4 tj + 32 (q / 4) + q % 4
+// (B in XC; 2 tj + q when TJ = 2).
+template <int I, int J, Lay LA, Lay LB>
+struct Frag {
+    static constexpr int TJ = I * J / (kNT * 4);
+    static constexpr int WJ = J / (8 * TJ);
+    static_assert(I % 16 == 0 && (TJ == 2 || TJ % 4 == 0) && (I / 16) * WJ * 32 == kNT, "fragment shape");
+    int ib, jb, ti, tj;
+    __device__ __forceinline__ Frag() {
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        ib = (w / WJ) * 16;
+        jb = (w % WJ) * 8 * TJ;
+        ti = l >> 3;
+        tj = l & 7;
+    }
+    __device__ __forceinline__ int row(int r) const { return LA == KC ? ib + ti + 4 * r : ib + 4 * ti + r; }
+    __device__ __forceinline__ int col(int q) const {
+        if (LB == KC) return jb + tj + 8 * q;
+        if (TJ == 2) return jb + 2 * tj + q;
+        return jb + 4 * tj + 32 * (q / 4) + q % 4;
+    }
 };
 
-// acc[r][q] += sum_k a(row r, k) b(k, col q)
-template <int I, int J, int K, typename FA, typename FB>
-__device__ __forceinline__ void mac(const Tile<I, J>& t, float (&acc)[Tile<I, J>::TI][Tile<I, J>::TJ], FA a,
-                                    FB b) {
-    constexpr int TI = Tile<I, J>::TI, TJ = Tile<I, J>::TJ;
+// acc[r][q] += sum_k A(row r, k) B(col q, k), four k per step, 16-byte (8-byte) loads
+template <int K, int I, int J, Lay LA, Lay LB>
+__device__ __forceinline__ void mac(const Frag<I, J, LA, LB>& f, float (&acc)[4][Frag<I, J, LA, LB>::TJ],
+                                    const float* A, int lda, const float* B, int ldb) {
+    constexpr int TJ = Frag<I, J, LA, LB>::TJ;
+    static_assert(K % 4 == 0, "contraction length");
 #pragma unroll kUnroll
-    for (int k = 0; k < K; ++k) {
-        float av[TI], bv[TJ];
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float a[4][4], b[4][TJ];  // [k - k0][r], [k - k0][q]
+        if constexpr (LA == KC) {
 #pragma unroll
-        for (int r = 0; r < TI; ++r) av[r] = a(t.row(r), k);
+            for (int r = 0; r < 4; ++r) {
+                const float4 v = *reinterpret_cast<const float4*>(A + f.row(r) * lda + k0);
+                a[0][r] = v.x;
+                a[1][r] = v.y;
+                a[2][r] = v.z;
+                a[3][r] = v.w;
+            }
+        } else {
 #pragma unroll
-        for (int q = 0; q < TJ; ++q) bv[q] = b(k, t.col(q));
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 v = *reinterpret_cast<const float4*>(A + (k0 + kk) * lda + f.row(0));
+                a[kk][0] = v.x;
+                a[kk][1] = v.y;
+                a[kk][2] = v.z;
+                a[kk][3] = v.w;
+            }
+        }
+        if constexpr (LB == KC) {
 #pragma unroll
-        for (int r = 0; r < TI; ++r)
+            for (int q = 0; q < TJ; ++q) {
+                const float4 v = *reinterpret_cast<const float4*>(B + f.col(q) * ldb + k0);
+                b[0][q] = v.x;
+                b[1][q] = v.y;
+                b[2][q] = v.z;
+                b[3][q] = v.w;
+            }
+        } else if constexpr (TJ == 2) {
 #pragma unroll
-            for (int q = 0; q < TJ; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+            for (int kk = 0; kk < 4; ++kk) {
+                const float2 v = *reinterpret_cast<const float2*>(B + (k0 + kk) * ldb + f.col(0));
+                b[kk][0] = v.x;
+                b[kk][1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int q4 = 0; q4 < TJ / 4; ++q4) {
+                    const float4 v = *reinterpret_cast<const float4*>(B + (k0 + kk) * ldb + f.col(4 * q4));
+                    b[kk][4 * q4] = v.x;
+                    b[kk][4 * q4 + 1] = v.y;
+                    b[kk][4 * q4 + 2] = v.z;
+                    b[kk][4 * q4 + 3] = v.w;
+                }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < TJ; ++q) acc[r][q] = fmaf(a[kk][r], b[kk][q], acc[r][q]);
     }
 }
 
-template <int I, int J>
-__device__ __forceinline__ void zero(float (&acc)[Tile<I, J>::TI][Tile<I, J>::TJ]) {
+template <int TJ>
+__device__ __forceinline__ void zero(float (&acc)[4][TJ]) {
 #pragma unroll
-    for (int r = 0; r < Tile<I, J>::TI; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int q = 0; q < Tile<I, J>::TJ; ++q) acc[r][q] = 0.f;
+        for (int q = 0; q < TJ; ++q) acc[r][q] = 0.f;
 }
 
-// rows [Q][ld] of a [Bt, L, ., W] tensor (row stride `stride` elements), zero past L
-template <typename T, int W>
+// acc into a global [I][ld] float32 array (columns of a thread contiguous by fours in XC)
+template <int I, int J, Lay LA, Lay LB>
+__device__ __forceinline__ void store_tile(const Frag<I, J, LA, LB>& f,
+                                           const float (&acc)[4][Frag<I, J, LA, LB>::TJ], float* out, int ld) {
+    constexpr int TJ = Frag<I, J, LA, LB>::TJ;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if constexpr (LB == XC && TJ % 4 == 0) {
+#pragma unroll
+            for (int q4 = 0; q4 < TJ / 4; ++q4)
+                *reinterpret_cast<float4*>(out + static_cast<size_t>(f.row(r)) * ld + f.col(4 * q4)) =
+                    make_float4(acc[r][4 * q4], acc[r][4 * q4 + 1], acc[r][4 * q4 + 2], acc[r][4 * q4 + 3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < TJ; ++q) out[static_cast<size_t>(f.row(r)) * ld + f.col(q)] = acc[r][q];
+        }
+    }
+}
+
+// 16-byte vector of T as float32
+__device__ __forceinline__ void unpack16(const uint4& v, float* f, float) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& v, float* f, bf16_t) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f[2 * j] = lo_bf16(w[j]);
+        f[2 * j + 1] = hi_bf16(w[j]);
+    }
+}
+
+// Rows t < Q of a tensor (row t at element base + t * stride, W contiguous elements of T)
+// into shared memory as float32 rows of length ldst, zero from row `rows_valid` on.
+// Every thread issues all of its 16-byte loads before its first store, so their
+// latencies overlap.  With CT, also the transpose: element (t, w) at ct[w * ldct + t].
+template <typename T, int W, bool CT = false>
 __device__ __forceinline__ void load_rows(float* dst, int ldst, const void* src, size_t base, size_t stride,
-                                          int rows_valid) {
-    for (int i = threadIdx.x; i < kQ * W; i += kNT) {
-        const int t = i / W, w = i % W;
-        dst[t * ldst + w] = t < rows_valid ? ld<T>(src, base + t * stride + w) : 0.f;
+                                          int rows_valid, float* ct = nullptr, int ldct = 0) {
+    constexpr int V = 16 / sizeof(T);  // elements per load
+    constexpr int RV = W / V;          // loads per row
+    constexpr int PER = kQ * RV / kNT;
+    static_assert(W % V == 0 && (kQ * RV) % kNT == 0, "load shape");
+    const T* g = static_cast<const T*>(src) + base;
+    uint4 v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = threadIdx.x + j * kNT, t = i / RV, w = (i % RV) * V;
+        v[j] = t < rows_valid ? *reinterpret_cast<const uint4*>(g + t * stride + w) : make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = threadIdx.x + j * kNT, t = i / RV, w = (i % RV) * V;
+        float f[V];
+        unpack16(v[j], f, T{});
+#pragma unroll
+        for (int e = 0; e < V; e += 4)
+            *reinterpret_cast<float4*>(dst + t * ldst + w + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        if constexpr (CT) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) ct[(w + e) * ldct + t] = f[e];
+        }
+    }
+}
+
+// The P x N float32 block src ([p][n]) into shared memory: as (n, p) at dst[n * ld + p]
+// (TR) or as (p, n) at dst[p * ld + n]; with `other` (the same shape), also returns the
+// thread's part of sum(src * other).  Loads first, then stores.
+template <int N, int P, bool TR>
+__device__ __forceinline__ float load_state(float* dst, int ld, const float* src, const float* other = nullptr) {
+    constexpr int PER = P * N / 4 / kNT;
+    static_assert((P * N / 4) % kNT == 0, "state shape");
+    float4 v[PER], o[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i4 = threadIdx.x + j * kNT;
+        v[j] = reinterpret_cast<const float4*>(src)[i4];
+        if (other) o[j] = reinterpret_cast<const float4*>(other)[i4];
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int i = 4 * (threadIdx.x + j * kNT), p = i / N, n = i % N;
+        if (other) dot += v[j].x * o[j].x + v[j].y * o[j].y + v[j].z * o[j].z + v[j].w * o[j].w;
+        if constexpr (TR) {
+            dst[n * ld + p] = v[j].x;
+            dst[(n + 1) * ld + p] = v[j].y;
+            dst[(n + 2) * ld + p] = v[j].z;
+            dst[(n + 3) * ld + p] = v[j].w;
+        } else {
+            *reinterpret_cast<float4*>(dst + p * ld + n) = v[j];
+        }
+    }
+    return dot;
 }
 
 // block sum in a fixed order (every thread calls it; the result is returned to all)
@@ -216,34 +369,31 @@ struct ChunkId {
 // ---------------------------------------------------------------------------------------
 template <typename Tin, int N, int P>
 __global__ void __launch_bounds__(kNT) ssd_bwd_chunk_states(CkArgs a) {
-    constexpr int SX = P + 1, SN = N + 1;
-    extern __shared__ float sm[];
-    float* xs = sm;                // [Q][SX] x_s F_s
-    float* Bs = xs + kQ * SX;      // [Q][SN]
-    float* su = Bs + kQ * SN;
+    constexpr int LX = P + 4, LN = N + 4;
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                // [Q][LX] x_s F_s
+    float* Bs = xs + kQ * LX;      // [Q][LN]
+    float* su = Bs + kQ * LN;
     float* sdt = su + kQ;
     float* scum = sdt + kQ;
     const ChunkId id(a);
     const int H = a.nheads, G = a.ngroups;
     chunk_steps<Tin>(a, id.b, id.hd, id.c, su, sdt, scum);
-    load_rows<Tin, N>(Bs, SN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    load_rows<Tin, P>(xs, LX, a.x, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
+                      id.valid);
+    load_rows<Tin, N>(Bs, LN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
     __syncthreads();
     const float tot = scum[kQ - 1];
     for (int i = threadIdx.x; i < kQ * P; i += kNT) {
         const int s = i / P, p = i % P;
-        const float f = expf(tot - scum[s]) * sdt[s];
-        xs[s * SX + p] = s < id.valid ? ld<Tin>(a.x, ((id.row0 + s) * H + id.hd) * P + p) * f : 0.f;
+        xs[s * LX + p] *= expf(tot - scum[s]) * sdt[s];
     }
     __syncthreads();
-    const Tile<P, N> t;
-    float acc[Tile<P, N>::TI][Tile<P, N>::TJ];
-    zero<P, N>(acc);
-    mac<P, N, kQ>(t, acc, [&](int p, int s) { return xs[s * SX + p]; }, [&](int s, int n) { return Bs[s * SN + n]; });
-    float* out = a.st + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N;
-#pragma unroll
-    for (int r = 0; r < Tile<P, N>::TI; ++r)
-#pragma unroll
-        for (int q = 0; q < Tile<P, N>::TJ; ++q) out[t.row(r) * N + t.col(q)] = acc[r][q];
+    const Frag<P, N, XC, XC> f;
+    float acc[4][Frag<P, N, XC, XC>::TJ];
+    zero(acc);
+    mac<kQ>(f, acc, xs, LX, Bs, LN);
+    store_tile(f, acc, a.st + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N, N);
     if (threadIdx.x == 0) a.tot[static_cast<size_t>(id.q) * a.nch + id.c] = tot;
 }
 
@@ -290,65 +440,73 @@ __global__ void __launch_bounds__(256) ssd_bwd_pass(CkArgs a, int PN) {
 // ---------------------------------------------------------------------------------------
 template <typename Tin, int N, int P>
 __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_outputs(CkArgs a) {
-    constexpr int SX = P + 1, SN = N + 1;
-    extern __shared__ float sm[];
-    float* xs = sm;                // [Q][SX]
-    float* ds = xs + kQ * SX;      // [Q][SX] do_t e^{cum_t}
-    float* Bs = ds + kQ * SX;      // [Q][SN]
-    float* Cs = Bs + kQ * SN;      // [Q][SN]
-    float* Hs = Cs + kQ * SN;      // [P][SN] state entering the chunk
-    float* Wa = Hs + P * SN;       // [Q][kSQ]
-    float* su = Wa + kQ * kSQ;
+    constexpr int LX = P + 4, LN = N + 4;
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                // [Q][LX]
+    float* ds = xs + kQ * LX;      // [Q][LX] do_t e^{cum_t}
+    float* Bs = ds + kQ * LX;      // [Q][LN]
+    float* Cs = Bs + kQ * LN;      // [Q][LN]
+    float* Hs = Cs + kQ * LN;      // [N][LX] state entering the chunk, element (n, p)
+    float* Wa = Hs + N * LX;       // [Q][kLQ]
+    float* su = Wa + kQ * kLQ;
     float* sdt = su + kQ;
     float* scum = sdt + kQ;
     const ChunkId id(a);
     const int H = a.nheads, G = a.ngroups;
     chunk_steps<Tin>(a, id.b, id.hd, id.c, su, sdt, scum);
-    load_rows<Tin, P>(xs, SX, a.x, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
+    load_rows<Tin, P>(xs, LX, a.x, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
                       id.valid);
-    load_rows<Tin, N>(Bs, SN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
-    load_rows<Tin, N>(Cs, SN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
-    {
-        const float* hp = a.st + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N;
-        for (int i = threadIdx.x; i < P * N; i += kNT) Hs[(i / N) * SN + i % N] = hp[i];
-    }
+    load_rows<Tin, N>(Bs, LN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    load_rows<Tin, N>(Cs, LN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    load_state<N, P, true>(Hs, LX, a.st + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N);
     __syncthreads();
     {  // Wa = (C B^T) E dt_s, lower triangle
-        const Tile<kQ, kQ> t;
-        float acc[Tile<kQ, kQ>::TI][Tile<kQ, kQ>::TJ];
-        zero<kQ, kQ>(acc);
-        mac<kQ, kQ, N>(t, acc, [&](int i, int n) { return Cs[i * SN + n]; }, [&](int n, int s) { return Bs[s * SN + n]; });
+        const Frag<kQ, kQ, KC, KC> f;
+        float acc[4][Frag<kQ, kQ, KC, KC>::TJ];
+        zero(acc);
+        mac<N>(f, acc, Cs, LN, Bs, LN);
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, kQ>::TI; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, kQ>::TJ; ++q) {
-                const int i = t.row(r), s = t.col(q);
-                Wa[i * kSQ + s] = s <= i ? acc[r][q] * expf(scum[i] - scum[s]) * sdt[s] : 0.f;
+            for (int q = 0; q < Frag<kQ, kQ, KC, KC>::TJ; ++q) {
+                const int i = f.row(r), s = f.col(q);
+                Wa[i * kLQ + s] = s <= i ? acc[r][q] * expf(scum[i] - scum[s]) * sdt[s] : 0.f;
             }
     }
     __syncthreads();
     {  // o = Wa x + e^{cum_t} C h_p + D x, then the gate
-        const Tile<kQ, P> t;
-        float a1[Tile<kQ, P>::TI][Tile<kQ, P>::TJ], a2[Tile<kQ, P>::TI][Tile<kQ, P>::TJ];
-        zero<kQ, P>(a1);
-        zero<kQ, P>(a2);
-        mac<kQ, P, kQ>(t, a1, [&](int i, int s) { return Wa[i * kSQ + s]; }, [&](int s, int p) { return xs[s * SX + p]; });
-        mac<kQ, P, N>(t, a2, [&](int i, int n) { return Cs[i * SN + n]; }, [&](int n, int p) { return Hs[p * SN + n]; });
+        using F = Frag<kQ, P, KC, XC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<kQ>(f, a1, Wa, kLQ, xs, LX);
+        mac<N>(f, a2, Cs, LN, Hs, LX);
         const float Dh = a.D ? a.D[id.hd] : 0.f;
+        float dyv[4][F::TJ], zv[4][F::TJ];  // loaded before any store, so that they overlap
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, P>::TI; ++r) {
-            const int i = t.row(r);
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < F::TJ; ++q) {
+                const int i = f.row(r);
+                const size_t gi = ((id.row0 + i) * H + id.hd) * P + f.col(q);
+                dyv[r][q] = i < id.valid ? ld<Tin>(a.dy, gi) : 0.f;
+                zv[r][q] = (a.z && i < id.valid) ? ld<Tin>(a.z, gi) : 0.f;
+            }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = f.row(r);
             const float ec = expf(scum[i]);
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, P>::TJ; ++q) {
-                const int p = t.col(q);
+            for (int q = 0; q < F::TJ; ++q) {
+                const int p = f.col(q);
                 float dov = 0.f;
                 if (i < id.valid) {
                     const size_t gi = ((id.row0 + i) * H + id.hd) * P + p;
-                    const float o = a1[r][q] + ec * a2[r][q] + Dh * xs[i * SX + p];
-                    const float dout = ld<Tin>(a.dy, gi);
+                    const float o = a1[r][q] + ec * a2[r][q] + Dh * xs[i * LX + p];
+                    const float dout = dyv[r][q];
                     if (a.z) {
-                        const float zz = ld<Tin>(a.z, gi);
+                        const float zz = zv[r][q];
                         const float sg = sigmoid_accurate(zz);
                         dov = dout * zz * sg;
                         a.dz[gi] = dout * o * sg * (1.f + zz * (1.f - sg));
@@ -357,21 +515,17 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_outputs(CkArgs a) {
                     }
                     a.dx[gi] = dov;
                 }
-                ds[i * SX + p] = dov * ec;
+                ds[i * LX + p] = dov * ec;
             }
         }
     }
     __syncthreads();
     {  // R[p][n] = sum_t ds[t][p] C[t][n]
-        const Tile<P, N> t;
-        float acc[Tile<P, N>::TI][Tile<P, N>::TJ];
-        zero<P, N>(acc);
-        mac<P, N, kQ>(t, acc, [&](int p, int s) { return ds[s * SX + p]; }, [&](int s, int n) { return Cs[s * SN + n]; });
-        float* out = a.adj + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N;
-#pragma unroll
-        for (int r = 0; r < Tile<P, N>::TI; ++r)
-#pragma unroll
-            for (int q = 0; q < Tile<P, N>::TJ; ++q) out[t.row(r) * N + t.col(q)] = acc[r][q];
+        const Frag<P, N, XC, XC> f;
+        float acc[4][Frag<P, N, XC, XC>::TJ];
+        zero(acc);
+        mac<kQ>(f, acc, ds, LX, Cs, LN);
+        store_tile(f, acc, a.adj + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N, N);
     }
 }
 
@@ -380,52 +534,61 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_outputs(CkArgs a) {
 // ---------------------------------------------------------------------------------------
 template <typename Tin, int N, int P>
 __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
-    constexpr int SX = P + 1, SN = N + 1;
-    extern __shared__ float sm[];
-    float* xs = sm;                // [Q][SX]
-    float* ds = xs + kQ * SX;      // [Q][SX] do
-    float* Bs = ds + kQ * SX;      // [Q][SN]
-    float* Cs = Bs + kQ * SN;      // [Q][SN]
-    float* Hs = Cs + kQ * SN;      // [P][SN] adjoint leaving the chunk, then state entering it
-    float* Wa = Hs + P * SN;       // [Q][kSQ] C B^T, then C B^T E dt_s
-    float* Wb = Wa + kQ * kSQ;     // [Q][kSQ] T, then T E dt_s
-    float* Vb = Wb + kQ * kSQ;     // [Q][kSQ] C B^T E T
-    float* su = Vb + kQ * kSQ;
+    constexpr int LX = P + 4, LN = N + 4;
+    constexpr int GB = N * LX > P * LN ? N * LX : P * LN;
+    extern __shared__ __align__(16) float sm[];
+    float* xs = sm;                // [Q][LX]
+    float* ds = xs + kQ * LX;      // [Q][LX] do
+    float* Bs = ds + kQ * LX;      // [Q][LN]
+    float* Cs = Bs + kQ * LN;      // [Q][LN]
+    float* CsT = Cs + kQ * LN;     // [N][kLQ] C, element (n, t)
+    float* Gb = CsT + N * kLQ;     // adjoint leaving the chunk [N][LX], then state entering it [P][LN]
+    float* WaT = Gb + GB;          // [Q][kLQ] (C B^T E dt_s)[t][s] at s * kLQ + t
+    float* Wb = WaT + kQ * kLQ;    // [Q][kLQ] (T E dt_s)[t][s] at t * kLQ + s
+    float* WbT = Wb + kQ * kLQ;    // [Q][kLQ] the same at s * kLQ + t
+    float* su = WbT + kQ * kLQ;
     float* sdt = su + kQ;
     float* scum = sdt + kQ;
     float* sdw = scum + kQ;        // dt_s as input weight: intra-chunk part
-    float* sdc = sdw + kQ;         // d cum, intra-chunk part
+    float* sdc = sdw + kQ;         // d cum, intra-chunk part (dt-weighted row sums)
     float* sdc2 = sdc + kQ;        // d cum, through the state entering the chunk
     float* sdF = sdc2 + kQ;        // B_s^T G x_s
-    float* red = sdF + kQ;         // [32]
+    float* colp = sdF + kQ;        // [4][Q] column sums of C B^T E T per warp row
+    float* red = colp + 4 * kQ;    // [32]
     const ChunkId id(a);
     const int H = a.nheads, G = a.ngroups;
     const size_t PN = static_cast<size_t>(P) * N;
     const size_t cidx = static_cast<size_t>(id.ql) * a.nch + id.c;
     chunk_steps<Tin>(a, id.b, id.hd, id.c, su, sdt, scum);
-    load_rows<Tin, P>(xs, SX, a.x, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
+    load_rows<Tin, P>(xs, LX, a.x, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
                       id.valid);
-    load_rows<float, P>(ds, SX, a.dx, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
+    load_rows<float, P>(ds, LX, a.dx, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
                         id.valid);
-    load_rows<Tin, N>(Bs, SN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
-    load_rows<Tin, N>(Cs, SN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    load_rows<Tin, N>(Bs, LN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    load_rows<Tin, N, true>(Cs, LN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid, CsT,
+                            kLQ);
     if (threadIdx.x < kQ) {
+        sdc[threadIdx.x] = 0.f;
         sdc2[threadIdx.x] = 0.f;
         sdF[threadIdx.x] = 0.f;
     }
     __syncthreads();
-    {  // Wa = C B^T, Wb = T = do x^T
-        const Tile<kQ, kQ> t;
-        float a1[Tile<kQ, kQ>::TI][Tile<kQ, kQ>::TJ], a2[Tile<kQ, kQ>::TI][Tile<kQ, kQ>::TJ];
-        zero<kQ, kQ>(a1);
-        zero<kQ, kQ>(a2);
-        mac<kQ, kQ, N>(t, a1, [&](int i, int n) { return Cs[i * SN + n]; }, [&](int n, int s) { return Bs[s * SN + n]; });
-        mac<kQ, kQ, P>(t, a2, [&](int i, int p) { return ds[i * SX + p]; }, [&](int p, int s) { return xs[s * SX + p]; });
+    {  // C B^T and T = do x^T; the masked, decayed, weighted forms; sums of C B^T E T
+        using F = Frag<kQ, kQ, KC, KC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<N>(f, a1, Cs, LN, Bs, LN);
+        mac<P>(f, a2, ds, LX, xs, LX);
+        float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[F::TJ];
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, kQ>::TI; ++r)
+        for (int q = 0; q < F::TJ; ++q) cp[q] = 0.f;
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, kQ>::TJ; ++q) {
-                const int i = t.row(r), s = t.col(q);
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < F::TJ; ++q) {
+                const int i = f.row(r), s = f.col(q);
                 float w1 = 0.f, w2 = 0.f, v = 0.f;
                 if (s <= i) {
                     const float e = expf(scum[i] - scum[s]);
@@ -433,118 +596,122 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
                     w1 = a1[r][q] * e * sdt[s];
                     w2 = a2[r][q] * e * sdt[s];
                 }
-                Wa[i * kSQ + s] = w1;
-                Wb[i * kSQ + s] = w2;
-                Vb[i * kSQ + s] = v;
+                WaT[s * kLQ + i] = w1;
+                Wb[i * kLQ + s] = w2;
+                WbT[s * kLQ + i] = w2;
+                rp[r] = fmaf(sdt[s], v, rp[r]);
+                cp[q] += v;
             }
-    }
-    __syncthreads();
-    // column sums (dt_s as weight) and dt-weighted row sums (d cum) of C B^T E T; the
-    // adjoint leaving the chunk into Hs, and <adjoint, state entering the chunk>
-    if (threadIdx.x < kQ) {
-        const int s = threadIdx.x;
-        float cs = 0.f;
-        for (int i = 0; i < kQ; ++i) cs += Vb[i * kSQ + s];
-        sdw[s] = cs;
-    } else if (threadIdx.x < 2 * kQ) {
-        const int i = threadIdx.x - kQ;
-        float rs = 0.f;
-        for (int s = 0; s < kQ; ++s) rs += sdt[s] * Vb[i * kSQ + s];
-        sdc[i] = rs;
-    }
-    float dot = 0.f;
-    {
-        const float* gh = a.adj + cidx * PN;
-        const float* hp = a.st + cidx * PN;
-        for (int i = threadIdx.x; i < P * N; i += kNT) {
-            const float gv = gh[i];
-            Hs[(i / N) * SN + i % N] = gv;
-            dot = fmaf(gv, hp[i], dot);
+        // rows: the 8 lanes of a row, then the two warps of a row (atomic adds of two
+        // terms onto zero, so the order does not matter); columns: the 4 lanes of a
+        // column, then the four warp rows in a fixed order below
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) rp[r] += __shfl_xor_sync(0xffffffffu, rp[r], off);
+            if (f.tj == 0) atomicAdd(&sdc[f.row(r)], rp[r]);
+        }
+#pragma unroll
+        for (int q = 0; q < F::TJ; ++q) {
+            cp[q] += __shfl_xor_sync(0xffffffffu, cp[q], 8);
+            cp[q] += __shfl_xor_sync(0xffffffffu, cp[q], 16);
+            if (f.ti == 0) colp[(f.ib / 16) * kQ + f.col(q)] = cp[q];
         }
     }
-    dot = block_sum(dot, red);  // includes the barrier that publishes Hs, sdw, sdc
+    __syncthreads();
+    if (threadIdx.x < kQ) {
+        const int s = threadIdx.x;
+        sdw[s] = ((colp[s] + colp[kQ + s]) + colp[2 * kQ + s]) + colp[3 * kQ + s];
+    }
+    // the adjoint leaving the chunk as (n, p), and <adjoint, state entering the chunk>
+    float dot = load_state<N, P, true>(Gb, LX, a.adj + cidx * PN, a.st + cidx * PN);
+    dot = block_sum(dot, red);  // includes the barrier that publishes Gb and sdw
     const float tot = scum[kQ - 1];
     const float Dh = a.D ? a.D[id.hd] : 0.f;
     float ddsum = 0.f;  // sum do x (dD)
-    {  // dx = D do + Wa^T do + F_s B G
-        const Tile<kQ, P> t;
-        float a1[Tile<kQ, P>::TI][Tile<kQ, P>::TJ], a2[Tile<kQ, P>::TI][Tile<kQ, P>::TJ];
-        zero<kQ, P>(a1);
-        zero<kQ, P>(a2);
-        mac<kQ, P, kQ>(t, a1, [&](int s, int i) { return Wa[i * kSQ + s]; }, [&](int i, int p) { return ds[i * SX + p]; });
-        mac<kQ, P, N>(t, a2, [&](int s, int n) { return Bs[s * SN + n]; }, [&](int n, int p) { return Hs[p * SN + n]; });
+    {  // dx = D do + (C B^T E dt)^T do + F_s B G
+        using F = Frag<kQ, P, KC, XC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<kQ>(f, a1, WaT, kLQ, ds, LX);
+        mac<N>(f, a2, Bs, LN, Gb, LX);
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, P>::TI; ++r) {
-            const int s = t.row(r);
+        for (int r = 0; r < 4; ++r) {
+            const int s = f.row(r);
             if (s >= id.valid) continue;
-            const float F = expf(tot - scum[s]) * sdt[s];
+            const float Fs = expf(tot - scum[s]) * sdt[s];
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, P>::TJ; ++q) {
-                const int p = t.col(q);
-                const float dov = ds[s * SX + p];
-                ddsum = fmaf(dov, xs[s * SX + p], ddsum);
-                a.dx[((id.row0 + s) * H + id.hd) * P + p] = Dh * dov + a1[r][q] + F * a2[r][q];
+            for (int q = 0; q < F::TJ; ++q) {
+                const int p = f.col(q);
+                const float dov = ds[s * LX + p];
+                ddsum = fmaf(dov, xs[s * LX + p], ddsum);
+                a.dx[((id.row0 + s) * H + id.hd) * P + p] = Dh * dov + a1[r][q] + Fs * a2[r][q];
             }
         }
     }
-    {  // dB = Wb^T C + F_s x G^T, and B_s^T G x_s
-        const Tile<kQ, N> t;
-        float a1[Tile<kQ, N>::TI][Tile<kQ, N>::TJ], a2[Tile<kQ, N>::TI][Tile<kQ, N>::TJ];
-        zero<kQ, N>(a1);
-        zero<kQ, N>(a2);
-        mac<kQ, N, kQ>(t, a1, [&](int s, int i) { return Wb[i * kSQ + s]; }, [&](int i, int n) { return Cs[i * SN + n]; });
-        mac<kQ, N, P>(t, a2, [&](int s, int p) { return xs[s * SX + p]; }, [&](int p, int n) { return Hs[p * SN + n]; });
+    {  // dB = (T E dt)^T C + F_s G x, and B_s^T G x_s
+        using F = Frag<kQ, N, KC, KC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<kQ>(f, a1, WbT, kLQ, CsT, kLQ);
+        mac<P>(f, a2, xs, LX, Gb, LX);
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, N>::TI; ++r) {
-            const int s = t.row(r);
-            const float F = expf(tot - scum[s]) * sdt[s];
+        for (int r = 0; r < 4; ++r) {
+            const int s = f.row(r);
+            const float Fs = expf(tot - scum[s]) * sdt[s];
             float fsum = 0.f;
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, N>::TJ; ++q) {
-                const int n = t.col(q);
-                fsum = fmaf(Bs[s * SN + n], a2[r][q], fsum);
-                if (s < id.valid) atomicAdd(&a.dB[((id.row0 + s) * G + id.g) * N + n], a1[r][q] + F * a2[r][q]);
+            for (int q = 0; q < F::TJ; ++q) {
+                const int n = f.col(q);
+                fsum = fmaf(Bs[s * LN + n], a2[r][q], fsum);
+                if (s < id.valid) atomicAdd(&a.dB[((id.row0 + s) * G + id.g) * N + n], a1[r][q] + Fs * a2[r][q]);
             }
-            atomicAdd(&sdF[s], fsum);
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, off);
+            if (f.tj == 0) atomicAdd(&sdF[s], fsum);  // two warps per row
         }
     }
-    __syncthreads();  // Hs is read by every thread above
-    {
-        const float* hp = a.st + cidx * PN;
-        for (int i = threadIdx.x; i < P * N; i += kNT) Hs[(i / N) * SN + i % N] = hp[i];
-    }
+    __syncthreads();  // Gb is read by every thread above
+    load_state<N, P, false>(Gb, LN, a.st + cidx * PN);
     __syncthreads();
-    {  // dC = Wb B + e^{cum_t} do h_p^T, and C_t . (e^{cum_t} h_p do_t)
-        const Tile<kQ, N> t;
-        float a1[Tile<kQ, N>::TI][Tile<kQ, N>::TJ], a2[Tile<kQ, N>::TI][Tile<kQ, N>::TJ];
-        zero<kQ, N>(a1);
-        zero<kQ, N>(a2);
-        mac<kQ, N, kQ>(t, a1, [&](int i, int s) { return Wb[i * kSQ + s]; }, [&](int s, int n) { return Bs[s * SN + n]; });
-        mac<kQ, N, P>(t, a2, [&](int i, int p) { return ds[i * SX + p]; }, [&](int p, int n) { return Hs[p * SN + n]; });
+    {  // dC = (T E dt) B + e^{cum_t} h_p do, and C_t . (e^{cum_t} h_p do_t)
+        using F = Frag<kQ, N, KC, XC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<kQ>(f, a1, Wb, kLQ, Bs, LN);
+        mac<P>(f, a2, ds, LX, Gb, LN);
 #pragma unroll
-        for (int r = 0; r < Tile<kQ, N>::TI; ++r) {
-            const int i = t.row(r);
+        for (int r = 0; r < 4; ++r) {
+            const int i = f.row(r);
             const float ec = expf(scum[i]);
             float csum = 0.f;
 #pragma unroll
-            for (int q = 0; q < Tile<kQ, N>::TJ; ++q) {
-                const int n = t.col(q);
+            for (int q = 0; q < F::TJ; ++q) {
+                const int n = f.col(q);
                 const float u = ec * a2[r][q];
-                csum = fmaf(Cs[i * SN + n], u, csum);
+                csum = fmaf(Cs[i * LN + n], u, csum);
                 if (i < id.valid) atomicAdd(&a.dC[((id.row0 + i) * G + id.g) * N + n], a1[r][q] + u);
             }
-            atomicAdd(&sdc2[i], csum);
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) csum += __shfl_xor_sync(0xffffffffu, csum, off);
+            if (f.tj == 0) atomicAdd(&sdc2[i], csum);  // two warps per row
         }
     }
     ddsum = block_sum(ddsum, red);  // also publishes sdF, sdc2
     // per step: d cum, then d a by a reverse running sum, then d(dt) through softplus
-    float* fdf = Vb;  // F_s B_s^T G x_s, reusing the free Q x Q buffer
+    float* fdf = colp;  // F_s B_s^T G x_s
     if (threadIdx.x < kQ) {
         const int s = threadIdx.x;
         const float eT = expf(tot - scum[s]);
-        const float F = eT * sdt[s];
-        fdf[s] = F * sdF[s];
-        sdc[s] = sdc[s] - sdt[s] * sdw[s] + sdc2[s] - F * sdF[s];
+        const float Fs = eT * sdt[s];
+        fdf[s] = Fs * sdF[s];
+        sdc[s] = sdc[s] - sdt[s] * sdw[s] + sdc2[s] - Fs * sdF[s];
         sdw[s] += eT * sdF[s];
     }
     __syncthreads();
@@ -594,15 +761,16 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce(CkArgs a, float* dA, float
 
 template <int N, int P>
 constexpr size_t smem_outputs() {
-    return sizeof(float) * (2 * kQ * (P + 1) + 2 * kQ * (N + 1) + P * (N + 1) + kQ * kSQ + 3 * kQ);
+    return sizeof(float) * (2 * kQ * (P + 4) + 2 * kQ * (N + 4) + N * (P + 4) + kQ * kLQ + 3 * kQ);
 }
 template <int N, int P>
 constexpr size_t smem_grads() {
-    return sizeof(float) * (2 * kQ * (P + 1) + 2 * kQ * (N + 1) + P * (N + 1) + 3 * kQ * kSQ + 7 * kQ + 32);
+    constexpr int GB = N * (P + 4) > P * (N + 4) ? N * (P + 4) : P * (N + 4);
+    return sizeof(float) * (2 * kQ * (P + 4) + 2 * kQ * (N + 4) + N * kLQ + GB + 3 * kQ * kLQ + 11 * kQ + 32);
 }
 template <int N, int P>
 constexpr size_t smem_states() {
-    return sizeof(float) * (kQ * (P + 1) + kQ * (N + 1) + 3 * kQ);
+    return sizeof(float) * (kQ * (P + 4) + kQ * (N + 4) + 3 * kQ);
 }
 
 // the supported (dstate, headdim) pairs
