@@ -36,9 +36,11 @@
 // Each chunk launch runs one CTA of 256 threads per chunk with the chunk's operands in
 // shared memory as float32.  Each product is laid out so that both of its operands are
 // read with 16-byte loads: every operand is stored with either the contraction index or
-// the output index contiguous, whichever the product needs (C is kept both ways in the
-// gradient launch); a thread computes a 4 x TJ tile (4 x 8 lanes per warp) and takes four
-// steps of the contraction per load.
+// the output index contiguous, whichever the product needs (the adjoint is kept both ways
+// in the gradient launch); a thread computes a 4 x TJ tile (4 x 8 lanes per warp) and takes
+// four steps of the contraction per load.  Global loads are issued in batches before their
+// stores to shared memory (the state entering the chunk by asynchronous copies, the
+// adjoint while the dC products run), and dB, dC are added with 16-byte vector atomics.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -459,6 +461,19 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_outputs(CkArgs a) {
     load_rows<Tin, N>(Bs, LN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
     load_rows<Tin, N>(Cs, LN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
     load_state<N, P, true>(Hs, LX, a.st + (static_cast<size_t>(id.ql) * a.nch + id.c) * P * N);
+    // dy and z of this thread's outputs, in flight during the first product
+    using FY = Frag<kQ, P, KC, XC>;
+    const FY fy;
+    float dyv[4][FY::TJ], zv[4][FY::TJ];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < FY::TJ; ++q) {
+            const int i = fy.row(r);
+            const size_t gi = ((id.row0 + i) * H + id.hd) * P + fy.col(q);
+            dyv[r][q] = i < id.valid ? ld<Tin>(a.dy, gi) : 0.f;
+            zv[r][q] = (a.z && i < id.valid) ? ld<Tin>(a.z, gi) : 0.f;
+        }
     __syncthreads();
     {  // Wa = (C B^T) E dt_s, lower triangle
         const Frag<kQ, kQ, KC, KC> f;
@@ -475,24 +490,14 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_outputs(CkArgs a) {
     }
     __syncthreads();
     {  // o = Wa x + e^{cum_t} C h_p + D x, then the gate
-        using F = Frag<kQ, P, KC, XC>;
-        const F f;
+        using F = FY;
+        const F& f = fy;
         float a1[4][F::TJ], a2[4][F::TJ];
         zero(a1);
         zero(a2);
         mac<kQ>(f, a1, Wa, kLQ, xs, LX);
         mac<N>(f, a2, Cs, LN, Hs, LX);
         const float Dh = a.D ? a.D[id.hd] : 0.f;
-        float dyv[4][F::TJ], zv[4][F::TJ];  // loaded before any store, so that they overlap
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int q = 0; q < F::TJ; ++q) {
-                const int i = f.row(r);
-                const size_t gi = ((id.row0 + i) * H + id.hd) * P + f.col(q);
-                dyv[r][q] = i < id.valid ? ld<Tin>(a.dy, gi) : 0.f;
-                zv[r][q] = (a.z && i < id.valid) ? ld<Tin>(a.z, gi) : 0.f;
-            }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int i = f.row(r);
@@ -541,8 +546,8 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
     float* ds = xs + kQ * LX;      // [Q][LX] do
     float* Bs = ds + kQ * LX;      // [Q][LN]
     float* Cs = Bs + kQ * LN;      // [Q][LN]
-    float* CsT = Cs + kQ * LN;     // [N][kLQ] C, element (n, t)
-    float* Gb = CsT + N * kLQ;     // adjoint leaving the chunk [N][LX], then state entering it [P][LN]
+    float* Gn = Cs + kQ * LN;      // [P][LN] adjoint leaving the chunk, element (p, n)
+    float* Gb = Gn + P * LN;       // state entering the chunk [P][LN], then the adjoint as (n, p) [N][LX]
     float* WaT = Gb + GB;          // [Q][kLQ] (C B^T E dt_s)[t][s] at s * kLQ + t
     float* Wb = WaT + kQ * kLQ;    // [Q][kLQ] (T E dt_s)[t][s] at t * kLQ + s
     float* WbT = Wb + kQ * kLQ;    // [Q][kLQ] the same at s * kLQ + t
@@ -565,8 +570,15 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
     load_rows<float, P>(ds, LX, a.dx, id.row0 * H * P + static_cast<size_t>(id.hd) * P, static_cast<size_t>(H) * P,
                         id.valid);
     load_rows<Tin, N>(Bs, LN, a.B, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
-    load_rows<Tin, N, true>(Cs, LN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid, CsT,
-                            kLQ);
+    load_rows<Tin, N>(Cs, LN, a.C, (id.row0 * G + id.g) * N, static_cast<size_t>(G) * N, id.valid);
+    {  // the state entering the chunk into Gb as (p, n), asynchronously
+        const float* hp = a.st + cidx * PN;
+        for (int i4 = threadIdx.x; i4 < P * N / 4; i4 += kNT) {
+            const int i = 4 * i4;
+            cp_async16(Gb + (i / N) * LN + i % N, hp + i, 16);
+        }
+        cp_async_commit();
+    }
     if (threadIdx.x < kQ) {
         sdc[threadIdx.x] = 0.f;
         sdc2[threadIdx.x] = 0.f;
@@ -623,11 +635,65 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
         const int s = threadIdx.x;
         sdw[s] = ((colp[s] + colp[kQ + s]) + colp[2 * kQ + s]) + colp[3 * kQ + s];
     }
-    // the adjoint leaving the chunk as (n, p), and <adjoint, state entering the chunk>
-    float dot = load_state<N, P, true>(Gb, LX, a.adj + cidx * PN, a.st + cidx * PN);
-    dot = block_sum(dot, red);  // includes the barrier that publishes Gb and sdw
+    cp_async_wait<0>();
+    __syncthreads();  // the state entering the chunk is in Gb
+    // the adjoint leaving the chunk, in flight during the dC products
+    constexpr int GPER = P * N / 4 / kNT;
+    float4 gv[GPER];
+#pragma unroll
+    for (int j = 0; j < GPER; ++j) gv[j] = reinterpret_cast<const float4*>(a.adj + cidx * PN)[threadIdx.x + j * kNT];
     const float tot = scum[kQ - 1];
     const float Dh = a.D ? a.D[id.hd] : 0.f;
+    {  // dC = (T E dt) B + e^{cum_t} h_p do, and C_t . (e^{cum_t} h_p do_t)
+        using F = Frag<kQ, N, KC, XC>;
+        const F f;
+        float a1[4][F::TJ], a2[4][F::TJ];
+        zero(a1);
+        zero(a2);
+        mac<kQ>(f, a1, Wb, kLQ, Bs, LN);
+        mac<P>(f, a2, ds, LX, Gb, LN);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = f.row(r);
+            const float ec = expf(scum[i]);
+            float csum = 0.f, u[F::TJ];
+#pragma unroll
+            for (int q = 0; q < F::TJ; ++q) {
+                u[q] = ec * a2[r][q];
+                csum = fmaf(Cs[i * LN + f.col(q)], u[q], csum);
+            }
+            if (i < id.valid) {
+                float* dst = a.dC + ((id.row0 + i) * G + id.g) * N;
+#pragma unroll
+                for (int q = 0; q < F::TJ; q += 4)
+                    atomicAdd(reinterpret_cast<float4*>(dst + f.col(q)),
+                              make_float4(a1[r][q] + u[q], a1[r][q + 1] + u[q + 1], a1[r][q + 2] + u[q + 2],
+                                          a1[r][q + 3] + u[q + 3]));
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) csum += __shfl_xor_sync(0xffffffffu, csum, off);
+            if (f.tj == 0) atomicAdd(&sdc2[i], csum);  // two warps per row
+        }
+    }
+    // <adjoint, state entering the chunk>, then the adjoint into Gb as (n, p)
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < GPER; ++j) {
+        const int i = 4 * (threadIdx.x + j * kNT), pp = i / N, n = i % N;
+        const float4 h = *reinterpret_cast<const float4*>(Gb + pp * LN + n);
+        dot += gv[j].x * h.x + gv[j].y * h.y + gv[j].z * h.z + gv[j].w * h.w;
+    }
+    __syncthreads();  // every read of the state in Gb is done
+#pragma unroll
+    for (int j = 0; j < GPER; ++j) {
+        const int i = 4 * (threadIdx.x + j * kNT), pp = i / N, n = i % N;
+        *reinterpret_cast<float4*>(Gn + pp * LN + n) = gv[j];
+        Gb[n * LX + pp] = gv[j].x;
+        Gb[(n + 1) * LX + pp] = gv[j].y;
+        Gb[(n + 2) * LX + pp] = gv[j].z;
+        Gb[(n + 3) * LX + pp] = gv[j].w;
+    }
+    dot = block_sum(dot, red);  // includes the barrier that publishes Gb and Gn
     float ddsum = 0.f;  // sum do x (dD)
     {  // dx = D do + (C B^T E dt)^T do + F_s B G
         using F = Frag<kQ, P, KC, XC>;
@@ -652,55 +718,31 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
         }
     }
     {  // dB = (T E dt)^T C + F_s G x, and B_s^T G x_s
-        using F = Frag<kQ, N, KC, KC>;
+        using F = Frag<kQ, N, KC, XC>;
         const F f;
         float a1[4][F::TJ], a2[4][F::TJ];
         zero(a1);
         zero(a2);
-        mac<kQ>(f, a1, WbT, kLQ, CsT, kLQ);
-        mac<P>(f, a2, xs, LX, Gb, LX);
+        mac<kQ>(f, a1, WbT, kLQ, Cs, LN);
+        mac<P>(f, a2, xs, LX, Gn, LN);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int s = f.row(r);
             const float Fs = expf(tot - scum[s]) * sdt[s];
             float fsum = 0.f;
 #pragma unroll
-            for (int q = 0; q < F::TJ; ++q) {
-                const int n = f.col(q);
-                fsum = fmaf(Bs[s * LN + n], a2[r][q], fsum);
-                if (s < id.valid) atomicAdd(&a.dB[((id.row0 + s) * G + id.g) * N + n], a1[r][q] + Fs * a2[r][q]);
+            for (int q = 0; q < F::TJ; ++q) fsum = fmaf(Bs[s * LN + f.col(q)], a2[r][q], fsum);
+            if (s < id.valid) {
+                float* dst = a.dB + ((id.row0 + s) * G + id.g) * N;
+#pragma unroll
+                for (int q = 0; q < F::TJ; q += 4)
+                    atomicAdd(reinterpret_cast<float4*>(dst + f.col(q)),
+                              make_float4(a1[r][q] + Fs * a2[r][q], a1[r][q + 1] + Fs * a2[r][q + 1],
+                                          a1[r][q + 2] + Fs * a2[r][q + 2], a1[r][q + 3] + Fs * a2[r][q + 3]));
             }
 #pragma unroll
             for (int off = 1; off < 8; off <<= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, off);
             if (f.tj == 0) atomicAdd(&sdF[s], fsum);  // two warps per row
-        }
-    }
-    __syncthreads();  // Gb is read by every thread above
-    load_state<N, P, false>(Gb, LN, a.st + cidx * PN);
-    __syncthreads();
-    {  // dC = (T E dt) B + e^{cum_t} h_p do, and C_t . (e^{cum_t} h_p do_t)
-        using F = Frag<kQ, N, KC, XC>;
-        const F f;
-        float a1[4][F::TJ], a2[4][F::TJ];
-        zero(a1);
-        zero(a2);
-        mac<kQ>(f, a1, Wb, kLQ, Bs, LN);
-        mac<P>(f, a2, ds, LX, Gb, LN);
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int i = f.row(r);
-            const float ec = expf(scum[i]);
-            float csum = 0.f;
-#pragma unroll
-            for (int q = 0; q < F::TJ; ++q) {
-                const int n = f.col(q);
-                const float u = ec * a2[r][q];
-                csum = fmaf(Cs[i * LN + n], u, csum);
-                if (i < id.valid) atomicAdd(&a.dC[((id.row0 + i) * G + id.g) * N + n], a1[r][q] + u);
-            }
-#pragma unroll
-            for (int off = 1; off < 8; off <<= 1) csum += __shfl_xor_sync(0xffffffffu, csum, off);
-            if (f.tj == 0) atomicAdd(&sdc2[i], csum);  // two warps per row
         }
     }
     ddsum = block_sum(ddsum, red);  // also publishes sdF, sdc2
@@ -766,7 +808,7 @@ constexpr size_t smem_outputs() {
 template <int N, int P>
 constexpr size_t smem_grads() {
     constexpr int GB = N * (P + 4) > P * (N + 4) ? N * (P + 4) : P * (N + 4);
-    return sizeof(float) * (2 * kQ * (P + 4) + 2 * kQ * (N + 4) + N * kLQ + GB + 3 * kQ * kLQ + 11 * kQ + 32);
+    return sizeof(float) * (2 * kQ * (P + 4) + 2 * kQ * (N + 4) + P * (N + 4) + GB + 3 * kQ * kLQ + 11 * kQ + 32);
 }
 template <int N, int P>
 constexpr size_t smem_states() {
