@@ -55,7 +55,7 @@ constexpr int kQ = 64;     // steps per chunk
 #define SSD_BWD_THREADS 256
 #endif
 #ifndef SSD_BWD_UNROLL
-#define SSD_BWD_UNROLL 8
+#define SSD_BWD_UNROLL 2
 #endif
 constexpr int kNT = SSD_BWD_THREADS;  // threads per CTA of the chunk launches
 constexpr int kUnroll = SSD_BWD_UNROLL;  // unrolling of the products' inner loop
