@@ -103,6 +103,21 @@ def alu_peak_updates(sms, sm_max_mhz):
     return sms * sm_max_mhz * 1e6 * per_clk
 
 
+def ssd_bwd_macs(batch, L, H, P, N, Q=64):
+    """Multiply-adds of the chunked SSD backward: per (batch, head) and Q-step chunk,
+    C B^T twice (Q^2 N each), the decayed-weight products of dB and dC (Q^2 N each),
+    do x^T and the outputs' and dx's intra-chunk products (Q^2 P each), and six products
+    with a chunk state or adjoint (Q N P each: the chunk state, the outputs' state term,
+    the adjoint sum, and the state terms of dx, dB and dC)."""
+    nch = -(-L // Q)
+    return batch * H * nch * (4 * Q * Q * N + 3 * Q * Q * P + 6 * Q * N * P)
+
+
+def fp32_fma_peak(sms, sm_max_mhz):
+    """FP32 multiply-adds per second: 128 FMA lanes per SM clock."""
+    return sms * sm_max_mhz * 1e6 * FP32_LANES_PER_CLK_SM
+
+
 def bwd_bytes(batch, dim, N, L, G=1):
     """Backward of the Mamba-1 scan: x, delta, z, dy (bf16) and B, C read once; dx,
     ddelta, dz (float32) and dB, dC (float32) written once; A, D, bias and their
@@ -531,7 +546,8 @@ def run_metadata(torch, dev, seed):
 
 def path_rooflines(paths):
     """One roofline fraction per measured path (the SSD against max(HBM, bf16 tensor) time,
-    the others against HBM), compact, so that the line's head carries them."""
+    the SSD backward against the FP32 FMA rate, the others against HBM), compact, so that
+    the line's head carries them."""
     out = {}
     for q in ("64", "256"):
         r = paths.get(f"ssd_130m_chunk{q}")
@@ -541,6 +557,9 @@ def path_rooflines(paths):
     r = paths.get("decode_780m")
     if r:
         out["decode_780m"] = {"bound": "hbm", "frac": r["hbm_frac"], "us": r["us_per_step"]}
+    r = paths.get("ssd_130m_bwd")
+    if r and "fma_frac" in r:
+        out["ssd_130m_bwd"] = {"bound": "alu", "frac": r["fma_frac"], "ms": r["ms"]}
     r = paths.get("s4d_256")
     if r and "conv_hbm_frac" in r:
         out["s4d_256_conv"] = {"bound": "hbm", "frac": r["conv_hbm_frac"], "ms": r["conv_ms"]}
@@ -778,7 +797,11 @@ def other_paths(args, torch, ssm, peaks, stream, l2):
                          dt_bias=sb["dt_bias"], workspace=sbws)
     tsb = time_launches(torch, fsb, 3, 1, stream)
     upd_sb = c4["batch"] * c4["seqlen"] * c4["nheads"] * c4["headdim"] * c4["dstate"]
+    macs_sb = ssd_bwd_macs(c4["batch"], c4["seqlen"], c4["nheads"], c4["headdim"], c4["dstate"])
     out["ssd_130m_bwd"] = {"ms": tsb * 1e3, "state_updates_per_s": upd_sb / tsb,
+                           "multiply_adds": macs_sb,
+                           "fma_frac": macs_sb / tsb / fp32_fma_peak(sms, 2070.0),
+                           "fma_peak_source": f"derived: {sms} SMs x 2070 MHz x 128 FP32 FMA lanes/clk/SM",
                            "workspace_bytes": sbws.numel(),
                            "note": "x, dt, B, C, dy bf16 in; every gradient float32 out; "
                                    "chunked form (64-step chunks, float32 products)"}

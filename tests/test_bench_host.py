@@ -48,6 +48,15 @@ def test_bwd_bytes_130m_layer():
     assert b == 8 * 1536 * 2048 * 20 + 8 * 16 * 2048 * 12 + 1536 * 16 * 8 + 1536 * 16
 
 
+def test_ssd_bwd_macs_130m():
+    # per 64-step chunk: 4 Q^2 N + 3 Q^2 P + 6 Q N P with Q 64, N 128, P 64; 4 x 24 x 64 chunks
+    per_chunk = 4 * 64 * 64 * 128 + 3 * 64 * 64 * 64 + 6 * 64 * 128 * 64
+    assert per_chunk == 6029312
+    assert bench.ssd_bwd_macs(4, 4096, 24, 64, 128) == 4 * 24 * 64 * per_chunk
+    assert bench.ssd_bwd_macs(1, 65, 1, 64, 128) == 2 * per_chunk  # a ragged chunk counts whole
+    assert bench.fp32_fma_peak(152, 2070.0) == pytest.approx(152 * 2070e6 * 128)
+
+
 def test_percentile_interpolates_order_statistics():
     xs = [5.0, 1.0, 3.0, 2.0, 4.0]
     assert bench.percentile(xs, 0) == 1.0
@@ -60,8 +69,10 @@ def test_percentile_interpolates_order_statistics():
 def test_path_rooflines_carry_every_measured_path():
     paths = {"ssd_130m_chunk64": {"roofline_bound": "hbm", "roofline_frac": 0.2, "ms": 0.08},
              "decode_780m": {"hbm_frac": 0.75, "us_per_step": 40.0},
-             "m1_790m_long": {"4096": {"hbm_frac": 0.3, "ms": 0.05, "alu_frac": 0.5}}}
+             "m1_790m_long": {"4096": {"hbm_frac": 0.3, "ms": 0.05, "alu_frac": 0.5}},
+             "ssd_130m_bwd": {"ms": 2.8, "fma_frac": 0.33, "multiply_adds": 37e9}}
     r = bench.path_rooflines(paths)
+    assert r["ssd_130m_bwd"] == {"bound": "alu", "frac": 0.33, "ms": 2.8}
     assert r["ssd_130m_chunk64"] == {"bound": "hbm", "frac": 0.2, "ms": 0.08}
     assert r["decode_780m"]["frac"] == 0.75 and r["decode_780m"]["bound"] == "hbm"
     assert r["m1_790m_L4096"]["frac"] == 0.3 and r["m1_790m_L4096"]["alu_frac"] == 0.5
