@@ -303,6 +303,18 @@ __device__ __forceinline__ void load_rows(float* dst, int ldst, const void* src,
     }
 }
 
+// The thread's j-th 16-byte piece (p, n .. n + 3) of a P x N state block [p][n]: a warp
+// takes 16 rows and 8 columns, lane l row 16 rb + l % 16 and columns 4 (2 nb + l / 16)
+// .. + 3, so that the 32 lanes of a transposed store (n * ld + p, ld = 4 mod 32) fall in
+// distinct banks and each global load still reads whole 32-byte sectors.
+template <int N, int P>
+__device__ __forceinline__ void state_elem(int j, int& p, int& n) {
+    static_assert(P % 16 == 0 && N % 8 == 0, "state shape");
+    const int g = static_cast<int>(threadIdx.x) + j * kNT, c = g >> 5, l = g & 31;
+    p = (c % (P / 16)) * 16 + (l & 15);
+    n = ((c / (P / 16)) * 2 + (l >> 4)) * 4;
+}
+
 // The P x N float32 block src ([p][n]) into shared memory: as (n, p) at dst[n * ld + p]
 // (TR) or as (p, n) at dst[p * ld + n]; with `other` (the same shape), also returns the
 // thread's part of sum(src * other).  Loads first, then stores.
@@ -313,14 +325,16 @@ __device__ __forceinline__ float load_state(float* dst, int ld, const float* src
     float4 v[PER], o[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-        const int i4 = threadIdx.x + j * kNT;
-        v[j] = reinterpret_cast<const float4*>(src)[i4];
-        if (other) o[j] = reinterpret_cast<const float4*>(other)[i4];
+        int p, n;
+        state_elem<N, P>(j, p, n);
+        v[j] = *reinterpret_cast<const float4*>(src + p * N + n);
+        if (other) o[j] = *reinterpret_cast<const float4*>(other + p * N + n);
     }
     float dot = 0.f;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
-        const int i = 4 * (threadIdx.x + j * kNT), p = i / N, n = i % N;
+        int p, n;
+        state_elem<N, P>(j, p, n);
         if (other) dot += v[j].x * o[j].x + v[j].y * o[j].y + v[j].z * o[j].z + v[j].w * o[j].w;
         if constexpr (TR) {
             dst[n * ld + p] = v[j].x;
@@ -638,7 +652,11 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
     constexpr int GPER = P * N / 4 / kNT;
     float4 gv[GPER];
 #pragma unroll
-    for (int j = 0; j < GPER; ++j) gv[j] = reinterpret_cast<const float4*>(a.adj + cidx * PN)[threadIdx.x + j * kNT];
+    for (int j = 0; j < GPER; ++j) {
+        int pp, n;
+        state_elem<N, P>(j, pp, n);
+        gv[j] = *reinterpret_cast<const float4*>(a.adj + cidx * PN + pp * N + n);
+    }
     const float tot = scum[kQ - 1];
     const float Dh = a.D ? a.D[id.hd] : 0.f;
     {  // dC = (T E dt) B + e^{cum_t} h_p do, and C_t . (e^{cum_t} h_p do_t)
@@ -676,14 +694,16 @@ __global__ void __launch_bounds__(kNT, 1) ssd_bwd_chunk_grads(CkArgs a) {
     float dot = 0.f;
 #pragma unroll
     for (int j = 0; j < GPER; ++j) {
-        const int i = 4 * (threadIdx.x + j * kNT), pp = i / N, n = i % N;
+        int pp, n;
+        state_elem<N, P>(j, pp, n);
         const float4 h = *reinterpret_cast<const float4*>(Gb + pp * LN + n);
         dot += gv[j].x * h.x + gv[j].y * h.y + gv[j].z * h.z + gv[j].w * h.w;
     }
     __syncthreads();  // every read of the state in Gb is done
 #pragma unroll
     for (int j = 0; j < GPER; ++j) {
-        const int i = 4 * (threadIdx.x + j * kNT), pp = i / N, n = i % N;
+        int pp, n;
+        state_elem<N, P>(j, pp, n);
         *reinterpret_cast<float4*>(Gn + pp * LN + n) = gv[j];
         Gb[n * LX + pp] = gv[j].x;
         Gb[(n + 1) * LX + pp] = gv[j].y;
