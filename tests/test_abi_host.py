@@ -553,6 +553,14 @@ def test_ssd_bwd_workspace_size(lib):
                        fwd_out_dtype=_lib.SSM_F32)
     need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
     assert need == chunked_bwd_workspace_bytes(3, 1000, 5, 64, 128, es=4)
+    # dy in another dtype than the inputs: the tied recurrence
+    p = ssd_bwd_params(fwd_out_dtype=_lib.SSM_F32)
+    need = lib.ssd_scan_bwd_workspace_size(ctypes.byref(p))
+    assert need == bwd_workspace_bytes(2 * 4 * 64, 128, 64, dy_bytes=4)
+    # the other chunked shapes, and one slice per sequence when x and dy are small
+    for N, P in ((64, 64), (128, 32), (64, 32)):
+        p = ssd_bwd_params(fwd_dstate=N, fwd_headdim=P, fwd_seqlen=130)
+        assert lib.ssd_scan_bwd_workspace_size(ctypes.byref(p)) == chunked_bwd_workspace_bytes(2, 130, 4, P, N)
 
 
 def test_backward_workspace_at_most_the_inputs(lib):
