@@ -437,7 +437,10 @@ def bench_ours(args, rank, world):
 
     paths = {}
     if rank == 0 and not args.headline_only:
-        paths = other_paths(args, torch, ssm, peaks, stream, l2)
+        try:
+            paths = other_paths(args, torch, ssm, peaks, stream, l2)
+        except Exception as exc:  # a failing secondary path is reported, not fatal to the line
+            paths = {"error": f"{type(exc).__name__}: {exc}"}
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

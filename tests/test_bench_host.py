@@ -77,6 +77,7 @@ def test_path_rooflines_carry_every_measured_path():
     assert r["decode_780m"]["frac"] == 0.75 and r["decode_780m"]["bound"] == "hbm"
     assert r["m1_790m_L4096"]["frac"] == 0.3 and r["m1_790m_L4096"]["alu_frac"] == 0.5
     assert bench.path_rooflines({}) == {}
+    assert bench.path_rooflines({"error": "RuntimeError: x"}) == {}
 
 
 def test_sources_digest_is_stable():
