@@ -72,10 +72,15 @@ def test_chunked_form_ragged_groups(oracle_mod):
     _run(oracle_mod, 2, 1000, 4, 64, 128, 2, synth.BF16, seed=5)
 
 
-@pytest.mark.parametrize("N,P", [(64, 64), (128, 32)])
+@pytest.mark.parametrize("N,P", [(64, 64), (128, 32), (64, 32)])
 def test_chunked_form_fp32_gated(oracle_mod, N, P):
     """float32 inputs and dy through the chunked form, with the gate and a short tail."""
     _run(oracle_mod, 2, 300, 3, P, N, 1, synth.F32, seed=6)
+
+
+def test_chunked_form_bf16_narrow_heads(oracle_mod):
+    """bf16 through the chunked form with headdim 32 and dstate 64 (the narrowest tiles)."""
+    _run(oracle_mod, 2, 200, 3, 32, 64, 1, synth.BF16, seed=8)
 
 
 def test_chunked_form_single_step(oracle_mod):
